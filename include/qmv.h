@@ -1,0 +1,228 @@
+/*
+ * qmv.h - C ABI of the GB300 quantized small-batch matvec / MoE library.
+ *
+ * The operation: LLM decode multiplies a handful of token activations
+ * (1 to 64 rows) by block-quantized weight matrices that are consumed in
+ * their compressed form, dequantized on the fly.  The pages this library is
+ * built from name the pieces:
+ *   - small-batch matvecs for K-quants, IQ4_XS and Q8_0 (with a split-K
+ *     variant) for 1..16 tokens: "Castagna Veloce", section "Kernels for the
+ *     MI50", third bullet;
+ *   - i-quant MoE decode kernels for batches up to 64 tokens and the
+ *     expert-grouped quantized MoE scheme: same section, first two bullets;
+ *   - gate/up + SwiGLU fusion and Q8 activations reused across weight types:
+ *     "Castagna Veloce", section "Fused operations", fourth and fifth bullets;
+ *   - a decode row is a matrix-vector product bound by weight reads, and the
+ *     hot path must consume compressed weights directly: "Running GLM-5.3 on
+ *     Two 8-GPU AMD W7900D Machines", sections "A single decode row is not a
+ *     large matrix multiplication" and "Keep quantized weights compressed in
+ *     memory";
+ *   - effective bandwidth = weight bytes / kernel time: same page, section
+ *     "A faster kernel can still leave the full chain slower" (the paragraph
+ *     under the constraint table).
+ * The pages give no byte layouts; the layouts below are this library's own.
+ *
+ * ------------------------------------------------------------------------
+ * Conventions shared by every entry point
+ * ------------------------------------------------------------------------
+ *   - Activations X are fp32 row-major [n_tok][K]; outputs Y are fp32
+ *     row-major [n_tok][M]:  Y[t][m] = sum_k What[m][k] * Xhat[t][k].
+ *   - A weight matrix W has M rows; row m occupies qmv_row_bytes(fmt, K)
+ *     contiguous bytes starting at W + m * qmv_row_bytes(fmt, K).  A row is a
+ *     sequence of GROUPS; every group is a 16-byte header followed by its
+ *     payload, so every group (and row) starts on a 16-byte boundary.
+ *   - Every pointer argument is device memory owned by the caller (unless a
+ *     comment says otherwise).  The library allocates nothing, keeps no
+ *     per-call state and never synchronises the stream (except
+ *     qmv_get_device_error).  Calls are stream-ordered and asynchronous.
+ *   - Every data pointer must be 16-byte aligned (QMV_ERR_ALIGN otherwise).
+ *   - Return value: 0 on success, a negative QMV_ERR_* code on a host-side
+ *     argument error (nothing is launched then).  Errors detected on the
+ *     device (bad expert ids, a stalled pipeline) set a device error word,
+ *     read with qmv_get_device_error(); kernels never trap.
+ *
+ * ------------------------------------------------------------------------
+ * Activation quantization (shared by every weight format)
+ * ------------------------------------------------------------------------
+ *   Per token, per 32-element block j of x (K % 32 == 0):
+ *     amax = max_i |x_i|                         (exact)
+ *     d    = amax / 127                          (fp32, IEEE round-to-nearest)
+ *     id   = (d > 0) ? 1 / d : 0                 (fp32, IEEE round-to-nearest)
+ *     q_i  = clamp(rne(x_i * id), -127, 127)     (fp32 product, then round
+ *                                                 half to even to an integer)
+ *     s    = sum_i q_i                           (int32)
+ *   and Xhat_i = d * q_i.  Non-finite x is outside the contract.
+ *
+ * ------------------------------------------------------------------------
+ * Weight formats (values are What; fp16 fields are IEEE binary16, little
+ * endian; bit strings are little endian across bytes)
+ * ------------------------------------------------------------------------
+ * QMV_Q8_0: blocks of 32 weights, What = d * q, d fp16, q int8.
+ *   Group = 8 blocks (256 weights), 272 bytes:
+ *     header  bytes [2j, 2j+2)   : d of block j (j = 0..7)
+ *     payload bytes [32j, 32j+32): q_0..q_31 of block j (int8)
+ *   K % 256 == 0; row bytes = 272 * K / 256.
+ *
+ * QMV_Q4_K: superblocks of 256 weights = 8 sub-blocks of 32,
+ *   What = d * sc_j * q - dmin * m_j, q in [0,15], sc_j, m_j in [0,63].
+ *   Group = 1 superblock, 144 bytes:
+ *     header  bytes 0-1 : d (fp16);  bytes 2-3: dmin (fp16)
+ *             bytes 4-15: 96-bit string; bits [12j, 12j+6) = sc_j and
+ *                         bits [12j+6, 12j+12) = m_j  (j = 0..7)
+ *     payload bytes [16j, 16j+16): sub-block j; byte i holds q_i in its low
+ *                         nibble and q_{i+16} in its high nibble (i = 0..15)
+ *   K % 256 == 0; row bytes = 144 * K / 256.
+ *
+ * QMV_IQ4_XS: superblocks of 256 weights = 8 sub-blocks of 32,
+ *   What = d * (ls_j - 32) * CB[c], c in [0,15], ls_j in [0,63], with the
+ *   int8 codebook CB = {-127,-104,-83,-65,-49,-35,-22,-10,
+ *                       1,13,25,38,53,69,89,113}.
+ *   Group = 2 superblocks (512 weights), 272 bytes:
+ *     header  bytes [8s, 8s+2)  : d of superblock s (s = 0,1)
+ *             bytes [8s+2, 8s+8): 48-bit string, bits [6j, 6j+6) = ls_j
+ *     payload bytes [128s + 16j, +16): superblock s, sub-block j, nibbles
+ *                         arranged as for QMV_Q4_K (byte i: c_i | c_{i+16}<<4)
+ *   K % 512 == 0; row bytes = 272 * K / 512.
+ *
+ * Bytes per weight: Q8_0 1.0625, Q4_K 0.5625, IQ4_XS 0.53125 (the same
+ * densities as the GGML formats of the same names; GGUF byte compatibility is
+ * not a goal).
+ */
+#ifndef QMV_H
+#define QMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum qmv_format { QMV_Q8_0 = 0, QMV_Q4_K = 1, QMV_IQ4_XS = 2 };
+
+enum qmv_status {
+  QMV_OK = 0,
+  QMV_ERR_FORMAT = -1,    /* unknown format code */
+  QMV_ERR_SHAPE = -2,     /* M <= 0, K not a multiple of the group size, ... */
+  QMV_ERR_NTOK = -3,      /* n_tok not in [1, 64] or top_k not in [1, 8] */
+  QMV_ERR_NULL = -4,      /* a required pointer is NULL */
+  QMV_ERR_ALIGN = -5,     /* a pointer is not 16-byte aligned */
+  QMV_ERR_WORKSPACE = -6, /* workspace too small */
+  QMV_ERR_CUDA = -7,      /* a CUDA runtime call or launch failed */
+  QMV_ERR_DEVICE = -8     /* no usable sm_103 device */
+};
+
+/* Device error word bits (qmv_get_device_error). */
+#define QMV_DEVERR_EXPERT_RANGE 0x1 /* an expert id outside [0, n_experts) */
+#define QMV_DEVERR_EXPERT_DUP 0x2   /* an expert id repeated within a token */
+#define QMV_DEVERR_TIMEOUT 0x4      /* a pipeline wait exceeded its limit */
+
+#define QMV_MAX_TOKENS 64
+#define QMV_MAX_TOPK 8
+
+/* Bytes of one quantized row of K weights; negative QMV_ERR_* if fmt or K is
+ * invalid. */
+int64_t qmv_row_bytes(int fmt, int64_t K);
+
+/* Quantize fp32 weights w [M][K] (device) into format fmt, writing
+ * M * qmv_row_bytes(fmt, K) bytes at W (device).  Per block the scale is
+ * chosen from the block's range and each code is the nearest grid point
+ * (ties to the even / lower code), all in fp64:
+ *   Q8_0  : d = fp16(amax / 127); q = rne(w / d) clamped to [-127,127].
+ *   Q4_K  : per sub-block lo = min(0, min w), hi = max w, a = (hi-lo)/15,
+ *           b = -lo; d = fp16(max a / 63), dmin = fp16(max b / 63);
+ *           sc = rne(a / d), m = rne(b / dmin) clamped to [0,63];
+ *           q = argmin_{0..15} |w - (d*sc*q - dmin*m)| (ties: lower q).
+ *   IQ4_XS: per sub-block s = amax / 113; d = fp16(max s / 31);
+ *           ls = 32 + clamp(rne(s / d), 0, 31);
+ *           c = argmin_{0..15} |w - d*(ls-32)*CB[c]| (ties: lower c).
+ * (fp16(.) rounds to nearest even; a zero scale gives zero codes.)  This is a
+ * preparation step, not part of the decode hot path. */
+int qmv_quantize_weights(int fmt, const float* w, int64_t M, int64_t K, void* W,
+                         cudaStream_t stream);
+
+/* Activation quantization (rule above) of x [n_tok][K] into q int8
+ * [n_tok][K], d fp32 [n_tok][K/32] and sum int32 [n_tok][K/32].
+ * K % 256 == 0, 1 <= n_tok <= 64.  "Q8 activations reused across weight
+ * types": the result feeds qmv_run_q8 for any weight format. */
+int qmv_quantize_act(const float* x, int64_t K, int n_tok, int8_t* q, float* d,
+                     int32_t* sum, cudaStream_t stream);
+
+/* Y[t][m] = sum_k What[m][k] * Xhat[t][k] for t < n_tok, m < M: the
+ * small-batch quantized matvec.  x fp32 [n_tok][K] is quantized inside the
+ * kernel (rule above); every integer block dot product is exact and the block
+ * scales are applied in fp32.  Accuracy: |Y - Y_exact| <= 1e-5 *
+ * sum_k |What[m][k] * Xhat[t][k]|.  1 <= n_tok <= 64. */
+int qmv_run(int fmt, const void* W, const float* x, float* y, int64_t M,
+            int64_t K, int n_tok, cudaStream_t stream);
+
+/* Same as qmv_run with pre-quantized activations (layout of
+ * qmv_quantize_act). */
+int qmv_run_q8(int fmt, const void* W, const int8_t* xq, const float* xd,
+               const int32_t* xs, float* y, int64_t M, int64_t K, int n_tok,
+               cudaStream_t stream);
+
+/* Split-K matvec for few-row, long-K shapes: K is cut into n_split contiguous
+ * ranges of whole groups; pass 1 writes partial sums partial[s][t][m] into
+ * the workspace, pass 2 adds them in the fixed order s = 0..n_split-1, so the
+ * result is bitwise reproducible for a given (shape, n_tok, n_split).
+ * n_split = 0 picks a split count from the shape (qmv_splitk_choose).
+ * ws must hold qmv_splitk_workspace_bytes(M, n_tok, n_split) bytes. */
+int qmv_splitk_choose(int fmt, int64_t M, int64_t K, int n_tok);
+size_t qmv_splitk_workspace_bytes(int64_t M, int n_tok, int n_split);
+int qmv_splitk_run(int fmt, const void* W, const float* x, float* y, int64_t M,
+                   int64_t K, int n_tok, int n_split, void* ws, size_t ws_bytes,
+                   cudaStream_t stream);
+
+/* Expert pool of one MoE FFN layer. */
+typedef struct moe_experts {
+  int32_t n_experts;   /* E */
+  int32_t hidden;      /* H: K of gate/up, M of down */
+  int32_t ffn;         /* F: rows of gate (and of up), K of down */
+  int32_t fmt_gate_up; /* any qmv_format */
+  int32_t fmt_down;    /* any qmv_format */
+  int32_t reserved;
+  const void* w_gate_up; /* [E][2F rows][row_bytes(fmt_gate_up, H)]:
+                            rows 0..F-1 gate, rows F..2F-1 up */
+  const void* w_down;    /* [E][H rows][row_bytes(fmt_down, F)] */
+} moe_experts;
+
+/* Expert-grouped MoE decode layer:
+ *   for each token t and slot k < top_k with expert e = ids[t][k]:
+ *     g = Wgate_e Xhat_t,  u = Wup_e Xhat_t          (F values each)
+ *     h = silu(g) * u,  silu(z) = z / (1 + exp(-z))  (fp32)
+ *     o_{t,k} = Wdown_e Hhat_{t,k}                   (Hhat: h quantized by
+ *                                                     the activation rule)
+ *   y[t] = sum_{k=0..top_k-1} gates[t][k] * o_{t,k}, added in k order.
+ * ids int32 [n_tok][top_k], gates fp32 [n_tok][top_k], x fp32 [n_tok][H],
+ * y fp32 [n_tok][H].  Every routed expert's weights are read once per call,
+ * for all of the tokens routed to it.  A slot whose id is outside
+ * [0, n_experts) or repeats an earlier id of the same token contributes 0 and
+ * sets the device error word.  gates are used as given (not renormalised).
+ * The workspace holds the intermediates at the offsets of
+ * moe_qmv_workspace_offsets (slot p = t * top_k + k):
+ *   [0] xq int8 [n_tok][H]   [1] xd f32 [n_tok][H/32]  [2] xs i32 [n_tok][H/32]
+ *   [3] h  f32 [n_tok*top_k][F]
+ *   [4] hq int8 [n_tok*top_k][F]  [5] hd f32 [..][F/32]  [6] hs i32 [..][F/32]
+ *   [7] o  f32 [n_tok*top_k][H]
+ * Constraints: H and F multiples of the group sizes of the two formats,
+ * 1 <= n_tok <= 64, 1 <= top_k <= 8, top_k <= n_experts. */
+size_t moe_qmv_workspace_bytes(const moe_experts* e, int n_tok, int top_k);
+int moe_qmv_workspace_offsets(const moe_experts* e, int n_tok, int top_k,
+                              size_t offsets[8]);
+int moe_qmv_run(const moe_experts* e, const int32_t* ids, const float* gates,
+                const float* x, float* y, int n_tok, int top_k, void* ws,
+                size_t ws_bytes, cudaStream_t stream);
+
+/* Synchronises `stream`, then reads and clears the device error word
+ * (QMV_DEVERR_* bits, 0 if none) into *err. */
+int qmv_get_device_error(cudaStream_t stream, int* err);
+
+/* Static description of a status code. */
+const char* qmv_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QMV_H */

@@ -1,0 +1,107 @@
+"""A second, independent reading of the byte layouts written out in
+include/qmv.h, used by the tests to build weight groups from chosen fields
+(scales, codes) and to read fields back.  It decodes nothing into values: the
+tests compute expected values from the fields themselves."""
+from __future__ import annotations
+
+import numpy as np
+
+CODEBOOK = np.array([-127, -104, -83, -65, -49, -35, -22, -10,
+                     1, 13, 25, 38, 53, 69, 89, 113], dtype=np.int64)
+
+
+def f16_bits(v) -> int:
+    return int(np.array(v, dtype=np.float64).astype(np.float16).view(np.uint16))
+
+
+def f16_value(bits) -> float:
+    return float(np.array(bits, dtype=np.uint16).view(np.float16).astype(np.float64))
+
+
+def _set_bits(buf: bytearray, byte0: int, bit: int, nbits: int, v: int):
+    for i in range(nbits):
+        b = bit + i
+        idx = byte0 + b // 8
+        if (v >> i) & 1:
+            buf[idx] |= 1 << (b % 8)
+        else:
+            buf[idx] &= ~(1 << (b % 8)) & 0xFF
+
+
+def _get_bits(buf, byte0: int, bit: int, nbits: int) -> int:
+    v = 0
+    for i in range(nbits):
+        b = bit + i
+        v |= ((buf[byte0 + b // 8] >> (b % 8)) & 1) << i
+    return v
+
+
+def _put_codes(buf: bytearray, off: int, codes):
+    """32 four-bit codes of one sub-block: byte i = c_i | c_{i+16} << 4."""
+    for i in range(16):
+        buf[off + i] = (int(codes[i]) & 0xF) | ((int(codes[i + 16]) & 0xF) << 4)
+
+
+def _get_codes(buf, off: int):
+    return [buf[off + (i % 16)] >> (0 if i < 16 else 4) & 0xF for i in range(32)]
+
+
+def pack_q8_0(d_bits, q) -> bytes:
+    """One Q8_0 group: d_bits[8] fp16 patterns, q[8][32] int8."""
+    g = bytearray(272)
+    for j in range(8):
+        g[2 * j] = d_bits[j] & 0xFF
+        g[2 * j + 1] = d_bits[j] >> 8
+        for i in range(32):
+            g[16 + 32 * j + i] = int(q[j][i]) & 0xFF
+    return bytes(g)
+
+
+def pack_q4_k(d_bits, dmin_bits, sc, m, q) -> bytes:
+    """One Q4_K group: fp16 d, dmin; sc[8], m[8] in [0,63]; q[8][32] in [0,15]."""
+    g = bytearray(144)
+    g[0], g[1] = d_bits & 0xFF, d_bits >> 8
+    g[2], g[3] = dmin_bits & 0xFF, dmin_bits >> 8
+    for j in range(8):
+        _set_bits(g, 4, 12 * j, 6, int(sc[j]))
+        _set_bits(g, 4, 12 * j + 6, 6, int(m[j]))
+        _put_codes(g, 16 + 16 * j, q[j])
+    return bytes(g)
+
+
+def pack_iq4_xs(d_bits, ls, c) -> bytes:
+    """One IQ4_XS group (2 superblocks): d_bits[2]; ls[2][8] in [0,63];
+    c[2][8][32] codebook indices."""
+    g = bytearray(272)
+    for s in range(2):
+        g[8 * s] = d_bits[s] & 0xFF
+        g[8 * s + 1] = d_bits[s] >> 8
+        for j in range(8):
+            _set_bits(g, 8 * s + 2, 6 * j, 6, int(ls[s][j]))
+            _put_codes(g, 16 + 128 * s + 16 * j, c[s][j])
+    return bytes(g)
+
+
+def unpack_q8_0(g):
+    g = [int(v) for v in bytes(bytearray(g))]
+    d_bits = [g[2 * j] | (g[2 * j + 1] << 8) for j in range(8)]
+    q = [[int(np.int8(np.uint8(g[16 + 32 * j + i]))) for i in range(32)] for j in range(8)]
+    return d_bits, q
+
+
+def unpack_q4_k(g):
+    g = [int(v) for v in bytes(bytearray(g))]
+    d_bits = g[0] | (g[1] << 8)
+    dmin_bits = g[2] | (g[3] << 8)
+    sc = [_get_bits(g, 4, 12 * j, 6) for j in range(8)]
+    m = [_get_bits(g, 4, 12 * j + 6, 6) for j in range(8)]
+    q = [_get_codes(g, 16 + 16 * j) for j in range(8)]
+    return d_bits, dmin_bits, sc, m, q
+
+
+def unpack_iq4_xs(g):
+    g = [int(v) for v in bytes(bytearray(g))]
+    d_bits = [g[8 * s] | (g[8 * s + 1] << 8) for s in range(2)]
+    ls = [[_get_bits(g, 8 * s + 2, 6 * j, 6) for j in range(8)] for s in range(2)]
+    c = [[_get_codes(g, 16 + 128 * s + 16 * j) for j in range(8)] for s in range(2)]
+    return d_bits, ls, c

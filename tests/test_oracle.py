@@ -1,0 +1,439 @@
+"""Pins of the CPU oracle against things other than itself: numpy's binary16
+rounding, brute-force argmins, hand-worked blocks, closed forms, a library
+matmul, and invariants of the method.  CPU only."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from moe_matvec_gb300 import synth
+from tests import layout_ref as L
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng0 = np.random.default_rng(12345)
+
+
+# --------------------------------------------------------------------------
+# binary16 conversions (reduce to numpy's IEEE conversion)
+# --------------------------------------------------------------------------
+
+def test_f16_decode_every_pattern():
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = pats.view(np.float16).astype(np.float64)
+    got = np.array([oracle.f16_to_f64(int(h)) for h in pats])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_f16_encode_matches_numpy_including_ties_and_subnormals():
+    vals = []
+    # random magnitudes over the whole fp16 range, both signs
+    vals += list(np.exp(rng0.uniform(np.log(1e-9), np.log(7e4), 20000)) * rng0.choice([-1, 1], 20000))
+    # exact midpoints between neighbouring fp16 values (ties), normal and subnormal
+    hs = np.arange(1, 0x7BFF, 7, dtype=np.uint16)
+    lo = hs.view(np.float16).astype(np.float64)
+    hi = (hs + 1).view(np.float16).astype(np.float64)
+    vals += list((lo + hi) / 2)
+    vals += [65504.0, 65519.99, 65520.0, 65536.0, 1e6, 2 ** -24, 2 ** -25, 3 * 2 ** -26, 2 ** -26,
+             6.1e-5, 0.0, -0.0]
+    for v in vals:
+        ref = int(np.array(v, np.float64).astype(np.float16).view(np.uint16))
+        assert oracle.f64_to_f16(v) == ref, (v, hex(ref))
+
+
+# --------------------------------------------------------------------------
+# activation quantizer
+# --------------------------------------------------------------------------
+
+def _read_golden(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            k, v = line.split(":", 1)
+            out[k.strip()] = [float(t) for t in v.split()]
+    return out
+
+
+def test_act_quant_golden_block():
+    g = _read_golden("act_quant_block.txt")
+    x = np.array(g["x"], np.float32)[None, :]
+    q, d, s = oracle.act_quant(x)
+    assert d[0, 0] == np.float32(g["d"][0])
+    assert q[0].tolist() == [int(v) for v in g["q"]]
+    assert s[0, 0] == int(g["s"][0])
+
+
+def test_act_quant_integer_block_is_exact():
+    # amax = 127 gives d = 1 and id = 1, so q = x exactly
+    x = rng0.integers(-127, 128, size=(3, 256)).astype(np.float32)
+    x[:, ::32] = 127.0
+    q, d, s = oracle.act_quant(x)
+    assert np.all(d == 1.0)
+    assert np.array_equal(q.astype(np.float32), x)
+    assert np.array_equal(s, x.reshape(3, 8, 32).sum(-1).astype(np.int32))
+
+
+def test_act_quant_power_of_two_scale():
+    k = rng0.integers(-127, 128, size=(2, 512))
+    k[:, ::32] = -127
+    x = (k * 2.0 ** -9).astype(np.float32)
+    q, d, s = oracle.act_quant(x)
+    assert np.all(d == np.float32(2.0 ** -9))
+    assert np.array_equal(q.astype(np.int64), k)
+
+
+def test_act_quant_zero_block():
+    x = rng0.standard_normal((1, 128)).astype(np.float32)
+    x[0, 32:64] = 0.0
+    q, d, s = oracle.act_quant(x)
+    assert d[0, 1] == 0.0 and s[0, 1] == 0 and not q[0, 32:64].any()
+
+
+@pytest.mark.parametrize("scale", [1.0, 1e-3, 37.0])
+def test_act_quant_invariants(scale):
+    x = (rng0.standard_normal((4, 1024)) * scale).astype(np.float32)
+    x[1] = rng0.standard_cauchy(1024).astype(np.float32) * np.float32(scale)
+    q, d, s = oracle.act_quant(x)
+    qb = q.reshape(4, 32, 32).astype(np.int64)
+    xb = x.reshape(4, 32, 32).astype(np.float64)
+    amax = np.abs(xb).max(-1)
+    assert np.all(d == (amax.astype(np.float32) / np.float32(127)))
+    assert np.all(np.abs(qb) <= 127)
+    assert np.all(np.abs(qb).max(-1) == 127)           # the largest element maps to 127
+    assert np.array_equal(s, qb.sum(-1).astype(np.int32))
+    assert np.all(np.sign(qb) * np.sign(xb) >= 0)       # never flips a sign
+    err = np.abs(xb - d[..., None].astype(np.float64) * qb)
+    assert np.all(err <= d[..., None] * (0.5 + 1e-5))   # nearest grid point
+
+
+# --------------------------------------------------------------------------
+# weight quantizers
+# --------------------------------------------------------------------------
+
+def _rand_w(M, K, std=0.02, seed=7):
+    return synth.weights(seed, M, K, std)
+
+
+def test_q8_0_scales_and_codes_are_argmins():
+    w = _rand_w(3, 512)
+    W = oracle.quantize(0, w)
+    for m in range(3):
+        for gi in range(2):
+            d_bits, q = L.unpack_q8_0(W[m, 272 * gi:272 * (gi + 1)])
+            for j in range(8):
+                wb = w[m, 256 * gi + 32 * j: 256 * gi + 32 * j + 32].astype(np.float64)
+                assert d_bits[j] == L.f16_bits(np.abs(wb).max() / 127.0)
+                dv = L.f16_value(d_bits[j])
+                cand = np.arange(-127, 128)
+                err = np.abs(wb[:, None] - dv * cand[None, :])
+                best = cand[np.argmin(err, axis=1)]
+                assert q[j] == best.tolist()
+
+
+def test_q8_0_ties_go_to_even():
+    # d = 2^-7 exactly (amax = 127 * 2^-7); weights on exact half-steps
+    w = np.zeros((1, 256), np.float32)
+    w[0, 0] = 127 * 2.0 ** -7
+    w[0, 1:6] = np.array([2.5, 3.5, -2.5, -3.5, 0.5]) * 2.0 ** -7
+    W = oracle.quantize(0, w)
+    d_bits, q = L.unpack_q8_0(W[0])
+    assert L.f16_value(d_bits[0]) == 2.0 ** -7
+    assert q[0][:6] == [127, 2, 4, -2, -4, 0]
+
+
+def test_q8_0_requantization_is_idempotent():
+    w = _rand_w(4, 1024)
+    W = oracle.quantize(0, w)
+    wh = oracle.dequant(0, W, 1024).astype(np.float32)
+    assert np.array_equal(oracle.quantize(0, wh), W)
+
+
+def test_q4_k_fields_follow_the_rule_and_codes_are_argmins():
+    w = _rand_w(2, 512)
+    w[1, :32] = np.abs(w[1, :32])          # a sub-block with no negative weight
+    w[1, 32:64] = -np.abs(w[1, 32:64])     # and one with no positive weight
+    W = oracle.quantize(1, w)
+    for m in range(2):
+        for gi in range(2):
+            d_bits, dmin_bits, sc, mm, q = L.unpack_q4_k(W[m, 144 * gi:144 * (gi + 1)])
+            wg = w[m, 256 * gi:256 * (gi + 1)].astype(np.float64).reshape(8, 32)
+            lo = np.minimum(0.0, wg.min(1))
+            a = (wg.max(1) - lo) / 15.0
+            b = -lo
+            assert d_bits == L.f16_bits(a.max() / 63.0)
+            assert dmin_bits == L.f16_bits(b.max() / 63.0)
+            d, dmin = L.f16_value(d_bits), L.f16_value(dmin_bits)
+            assert sc == np.clip(np.rint(a / d), 0, 63).astype(int).tolist()
+            assert mm == np.clip(np.rint(b / dmin), 0, 63).astype(int).tolist()
+            for j in range(8):
+                grid = d * sc[j] * np.arange(16) - dmin * mm[j]
+                err = np.abs(wg[j][:, None] - grid[None, :])
+                assert q[j] == np.argmin(err, axis=1).tolist()   # argmin keeps the lower q on ties
+
+
+def test_iq4_xs_fields_follow_the_rule_and_codes_are_argmins():
+    w = _rand_w(2, 1024)
+    W = oracle.quantize(2, w)
+    for m in range(2):
+        for gi in range(2):
+            d_bits, ls, c = L.unpack_iq4_xs(W[m, 272 * gi:272 * (gi + 1)])
+            for s in range(2):
+                wg = w[m, 512 * gi + 256 * s: 512 * gi + 256 * (s + 1)].astype(np.float64).reshape(8, 32)
+                sj = np.abs(wg).max(1) / 113.0
+                assert d_bits[s] == L.f16_bits(sj.max() / 31.0)
+                d = L.f16_value(d_bits[s])
+                assert ls[s] == (32 + np.clip(np.rint(sj / d), 0, 31)).astype(int).tolist()
+                for j in range(8):
+                    grid = d * (ls[s][j] - 32) * L.CODEBOOK
+                    err = np.abs(wg[j][:, None] - grid[None, :])
+                    assert c[s][j] == np.argmin(err, axis=1).tolist()
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+def test_zero_weights_dequantize_to_zero(fmt):
+    w = _rand_w(2, 512)
+    w[0] = 0.0
+    W = oracle.quantize(fmt, w)
+    wh = oracle.dequant(fmt, W, 512)
+    assert np.all(wh[0] == 0.0)
+
+
+def test_round_trip_error_bounds():
+    w = _rand_w(8, 1024).astype(np.float64)
+    # Q8_0: at most half a step of the stored scale, plus the scale's own rounding
+    W = oracle.quantize(0, w.astype(np.float32))
+    err = np.abs(oracle.dequant(0, W, 1024) - w).reshape(8, 32, 32)
+    amax = np.abs(w).reshape(8, 32, 32).max(-1)
+    d = amax / 127.0
+    assert np.all(err.max(-1) <= d * (0.5 + 127 * 2.0 ** -11) + 1e-12)
+    # Q4_K: codes land on a 16-point grid covering [lo, hi] of each sub-block
+    W = oracle.quantize(1, w.astype(np.float32))
+    err = np.abs(oracle.dequant(1, W, 1024) - w).reshape(8, 32, 32)
+    rngb = (w.reshape(8, 32, 32).max(-1) - np.minimum(0, w.reshape(8, 32, 32).min(-1)))
+    assert np.all(err.max(-1) <= rngb / 15.0 * 0.5 * 1.2 + 1e-4)
+    # IQ4_XS: the largest codebook gap is 24 (89 -> 113), so half a gap is 12 steps
+    W = oracle.quantize(2, w.astype(np.float32))
+    err = np.abs(oracle.dequant(2, W, 1024) - w).reshape(8, 32, 32)
+    s = np.abs(w).reshape(8, 32, 32).max(-1) / 113.0
+    assert np.all(err.max(-1) <= 14.5 * s * 1.1 + 1e-4)
+
+
+# --------------------------------------------------------------------------
+# dequantizers: hand-worked groups
+# --------------------------------------------------------------------------
+
+def test_dequant_q8_0_hand_worked():
+    d_bits = [0x3800] * 8          # 0.5
+    d_bits[3] = 0xB400             # -0.25
+    q = [[(i - 16) for i in range(32)] for _ in range(8)]
+    g = np.frombuffer(L.pack_q8_0(d_bits, q), np.uint8)[None, :]
+    wh = oracle.dequant(0, g, 256)
+    assert wh[0, 0] == -8.0 and wh[0, 31] == 7.5 and wh[0, 17] == 0.5
+    assert wh[0, 96] == 4.0 and wh[0, 127] == -3.75          # block 3 scaled by -0.25
+
+
+def test_dequant_q4_k_hand_worked():
+    sc = [1, 2, 3, 4, 5, 6, 7, 63]
+    m = [0, 1, 2, 3, 4, 5, 62, 63]
+    q = [[i % 16 for i in range(32)] for _ in range(8)]
+    q[7] = [15 - (i % 16) for i in range(32)]
+    g = np.frombuffer(L.pack_q4_k(0x3400, 0x3000, sc, m, q), np.uint8)[None, :]   # d 0.25, dmin 0.125
+    wh = oracle.dequant(1, g, 256)
+    # weight 5 of sub-block 1: 0.25*2*5 - 0.125*1
+    assert wh[0, 32 + 5] == 2.375
+    # weight 20 of sub-block 6 (high nibble of byte 4): 0.25*7*4 - 0.125*62
+    assert wh[0, 6 * 32 + 20] == 7.0 - 7.75
+    # weight 0 of sub-block 7: q = 15: 0.25*63*15 - 0.125*63
+    assert wh[0, 224] == 236.25 - 7.875
+
+
+def test_dequant_iq4_xs_hand_worked():
+    ls = [[32, 33, 31, 63, 0, 40, 32, 34], [35] * 8]
+    c = [[[i % 16 for i in range(32)] for _ in range(8)] for _ in range(2)]
+    g = np.frombuffer(L.pack_iq4_xs([0x2400, 0x3C00], ls, c), np.uint8)[None, :]   # 2^-6, 1.0
+    wh = oracle.dequant(2, g, 512)
+    assert wh[0, 0] == 0.0                                   # ls 32 -> zero scale
+    assert wh[0, 32 + 3] == 2.0 ** -6 * 1 * -65              # ls 33, code 3
+    assert wh[0, 64 + 17] == 2.0 ** -6 * -1 * -104           # ls 31 (negative scale), code 1
+    assert wh[0, 96 + 31] == 2.0 ** -6 * 31 * 113            # ls 63, code 15
+    assert wh[0, 128 + 8] == 2.0 ** -6 * -32 * 1             # ls 0, code 8
+    assert wh[0, 256 + 100] == 3.0 * L.CODEBOOK[100 % 32 % 16]
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+def test_dequant_random_fields(fmt):
+    r = np.random.default_rng(fmt + 100)
+    if fmt == 0:
+        d = [L.f16_bits(v) for v in r.uniform(-1, 1, 8)]
+        q = r.integers(-128, 128, (8, 32)).tolist()
+        g = L.pack_q8_0(d, q)
+        exp = np.concatenate([L.f16_value(d[j]) * np.array(q[j], float) for j in range(8)])
+        K = 256
+    elif fmt == 1:
+        d, dm = L.f16_bits(r.uniform(0, 1)), L.f16_bits(r.uniform(0, 1))
+        sc, m = r.integers(0, 64, 8).tolist(), r.integers(0, 64, 8).tolist()
+        q = r.integers(0, 16, (8, 32)).tolist()
+        g = L.pack_q4_k(d, dm, sc, m, q)
+        exp = np.concatenate([L.f16_value(d) * sc[j] * np.array(q[j], float) - L.f16_value(dm) * m[j]
+                              for j in range(8)])
+        K = 256
+    else:
+        d = [L.f16_bits(v) for v in r.uniform(-1, 1, 2)]
+        ls = r.integers(0, 64, (2, 8)).tolist()
+        c = r.integers(0, 16, (2, 8, 32)).tolist()
+        g = L.pack_iq4_xs(d, ls, c)
+        exp = np.concatenate([L.f16_value(d[s]) * (ls[s][j] - 32) * L.CODEBOOK[np.array(c[s][j])]
+                              for s in range(2) for j in range(8)])
+        K = 512
+    wh = oracle.dequant(fmt, np.frombuffer(g, np.uint8)[None, :], K)
+    assert np.array_equal(wh[0], exp)
+
+
+# --------------------------------------------------------------------------
+# matvec
+# --------------------------------------------------------------------------
+
+def _xhat(x):
+    q, d, _ = oracle.act_quant(x)
+    return q.astype(np.float64) * np.repeat(d.astype(np.float64), 32, axis=1)
+
+
+@pytest.mark.parametrize("fmt,K", [(0, 512), (1, 768), (2, 1024)])
+def test_qmv_matches_library_matmul(fmt, K):
+    w = _rand_w(37, K, seed=fmt)
+    x = synth.activations(fmt, 5, K)
+    W = oracle.quantize(fmt, w)
+    y, sabs = oracle.qmv(fmt, W, x, K)
+    wh = oracle.dequant(fmt, W, K)
+    xh = _xhat(x)
+    ref = xh @ wh.T
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+    assert np.allclose(sabs, np.abs(xh) @ np.abs(wh).T, rtol=1e-12)
+    assert np.all(sabs >= np.abs(y))
+
+
+def test_qmv_closed_form_power_of_two():
+    r = np.random.default_rng(3)
+    K = 512
+    q = r.integers(-127, 128, (2, 16, 32))
+    W = np.stack([np.concatenate([np.frombuffer(L.pack_q8_0([0x3000] * 8, q[m, 8 * gi:8 * gi + 8]), np.uint8)
+                                  for gi in range(2)]) for m in range(2)])   # d = 2^-3
+    kx = r.integers(-127, 128, (3, K))
+    kx[:, ::32] = 127
+    x = (kx * 2.0 ** -2).astype(np.float32)    # d_x = 2^-2, q_x = kx
+    y, _ = oracle.qmv(0, W, x, K)
+    exact = (kx @ q.reshape(2, K).T) * 2.0 ** -5
+    assert np.array_equal(y, exact.astype(np.float64))
+
+
+def test_qmv_one_hot_row_selects_xhat():
+    K = 256
+    q = [[0] * 32 for _ in range(8)]
+    q[5][7] = 1
+    W = np.frombuffer(L.pack_q8_0([0x3C00] * 8, q), np.uint8)[None, :]
+    x = synth.activations(11, 4, K)
+    y, _ = oracle.qmv(0, W, x, K)
+    assert np.array_equal(y[:, 0], _xhat(x)[:, 5 * 32 + 7])
+
+
+def test_qmv_tokens_are_independent_and_threads_agree():
+    K = 1024
+    W = oracle.quantize(2, _rand_w(50, K))
+    x = synth.activations(3, 6, K)
+    y, _ = oracle.qmv(2, W, x, K)
+    for t in range(6):
+        yt, _ = oracle.qmv(2, W, x[t:t + 1], K)
+        assert np.array_equal(yt[0], y[t])
+    y4, _ = oracle.qmv(2, W, x, K, nthreads=4)
+    assert np.array_equal(y4, y)
+
+
+# --------------------------------------------------------------------------
+# MoE
+# --------------------------------------------------------------------------
+
+E, H, F, TOPK = 6, 512, 512, 3
+
+
+def _moe_pool(seed=5, identical=False):
+    Wgu = np.stack([oracle.quantize(2, _rand_w(2 * F, H, seed=seed + (0 if identical else e)))
+                    for e in range(E)])
+    Wd = np.stack([oracle.quantize(1, _rand_w(H, F, seed=seed + 50 + (0 if identical else e)))
+                   for e in range(E)])
+    return Wgu, Wd
+
+
+def test_synth_routing_properties():
+    ids, g = synth.routing(9, 64, 128, 8)
+    assert all(len(set(r)) == 8 for r in ids.tolist())
+    assert ids.min() >= 0 and ids.max() < 128
+    assert np.all(np.abs(g.sum(1, dtype=np.float64) - 1.0) <= 8 * 2.0 ** -24)
+    assert np.all(g > 0)
+
+
+def test_moe_top1_reduces_to_matvec_chain():
+    Wgu, Wd = _moe_pool()
+    x = synth.activations(1, 2, H)
+    ids = np.array([[4], [1]], np.int32)
+    gates = np.ones((2, 1), np.float32)
+    out = oracle.moe(2, Wgu, 1, Wd, E, H, F, ids, gates, x)
+    for t in range(2):
+        e = ids[t, 0]
+        gu, _ = oracle.qmv(2, Wgu[e], x[t:t + 1], H)
+        g, u = gu[0, :F], gu[0, F:]
+        h = (g / (1.0 + np.exp(-g)) * u).astype(np.float32)
+        assert np.array_equal(out["h32"][t], h)
+        yd, _ = oracle.qmv(1, Wd[e], h[None, :], F)
+        assert np.allclose(out["y"][t], yd[0], rtol=1e-13, atol=1e-15)
+
+
+def test_moe_identical_experts_give_the_dense_ffn():
+    Wgu, Wd = _moe_pool(identical=True)
+    x = synth.activations(2, 3, H)
+    ids, gates = synth.routing(4, 3, E, TOPK)
+    out = oracle.moe(2, Wgu, 1, Wd, E, H, F, ids, gates, x)
+    one = oracle.moe(2, Wgu, 1, Wd, E, H, F, ids[:, :1], np.ones((3, 1), np.float32), x)
+    gs = gates.astype(np.float64).sum(1, keepdims=True)
+    assert np.allclose(out["y"], one["y"] * gs, rtol=1e-12, atol=1e-14)
+
+
+def test_moe_expert_relabelling_is_bitwise_invariant():
+    Wgu, Wd = _moe_pool()
+    x = synth.activations(3, 4, H)
+    ids, gates = synth.routing(6, 4, E, TOPK)
+    perm = np.random.default_rng(0).permutation(E)       # new label of old expert e is perm[e]
+    Wgu2 = np.empty_like(Wgu)
+    Wd2 = np.empty_like(Wd)
+    Wgu2[perm] = Wgu
+    Wd2[perm] = Wd
+    a = oracle.moe(2, Wgu, 1, Wd, E, H, F, ids, gates, x)["y"]
+    b = oracle.moe(2, Wgu2, 1, Wd2, E, H, F, perm[ids].astype(np.int32), gates, x)["y"]
+    assert np.array_equal(a, b)
+
+
+def test_moe_invalid_slots_contribute_zero():
+    Wgu, Wd = _moe_pool()
+    x = synth.activations(4, 2, H)
+    ids = np.array([[0, 9, 2], [3, 3, 1]], np.int32)      # out of range; duplicate
+    gates = np.array([[0.5, 0.3, 0.2], [0.4, 0.35, 0.25]], np.float32)
+    bad = oracle.moe(2, Wgu, 1, Wd, E, H, F, ids, gates, x)
+    ok_ids = np.array([[0, 5, 2], [3, 4, 1]], np.int32)
+    ok_g = gates.copy()
+    ok_g[0, 1] = 0.0
+    ok_g[1, 1] = 0.0
+    ref = oracle.moe(2, Wgu, 1, Wd, E, H, F, ok_ids, ok_g, x)
+    assert np.array_equal(bad["y"], ref["y"])
+    assert not oracle.moe_slot_valid(ids, E, 0, 1) and not oracle.moe_slot_valid(ids, E, 1, 1)
+
+
+def test_moe_given_h_reproduces_the_computed_path():
+    Wgu, Wd = _moe_pool()
+    x = synth.activations(5, 3, H)
+    ids, gates = synth.routing(8, 3, E, TOPK)
+    a = oracle.moe(2, Wgu, 1, Wd, E, H, F, ids, gates, x)
+    b = oracle.moe(2, Wgu, 1, Wd, E, H, F, ids, gates, x, h_in=a["h32"])
+    assert np.array_equal(a["y"], b["y"]) and np.array_equal(a["hq"], b["hq"])
