@@ -59,8 +59,9 @@
  * ------------------------------------------------------------------------
  * QMV_Q8_0: blocks of 32 weights, What = d * q, d fp16, q int8.
  *   Group = 8 blocks (256 weights), 272 bytes:
- *     header  bytes [2j, 2j+2)   : d of block j (j = 0..7)
- *     payload bytes [32j, 32j+32): q_0..q_31 of block j (int8)
+ *     header  bytes [2j, 2j+2)        : d of block j (j = 0..7)
+ *     payload bytes [16j, 16j+16)     : q_0..q_15 of block j (int8)
+ *             bytes [128+16j, 144+16j): q_16..q_31 of block j
  *   K % 256 == 0; row bytes = 272 * K / 256.
  *
  * QMV_Q4_K: superblocks of 256 weights = 8 sub-blocks of 32,

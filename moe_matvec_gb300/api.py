@@ -1,0 +1,211 @@
+"""Python binding of the C-ABI library libqmv.so (see include/qmv.h).
+
+Argument marshalling only: every computation runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors (PyTorch supplies device memory and
+the current stream); results are returned as new tensors unless `out` is
+given.  There is no CPU fallback: importing this module without a buildable
+library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+Q8_0, Q4_K, IQ4_XS = 0, 1, 2
+FORMATS = {"Q8_0": Q8_0, "Q4_K": Q4_K, "IQ4_XS": IQ4_XS}
+GROUP_WEIGHTS = {Q8_0: 256, Q4_K: 256, IQ4_XS: 512}
+BYTES_PER_WEIGHT = {Q8_0: 272 / 256, Q4_K: 144 / 256, IQ4_XS: 272 / 512}
+MAX_TOKENS = 64
+MAX_TOPK = 8
+
+DEVERR_EXPERT_RANGE = 0x1
+DEVERR_EXPERT_DUP = 0x2
+DEVERR_TIMEOUT = 0x4
+
+
+class QmvError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {strerror(code)} ({code})")
+        self.code = code
+
+
+class MoeExperts(ctypes.Structure):
+    _fields_ = [("n_experts", ctypes.c_int32), ("hidden", ctypes.c_int32), ("ffn", ctypes.c_int32),
+                ("fmt_gate_up", ctypes.c_int32), ("fmt_down", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("w_gate_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p)]
+
+
+_i64, _vp, _int, _sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_SIGS = {
+    "qmv_row_bytes": (_i64, [_int, _i64]),
+    "qmv_quantize_weights": (_int, [_int, _vp, _i64, _i64, _vp, _vp]),
+    "qmv_quantize_act": (_int, [_vp, _i64, _int, _vp, _vp, _vp, _vp]),
+    "qmv_run": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _int, _vp]),
+    "qmv_run_q8": (_int, [_int, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _vp]),
+    "qmv_splitk_choose": (_int, [_int, _i64, _i64, _int]),
+    "qmv_splitk_workspace_bytes": (_sz, [_i64, _int, _int]),
+    "qmv_splitk_run": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _int, _int, _vp, _sz, _vp]),
+    "moe_qmv_workspace_bytes": (_sz, [ctypes.POINTER(MoeExperts), _int, _int]),
+    "moe_qmv_workspace_offsets": (_int, [ctypes.POINTER(MoeExperts), _int, _int, ctypes.POINTER(_sz * 8)]),
+    "moe_qmv_run": (_int, [ctypes.POINTER(MoeExperts), _vp, _vp, _vp, _vp, _int, _int, _vp, _sz, _vp]),
+    "qmv_get_device_error": (_int, [_vp, ctypes.POINTER(_int)]),
+    "qmv_strerror": (ctypes.c_char_p, [_int]),
+}
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) libqmv.so and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.build()
+    if not os.path.exists(path):
+        raise ImportError(f"libqmv.so not found at {path}")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name, None)
+        if fn is None:
+            continue
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def strerror(code: int) -> str:
+    return load().qmv_strerror(int(code)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise QmvError(rc, what)
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def row_bytes(fmt: int, K: int) -> int:
+    rb = load().qmv_row_bytes(int(fmt), int(K))
+    _check(rb if rb < 0 else 0, "qmv_row_bytes")
+    return int(rb)
+
+
+def quantize_weights(fmt: int, w: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """fp32 weights [M][K] -> quantized rows uint8 [M][row_bytes]."""
+    M, K = w.shape
+    rb = row_bytes(fmt, K)
+    if out is None:
+        out = torch.empty((M, rb), dtype=torch.uint8, device=w.device)
+    _check(load().qmv_quantize_weights(int(fmt), _ptr(w), M, K, _ptr(out), _stream(stream)), "qmv_quantize_weights")
+    return out
+
+
+def quantize_act(x: torch.Tensor, stream=None):
+    """Activation rule on x fp32 [n][K] -> (q int8 [n][K], d fp32 [n][K/32], s int32 [n][K/32])."""
+    n, K = x.shape
+    q = torch.empty((n, K), dtype=torch.int8, device=x.device)
+    d = torch.empty((n, K // 32), dtype=torch.float32, device=x.device)
+    s = torch.empty((n, K // 32), dtype=torch.int32, device=x.device)
+    _check(load().qmv_quantize_act(_ptr(x), K, n, _ptr(q), _ptr(d), _ptr(s), _stream(stream)), "qmv_quantize_act")
+    return q, d, s
+
+
+def run(fmt: int, W: torch.Tensor, x: torch.Tensor, M: int, K: int, out: torch.Tensor | None = None,
+        stream=None) -> torch.Tensor:
+    """y [n][M] = What x Xhat (quantized matvec), x fp32 [n][K]."""
+    n = x.shape[0]
+    if out is None:
+        out = torch.empty((n, M), dtype=torch.float32, device=x.device)
+    _check(load().qmv_run(int(fmt), _ptr(W), _ptr(x), _ptr(out), M, K, n, _stream(stream)), "qmv_run")
+    return out
+
+
+def run_q8(fmt: int, W: torch.Tensor, xq: torch.Tensor, xd: torch.Tensor, xs: torch.Tensor, M: int, K: int,
+           out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Matvec with activations already quantized by quantize_act."""
+    n = xq.shape[0]
+    if out is None:
+        out = torch.empty((n, M), dtype=torch.float32, device=xq.device)
+    _check(load().qmv_run_q8(int(fmt), _ptr(W), _ptr(xq), _ptr(xd), _ptr(xs), _ptr(out), M, K, n, _stream(stream)),
+           "qmv_run_q8")
+    return out
+
+
+def splitk_choose(fmt: int, M: int, K: int, n_tok: int) -> int:
+    s = load().qmv_splitk_choose(int(fmt), M, K, n_tok)
+    _check(s if s < 0 else 0, "qmv_splitk_choose")
+    return int(s)
+
+
+def splitk_workspace_bytes(M: int, n_tok: int, n_split: int) -> int:
+    return int(load().qmv_splitk_workspace_bytes(M, n_tok, n_split))
+
+
+def splitk_run(fmt: int, W: torch.Tensor, x: torch.Tensor, M: int, K: int, n_split: int = 0,
+               ws: torch.Tensor | None = None, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Split-K matvec; n_split = 0 picks the split from the shape."""
+    n = x.shape[0]
+    if n_split == 0:
+        n_split = splitk_choose(fmt, M, K, n)
+    if out is None:
+        out = torch.empty((n, M), dtype=torch.float32, device=x.device)
+    need = splitk_workspace_bytes(M, n, n_split) if n_split > 1 else 0
+    if ws is None and need:
+        ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+    wsb = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(load().qmv_splitk_run(int(fmt), _ptr(W), _ptr(x), _ptr(out), M, K, n, n_split, _ptr(ws), wsb,
+                                 _stream(stream)), "qmv_splitk_run")
+    return out
+
+
+def moe_experts(n_experts: int, hidden: int, ffn: int, fmt_gate_up: int, fmt_down: int, w_gate_up: torch.Tensor,
+                w_down: torch.Tensor) -> MoeExperts:
+    return MoeExperts(n_experts, hidden, ffn, fmt_gate_up, fmt_down, 0, _ptr(w_gate_up), _ptr(w_down))
+
+
+def moe_workspace_bytes(e: MoeExperts, n_tok: int, top_k: int) -> int:
+    return int(load().moe_qmv_workspace_bytes(ctypes.byref(e), n_tok, top_k))
+
+
+def moe_workspace_offsets(e: MoeExperts, n_tok: int, top_k: int):
+    arr = (_sz * 8)()
+    _check(load().moe_qmv_workspace_offsets(ctypes.byref(e), n_tok, top_k, ctypes.byref(arr)),
+           "moe_qmv_workspace_offsets")
+    return list(arr)
+
+
+def moe_run(e: MoeExperts, ids: torch.Tensor, gates: torch.Tensor, x: torch.Tensor, ws: torch.Tensor | None = None,
+            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Expert-grouped MoE decode layer; ids int32 [n][top_k], gates fp32 [n][top_k], x fp32 [n][hidden]."""
+    n, top_k = ids.shape
+    if out is None:
+        out = torch.empty((n, e.hidden), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = torch.empty(moe_workspace_bytes(e, n, top_k), dtype=torch.uint8, device=x.device)
+    _check(load().moe_qmv_run(ctypes.byref(e), _ptr(ids), _ptr(gates), _ptr(x), _ptr(out), n, top_k, _ptr(ws),
+                              ws.numel(), _stream(stream)), "moe_qmv_run")
+    return out
+
+
+def get_device_error(stream=None) -> int:
+    v = _int(0)
+    _check(load().qmv_get_device_error(_stream(stream), ctypes.byref(v)), "qmv_get_device_error")
+    return int(v.value)

@@ -1,0 +1,163 @@
+// Device-side building blocks shared by the qmv kernels: format constants,
+// mbarrier / TMA wrappers (inline PTX for sm_103a), bounded waits, the device
+// error word and the per-32 activation quantizer.
+#pragma once
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qmv.h"
+
+namespace qmv {
+
+// ---------------------------------------------------------------------------
+// Format geometry.  A "chunk" is the K-slice one pipeline stage carries:
+// 1024 weights = 32 sub-blocks of 32, one sub-block per lane.
+// ---------------------------------------------------------------------------
+constexpr int KCHUNK = 1024;
+constexpr int BLK = 32;
+
+template <int F>
+struct Fmt;
+template <>
+struct Fmt<QMV_Q8_0> {
+  static constexpr int GW = 256, GB = 272;  // weights / bytes per group
+};
+template <>
+struct Fmt<QMV_Q4_K> {
+  static constexpr int GW = 256, GB = 144;
+};
+template <>
+struct Fmt<QMV_IQ4_XS> {
+  static constexpr int GW = 512, GB = 272;
+};
+template <int F>
+constexpr int chunk_bytes() {
+  return (KCHUNK / Fmt<F>::GW) * Fmt<F>::GB;
+}
+
+// ---------------------------------------------------------------------------
+// Device error word (QMV_DEVERR_* bits).
+// ---------------------------------------------------------------------------
+// The word lives in the dispatcher's unit; kernels receive its address.
+__device__ __forceinline__ void set_error(unsigned* err, unsigned bits) {
+  if (err) atomicOr(err, bits);
+}
+
+// ---------------------------------------------------------------------------
+// Shared-memory address helpers and mbarriers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: gives up after ~2^31 SM cycles (about a second), sets the
+// timeout bit and returns false.  No wait in this library is unbounded.
+constexpr long long WAIT_CYCLES = 1ll << 31;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > WAIT_CYCLES) {
+      set_error(err, QMV_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// L2 policy for streamed weights: evict first, so activations and outputs
+// stay resident.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 2-D tiled TMA load (global -> shared, completion on an mbarrier).  x is the
+// innermost coordinate in elements of the map (8-byte elements here), which
+// keeps every x * 8 a multiple of 16 bytes because group sizes are.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Named barrier over `nthreads` threads (the consumer warps).
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Programmatic dependent launch: wait for the preceding grid's results
+// (no-op when launched without the attribute).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Loads that bypass L1 for data read once.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float ldg_stream(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Activation quantization of one 32-element block held one element per lane
+// (every lane of the warp participates).  Rule: amax = max |x|;
+// d = amax / 127; id = 1 / d (0 if d == 0); q = rne(x * id) in [-127, 127];
+// s = sum q.  The divisions are IEEE (no fast-math), the product is an
+// explicit round-to-nearest multiply, so the codes are bit-identical to any
+// IEEE fp32 implementation of the rule.
+// ---------------------------------------------------------------------------
+struct ActQ {
+  int q;
+  float d;
+  int s;
+};
+__device__ __forceinline__ ActQ act_quant_lane(float x) {
+  unsigned ab = __float_as_uint(fabsf(x));
+  unsigned mb = __reduce_max_sync(0xffffffffu, ab);
+  float amax = __uint_as_float(mb);
+  float d = __fdiv_rn(amax, 127.0f);
+  float id = d > 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+  int q = __float2int_rn(__fmul_rn(x, id));
+  q = max(-127, min(127, q));
+  int s = __reduce_add_sync(0xffffffffu, q);
+  return {q, d, s};
+}
+
+}  // namespace qmv

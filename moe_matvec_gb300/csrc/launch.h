@@ -1,0 +1,43 @@
+// Host-side launch descriptors shared between the C-ABI dispatcher and the
+// per-format kernel instantiation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qmv {
+
+struct DenseParams;
+
+struct DenseLaunch {
+  const DenseParams* p;
+  CUtensorMap map_tile;  // box: TILE_ROWS rows x one chunk
+  CUtensorMap map_unit;  // box: UNIT_ROWS rows x one chunk
+  int nt_tmpl;           // compiled token count (1, 2, 4, 8, 16)
+  int grid;
+  size_t smem;
+  cudaStream_t stream;
+  bool pdl;
+};
+
+cudaError_t launch_dense_q8_0(const DenseLaunch& L);
+cudaError_t launch_dense_q4_k(const DenseLaunch& L);
+cudaError_t launch_dense_iq4_xs(const DenseLaunch& L);
+
+cudaError_t launch_act_quant(const float* x, int K, int n_tok, int8_t* q, float* d, int32_t* s,
+                             cudaStream_t stream, bool pdl);
+cudaError_t launch_splitk_reduce(const float* partial, float* y, long long M, int n_tok, int n_split,
+                                 cudaStream_t stream, bool pdl);
+cudaError_t launch_quantize_weights(int fmt, const float* w, long long M, int K, void* W, cudaStream_t stream);
+
+// Maximum dynamic shared memory a CTA may use on the current device.
+int device_smem_optin();
+unsigned* device_error_word();  // address of the device error word (current device)
+int device_sm_count();
+
+// Fill a launch config with the optional programmatic-dependent-launch
+// attribute (attr must outlive the launch call).
+void make_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, dim3 grid, dim3 block, size_t smem,
+                 cudaStream_t stream, bool pdl);
+
+}  // namespace qmv

@@ -1,0 +1,337 @@
+// C ABI of the library (declared in include/qmv.h): argument checking, launch
+// geometry, TMA descriptors and kernel dispatch.  Nothing here allocates.
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "launch.h"
+#include "qmv_dense.cuh"
+
+namespace qmv {
+
+static __device__ unsigned int g_qmv_error = 0;
+
+// ---------------------------------------------------------------------------
+// Device facts (cached per device ordinal).
+// ---------------------------------------------------------------------------
+struct DevInfo {
+  int sms = 0, smem_optin = 0, major = 0, minor = 0;
+  unsigned* err = nullptr;
+  bool ok = false;
+};
+static DevInfo g_dev[64];
+static std::mutex g_dev_mu;
+
+static const DevInfo* dev_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.ok) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return nullptr;
+    if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return nullptr;
+    cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
+    void* ep = nullptr;
+    if (cudaGetSymbolAddress(&ep, g_qmv_error) == cudaSuccess) d.err = static_cast<unsigned*>(ep);
+    d.ok = true;
+  }
+  return &d;
+}
+
+int device_smem_optin() {
+  const DevInfo* d = dev_info();
+  return d ? d->smem_optin : 0;
+}
+unsigned* device_error_word() {
+  const DevInfo* d = dev_info();
+  return d ? d->err : nullptr;
+}
+int device_sm_count() {
+  const DevInfo* d = dev_info();
+  return d ? d->sms : 1;
+}
+
+// ---------------------------------------------------------------------------
+// Tensor-map encoder from the driver, reached through the runtime (no link
+// against libcuda).
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
+
+static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// 2-D map over a weight matrix seen as rows x (row_bytes / 8) 8-byte
+// elements; box = box_rows x (box_bytes / 8).
+static bool encode_rows(CUtensorMap* map, const void* W, long long rows, long long row_bytes, int box_bytes,
+                        int box_rows) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 8), (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)(box_bytes / 8), (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(W), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// Validation helpers.
+// ---------------------------------------------------------------------------
+static int group_weights(int fmt) { return fmt == QMV_IQ4_XS ? 512 : 256; }
+static int group_bytes(int fmt) { return fmt == QMV_Q4_K ? 144 : 272; }
+static int chunk_bytes_of(int fmt) { return (KCHUNK / group_weights(fmt)) * group_bytes(fmt); }
+static bool fmt_ok(int fmt) { return fmt == QMV_Q8_0 || fmt == QMV_Q4_K || fmt == QMV_IQ4_XS; }
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+constexpr long long MAX_K = 1ll << 20;
+constexpr long long MAX_M = 1ll << 30;
+
+static int check_device() {
+  const DevInfo* d = dev_info();
+  if (!d) return QMV_ERR_CUDA;
+  if (d->major != 10 || d->minor != 3) return QMV_ERR_DEVICE;
+  return QMV_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Dense / split-K launch planning.
+// ---------------------------------------------------------------------------
+struct Plan {
+  int nt_tmpl, passes_tok, stages, grid;
+  int act_stride, act_blk;
+  size_t smem;
+};
+
+static size_t act_bytes(int nt, int act_stride, int act_blk) {
+  return (size_t)nt * act_stride + 2 * (size_t)nt * act_blk * sizeof(float);
+}
+
+// Choose the compiled token count and the number of stages so that the
+// activation area plus at least two weight stages fit in shared memory.
+static bool plan_dense(int fmt, long long M, long long K, int n_tok, int n_split, Plan& pl) {
+  const int gw = group_weights(fmt);
+  const long long groups = K / gw;
+  const long long max_range = ((groups + n_split - 1) / n_split) * gw;  // weights
+  pl.act_stride = (int)(((max_range + 255) / 256) * 256);
+  pl.act_blk = pl.act_stride / 32;
+  const int stage_bytes = TILE_ROWS * chunk_bytes_of(fmt);
+  const size_t bar_bytes = 2 * MAX_STAGES * sizeof(uint64_t);
+  const size_t budget = (size_t)device_smem_optin();
+  int nt = 16;
+  while (nt > n_tok && nt > 1) nt >>= 1;
+  if (nt < n_tok && nt < 16) nt <<= 1;  // smallest power of two >= n_tok (<= 16)
+  for (;; nt >>= 1) {
+    size_t fixed = act_bytes(nt, pl.act_stride, pl.act_blk) + bar_bytes + 128;
+    if (fixed + 2 * (size_t)stage_bytes <= budget) {
+      int st = (int)((budget - fixed) / stage_bytes);
+      pl.stages = st > MAX_STAGES ? MAX_STAGES : st;
+      pl.smem = (size_t)pl.stages * stage_bytes + fixed;
+      break;
+    }
+    if (nt == 1) return false;
+  }
+  pl.nt_tmpl = nt;
+  pl.passes_tok = (n_tok + nt - 1) / nt;
+  const long long units = (M + UNIT_ROWS - 1) / UNIT_ROWS;
+  const long long work = units * n_split;
+  const int sms = device_sm_count();
+  pl.grid = (int)(work < sms ? work : sms);
+  return true;
+}
+
+static cudaError_t launch_dense_any(int fmt, const DenseLaunch& L) {
+  switch (fmt) {
+    case QMV_Q8_0: return launch_dense_q8_0(L);
+    case QMV_Q4_K: return launch_dense_q4_k(L);
+    default: return launch_dense_iq4_xs(L);
+  }
+}
+
+// Runs pass 1 (all token passes) writing `out` (y, or the split partials).
+static int run_dense(int fmt, const void* W, const float* x, const int8_t* xq, const float* xd, const int32_t* xs,
+                     float* out, long long M, long long K, int n_tok, int n_split, cudaStream_t stream) {
+  Plan pl;
+  if (!plan_dense(fmt, M, K, n_tok, n_split, pl)) return QMV_ERR_SHAPE;
+  const long long rb = qmv_row_bytes(fmt, K);
+  DenseLaunch L;
+  if (!encode_rows(&L.map_tile, W, M, rb, chunk_bytes_of(fmt), TILE_ROWS)) return QMV_ERR_CUDA;
+  if (!encode_rows(&L.map_unit, W, M, rb, chunk_bytes_of(fmt), UNIT_ROWS)) return QMV_ERR_CUDA;
+  DenseParams p;
+  p.x = x;
+  p.xq = xq;
+  p.xd = xd;
+  p.xs = xs;
+  p.out = out;
+  p.M = M;
+  p.K = (int)K;
+  p.ntot = n_tok;
+  p.n_split = n_split;
+  p.groups = (int)(K / group_weights(fmt));
+  p.units = (int)((M + UNIT_ROWS - 1) / UNIT_ROWS);
+  p.stages = pl.stages;
+  p.act_stride = pl.act_stride;
+  p.act_blk = pl.act_blk;
+  p.err = device_error_word();
+  L.p = &p;
+  L.nt_tmpl = pl.nt_tmpl;
+  L.grid = pl.grid;
+  L.smem = pl.smem;
+  L.stream = stream;
+  L.pdl = true;
+  for (int t0 = 0; t0 < n_tok; t0 += pl.nt_tmpl) {
+    p.t0 = t0;
+    p.nt = n_tok - t0 < pl.nt_tmpl ? n_tok - t0 : pl.nt_tmpl;
+    if (launch_dense_any(fmt, L) != cudaSuccess) return QMV_ERR_CUDA;
+  }
+  return QMV_OK;
+}
+
+static int check_dense_args(int fmt, const void* W, const void* x, const float* y, long long M, long long K,
+                            int n_tok) {
+  if (!fmt_ok(fmt)) return QMV_ERR_FORMAT;
+  if (M <= 0 || M > MAX_M || K <= 0 || K > MAX_K || K % group_weights(fmt)) return QMV_ERR_SHAPE;
+  if (n_tok < 1 || n_tok > QMV_MAX_TOKENS) return QMV_ERR_NTOK;
+  if (!W || !x || !y) return QMV_ERR_NULL;
+  if (!aligned16(W) || !aligned16(x) || !aligned16(y)) return QMV_ERR_ALIGN;
+  return QMV_OK;
+}
+
+}  // namespace qmv
+
+using namespace qmv;
+
+extern "C" {
+
+int64_t qmv_row_bytes(int fmt, int64_t K) {
+  if (!fmt_ok(fmt)) return QMV_ERR_FORMAT;
+  if (K <= 0 || K > MAX_K || K % group_weights(fmt)) return QMV_ERR_SHAPE;
+  return (K / group_weights(fmt)) * group_bytes(fmt);
+}
+
+int qmv_quantize_weights(int fmt, const float* w, int64_t M, int64_t K, void* W, cudaStream_t stream) {
+  if (!fmt_ok(fmt)) return QMV_ERR_FORMAT;
+  if (M <= 0 || M > MAX_M || K <= 0 || K > MAX_K || K % group_weights(fmt)) return QMV_ERR_SHAPE;
+  if (!w || !W) return QMV_ERR_NULL;
+  if (!aligned16(w) || !aligned16(W)) return QMV_ERR_ALIGN;
+  int rc = check_device();
+  if (rc) return rc;
+  return launch_quantize_weights(fmt, w, M, (int)K, W, stream) == cudaSuccess ? QMV_OK : QMV_ERR_CUDA;
+}
+
+int qmv_quantize_act(const float* x, int64_t K, int n_tok, int8_t* q, float* d, int32_t* sum,
+                     cudaStream_t stream) {
+  if (K <= 0 || K > MAX_K || K % 256) return QMV_ERR_SHAPE;
+  if (n_tok < 1 || n_tok > QMV_MAX_TOKENS) return QMV_ERR_NTOK;
+  if (!x || !q || !d || !sum) return QMV_ERR_NULL;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(d) || !aligned16(sum)) return QMV_ERR_ALIGN;
+  int rc = check_device();
+  if (rc) return rc;
+  return launch_act_quant(x, (int)K, n_tok, q, d, sum, stream, true) == cudaSuccess ? QMV_OK : QMV_ERR_CUDA;
+}
+
+int qmv_run(int fmt, const void* W, const float* x, float* y, int64_t M, int64_t K, int n_tok,
+            cudaStream_t stream) {
+  int rc = check_dense_args(fmt, W, x, y, M, K, n_tok);
+  if (rc) return rc;
+  if ((rc = check_device())) return rc;
+  return run_dense(fmt, W, x, nullptr, nullptr, nullptr, y, M, K, n_tok, 1, stream);
+}
+
+int qmv_run_q8(int fmt, const void* W, const int8_t* xq, const float* xd, const int32_t* xs, float* y, int64_t M,
+               int64_t K, int n_tok, cudaStream_t stream) {
+  int rc = check_dense_args(fmt, W, xq, y, M, K, n_tok);
+  if (rc) return rc;
+  if (!xd || !xs) return QMV_ERR_NULL;
+  if (!aligned16(xd) || !aligned16(xs)) return QMV_ERR_ALIGN;
+  if ((rc = check_device())) return rc;
+  return run_dense(fmt, W, nullptr, xq, xd, xs, y, M, K, n_tok, 1, stream);
+}
+
+int qmv_splitk_choose(int fmt, int64_t M, int64_t K, int n_tok) {
+  (void)n_tok;
+  if (!fmt_ok(fmt)) return QMV_ERR_FORMAT;
+  if (M <= 0 || K <= 0 || K % group_weights(fmt)) return QMV_ERR_SHAPE;
+  const long long units = (M + UNIT_ROWS - 1) / UNIT_ROWS;
+  const long long want = 4ll * device_sm_count();  // >= 4 row units per CTA
+  if (units >= want) return 1;
+  const long long chunks = (K + KCHUNK - 1) / KCHUNK;
+  long long target = (want + units - 1) / units;
+  if (target > 64) target = 64;
+  // smallest divisor of the chunk count that reaches the target, so that
+  // every split covers whole chunks
+  for (long long s = target; s <= 64 && s <= chunks; s++)
+    if (chunks % s == 0) return (int)s;
+  return (int)(target < chunks ? target : chunks);
+}
+
+size_t qmv_splitk_workspace_bytes(int64_t M, int n_tok, int n_split) {
+  if (M <= 0 || n_tok <= 0 || n_split <= 0) return 0;
+  return (size_t)n_split * n_tok * M * sizeof(float);
+}
+
+int qmv_splitk_run(int fmt, const void* W, const float* x, float* y, int64_t M, int64_t K, int n_tok, int n_split,
+                   void* ws, size_t ws_bytes, cudaStream_t stream) {
+  int rc = check_dense_args(fmt, W, x, y, M, K, n_tok);
+  if (rc) return rc;
+  if (n_split < 0 || n_split > 256 || n_split > K / group_weights(fmt)) return QMV_ERR_SHAPE;
+  if (n_split > 1) {
+    if (!ws) return QMV_ERR_NULL;
+    if (!aligned16(ws)) return QMV_ERR_ALIGN;
+    if (ws_bytes < qmv_splitk_workspace_bytes(M, n_tok, n_split)) return QMV_ERR_WORKSPACE;
+  }
+  if ((rc = check_device())) return rc;
+  if (n_split == 0) {
+    n_split = qmv_splitk_choose(fmt, M, K, n_tok);
+    if (n_split > 1) {
+      if (!ws) return QMV_ERR_NULL;
+      if (!aligned16(ws)) return QMV_ERR_ALIGN;
+      if (ws_bytes < qmv_splitk_workspace_bytes(M, n_tok, n_split)) return QMV_ERR_WORKSPACE;
+    }
+  }
+  if (n_split == 1) return run_dense(fmt, W, x, nullptr, nullptr, nullptr, y, M, K, n_tok, 1, stream);
+  float* partial = static_cast<float*>(ws);
+  rc = run_dense(fmt, W, x, nullptr, nullptr, nullptr, partial, M, K, n_tok, n_split, stream);
+  if (rc) return rc;
+  return launch_splitk_reduce(partial, y, M, n_tok, n_split, stream, true) == cudaSuccess ? QMV_OK : QMV_ERR_CUDA;
+}
+
+int qmv_get_device_error(cudaStream_t stream, int* err) {
+  if (!err) return QMV_ERR_NULL;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return QMV_ERR_CUDA;
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_qmv_error, sizeof(v)) != cudaSuccess) return QMV_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_qmv_error, &zero, sizeof(zero)) != cudaSuccess) return QMV_ERR_CUDA;
+  *err = (int)v;
+  return QMV_OK;
+}
+
+const char* qmv_strerror(int code) {
+  switch (code) {
+    case QMV_OK: return "success";
+    case QMV_ERR_FORMAT: return "unknown weight format";
+    case QMV_ERR_SHAPE: return "invalid shape (M, K, ffn, hidden or split count)";
+    case QMV_ERR_NTOK: return "n_tok outside [1, 64] or top_k outside [1, 8]";
+    case QMV_ERR_NULL: return "a required pointer is NULL";
+    case QMV_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case QMV_ERR_WORKSPACE: return "workspace too small";
+    case QMV_ERR_CUDA: return "CUDA runtime error";
+    case QMV_ERR_DEVICE: return "no usable sm_103 device";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,38 @@
+// Launcher of the dense matvec kernel for one format: picks the compiled
+// token count and raises the dynamic shared-memory limit once per device.
+#pragma once
+#include "launch.h"
+#include "qmv_dense.cuh"
+
+namespace qmv {
+
+template <int F, int NT>
+static cudaError_t launch_dense_nt(const DenseLaunch& L) {
+  auto kern = qmv_dense_kernel<F, NT>;
+  static unsigned long long configured = 0;  // bit per device ordinal
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !((configured >> dev) & 1ull)) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, device_smem_optin());
+    if (e != cudaSuccess) return e;
+    configured |= 1ull << dev;
+  }
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  make_config(cfg, attr, dim3(L.grid), dim3(THREADS), L.smem, L.stream, L.pdl);
+  return cudaLaunchKernelEx(&cfg, kern, L.map_tile, L.map_unit, *L.p);
+}
+
+template <int F>
+static cudaError_t launch_dense_fmt(const DenseLaunch& L) {
+  switch (L.nt_tmpl) {
+    case 1: return launch_dense_nt<F, 1>(L);
+    case 2: return launch_dense_nt<F, 2>(L);
+    case 4: return launch_dense_nt<F, 4>(L);
+    case 8: return launch_dense_nt<F, 8>(L);
+    case 16: return launch_dense_nt<F, 16>(L);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace qmv

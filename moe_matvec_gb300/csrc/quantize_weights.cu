@@ -1,0 +1,169 @@
+// Weight quantizers (a preparation step, not part of the decode hot path):
+// fp32 weights -> the library's Q8_0 / Q4_K / IQ4_XS groups.  Each scale is
+// chosen from its block's range and each code is the nearest grid point, in
+// fp64 with every operation written as an explicitly rounded IEEE intrinsic
+// (no contraction), so the bytes do not depend on the compiler.  One thread
+// builds one group in registers / local memory and writes it out.
+#include "common.cuh"
+#include "launch.h"
+
+namespace qmv {
+
+namespace {
+
+__device__ __forceinline__ uint16_t f16_bits(double v) { return __half_as_ushort(__double2half(v)); }
+__device__ __forceinline__ double f16_val(uint16_t b) { return (double)__half2float(__ushort_as_half(b)); }
+
+__device__ __forceinline__ void put_bits(uint8_t* s, int bit, int nbits, unsigned v) {
+  for (int i = 0; i < nbits; i++) {
+    const int b = bit + i;
+    if ((v >> i) & 1u)
+      s[b >> 3] |= (uint8_t)(1u << (b & 7));
+    else
+      s[b >> 3] &= (uint8_t)~(1u << (b & 7));
+  }
+}
+__device__ __forceinline__ void put_nib(uint8_t* p, int i, unsigned c) {
+  if (i < 16)
+    p[i] = (uint8_t)((p[i] & 0xF0) | (c & 0xF));
+  else
+    p[i - 16] = (uint8_t)((p[i - 16] & 0x0F) | ((c & 0xF) << 4));
+}
+
+__device__ __forceinline__ double clampd(double v, double lo, double hi) { return v < lo ? lo : (v > hi ? hi : v); }
+
+__device__ void group_q8_0(const float* w, uint8_t* g) {
+  for (int b = 0; b < 8; b++) {
+    double amax = 0.0;
+    for (int i = 0; i < 32; i++) amax = fmax(amax, fabs((double)w[32 * b + i]));
+    const uint16_t d16 = f16_bits(__ddiv_rn(amax, 127.0));
+    const double dv = f16_val(d16);
+    g[2 * b] = (uint8_t)(d16 & 0xFF);
+    g[2 * b + 1] = (uint8_t)(d16 >> 8);
+    for (int i = 0; i < 32; i++) {
+      double r = 0.0;
+      if (dv > 0.0) r = clampd(rint(__ddiv_rn((double)w[32 * b + i], dv)), -127.0, 127.0);
+      const int off = i < 16 ? 16 * b + i : 128 + 16 * b + (i - 16);
+      g[16 + off] = (uint8_t)(int8_t)(int)r;
+    }
+  }
+}
+
+__device__ void group_q4_k(const float* w, uint8_t* g) {
+  double a[8], bm[8], amax = 0.0, bmax = 0.0;
+  for (int j = 0; j < 8; j++) {
+    double lo = 0.0, hi = -INFINITY;
+    for (int i = 0; i < 32; i++) {
+      const double v = (double)w[32 * j + i];
+      lo = fmin(lo, v);
+      hi = fmax(hi, v);
+    }
+    a[j] = __ddiv_rn(__dsub_rn(hi, lo), 15.0);
+    bm[j] = -lo;
+    amax = fmax(amax, a[j]);
+    bmax = fmax(bmax, bm[j]);
+  }
+  const uint16_t d16 = f16_bits(__ddiv_rn(amax, 63.0)), dm16 = f16_bits(__ddiv_rn(bmax, 63.0));
+  const double dv = f16_val(d16), dmv = f16_val(dm16);
+  g[0] = (uint8_t)(d16 & 0xFF);
+  g[1] = (uint8_t)(d16 >> 8);
+  g[2] = (uint8_t)(dm16 & 0xFF);
+  g[3] = (uint8_t)(dm16 >> 8);
+  for (int j = 0; j < 8; j++) {
+    const double sc = dv > 0.0 ? clampd(rint(__ddiv_rn(a[j], dv)), 0.0, 63.0) : 0.0;
+    const double m = dmv > 0.0 ? clampd(rint(__ddiv_rn(bm[j], dmv)), 0.0, 63.0) : 0.0;
+    put_bits(g + 4, 12 * j, 6, (unsigned)sc);
+    put_bits(g + 4, 12 * j + 6, 6, (unsigned)m);
+    const double S = __dmul_rn(dv, sc), O = __dmul_rn(dmv, m);
+    for (int i = 0; i < 32; i++) {
+      const double v = (double)w[32 * j + i];
+      int best = 0;
+      double berr = fabs(__dsub_rn(v, __dsub_rn(__dmul_rn(S, 0.0), O)));
+      for (int q = 1; q < 16; q++) {
+        const double e = fabs(__dsub_rn(v, __dsub_rn(__dmul_rn(S, (double)q), O)));
+        if (e < berr) {
+          berr = e;
+          best = q;
+        }
+      }
+      put_nib(g + 16 + 16 * j, i, (unsigned)best);
+    }
+  }
+}
+
+__device__ void superblock_iq4_xs(const float* w, uint8_t* meta, uint8_t* payload) {
+  const double cb[16] = {-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113};
+  double s[8], smax = 0.0;
+  for (int j = 0; j < 8; j++) {
+    double amax = 0.0;
+    for (int i = 0; i < 32; i++) amax = fmax(amax, fabs((double)w[32 * j + i]));
+    s[j] = __ddiv_rn(amax, 113.0);
+    smax = fmax(smax, s[j]);
+  }
+  const uint16_t d16 = f16_bits(__ddiv_rn(smax, 31.0));
+  const double dv = f16_val(d16);
+  meta[0] = (uint8_t)(d16 & 0xFF);
+  meta[1] = (uint8_t)(d16 >> 8);
+  for (int j = 0; j < 8; j++) {
+    const double l = dv > 0.0 ? clampd(rint(__ddiv_rn(s[j], dv)), 0.0, 31.0) : 0.0;
+    const int ls = 32 + (int)l;
+    put_bits(meta + 2, 6 * j, 6, (unsigned)ls);
+    const double e = __dmul_rn(dv, (double)(ls - 32));
+    for (int i = 0; i < 32; i++) {
+      const double v = (double)w[32 * j + i];
+      int best = 0;
+      double berr = fabs(__dsub_rn(v, __dmul_rn(e, cb[0])));
+      for (int c = 1; c < 16; c++) {
+        const double err = fabs(__dsub_rn(v, __dmul_rn(e, cb[c])));
+        if (err < berr) {
+          berr = err;
+          best = c;
+        }
+      }
+      put_nib(payload + 16 * j, i, (unsigned)best);
+    }
+  }
+}
+
+template <int F>
+__global__ void __launch_bounds__(128) quantize_kernel(const float* __restrict__ w, long long n_groups, int K,
+                                                       uint8_t* __restrict__ W) {
+  constexpr int GW = Fmt<F>::GW, GB = Fmt<F>::GB;
+  const long long gpr = K / GW;
+  for (long long gi = (long long)blockIdx.x * blockDim.x + threadIdx.x; gi < n_groups;
+       gi += (long long)gridDim.x * blockDim.x) {
+    const long long row = gi / gpr, col = gi - row * gpr;
+    const float* src = w + row * K + col * GW;
+    __align__(16) uint8_t g[GB];
+    for (int i = 0; i < GB; i++) g[i] = 0;
+    if constexpr (F == QMV_Q8_0)
+      group_q8_0(src, g);
+    else if constexpr (F == QMV_Q4_K)
+      group_q4_k(src, g);
+    else {
+      superblock_iq4_xs(src, g, g + 16);
+      superblock_iq4_xs(src + 256, g + 8, g + 16 + 128);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(W + gi * GB);
+    const uint4* s4 = reinterpret_cast<const uint4*>(g);
+    for (int i = 0; i < GB / 16; i++) dst[i] = s4[i];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_weights(int fmt, const float* w, long long M, int K, void* W, cudaStream_t stream) {
+  long long groups = M * (K / (fmt == QMV_IQ4_XS ? 512 : 256));
+  long long ctas = (groups + 127) / 128;
+  const long long cap = 32ll * device_sm_count();
+  if (ctas > cap) ctas = cap;
+  uint8_t* out = static_cast<uint8_t*>(W);
+  switch (fmt) {
+    case QMV_Q8_0: quantize_kernel<QMV_Q8_0><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
+    case QMV_Q4_K: quantize_kernel<QMV_Q4_K><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
+    default: quantize_kernel<QMV_IQ4_XS><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace qmv

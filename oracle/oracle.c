@@ -144,6 +144,10 @@ static void put_nib(uint8_t* p, int i, unsigned c) {
     p[i - 16] = (uint8_t)((p[i - 16] & 0x0F) | ((c & 0xF) << 4));
 }
 
+/* Payload byte of weight i (0..31) of Q8_0 block b (0..7) within a group:
+ * the first 16 weights of the 8 blocks come first, then the last 16. */
+static int q8_0_offset(int b, int i) { return i < 16 ? 16 * b + i : 128 + 16 * b + (i - 16); }
+
 /* ------------------------------------------------------------------------ */
 /* activation quantizer (fp32 rule)                                          */
 /* ------------------------------------------------------------------------ */
@@ -199,7 +203,7 @@ static void quant_q8_0_group(const float* w, uint8_t* g) {
         if (r > 127.0) r = 127.0;
         if (r < -127.0) r = -127.0;
       }
-      g[16 + 32 * b + i] = (uint8_t)(int8_t)r;
+      g[16 + q8_0_offset(b, i)] = (uint8_t)(int8_t)r;
     }
   }
 }
@@ -337,7 +341,7 @@ static void dequant_row(int fmt, const uint8_t* row, int64_t K, double* out) {
     if (fmt == OR_Q8_0) {
       for (int b = 0; b < 8; b++) {
         double d = oracle_f16_to_f64(rd16(g + 2 * b));
-        for (int i = 0; i < 32; i++) o[32 * b + i] = d * (double)(int8_t)g[16 + 32 * b + i];
+        for (int i = 0; i < 32; i++) o[32 * b + i] = d * (double)(int8_t)g[16 + q8_0_offset(b, i)];
       }
     } else if (fmt == OR_Q4_K) {
       double d = oracle_f16_to_f64(rd16(g)), dmin = oracle_f16_to_f64(rd16(g + 2));

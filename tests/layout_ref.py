@@ -53,7 +53,8 @@ def pack_q8_0(d_bits, q) -> bytes:
         g[2 * j] = d_bits[j] & 0xFF
         g[2 * j + 1] = d_bits[j] >> 8
         for i in range(32):
-            g[16 + 32 * j + i] = int(q[j][i]) & 0xFF
+            off = 16 * j + i if i < 16 else 128 + 16 * j + (i - 16)
+            g[16 + off] = int(q[j][i]) & 0xFF
     return bytes(g)
 
 
@@ -85,7 +86,8 @@ def pack_iq4_xs(d_bits, ls, c) -> bytes:
 def unpack_q8_0(g):
     g = [int(v) for v in bytes(bytearray(g))]
     d_bits = [g[2 * j] | (g[2 * j + 1] << 8) for j in range(8)]
-    q = [[int(np.int8(np.uint8(g[16 + 32 * j + i]))) for i in range(32)] for j in range(8)]
+    off = lambda j, i: 16 * j + i if i < 16 else 128 + 16 * j + (i - 16)
+    q = [[int(np.int8(np.uint8(g[16 + off(j, i)]))) for i in range(32)] for j in range(8)]
     return d_bits, q
 
 

@@ -1,0 +1,51 @@
+"""Host-side argument checking of the C ABI.  Every call here is invalid, so
+the library returns its error code before touching any device (these run
+with or without a GPU, and never launch)."""
+import ctypes
+
+import pytest
+
+from moe_matvec_gb300 import api
+
+A = 0x10000          # an aligned, never dereferenced address
+MIS = 0x10004        # misaligned
+
+
+@pytest.fixture(scope="module")
+def L():
+    return api.load()
+
+
+def test_qmv_run_rejects_bad_arguments(L):
+    assert L.qmv_run(7, A, A, A, 16, 256, 1, None) == -1
+    assert L.qmv_run(0, A, A, A, 0, 256, 1, None) == -2
+    assert L.qmv_run(0, A, A, A, 16, 100, 1, None) == -2
+    assert L.qmv_run(2, A, A, A, 16, 256, 1, None) == -2        # IQ4_XS needs K % 512
+    assert L.qmv_run(0, A, A, A, 16, 256, 0, None) == -3
+    assert L.qmv_run(0, A, A, A, 16, 256, 65, None) == -3
+    assert L.qmv_run(0, None, A, A, 16, 256, 1, None) == -4
+    assert L.qmv_run(0, A, MIS, A, 16, 256, 1, None) == -5
+    assert L.qmv_run_q8(1, A, A, None, A, A, 16, 256, 1, None) == -4
+
+
+def test_splitk_rejects_bad_workspace(L):
+    need = L.qmv_splitk_workspace_bytes(64, 2, 4)
+    assert need == 4 * 2 * 64 * 4
+    assert L.qmv_splitk_run(0, A, A, A, 64, 4096, 2, 4, A, need - 1, None) == -6
+    assert L.qmv_splitk_run(0, A, A, A, 64, 4096, 2, 4, None, need, None) == -4
+    assert L.qmv_splitk_run(0, A, A, A, 64, 4096, 2, 4, MIS, need, None) == -5
+    assert L.qmv_splitk_run(0, A, A, A, 64, 4096, 2, 17, A, 1 << 30, None) == -2   # more splits than groups
+    assert L.qmv_splitk_run(0, A, A, A, 64, 4096, 2, -1, A, need, None) == -2
+
+
+def test_quantize_entry_points_reject_bad_arguments(L):
+    assert L.qmv_quantize_act(A, 100, 1, A, A, A, None) == -2
+    assert L.qmv_quantize_act(A, 256, 0, A, A, A, None) == -3
+    assert L.qmv_quantize_act(A, 256, 1, A, None, A, None) == -4
+    assert L.qmv_quantize_weights(3, A, 4, 256, A, None) == -1
+    assert L.qmv_quantize_weights(1, A, 4, 128, A, None) == -2
+    assert L.qmv_quantize_weights(1, A, 4, 256, MIS, None) == -5
+
+
+def test_device_error_needs_an_output_pointer(L):
+    assert L.qmv_get_device_error(None, None) == -4

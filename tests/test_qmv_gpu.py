@@ -1,0 +1,207 @@
+"""GPU parity of the dense quantized matvec, the activation quantizer, the
+weight quantizer and split-K, against the CPU oracle on the same seeded
+inputs.  Integer work is compared bit for bit; fp32 results within
+1e-5 * sum_k |What x Xhat| per output."""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_matvec_gb300 import synth
+from tests import layout_ref as L
+from tests.gpu_util import TOL, assert_within, dev, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+GW = {0: 256, 1: 256, 2: 512}
+
+
+# --------------------------------------------------------------------------
+# activation quantizer: bit-exact
+# --------------------------------------------------------------------------
+
+def _tricky_activations(n, K, seed):
+    x = synth.activations(seed, n, K)
+    x[0, :32] = 0.0                                     # zero block
+    x[0, 32:64] = np.arange(-16, 16, dtype=np.float32) * 8.0   # exact halves after scaling
+    x[0, 64] = 127 * 3.0
+    x[min(1, n - 1), 96:128] *= 1e-30                    # tiny but normal
+    x[n - 1, -32:] = np.float32(1e30)                    # huge, all equal
+    return x
+
+
+@pytest.mark.parametrize("n,K", [(1, 256), (3, 4096), (16, 5120), (64, 2048)])
+def test_act_quant_bit_exact(lib, n, K):
+    x = _tricky_activations(n, K, seed=n + K)
+    q, d, s = lib.quantize_act(dev(x))
+    rq, rd, rs = oracle.act_quant(x)
+    assert np.array_equal(q.cpu().numpy(), rq)
+    assert np.array_equal(d.cpu().numpy().view(np.uint32), rd.view(np.uint32))
+    assert np.array_equal(s.cpu().numpy(), rs)
+
+
+# --------------------------------------------------------------------------
+# weight quantizer: bit-exact bytes
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+def test_quantize_weights_bit_exact(lib, fmt):
+    K = 2048
+    w = synth.weights(70 + fmt, 300, K)
+    w[3] = 0.0
+    w[4] *= 1e-4                                          # subnormal fp16 scales
+    w[5, :256] = np.abs(w[5, :256])                       # one-signed blocks
+    w[6, :256] = -np.abs(w[6, :256])
+    w[7] *= 100.0
+    W = lib.quantize_weights(fmt, dev(w))
+    ref = oracle.quantize(fmt, w)
+    got = W.cpu().numpy()
+    assert got.shape == ref.shape
+    assert np.array_equal(got, ref)
+
+
+# --------------------------------------------------------------------------
+# dense matvec on small shapes (several tiles and ragged tails)
+# --------------------------------------------------------------------------
+
+SMALL = []
+for fmt in (0, 1, 2):
+    for M, K, ns in [(1, 512, (1, 3)), (37, 1536, (1, 2, 5)), (333, 3072, (1, 4, 8, 16)),
+                     (1000, 1024, (7, 17, 33, 64)), (64, 7168, (2, 13))]:
+        if K % GW[fmt]:
+            continue
+        for n in ns:
+            SMALL.append((fmt, M, K, n))
+
+
+@pytest.mark.parametrize("fmt,M,K,n", SMALL)
+def test_qmv_small(lib, fmt, M, K, n):
+    seed = 1000 * fmt + M + K + n
+    w = synth.weights(seed, M, K)
+    x = synth.activations(seed, n, K)
+    Wn = oracle.quantize(fmt, w)
+    y = lib.run(fmt, dev(Wn), dev(x), M, K).cpu().numpy()
+    yr, sabs = oracle.qmv(fmt, Wn, x, K)
+    assert_within(y, yr, sabs, what=f"fmt{fmt} M{M} K{K} n{n}")
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+def test_qmv_prequantized_input_matches_fused(lib, fmt):
+    M, K, n = 200, 2048, 5
+    w = synth.weights(5 + fmt, M, K)
+    x = synth.activations(6, n, K)
+    Wd = dev(oracle.quantize(fmt, w))
+    xd = dev(x)
+    y1 = lib.run(fmt, Wd, xd, M, K)
+    q, d, s = lib.quantize_act(xd)
+    y2 = lib.run_q8(fmt, Wd, q, d, s, M, K)
+    assert torch.equal(y1, y2)
+    assert torch.equal(y1, lib.run(fmt, Wd, xd, M, K))     # bitwise reproducible
+
+
+def _exact_case(fmt, r):
+    """Weights and activations whose products and sums are exact in fp32:
+    power-of-two scales, small integer codes, K = 512."""
+    K, M, n = 512, 40, 3
+    groups = []
+    for m in range(M):
+        row = b""
+        for gi in range(K // GW[fmt]):
+            if fmt == 0:
+                row += L.pack_q8_0([L.f16_bits(2.0 ** -3)] * 8, r.integers(-127, 128, (8, 32)).tolist())
+            elif fmt == 1:
+                row += L.pack_q4_k(L.f16_bits(2.0 ** -4), L.f16_bits(2.0 ** -5), r.integers(0, 4, 8).tolist(),
+                                   r.integers(0, 4, 8).tolist(), r.integers(0, 16, (8, 32)).tolist())
+            else:
+                row += L.pack_iq4_xs([L.f16_bits(2.0 ** -6)] * 2, r.integers(31, 34, (2, 8)).tolist(),
+                                     r.integers(0, 16, (2, 8, 32)).tolist())
+        groups.append(np.frombuffer(row, np.uint8))
+    W = np.stack(groups)
+    kx = r.integers(-127, 128, (n, K))
+    kx[:, ::32] = 127
+    x = (kx * 2.0 ** -2).astype(np.float32)
+    return W, x, K, M
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+def test_qmv_exact_integer_sums(lib, fmt):
+    # every partial sum is an integer multiple of 2^-8 below 2^24 * 2^-8, so an
+    # exact int32 block sum gives a bit-exact fp32 result in any order
+    W, x, K, M = _exact_case(fmt, np.random.default_rng(fmt))
+    yr, sabs = oracle.qmv(fmt, W, x, K)
+    unit = {0: 2.0 ** -5, 1: 2.0 ** -7, 2: 2.0 ** -8}[fmt]   # d_w * d_x (and dmin * d_x)
+    assert np.all(sabs < 2.0 ** 22 * unit)
+    y = lib.run(fmt, dev(W), dev(x), M, K).cpu().numpy()
+    assert np.array_equal(y.astype(np.float64), yr)
+
+
+# --------------------------------------------------------------------------
+# full-size workloads, sampled rows, in the benchmark's launch configuration
+# --------------------------------------------------------------------------
+
+@functools.lru_cache(maxsize=2)
+def _full_weights(fmt, M, K, seed):
+    w = synth.weights(seed, M, K)
+    return oracle.quantize(fmt, w)
+
+
+FULL = []
+for c in synth.DENSE_CASES:
+    if c.workload == "splitk_q8_0":
+        continue
+    for i, n in enumerate(c.n_toks):
+        FULL.append((c.workload, c.fmt, c.M, c.K, n, synth.seed_for(c.index, c.shape_index, i),
+                     synth.seed_for(c.index, c.shape_index, 0)))
+
+
+@pytest.mark.parametrize("name,fmt,M,K,n,seed,wseed", FULL)
+def test_qmv_full_size_sampled(lib, name, fmt, M, K, n, seed, wseed):
+    Wn = _full_weights(fmt, M, K, wseed)
+    x = synth.activations(seed, n, K)
+    y = lib.run(fmt, dev(Wn), dev(x), M, K).cpu().numpy()
+    rows = sample_rows(M)
+    yr, sabs = oracle.qmv(fmt, Wn[rows], x, K)
+    assert_within(y[:, rows], yr, sabs, what=f"{name} n{n}")
+    assert np.all(np.isfinite(y))
+
+
+# --------------------------------------------------------------------------
+# split-K
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt,M,K,n,S", [(0, 64, 8192, 3, 4), (0, 100, 16384, 16, 0), (1, 40, 6144, 2, 3),
+                                         (2, 72, 8192, 5, 8), (0, 17, 4096, 1, 16)])
+def test_splitk_small(lib, fmt, M, K, n, S):
+    seed = 77 + fmt + M
+    w = synth.weights(seed, M, K)
+    x = synth.activations(seed, n, K)
+    Wn = oracle.quantize(fmt, w)
+    Wd, xd = dev(Wn), dev(x)
+    y = lib.splitk_run(fmt, Wd, xd, M, K, n_split=S)
+    yr, sabs = oracle.qmv(fmt, Wn, x, K)
+    assert_within(y.cpu().numpy(), yr, sabs, what=f"splitk S{S}")
+    assert torch.equal(y, lib.splitk_run(fmt, Wd, xd, M, K, n_split=S))   # deterministic
+    y1 = lib.run(fmt, Wd, xd, M, K).cpu().numpy()
+    assert_within(y1, yr, sabs, what="unsplit")
+
+
+SPLITK_FULL = []
+for c in synth.DENSE_CASES:
+    if c.workload != "splitk_q8_0":
+        continue
+    for i, n in enumerate(c.n_toks):
+        SPLITK_FULL.append((c.M, c.K, n, synth.seed_for(c.index, c.shape_index, i),
+                            synth.seed_for(c.index, c.shape_index, 0)))
+
+
+@pytest.mark.parametrize("M,K,n,seed,wseed", SPLITK_FULL)
+def test_splitk_full_size_sampled(lib, M, K, n, seed, wseed):
+    Wn = _full_weights(0, M, K, wseed)
+    x = synth.activations(seed, n, K)
+    Wd, xd = dev(Wn), dev(x)
+    y = lib.splitk_run(0, Wd, xd, M, K, n_split=0).cpu().numpy()
+    rows = sample_rows(M)
+    yr, sabs = oracle.qmv(0, Wn[rows], x, K)
+    assert_within(y[:, rows], yr, sabs, what=f"splitk {M}x{K} n{n}")
