@@ -1,0 +1,413 @@
+"""Benchmark of the quantized small-batch matvec on GB300.
+
+Metric: effective weight bandwidth (algorithmic weight bytes / time, GB/s)
+and microseconds per call, for the small-batch Q4_K matvec M = 17408,
+K = 5120 at 1, 2, 4, 8 and 16 tokens; one step = one call at each of those
+token counts.  Effective bandwidth = weight bytes / kernel time is the pages'
+own measure ("Running GLM-5.3 on Two 8-GPU AMD W7900D Machines", paragraph
+under the constraint table of "A faster kernel can still leave the full
+chain slower").
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Inputs are synthetic and seeded (N(0, 0.02) weights quantized on the GPU by
+the library's quantizer, N(0, 1) activations).  Weights rotate over 12
+replicas (600 MB, > 4x the 129 MB L2), so every call streams from HBM.
+Timed region: CUDA-graph replays of whole steps, CUDA events on the
+launching stream.  `e2e` repeats the steps through the public API with the
+activations copied in from pinned host memory and the outputs copied back,
+every step.  `--impl reference` times the CPU oracle on a bounded sample of
+the same workload on the host cores.  Under torchrun (N > 1) every rank runs
+the same single-GPU workload (replicas: nothing in the path is sharded), the
+time is the maximum over ranks and the value sums the ranks' bytes.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "µs/call and effective weight GB/s (fraction of GB300 HBM peak), 1–64 tokens"
+WORKLOAD = "q4_k_matvec_17408x5120"
+FMT, M, K = 1, 17408, 5120
+NTOKS = (1, 2, 4, 8, 16)
+REPLICAS = 12
+BYTES_PER_CALL = M * (K // 256) * 144
+KERNEL_SOURCES = ("moe_matvec_gb300/csrc/qmv_dense.cuh", "moe_matvec_gb300/csrc/common.cuh",
+                  "moe_matvec_gb300/csrc/qmv_dense_inst.cuh")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "qmv_dense_q4_k_traffic.json")
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def recorded_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current kernel sources."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except OSError:
+        return None
+    if rec.get("kernel_hash") != kernel_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def __enter__(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.tmp is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.tmp.flush()
+        with open(self.tmp.name) as f:
+            rows = [r.strip().split(", ") for r in f if r.strip()]
+        os.unlink(self.tmp.name)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                for nm, v in zip(names, r[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(nm)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# --------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(times_ms, bytes_per_rank):
+    """Whole-job throughput: all ranks' bytes over the slowest rank's time."""
+    t = max(times_ms)
+    return sum(bytes_per_rank) / (t * 1e-3) / 1e9, t
+
+
+def gather_floats(value: float, world: int):
+    if world == 1:
+        return [value]
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    out = [torch.zeros_like(t) for _ in range(world)]
+    dist.all_gather(out, t)
+    return [float(o.item()) for o in out]
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------
+# CPU baseline (the oracle, as it stands)
+# --------------------------------------------------------------------------
+
+def oracle_sample(rows: int, seed: int = 4242):
+    import oracle
+    from moe_matvec_gb300 import synth
+    w = synth.weights(seed, rows, K)
+    Wn = oracle.quantize(FMT, w)
+    xs = {n: synth.activations(seed + n, n, K) for n in NTOKS}
+    return Wn, xs
+
+
+def time_oracle(Wn, xs, threads: int):
+    import oracle
+    t0 = time.perf_counter()
+    for n in NTOKS:
+        oracle.qmv(FMT, Wn, xs[n], K, nthreads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(budget_s: float = 12.0):
+    threads = os.cpu_count() or 1
+    Wn, xs = oracle_sample(64)
+    t = time_oracle(Wn, xs, threads)
+    rows = int(min(M, max(64, 64 * budget_s / max(t, 1e-6))))
+    Wn, xs = oracle_sample(rows)
+    t = time_oracle(Wn, xs, threads)
+    sample_bytes = rows * (K // 256) * 144 * len(NTOKS)
+    return {"value": sample_bytes / t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rows} of {M} rows, n_tok in {list(NTOKS)}, one pass each ({t:.1f} s)"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    threads = os.cpu_count() or 1
+    # per-step sample sized so that warmup + steps finish in about two minutes
+    Wn, xs = oracle_sample(16)
+    t16 = time_oracle(Wn, xs, threads)
+    per_step = 100.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(M, 16 * per_step / max(t16, 1e-6))))
+    Wn, xs = oracle_sample(rows)
+    for _ in range(args.warmup):
+        time_oracle(Wn, xs, threads)
+    t = 0.0
+    for _ in range(args.steps):
+        t += time_oracle(Wn, xs, threads)
+    step_bytes = rows * (K // 256) * 144 * len(NTOKS)
+    value = step_bytes * args.steps / t / 1e9
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8xint8->int32, f32",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "n_tok": list(NTOKS), "format": "Q4_K"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{rows} of {M} rows per step, n_tok in {list(NTOKS)}"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    from moe_matvec_gb300 import api, synth
+    api.load()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+
+    # weights: N(0, 0.02) drawn on the GPU, quantized by the library, replicated
+    g = torch.Generator(device=dev)
+    g.manual_seed(1001 + rank)
+    w = torch.randn((M, K), generator=g, device=dev, dtype=torch.float32) * 0.02
+    W0 = api.quantize_weights(FMT, w)
+    del w
+    Ws = [W0] + [W0.clone() for _ in range(REPLICAS - 1)]
+    xs = {n: torch.from_numpy(synth.activations(1010 + n, n, K)).to(dev) for n in NTOKS}
+    ys = {n: torch.empty((n, M), device=dev) for n in NTOKS}
+    torch.cuda.synchronize()
+
+    def step(r, s):
+        for n in NTOKS:
+            api.run(FMT, Ws[r % REPLICAS], xs[n], M, K, out=ys[n], stream=s)
+
+    # one graph = REPLICAS steps, each on its own replica
+    with torch.cuda.stream(stream):
+        for r in range(REPLICAS):          # eager warm-up (also builds everything)
+            step(r, stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for r in range(REPLICAS):
+            step(r, stream)
+    reps = max(1, (args.steps + REPLICAS - 1) // REPLICAS)
+    steps = reps * REPLICAS
+    warm_reps = max(1, (args.warmup + REPLICAS - 1) // REPLICAS)
+    with torch.cuda.stream(stream):
+        for _ in range(warm_reps):
+            graph.replay()
+    stream.synchronize()
+
+    # per-token-count graphs for the per-call breakdown
+    per_n = {}
+    for n in NTOKS:
+        gn = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gn, stream=stream):
+            for r in range(REPLICAS):
+                api.run(FMT, Ws[r], xs[n], M, K, out=ys[n], stream=stream)
+        with torch.cuda.stream(stream):
+            gn.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        nrep = 50
+        stream.synchronize()
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(nrep):
+                gn.replay()
+        e1.record(stream)
+        e1.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (nrep * REPLICAS)
+        per_n[str(n)] = {"us_per_call": round(us, 3), "gbs": round(BYTES_PER_CALL / (us * 1e-6) / 1e9, 1)}
+
+    # timed region
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        time.sleep(0.25)
+        e0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(reps):
+                graph.replay()
+        e1.record(stream)
+        e1.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    step_bytes = BYTES_PER_CALL * len(NTOKS)
+    value, tmax = aggregate(gather_floats(ms, world), [step_bytes * steps] * world)
+    launches = steps * len(NTOKS)
+
+    # e2e: public API with host buffers, eager launches, copies every step
+    xh = {n: xs[n].cpu().pin_memory() for n in NTOKS}
+    yh = {n: torch.empty((n, M)).pin_memory() for n in NTOKS}
+    e2e_steps = max(REPLICAS, min(steps, 2000))
+    barrier(world)
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    with torch.cuda.stream(stream):
+        for i in range(e2e_steps):
+            for n in NTOKS:
+                xs[n].copy_(xh[n], non_blocking=True)
+                api.run(FMT, Ws[i % REPLICAS], xs[n], M, K, out=ys[n], stream=stream)
+                yh[n].copy_(ys[n], non_blocking=True)
+    a1.record(stream)
+    a1.synchronize()
+    barrier(world)
+    e2e_ms = a0.elapsed_time(a1)
+    e2e_value, _ = aggregate(gather_floats(e2e_ms, world), [step_bytes * e2e_steps] * world)
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_kind = measured_peaks()
+    achieved = step_bytes * steps / (ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": recorded_traffic(),
+            "peak_kind": peak_kind, "kernel": "qmv_dense_kernel<Q4_K>",
+            "algorithmic_bytes_per_launch": BYTES_PER_CALL}
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": steps,
+            "warmup": warm_reps * REPLICAS, "ms_per_step": tmax / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int8xint8->int32, f32",
+            "data": "synthetic N(0,0.02) weights quantized on GPU, N(0,1) activations",
+            "config": {"workload": WORKLOAD, "format": "Q4_K", "M": M, "K": K, "n_tok": list(NTOKS),
+                       "l2": f"weights rotate over {REPLICAS} replicas ({REPLICAS * BYTES_PER_CALL / 1e6:.0f} MB "
+                             "> 4x L2), inputs larger than L2", "timing": "CUDA graph replay, CUDA events",
+                       "parallelism": f"replicas x{world}"},
+            "us_per_call": per_n, "roofline": roof,
+            "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
+                    "h2d_bytes_per_step": sum(n * K * 4 for n in NTOKS),
+                    "d2h_bytes_per_step": sum(n * M * 4 for n in NTOKS),
+                    "ms_per_step": e2e_ms / e2e_steps},
+            "gpu_launches": launches, "clocks": clk.summary()}
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_profile(args):
+    """A few eager calls of the timed workload (for ncu captures)."""
+    import torch
+    from moe_matvec_gb300 import api, synth
+    api.load()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1001)
+    w = torch.randn((M, K), generator=g, device="cuda", dtype=torch.float32) * 0.02
+    Ws = [api.quantize_weights(FMT, w) for _ in range(3)]
+    del w
+    for rnd in range(2):
+        for n in NTOKS:
+            x = torch.from_numpy(synth.activations(1010 + n, n, K)).cuda()
+            api.run(FMT, Ws[(rnd * len(NTOKS) + n) % 3], x, M, K)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_run": WORKLOAD, "calls": 2 * len(NTOKS)}))
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=12000)
+    ap.add_argument("--warmup", type=int, default=24)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true", help="a few eager calls only (for ncu)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.profile:
+        return run_profile(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

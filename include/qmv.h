@@ -202,16 +202,17 @@ typedef struct moe_experts {
  * [0, n_experts) or repeats an earlier id of the same token contributes 0 and
  * sets the device error word.  gates are used as given (not renormalised).
  * The workspace holds the intermediates at the offsets of
- * moe_qmv_workspace_offsets (slot p = t * top_k + k):
- *   [0] xq int8 [n_tok][H]   [1] xd f32 [n_tok][H/32]  [2] xs i32 [n_tok][H/32]
- *   [3] h  f32 [n_tok*top_k][F]
- *   [4] hq int8 [n_tok*top_k][F]  [5] hd f32 [..][F/32]  [6] hs i32 [..][F/32]
- *   [7] o  f32 [n_tok*top_k][H]
+ * moe_qmv_workspace_offsets (slot p = t * top_k + k; rows of slots that do
+ * not route are left unwritten):
+ *   [0] h  f32 [n_tok*top_k][F]     (SwiGLU output)
+ *   [1] hq int8 [n_tok*top_k][F]    (h quantized by the activation rule)
+ *   [2] hd f32 [n_tok*top_k][F/32]  [3] hs i32 [n_tok*top_k][F/32]
+ *   [4] o  f32 [n_tok*top_k][H]     (down projection of each slot)
  * Constraints: H and F multiples of the group sizes of the two formats,
- * 1 <= n_tok <= 64, 1 <= top_k <= 8, top_k <= n_experts. */
+ * n_experts <= 512, 1 <= n_tok <= 64, 1 <= top_k <= 8, top_k <= n_experts. */
 size_t moe_qmv_workspace_bytes(const moe_experts* e, int n_tok, int top_k);
 int moe_qmv_workspace_offsets(const moe_experts* e, int n_tok, int top_k,
-                              size_t offsets[8]);
+                              size_t offsets[5]);
 int moe_qmv_run(const moe_experts* e, const int32_t* ids, const float* gates,
                 const float* x, float* y, int n_tok, int top_k, void* ws,
                 size_t ws_bytes, cudaStream_t stream);

@@ -50,7 +50,7 @@ _SIGS = {
     "qmv_splitk_workspace_bytes": (_sz, [_i64, _int, _int]),
     "qmv_splitk_run": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _int, _int, _vp, _sz, _vp]),
     "moe_qmv_workspace_bytes": (_sz, [ctypes.POINTER(MoeExperts), _int, _int]),
-    "moe_qmv_workspace_offsets": (_int, [ctypes.POINTER(MoeExperts), _int, _int, ctypes.POINTER(_sz * 8)]),
+    "moe_qmv_workspace_offsets": (_int, [ctypes.POINTER(MoeExperts), _int, _int, ctypes.POINTER(_sz * 5)]),
     "moe_qmv_run": (_int, [ctypes.POINTER(MoeExperts), _vp, _vp, _vp, _vp, _int, _int, _vp, _sz, _vp]),
     "qmv_get_device_error": (_int, [_vp, ctypes.POINTER(_int)]),
     "qmv_strerror": (ctypes.c_char_p, [_int]),
@@ -186,7 +186,7 @@ def moe_workspace_bytes(e: MoeExperts, n_tok: int, top_k: int) -> int:
 
 
 def moe_workspace_offsets(e: MoeExperts, n_tok: int, top_k: int):
-    arr = (_sz * 8)()
+    arr = (_sz * 5)()
     _check(load().moe_qmv_workspace_offsets(ctypes.byref(e), n_tok, top_k, ctypes.byref(arr)),
            "moe_qmv_workspace_offsets")
     return list(arr)

@@ -24,6 +24,28 @@ cudaError_t launch_dense_q8_0(const DenseLaunch& L);
 cudaError_t launch_dense_q4_k(const DenseLaunch& L);
 cudaError_t launch_dense_iq4_xs(const DenseLaunch& L);
 
+struct MoeParams;
+
+struct MoeLaunch {
+  const MoeParams* p;
+  CUtensorMap map_tile;
+  CUtensorMap map_unit;
+  int nt_tmpl;
+  int grid;
+  size_t smem;
+  cudaStream_t stream;
+  bool pdl;
+};
+
+cudaError_t launch_moe_gate_up_q8_0(const MoeLaunch& L);
+cudaError_t launch_moe_gate_up_q4_k(const MoeLaunch& L);
+cudaError_t launch_moe_gate_up_iq4_xs(const MoeLaunch& L);
+cudaError_t launch_moe_down_q8_0(const MoeLaunch& L);
+cudaError_t launch_moe_down_q4_k(const MoeLaunch& L);
+cudaError_t launch_moe_down_iq4_xs(const MoeLaunch& L);
+cudaError_t launch_moe_combine(const int32_t* ids, const float* gates, const float* o, float* y, int n_tok,
+                               int top_k, int n_experts, int hidden, cudaStream_t stream, bool pdl);
+
 cudaError_t launch_act_quant(const float* x, int K, int n_tok, int8_t* q, float* d, int32_t* s,
                              cudaStream_t stream, bool pdl);
 cudaError_t launch_splitk_reduce(const float* partial, float* y, long long M, int n_tok, int n_split,

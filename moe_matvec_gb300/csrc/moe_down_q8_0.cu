@@ -1,0 +1,6 @@
+// Expert-grouped MoE down kernels for the QMV_Q8_0 weight format.
+#include "moe_inst.cuh"
+
+namespace qmv {
+cudaError_t launch_moe_down_q8_0(const MoeLaunch& L) { return launch_moe_fmt<QMV_Q8_0, MOE_DOWN>(L); }
+}  // namespace qmv

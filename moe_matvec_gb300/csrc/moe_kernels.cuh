@@ -1,0 +1,309 @@
+// Expert-grouped MoE decode kernels.
+//
+// One MoE FFN layer for a batch of up to 64 tokens, each routed to top_k
+// experts ("Castagna Veloce", section "Kernels for the MI50": i-quant MoE
+// decode kernels for batches of up to 64 tokens and the expert-grouped
+// quantized MoE scheme; section "Fused operations": gate/up + SwiGLU):
+//   kernel GATE_UP: for every routed expert, stream its gate and up rows once
+//     and, for all tokens routed to it, g = Wgate x, u = Wup x,
+//     h = silu(g) * u  (SwiGLU in the epilogue, fp32);
+//   kernel DOWN:   for every routed expert, quantize its tokens' h by the
+//     activation rule while staging (writing q8(h) back to the workspace) and
+//     stream its down rows once: o = Wdown h;
+//   kernel COMBINE: y[t] = sum_k gates[t][k] * o[t, k], added in k order.
+// Expert grouping: every CTA rebuilds the groups from ids in its prologue
+// (at most 512 slots): a 64-bit mask of the tokens routed to each expert
+// gives each slot its rank within the expert, so the slot lists come out in
+// token order without sorting, identically in every CTA.  Work is the
+// flattened (expert group, 8-row unit) space, split evenly over persistent
+// CTAs; a tile stays inside one expert group, whose activations are staged
+// once per CTA.
+#pragma once
+#include "qmv_core.cuh"
+
+namespace qmv {
+
+constexpr int MOE_MAX_EXPERTS = 512;
+constexpr int MOE_MAX_SLOTS = QMV_MAX_TOKENS * QMV_MAX_TOPK;  // 512
+constexpr int MOE_GATE_UP = 0, MOE_DOWN = 1;
+
+struct MoeParams {
+  const int32_t* ids;   // [n_tok][top_k]
+  const float* src;     // GATE_UP: x [n_tok][K]; DOWN: h [S][K]
+  float* dst;           // GATE_UP: h [S][R];     DOWN: o [S][R]
+  int8_t* hq;           // DOWN: write-back of the quantized h [S][K]
+  float* hd;            // [S][K/32]
+  int32_t* hs;          // [S][K/32]
+  int n_tok, top_k, n_experts;
+  int K;                // reduction length (hidden for GATE_UP, ffn for DOWN)
+  int R;                // outputs per expert (ffn for GATE_UP, hidden for DOWN)
+  int pool_rows;        // rows per expert in the weight pool (2*ffn or hidden)
+  int groups;           // K / group weights
+  int stages, act_stride, act_blk;
+  unsigned* err;
+};
+
+// Expert groups of one launch, in shared memory.
+struct MoeRouting {
+  unsigned long long mask[MOE_MAX_EXPERTS];  // tokens routed to each expert
+  int off[MOE_MAX_EXPERTS];                  // first slot-list index of each expert
+  int slots[MOE_MAX_SLOTS];                  // slots (t * top_k + k), grouped by expert, in token order
+  int pair_expert[MOE_MAX_SLOTS];            // per (expert, token group)
+  int pair_first[MOE_MAX_SLOTS];
+  int pair_count[MOE_MAX_SLOTS];
+  int n_pairs;
+};
+
+// A slot routes when its id lies in [0, E) and does not repeat an earlier id
+// of the same token.
+__device__ __forceinline__ int slot_status(const int32_t* ids, int top_k, int E, int p) {
+  const int t = p / top_k, k = p - t * top_k;
+  const int e = ids[p];
+  if (e < 0 || e >= E) return QMV_DEVERR_EXPERT_RANGE;
+  for (int kk = 0; kk < k; kk++)
+    if (ids[t * top_k + kk] == e) return QMV_DEVERR_EXPERT_DUP;
+  return 0;
+}
+
+// Build the expert groups (called by all threads of the CTA).
+__device__ __forceinline__ void build_routing(MoeRouting& rt, const MoeParams& p, int nt_group, bool report) {
+  const int S = p.n_tok * p.top_k;
+  const int E = p.n_experts;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) rt.mask[e] = 0ull;
+  __syncthreads();
+  for (int s = threadIdx.x; s < S; s += blockDim.x) {
+    const int st = slot_status(p.ids, p.top_k, E, s);
+    if (st == 0)
+      atomicOr(&rt.mask[p.ids[s]], 1ull << (s / p.top_k));
+    else if (report)
+      set_error(p.err, (unsigned)st);
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int carry_slots = 0, carry_pairs = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const int c = e < E ? __popcll(rt.mask[e]) : 0;
+      const int ng = (c + nt_group - 1) / nt_group;
+      int cs = c, cp = ng;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(FULL, cs, o), b = __shfl_up_sync(FULL, cp, o);
+        if (lane >= o) {
+          cs += a;
+          cp += b;
+        }
+      }
+      const int off = carry_slots + cs - c, poff = carry_pairs + cp - ng;
+      if (e < E) {
+        rt.off[e] = off;
+        for (int g = 0; g < ng; g++) {
+          rt.pair_expert[poff + g] = e;
+          rt.pair_first[poff + g] = off + g * nt_group;
+          rt.pair_count[poff + g] = min(nt_group, c - g * nt_group);
+        }
+      }
+      carry_slots += __shfl_sync(FULL, cs, 31);
+      carry_pairs += __shfl_sync(FULL, cp, 31);
+    }
+    if (lane == 0) rt.n_pairs = carry_pairs;
+  }
+  __syncthreads();
+  for (int s = threadIdx.x; s < S; s += blockDim.x) {
+    if (slot_status(p.ids, p.top_k, E, s) == 0) {
+      const int e = p.ids[s], t = s / p.top_k;
+      const int rank = __popcll(rt.mask[e] & ((1ull << t) - 1ull));
+      rt.slots[rt.off[e] + rank] = s;
+    }
+  }
+  __syncthreads();
+}
+
+// Walk over the flattened (pair, unit) space of this CTA.
+struct MoeWalk {
+  long long f, f_end;
+  int units, tile_units;
+  __device__ MoeWalk(int n_pairs, int units_per_pair, int tile_units_) {
+    const long long total = (long long)n_pairs * units_per_pair;
+    f = total * blockIdx.x / gridDim.x;
+    f_end = total * (blockIdx.x + 1) / gridDim.x;
+    units = units_per_pair;
+    tile_units = tile_units_;
+  }
+  __device__ bool next(int& q, int& u, int& nu) {
+    if (f >= f_end) return false;
+    q = (int)(f / units);
+    u = (int)(f - (long long)q * units);
+    const long long lim = f_end - f;
+    nu = (int)min((long long)min(tile_units, units - u), lim);
+    f += nu;
+    return true;
+  }
+};
+
+template <int F, int NT, int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+    moe_qmv_kernel(const __grid_constant__ CUtensorMap map_tile, const __grid_constant__ CUtensorMap map_unit,
+                   const MoeParams p) {
+  constexpr int CB = chunk_bytes<F>();
+  constexpr int STAGE_BYTES = TILE_ROWS * CB;
+  // GATE_UP: a tile is up to 2 units of 8 outputs j: gate rows j in stage rows
+  // 0..15, up rows j in stage rows 16..31; warp w takes output j0 + w.
+  // DOWN: a tile is up to 4 units of 8 rows; warp w takes rows 2w, 2w+1.
+  constexpr int TILE_UNITS = MODE == MOE_GATE_UP ? 2 : 4;
+  __shared__ MoeRouting rt;
+  __shared__ int s_rows[16];
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* stages = smem;
+  ActView a;
+  a.q = stages + p.stages * STAGE_BYTES;
+  a.d = reinterpret_cast<float*>(a.q + NT * p.act_stride);
+  a.ds = a.d + NT * p.act_blk;
+  a.stride = p.act_stride;
+  a.blk = p.act_blk;
+  uint64_t* full = reinterpret_cast<uint64_t*>(a.ds + NT * p.act_blk);
+  uint64_t* empty = full + MAX_STAGES;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  init_pipeline(full, empty, p.stages);
+  pdl_launch_dependents();
+  build_routing(rt, p, NT, MODE == MOE_GATE_UP && blockIdx.x == 0);
+  const int units_per_pair = p.R / UNIT_ROWS;
+  const int nck = (p.K + KCHUNK - 1) / KCHUNK;
+
+  if (warp == CONSUMER_WARPS) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      prefetch_tensormap(&map_tile);
+      prefetch_tensormap(&map_unit);
+      const uint64_t pol = policy_evict_first();
+      pdl_wait();
+      MoeWalk walk(rt.n_pairs, units_per_pair, TILE_UNITS);
+      int q, u, nu;
+      Ring ring;
+      bool alive = true;
+      while (alive && walk.next(q, u, nu)) {
+        const int base = rt.pair_expert[q] * p.pool_rows;
+        for (int c = 0; c < nck; c++, ring.advance(p.stages)) {
+          if (!producer_acquire(empty, ring, p.stages, p.err)) {
+            alive = false;
+            break;
+          }
+          const int st = ring.st;
+          uint8_t* dst = stages + st * STAGE_BYTES;
+          const int x = c * CB / 8;
+          if constexpr (MODE == MOE_GATE_UP) {
+            mbar_arrive_expect_tx(&full[st], 2 * nu * UNIT_ROWS * CB);
+            for (int i = 0; i < nu; i++) {
+              const int j = (u + i) * UNIT_ROWS;
+              tma_load_2d(dst + i * UNIT_ROWS * CB, &map_unit, &full[st], x, base + j, pol);
+              tma_load_2d(dst + (16 + i * UNIT_ROWS) * CB, &map_unit, &full[st], x, base + p.R + j, pol);
+            }
+          } else {
+            if (nu == TILE_UNITS) {
+              mbar_arrive_expect_tx(&full[st], STAGE_BYTES);
+              tma_load_2d(dst, &map_tile, &full[st], x, base + u * UNIT_ROWS, pol);
+            } else {
+              mbar_arrive_expect_tx(&full[st], nu * UNIT_ROWS * CB);
+              for (int i = 0; i < nu; i++)
+                tma_load_2d(dst + i * UNIT_ROWS * CB, &map_unit, &full[st], x, base + (u + i) * UNIT_ROWS, pol);
+            }
+          }
+        }
+      }
+      producer_drain(full, ring.n, p.stages, p.err);
+    }
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  pdl_wait();  // x (or h) may come from the preceding kernel
+  const int cw = warp;
+  bool alive = true;
+  MoeWalk walk(rt.n_pairs, units_per_pair, TILE_UNITS);
+  int q, u, nu;
+  Ring ring;
+  int staged_pair = -1;
+  float acc[RW][NT];
+#pragma unroll
+  for (int r = 0; r < RW; r++)
+#pragma unroll
+    for (int t = 0; t < NT; t++) acc[r][t] = 0.f;
+  int srow[RW];
+  if constexpr (MODE == MOE_GATE_UP) {
+    srow[0] = cw;
+    srow[1] = 16 + cw;
+  } else {
+#pragma unroll
+    for (int r = 0; r < RW; r++) srow[r] = cw * RW + r;
+  }
+  const int nblk = p.K / BLK;
+
+  while (walk.next(q, u, nu)) {
+    const int first = rt.pair_first[q];
+    a.nt = rt.pair_count[q];
+    if (q != staged_pair) {
+      named_sync(1, CONSUMER_THREADS);
+      if (threadIdx.x < a.nt) {
+        const int slot = rt.slots[first + threadIdx.x];
+        s_rows[threadIdx.x] = MODE == MOE_GATE_UP ? slot / p.top_k : slot;
+      }
+      named_sync(1, CONSUMER_THREADS);
+      ActSource src{p.src, nullptr, nullptr, nullptr, p.K, s_rows, 0, nullptr, nullptr, nullptr};
+      if (MODE == MOE_DOWN && u == 0) {  // the CTA that owns the group's first unit publishes q8(h)
+        src.wq = p.hq;
+        src.wd = p.hd;
+        src.ws = p.hs;
+      }
+      stage_activations<F>(src, 0, nblk, a, cw, lane);
+      named_sync(1, CONSUMER_THREADS);
+      staged_pair = q;
+    }
+    const int nvalid = nu * UNIT_ROWS;
+    unsigned rmask = 0;
+    if constexpr (MODE == MOE_GATE_UP) {
+      if (cw < nvalid) rmask = 3u;
+    } else {
+#pragma unroll
+      for (int r = 0; r < RW; r++)
+        if (srow[r] < nvalid) rmask |= 1u << r;
+    }
+    for (int c = 0; c < nck && alive; c++, ring.advance(p.stages)) {
+      const int st = ring.st;
+      if (!mbar_wait(&full[st], ring.parity(), p.err)) {
+        alive = false;
+        break;
+      }
+      const int kb = c * (KCHUNK / BLK) + lane;
+      if (rmask && kb < nblk) Consumer<F, NT>::chunk(stages + st * STAGE_BYTES, srow, rmask, lane, kb, a, acc);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+    alive = __all_sync(FULL, alive);
+    if (!alive) continue;
+    const int row0 = u * UNIT_ROWS;
+#pragma unroll
+    for (int t = 0; t < NT; t++) {
+      if constexpr (MODE == MOE_GATE_UP) {
+        const float g = warp_sum(acc[0][t]);
+        const float v = warp_sum(acc[1][t]);
+        if (lane == (t & 31) && t < a.nt && rmask) {
+          const float h = g / (1.0f + expf(-g)) * v;
+          p.dst[(long long)rt.slots[first + t] * p.R + row0 + cw] = h;
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < RW; r++) {
+          const float v = warp_sum(acc[r][t]);
+          if (lane == ((r * NT + t) & 31) && t < a.nt && ((rmask >> r) & 1u))
+            p.dst[(long long)rt.slots[first + t] * p.R + row0 + srow[r]] = v;
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < RW; r++) acc[r][t] = 0.f;
+    }
+  }
+}
+
+}  // namespace qmv

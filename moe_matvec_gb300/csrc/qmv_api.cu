@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "launch.h"
+#include "moe_kernels.cuh"
 #include "qmv_dense.cuh"
 
 namespace qmv {
@@ -210,6 +211,82 @@ static int check_dense_args(int fmt, const void* W, const void* x, const float* 
   return QMV_OK;
 }
 
+// ---------------------------------------------------------------------------
+// MoE planning.
+// ---------------------------------------------------------------------------
+constexpr int MOE_NOFF = 5;
+
+static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// Workspace: [0] h f32 [S][F], [1] hq i8 [S][F], [2] hd f32 [S][F/32],
+// [3] hs i32 [S][F/32], [4] o f32 [S][H]; S = n_tok * top_k.
+static size_t moe_layout(const moe_experts* e, int n_tok, int top_k, size_t off[MOE_NOFF]) {
+  const size_t S = (size_t)n_tok * top_k, F = (size_t)e->ffn, H = (size_t)e->hidden;
+  const size_t sizes[MOE_NOFF] = {S * F * 4, S * F, S * (F / 32) * 4, S * (F / 32) * 4, S * H * 4};
+  size_t cur = 0;
+  for (int i = 0; i < MOE_NOFF; i++) {
+    off[i] = cur;
+    cur = align256(cur + sizes[i]);
+  }
+  return cur;
+}
+
+static int check_moe_shape(const moe_experts* e, int n_tok, int top_k) {
+  if (!e) return QMV_ERR_NULL;
+  if (!fmt_ok(e->fmt_gate_up) || !fmt_ok(e->fmt_down)) return QMV_ERR_FORMAT;
+  if (e->n_experts < 1 || e->n_experts > MOE_MAX_EXPERTS || e->hidden <= 0 || e->ffn <= 0 ||
+      e->hidden > MAX_K || e->ffn > MAX_K || e->hidden % group_weights(e->fmt_gate_up) ||
+      e->ffn % group_weights(e->fmt_down) || e->hidden % UNIT_ROWS || e->ffn % UNIT_ROWS)
+    return QMV_ERR_SHAPE;
+  if ((long long)e->n_experts * 2 * e->ffn > MAX_M || (long long)e->n_experts * e->hidden > MAX_M)
+    return QMV_ERR_SHAPE;
+  if (n_tok < 1 || n_tok > QMV_MAX_TOKENS || top_k < 1 || top_k > QMV_MAX_TOPK || top_k > e->n_experts)
+    return QMV_ERR_NTOK;
+  return QMV_OK;
+}
+
+static cudaError_t launch_moe_any(int mode, int fmt, const MoeLaunch& L) {
+  if (mode == MOE_GATE_UP) {
+    switch (fmt) {
+      case QMV_Q8_0: return launch_moe_gate_up_q8_0(L);
+      case QMV_Q4_K: return launch_moe_gate_up_q4_k(L);
+      default: return launch_moe_gate_up_iq4_xs(L);
+    }
+  }
+  switch (fmt) {
+    case QMV_Q8_0: return launch_moe_down_q8_0(L);
+    case QMV_Q4_K: return launch_moe_down_q4_k(L);
+    default: return launch_moe_down_iq4_xs(L);
+  }
+}
+
+// One expert-grouped projection: weights `pool` (E experts x pool_rows rows
+// of K weights in format fmt).
+static int run_moe_proj(int mode, int fmt, const void* pool, MoeParams& p, int nt, cudaStream_t stream) {
+  const long long rb = qmv_row_bytes(fmt, p.K);
+  const long long rows = (long long)p.n_experts * p.pool_rows;
+  MoeLaunch L;
+  if (!encode_rows(&L.map_tile, pool, rows, rb, chunk_bytes_of(fmt), TILE_ROWS)) return QMV_ERR_CUDA;
+  if (!encode_rows(&L.map_unit, pool, rows, rb, chunk_bytes_of(fmt), UNIT_ROWS)) return QMV_ERR_CUDA;
+  p.act_stride = (int)(((long long)p.K + 255) / 256 * 256);
+  p.act_blk = p.act_stride / 32;
+  p.groups = p.K / group_weights(fmt);
+  const int stage_bytes = TILE_ROWS * chunk_bytes_of(fmt);
+  const size_t static_bytes = sizeof(MoeRouting) + 16 * sizeof(int) + 256;
+  const size_t budget = (size_t)device_smem_optin() - static_bytes;
+  const size_t fixed = act_bytes(nt, p.act_stride, p.act_blk) + 2 * MAX_STAGES * sizeof(uint64_t) + 128;
+  if (fixed + 2 * (size_t)stage_bytes > budget) return QMV_ERR_SHAPE;
+  int st = (int)((budget - fixed) / stage_bytes);
+  p.stages = st > MAX_STAGES ? MAX_STAGES : st;
+  L.p = &p;
+  L.nt_tmpl = nt;
+  L.grid = device_sm_count();
+  L.smem = (size_t)p.stages * stage_bytes + fixed;
+  L.stream = stream;
+  L.pdl = true;
+  return launch_moe_any(mode, fmt, L) == cudaSuccess ? QMV_OK : QMV_ERR_CUDA;
+}
+
 }  // namespace qmv
 
 using namespace qmv;
@@ -307,6 +384,67 @@ int qmv_splitk_run(int fmt, const void* W, const float* x, float* y, int64_t M, 
   rc = run_dense(fmt, W, x, nullptr, nullptr, nullptr, partial, M, K, n_tok, n_split, stream);
   if (rc) return rc;
   return launch_splitk_reduce(partial, y, M, n_tok, n_split, stream, true) == cudaSuccess ? QMV_OK : QMV_ERR_CUDA;
+}
+
+size_t moe_qmv_workspace_bytes(const moe_experts* e, int n_tok, int top_k) {
+  if (check_moe_shape(e, n_tok, top_k)) return 0;
+  size_t off[MOE_NOFF];
+  return moe_layout(e, n_tok, top_k, off);
+}
+
+int moe_qmv_workspace_offsets(const moe_experts* e, int n_tok, int top_k, size_t offsets[5]) {
+  int rc = check_moe_shape(e, n_tok, top_k);
+  if (rc) return rc;
+  if (!offsets) return QMV_ERR_NULL;
+  moe_layout(e, n_tok, top_k, offsets);
+  return QMV_OK;
+}
+
+int moe_qmv_run(const moe_experts* e, const int32_t* ids, const float* gates, const float* x, float* y, int n_tok,
+                int top_k, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  int rc = check_moe_shape(e, n_tok, top_k);
+  if (rc) return rc;
+  if (!ids || !gates || !x || !y || !ws || !e->w_gate_up || !e->w_down) return QMV_ERR_NULL;
+  if (!aligned16(ids) || !aligned16(gates) || !aligned16(x) || !aligned16(y) || !aligned16(ws) ||
+      !aligned16(e->w_gate_up) || !aligned16(e->w_down))
+    return QMV_ERR_ALIGN;
+  size_t off[MOE_NOFF];
+  if (ws_bytes < moe_layout(e, n_tok, top_k, off)) return QMV_ERR_WORKSPACE;
+  if ((rc = check_device())) return rc;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  float* h = reinterpret_cast<float*>(w + off[0]);
+  float* o = reinterpret_cast<float*>(w + off[4]);
+  int nt = 16;
+  while (nt > n_tok && nt > 1) nt >>= 1;
+  if (nt < n_tok && nt < 16) nt <<= 1;
+
+  MoeParams p{};
+  p.ids = ids;
+  p.n_tok = n_tok;
+  p.top_k = top_k;
+  p.n_experts = e->n_experts;
+  p.err = device_error_word();
+  // gate / up + SwiGLU: h [S][F]
+  p.src = x;
+  p.dst = h;
+  p.K = e->hidden;
+  p.R = e->ffn;
+  p.pool_rows = 2 * e->ffn;
+  if ((rc = run_moe_proj(MOE_GATE_UP, e->fmt_gate_up, e->w_gate_up, p, nt, stream))) return rc;
+  // down (h quantized while staging, published to the workspace): o [S][H]
+  MoeParams pd = p;
+  pd.src = h;
+  pd.dst = o;
+  pd.hq = reinterpret_cast<int8_t*>(w + off[1]);
+  pd.hd = reinterpret_cast<float*>(w + off[2]);
+  pd.hs = reinterpret_cast<int32_t*>(w + off[3]);
+  pd.K = e->ffn;
+  pd.R = e->hidden;
+  pd.pool_rows = e->hidden;
+  if ((rc = run_moe_proj(MOE_DOWN, e->fmt_down, e->w_down, pd, nt, stream))) return rc;
+  return launch_moe_combine(ids, gates, o, y, n_tok, top_k, e->n_experts, e->hidden, stream, true) == cudaSuccess
+             ? QMV_OK
+             : QMV_ERR_CUDA;
 }
 
 int qmv_get_device_error(cudaStream_t stream, int* err) {

@@ -1,0 +1,353 @@
+// Core of every quantized matvec kernel in the library: the activation
+// staging (per-32 int8 quantization into shared memory, in the byte order each
+// weight format consumes) and the consumer step that decodes one 1024-weight
+// chunk of up to RW weight rows in registers and accumulates exact int32
+// block dot products (dp4a) scaled in fp32.
+//
+// Shared by the dense matvec / split-K kernel and the expert-grouped MoE
+// kernels ("Castagna Veloce", section "Kernels for the MI50": small-batch
+// matvecs and MoE decode kernels; section "Fused operations": Q8 activations
+// reused across weight types).
+#pragma once
+#include "common.cuh"
+
+namespace qmv {
+
+constexpr int CONSUMER_WARPS = 16;
+constexpr int RW = 2;                                 // rows per consumer warp
+constexpr int TILE_ROWS = CONSUMER_WARPS * RW;        // 32
+constexpr int UNIT_ROWS = 8;                          // partition / tail-box granularity
+constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;    // + producer warp
+constexpr int CONSUMER_THREADS = CONSUMER_WARPS * 32;
+constexpr int MAX_STAGES = 8;
+constexpr unsigned FULL = 0xffffffffu;
+
+// Shared-memory position of byte p (0..31) of activation block b of a token
+// row: within every 256-weight group, the first 16 bytes of the 8 blocks come
+// first, then the last 16, so that the 8 lanes of a quarter-warp read 128
+// contiguous bytes.
+__device__ __forceinline__ int act_pos(int b, int p) {
+  return (b >> 3) * 256 + (p >> 4) * 128 + (b & 7) * 16 + (p & 15);
+}
+
+// The activation area of a CTA: nt token rows of codes, scales d and, for
+// Q4_K, d * s.
+struct ActView {
+  uint8_t* q;
+  float* d;
+  float* ds;
+  int nt;
+  int stride;  // bytes per token row of q (multiple of 256)
+  int blk;     // floats per token row of d / ds (stride / 32)
+};
+
+// Quantize four consecutive elements of a 32-block spread over 8 lanes
+// (lanes 8g..8g+7 hold block g of the warp); returns the packed int8 codes of
+// this lane, the block scale d and the block sum s (identical in the 8 lanes).
+struct Quad {
+  uint32_t q;
+  float d;
+  int s;
+};
+__device__ __forceinline__ Quad quant_quad(float4 v) {
+  float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+  m = fmaxf(m, __shfl_xor_sync(FULL, m, 1));
+  m = fmaxf(m, __shfl_xor_sync(FULL, m, 2));
+  m = fmaxf(m, __shfl_xor_sync(FULL, m, 4));
+  float d = __fdiv_rn(m, 127.0f);
+  float id = d > 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+  int q0 = max(-127, min(127, __float2int_rn(__fmul_rn(v.x, id))));
+  int q1 = max(-127, min(127, __float2int_rn(__fmul_rn(v.y, id))));
+  int q2 = max(-127, min(127, __float2int_rn(__fmul_rn(v.z, id))));
+  int q3 = max(-127, min(127, __float2int_rn(__fmul_rn(v.w, id))));
+  int s = q0 + q1 + q2 + q3;
+  s += __shfl_xor_sync(FULL, s, 1);
+  s += __shfl_xor_sync(FULL, s, 2);
+  s += __shfl_xor_sync(FULL, s, 4);
+  uint32_t packed = (uint32_t)(q0 & 0xFF) | ((uint32_t)(q1 & 0xFF) << 8) | ((uint32_t)(q2 & 0xFF) << 16) |
+                    ((uint32_t)(q3 & 0xFF) << 24);
+  return {packed, d, s};
+}
+
+// Store the packed codes of elements 4*li..4*li+3 of block b (li = lane & 7)
+// into the activation area in the byte order format F consumes.  For IQ4_XS
+// a block is stored interleaved (byte 2i = x_i, byte 2i+1 = x_{i+16}), the
+// order in which its codebook lookups come out; the other formats use the
+// natural order.  Must be called by all 32 lanes (it shuffles).
+template <int F>
+__device__ __forceinline__ void store_act_quad(uint8_t* row, int b, int li, uint32_t packed, bool ok) {
+  if constexpr (F == QMV_IQ4_XS) {
+    uint32_t hi = __shfl_xor_sync(FULL, packed, 4);  // elements 16 + 4*li ..
+    if (ok && li < 4) {
+      uint2 w;
+      w.x = __byte_perm(packed, hi, 0x5140);
+      w.y = __byte_perm(packed, hi, 0x7362);
+      *reinterpret_cast<uint2*>(row + act_pos(b, 8 * li)) = w;
+    }
+  } else {
+    if (ok) *reinterpret_cast<uint32_t*>(row + act_pos(b, 4 * li)) = packed;
+  }
+}
+
+// Where the activation rows of a stage come from: fp32 rows (quantized while
+// staging) or pre-quantized rows; token slot t reads source row rows[t] (a
+// shared-memory list) or row0 + t.  When wq is set, the quantized codes,
+// scales and sums are also written back to global memory (natural order),
+// which is how the MoE path exposes the quantized h.
+struct ActSource {
+  const float* x;
+  const int8_t* xq;
+  const float* xd;
+  const int32_t* xs;
+  long long ld;      // elements per source row (K of the rows)
+  const int* rows;   // nullptr: rows row0 .. row0 + nt - 1
+  long long row0;
+  int8_t* wq;
+  float* wd;
+  int32_t* ws;
+  __device__ __forceinline__ long long row(int t) const { return rows ? (long long)rows[t] : row0 + t; }
+};
+
+// Stage blocks [kb0, kb0 + nblk) of the a.nt token rows of `src` into the
+// activation area.  Called by all consumer warps (cw = warp index).
+template <int F>
+__device__ __forceinline__ void stage_activations(const ActSource& src, int kb0, int nblk, const ActView& a, int cw, int lane) {
+  const int sub = lane >> 3, li = lane & 7;
+  const int total = a.nt * nblk;
+  for (int base = cw * 4; base < total; base += CONSUMER_WARPS * 4) {
+    const int idx = base + sub;
+    const bool ok = idx < total;
+    const int t = ok ? idx / nblk : 0;
+    const int b = ok ? idx - t * nblk : 0;
+    const long long r = ok ? src.row(t) : 0;
+    const long long blk = r * (src.ld / 32) + kb0 + b;  // global block index
+    uint32_t packed;
+    float d;
+    int s;
+    if (src.x != nullptr) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ok) v = __ldg(reinterpret_cast<const float4*>(src.x + blk * 32) + li);
+      Quad qd = quant_quad(v);
+      packed = qd.q;
+      d = qd.d;
+      s = qd.s;
+      if (src.wq != nullptr && ok) {
+        reinterpret_cast<uint32_t*>(src.wq + blk * 32)[li] = packed;
+        if (li == 0) {
+          src.wd[blk] = d;
+          src.ws[blk] = s;
+        }
+      }
+    } else {
+      packed = 0;
+      d = 0.f;
+      s = 0;
+      if (ok) {
+        packed = __ldg(reinterpret_cast<const uint32_t*>(src.xq + blk * 32) + li);
+        d = __ldg(src.xd + blk);
+        s = __ldg(src.xs + blk);
+      }
+    }
+    store_act_quad<F>(a.q + t * a.stride, b, li, packed, ok);
+    if (ok && li == 0) {
+      a.d[t * a.blk + b] = d;
+      if constexpr (F == QMV_Q4_K) a.ds[t * a.blk + b] = d * (float)s;
+    }
+  }
+}
+
+// dp4a with unsigned bytes in a and signed bytes in b.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// Codebook lookup of four 4-bit codes held as the nibbles of the low 16 bits
+// of a word (nibble k -> byte k of the result).  pl (the word & 0x7777...)
+// picks from the lower and the upper half of the codebook with two byte
+// permutes; the fourth bit of each code becomes a byte mask through the
+// sign-replicating mode of a third permute (msb of the selected byte copied
+// to all 8 bits), fed with the word and the word << 4 so that the fourth bits
+// of the four codes sit at byte msbs.
+__device__ __forceinline__ uint32_t iq4_lookup4(uint32_t pl, uint32_t p, uint32_t p4, uint32_t mask_sel) {
+  constexpr uint32_t T0 = 0xBFAD9881u, T1 = 0xF6EADDCFu;  // codes 0..7
+  constexpr uint32_t T2 = 0x26190D01u, T3 = 0x71594535u;  // codes 8..15
+  uint32_t lo = prmt(T0, T1, pl);
+  uint32_t hi = prmt(T2, T3, pl);
+  uint32_t m = prmt(p4, p, mask_sel);
+  return (hi & m) | (lo & ~m);
+}
+
+template <int F, int NT>
+struct Consumer {
+  // Accumulate one chunk for the warp's RW rows (stage rows srow[r], active
+  // when bit r of rmask is set) and the lane's 32-weight block: l = lane
+  // within the chunk, kb = block index within the staged K-range.
+  static __device__ __forceinline__ void chunk(const uint8_t* stage, const int (&srow)[RW], unsigned rmask,
+                                               int lane, int kb, const ActView& a, float (&acc)[RW][NT]) {
+    constexpr int CB = chunk_bytes<F>();
+    uint32_t w[RW][8];   // decoded int8 operands, paired with act words 0..7
+    float sA[RW];        // per-row multiplier of d_x * isum
+    float sB[RW];        // Q4_K: dmin * m (multiplier of d_x * s)
+#pragma unroll
+    for (int r = 0; r < RW; r++) {
+      sA[r] = 0.f;
+      sB[r] = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; i++) w[r][i] = 0;
+      if ((rmask >> r) & 1u) {
+        const uint8_t* row = stage + srow[r] * CB;
+        if constexpr (F == QMV_Q8_0) {
+          const int g = lane >> 3, b8 = lane & 7;
+          const uint8_t* grp = row + g * 272;
+          uint4 x0 = *reinterpret_cast<const uint4*>(grp + 16 + 16 * b8);
+          uint4 x1 = *reinterpret_cast<const uint4*>(grp + 16 + 128 + 16 * b8);
+          w[r][0] = x0.x; w[r][1] = x0.y; w[r][2] = x0.z; w[r][3] = x0.w;
+          w[r][4] = x1.x; w[r][5] = x1.y; w[r][6] = x1.z; w[r][7] = x1.w;
+          sA[r] = __half2float(*reinterpret_cast<const __half*>(grp + 2 * b8));
+        } else if constexpr (F == QMV_Q4_K) {
+          const int g = lane >> 3, j = lane & 7;
+          const uint8_t* grp = row + g * 144;
+          uint4 h = *reinterpret_cast<const uint4*>(grp);
+          uint4 q = *reinterpret_cast<const uint4*>(grp + 16 + 16 * j);
+          const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
+          // low nibbles as bytes; high nibbles left in place (16 x code), taken
+          // by an unsigned-byte dp4a: isum = 16 * sum_lo + sum_hi16, and the
+          // 1/16 goes into the scale (exact: a power of two)
+#pragma unroll
+          for (int i = 0; i < 4; i++) {
+            w[r][i] = qq[i] & 0x0F0F0F0Fu;
+            w[r][4 + i] = qq[i] & 0xF0F0F0F0u;
+          }
+          // 12-bit field j (sc | m << 6) of the 96-bit string in h.y..h.w
+          const int bit = 12 * j;
+          const uint32_t wa = bit < 32 ? h.y : (bit < 64 ? h.z : h.w);
+          const uint32_t wb = bit < 32 ? h.z : (bit < 64 ? h.w : 0u);
+          const uint32_t f = __funnelshift_r(wa, wb, bit & 31) & 0xFFFu;
+          const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFF)));
+          const float dmin = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
+          sA[r] = d * (float)(f & 63u) * 0.0625f;
+          sB[r] = dmin * (float)(f >> 6);
+        } else {
+          const int g = lane >> 4, sb = (lane >> 3) & 1, j = lane & 7;
+          const uint8_t* grp = row + g * 272;
+          const uint2 meta = *reinterpret_cast<const uint2*>(grp + 8 * sb);
+          const uint4 q = *reinterpret_cast<const uint4*>(grp + 16 + 128 * sb + 16 * j);
+          const uint64_t m64 = ((uint64_t)meta.y << 32) | meta.x;
+          const int ls = (int)((m64 >> (16 + 6 * j)) & 63u);
+          const float d = __half2float(__ushort_as_half((unsigned short)(meta.x & 0xFFFF)));
+          sA[r] = d * (float)(ls - 32);
+          const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int i = 0; i < 4; i++) {
+            const uint32_t pw = qq[i];
+            const uint32_t pl = pw & 0x77777777u;
+            const uint32_t p4 = pw << 4;
+            w[r][2 * i] = iq4_lookup4(pl, pw, p4, 0xD9C8u);
+            w[r][2 * i + 1] = iq4_lookup4(pl >> 16, pw, p4, 0xFBEAu);
+          }
+        }
+      }
+    }
+    const int pos = act_pos(kb, 0);
+#pragma unroll
+    for (int t = 0; t < NT; t++) {
+      if (t < a.nt) {
+        const uint8_t* arow = a.q + t * a.stride;
+        const uint4 xa = *reinterpret_cast<const uint4*>(arow + pos);
+        const uint4 xb = *reinterpret_cast<const uint4*>(arow + pos + 128);
+        const float dx = a.d[t * a.blk + kb];
+        float dxs = 0.f;
+        if constexpr (F == QMV_Q4_K) dxs = a.ds[t * a.blk + kb];
+#pragma unroll
+        for (int r = 0; r < RW; r++) {
+          // two independent chains (first / second half of the block)
+          int ia, ib;
+          if constexpr (F == QMV_Q4_K) {
+            ia = dp4a_us(w[r][0], xa.x, 0);
+            ib = dp4a_us(w[r][4], xb.x, 0);
+            ia = dp4a_us(w[r][1], xa.y, ia);
+            ib = dp4a_us(w[r][5], xb.y, ib);
+            ia = dp4a_us(w[r][2], xa.z, ia);
+            ib = dp4a_us(w[r][6], xb.z, ib);
+            ia = dp4a_us(w[r][3], xa.w, ia);
+            ib = dp4a_us(w[r][7], xb.w, ib);
+          } else {
+            ia = __dp4a((int)w[r][0], (int)xa.x, 0);
+            ib = __dp4a((int)w[r][4], (int)xb.x, 0);
+            ia = __dp4a((int)w[r][1], (int)xa.y, ia);
+            ib = __dp4a((int)w[r][5], (int)xb.y, ib);
+            ia = __dp4a((int)w[r][2], (int)xa.z, ia);
+            ib = __dp4a((int)w[r][6], (int)xb.z, ib);
+            ia = __dp4a((int)w[r][3], (int)xa.w, ia);
+            ib = __dp4a((int)w[r][7], (int)xb.w, ib);
+          }
+          const int is = (F == QMV_Q4_K) ? ia * 16 + ib : ia + ib;
+          float v = acc[r][t] + (sA[r] * dx) * (float)is;
+          if constexpr (F == QMV_Q4_K) v -= sB[r] * dxs;
+          acc[r][t] = v;
+        }
+      }
+    }
+  }
+};
+
+// Sum of v over the 32 lanes, returned in every lane.
+__device__ __forceinline__ float warp_sum(float v) {
+  v += __shfl_xor_sync(FULL, v, 16);
+  v += __shfl_xor_sync(FULL, v, 8);
+  v += __shfl_xor_sync(FULL, v, 4);
+  v += __shfl_xor_sync(FULL, v, 2);
+  v += __shfl_xor_sync(FULL, v, 1);
+  return v;
+}
+
+// Pipeline barriers of a CTA: init by thread 0, then __syncthreads.
+__device__ __forceinline__ void init_pipeline(uint64_t* full, uint64_t* empty, int stages) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; s++) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], CONSUMER_WARPS);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+}
+
+// Position in the stage ring: iteration n uses stage st = n % stages in round
+// n / stages (tracked incrementally; the full barrier of round r completes
+// phase r, i.e. parity r & 1).
+struct Ring {
+  int st = 0, round = 0;
+  long long n = 0;
+  __device__ __forceinline__ void advance(int stages) {
+    n++;
+    if (++st == stages) {
+      st = 0;
+      round++;
+    }
+  }
+  __device__ __forceinline__ uint32_t parity() const { return (uint32_t)(round & 1); }
+};
+
+// Producer side: wait until the ring's current stage is free.
+__device__ __forceinline__ bool producer_acquire(uint64_t* empty, const Ring& r, int stages, unsigned* err) {
+  if (r.n < stages) return true;
+  return mbar_wait(&empty[r.st], (uint32_t)((r.round - 1) & 1), err);
+}
+
+// Producer side, before leaving: wait (bounded) for the copies of the last
+// `stages` iterations, so no copy lands in shared memory after exit.
+__device__ __forceinline__ void producer_drain(uint64_t* full, long long issued, int stages, unsigned* err) {
+  const long long first = issued > stages ? issued - stages : 0;
+  for (long long j = first; j < issued; j++) mbar_wait(&full[j % stages], (uint32_t)((j / stages) & 1), err);
+}
+
+}  // namespace qmv

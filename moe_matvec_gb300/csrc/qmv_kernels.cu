@@ -48,6 +48,50 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
   pdl_launch_dependents();
 }
 
+// MoE combine: y[t][m] = sum over routed slots k (in k order) of
+// gates[t][k] * o[t * top_k + k][m]; a slot that does not route (id out of
+// range, or repeating an earlier id of the token) adds nothing.  One thread
+// per 4 consecutive outputs of a token.
+__global__ void __launch_bounds__(256) moe_combine_kernel(const int32_t* __restrict__ ids,
+                                                          const float* __restrict__ gates,
+                                                          const float* __restrict__ o, float* __restrict__ y,
+                                                          int n_tok, int top_k, int n_experts, int hidden) {
+  pdl_wait();
+  const int q4 = hidden / 4;
+  const long long total = (long long)n_tok * q4;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(i / q4), m4 = (int)(i - (long long)t * q4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < top_k; k++) {
+      const int e = ids[t * top_k + k];
+      bool ok = e >= 0 && e < n_experts;
+      for (int kk = 0; kk < k && ok; kk++) ok = ids[t * top_k + kk] != e;
+      if (!ok) continue;
+      const float g = gates[t * top_k + k];
+      const float4 v = reinterpret_cast<const float4*>(o + ((long long)t * top_k + k) * hidden)[m4];
+      acc.x = fmaf(g, v.x, acc.x);
+      acc.y = fmaf(g, v.y, acc.y);
+      acc.z = fmaf(g, v.z, acc.z);
+      acc.w = fmaf(g, v.w, acc.w);
+    }
+    reinterpret_cast<float4*>(y + (long long)t * hidden)[m4] = acc;
+  }
+  pdl_launch_dependents();
+}
+
+cudaError_t launch_moe_combine(const int32_t* ids, const float* gates, const float* o, float* y, int n_tok,
+                               int top_k, int n_experts, int hidden, cudaStream_t stream, bool pdl) {
+  const long long total = (long long)n_tok * (hidden / 4);
+  long long ctas = (total + 255) / 256;
+  const long long cap = 4ll * device_sm_count();
+  if (ctas > cap) ctas = cap;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  make_config(cfg, attr, dim3((unsigned)ctas), dim3(256), 0, stream, pdl);
+  return cudaLaunchKernelEx(&cfg, moe_combine_kernel, ids, gates, o, y, n_tok, top_k, n_experts, hidden);
+}
+
 void make_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, dim3 grid, dim3 block, size_t smem,
                  cudaStream_t stream, bool pdl) {
   cfg = cudaLaunchConfig_t{};
