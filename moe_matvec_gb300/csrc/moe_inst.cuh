@@ -20,6 +20,8 @@ static cudaError_t launch_moe_nt(const MoeLaunch& L) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              device_smem_optin() - (int)fa.sharedSizeBytes);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
     configured |= 1ull << dev;
   }
   cudaLaunchConfig_t cfg;

@@ -39,7 +39,7 @@ struct MoeParams {
   int R;                // outputs per expert (ffn for GATE_UP, hidden for DOWN)
   int pool_rows;        // rows per expert in the weight pool (2*ffn or hidden)
   int groups;           // K / group weights
-  int stages, act_stride, act_blk;
+  int stages, act_nck;
   unsigned* err;
 };
 
@@ -143,30 +143,31 @@ struct MoeWalk {
 };
 
 template <int F, int NT, int MODE>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
     moe_qmv_kernel(const __grid_constant__ CUtensorMap map_tile, const __grid_constant__ CUtensorMap map_unit,
                    const MoeParams p) {
   constexpr int CB = chunk_bytes<F>();
   constexpr int STAGE_BYTES = TILE_ROWS * CB;
   // GATE_UP: a tile is up to 2 units of 8 outputs j: gate rows j in stage rows
-  // 0..15, up rows j in stage rows 16..31; warp w takes output j0 + w.
-  // DOWN: a tile is up to 4 units of 8 rows; warp w takes rows 2w, 2w+1.
+  // 0..15, up rows j in stage rows 16..31; warp w takes outputs j0 + 2w and
+  // j0 + 2w + 1 (stage rows 2w, 2w+1 and 16+2w, 17+2w).
+  // DOWN: a tile is up to 4 units of 8 rows; warp w takes rows 4w .. 4w+3.
   constexpr int TILE_UNITS = MODE == MOE_GATE_UP ? 2 : 4;
   __shared__ MoeRouting rt;
   __shared__ int s_rows[16];
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stages = smem;
-  ActView a;
-  a.q = stages + p.stages * STAGE_BYTES;
-  a.d = reinterpret_cast<float*>(a.q + NT * p.act_stride);
-  a.ds = a.d + NT * p.act_blk;
-  a.stride = p.act_stride;
-  a.blk = p.act_blk;
-  uint64_t* full = reinterpret_cast<uint64_t*>(a.ds + NT * p.act_blk);
+  ActArea a;
+  a.carve(stages + p.stages * STAGE_BYTES, F, NT, p.act_nck);
+  uint64_t* full = reinterpret_cast<uint64_t*>(stages + p.stages * STAGE_BYTES + act_area_bytes(F, NT, p.act_nck));
   uint64_t* empty = full + MAX_STAGES;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   init_pipeline(full, empty, p.stages);
+  // GATE_UP reads ids, which the preceding kernel may produce, so it waits
+  // before routing and only then lets the next kernel launch; DOWN launches
+  // after every GATE_UP CTA passed that wait, so its ids are complete.
+  if (MODE == MOE_GATE_UP) pdl_wait();
   pdl_launch_dependents();
   build_routing(rt, p, NT, MODE == MOE_GATE_UP && blockIdx.x == 0);
   const int units_per_pair = p.R / UNIT_ROWS;
@@ -178,7 +179,35 @@ __global__ void __launch_bounds__(THREADS, 1)
       prefetch_tensormap(&map_tile);
       prefetch_tensormap(&map_unit);
       const uint64_t pol = policy_evict_first();
-      pdl_wait();
+      // L2 lookahead of PREFETCH_STAGES iterations past the ring (see the
+      // dense kernel): the expert rows keep streaming while the consumers
+      // stage activations or wait for the preceding grid.
+      MoeWalk pw(rt.n_pairs, units_per_pair, TILE_UNITS);
+      int pq = 0, pu = 0, pnu = 0, pc = 0;
+      bool pvalid = pw.next(pq, pu, pnu);
+      long long pf_n = 0;
+      auto prefetch_to = [&](long long target) {
+        for (; pvalid && pf_n < target; pf_n++) {
+          if (pf_n >= p.stages) {
+            const int base = rt.pair_expert[pq] * p.pool_rows;
+            const int x = pc * CB / 8;
+            if (MODE == MOE_GATE_UP) {
+              for (int i = 0; i < pnu; i++) {
+                tma_prefetch_2d(&map_unit, x, base + (pu + i) * UNIT_ROWS);
+                tma_prefetch_2d(&map_unit, x, base + p.R + (pu + i) * UNIT_ROWS);
+              }
+            } else if (pnu == TILE_UNITS) {
+              tma_prefetch_2d(&map_tile, x, base + pu * UNIT_ROWS);
+            } else {
+              for (int i = 0; i < pnu; i++) tma_prefetch_2d(&map_unit, x, base + (pu + i) * UNIT_ROWS);
+            }
+          }
+          if (++pc == nck) {
+            pc = 0;
+            pvalid = pw.next(pq, pu, pnu);
+          }
+        }
+      };
       MoeWalk walk(rt.n_pairs, units_per_pair, TILE_UNITS);
       int q, u, nu;
       Ring ring;
@@ -186,6 +215,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       while (alive && walk.next(q, u, nu)) {
         const int base = rt.pair_expert[q] * p.pool_rows;
         for (int c = 0; c < nck; c++, ring.advance(p.stages)) {
+          if (ring.n >= p.stages) prefetch_to(ring.n + PREFETCH_STAGES);
           if (!producer_acquire(empty, ring, p.stages, p.err)) {
             alive = false;
             break;
@@ -218,34 +248,37 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   // ---------------- consumers ----------------
-  pdl_wait();  // x (or h) may come from the preceding kernel
+  if (MODE == MOE_DOWN) pdl_wait();  // h comes from the preceding kernel
   const int cw = warp;
   bool alive = true;
   MoeWalk walk(rt.n_pairs, units_per_pair, TILE_UNITS);
   int q, u, nu;
   Ring ring;
-  int staged_pair = -1;
+  int staged_pair = -1, nt = 0, first = 0;
+  const Consumer<F, NT> cons(lane);
   float acc[RW][NT];
 #pragma unroll
   for (int r = 0; r < RW; r++)
 #pragma unroll
     for (int t = 0; t < NT; t++) acc[r][t] = 0.f;
-  int srow[RW];
+  int roff[RW];  // stage row of each of the warp's rows
   if constexpr (MODE == MOE_GATE_UP) {
-    srow[0] = cw;
-    srow[1] = 16 + cw;
+    roff[0] = 2 * cw;
+    roff[1] = 2 * cw + 1;
+    roff[2] = 16 + 2 * cw;
+    roff[3] = 17 + 2 * cw;
   } else {
 #pragma unroll
-    for (int r = 0; r < RW; r++) srow[r] = cw * RW + r;
+    for (int r = 0; r < RW; r++) roff[r] = cw * RW + r;
   }
   const int nblk = p.K / BLK;
 
   while (walk.next(q, u, nu)) {
-    const int first = rt.pair_first[q];
-    a.nt = rt.pair_count[q];
     if (q != staged_pair) {
+      first = rt.pair_first[q];
+      nt = rt.pair_count[q];
       named_sync(1, CONSUMER_THREADS);
-      if (threadIdx.x < a.nt) {
+      if (threadIdx.x < nt) {
         const int slot = rt.slots[first + threadIdx.x];
         s_rows[threadIdx.x] = MODE == MOE_GATE_UP ? slot / p.top_k : slot;
       }
@@ -256,27 +289,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         src.wd = p.hd;
         src.ws = p.hs;
       }
-      stage_activations<F>(src, 0, nblk, a, cw, lane);
+      stage_activations<F, NT>(src, 0, nblk, nt, a, cw, lane);
       named_sync(1, CONSUMER_THREADS);
       staged_pair = q;
     }
+    // valid outputs of this tile: GATE_UP nu * 8 columns j, DOWN nu * 8 rows
     const int nvalid = nu * UNIT_ROWS;
-    unsigned rmask = 0;
-    if constexpr (MODE == MOE_GATE_UP) {
-      if (cw < nvalid) rmask = 3u;
-    } else {
-#pragma unroll
-      for (int r = 0; r < RW; r++)
-        if (srow[r] < nvalid) rmask |= 1u << r;
-    }
+    const bool active = MODE == MOE_GATE_UP ? 2 * cw < nvalid : cw * RW < nvalid;
     for (int c = 0; c < nck && alive; c++, ring.advance(p.stages)) {
       const int st = ring.st;
       if (!mbar_wait(&full[st], ring.parity(), p.err)) {
         alive = false;
         break;
       }
-      const int kb = c * (KCHUNK / BLK) + lane;
-      if (rmask && kb < nblk) Consumer<F, NT>::chunk(stages + st * STAGE_BYTES, srow, rmask, lane, kb, a, acc);
+      if (active) {
+        const uint8_t* sb = stages + st * STAGE_BYTES;
+        const uint8_t* rows[RW];
+#pragma unroll
+        for (int r = 0; r < RW; r++) rows[r] = sb + roff[r] * CB;
+        cons.chunk(rows, a.q + (size_t)c * NT * ACT_BYTES, a.d + c * NT * 32 + lane, a.ds + c * NT * 32 + lane,
+                   lane, acc);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
@@ -286,18 +319,22 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
     for (int t = 0; t < NT; t++) {
       if constexpr (MODE == MOE_GATE_UP) {
-        const float g = warp_sum(acc[0][t]);
-        const float v = warp_sum(acc[1][t]);
-        if (lane == (t & 31) && t < a.nt && rmask) {
-          const float h = g / (1.0f + expf(-g)) * v;
-          p.dst[(long long)rt.slots[first + t] * p.R + row0 + cw] = h;
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+          const float g = warp_sum(acc[i][t]);
+          const float v = warp_sum(acc[2 + i][t]);
+          const int j = 2 * cw + i;
+          if (lane == ((2 * t + i) & 31) && t < nt && j < nvalid) {
+            const float h = g / (1.0f + expf(-g)) * v;
+            p.dst[(long long)rt.slots[first + t] * p.R + row0 + j] = h;
+          }
         }
       } else {
 #pragma unroll
         for (int r = 0; r < RW; r++) {
           const float v = warp_sum(acc[r][t]);
-          if (lane == ((r * NT + t) & 31) && t < a.nt && ((rmask >> r) & 1u))
-            p.dst[(long long)rt.slots[first + t] * p.R + row0 + srow[r]] = v;
+          if (lane == ((r * NT + t) & 31) && t < nt && roff[r] < nvalid)
+            p.dst[(long long)rt.slots[first + t] * p.R + row0 + roff[r]] = v;
         }
       }
 #pragma unroll

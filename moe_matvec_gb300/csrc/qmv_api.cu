@@ -113,12 +113,32 @@ static int check_device() {
 // ---------------------------------------------------------------------------
 struct Plan {
   int nt_tmpl, passes_tok, stages, grid;
-  int act_stride, act_blk;
+  int act_nck;
   size_t smem;
 };
 
-static size_t act_bytes(int nt, int act_stride, int act_blk) {
-  return (size_t)nt * act_stride + 2 * (size_t)nt * act_blk * sizeof(float);
+// Shared memory a CTA may take so that two fit on one SM (each CTA also
+// carries 1 KB reserved by the system).
+constexpr size_t TWO_PER_SM_BYTES = 112 * 1024;
+constexpr int TWO_PER_SM_STAGES = 4;
+
+// Stage count and shared-memory size for an activation area of `act` bytes:
+// small token counts aim for two CTAs per SM (so that consecutive calls
+// overlap under programmatic dependent launch) with a short ring; otherwise
+// one CTA per SM with a deeper ring.
+static bool plan_stages(int nt, size_t act, int stage_bytes, size_t budget, int& stages, size_t& smem) {
+  const size_t fixed = act + 2 * MAX_STAGES * sizeof(uint64_t) + 128;
+  if (nt <= 4 && fixed + 2 * (size_t)stage_bytes <= TWO_PER_SM_BYTES) {
+    int st = (int)((TWO_PER_SM_BYTES - fixed) / stage_bytes);
+    stages = st > TWO_PER_SM_STAGES ? TWO_PER_SM_STAGES : st;
+  } else if (fixed + 2 * (size_t)stage_bytes <= budget) {
+    int st = (int)((budget - fixed) / stage_bytes);
+    stages = st > MAX_STAGES ? MAX_STAGES : st;
+  } else {
+    return false;
+  }
+  smem = (size_t)stages * stage_bytes + fixed;
+  return true;
 }
 
 // Choose the compiled token count and the number of stages so that the
@@ -127,30 +147,23 @@ static bool plan_dense(int fmt, long long M, long long K, int n_tok, int n_split
   const int gw = group_weights(fmt);
   const long long groups = K / gw;
   const long long max_range = ((groups + n_split - 1) / n_split) * gw;  // weights
-  pl.act_stride = (int)(((max_range + 255) / 256) * 256);
-  pl.act_blk = pl.act_stride / 32;
+  pl.act_nck = (int)((max_range + KCHUNK - 1) / KCHUNK);
   const int stage_bytes = TILE_ROWS * chunk_bytes_of(fmt);
-  const size_t bar_bytes = 2 * MAX_STAGES * sizeof(uint64_t);
   const size_t budget = (size_t)device_smem_optin();
   int nt = 16;
   while (nt > n_tok && nt > 1) nt >>= 1;
   if (nt < n_tok && nt < 16) nt <<= 1;  // smallest power of two >= n_tok (<= 16)
   for (;; nt >>= 1) {
-    size_t fixed = act_bytes(nt, pl.act_stride, pl.act_blk) + bar_bytes + 128;
-    if (fixed + 2 * (size_t)stage_bytes <= budget) {
-      int st = (int)((budget - fixed) / stage_bytes);
-      pl.stages = st > MAX_STAGES ? MAX_STAGES : st;
-      pl.smem = (size_t)pl.stages * stage_bytes + fixed;
-      break;
-    }
+    if (plan_stages(nt, act_area_bytes(fmt, nt, pl.act_nck), stage_bytes, budget, pl.stages, pl.smem)) break;
     if (nt == 1) return false;
   }
   pl.nt_tmpl = nt;
   pl.passes_tok = (n_tok + nt - 1) / nt;
   const long long units = (M + UNIT_ROWS - 1) / UNIT_ROWS;
   const long long work = units * n_split;
-  const int sms = device_sm_count();
-  pl.grid = (int)(work < sms ? work : sms);
+  // two CTAs per SM when they fit (more warps to hide latency), else one
+  const int ctas = device_sm_count() * (pl.smem <= TWO_PER_SM_BYTES && nt <= 4 ? 2 : 1);
+  pl.grid = (int)(work < ctas ? work : ctas);
   return true;
 }
 
@@ -184,8 +197,7 @@ static int run_dense(int fmt, const void* W, const float* x, const int8_t* xq, c
   p.groups = (int)(K / group_weights(fmt));
   p.units = (int)((M + UNIT_ROWS - 1) / UNIT_ROWS);
   p.stages = pl.stages;
-  p.act_stride = pl.act_stride;
-  p.act_blk = pl.act_blk;
+  p.act_nck = pl.act_nck;
   p.err = device_error_word();
   L.p = &p;
   L.nt_tmpl = pl.nt_tmpl;
@@ -268,20 +280,20 @@ static int run_moe_proj(int mode, int fmt, const void* pool, MoeParams& p, int n
   MoeLaunch L;
   if (!encode_rows(&L.map_tile, pool, rows, rb, chunk_bytes_of(fmt), TILE_ROWS)) return QMV_ERR_CUDA;
   if (!encode_rows(&L.map_unit, pool, rows, rb, chunk_bytes_of(fmt), UNIT_ROWS)) return QMV_ERR_CUDA;
-  p.act_stride = (int)(((long long)p.K + 255) / 256 * 256);
-  p.act_blk = p.act_stride / 32;
+  p.act_nck = (p.K + KCHUNK - 1) / KCHUNK;
   p.groups = p.K / group_weights(fmt);
   const int stage_bytes = TILE_ROWS * chunk_bytes_of(fmt);
+  // the routing tables are static shared memory: count them with the
+  // activation area when sizing, and leave them out of the dynamic size
   const size_t static_bytes = sizeof(MoeRouting) + 16 * sizeof(int) + 256;
-  const size_t budget = (size_t)device_smem_optin() - static_bytes;
-  const size_t fixed = act_bytes(nt, p.act_stride, p.act_blk) + 2 * MAX_STAGES * sizeof(uint64_t) + 128;
-  if (fixed + 2 * (size_t)stage_bytes > budget) return QMV_ERR_SHAPE;
-  int st = (int)((budget - fixed) / stage_bytes);
-  p.stages = st > MAX_STAGES ? MAX_STAGES : st;
+  size_t smem = 0;
+  if (!plan_stages(nt, act_area_bytes(fmt, nt, p.act_nck) + static_bytes, stage_bytes,
+                   (size_t)device_smem_optin(), p.stages, smem))
+    return QMV_ERR_SHAPE;
   L.p = &p;
   L.nt_tmpl = nt;
   L.grid = device_sm_count();
-  L.smem = (size_t)p.stages * stage_bytes + fixed;
+  L.smem = smem - static_bytes;
   L.stream = stream;
   L.pdl = true;
   return launch_moe_any(mode, fmt, L) == cudaSuccess ? QMV_OK : QMV_ERR_CUDA;

@@ -1,44 +1,59 @@
 // Core of every quantized matvec kernel in the library: the activation
 // staging (per-32 int8 quantization into shared memory, in the byte order each
 // weight format consumes) and the consumer step that decodes one 1024-weight
-// chunk of up to RW weight rows in registers and accumulates exact int32
-// block dot products (dp4a) scaled in fp32.
+// chunk of RW weight rows in registers and accumulates exact int32 block dot
+// products (dp4a) scaled in fp32.
 //
 // Shared by the dense matvec / split-K kernel and the expert-grouped MoE
 // kernels ("Castagna Veloce", section "Kernels for the MI50": small-batch
 // matvecs and MoE decode kernels; section "Fused operations": Q8 activations
 // reused across weight types).
+//
+// Shared-memory activation area (NT token slots, nck chunks of 1024 weights):
+//   q  [nck][NT][1024] int8   codes, blocks of one chunk interleaved (act_pos)
+//   d  [nck][NT][32]   f32    block scales
+//   ds [nck][NT][32]   f32    block scale x block code sum (Q4_K only)
+// Token slots past the staged tokens and blocks past the K-range are zero, so
+// the consumer needs no per-token or per-block predicates: a zero code and a
+// zero scale add exactly nothing.
 #pragma once
 #include "common.cuh"
 
 namespace qmv {
 
-constexpr int CONSUMER_WARPS = 16;
-constexpr int RW = 2;                                 // rows per consumer warp
+constexpr int CONSUMER_WARPS = 8;
+constexpr int RW = 4;                                 // rows per consumer warp
 constexpr int TILE_ROWS = CONSUMER_WARPS * RW;        // 32
 constexpr int UNIT_ROWS = 8;                          // partition / tail-box granularity
 constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;    // + producer warp
 constexpr int CONSUMER_THREADS = CONSUMER_WARPS * 32;
 constexpr int MAX_STAGES = 8;
+constexpr int PREFETCH_STAGES = 16;                   // L2 lookahead of the producer (iterations)
+constexpr int ACT_BYTES = KCHUNK;                     // codes per token per chunk
 constexpr unsigned FULL = 0xffffffffu;
 
-// Shared-memory position of byte p (0..31) of activation block b of a token
-// row: within every 256-weight group, the first 16 bytes of the 8 blocks come
-// first, then the last 16, so that the 8 lanes of a quarter-warp read 128
-// contiguous bytes.
-__device__ __forceinline__ int act_pos(int b, int p) {
-  return (b >> 3) * 256 + (p >> 4) * 128 + (b & 7) * 16 + (p & 15);
+// Byte p (0..31) of block l (0..31) of a token's 1024-byte chunk of codes:
+// within every 8 blocks the first 16 bytes come first, then the last 16, so
+// that the 8 lanes of a quarter-warp read 128 contiguous bytes.
+__device__ __forceinline__ int act_pos(int l, int p) {
+  return (l >> 3) * 256 + (p >> 4) * 128 + (l & 7) * 16 + (p & 15);
 }
 
-// The activation area of a CTA: nt token rows of codes, scales d and, for
-// Q4_K, d * s.
-struct ActView {
+// Bytes of the activation area for nt_slots token slots and nck chunks.
+__host__ __device__ constexpr size_t act_area_bytes(int F, int nt_slots, int nck) {
+  return (size_t)nck * nt_slots * (ACT_BYTES + 32 * sizeof(float) * (F == QMV_Q4_K ? 2 : 1));
+}
+
+struct ActArea {
   uint8_t* q;
   float* d;
   float* ds;
-  int nt;
-  int stride;  // bytes per token row of q (multiple of 256)
-  int blk;     // floats per token row of d / ds (stride / 32)
+  __device__ void carve(uint8_t* base, int F, int nt_slots, int nck) {
+    q = base;
+    d = reinterpret_cast<float*>(base + (size_t)nck * nt_slots * ACT_BYTES);
+    ds = d + (size_t)nck * nt_slots * 32;
+    (void)F;
+  }
 };
 
 // Quantize four consecutive elements of a 32-block spread over 8 lanes
@@ -69,28 +84,28 @@ __device__ __forceinline__ Quad quant_quad(float4 v) {
   return {packed, d, s};
 }
 
-// Store the packed codes of elements 4*li..4*li+3 of block b (li = lane & 7)
-// into the activation area in the byte order format F consumes.  For IQ4_XS
-// a block is stored interleaved (byte 2i = x_i, byte 2i+1 = x_{i+16}), the
-// order in which its codebook lookups come out; the other formats use the
+// Store the packed codes of elements 4*li..4*li+3 of block l (li = lane & 7)
+// into a token's chunk of codes in the byte order format F consumes.  For
+// IQ4_XS a block is stored interleaved (byte 2i = x_i, byte 2i+1 = x_{i+16}),
+// the order in which its codebook lookups come out; the other formats use the
 // natural order.  Must be called by all 32 lanes (it shuffles).
 template <int F>
-__device__ __forceinline__ void store_act_quad(uint8_t* row, int b, int li, uint32_t packed, bool ok) {
+__device__ __forceinline__ void store_act_quad(uint8_t* chunk, int l, int li, uint32_t packed) {
   if constexpr (F == QMV_IQ4_XS) {
     uint32_t hi = __shfl_xor_sync(FULL, packed, 4);  // elements 16 + 4*li ..
-    if (ok && li < 4) {
+    if (li < 4) {
       uint2 w;
       w.x = __byte_perm(packed, hi, 0x5140);
       w.y = __byte_perm(packed, hi, 0x7362);
-      *reinterpret_cast<uint2*>(row + act_pos(b, 8 * li)) = w;
+      *reinterpret_cast<uint2*>(chunk + act_pos(l, 8 * li)) = w;
     }
   } else {
-    if (ok) *reinterpret_cast<uint32_t*>(row + act_pos(b, 4 * li)) = packed;
+    *reinterpret_cast<uint32_t*>(chunk + act_pos(l, 4 * li)) = packed;
   }
 }
 
-// Where the activation rows of a stage come from: fp32 rows (quantized while
-// staging) or pre-quantized rows; token slot t reads source row rows[t] (a
+// Where the activation rows come from: fp32 rows (quantized while staging)
+// or pre-quantized rows; token slot t reads source row rows[t] (a
 // shared-memory list) or row0 + t.  When wq is set, the quantized codes,
 // scales and sums are also written back to global memory (natural order),
 // which is how the MoE path exposes the quantized h.
@@ -99,7 +114,7 @@ struct ActSource {
   const int8_t* xq;
   const float* xd;
   const int32_t* xs;
-  long long ld;      // elements per source row (K of the rows)
+  long long ld;      // elements per source row
   const int* rows;   // nullptr: rows row0 .. row0 + nt - 1
   long long row0;
   int8_t* wq;
@@ -108,50 +123,71 @@ struct ActSource {
   __device__ __forceinline__ long long row(int t) const { return rows ? (long long)rows[t] : row0 + t; }
 };
 
-// Stage blocks [kb0, kb0 + nblk) of the a.nt token rows of `src` into the
-// activation area.  Called by all consumer warps (cw = warp index).
-template <int F>
-__device__ __forceinline__ void stage_activations(const ActSource& src, int kb0, int nblk, const ActView& a, int cw, int lane) {
+// Stage blocks [kb0, kb0 + nblk) of tokens [0, nt) of `src` into the area
+// (NT slots, ceil(nblk / 32) chunks), zero-filling the padding.  Called by all
+// consumer warps; each warp handles 16 blocks per step (8 lanes per block,
+// 4 elements per lane) with all of the step's loads issued before any use.
+template <int F, int NT>
+__device__ __forceinline__ void stage_activations(const ActSource& src, int kb0, int nblk, int nt, const ActArea& a,
+                                                  int cw, int lane) {
   const int sub = lane >> 3, li = lane & 7;
-  const int total = a.nt * nblk;
-  for (int base = cw * 4; base < total; base += CONSUMER_WARPS * 4) {
-    const int idx = base + sub;
-    const bool ok = idx < total;
-    const int t = ok ? idx / nblk : 0;
-    const int b = ok ? idx - t * nblk : 0;
-    const long long r = ok ? src.row(t) : 0;
-    const long long blk = r * (src.ld / 32) + kb0 + b;  // global block index
-    uint32_t packed;
-    float d;
-    int s;
-    if (src.x != nullptr) {
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (ok) v = __ldg(reinterpret_cast<const float4*>(src.x + blk * 32) + li);
-      Quad qd = quant_quad(v);
-      packed = qd.q;
-      d = qd.d;
-      s = qd.s;
-      if (src.wq != nullptr && ok) {
-        reinterpret_cast<uint32_t*>(src.wq + blk * 32)[li] = packed;
-        if (li == 0) {
-          src.wd[blk] = d;
-          src.ws[blk] = s;
+  const int nck = (nblk + 31) / 32;
+  const int total = nck * NT * 32;
+  for (int base = cw * 16; base < total; base += CONSUMER_WARPS * 16) {
+    int ct[4], l[4];
+    bool real[4];
+    long long gblk[4];
+    float4 v[4];
+    uint32_t pk[4];
+    float dd[4];
+    int ss[4];
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const int idx = base + 4 * u + sub;
+      l[u] = idx & 31;
+      ct[u] = idx >> 5;
+      const int t = ct[u] & (NT - 1), c = ct[u] / NT;
+      const int b = c * 32 + l[u];
+      real[u] = idx < total && t < nt && b < nblk;
+      gblk[u] = real[u] ? src.row(t) * (src.ld / 32) + kb0 + b : 0;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      pk[u] = 0;
+      dd[u] = 0.f;
+      ss[u] = 0;
+      if (real[u]) {
+        if (src.x != nullptr) {
+          v[u] = __ldg(reinterpret_cast<const float4*>(src.x + gblk[u] * 32) + li);
+        } else {
+          pk[u] = __ldg(reinterpret_cast<const uint32_t*>(src.xq + gblk[u] * 32) + li);
+          dd[u] = __ldg(src.xd + gblk[u]);
+          ss[u] = __ldg(src.xs + gblk[u]);
         }
       }
-    } else {
-      packed = 0;
-      d = 0.f;
-      s = 0;
-      if (ok) {
-        packed = __ldg(reinterpret_cast<const uint32_t*>(src.xq + blk * 32) + li);
-        d = __ldg(src.xd + blk);
-        s = __ldg(src.xs + blk);
-      }
     }
-    store_act_quad<F>(a.q + t * a.stride, b, li, packed, ok);
-    if (ok && li == 0) {
-      a.d[t * a.blk + b] = d;
-      if constexpr (F == QMV_Q4_K) a.ds[t * a.blk + b] = d * (float)s;
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      if (src.x != nullptr) {
+        const Quad qd = quant_quad(v[u]);
+        pk[u] = qd.q;
+        dd[u] = qd.d;
+        ss[u] = qd.s;
+        if (src.wq != nullptr && real[u]) {
+          reinterpret_cast<uint32_t*>(src.wq + gblk[u] * 32)[li] = pk[u];
+          if (li == 0) {
+            src.wd[gblk[u]] = dd[u];
+            src.ws[gblk[u]] = ss[u];
+          }
+        }
+      }
+      // total is a multiple of 32 and a step covers 16 aligned blocks, so this
+      // test is the same in every lane (store_act_quad shuffles)
+      if (base + 4 * u < total) {
+        store_act_quad<F>(a.q + (size_t)ct[u] * ACT_BYTES, l[u], li, pk[u]);
+        if (li == 0) {
+          a.d[ct[u] * 32 + l[u]] = dd[u];
+          if constexpr (F == QMV_Q4_K) a.ds[ct[u] * 32 + l[u]] = dd[u] * (float)ss[u];
+        }
+      }
     }
   }
 }
@@ -185,119 +221,138 @@ __device__ __forceinline__ uint32_t iq4_lookup4(uint32_t pl, uint32_t p, uint32_
   return (hi & m) | (lo & ~m);
 }
 
+// The consumer step.  Each lane owns one 32-weight block of every chunk; its
+// byte offsets inside a staged row chunk and inside the activation chunk are
+// fixed for the whole kernel.
 template <int F, int NT>
 struct Consumer {
-  // Accumulate one chunk for the warp's RW rows (stage rows srow[r], active
-  // when bit r of rmask is set) and the lane's 32-weight block: l = lane
-  // within the chunk, kb = block index within the staged K-range.
-  static __device__ __forceinline__ void chunk(const uint8_t* stage, const int (&srow)[RW], unsigned rmask,
-                                               int lane, int kb, const ActView& a, float (&acc)[RW][NT]) {
-    constexpr int CB = chunk_bytes<F>();
-    uint32_t w[RW][8];   // decoded int8 operands, paired with act words 0..7
-    float sA[RW];        // per-row multiplier of d_x * isum
-    float sB[RW];        // Q4_K: dmin * m (multiplier of d_x * s)
+  int w_off;  // payload of the lane's block in a row chunk
+  int h_off;  // header bytes the lane needs in a row chunk
+  int a_off;  // the lane's block in a token's activation chunk
+  int fsel;   // Q4_K: which word pair holds the lane's 12-bit scale field
+  int fsh;    // Q4_K: its bit offset in that pair
+
+  __device__ explicit Consumer(int lane) {
+    if constexpr (F == QMV_Q8_0) {
+      const int g = lane >> 3, b8 = lane & 7;
+      w_off = g * 272 + 16 + 16 * b8;
+      h_off = g * 272 + 2 * b8;
+    } else if constexpr (F == QMV_Q4_K) {
+      const int g = lane >> 3, j = lane & 7;
+      w_off = g * 144 + 16 + 16 * j;
+      h_off = g * 144;
+    } else {
+      const int g = lane >> 4, sb = (lane >> 3) & 1, j = lane & 7;
+      w_off = g * 272 + 16 + 128 * sb + 16 * j;
+      h_off = g * 272 + 8 * sb;
+    }
+    a_off = act_pos(lane, 0);
+    fsel = (12 * (lane & 7)) >> 5;
+    fsh = (12 * (lane & 7)) & 31;
+  }
+
+  // rows[r]: start of row r's chunk in the stage; aq / ad / ads: this chunk's
+  // activation codes / scales / scale-sums (token slot 0).
+  __device__ __forceinline__ void chunk(const uint8_t* const (&rows)[RW], const uint8_t* aq, const float* ad,
+                                        const float* ads, int lane, float (&acc)[RW][NT]) const {
+    uint32_t w[RW][8];  // decoded operands, paired with activation words 0..7
+    float sA[RW];       // multiplier of d_x * isum
+    float sB[RW];       // Q4_K: dmin * m, multiplier of d_x * s
 #pragma unroll
     for (int r = 0; r < RW; r++) {
-      sA[r] = 0.f;
-      sB[r] = 0.f;
+      const uint8_t* row = rows[r];
+      if constexpr (F == QMV_Q8_0) {
+        const uint4 x0 = *reinterpret_cast<const uint4*>(row + w_off);
+        const uint4 x1 = *reinterpret_cast<const uint4*>(row + w_off + 128);
+        w[r][0] = x0.x; w[r][1] = x0.y; w[r][2] = x0.z; w[r][3] = x0.w;
+        w[r][4] = x1.x; w[r][5] = x1.y; w[r][6] = x1.z; w[r][7] = x1.w;
+        sA[r] = __half2float(*reinterpret_cast<const __half*>(row + h_off));
+        sB[r] = 0.f;
+      } else if constexpr (F == QMV_Q4_K) {
+        const uint4 h = *reinterpret_cast<const uint4*>(row + h_off);
+        const uint4 q = *reinterpret_cast<const uint4*>(row + w_off);
+        const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
+        // low nibbles as bytes; high nibbles left in place (16 x code) for an
+        // unsigned-byte dp4a: isum = 16 * sum_lo + sum_hi16, and the 1/16 is
+        // folded into the scale (exact: a power of two)
 #pragma unroll
-      for (int i = 0; i < 8; i++) w[r][i] = 0;
-      if ((rmask >> r) & 1u) {
-        const uint8_t* row = stage + srow[r] * CB;
-        if constexpr (F == QMV_Q8_0) {
-          const int g = lane >> 3, b8 = lane & 7;
-          const uint8_t* grp = row + g * 272;
-          uint4 x0 = *reinterpret_cast<const uint4*>(grp + 16 + 16 * b8);
-          uint4 x1 = *reinterpret_cast<const uint4*>(grp + 16 + 128 + 16 * b8);
-          w[r][0] = x0.x; w[r][1] = x0.y; w[r][2] = x0.z; w[r][3] = x0.w;
-          w[r][4] = x1.x; w[r][5] = x1.y; w[r][6] = x1.z; w[r][7] = x1.w;
-          sA[r] = __half2float(*reinterpret_cast<const __half*>(grp + 2 * b8));
-        } else if constexpr (F == QMV_Q4_K) {
-          const int g = lane >> 3, j = lane & 7;
-          const uint8_t* grp = row + g * 144;
-          uint4 h = *reinterpret_cast<const uint4*>(grp);
-          uint4 q = *reinterpret_cast<const uint4*>(grp + 16 + 16 * j);
-          const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
-          // low nibbles as bytes; high nibbles left in place (16 x code), taken
-          // by an unsigned-byte dp4a: isum = 16 * sum_lo + sum_hi16, and the
-          // 1/16 goes into the scale (exact: a power of two)
+        for (int i = 0; i < 4; i++) {
+          w[r][i] = qq[i] & 0x0F0F0F0Fu;
+          w[r][4 + i] = qq[i] & 0xF0F0F0F0u;
+        }
+        const uint32_t wa = fsel == 0 ? h.y : (fsel == 1 ? h.z : h.w);
+        const uint32_t wb = fsel == 0 ? h.z : (fsel == 1 ? h.w : 0u);
+        const uint32_t f = __funnelshift_r(wa, wb, fsh);
+        const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFF)));
+        const float dmin = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
+        sA[r] = d * (0.0625f * (float)(f & 63u));
+        sB[r] = dmin * (float)((f >> 6) & 63u);
+      } else {
+        const uint2 meta = *reinterpret_cast<const uint2*>(row + h_off);
+        const uint4 q = *reinterpret_cast<const uint4*>(row + w_off);
+        const int j = lane & 7;
+        const uint64_t m64 = ((uint64_t)meta.y << 32) | meta.x;
+        const int ls = (int)((m64 >> (16 + 6 * j)) & 63u);
+        sA[r] = __half2float(__ushort_as_half((unsigned short)(meta.x & 0xFFFF))) * (float)(ls - 32);
+        sB[r] = 0.f;
+        const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-          for (int i = 0; i < 4; i++) {
-            w[r][i] = qq[i] & 0x0F0F0F0Fu;
-            w[r][4 + i] = qq[i] & 0xF0F0F0F0u;
-          }
-          // 12-bit field j (sc | m << 6) of the 96-bit string in h.y..h.w
-          const int bit = 12 * j;
-          const uint32_t wa = bit < 32 ? h.y : (bit < 64 ? h.z : h.w);
-          const uint32_t wb = bit < 32 ? h.z : (bit < 64 ? h.w : 0u);
-          const uint32_t f = __funnelshift_r(wa, wb, bit & 31) & 0xFFFu;
-          const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFF)));
-          const float dmin = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
-          sA[r] = d * (float)(f & 63u) * 0.0625f;
-          sB[r] = dmin * (float)(f >> 6);
-        } else {
-          const int g = lane >> 4, sb = (lane >> 3) & 1, j = lane & 7;
-          const uint8_t* grp = row + g * 272;
-          const uint2 meta = *reinterpret_cast<const uint2*>(grp + 8 * sb);
-          const uint4 q = *reinterpret_cast<const uint4*>(grp + 16 + 128 * sb + 16 * j);
-          const uint64_t m64 = ((uint64_t)meta.y << 32) | meta.x;
-          const int ls = (int)((m64 >> (16 + 6 * j)) & 63u);
-          const float d = __half2float(__ushort_as_half((unsigned short)(meta.x & 0xFFFF)));
-          sA[r] = d * (float)(ls - 32);
-          const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-          for (int i = 0; i < 4; i++) {
-            const uint32_t pw = qq[i];
-            const uint32_t pl = pw & 0x77777777u;
-            const uint32_t p4 = pw << 4;
-            w[r][2 * i] = iq4_lookup4(pl, pw, p4, 0xD9C8u);
-            w[r][2 * i + 1] = iq4_lookup4(pl >> 16, pw, p4, 0xFBEAu);
-          }
+        for (int i = 0; i < 4; i++) {
+          const uint32_t pw = qq[i];
+          const uint32_t pl = pw & 0x77777777u;
+          const uint32_t p4 = pw << 4;
+          w[r][2 * i] = iq4_lookup4(pl, pw, p4, 0xD9C8u);
+          w[r][2 * i + 1] = iq4_lookup4(pl >> 16, pw, p4, 0xFBEAu);
         }
       }
     }
-    const int pos = act_pos(kb, 0);
+    const uint8_t* ap = aq + a_off;
 #pragma unroll
     for (int t = 0; t < NT; t++) {
-      if (t < a.nt) {
-        const uint8_t* arow = a.q + t * a.stride;
-        const uint4 xa = *reinterpret_cast<const uint4*>(arow + pos);
-        const uint4 xb = *reinterpret_cast<const uint4*>(arow + pos + 128);
-        const float dx = a.d[t * a.blk + kb];
-        float dxs = 0.f;
-        if constexpr (F == QMV_Q4_K) dxs = a.ds[t * a.blk + kb];
+      const uint4 xa = *reinterpret_cast<const uint4*>(ap + t * ACT_BYTES);
+      const uint4 xb = *reinterpret_cast<const uint4*>(ap + t * ACT_BYTES + 128);
+      const float dx = ad[t * 32];
+      float dxs = 0.f;
+      if constexpr (F == QMV_Q4_K) dxs = ads[t * 32];
 #pragma unroll
-        for (int r = 0; r < RW; r++) {
-          // two independent chains (first / second half of the block)
-          int ia, ib;
-          if constexpr (F == QMV_Q4_K) {
-            ia = dp4a_us(w[r][0], xa.x, 0);
-            ib = dp4a_us(w[r][4], xb.x, 0);
-            ia = dp4a_us(w[r][1], xa.y, ia);
-            ib = dp4a_us(w[r][5], xb.y, ib);
-            ia = dp4a_us(w[r][2], xa.z, ia);
-            ib = dp4a_us(w[r][6], xb.z, ib);
-            ia = dp4a_us(w[r][3], xa.w, ia);
-            ib = dp4a_us(w[r][7], xb.w, ib);
-          } else {
-            ia = __dp4a((int)w[r][0], (int)xa.x, 0);
-            ib = __dp4a((int)w[r][4], (int)xb.x, 0);
-            ia = __dp4a((int)w[r][1], (int)xa.y, ia);
-            ib = __dp4a((int)w[r][5], (int)xb.y, ib);
-            ia = __dp4a((int)w[r][2], (int)xa.z, ia);
-            ib = __dp4a((int)w[r][6], (int)xb.z, ib);
-            ia = __dp4a((int)w[r][3], (int)xa.w, ia);
-            ib = __dp4a((int)w[r][7], (int)xb.w, ib);
-          }
-          const int is = (F == QMV_Q4_K) ? ia * 16 + ib : ia + ib;
-          float v = acc[r][t] + (sA[r] * dx) * (float)is;
-          if constexpr (F == QMV_Q4_K) v -= sB[r] * dxs;
-          acc[r][t] = v;
+      for (int r = 0; r < RW; r++) {
+        // two independent chains (first / second half of the block)
+        int ia, ib;
+        if constexpr (F == QMV_Q4_K) {
+          ia = dp4a_us(w[r][0], xa.x, 0);
+          ib = dp4a_us(w[r][4], xb.x, 0);
+          ia = dp4a_us(w[r][1], xa.y, ia);
+          ib = dp4a_us(w[r][5], xb.y, ib);
+          ia = dp4a_us(w[r][2], xa.z, ia);
+          ib = dp4a_us(w[r][6], xb.z, ib);
+          ia = dp4a_us(w[r][3], xa.w, ia);
+          ib = dp4a_us(w[r][7], xb.w, ib);
+        } else {
+          ia = __dp4a((int)w[r][0], (int)xa.x, 0);
+          ib = __dp4a((int)w[r][4], (int)xb.x, 0);
+          ia = __dp4a((int)w[r][1], (int)xa.y, ia);
+          ib = __dp4a((int)w[r][5], (int)xb.y, ib);
+          ia = __dp4a((int)w[r][2], (int)xa.z, ia);
+          ib = __dp4a((int)w[r][6], (int)xb.z, ib);
+          ia = __dp4a((int)w[r][3], (int)xa.w, ia);
+          ib = __dp4a((int)w[r][7], (int)xb.w, ib);
         }
+        const int is = (F == QMV_Q4_K) ? ia * 16 + ib : ia + ib;
+        float v = fmaf(sA[r] * dx, (float)is, acc[r][t]);
+        if constexpr (F == QMV_Q4_K) v = fmaf(-sB[r], dxs, v);
+        acc[r][t] = v;
       }
     }
   }
 };
+
+// Two CTAs fit on an SM for small token counts (so that consecutive calls
+// overlap under programmatic dependent launch); larger token counts keep more
+// accumulators in registers.
+template <int NT>
+constexpr int dense_min_blocks() {
+  return NT <= 4 ? 2 : 1;
+}
 
 // Sum of v over the 32 lanes, returned in every lane.
 __device__ __forceinline__ float warp_sum(float v) {

@@ -7,15 +7,18 @@
 // Machines", section "A single decode row is not a large matrix
 // multiplication": weight reads dominate).
 //
-// Structure (one persistent CTA per SM):
+// Structure (persistent CTAs):
 //   - the last warp (producer): one elected lane streams the CTA's weight
 //     tiles, TILE_ROWS rows x 1024 weights, with 2-D TMA loads into a ring of
-//     shared-memory stages guarded by full/empty mbarriers;
-//   - the consumer warps: quantize the activations of the K-range into shared
-//     memory (per-32 int8, the activation rule), then for every stage decode
-//     RW rows each in registers (one 32-weight block per lane), form exact
-//     int32 block dot products with dp4a, apply the block scales in fp32 and,
-//     at the end of a tile, reduce across lanes and store.
+//     shared-memory stages guarded by full/empty mbarriers.  The weights are
+//     read-only inputs, so streaming starts at once, before the preceding
+//     grid in the stream has finished (programmatic dependent launch);
+//   - the consumer warps: wait for the preceding grid, quantize the
+//     activations of the K-range into shared memory (per-32 int8, the
+//     activation rule), then for every stage decode RW rows each in registers
+//     (one 32-weight block per lane), form exact int32 block dot products with
+//     dp4a, apply the block scales in fp32 and, at the end of a tile, reduce
+//     across lanes and store.
 // Work split: the (split, 8-row unit) space is cut into contiguous,
 // equal-sized ranges, one per CTA; a tile never crosses a split.
 #pragma once
@@ -38,8 +41,7 @@ struct DenseParams {
   int groups;          // K / group weights
   int units;           // ceil(M / UNIT_ROWS)
   int stages;
-  int act_stride;      // bytes per token row of the activation area
-  int act_blk;         // blocks per token row of the scale areas (act_stride / 32)
+  int act_nck;         // chunks of the activation area
   unsigned* err;       // device error word
 };
 
@@ -74,7 +76,7 @@ __device__ __forceinline__ void split_range(const DenseParams& p, int s, int& g0
 }
 
 template <int F, int NT>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
     qmv_dense_kernel(const __grid_constant__ CUtensorMap map_tile, const __grid_constant__ CUtensorMap map_unit,
                      const DenseParams p) {
   constexpr int CB = chunk_bytes<F>();
@@ -82,14 +84,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int STAGE_BYTES = TILE_ROWS * CB;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stages = smem;
-  ActView a;
-  a.q = stages + p.stages * STAGE_BYTES;
-  a.d = reinterpret_cast<float*>(a.q + NT * p.act_stride);
-  a.ds = a.d + NT * p.act_blk;
-  a.nt = p.nt;
-  a.stride = p.act_stride;
-  a.blk = p.act_blk;
-  uint64_t* full = reinterpret_cast<uint64_t*>(a.ds + NT * p.act_blk);
+  ActArea a;
+  a.carve(stages + p.stages * STAGE_BYTES, F, NT, p.act_nck);
+  uint64_t* full = reinterpret_cast<uint64_t*>(stages + p.stages * STAGE_BYTES + act_area_bytes(F, NT, p.act_nck));
   uint64_t* empty = full + MAX_STAGES;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -102,7 +99,37 @@ __global__ void __launch_bounds__(THREADS, 1)
       prefetch_tensormap(&map_tile);
       prefetch_tensormap(&map_unit);
       const uint64_t pol = policy_evict_first();
-      pdl_wait();  // the weights may have been written by the preceding kernel
+      // A cursor PREFETCH_STAGES iterations ahead of the ring requests tiles
+      // into L2, so the CTA's weights keep streaming from HBM while the
+      // preceding grid finishes and while the consumers wait for it.
+      struct Cursor {
+        TileWalk w;
+        int s, u, nu, g0, g1, nck, c;
+        bool valid;
+        __device__ Cursor(const DenseParams& p) : w(p), c(0) { load(p); }
+        __device__ void load(const DenseParams& p) {
+          valid = w.next(s, u, nu);
+          if (valid) {
+            split_range(p, s, g0, g1);
+            nck = ((g1 - g0) * GW + KCHUNK - 1) / KCHUNK;
+          }
+          c = 0;
+        }
+        __device__ void advance(const DenseParams& p) {
+          if (++c == nck) load(p);
+        }
+      } pf(p);
+      long long pf_n = 0;
+      auto prefetch_to = [&](long long target) {
+        for (; pf.valid && pf_n < target; pf_n++, pf.advance(p)) {
+          if (pf_n < p.stages) continue;  // these go straight to shared memory
+          const int x = (pf.g0 * GB + pf.c * CB) / 8;
+          if (pf.nu == TILE_ROWS / UNIT_ROWS)
+            tma_prefetch_2d(&map_tile, x, pf.u * UNIT_ROWS);
+          else
+            for (int i = 0; i < pf.nu; i++) tma_prefetch_2d(&map_unit, x, (pf.u + i) * UNIT_ROWS);
+        }
+      };
       TileWalk walk(p);
       int s, u, nu;
       Ring ring;
@@ -112,6 +139,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         split_range(p, s, g0, g1);
         const int nck = ((g1 - g0) * GW + KCHUNK - 1) / KCHUNK;
         for (int c = 0; c < nck; c++, ring.advance(p.stages)) {
+          if (ring.n >= p.stages) prefetch_to(ring.n + PREFETCH_STAGES);
           if (!producer_acquire(empty, ring, p.stages, p.err)) {
             alive = false;
             break;
@@ -145,15 +173,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   int s, u, nu;
   Ring ring;
   int staged_split = -1;
+  const Consumer<F, NT> cons(lane);
   float acc[RW][NT];
 #pragma unroll
   for (int r = 0; r < RW; r++)
 #pragma unroll
     for (int t = 0; t < NT; t++) acc[r][t] = 0.f;
-  ActSource src{p.x, p.xq, p.xd, p.xs, p.K, nullptr, p.t0, nullptr, nullptr, nullptr};
-  int srow[RW];
-#pragma unroll
-  for (int r = 0; r < RW; r++) srow[r] = cw * RW + r;
+  const ActSource src{p.x, p.xq, p.xd, p.xs, p.K, nullptr, p.t0, nullptr, nullptr, nullptr};
 
   while (walk.next(s, u, nu)) {
     int g0, g1;
@@ -161,16 +187,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int kb0 = g0 * (GW / BLK), nblk = (g1 - g0) * (GW / BLK);
     if (s != staged_split) {
       named_sync(1, CONSUMER_THREADS);  // nobody still reads the previous range
-      stage_activations<F>(src, kb0, nblk, a, cw, lane);
+      stage_activations<F, NT>(src, kb0, nblk, p.nt, a, cw, lane);
       named_sync(1, CONSUMER_THREADS);
       staged_split = s;
     }
     const long long row0 = (long long)u * UNIT_ROWS;
     const int nrows = (int)min((long long)nu * UNIT_ROWS, p.M - row0);
-    unsigned rmask = 0;
-#pragma unroll
-    for (int r = 0; r < RW; r++)
-      if (srow[r] < nrows) rmask |= 1u << r;
     const int nck = (nblk * BLK + KCHUNK - 1) / KCHUNK;
     for (int c = 0; c < nck && alive; c++, ring.advance(p.stages)) {
       const int st = ring.st;
@@ -178,22 +200,29 @@ __global__ void __launch_bounds__(THREADS, 1)
         alive = false;
         break;
       }
-      const int kb = c * (KCHUNK / BLK) + lane;
-      if (rmask && kb < nblk) Consumer<F, NT>::chunk(stages + st * STAGE_BYTES, srow, rmask, lane, kb, a, acc);
+      if (cw * RW < nrows) {
+        const uint8_t* sb = stages + st * STAGE_BYTES + cw * RW * CB;
+        const uint8_t* rows[RW];
+#pragma unroll
+        for (int r = 0; r < RW; r++) rows[r] = sb + r * CB;
+        cons.chunk(rows, a.q + (size_t)c * NT * ACT_BYTES, a.d + c * NT * 32 + lane, a.ds + c * NT * 32 + lane,
+                   lane, acc);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
     alive = __all_sync(FULL, alive);
     if (!alive) continue;
-    // reduce across lanes and store rows row0 + srow[r]
+    // reduce across lanes and store rows row0 + cw * RW + r
     float* out = p.out + (long long)s * p.ntot * p.M;
 #pragma unroll
     for (int r = 0; r < RW; r++) {
 #pragma unroll
       for (int t = 0; t < NT; t++) {
         const float v = warp_sum(acc[r][t]);
-        if (lane == ((r * NT + t) & 31) && t < p.nt && ((rmask >> r) & 1u))
-          out[(long long)(p.t0 + t) * p.M + row0 + srow[r]] = v;
+        const int row = cw * RW + r;
+        if (lane == ((r * NT + t) & 31) && t < p.nt && row < nrows)
+          out[(long long)(p.t0 + t) * p.M + row0 + row] = v;
         acc[r][t] = 0.f;
       }
     }

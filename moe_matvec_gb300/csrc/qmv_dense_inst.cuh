@@ -15,6 +15,10 @@ static cudaError_t launch_dense_nt(const DenseLaunch& L) {
   if (dev < 64 && !((configured >> dev) & 1ull)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, device_smem_optin());
     if (e != cudaSuccess) return e;
+    // all of the unified L1/shared array as shared memory, so that two CTAs
+    // (of this call or of the next one) can be resident together
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
     configured |= 1ull << dev;
   }
   cudaLaunchConfig_t cfg;
