@@ -176,6 +176,30 @@ int qmv_splitk_run(int fmt, const void* W, const float* x, float* y, int64_t M,
                    int64_t K, int n_tok, int n_split, void* ws, size_t ws_bytes,
                    cudaStream_t stream);
 
+/* qmv_splitk_run for callers that cannot allocate device memory (the pages
+ * have no counterpart to this entry point; it exists for embedding).  Some
+ * callers may not call cudaMalloc: a plugin running while its host framework
+ * captures a CUDA graph (allocation is not allowed during capture), or a host
+ * that owns all device memory.  This variant takes no workspace: the partial
+ * sums go to a static device array of QMV_STATIC_SCRATCH_BYTES that the
+ * library holds on every GPU that loads it, until the process exits.
+ *   - Rejects split shapes whose partial sums exceed that size with
+ *     QMV_ERR_WORKSPACE (qmv_splitk_workspace_bytes(M, n_tok, n_split) must
+ *     be <= QMV_STATIC_SCRATCH_BYTES; n_split = 0 picks the split as
+ *     qmv_splitk_run does, n_split = 1 uses no scratch).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call shares the array: calls that can overlap on the GPU (other
+ *     streams, concurrently launched graphs) race.  Nothing needs clearing:
+ *     each call overwrites every partial sum it reads.
+ *   - Allocates nothing (no cudaMalloc / cudaFree, no allocating library).
+ * Results are bitwise equal to qmv_splitk_run with the same n_split. */
+#define QMV_STATIC_SCRATCH_BYTES (8u << 20)
+int qmv_splitk_run_static(int fmt, const void* W, const float* x, float* y,
+                          int64_t M, int64_t K, int n_tok, int n_split,
+                          cudaStream_t stream);
+
 /* Expert pool of one MoE FFN layer. */
 typedef struct moe_experts {
   int32_t n_experts;   /* E */

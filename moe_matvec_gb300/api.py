@@ -49,6 +49,7 @@ _SIGS = {
     "qmv_splitk_choose": (_int, [_int, _i64, _i64, _int]),
     "qmv_splitk_workspace_bytes": (_sz, [_i64, _int, _int]),
     "qmv_splitk_run": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _int, _int, _vp, _sz, _vp]),
+    "qmv_splitk_run_static": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _int, _int, _vp]),
     "moe_qmv_workspace_bytes": (_sz, [ctypes.POINTER(MoeExperts), _int, _int]),
     "moe_qmv_workspace_offsets": (_int, [ctypes.POINTER(MoeExperts), _int, _int, ctypes.POINTER(_sz * 5)]),
     "moe_qmv_run": (_int, [ctypes.POINTER(MoeExperts), _vp, _vp, _vp, _vp, _int, _int, _vp, _sz, _vp]),
@@ -173,6 +174,21 @@ def splitk_run(fmt: int, W: torch.Tensor, x: torch.Tensor, M: int, K: int, n_spl
     wsb = ws.numel() * ws.element_size() if ws is not None else 0
     _check(load().qmv_splitk_run(int(fmt), _ptr(W), _ptr(x), _ptr(out), M, K, n, n_split, _ptr(ws), wsb,
                                  _stream(stream)), "qmv_splitk_run")
+    return out
+
+
+STATIC_SCRATCH_BYTES = 8 << 20
+
+
+def splitk_run_static(fmt: int, W: torch.Tensor, x: torch.Tensor, M: int, K: int, n_split: int = 0,
+                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Split-K matvec for callers that cannot allocate: the partial sums use
+    the library's static device array (see qmv_splitk_run_static)."""
+    n = x.shape[0]
+    if out is None:
+        out = torch.empty((n, M), dtype=torch.float32, device=x.device)
+    _check(load().qmv_splitk_run_static(int(fmt), _ptr(W), _ptr(x), _ptr(out), M, K, n, n_split, _stream(stream)),
+           "qmv_splitk_run_static")
     return out
 
 
