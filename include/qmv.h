@@ -241,6 +241,14 @@ int moe_qmv_run(const moe_experts* e, const int32_t* ids, const float* gates,
                 const float* x, float* y, int n_tok, int top_k, void* ws,
                 size_t ws_bytes, cudaStream_t stream);
 
+/* Diagnostic (no counterpart on the pages): the activation quantizer uses
+ * branch-free FMA sequences for d = amax / 127 and 1 / d; this compares them
+ * with the IEEE round-to-nearest division and reciprocal on every
+ * non-negative float of their ranges and ADDS the mismatch counts to
+ * mismatches[0] (division) and mismatches[1] (reciprocal), device memory,
+ * 16-byte aligned.  Both must stay 0. */
+int qmv_check_rounding(unsigned long long* mismatches, cudaStream_t stream);
+
 /* Synchronises `stream`, then reads and clears the device error word
  * (QMV_DEVERR_* bits, 0 if none) into *err. */
 int qmv_get_device_error(cudaStream_t stream, int* err);

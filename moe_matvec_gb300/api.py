@@ -54,6 +54,7 @@ _SIGS = {
     "moe_qmv_workspace_offsets": (_int, [ctypes.POINTER(MoeExperts), _int, _int, ctypes.POINTER(_sz * 5)]),
     "moe_qmv_run": (_int, [ctypes.POINTER(MoeExperts), _vp, _vp, _vp, _vp, _int, _int, _vp, _sz, _vp]),
     "qmv_get_device_error": (_int, [_vp, ctypes.POINTER(_int)]),
+    "qmv_check_rounding": (_int, [_vp, _vp]),
     "qmv_strerror": (ctypes.c_char_p, [_int]),
 }
 
@@ -219,6 +220,14 @@ def moe_run(e: MoeExperts, ids: torch.Tensor, gates: torch.Tensor, x: torch.Tens
     _check(load().moe_qmv_run(ctypes.byref(e), _ptr(ids), _ptr(gates), _ptr(x), _ptr(out), n, top_k, _ptr(ws),
                               ws.numel(), _stream(stream)), "moe_qmv_run")
     return out
+
+
+def check_rounding(stream=None):
+    """Mismatch counts (division, reciprocal) of the quantizer's branch-free
+    arithmetic against IEEE round-to-nearest over every input of its range."""
+    bad = torch.zeros(2, dtype=torch.int64, device="cuda")
+    _check(load().qmv_check_rounding(_ptr(bad), _stream(stream)), "qmv_check_rounding")
+    return [int(v) for v in bad.cpu()]
 
 
 def get_device_error(stream=None) -> int:

@@ -135,6 +135,34 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 
 // ---------------------------------------------------------------------------
+// Branch-free correctly rounded a / 127 and 1 / d for the activation rule.
+// The IEEE division / reciprocal of the toolkit carry a branch to a slow path
+// for special operands, which keeps independent quantizations from being
+// interleaved.  Both functions below use the FMA-based correction of a
+// quotient or reciprocal (Newton-Raphson with an exact FMA residual, as in
+// P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990) and are equal to the
+// IEEE round-to-nearest results on their stated ranges; tests compare them
+// exhaustively against __fdiv_rn / __frcp_rn (qmv_check_rounding).
+// ---------------------------------------------------------------------------
+// RN(a / 127) for 0 <= a <= FLT_MAX with a / 127 >= 2^-126 or a == 0.
+__device__ __forceinline__ float div127_rn(float a) {
+  const float c = 0.007874015718698502f;  // RN(1 / 127)
+  const float q0 = __fmul_rn(a, c);
+  const float r = __fmaf_rn(-q0, 127.0f, a);  // exact residual
+  return __fmaf_rn(r, c, q0);
+}
+// RN(1 / d) for 2^-126 <= d <= 2^126.
+__device__ __forceinline__ float rcp_rn(float d) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(d));
+  float e = __fmaf_rn(-d, y, 1.0f);
+  y = __fmaf_rn(y, e, y);
+  e = __fmaf_rn(-d, y, 1.0f);
+  return __fmaf_rn(y, e, y);
+}
+
+// ---------------------------------------------------------------------------
 // Loads that bypass L1 for data read once.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float ldg_stream(const float* p) {

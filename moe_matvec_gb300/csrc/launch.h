@@ -51,6 +51,7 @@ cudaError_t launch_act_quant(const float* x, int K, int n_tok, int8_t* q, float*
 cudaError_t launch_splitk_reduce(const float* partial, float* y, long long M, int n_tok, int n_split,
                                  cudaStream_t stream, bool pdl);
 cudaError_t launch_quantize_weights(int fmt, const float* w, long long M, int K, void* W, cudaStream_t stream);
+cudaError_t launch_check_rounding(unsigned long long* bad, cudaStream_t stream);
 
 // Maximum dynamic shared memory a CTA may use on the current device.
 int device_smem_optin();

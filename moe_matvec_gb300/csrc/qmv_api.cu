@@ -459,6 +459,14 @@ int moe_qmv_run(const moe_experts* e, const int32_t* ids, const float* gates, co
              : QMV_ERR_CUDA;
 }
 
+int qmv_check_rounding(unsigned long long* mismatches, cudaStream_t stream) {
+  if (!mismatches) return QMV_ERR_NULL;
+  if (!aligned16(mismatches)) return QMV_ERR_ALIGN;
+  int rc = check_device();
+  if (rc) return rc;
+  return launch_check_rounding(mismatches, stream) == cudaSuccess ? QMV_OK : QMV_ERR_CUDA;
+}
+
 int qmv_get_device_error(cudaStream_t stream, int* err) {
   if (!err) return QMV_ERR_NULL;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return QMV_ERR_CUDA;

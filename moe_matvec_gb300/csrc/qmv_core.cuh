@@ -56,54 +56,6 @@ struct ActArea {
   }
 };
 
-// Quantize four consecutive elements of a 32-block spread over 8 lanes
-// (lanes 8g..8g+7 hold block g of the warp); returns the packed int8 codes of
-// this lane, the block scale d and the block sum s (identical in the 8 lanes).
-struct Quad {
-  uint32_t q;
-  float d;
-  int s;
-};
-__device__ __forceinline__ Quad quant_quad(float4 v) {
-  float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-  m = fmaxf(m, __shfl_xor_sync(FULL, m, 1));
-  m = fmaxf(m, __shfl_xor_sync(FULL, m, 2));
-  m = fmaxf(m, __shfl_xor_sync(FULL, m, 4));
-  float d = __fdiv_rn(m, 127.0f);
-  float id = d > 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
-  int q0 = max(-127, min(127, __float2int_rn(__fmul_rn(v.x, id))));
-  int q1 = max(-127, min(127, __float2int_rn(__fmul_rn(v.y, id))));
-  int q2 = max(-127, min(127, __float2int_rn(__fmul_rn(v.z, id))));
-  int q3 = max(-127, min(127, __float2int_rn(__fmul_rn(v.w, id))));
-  int s = q0 + q1 + q2 + q3;
-  s += __shfl_xor_sync(FULL, s, 1);
-  s += __shfl_xor_sync(FULL, s, 2);
-  s += __shfl_xor_sync(FULL, s, 4);
-  uint32_t packed = (uint32_t)(q0 & 0xFF) | ((uint32_t)(q1 & 0xFF) << 8) | ((uint32_t)(q2 & 0xFF) << 16) |
-                    ((uint32_t)(q3 & 0xFF) << 24);
-  return {packed, d, s};
-}
-
-// Store the packed codes of elements 4*li..4*li+3 of block l (li = lane & 7)
-// into a token's chunk of codes in the byte order format F consumes.  For
-// IQ4_XS a block is stored interleaved (byte 2i = x_i, byte 2i+1 = x_{i+16}),
-// the order in which its codebook lookups come out; the other formats use the
-// natural order.  Must be called by all 32 lanes (it shuffles).
-template <int F>
-__device__ __forceinline__ void store_act_quad(uint8_t* chunk, int l, int li, uint32_t packed) {
-  if constexpr (F == QMV_IQ4_XS) {
-    uint32_t hi = __shfl_xor_sync(FULL, packed, 4);  // elements 16 + 4*li ..
-    if (li < 4) {
-      uint2 w;
-      w.x = __byte_perm(packed, hi, 0x5140);
-      w.y = __byte_perm(packed, hi, 0x7362);
-      *reinterpret_cast<uint2*>(chunk + act_pos(l, 8 * li)) = w;
-    }
-  } else {
-    *reinterpret_cast<uint32_t*>(chunk + act_pos(l, 4 * li)) = packed;
-  }
-}
-
 // Where the activation rows come from: fp32 rows (quantized while staging)
 // or pre-quantized rows; token slot t reads source row rows[t] (a
 // shared-memory list) or row0 + t.  When wq is set, the quantized codes,
@@ -123,69 +75,168 @@ struct ActSource {
   __device__ __forceinline__ long long row(int t) const { return rows ? (long long)rows[t] : row0 + t; }
 };
 
+// Quantize one 32-element block held entirely by this lane (activation rule:
+// amax, d = amax / 127, id = 1 / d, q = rne(x * id) in [-127, 127],
+// s = sum q) and pack the codes four per word, natural order.
+struct BlockQ {
+  uint32_t w[8];
+  float d;
+  int s;
+};
+__device__ __forceinline__ BlockQ quant_block(const float4 (&v)[8]) {
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; i++) m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+  BlockQ r;
+  r.d = __fdiv_rn(m, 127.0f);
+  const float id = r.d > 0.0f ? __frcp_rn(r.d) : 0.0f;  // correctly rounded 1 / d
+  // With a normal d, |x * id| <= amax * id < 127.5, so no code needs the
+  // clamp; it only matters for blocks with amax below about 2^-100.
+  const bool tiny = m < 0x1p-100f;
+  int s = 0;
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    float f[4] = {__fmul_rn(v[i].x, id), __fmul_rn(v[i].y, id), __fmul_rn(v[i].z, id), __fmul_rn(v[i].w, id)};
+    if (tiny) {
+#pragma unroll
+      for (int k = 0; k < 4; k++) f[k] = fminf(fmaxf(f[k], -127.0f), 127.0f);
+    }
+    const int q0 = __float2int_rn(f[0]), q1 = __float2int_rn(f[1]), q2 = __float2int_rn(f[2]),
+              q3 = __float2int_rn(f[3]);
+    r.w[i] = (uint32_t)(q0 & 0xFF) | ((uint32_t)(q1 & 0xFF) << 8) | ((uint32_t)(q2 & 0xFF) << 16) |
+             ((uint32_t)q3 << 24);
+    s = __dp4a((int)r.w[i], 0x01010101, s);
+  }
+  r.s = s;
+  return r;
+}
+
 // Stage blocks [kb0, kb0 + nblk) of tokens [0, nt) of `src` into the area
 // (NT slots, ceil(nblk / 32) chunks), zero-filling the padding.  Called by all
-// consumer warps; each warp handles 16 blocks per step (8 lanes per block,
-// 4 elements per lane) with all of the step's loads issued before any use.
+// consumer warps.  Four lanes share a block (8 elements each: a load
+// instruction of the warp touches 8 blocks, two shuffle steps combine the
+// maximum and the sum); a warp step covers SU units of 8 blocks with all of
+// its loads issued first and no branch inside a unit, so the units overlap.
 template <int F, int NT>
 __device__ __forceinline__ void stage_activations(const ActSource& src, int kb0, int nblk, int nt, const ActArea& a,
                                                   int cw, int lane) {
-  const int sub = lane >> 3, li = lane & 7;
+  constexpr int SU = 4;
+  const int sub = lane >> 2, li = lane & 3;
   const int nck = (nblk + 31) / 32;
-  const int total = nck * NT * 32;
-  for (int base = cw * 16; base < total; base += CONSUMER_WARPS * 16) {
-    int ct[4], l[4];
-    bool real[4];
-    long long gblk[4];
-    float4 v[4];
-    uint32_t pk[4];
-    float dd[4];
-    int ss[4];
+  const int total = nck * NT * 32;  // a multiple of 32 = blocks of one warp step
+  for (int base = cw * 8 * SU; base < total; base += CONSUMER_WARPS * 8 * SU) {
+    int ct[SU], l[SU];
+    long long gblk[SU];
+    bool real[SU];
+    uint32_t w0[SU], w1[SU];
+    float dd[SU];
+    int ss[SU];
+    float4 v[SU][2];
 #pragma unroll
-    for (int u = 0; u < 4; u++) {
-      const int idx = base + 4 * u + sub;
+    for (int u = 0; u < SU; u++) {
+      const int idx = base + 8 * u + sub;
       l[u] = idx & 31;
       ct[u] = idx >> 5;
       const int t = ct[u] & (NT - 1), c = ct[u] / NT;
       const int b = c * 32 + l[u];
-      real[u] = idx < total && t < nt && b < nblk;
+      real[u] = t < nt && b < nblk;
       gblk[u] = real[u] ? src.row(t) * (src.ld / 32) + kb0 + b : 0;
-      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      pk[u] = 0;
+      v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      w0[u] = w1[u] = 0u;
       dd[u] = 0.f;
       ss[u] = 0;
       if (real[u]) {
         if (src.x != nullptr) {
-          v[u] = __ldg(reinterpret_cast<const float4*>(src.x + gblk[u] * 32) + li);
+          const float4* p = reinterpret_cast<const float4*>(src.x + gblk[u] * 32) + 2 * li;
+          v[u][0] = __ldg(p);
+          v[u][1] = __ldg(p + 1);
         } else {
-          pk[u] = __ldg(reinterpret_cast<const uint32_t*>(src.xq + gblk[u] * 32) + li);
+          const uint2 q = __ldg(reinterpret_cast<const uint2*>(src.xq + gblk[u] * 32) + li);
+          w0[u] = q.x;
+          w1[u] = q.y;
           dd[u] = __ldg(src.xd + gblk[u]);
           ss[u] = __ldg(src.xs + gblk[u]);
         }
       }
     }
+    if (src.x != nullptr) {
+      float m[SU];
 #pragma unroll
-    for (int u = 0; u < 4; u++) {
-      if (src.x != nullptr) {
-        const Quad qd = quant_quad(v[u]);
-        pk[u] = qd.q;
-        dd[u] = qd.d;
-        ss[u] = qd.s;
+      for (int u = 0; u < SU; u++) {
+        m[u] = fmaxf(fmaxf(fmaxf(fabsf(v[u][0].x), fabsf(v[u][0].y)), fmaxf(fabsf(v[u][0].z), fabsf(v[u][0].w))),
+                     fmaxf(fmaxf(fabsf(v[u][1].x), fabsf(v[u][1].y)), fmaxf(fabsf(v[u][1].z), fabsf(v[u][1].w))));
+        m[u] = fmaxf(m[u], __shfl_xor_sync(FULL, m[u], 1));
+        m[u] = fmaxf(m[u], __shfl_xor_sync(FULL, m[u], 2));
+      }
+      // Fast path: every block of the step has amax == 0 or amax >= 2^-100,
+      // where the branch-free sequences are exact and no code needs clamping
+      // (|x * id| <= amax * id < 127.5).  Otherwise the whole warp takes the
+      // IEEE operations with the clamp.
+      bool slow = false;
+#pragma unroll
+      for (int u = 0; u < SU; u++) slow |= m[u] > 0.0f && m[u] < 0x1p-100f;
+      slow = __any_sync(FULL, slow);
+      float id[SU];
+      if (!slow) {
+#pragma unroll
+        for (int u = 0; u < SU; u++) {
+          dd[u] = div127_rn(m[u]);
+          id[u] = m[u] > 0.0f ? rcp_rn(fmaxf(dd[u], 0x1p-126f)) : 0.0f;
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < SU; u++) {
+          dd[u] = __fdiv_rn(m[u], 127.0f);
+          id[u] = dd[u] > 0.0f ? __frcp_rn(dd[u]) : 0.0f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < SU; u++) {
+        float f[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
+        int q[8];
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+          float p = __fmul_rn(f[k], id[u]);
+          if (slow) p = fminf(fmaxf(p, -127.0f), 127.0f);
+          q[k] = __float2int_rn(p);
+        }
+        w0[u] = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) | ((uint32_t)(q[2] & 0xFF) << 16) |
+                ((uint32_t)q[3] << 24);
+        w1[u] = (uint32_t)(q[4] & 0xFF) | ((uint32_t)(q[5] & 0xFF) << 8) | ((uint32_t)(q[6] & 0xFF) << 16) |
+                ((uint32_t)q[7] << 24);
+        int s = __dp4a((int)w1[u], 0x01010101, __dp4a((int)w0[u], 0x01010101, 0));
+        s += __shfl_xor_sync(FULL, s, 1);
+        s += __shfl_xor_sync(FULL, s, 2);
+        ss[u] = s;
         if (src.wq != nullptr && real[u]) {
-          reinterpret_cast<uint32_t*>(src.wq + gblk[u] * 32)[li] = pk[u];
+          reinterpret_cast<uint2*>(src.wq + gblk[u] * 32)[li] = make_uint2(w0[u], w1[u]);
           if (li == 0) {
             src.wd[gblk[u]] = dd[u];
-            src.ws[gblk[u]] = ss[u];
+            src.ws[gblk[u]] = s;
           }
         }
       }
-      // total is a multiple of 32 and a step covers 16 aligned blocks, so this
-      // test is the same in every lane (store_act_quad shuffles)
-      if (base + 4 * u < total) {
-        store_act_quad<F>(a.q + (size_t)ct[u] * ACT_BYTES, l[u], li, pk[u]);
-        if (li == 0) {
+    }
+#pragma unroll
+    for (int u = 0; u < SU; u++) {
+      uint8_t* chunk = a.q + (size_t)ct[u] * ACT_BYTES;
+      if constexpr (F == QMV_IQ4_XS) {
+        // interleaved: byte 2i = x_i, byte 2i+1 = x_{i+16}; lanes 0, 1 of the
+        // block take the elements 16.. of lanes 2, 3
+        const uint32_t h0 = __shfl_xor_sync(FULL, w0[u], 2), h1 = __shfl_xor_sync(FULL, w1[u], 2);
+        if (li < 2)
+          *reinterpret_cast<uint4*>(chunk + act_pos(l[u], 16 * li)) =
+              make_uint4(__byte_perm(w0[u], h0, 0x5140), __byte_perm(w0[u], h0, 0x7362),
+                         __byte_perm(w1[u], h1, 0x5140), __byte_perm(w1[u], h1, 0x7362));
+      } else {
+        *reinterpret_cast<uint2*>(chunk + act_pos(l[u], 8 * li)) = make_uint2(w0[u], w1[u]);
+      }
+      if (li == 0) {
+        if constexpr (F == QMV_Q4_K) {
+          a.d[ct[u] * 32 + l[u]] = dd[u] * 0.0625f;  // the consumer's isum is 16 x the block sum
+          a.ds[ct[u] * 32 + l[u]] = dd[u] * (float)ss[u];
+        } else {
           a.d[ct[u] * 32 + l[u]] = dd[u];
-          if constexpr (F == QMV_Q4_K) a.ds[ct[u] * 32 + l[u]] = dd[u] * (float)ss[u];
         }
       }
     }
@@ -269,24 +320,26 @@ struct Consumer {
         sA[r] = __half2float(*reinterpret_cast<const __half*>(row + h_off));
         sB[r] = 0.f;
       } else if constexpr (F == QMV_Q4_K) {
-        const uint4 h = *reinterpret_cast<const uint4*>(row + h_off);
+        // d | dmin, and the two header words holding the lane's 12-bit
+        // (sc | m << 6) field (for the last fields the second word is the
+        // first payload word; only bits of the first word are used then)
+        const __half2 dh = *reinterpret_cast<const __half2*>(row + h_off);
+        const uint32_t f0 = *reinterpret_cast<const uint32_t*>(row + h_off + 4 + 4 * fsel);
+        const uint32_t f1 = *reinterpret_cast<const uint32_t*>(row + h_off + 8 + 4 * fsel);
         const uint4 q = *reinterpret_cast<const uint4*>(row + w_off);
         const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
         // low nibbles as bytes; high nibbles left in place (16 x code) for an
-        // unsigned-byte dp4a: isum = 16 * sum_lo + sum_hi16, and the 1/16 is
-        // folded into the scale (exact: a power of two)
+        // unsigned-byte dp4a: isum = 16 * sum_lo + sum_hi16; the staged d_x of
+        // Q4_K carries the 1/16 (exact: a power of two)
 #pragma unroll
         for (int i = 0; i < 4; i++) {
           w[r][i] = qq[i] & 0x0F0F0F0Fu;
           w[r][4 + i] = qq[i] & 0xF0F0F0F0u;
         }
-        const uint32_t wa = fsel == 0 ? h.y : (fsel == 1 ? h.z : h.w);
-        const uint32_t wb = fsel == 0 ? h.z : (fsel == 1 ? h.w : 0u);
-        const uint32_t f = __funnelshift_r(wa, wb, fsh);
-        const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xFFFF)));
-        const float dmin = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
-        sA[r] = d * (0.0625f * (float)(f & 63u));
-        sB[r] = dmin * (float)((f >> 6) & 63u);
+        const uint32_t f = __funnelshift_r(f0, f1, fsh);
+        const float2 dd = __half22float2(dh);
+        sA[r] = dd.x * (float)(f & 63u);
+        sB[r] = dd.y * (float)((f >> 6) & 63u);
       } else {
         const uint2 meta = *reinterpret_cast<const uint2*>(row + h_off);
         const uint4 q = *reinterpret_cast<const uint4*>(row + w_off);

@@ -6,31 +6,24 @@
 namespace qmv {
 
 // Activation rule over x [n_tok][K]: codes in natural order, per-32 scale d
-// and code sum s.  Each warp handles 4 blocks per step, 8 lanes per block,
-// 4 elements per lane.
+// and code sum s; one block per thread.
 __global__ void __launch_bounds__(256) act_quant_kernel(const float* __restrict__ x, int K, int n_tok,
                                                         int8_t* __restrict__ q, float* __restrict__ d,
                                                         int32_t* __restrict__ s) {
   pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int sub = lane >> 3, li = lane & 7;
-  const long long nblk = (long long)K / 32;
-  const long long total = nblk * n_tok;
-  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-  long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  for (long long base = wid * 4; base < total; base += warps * 4) {
-    const long long idx = base + sub;
-    const bool ok = idx < total;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (ok) v = __ldg(reinterpret_cast<const float4*>(x + idx * 32) + li);
-    Quad qd = quant_quad(v);
-    if (ok) {
-      reinterpret_cast<uint32_t*>(q + idx * 32)[li] = qd.q;
-      if (li == 0) {
-        d[idx] = qd.d;
-        s[idx] = qd.s;
-      }
-    }
+  const long long total = (long long)K / 32 * n_tok;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    float4 v[8];
+    const float4* p = reinterpret_cast<const float4*>(x + i * 32);
+#pragma unroll
+    for (int k = 0; k < 8; k++) v[k] = __ldg(p + k);
+    const BlockQ b = quant_block(v);
+    uint4* o = reinterpret_cast<uint4*>(q + i * 32);
+    o[0] = make_uint4(b.w[0], b.w[1], b.w[2], b.w[3]);
+    o[1] = make_uint4(b.w[4], b.w[5], b.w[6], b.w[7]);
+    d[i] = b.d;
+    s[i] = b.s;
   }
   pdl_launch_dependents();
 }
@@ -92,6 +85,28 @@ cudaError_t launch_moe_combine(const int32_t* ids, const float* gates, const flo
   return cudaLaunchKernelEx(&cfg, moe_combine_kernel, ids, gates, o, y, n_tok, top_k, n_experts, hidden);
 }
 
+// Every non-negative float against the IEEE operations: [0] counts inputs
+// where div127_rn differs from __fdiv_rn(a, 127) (a == 0 or a / 127 normal),
+// [1] inputs where rcp_rn differs from __frcp_rn (2^-126 <= d <= 2^126).
+__global__ void __launch_bounds__(256) check_rounding_kernel(unsigned long long* bad) {
+  unsigned long long nd = 0, nr = 0;
+  const unsigned stride = gridDim.x * blockDim.x;
+  for (unsigned u = blockIdx.x * blockDim.x + threadIdx.x; u <= 0x7F7FFFFFu; u += stride) {
+    const float a = __uint_as_float(u);
+    if (a == 0.0f || a >= 127.0f * 0x1p-126f)
+      nd += __float_as_uint(div127_rn(a)) != __float_as_uint(__fdiv_rn(a, 127.0f));
+    if (a >= 0x1p-126f && a <= 0x1p126f) nr += __float_as_uint(rcp_rn(a)) != __float_as_uint(__frcp_rn(a));
+    if (u > 0x7F7FFFFFu - stride) break;  // the next step would wrap past FLT_MAX
+  }
+  if (nd) atomicAdd(&bad[0], nd);
+  if (nr) atomicAdd(&bad[1], nr);
+}
+
+cudaError_t launch_check_rounding(unsigned long long* bad, cudaStream_t stream) {
+  check_rounding_kernel<<<8 * device_sm_count(), 256, 0, stream>>>(bad);
+  return cudaGetLastError();
+}
+
 void make_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, dim3 grid, dim3 block, size_t smem,
                  cudaStream_t stream, bool pdl) {
   cfg = cudaLaunchConfig_t{};
@@ -108,8 +123,8 @@ void make_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, dim3 grid, 
 cudaError_t launch_act_quant(const float* x, int K, int n_tok, int8_t* q, float* d, int32_t* s,
                              cudaStream_t stream, bool pdl) {
   const long long blocks = (long long)K / 32 * n_tok;
-  long long ctas = (blocks + 31) / 32;  // 8 warps x 4 blocks per CTA step
-  const long long cap = 4ll * device_sm_count();
+  long long ctas = (blocks + 255) / 256;  // one block per thread
+  const long long cap = 8ll * device_sm_count();
   if (ctas > cap) ctas = cap;
   if (ctas < 1) ctas = 1;
   cudaLaunchConfig_t cfg;

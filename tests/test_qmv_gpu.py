@@ -32,6 +32,27 @@ def _tricky_activations(n, K, seed):
     return x
 
 
+def test_branch_free_rounding_is_ieee_on_every_input(lib):
+    # the staging's a / 127 and 1 / d against div.rn / rcp.rn, all 2^31 inputs
+    assert lib.check_rounding() == [0, 0]
+
+
+@pytest.mark.parametrize("fmt,n,K", [(f, n, K) for f in (0, 1, 2) for n, K in ((1, 1024), (5, 2048), (16, 4096))])
+def test_fused_staging_matches_standalone_quantizer(lib, fmt, n, K):
+    # the in-kernel quantization of x must produce exactly the codes and scales
+    # of the standalone quantizer (itself bit-exact against the oracle): the
+    # two paths then run the same arithmetic and agree bit for bit
+    M = 96
+    x = _tricky_activations(n, K, seed=n + K + fmt)
+    x[n // 2, 256:288] *= 1e-38          # blocks far below 2^-100 take the exact slow path
+    Wd = dev(oracle.quantize(fmt, synth.weights(40 + fmt, M, K)))
+    xd = dev(x)
+    q, d, s = lib.quantize_act(xd)
+    rq, rd, rs = oracle.act_quant(x)
+    assert np.array_equal(q.cpu().numpy(), rq) and np.array_equal(s.cpu().numpy(), rs)
+    assert torch.equal(lib.run(fmt, Wd, xd, M, K), lib.run_q8(fmt, Wd, q, d, s, M, K))
+
+
 @pytest.mark.parametrize("n,K", [(1, 256), (3, 4096), (16, 5120), (64, 2048)])
 def test_act_quant_bit_exact(lib, n, K):
     x = _tricky_activations(n, K, seed=n + K)
