@@ -75,13 +75,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that may suspend the thread (up to `ns` nanoseconds) until the
+// phase completes, instead of returning at once: a waiting warp then takes
+// no issue slots from the warps that compute.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait: gives up after ~2^31 SM cycles (about a second), sets the
 // timeout bit and returns false.  No wait in this library is unbounded.
 constexpr long long WAIT_CYCLES = 1ll << 31;
+constexpr uint32_t WAIT_SUSPEND_NS = 1u << 20;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
   if (mbar_try_wait(bar, parity)) return true;
   long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_suspend(bar, parity, WAIT_SUSPEND_NS)) {
     if (clock64() - t0 > WAIT_CYCLES) {
       set_error(err, QMV_DEVERR_TIMEOUT);
       return false;

@@ -39,6 +39,14 @@ __device__ __forceinline__ int act_pos(int l, int p) {
   return (l >> 3) * 256 + (p >> 4) * 128 + (l & 7) * 16 + (p & 15);
 }
 
+// Position of the scale of block l, token slot t within a chunk's NT * 32
+// scales: with two or more slots the slots go in pairs (t, t + 1)
+// interleaved, so that a lane loads the scales of a token pair at once.
+template <int NT>
+__device__ __forceinline__ int act_dpos(int t, int l) {
+  return NT == 1 ? l : (t & ~1) * 32 + 2 * l + (t & 1);
+}
+
 // Bytes of the activation area for nt_slots token slots and nck chunks.
 __host__ __device__ constexpr size_t act_area_bytes(int F, int nt_slots, int nck) {
   return (size_t)nck * nt_slots * (ACT_BYTES + 32 * sizeof(float) * (F == QMV_Q4_K ? 2 : 1));
@@ -232,11 +240,13 @@ __device__ __forceinline__ void stage_activations(const ActSource& src, int kb0,
         *reinterpret_cast<uint2*>(chunk + act_pos(l[u], 8 * li)) = make_uint2(w0[u], w1[u]);
       }
       if (li == 0) {
+        const int t = ct[u] & (NT - 1);
+        const int di = (ct[u] - t) * 32 + act_dpos<NT>(t, l[u]);
         if constexpr (F == QMV_Q4_K) {
-          a.d[ct[u] * 32 + l[u]] = dd[u] * 0.0625f;  // the consumer's isum is 16 x the block sum
-          a.ds[ct[u] * 32 + l[u]] = dd[u] * (float)ss[u];
+          a.d[di] = dd[u] * 0.0625f;  // the consumer's isum is 16 x the block sum
+          a.ds[di] = dd[u] * (float)ss[u];
         } else {
-          a.d[ct[u] * 32 + l[u]] = dd[u];
+          a.d[di] = dd[u];
         }
       }
     }
@@ -302,6 +312,9 @@ struct Consumer {
     fsh = (12 * (lane & 7)) & 31;
   }
 
+  // Q4_K with 4 or more tokens: both nibble halves as 16 x code, one chain.
+  static constexpr bool Q4K_LO16 = NT >= 4;
+
   // rows[r]: start of row r's chunk in the stage; aq / ad / ads: this chunk's
   // activation codes / scales / scale-sums (token slot 0).
   __device__ __forceinline__ void chunk(const uint8_t* const (&rows)[RW], const uint8_t* aq, const float* ad,
@@ -328,12 +341,13 @@ struct Consumer {
         const uint32_t f1 = *reinterpret_cast<const uint32_t*>(row + h_off + 8 + 4 * fsel);
         const uint4 q = *reinterpret_cast<const uint4*>(row + w_off);
         const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
-        // low nibbles as bytes; high nibbles left in place (16 x code) for an
-        // unsigned-byte dp4a: isum = 16 * sum_lo + sum_hi16; the staged d_x of
-        // Q4_K carries the 1/16 (exact: a power of two)
+        // high nibbles left in place (16 x code) for an unsigned-byte dp4a;
+        // low nibbles as bytes (the dot product scales their sum by 16) or,
+        // for one dp4a chain, shifted up to 16 x code as well.  The staged d_x
+        // of Q4_K carries the 1/16 (exact: a power of two).
 #pragma unroll
         for (int i = 0; i < 4; i++) {
-          w[r][i] = qq[i] & 0x0F0F0F0Fu;
+          w[r][i] = Q4K_LO16 ? (qq[i] << 4) & 0xF0F0F0F0u : qq[i] & 0x0F0F0F0Fu;
           w[r][4 + i] = qq[i] & 0xF0F0F0F0u;
         }
         const uint32_t f = __funnelshift_r(f0, f1, fsh);
@@ -360,41 +374,88 @@ struct Consumer {
       }
     }
     const uint8_t* ap = aq + a_off;
-#pragma unroll
-    for (int t = 0; t < NT; t++) {
-      const uint4 xa = *reinterpret_cast<const uint4*>(ap + t * ACT_BYTES);
-      const uint4 xb = *reinterpret_cast<const uint4*>(ap + t * ACT_BYTES + 128);
-      const float dx = ad[t * 32];
+    if constexpr (NT == 1) {
+      const uint4 xa = *reinterpret_cast<const uint4*>(ap);
+      const uint4 xb = *reinterpret_cast<const uint4*>(ap + 128);
+      const float dx = ad[lane];
       float dxs = 0.f;
-      if constexpr (F == QMV_Q4_K) dxs = ads[t * 32];
+      if constexpr (F == QMV_Q4_K) dxs = ads[lane];
 #pragma unroll
       for (int r = 0; r < RW; r++) {
-        // two independent chains (first / second half of the block)
-        int ia, ib;
-        if constexpr (F == QMV_Q4_K) {
-          ia = dp4a_us(w[r][0], xa.x, 0);
-          ib = dp4a_us(w[r][4], xb.x, 0);
-          ia = dp4a_us(w[r][1], xa.y, ia);
-          ib = dp4a_us(w[r][5], xb.y, ib);
-          ia = dp4a_us(w[r][2], xa.z, ia);
-          ib = dp4a_us(w[r][6], xb.z, ib);
-          ia = dp4a_us(w[r][3], xa.w, ia);
-          ib = dp4a_us(w[r][7], xb.w, ib);
-        } else {
-          ia = __dp4a((int)w[r][0], (int)xa.x, 0);
-          ib = __dp4a((int)w[r][4], (int)xb.x, 0);
-          ia = __dp4a((int)w[r][1], (int)xa.y, ia);
-          ib = __dp4a((int)w[r][5], (int)xb.y, ib);
-          ia = __dp4a((int)w[r][2], (int)xa.z, ia);
-          ib = __dp4a((int)w[r][6], (int)xb.z, ib);
-          ia = __dp4a((int)w[r][3], (int)xa.w, ia);
-          ib = __dp4a((int)w[r][7], (int)xb.w, ib);
-        }
-        const int is = (F == QMV_Q4_K) ? ia * 16 + ib : ia + ib;
-        float v = fmaf(sA[r] * dx, (float)is, acc[r][t]);
+        float v = fmaf(sA[r] * dx, (float)dot(w[r], xa, xb), acc[r][0]);
         if constexpr (F == QMV_Q4_K) v = fmaf(-sB[r], dxs, v);
-        acc[r][t] = v;
+        acc[r][0] = v;
       }
+    } else {
+      // token pairs: the scale products and accumulations of two tokens go
+      // through packed fp32x2 multiply / fma (each lane of the pair rounds
+      // like the scalar operation)
+#pragma unroll
+      for (int t = 0; t < NT; t += 2) {
+        const uint4 xa0 = *reinterpret_cast<const uint4*>(ap + t * ACT_BYTES);
+        const uint4 xb0 = *reinterpret_cast<const uint4*>(ap + t * ACT_BYTES + 128);
+        const uint4 xa1 = *reinterpret_cast<const uint4*>(ap + (t + 1) * ACT_BYTES);
+        const uint4 xb1 = *reinterpret_cast<const uint4*>(ap + (t + 1) * ACT_BYTES + 128);
+        const float2 dx = *reinterpret_cast<const float2*>(ad + act_dpos<NT>(t, lane));
+        float2 dxs = make_float2(0.f, 0.f);
+        if constexpr (F == QMV_Q4_K) dxs = *reinterpret_cast<const float2*>(ads + act_dpos<NT>(t, lane));
+#pragma unroll
+        for (int r = 0; r < RW; r++) {
+          const float2 is = make_float2((float)dot(w[r], xa0, xb0), (float)dot(w[r], xa1, xb1));
+          float2 v = __ffma2_rn(__fmul2_rn(make_float2(sA[r], sA[r]), dx), is, make_float2(acc[r][t], acc[r][t + 1]));
+          if constexpr (F == QMV_Q4_K) v = __ffma2_rn(make_float2(-sB[r], -sB[r]), dxs, v);
+          acc[r][t] = v.x;
+          acc[r][t + 1] = v.y;
+        }
+      }
+    }
+  }
+
+  // Exact int32 dot product of one 32-weight block with the activation words
+  // xa (elements 0..15 of the block) and xb (16..31).  Q4_K: 16 x the sum
+  // (both nibble halves weigh 16; the staged d_x carries the 1/16).  With
+  // one token the two halves run as independent chains.
+  __device__ __forceinline__ int dot(const uint32_t (&w)[8], uint4 xa, uint4 xb) const {
+    if constexpr (F == QMV_Q4_K) {
+      if constexpr (Q4K_LO16) {
+        int s = dp4a_us(w[0], xa.x, 0);
+        s = dp4a_us(w[1], xa.y, s);
+        s = dp4a_us(w[2], xa.z, s);
+        s = dp4a_us(w[3], xa.w, s);
+        s = dp4a_us(w[4], xb.x, s);
+        s = dp4a_us(w[5], xb.y, s);
+        s = dp4a_us(w[6], xb.z, s);
+        return dp4a_us(w[7], xb.w, s);
+      } else {
+        int ia = dp4a_us(w[0], xa.x, 0);
+        int ib = dp4a_us(w[4], xb.x, 0);
+        ia = dp4a_us(w[1], xa.y, ia);
+        ib = dp4a_us(w[5], xb.y, ib);
+        ia = dp4a_us(w[2], xa.z, ia);
+        ib = dp4a_us(w[6], xb.z, ib);
+        ia = dp4a_us(w[3], xa.w, ia);
+        ib = dp4a_us(w[7], xb.w, ib);
+        return ia * 16 + ib;
+      }
+    } else if constexpr (NT == 1) {
+      int ia = __dp4a((int)w[0], (int)xa.x, 0);
+      int ib = __dp4a((int)w[4], (int)xb.x, 0);
+      ia = __dp4a((int)w[1], (int)xa.y, ia);
+      ib = __dp4a((int)w[5], (int)xb.y, ib);
+      ia = __dp4a((int)w[2], (int)xa.z, ia);
+      ib = __dp4a((int)w[6], (int)xb.z, ib);
+      ia = __dp4a((int)w[3], (int)xa.w, ia);
+      ib = __dp4a((int)w[7], (int)xb.w, ib);
+      return ia + ib;
+    } else {
+      int s = __dp4a((int)w[0], (int)xa.x, 0);
+      s = __dp4a((int)w[1], (int)xa.y, s);
+      s = __dp4a((int)w[2], (int)xa.z, s);
+      s = __dp4a((int)w[3], (int)xa.w, s);
+      s = __dp4a((int)w[4], (int)xb.x, s);
+      s = __dp4a((int)w[5], (int)xb.y, s);
+      s = __dp4a((int)w[6], (int)xb.z, s);
+      return __dp4a((int)w[7], (int)xb.w, s);
     }
   }
 };

@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
         const uint8_t* rows[RW];
 #pragma unroll
         for (int r = 0; r < RW; r++) rows[r] = sb + r * CB;
-        cons.chunk(rows, a.q + (size_t)c * NT * ACT_BYTES, a.d + c * NT * 32 + lane, a.ds + c * NT * 32 + lane,
+        cons.chunk(rows, a.q + (size_t)c * NT * ACT_BYTES, a.d + c * NT * 32, a.ds + c * NT * 32,
                    lane, acc);
       }
       __syncwarp();
