@@ -50,29 +50,42 @@ struct DenseParams {
 // units that stay inside one split.
 struct TileWalk {
   long long f, f_end;
-  int units;
+  int units, s, u;  // split and unit at f
   __device__ TileWalk(const DenseParams& p) {
     const long long total = (long long)p.n_split * p.units;
     f = total * blockIdx.x / gridDim.x;
     f_end = total * (blockIdx.x + 1) / gridDim.x;
     units = p.units;
-  }
-  // Next tile: split s, first unit u, number of units nu.
-  __device__ bool next(int& s, int& u, int& nu) {
-    if (f >= f_end) return false;
     s = (int)(f / units);
     u = (int)(f - (long long)s * units);
-    long long lim = f_end - f;
-    int rest = units - u;
+  }
+  // Next tile: split ts, first unit tu, number of units nu.
+  __device__ bool next(int& ts, int& tu, int& nu) {
+    if (f >= f_end) return false;
+    ts = s;
+    tu = u;
+    const long long lim = f_end - f;
+    const int rest = units - u;
     nu = (int)min((long long)min(TILE_ROWS / UNIT_ROWS, rest), lim);
     f += nu;
+    u += nu;
+    if (u == units) {
+      u = 0;
+      s++;
+    }
     return true;
   }
 };
 
+// Groups [g0, g1) of split s (groups * n_split <= 2^20: K <= 2^20, n_split <= 256).
 __device__ __forceinline__ void split_range(const DenseParams& p, int s, int& g0, int& g1) {
-  g0 = (int)((long long)p.groups * s / p.n_split);
-  g1 = (int)((long long)p.groups * (s + 1) / p.n_split);
+  if (p.n_split == 1) {
+    g0 = 0;
+    g1 = p.groups;
+  } else {
+    g0 = p.groups * s / p.n_split;
+    g1 = p.groups * (s + 1) / p.n_split;
+  }
 }
 
 template <int F, int NT>
