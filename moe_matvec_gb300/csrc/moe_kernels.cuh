@@ -256,11 +256,10 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
   Ring ring;
   int staged_pair = -1, nt = 0, first = 0;
   const Consumer<F, NT> cons(lane);
-  float acc[RW][NT];
-#pragma unroll
-  for (int r = 0; r < RW; r++)
-#pragma unroll
-    for (int t = 0; t < NT; t++) acc[r][t] = 0.f;
+  AccTile<NT> acc;
+  acc.zero();
+  const uint32_t stage_base = smem_u32(stages), aq_base = smem_u32(a.q), ad_base = smem_u32(a.d),
+                 ads_base = smem_u32(a.ds);
   int roff[RW];  // stage row of each of the warp's rows
   if constexpr (MODE == MOE_GATE_UP) {
     roff[0] = 2 * cw;
@@ -303,12 +302,11 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
         break;
       }
       if (active) {
-        const uint8_t* sb = stages + st * STAGE_BYTES;
-        const uint8_t* rows[RW];
-#pragma unroll
-        for (int r = 0; r < RW; r++) rows[r] = sb + roff[r] * CB;
-        cons.chunk(rows, a.q + (size_t)c * NT * ACT_BYTES, a.d + c * NT * 32, a.ds + c * NT * 32,
-                   lane, acc);
+        // GATE_UP: rows (2cw, 2cw + 1) of the gate half and the same of the
+        // up half, 16 rows apart; DOWN: 4 consecutive rows
+        constexpr int PS = (MODE == MOE_GATE_UP ? 16 : 2) * CB;
+        cons.template chunk<PS>(stage_base + st * STAGE_BYTES + roff[0] * CB, aq_base + c * NT * ACT_BYTES,
+                                ad_base + c * NT * 32 * 4, ads_base + c * NT * 32 * 4, acc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
@@ -321,8 +319,8 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
       if constexpr (MODE == MOE_GATE_UP) {
 #pragma unroll
         for (int i = 0; i < 2; i++) {
-          const float g = warp_sum(acc[i][t]);
-          const float v = warp_sum(acc[2 + i][t]);
+          const float g = warp_sum(acc.get(i, t));
+          const float v = warp_sum(acc.get(2 + i, t));
           const int j = 2 * cw + i;
           if (lane == ((2 * t + i) & 31) && t < nt && j < nvalid) {
             const float h = g / (1.0f + expf(-g)) * v;
@@ -332,14 +330,13 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
       } else {
 #pragma unroll
         for (int r = 0; r < RW; r++) {
-          const float v = warp_sum(acc[r][t]);
+          const float v = warp_sum(acc.get(r, t));
           if (lane == ((r * NT + t) & 31) && t < nt && roff[r] < nvalid)
             p.dst[(long long)rt.slots[first + t] * p.R + row0 + roff[r]] = v;
         }
       }
-#pragma unroll
-      for (int r = 0; r < RW; r++) acc[r][t] = 0.f;
     }
+    acc.zero();
   }
 }
 

@@ -282,64 +282,114 @@ __device__ __forceinline__ uint32_t iq4_lookup4(uint32_t pl, uint32_t p, uint32_
   return (hi & m) | (lo & ~m);
 }
 
+// Shared-memory loads by 32-bit shared address.
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float2 lds_f2(uint32_t a) {
+  const uint2 v = lds64(a);
+  return make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+}
+
+// The accumulators of a warp's RW rows x NT token slots, kept as fp32 pairs
+// of consecutive slots (a register pair each, operand of the packed fp32x2
+// instructions); with one slot only .x is used.
+template <int NT>
+struct AccTile {
+  static constexpr int NP = NT >= 2 ? NT / 2 : 1;
+  float2 v[RW][NP];
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int r = 0; r < RW; r++)
+#pragma unroll
+      for (int q = 0; q < NP; q++) v[r][q] = make_float2(0.f, 0.f);
+  }
+  __device__ __forceinline__ float get(int r, int t) const { return (t & 1) ? v[r][t >> 1].y : v[r][t >> 1].x; }
+};
+
 // The consumer step.  Each lane owns one 32-weight block of every chunk; its
 // byte offsets inside a staged row chunk and inside the activation chunk are
 // fixed for the whole kernel.
 template <int F, int NT>
 struct Consumer {
-  int w_off;  // payload of the lane's block in a row chunk
-  int h_off;  // header bytes the lane needs in a row chunk
-  int a_off;  // the lane's block in a token's activation chunk
-  int fsel;   // Q4_K: which word pair holds the lane's 12-bit scale field
-  int fsh;    // Q4_K: its bit offset in that pair
+  uint32_t w_off;  // payload of the lane's block in a row chunk
+  uint32_t h_off;  // first header word the lane reads in a row chunk
+  uint32_t f_off;  // Q4_K / IQ4_XS: word holding (the start of) the lane's 6/12-bit scale field
+  uint32_t fsh;    // bit offset of that field in the word pair at f_off
+  uint32_t a_off;  // the lane's block in a token's activation chunk
+  uint32_t d_off;  // the lane's scale in a chunk's scale array (token slot 0)
 
   __device__ explicit Consumer(int lane) {
+    const int j = lane & 7;
     if constexpr (F == QMV_Q8_0) {
-      const int g = lane >> 3, b8 = lane & 7;
-      w_off = g * 272 + 16 + 16 * b8;
-      h_off = g * 272 + 2 * b8;
+      const int g = lane >> 3;
+      w_off = g * 272 + 16 + 16 * j;
+      h_off = g * 272 + 2 * j;
+      f_off = fsh = 0;
     } else if constexpr (F == QMV_Q4_K) {
-      const int g = lane >> 3, j = lane & 7;
+      const int g = lane >> 3;
       w_off = g * 144 + 16 + 16 * j;
       h_off = g * 144;
+      // bits [12j, 12j + 12) of the 96-bit string at header byte 4 (for the
+      // last fields the second word is the first payload word, unused bits)
+      f_off = h_off + 4 + 4 * ((12 * j) >> 5);
+      fsh = (12 * j) & 31;
     } else {
-      const int g = lane >> 4, sb = (lane >> 3) & 1, j = lane & 7;
+      const int g = lane >> 4, sb = (lane >> 3) & 1;
       w_off = g * 272 + 16 + 128 * sb + 16 * j;
       h_off = g * 272 + 8 * sb;
+      // ls_j: bits [16 + 6j, 22 + 6j) of the superblock's 8-byte header
+      f_off = h_off + 4 * ((16 + 6 * j) >> 5);
+      fsh = (16 + 6 * j) & 31;
     }
     a_off = act_pos(lane, 0);
-    fsel = (12 * (lane & 7)) >> 5;
-    fsh = (12 * (lane & 7)) & 31;
+    d_off = 4 * act_dpos<NT>(0, lane);
   }
 
   // Q4_K with 4 or more tokens: both nibble halves as 16 x code, one chain.
   static constexpr bool Q4K_LO16 = NT >= 4;
 
-  // rows[r]: start of row r's chunk in the stage; aq / ad / ads: this chunk's
-  // activation codes / scales / scale-sums (token slot 0).
-  __device__ __forceinline__ void chunk(const uint8_t* const (&rows)[RW], const uint8_t* aq, const float* ad,
-                                        const float* ads, int lane, float (&acc)[RW][NT]) const {
+  // row0: shared address of the warp's first row chunk in the stage; row r
+  // starts at row0 + (r & 1) * chunk_bytes + (r >> 1) * PAIR_STRIDE (rows in
+  // pairs: consecutive rows use PAIR_STRIDE = 2 * chunk_bytes).  aq / ad /
+  // ads: shared addresses of this chunk's activation codes / scales /
+  // scale-sums (token slot 0).
+  template <int PAIR_STRIDE = 2 * chunk_bytes<F>()>
+  __device__ __forceinline__ void chunk(uint32_t row0, uint32_t aq, uint32_t ad, uint32_t ads,
+                                        AccTile<NT>& acc) const {
+    constexpr int CB = chunk_bytes<F>();
     uint32_t w[RW][8];  // decoded operands, paired with activation words 0..7
     float sA[RW];       // multiplier of d_x * isum
     float sB[RW];       // Q4_K: dmin * m, multiplier of d_x * s
 #pragma unroll
     for (int r = 0; r < RW; r++) {
-      const uint8_t* row = rows[r];
+      const uint32_t row = row0 + (r & 1) * CB + (r >> 1) * PAIR_STRIDE;
       if constexpr (F == QMV_Q8_0) {
-        const uint4 x0 = *reinterpret_cast<const uint4*>(row + w_off);
-        const uint4 x1 = *reinterpret_cast<const uint4*>(row + w_off + 128);
+        const uint4 x0 = lds128(row + w_off);
+        const uint4 x1 = lds128(row + w_off + 128);
         w[r][0] = x0.x; w[r][1] = x0.y; w[r][2] = x0.z; w[r][3] = x0.w;
         w[r][4] = x1.x; w[r][5] = x1.y; w[r][6] = x1.z; w[r][7] = x1.w;
-        sA[r] = __half2float(*reinterpret_cast<const __half*>(row + h_off));
+        // the lane's fp16 d is the low or high half of an aligned word
+        const uint32_t hw = lds32(row + (h_off & ~3u));
+        sA[r] = __half2float(__ushort_as_half((unsigned short)((h_off & 2) ? hw >> 16 : hw & 0xFFFF)));
         sB[r] = 0.f;
       } else if constexpr (F == QMV_Q4_K) {
-        // d | dmin, and the two header words holding the lane's 12-bit
-        // (sc | m << 6) field (for the last fields the second word is the
-        // first payload word; only bits of the first word are used then)
-        const __half2 dh = *reinterpret_cast<const __half2*>(row + h_off);
-        const uint32_t f0 = *reinterpret_cast<const uint32_t*>(row + h_off + 4 + 4 * fsel);
-        const uint32_t f1 = *reinterpret_cast<const uint32_t*>(row + h_off + 8 + 4 * fsel);
-        const uint4 q = *reinterpret_cast<const uint4*>(row + w_off);
+        const uint32_t dh = lds32(row + h_off);  // d | dmin
+        const uint32_t f0 = lds32(row + f_off);
+        const uint32_t f1 = lds32(row + f_off + 4);
+        const uint4 q = lds128(row + w_off);
         const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
         // high nibbles left in place (16 x code) for an unsigned-byte dp4a;
         // low nibbles as bytes (the dot product scales their sum by 16) or,
@@ -351,16 +401,16 @@ struct Consumer {
           w[r][4 + i] = qq[i] & 0xF0F0F0F0u;
         }
         const uint32_t f = __funnelshift_r(f0, f1, fsh);
-        const float2 dd = __half22float2(dh);
+        const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&dh));
         sA[r] = dd.x * (float)(f & 63u);
         sB[r] = dd.y * (float)((f >> 6) & 63u);
       } else {
-        const uint2 meta = *reinterpret_cast<const uint2*>(row + h_off);
-        const uint4 q = *reinterpret_cast<const uint4*>(row + w_off);
-        const int j = lane & 7;
-        const uint64_t m64 = ((uint64_t)meta.y << 32) | meta.x;
-        const int ls = (int)((m64 >> (16 + 6 * j)) & 63u);
-        sA[r] = __half2float(__ushort_as_half((unsigned short)(meta.x & 0xFFFF))) * (float)(ls - 32);
+        const uint32_t dw = lds32(row + h_off);
+        const uint32_t f0 = lds32(row + f_off);
+        const uint32_t f1 = lds32(row + f_off + 4);
+        const uint4 q = lds128(row + w_off);
+        const int ls = (int)(__funnelshift_r(f0, f1, fsh) & 63u);
+        sA[r] = __half2float(__ushort_as_half((unsigned short)(dw & 0xFFFF))) * (float)(ls - 32);
         sB[r] = 0.f;
         const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -373,39 +423,44 @@ struct Consumer {
         }
       }
     }
-    const uint8_t* ap = aq + a_off;
+    const uint32_t ap = aq + a_off;
     if constexpr (NT == 1) {
-      const uint4 xa = *reinterpret_cast<const uint4*>(ap);
-      const uint4 xb = *reinterpret_cast<const uint4*>(ap + 128);
-      const float dx = ad[lane];
+      const uint4 xa = lds128(ap);
+      const uint4 xb = lds128(ap + 128);
+      const float dx = __uint_as_float(lds32(ad + d_off));
       float dxs = 0.f;
-      if constexpr (F == QMV_Q4_K) dxs = ads[lane];
+      if constexpr (F == QMV_Q4_K) dxs = __uint_as_float(lds32(ads + d_off));
 #pragma unroll
       for (int r = 0; r < RW; r++) {
-        float v = fmaf(sA[r] * dx, (float)dot(w[r], xa, xb), acc[r][0]);
+        float v = fmaf(sA[r] * dx, (float)dot(w[r], xa, xb), acc.v[r][0].x);
         if constexpr (F == QMV_Q4_K) v = fmaf(-sB[r], dxs, v);
-        acc[r][0] = v;
+        acc.v[r][0].x = v;
       }
     } else {
       // token pairs: the scale products and accumulations of two tokens go
       // through packed fp32x2 multiply / fma (each lane of the pair rounds
       // like the scalar operation)
+      float2 sA2[RW], nsB2[RW];
+#pragma unroll
+      for (int r = 0; r < RW; r++) {
+        sA2[r] = make_float2(sA[r], sA[r]);
+        nsB2[r] = make_float2(-sB[r], -sB[r]);
+      }
 #pragma unroll
       for (int t = 0; t < NT; t += 2) {
-        const uint4 xa0 = *reinterpret_cast<const uint4*>(ap + t * ACT_BYTES);
-        const uint4 xb0 = *reinterpret_cast<const uint4*>(ap + t * ACT_BYTES + 128);
-        const uint4 xa1 = *reinterpret_cast<const uint4*>(ap + (t + 1) * ACT_BYTES);
-        const uint4 xb1 = *reinterpret_cast<const uint4*>(ap + (t + 1) * ACT_BYTES + 128);
-        const float2 dx = *reinterpret_cast<const float2*>(ad + act_dpos<NT>(t, lane));
+        const uint4 xa0 = lds128(ap + t * ACT_BYTES);
+        const uint4 xb0 = lds128(ap + t * ACT_BYTES + 128);
+        const uint4 xa1 = lds128(ap + (t + 1) * ACT_BYTES);
+        const uint4 xb1 = lds128(ap + (t + 1) * ACT_BYTES + 128);
+        const float2 dx = lds_f2(ad + d_off + t * 128);
         float2 dxs = make_float2(0.f, 0.f);
-        if constexpr (F == QMV_Q4_K) dxs = *reinterpret_cast<const float2*>(ads + act_dpos<NT>(t, lane));
+        if constexpr (F == QMV_Q4_K) dxs = lds_f2(ads + d_off + t * 128);
 #pragma unroll
         for (int r = 0; r < RW; r++) {
           const float2 is = make_float2((float)dot(w[r], xa0, xb0), (float)dot(w[r], xa1, xb1));
-          float2 v = __ffma2_rn(__fmul2_rn(make_float2(sA[r], sA[r]), dx), is, make_float2(acc[r][t], acc[r][t + 1]));
-          if constexpr (F == QMV_Q4_K) v = __ffma2_rn(make_float2(-sB[r], -sB[r]), dxs, v);
-          acc[r][t] = v.x;
-          acc[r][t + 1] = v.y;
+          float2 v = __ffma2_rn(__fmul2_rn(sA2[r], dx), is, acc.v[r][t >> 1]);
+          if constexpr (F == QMV_Q4_K) v = __ffma2_rn(nsB2[r], dxs, v);
+          acc.v[r][t >> 1] = v;
         }
       }
     }

@@ -187,11 +187,10 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
   Ring ring;
   int staged_split = -1;
   const Consumer<F, NT> cons(lane);
-  float acc[RW][NT];
-#pragma unroll
-  for (int r = 0; r < RW; r++)
-#pragma unroll
-    for (int t = 0; t < NT; t++) acc[r][t] = 0.f;
+  AccTile<NT> acc;
+  acc.zero();
+  const uint32_t stage_base = smem_u32(stages), aq_base = smem_u32(a.q), ad_base = smem_u32(a.d),
+                 ads_base = smem_u32(a.ds);
   const ActSource src{p.x, p.xq, p.xd, p.xs, p.K, nullptr, p.t0, nullptr, nullptr, nullptr};
 
   while (walk.next(s, u, nu)) {
@@ -213,14 +212,9 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
         alive = false;
         break;
       }
-      if (cw * RW < nrows) {
-        const uint8_t* sb = stages + st * STAGE_BYTES + cw * RW * CB;
-        const uint8_t* rows[RW];
-#pragma unroll
-        for (int r = 0; r < RW; r++) rows[r] = sb + r * CB;
-        cons.chunk(rows, a.q + (size_t)c * NT * ACT_BYTES, a.d + c * NT * 32, a.ds + c * NT * 32,
-                   lane, acc);
-      }
+      if (cw * RW < nrows)
+        cons.chunk(stage_base + st * STAGE_BYTES + cw * RW * CB, aq_base + c * NT * ACT_BYTES,
+                   ad_base + c * NT * 32 * 4, ads_base + c * NT * 32 * 4, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
@@ -232,13 +226,13 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
     for (int r = 0; r < RW; r++) {
 #pragma unroll
       for (int t = 0; t < NT; t++) {
-        const float v = warp_sum(acc[r][t]);
+        const float v = warp_sum(acc.get(r, t));
         const int row = cw * RW + r;
         if (lane == ((r * NT + t) & 31) && t < p.nt && row < nrows)
           out[(long long)(p.t0 + t) * p.M + row0 + row] = v;
-        acc[r][t] = 0.f;
       }
     }
+    acc.zero();
   }
 }
 
