@@ -324,6 +324,10 @@ def run_ours(args):
     value, tmax = aggregate(gather_floats(ms, world), [step_bytes * steps] * world)
     launches = steps * len(NTOKS)
 
+    extra = None
+    if not args.no_extra:
+        extra = run_extra(torch, api, synth, stream, dev, measured_peaks()[0]["hbm_gbs"])
+
     # e2e: public API with host buffers, eager launches, copies every step
     xh = {n: xs[n].cpu().pin_memory() for n in NTOKS}
     yh = {n: torch.empty((n, M)).pin_memory() for n in NTOKS}
@@ -370,6 +374,8 @@ def run_ours(args):
                     "d2h_bytes_per_step": sum(n * M * 4 for n in NTOKS),
                     "ms_per_step": e2e_ms / e2e_steps},
             "gpu_launches": launches, "clocks": clk.summary()}
+    if extra is not None:
+        line["workloads"] = extra
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line), flush=True)
@@ -377,6 +383,121 @@ def run_ours(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+# --------------------------------------------------------------------------
+# the other workloads (parity-test configurations), timed the same way
+# --------------------------------------------------------------------------
+
+def _graph_us(torch, stream, calls, reps=20):
+    """µs per call of `calls` (callables launching on `stream`) replayed as one
+    CUDA graph `reps` times, after an eager pass and a warm replay."""
+    with torch.cuda.stream(stream):
+        for c in calls:
+            c()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for c in calls:
+            c()
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            g.replay()
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (reps * len(calls))
+
+
+def _replicas(torch, api, fmt, M, K, nbytes_min, dev, seed):
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    w = torch.randn((M, K), generator=g, device=dev, dtype=torch.float32) * 0.02
+    W0 = api.quantize_weights(fmt, w)
+    del w
+    rb = M * api.row_bytes(fmt, K)
+    n = max(1, -(-nbytes_min // rb))
+    return [W0] + [W0.clone() for _ in range(n - 1)], rb
+
+
+def run_extra(torch, api, synth, stream, dev, peak):
+    """µs/call and effective weight GB/s of every other configuration: the
+    Q8_0 GEMV, the IQ4_XS matvecs, split-K (LM head and long K) and the MoE
+    decode layer.  Weight sets rotate over replicas totalling > 2 x L2 (the
+    LM head alone is > 6 x L2); MoE calls rotate over 16 routing draws."""
+    out = {}
+    l2x2 = 2 * 135 * 2 ** 20
+
+    def line(bytes_per_call, us):
+        gbs = bytes_per_call / (us * 1e-6) / 1e9
+        return {"us_per_call": round(us, 3), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+
+    dense = [("q8_0_gemv_4096x4096", 0, 4096, 4096, (1,)),
+             ("iq4_xs_6144x2048", 2, 6144, 2048, (1, 4, 8)),
+             ("iq4_xs_2048x6144", 2, 2048, 6144, (1, 4, 8))]
+    for i, (name, fmt, M, K, ns) in enumerate(dense):
+        Ws, rb = _replicas(torch, api, fmt, M, K, l2x2, dev, 2000 + i)
+        res = {}
+        for n in ns:
+            x = torch.from_numpy(synth.activations(3000 + n, n, K)).to(dev)
+            y = torch.empty((n, M), device=dev)
+            calls = [(lambda W=W: api.run(fmt, W, x, M, K, out=y, stream=stream)) for W in Ws]
+            res[str(n)] = line(rb, _graph_us(torch, stream, calls))
+        out[name] = {"format": ["Q8_0", "Q4_K", "IQ4_XS"][fmt], "bytes_per_call": rb, "replicas": len(Ws),
+                     "n_tok": res}
+        del Ws
+
+    splitk = [("splitk_q8_0_151936x5120", 151936, 5120, 2), ("splitk_q8_0_512x65536", 512, 65536, None)]
+    for i, (name, M, K, reps_min) in enumerate(splitk):
+        Ws, rb = _replicas(torch, api, 0, M, K, l2x2, dev, 2100 + i)
+        res = {}
+        for n in (1, 2, 4, 8, 16):
+            x = torch.from_numpy(synth.activations(3100 + n, n, K)).to(dev)
+            y = torch.empty((n, M), device=dev)
+            S = api.splitk_choose(0, M, K, n)
+            ws = torch.empty(max(16, api.splitk_workspace_bytes(M, n, S)), dtype=torch.uint8, device=dev)
+            calls = [(lambda W=W: api.splitk_run(0, W, x, M, K, n_split=S, ws=ws, out=y, stream=stream))
+                     for W in Ws]
+            r = line(rb, _graph_us(torch, stream, calls, reps=10 if rb > 2 ** 28 else 20))
+            r["n_split"] = S
+            res[str(n)] = r
+        out[name] = {"format": "Q8_0", "bytes_per_call": rb, "replicas": len(Ws), "n_tok": res}
+        del Ws
+
+    c = synth.MOE_CASE
+    g = torch.Generator(device=dev)
+    g.manual_seed(2200)
+    H, F, E = c.hidden, c.ffn, c.n_experts
+    wg = torch.empty((E, 2 * F, api.row_bytes(c.fmt_gate_up, H)), dtype=torch.uint8, device=dev)
+    wd = torch.empty((E, H, api.row_bytes(c.fmt_down, F)), dtype=torch.uint8, device=dev)
+    for e in range(E):
+        wg[e] = api.quantize_weights(c.fmt_gate_up, torch.randn((2 * F, H), generator=g, device=dev) * 0.02)
+        wd[e] = api.quantize_weights(c.fmt_down, torch.randn((H, F), generator=g, device=dev) * 0.02)
+    ex = api.moe_experts(E, H, F, c.fmt_gate_up, c.fmt_down, wg, wd)
+    per_expert = wg[0].numel() + wd[0].numel()
+    res = {}
+    for n in c.n_toks:
+        sets = [synth.routing(2300 + 17 * n + k, n, E, c.top_k) for k in range(16)]
+        ids = [torch.from_numpy(a).to(dev) for a, _ in sets]
+        gates = [torch.from_numpy(b).to(dev) for _, b in sets]
+        x = torch.from_numpy(synth.activations(2400 + n, n, H)).to(dev)
+        y = torch.empty((n, H), device=dev)
+        ws = torch.empty(api.moe_workspace_bytes(ex, n, c.top_k), dtype=torch.uint8, device=dev)
+        calls = [(lambda k=k: api.moe_run(ex, ids[k], gates[k], x, ws=ws, out=y, stream=stream))
+                 for k in range(len(sets))]
+        us = _graph_us(torch, stream, calls)
+        distinct = sum(len(np.unique(a)) for a, _ in sets) / len(sets)
+        r = line(distinct * per_expert, us)
+        r["distinct_experts"] = round(distinct, 2)
+        res[str(n)] = r
+    out["moe_128x_top8_h4096_f1536"] = {"format": "gate/up IQ4_XS, down Q4_K", "bytes_per_expert": per_expert,
+                                        "routing_draws": 16, "n_tok": res}
+    del wg, wd
+    return out
 
 
 def run_profile(args):
@@ -405,6 +526,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=24)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--profile", action="store_true", help="a few eager calls only (for ncu)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -143,7 +143,7 @@ struct MoeWalk {
 };
 
 template <int F, int NT, int MODE>
-__global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
+__global__ void __launch_bounds__(THREADS, 1)
     moe_qmv_kernel(const __grid_constant__ CUtensorMap map_tile, const __grid_constant__ CUtensorMap map_unit,
                    const MoeParams p) {
   constexpr int CB = chunk_bytes<F>();
@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
         // up half, 16 rows apart; DOWN: 4 consecutive rows
         constexpr int PS = (MODE == MOE_GATE_UP ? 16 : 2) * CB;
         cons.template chunk<PS>(stage_base + st * STAGE_BYTES + roff[0] * CB, aq_base + c * NT * ACT_BYTES,
-                                ad_base + c * NT * 32 * 4, ads_base + c * NT * 32 * 4, acc);
+                                ad_base + c * NT * 32 * 4, ads_base + c * NT * 32 * 4, nt, acc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
@@ -316,13 +316,14 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
     const int row0 = u * UNIT_ROWS;
 #pragma unroll
     for (int t = 0; t < NT; t++) {
+      if (t >= nt) break;  // slots of this group without a token
       if constexpr (MODE == MOE_GATE_UP) {
 #pragma unroll
         for (int i = 0; i < 2; i++) {
           const float g = warp_sum(acc.get(i, t));
           const float v = warp_sum(acc.get(2 + i, t));
           const int j = 2 * cw + i;
-          if (lane == ((2 * t + i) & 31) && t < nt && j < nvalid) {
+          if (lane == ((2 * t + i) & 31) && j < nvalid) {
             const float h = g / (1.0f + expf(-g)) * v;
             p.dst[(long long)rt.slots[first + t] * p.R + row0 + j] = h;
           }
@@ -331,7 +332,7 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
 #pragma unroll
         for (int r = 0; r < RW; r++) {
           const float v = warp_sum(acc.get(r, t));
-          if (lane == ((r * NT + t) & 31) && t < nt && roff[r] < nvalid)
+          if (lane == ((r * NT + t) & 31) && roff[r] < nvalid)
             p.dst[(long long)rt.slots[first + t] * p.R + row0 + roff[r]] = v;
         }
       }

@@ -5,6 +5,8 @@
 
 #include <mutex>
 
+#include <cmath>
+
 #include "launch.h"
 #include "moe_kernels.cuh"
 #include "qmv_dense.cuh"
@@ -426,9 +428,16 @@ int moe_qmv_run(const moe_experts* e, const int32_t* ids, const float* gates, co
   uint8_t* w = static_cast<uint8_t*>(ws);
   float* h = reinterpret_cast<float*>(w + off[0]);
   float* o = reinterpret_cast<float*>(w + off[4]);
-  int nt = 16;
+  // Token slots per expert group: a power of two covering the typical group
+  // (tokens per expert ~ lambda = n_tok * top_k / E, plus two standard
+  // deviations); larger groups are split into several groups, each reading the
+  // expert's weights again.  Smaller slot counts keep the kernels free of
+  // register spills.
+  const double lam = (double)n_tok * top_k / e->n_experts;
+  const double want = lam + 2.0 * sqrt(lam);
+  int nt = 1;
+  while (nt < want && nt < 16) nt <<= 1;
   while (nt > n_tok && nt > 1) nt >>= 1;
-  if (nt < n_tok && nt < 16) nt <<= 1;
 
   MoeParams p{};
   p.ids = ids;

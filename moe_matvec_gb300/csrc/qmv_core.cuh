@@ -120,7 +120,8 @@ __device__ __forceinline__ BlockQ quant_block(const float4 (&v)[8]) {
 }
 
 // Stage blocks [kb0, kb0 + nblk) of tokens [0, nt) of `src` into the area
-// (NT slots, ceil(nblk / 32) chunks), zero-filling the padding.  Called by all
+// (NT slots, ceil(nblk / 32) chunks), zero-filling the padding of the slots
+// the consumers read.  Called by all
 // consumer warps.  Four lanes share a block (8 elements each: a load
 // instruction of the warp touches 8 blocks, two shuffle steps combine the
 // maximum and the sum); a warp step covers SU units of 8 blocks with all of
@@ -131,7 +132,12 @@ __device__ __forceinline__ void stage_activations(const ActSource& src, int kb0,
   constexpr int SU = 4;
   const int sub = lane >> 2, li = lane & 3;
   const int nck = (nblk + 31) / 32;
-  const int total = nck * NT * 32;  // a multiple of 32 = blocks of one warp step
+  // slots staged: the smallest power of two >= nt (at least 2 when NT >= 2:
+  // consumers read slots in pairs); the slots above it are never read
+  int sh = 0;
+  while ((1 << sh) < nt) sh++;
+  if (NT >= 2 && sh == 0) sh = 1;
+  const int total = nck * 32 << sh;  // a multiple of 32 = blocks of one warp step
   for (int base = cw * 8 * SU; base < total; base += CONSUMER_WARPS * 8 * SU) {
     int ct[SU], l[SU];
     long long gblk[SU];
@@ -144,8 +150,8 @@ __device__ __forceinline__ void stage_activations(const ActSource& src, int kb0,
     for (int u = 0; u < SU; u++) {
       const int idx = base + 8 * u + sub;
       l[u] = idx & 31;
-      ct[u] = idx >> 5;
-      const int t = ct[u] & (NT - 1), c = ct[u] / NT;
+      const int t = (idx >> 5) & ((1 << sh) - 1), c = idx >> (5 + sh);
+      ct[u] = c * NT + t;  // slot position in the area
       const int b = c * 32 + l[u];
       real[u] = t < nt && b < nblk;
       gblk[u] = real[u] ? src.row(t) * (src.ld / 32) + kb0 + b : 0;
@@ -365,9 +371,10 @@ struct Consumer {
   // starts at row0 + (r & 1) * chunk_bytes + (r >> 1) * PAIR_STRIDE (rows in
   // pairs: consecutive rows use PAIR_STRIDE = 2 * chunk_bytes).  aq / ad /
   // ads: shared addresses of this chunk's activation codes / scales /
-  // scale-sums (token slot 0).
+  // scale-sums (token slot 0); nt: slots holding tokens (the accumulators of
+  // the others are left as they are).
   template <int PAIR_STRIDE = 2 * chunk_bytes<F>()>
-  __device__ __forceinline__ void chunk(uint32_t row0, uint32_t aq, uint32_t ad, uint32_t ads,
+  __device__ __forceinline__ void chunk(uint32_t row0, uint32_t aq, uint32_t ad, uint32_t ads, int nt,
                                         AccTile<NT>& acc) const {
     constexpr int CB = chunk_bytes<F>();
     uint32_t w[RW][8];  // decoded operands, paired with activation words 0..7
@@ -448,6 +455,7 @@ struct Consumer {
       }
 #pragma unroll
       for (int t = 0; t < NT; t += 2) {
+        if (t >= nt) break;  // slots without a token (a short MoE group, a last pass)
         const uint4 xa0 = lds128(ap + t * ACT_BYTES);
         const uint4 xb0 = lds128(ap + t * ACT_BYTES + 128);
         const uint4 xa1 = lds128(ap + (t + 1) * ACT_BYTES);

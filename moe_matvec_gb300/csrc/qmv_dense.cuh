@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
       }
       if (cw * RW < nrows)
         cons.chunk(stage_base + st * STAGE_BYTES + cw * RW * CB, aq_base + c * NT * ACT_BYTES,
-                   ad_base + c * NT * 32 * 4, ads_base + c * NT * 32 * 4, acc);
+                   ad_base + c * NT * 32 * 4, ads_base + c * NT * 32 * 4, p.nt, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
