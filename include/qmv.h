@@ -143,10 +143,15 @@ int64_t qmv_row_bytes(int fmt, int64_t K);
 int qmv_quantize_weights(int fmt, const float* w, int64_t M, int64_t K, void* W,
                          cudaStream_t stream);
 
-/* Activation quantization (rule above) of x [n_tok][K] into q int8
- * [n_tok][K], d fp32 [n_tok][K/32] and sum int32 [n_tok][K/32].
- * K % 256 == 0, 1 <= n_tok <= 64.  "Q8 activations reused across weight
- * types": the result feeds qmv_run_q8 for any weight format. */
+/* Activation quantization (rule above) of x [n_tok][K] into the library's
+ * Q8 activation layout: q int8 [n_tok][K], d fp32 [n_tok][K/32] and sum
+ * int32 [n_tok][K/32], where d and sum are per block in order and the codes
+ * of each 256-element group (8 blocks) are stored halves first: element p of
+ * block l of the group at byte (p / 16) * 128 + l * 16 + p % 16 of the
+ * group.  (That is the order the matvec kernels read, so qmv_run_q8 brings
+ * the rows into shared memory with bulk copies.)  K % 256 == 0,
+ * 1 <= n_tok <= 64.  "Q8 activations reused across weight types": the
+ * result feeds qmv_run_q8 for any weight format. */
 int qmv_quantize_act(const float* x, int64_t K, int n_tok, int8_t* q, float* d,
                      int32_t* sum, cudaStream_t stream);
 
@@ -158,8 +163,9 @@ int qmv_quantize_act(const float* x, int64_t K, int n_tok, int8_t* q, float* d,
 int qmv_run(int fmt, const void* W, const float* x, float* y, int64_t M,
             int64_t K, int n_tok, cudaStream_t stream);
 
-/* Same as qmv_run with pre-quantized activations (layout of
- * qmv_quantize_act). */
+/* Same as qmv_run with pre-quantized activations (the layout of
+ * qmv_quantize_act); results are bitwise equal to qmv_run on the x they
+ * were quantized from. */
 int qmv_run_q8(int fmt, const void* W, const int8_t* xq, const float* xd,
                const int32_t* xs, float* y, int64_t M, int64_t K, int n_tok,
                cudaStream_t stream);

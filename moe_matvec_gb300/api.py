@@ -121,7 +121,8 @@ def quantize_weights(fmt: int, w: torch.Tensor, out: torch.Tensor | None = None,
 
 
 def quantize_act(x: torch.Tensor, stream=None):
-    """Activation rule on x fp32 [n][K] -> (q int8 [n][K], d fp32 [n][K/32], s int32 [n][K/32])."""
+    """Activation rule on x fp32 [n][K] -> (q int8 [n][K], d fp32 [n][K/32], s int32 [n][K/32]) in the
+    library's Q8 activation layout (codes of each 256-element group halves first, see qmv.h)."""
     n, K = x.shape
     q = torch.empty((n, K), dtype=torch.int8, device=x.device)
     d = torch.empty((n, K // 32), dtype=torch.float32, device=x.device)

@@ -39,36 +39,37 @@ __device__ __forceinline__ int act_pos(int l, int p) {
   return (l >> 3) * 256 + (p >> 4) * 128 + (l & 7) * 16 + (p & 15);
 }
 
-// Position of the scale of block l, token slot t within a chunk's NT * 32
-// scales: with two or more slots the slots go in pairs (t, t + 1)
-// interleaved, so that a lane loads the scales of a token pair at once.
-template <int NT>
-__device__ __forceinline__ int act_dpos(int t, int l) {
-  return NT == 1 ? l : (t & ~1) * 32 + 2 * l + (t & 1);
-}
-
-// Bytes of the activation area for nt_slots token slots and nck chunks.
+// Activation area of nt_slots token slots over nck chunks, per slot:
+//   codes  nck * 1024 bytes (each 256-element group in act_pos order),
+//   scales nck * 32 fp32 d (block order),
+//   sums   nck * 32 int32 s (Q4_K only: its min term needs them).
+// This is also the order of the library's pre-quantized activation rows
+// (codes) and of their scale / sum rows, so those arrive by bulk copies.
 __host__ __device__ constexpr size_t act_area_bytes(int F, int nt_slots, int nck) {
   return (size_t)nck * nt_slots * (ACT_BYTES + 32 * sizeof(float) * (F == QMV_Q4_K ? 2 : 1));
 }
 
 struct ActArea {
-  uint8_t* q;
-  float* d;
-  float* ds;
-  __device__ void carve(uint8_t* base, int F, int nt_slots, int nck) {
+  uint8_t* q;  // [slot][nck * 1024]
+  float* d;    // [slot][nck * 32]
+  int32_t* s;  // [slot][nck * 32]
+  int nck;
+  __device__ void carve(uint8_t* base, int F, int nt_slots, int nck_) {
+    nck = nck_;
     q = base;
     d = reinterpret_cast<float*>(base + (size_t)nck * nt_slots * ACT_BYTES);
-    ds = d + (size_t)nck * nt_slots * 32;
+    s = reinterpret_cast<int32_t*>(d + (size_t)nck * nt_slots * 32);
     (void)F;
   }
 };
 
 // Where the activation rows come from: fp32 rows (quantized while staging)
-// or pre-quantized rows; token slot t reads source row rows[t] (a
-// shared-memory list) or row0 + t.  When wq is set, the quantized codes,
-// scales and sums are also written back to global memory (natural order),
-// which is how the MoE path exposes the quantized h.
+// or pre-quantized rows in the library's Q8 activation layout (codes of each
+// 256-element group in act_pos order, one scale and one sum per block); token
+// slot t reads source row rows[t] (a shared-memory list) or row0 + t.  When
+// wq is set, the quantized codes, scales and sums are also written back to
+// global memory (natural order), which is how the MoE path exposes the
+// quantized h.
 struct ActSource {
   const float* x;
   const int8_t* xq;
@@ -83,63 +84,101 @@ struct ActSource {
   __device__ __forceinline__ long long row(int t) const { return rows ? (long long)rows[t] : row0 + t; }
 };
 
-// Quantize one 32-element block held entirely by this lane (activation rule:
-// amax, d = amax / 127, id = 1 / d, q = rne(x * id) in [-127, 127],
-// s = sum q) and pack the codes four per word, natural order.
-struct BlockQ {
-  uint32_t w[8];
-  float d;
-  int s;
-};
-__device__ __forceinline__ BlockQ quant_block(const float4 (&v)[8]) {
-  float m = 0.f;
+// The activation rule for SU units of 8 blocks, four lanes per block (lane
+// group sub = lane / 4 holds block sub of each unit, lane li = lane % 4 its
+// elements 8 li .. 8 li + 7 in v[u][0..1]); called by full warps.  Returns the
+// lane's 8 codes packed in w0 / w1 (natural order) and the block's d and s
+// in every lane of the block.  Four lanes share a block: a load instruction
+// of the warp touches 8 blocks; two shuffle steps combine maximum and sum.
+template <int SU>
+__device__ __forceinline__ void quant_units(const float4 (&v)[SU][2], uint32_t (&w0)[SU], uint32_t (&w1)[SU],
+                                            float (&dd)[SU], int (&ss)[SU]) {
+  float m[SU];
 #pragma unroll
-  for (int i = 0; i < 8; i++) m = fmaxf(m, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
-  BlockQ r;
-  r.d = __fdiv_rn(m, 127.0f);
-  const float id = r.d > 0.0f ? __frcp_rn(r.d) : 0.0f;  // correctly rounded 1 / d
-  // With a normal d, |x * id| <= amax * id < 127.5, so no code needs the
-  // clamp; it only matters for blocks with amax below about 2^-100.
-  const bool tiny = m < 0x1p-100f;
-  int s = 0;
-#pragma unroll
-  for (int i = 0; i < 8; i++) {
-    float f[4] = {__fmul_rn(v[i].x, id), __fmul_rn(v[i].y, id), __fmul_rn(v[i].z, id), __fmul_rn(v[i].w, id)};
-    if (tiny) {
-#pragma unroll
-      for (int k = 0; k < 4; k++) f[k] = fminf(fmaxf(f[k], -127.0f), 127.0f);
-    }
-    const int q0 = __float2int_rn(f[0]), q1 = __float2int_rn(f[1]), q2 = __float2int_rn(f[2]),
-              q3 = __float2int_rn(f[3]);
-    r.w[i] = (uint32_t)(q0 & 0xFF) | ((uint32_t)(q1 & 0xFF) << 8) | ((uint32_t)(q2 & 0xFF) << 16) |
-             ((uint32_t)q3 << 24);
-    s = __dp4a((int)r.w[i], 0x01010101, s);
+  for (int u = 0; u < SU; u++) {
+    m[u] = fmaxf(fmaxf(fmaxf(fabsf(v[u][0].x), fabsf(v[u][0].y)), fmaxf(fabsf(v[u][0].z), fabsf(v[u][0].w))),
+                 fmaxf(fmaxf(fabsf(v[u][1].x), fabsf(v[u][1].y)), fmaxf(fabsf(v[u][1].z), fabsf(v[u][1].w))));
+    m[u] = fmaxf(m[u], __shfl_xor_sync(FULL, m[u], 1));
+    m[u] = fmaxf(m[u], __shfl_xor_sync(FULL, m[u], 2));
   }
-  r.s = s;
-  return r;
+  // Fast path: every block has amax == 0 or amax >= 2^-100, where the
+  // branch-free sequences are exact and no code needs clamping
+  // (|x * id| <= amax * id < 127.5).  Otherwise the whole warp takes the IEEE
+  // operations with the clamp.
+  bool slow = false;
+#pragma unroll
+  for (int u = 0; u < SU; u++) slow |= m[u] > 0.0f && m[u] < 0x1p-100f;
+  slow = __any_sync(FULL, slow);
+  float id[SU];
+  if (!slow) {
+#pragma unroll
+    for (int u = 0; u < SU; u++) {
+      dd[u] = div127_rn(m[u]);
+      id[u] = m[u] > 0.0f ? rcp_rn(fmaxf(dd[u], 0x1p-126f)) : 0.0f;
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < SU; u++) {
+      dd[u] = __fdiv_rn(m[u], 127.0f);
+      id[u] = dd[u] > 0.0f ? __frcp_rn(dd[u]) : 0.0f;
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < SU; u++) {
+    float f[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
+    int q[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+      float p = __fmul_rn(f[k], id[u]);
+      if (slow) p = fminf(fmaxf(p, -127.0f), 127.0f);
+      q[k] = __float2int_rn(p);
+    }
+    w0[u] = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) | ((uint32_t)(q[2] & 0xFF) << 16) |
+            ((uint32_t)q[3] << 24);
+    w1[u] = (uint32_t)(q[4] & 0xFF) | ((uint32_t)(q[5] & 0xFF) << 8) | ((uint32_t)(q[6] & 0xFF) << 16) |
+            ((uint32_t)q[7] << 24);
+    int sm = __dp4a((int)w1[u], 0x01010101, __dp4a((int)w0[u], 0x01010101, 0));
+    sm += __shfl_xor_sync(FULL, sm, 1);
+    sm += __shfl_xor_sync(FULL, sm, 2);
+    ss[u] = sm;
+  }
 }
 
-// Stage blocks [kb0, kb0 + nblk) of tokens [0, nt) of `src` into the area
-// (NT slots, ceil(nblk / 32) chunks), zero-filling the padding of the slots
-// the consumers read.  Called by all
-// consumer warps.  Four lanes share a block (8 elements each: a load
-// instruction of the warp touches 8 blocks, two shuffle steps combine the
-// maximum and the sum); a warp step covers SU units of 8 blocks with all of
-// its loads issued first and no branch inside a unit, so the units overlap.
+// Store a lane's 8 codes of block l (lane li of the block's four) into a
+// slot's chunk of codes.  IQ4_XS reads its activations interleaved (byte
+// 2i = x_i, byte 2i + 1 = x_{i+16}, the order its codebook decode yields):
+// lanes 0, 1 of the block take the elements 16.. of lanes 2, 3.  Called by
+// full warps.
+template <int F>
+__device__ __forceinline__ void store_codes(uint8_t* chunk, int l, int li, uint32_t w0, uint32_t w1) {
+  if constexpr (F == QMV_IQ4_XS) {
+    const uint32_t h0 = __shfl_xor_sync(FULL, w0, 2), h1 = __shfl_xor_sync(FULL, w1, 2);
+    if (li < 2)
+      *reinterpret_cast<uint4*>(chunk + act_pos(l, 16 * li)) =
+          make_uint4(__byte_perm(w0, h0, 0x5140), __byte_perm(w0, h0, 0x7362), __byte_perm(w1, h1, 0x5140),
+                     __byte_perm(w1, h1, 0x7362));
+  } else {
+    *reinterpret_cast<uint2*>(chunk + act_pos(l, 8 * li)) = make_uint2(w0, w1);
+  }
+}
+
+// Stage blocks [kb0, kb0 + nblk) of tokens [0, nt) of `src` into the area,
+// zero-filling the blocks past nblk of the last chunk (and the slots up to
+// the next power of two, which the consumers read in pairs).  Called by all
+// consumer warps; a warp step covers SU units of 8 blocks with all of its
+// loads issued first and no branch inside a unit, so the units overlap.
 template <int F, int NT>
 __device__ __forceinline__ void stage_activations(const ActSource& src, int kb0, int nblk, int nt, const ActArea& a,
                                                   int cw, int lane) {
   constexpr int SU = 4;
   const int sub = lane >> 2, li = lane & 3;
   const int nck = (nblk + 31) / 32;
-  // slots staged: the smallest power of two >= nt (at least 2 when NT >= 2:
-  // consumers read slots in pairs); the slots above it are never read
   int sh = 0;
   while ((1 << sh) < nt) sh++;
   if (NT >= 2 && sh == 0) sh = 1;
   const int total = nck * 32 << sh;  // a multiple of 32 = blocks of one warp step
   for (int base = cw * 8 * SU; base < total; base += CONSUMER_WARPS * 8 * SU) {
-    int ct[SU], l[SU];
+    int tt[SU], cc[SU], l[SU];
     long long gblk[SU];
     bool real[SU];
     uint32_t w0[SU], w1[SU];
@@ -150,11 +189,11 @@ __device__ __forceinline__ void stage_activations(const ActSource& src, int kb0,
     for (int u = 0; u < SU; u++) {
       const int idx = base + 8 * u + sub;
       l[u] = idx & 31;
-      const int t = (idx >> 5) & ((1 << sh) - 1), c = idx >> (5 + sh);
-      ct[u] = c * NT + t;  // slot position in the area
-      const int b = c * 32 + l[u];
-      real[u] = t < nt && b < nblk;
-      gblk[u] = real[u] ? src.row(t) * (src.ld / 32) + kb0 + b : 0;
+      tt[u] = (idx >> 5) & ((1 << sh) - 1);
+      cc[u] = idx >> (5 + sh);
+      const int b = cc[u] * 32 + l[u];
+      real[u] = tt[u] < nt && b < nblk;
+      gblk[u] = real[u] ? src.row(tt[u]) * (src.ld / 32) + kb0 + b : 0;
       v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
       w0[u] = w1[u] = 0u;
       dd[u] = 0.f;
@@ -165,7 +204,10 @@ __device__ __forceinline__ void stage_activations(const ActSource& src, int kb0,
           v[u][0] = __ldg(p);
           v[u][1] = __ldg(p + 1);
         } else {
-          const uint2 q = __ldg(reinterpret_cast<const uint2*>(src.xq + gblk[u] * 32) + li);
+          // pre-quantized rows: codes in act_pos order within each group
+          const int gb = (int)(gblk[u] & 7);
+          const uint2 q = __ldg(reinterpret_cast<const uint2*>(src.xq + (gblk[u] - gb) * 32 +
+                                                               act_pos(gb, 8 * li)));
           w0[u] = q.x;
           w1[u] = q.y;
           dd[u] = __ldg(src.xd + gblk[u]);
@@ -174,89 +216,82 @@ __device__ __forceinline__ void stage_activations(const ActSource& src, int kb0,
       }
     }
     if (src.x != nullptr) {
-      float m[SU];
-#pragma unroll
-      for (int u = 0; u < SU; u++) {
-        m[u] = fmaxf(fmaxf(fmaxf(fabsf(v[u][0].x), fabsf(v[u][0].y)), fmaxf(fabsf(v[u][0].z), fabsf(v[u][0].w))),
-                     fmaxf(fmaxf(fabsf(v[u][1].x), fabsf(v[u][1].y)), fmaxf(fabsf(v[u][1].z), fabsf(v[u][1].w))));
-        m[u] = fmaxf(m[u], __shfl_xor_sync(FULL, m[u], 1));
-        m[u] = fmaxf(m[u], __shfl_xor_sync(FULL, m[u], 2));
-      }
-      // Fast path: every block of the step has amax == 0 or amax >= 2^-100,
-      // where the branch-free sequences are exact and no code needs clamping
-      // (|x * id| <= amax * id < 127.5).  Otherwise the whole warp takes the
-      // IEEE operations with the clamp.
-      bool slow = false;
-#pragma unroll
-      for (int u = 0; u < SU; u++) slow |= m[u] > 0.0f && m[u] < 0x1p-100f;
-      slow = __any_sync(FULL, slow);
-      float id[SU];
-      if (!slow) {
+      quant_units<SU>(v, w0, w1, dd, ss);
+      if (src.wq != nullptr) {
 #pragma unroll
         for (int u = 0; u < SU; u++) {
-          dd[u] = div127_rn(m[u]);
-          id[u] = m[u] > 0.0f ? rcp_rn(fmaxf(dd[u], 0x1p-126f)) : 0.0f;
-        }
-      } else {
-#pragma unroll
-        for (int u = 0; u < SU; u++) {
-          dd[u] = __fdiv_rn(m[u], 127.0f);
-          id[u] = dd[u] > 0.0f ? __frcp_rn(dd[u]) : 0.0f;
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < SU; u++) {
-        float f[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
-        int q[8];
-#pragma unroll
-        for (int k = 0; k < 8; k++) {
-          float p = __fmul_rn(f[k], id[u]);
-          if (slow) p = fminf(fmaxf(p, -127.0f), 127.0f);
-          q[k] = __float2int_rn(p);
-        }
-        w0[u] = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) | ((uint32_t)(q[2] & 0xFF) << 16) |
-                ((uint32_t)q[3] << 24);
-        w1[u] = (uint32_t)(q[4] & 0xFF) | ((uint32_t)(q[5] & 0xFF) << 8) | ((uint32_t)(q[6] & 0xFF) << 16) |
-                ((uint32_t)q[7] << 24);
-        int s = __dp4a((int)w1[u], 0x01010101, __dp4a((int)w0[u], 0x01010101, 0));
-        s += __shfl_xor_sync(FULL, s, 1);
-        s += __shfl_xor_sync(FULL, s, 2);
-        ss[u] = s;
-        if (src.wq != nullptr && real[u]) {
-          reinterpret_cast<uint2*>(src.wq + gblk[u] * 32)[li] = make_uint2(w0[u], w1[u]);
-          if (li == 0) {
-            src.wd[gblk[u]] = dd[u];
-            src.ws[gblk[u]] = s;
+          if (real[u]) {
+            reinterpret_cast<uint2*>(src.wq + gblk[u] * 32)[li] = make_uint2(w0[u], w1[u]);
+            if (li == 0) {
+              src.wd[gblk[u]] = dd[u];
+              src.ws[gblk[u]] = ss[u];
+            }
           }
         }
       }
     }
 #pragma unroll
     for (int u = 0; u < SU; u++) {
-      uint8_t* chunk = a.q + (size_t)ct[u] * ACT_BYTES;
-      if constexpr (F == QMV_IQ4_XS) {
-        // interleaved: byte 2i = x_i, byte 2i+1 = x_{i+16}; lanes 0, 1 of the
-        // block take the elements 16.. of lanes 2, 3
-        const uint32_t h0 = __shfl_xor_sync(FULL, w0[u], 2), h1 = __shfl_xor_sync(FULL, w1[u], 2);
-        if (li < 2)
-          *reinterpret_cast<uint4*>(chunk + act_pos(l[u], 16 * li)) =
-              make_uint4(__byte_perm(w0[u], h0, 0x5140), __byte_perm(w0[u], h0, 0x7362),
-                         __byte_perm(w1[u], h1, 0x5140), __byte_perm(w1[u], h1, 0x7362));
-      } else {
-        *reinterpret_cast<uint2*>(chunk + act_pos(l[u], 8 * li)) = make_uint2(w0[u], w1[u]);
-      }
+      store_codes<F>(a.q + ((size_t)tt[u] * a.nck + cc[u]) * ACT_BYTES, l[u], li, w0[u], w1[u]);
       if (li == 0) {
-        const int t = ct[u] & (NT - 1);
-        const int di = (ct[u] - t) * 32 + act_dpos<NT>(t, l[u]);
-        if constexpr (F == QMV_Q4_K) {
-          a.d[di] = dd[u] * 0.0625f;  // the consumer's isum is 16 x the block sum
-          a.ds[di] = dd[u] * (float)ss[u];
-        } else {
-          a.d[di] = dd[u];
-        }
+        const int di = (tt[u] * a.nck + cc[u]) * 32 + l[u];
+        a.d[di] = dd[u];
+        if constexpr (F == QMV_Q4_K) a.s[di] = ss[u];
       }
     }
   }
+}
+
+// Pre-quantized activations (the library's layout) of blocks [kb0, kb0 +
+// nblk) of tokens [0, nt), brought into the area by bulk copies: per token
+// the codes, the scales and (Q4_K) the sums are contiguous in global memory
+// and land contiguous in the slot.  Warp 0 issues them (its lane 0 first
+// posts the byte count on `bar`); every consumer zeroes the scales past
+// nblk of the last chunk meanwhile, waits for `bar` (phase `parity`) and,
+// for IQ4_XS, reorders each block's codes into the interleaved order its
+// decode reads.  Returns false (timeout bit set) if the copies never land.
+template <int F, int NT>
+__device__ __forceinline__ bool stage_q8_bulk(const ActSource& src, int kb0, int nblk, int nt, const ActArea& a,
+                                              uint64_t* bar, uint32_t parity, unsigned* err, int cw, int lane) {
+  constexpr int NCOPY = F == QMV_Q4_K ? 3 : 2;
+  const int nck = (nblk + 31) / 32;
+  if (cw == 0) {
+    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nt * nblk * (32 + 4 * (NCOPY - 1))));
+    __syncwarp();
+    for (int i = lane; i < nt * NCOPY; i += 32) {
+      const int t = i / NCOPY, k = i - t * NCOPY;
+      const long long row = src.row(t);
+      if (k == 0)
+        bulk_copy_g2s(a.q + (size_t)t * a.nck * ACT_BYTES, src.xq + row * src.ld + (long long)kb0 * 32,
+                      (uint32_t)nblk * 32, bar);
+      else if (k == 1)
+        bulk_copy_g2s(a.d + (size_t)t * a.nck * 32, src.xd + row * (src.ld / 32) + kb0, (uint32_t)nblk * 4, bar);
+      else
+        bulk_copy_g2s(a.s + (size_t)t * a.nck * 32, src.xs + row * (src.ld / 32) + kb0, (uint32_t)nblk * 4, bar);
+    }
+  }
+  const int tail = nck * 32 - nblk;
+  for (int i = cw * 32 + lane; i < nt * tail; i += CONSUMER_THREADS) {
+    const int t = i / tail, b = nblk + (i - t * tail);
+    a.d[t * a.nck * 32 + b] = 0.f;
+    if constexpr (F == QMV_Q4_K) a.s[t * a.nck * 32 + b] = 0;
+  }
+  const bool ok = mbar_wait(bar, parity, err);
+  if constexpr (F == QMV_IQ4_XS) {
+    // x_0..15 and x_16..31 of a block sit in two 16-byte pieces; interleave
+    for (int i = cw * 32 + lane; i < nt * nck * 32; i += CONSUMER_THREADS) {
+      const int t = i / (nck * 32), r = i - t * nck * 32, c = r >> 5, l = r & 31;
+      uint8_t* chunk = a.q + ((size_t)t * a.nck + c) * ACT_BYTES;
+      uint4* p0 = reinterpret_cast<uint4*>(chunk + act_pos(l, 0));
+      uint4* p1 = reinterpret_cast<uint4*>(chunk + act_pos(l, 16));
+      const uint4 lo = *p0, hi = *p1;
+      *p0 = make_uint4(__byte_perm(lo.x, hi.x, 0x5140), __byte_perm(lo.x, hi.x, 0x7362),
+                       __byte_perm(lo.y, hi.y, 0x5140), __byte_perm(lo.y, hi.y, 0x7362));
+      *p1 = make_uint4(__byte_perm(lo.z, hi.z, 0x5140), __byte_perm(lo.z, hi.z, 0x7362),
+                       __byte_perm(lo.w, hi.w, 0x5140), __byte_perm(lo.w, hi.w, 0x7362));
+    }
+  }
+  return ok;
 }
 
 // dp4a with unsigned bytes in a and signed bytes in b.
@@ -335,7 +370,7 @@ struct Consumer {
   uint32_t f_off;  // Q4_K / IQ4_XS: word holding (the start of) the lane's 6/12-bit scale field
   uint32_t fsh;    // bit offset of that field in the word pair at f_off
   uint32_t a_off;  // the lane's block in a token's activation chunk
-  uint32_t d_off;  // the lane's scale in a chunk's scale array (token slot 0)
+  uint32_t d_off;  // the lane's scale in a chunk's scales (token slot 0)
 
   __device__ explicit Consumer(int lane) {
     const int j = lane & 7;
@@ -361,7 +396,7 @@ struct Consumer {
       fsh = (16 + 6 * j) & 31;
     }
     a_off = act_pos(lane, 0);
-    d_off = 4 * act_dpos<NT>(0, lane);
+    d_off = 4 * lane;
   }
 
   // Q4_K with 4 or more tokens: both nibble halves as 16 x code, one chain.
@@ -370,12 +405,13 @@ struct Consumer {
   // row0: shared address of the warp's first row chunk in the stage; row r
   // starts at row0 + (r & 1) * chunk_bytes + (r >> 1) * PAIR_STRIDE (rows in
   // pairs: consecutive rows use PAIR_STRIDE = 2 * chunk_bytes).  aq / ad /
-  // ads: shared addresses of this chunk's activation codes / scales /
-  // scale-sums (token slot 0); nt: slots holding tokens (the accumulators of
-  // the others are left as they are).
+  // as: shared addresses of this chunk's activation codes / scales / sums in
+  // token slot 0; slot t is sq (codes) or sd (scales, sums) bytes further.
+  // nt: slots holding tokens (the accumulators of the others are left as
+  // they are).
   template <int PAIR_STRIDE = 2 * chunk_bytes<F>()>
-  __device__ __forceinline__ void chunk(uint32_t row0, uint32_t aq, uint32_t ad, uint32_t ads, int nt,
-                                        AccTile<NT>& acc) const {
+  __device__ __forceinline__ void chunk(uint32_t row0, uint32_t aq, uint32_t ad, uint32_t as, uint32_t sq,
+                                        uint32_t sd, int nt, AccTile<NT>& acc) const {
     constexpr int CB = chunk_bytes<F>();
     uint32_t w[RW][8];  // decoded operands, paired with activation words 0..7
     float sA[RW];       // multiplier of d_x * isum
@@ -400,8 +436,8 @@ struct Consumer {
         const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
         // high nibbles left in place (16 x code) for an unsigned-byte dp4a;
         // low nibbles as bytes (the dot product scales their sum by 16) or,
-        // for one dp4a chain, shifted up to 16 x code as well.  The staged d_x
-        // of Q4_K carries the 1/16 (exact: a power of two).
+        // for one dp4a chain, shifted up to 16 x code as well.  sA carries
+        // the 1/16 (exact: a power of two).
 #pragma unroll
         for (int i = 0; i < 4; i++) {
           w[r][i] = Q4K_LO16 ? (qq[i] << 4) & 0xF0F0F0F0u : qq[i] & 0x0F0F0F0Fu;
@@ -409,7 +445,7 @@ struct Consumer {
         }
         const uint32_t f = __funnelshift_r(f0, f1, fsh);
         const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&dh));
-        sA[r] = dd.x * (float)(f & 63u);
+        sA[r] = dd.x * (float)(f & 63u) * 0.0625f;  // the dot product is 16 x the block sum
         sB[r] = dd.y * (float)((f >> 6) & 63u);
       } else {
         const uint32_t dw = lds32(row + h_off);
@@ -430,13 +466,13 @@ struct Consumer {
         }
       }
     }
-    const uint32_t ap = aq + a_off;
+    const uint32_t ap = aq + a_off, dp = ad + d_off, sp = as + d_off;
     if constexpr (NT == 1) {
       const uint4 xa = lds128(ap);
       const uint4 xb = lds128(ap + 128);
-      const float dx = __uint_as_float(lds32(ad + d_off));
+      const float dx = __uint_as_float(lds32(dp));
       float dxs = 0.f;
-      if constexpr (F == QMV_Q4_K) dxs = __uint_as_float(lds32(ads + d_off));
+      if constexpr (F == QMV_Q4_K) dxs = dx * (float)(int)lds32(sp);
 #pragma unroll
       for (int r = 0; r < RW; r++) {
         float v = fmaf(sA[r] * dx, (float)dot(w[r], xa, xb), acc.v[r][0].x);
@@ -456,13 +492,14 @@ struct Consumer {
 #pragma unroll
       for (int t = 0; t < NT; t += 2) {
         if (t >= nt) break;  // slots without a token (a short MoE group, a last pass)
-        const uint4 xa0 = lds128(ap + t * ACT_BYTES);
-        const uint4 xb0 = lds128(ap + t * ACT_BYTES + 128);
-        const uint4 xa1 = lds128(ap + (t + 1) * ACT_BYTES);
-        const uint4 xb1 = lds128(ap + (t + 1) * ACT_BYTES + 128);
-        const float2 dx = lds_f2(ad + d_off + t * 128);
+        const uint4 xa0 = lds128(ap + t * sq);
+        const uint4 xb0 = lds128(ap + t * sq + 128);
+        const uint4 xa1 = lds128(ap + (t + 1) * sq);
+        const uint4 xb1 = lds128(ap + (t + 1) * sq + 128);
+        const float2 dx = make_float2(__uint_as_float(lds32(dp + t * sd)), __uint_as_float(lds32(dp + (t + 1) * sd)));
         float2 dxs = make_float2(0.f, 0.f);
-        if constexpr (F == QMV_Q4_K) dxs = lds_f2(ads + d_off + t * 128);
+        if constexpr (F == QMV_Q4_K)
+          dxs = __fmul2_rn(dx, make_float2((float)(int)lds32(sp + t * sd), (float)(int)lds32(sp + (t + 1) * sd)));
 #pragma unroll
         for (int r = 0; r < RW; r++) {
           const float2 is = make_float2((float)dot(w[r], xa0, xb0), (float)dot(w[r], xa1, xb1));
@@ -476,8 +513,8 @@ struct Consumer {
 
   // Exact int32 dot product of one 32-weight block with the activation words
   // xa (elements 0..15 of the block) and xb (16..31).  Q4_K: 16 x the sum
-  // (both nibble halves weigh 16; the staged d_x carries the 1/16).  With
-  // one token the two halves run as independent chains.
+  // (both nibble halves weigh 16; sA carries the 1/16).  With one token the
+  // two halves run as independent chains.
   __device__ __forceinline__ int dot(const uint32_t (&w)[8], uint4 xa, uint4 xb) const {
     if constexpr (F == QMV_Q4_K) {
       if constexpr (Q4K_LO16) {

@@ -101,8 +101,10 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
   a.carve(stages + p.stages * STAGE_BYTES, F, NT, p.act_nck);
   uint64_t* full = reinterpret_cast<uint64_t*>(stages + p.stages * STAGE_BYTES + act_area_bytes(F, NT, p.act_nck));
   uint64_t* empty = full + MAX_STAGES;
+  uint64_t* abar = full + 2 * MAX_STAGES;  // bulk copies of pre-quantized activations
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) mbar_init(abar, 1);
   init_pipeline(full, empty, p.stages);
   pdl_launch_dependents();
 
@@ -190,8 +192,10 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
   AccTile<NT> acc;
   acc.zero();
   const uint32_t stage_base = smem_u32(stages), aq_base = smem_u32(a.q), ad_base = smem_u32(a.d),
-                 ads_base = smem_u32(a.ds);
+                 as_base = smem_u32(a.s);
+  const uint32_t sq = p.act_nck * ACT_BYTES, sd = p.act_nck * 32 * 4;  // slot strides of the area
   const ActSource src{p.x, p.xq, p.xd, p.xs, p.K, nullptr, p.t0, nullptr, nullptr, nullptr};
+  uint32_t aphase = 0;
 
   while (walk.next(s, u, nu)) {
     int g0, g1;
@@ -199,7 +203,13 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
     const int kb0 = g0 * (GW / BLK), nblk = (g1 - g0) * (GW / BLK);
     if (s != staged_split) {
       named_sync(1, CONSUMER_THREADS);  // nobody still reads the previous range
-      stage_activations<F, NT>(src, kb0, nblk, p.nt, a, cw, lane);
+      if (p.x != nullptr) {
+        stage_activations<F, NT>(src, kb0, nblk, p.nt, a, cw, lane);
+      } else {
+        alive = __all_sync(FULL, stage_q8_bulk<F, NT>(src, kb0, nblk, p.nt, a, abar, aphase, p.err, cw, lane)) &&
+                alive;
+        aphase ^= 1;
+      }
       named_sync(1, CONSUMER_THREADS);
       staged_split = s;
     }
@@ -213,8 +223,8 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
         break;
       }
       if (cw * RW < nrows)
-        cons.chunk(stage_base + st * STAGE_BYTES + cw * RW * CB, aq_base + c * NT * ACT_BYTES,
-                   ad_base + c * NT * 32 * 4, ads_base + c * NT * 32 * 4, p.nt, acc);
+        cons.chunk(stage_base + st * STAGE_BYTES + cw * RW * CB, aq_base + c * ACT_BYTES, ad_base + c * 128,
+                   as_base + c * 128, sq, sd, p.nt, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }

@@ -5,27 +5,48 @@
 
 namespace qmv {
 
-// Activation rule over x [n_tok][K]: codes in natural order, per-32 scale d
-// and code sum s; one block per thread.
+// Activation rule over x [n_tok][K] into the library's Q8 activation layout:
+// the codes of each 256-element group in act_pos order, d and s per block in
+// order.  A warp quantizes SU groups per step, four lanes per block.  The
+// next kernel may launch at once (it streams weights); this one waits for its
+// predecessor before it reads x or writes q / d / s.
 __global__ void __launch_bounds__(256) act_quant_kernel(const float* __restrict__ x, int K, int n_tok,
                                                         int8_t* __restrict__ q, float* __restrict__ d,
                                                         int32_t* __restrict__ s) {
-  pdl_wait();
-  const long long total = (long long)K / 32 * n_tok;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    float4 v[8];
-    const float4* p = reinterpret_cast<const float4*>(x + i * 32);
-#pragma unroll
-    for (int k = 0; k < 8; k++) v[k] = __ldg(p + k);
-    const BlockQ b = quant_block(v);
-    uint4* o = reinterpret_cast<uint4*>(q + i * 32);
-    o[0] = make_uint4(b.w[0], b.w[1], b.w[2], b.w[3]);
-    o[1] = make_uint4(b.w[4], b.w[5], b.w[6], b.w[7]);
-    d[i] = b.d;
-    s[i] = b.s;
-  }
   pdl_launch_dependents();
+  pdl_wait();
+  constexpr int SU = 4;
+  const int lane = threadIdx.x & 31, sub = lane >> 2, li = lane & 3;
+  const long long groups = (long long)n_tok * (K / 256);
+  const long long nwarps = (long long)gridDim.x * (blockDim.x / 32);
+  for (long long g0 = ((long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5)) * SU; g0 < groups;
+       g0 += nwarps * SU) {
+    float4 v[SU][2];
+    uint32_t w0[SU], w1[SU];
+    float dd[SU];
+    int ss[SU];
+#pragma unroll
+    for (int u = 0; u < SU; u++) {
+      v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (g0 + u < groups) {
+        const float4* p = reinterpret_cast<const float4*>(x + (g0 + u) * 256 + sub * 32) + 2 * li;
+        v[u][0] = __ldg(p);
+        v[u][1] = __ldg(p + 1);
+      }
+    }
+    quant_units<SU>(v, w0, w1, dd, ss);
+#pragma unroll
+    for (int u = 0; u < SU; u++) {
+      if (g0 + u < groups) {
+        const long long g = g0 + u;
+        *reinterpret_cast<uint2*>(q + g * 256 + act_pos(sub, 8 * li)) = make_uint2(w0[u], w1[u]);
+        if (li == 0) {
+          d[g * 8 + sub] = dd[u];
+          s[g * 8 + sub] = ss[u];
+        }
+      }
+    }
+  }
 }
 
 // y[t][m] = sum_{s=0..S-1} partial[s][t][m], added in the fixed order of s.
@@ -122,8 +143,8 @@ void make_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, dim3 grid, 
 
 cudaError_t launch_act_quant(const float* x, int K, int n_tok, int8_t* q, float* d, int32_t* s,
                              cudaStream_t stream, bool pdl) {
-  const long long blocks = (long long)K / 32 * n_tok;
-  long long ctas = (blocks + 255) / 256;  // one block per thread
+  const long long groups = (long long)K / 256 * n_tok;
+  long long ctas = (groups + 31) / 32;  // 8 warps x 4 groups
   const long long cap = 8ll * device_sm_count();
   if (ctas > cap) ctas = cap;
   if (ctas < 1) ctas = 1;

@@ -107,3 +107,17 @@ def unpack_iq4_xs(g):
     ls = [[_get_bits(g, 8 * s + 2, 6 * j, 6) for j in range(8)] for s in range(2)]
     c = [[_get_codes(g, 16 + 128 * s + 16 * j) for j in range(8)] for s in range(2)]
     return d_bits, ls, c
+
+
+def q8_codes_natural(q):
+    """Codes of the library's Q8 activation layout [n][K] back in element
+    order.  Within every 256-element group (8 blocks of 32), element p of
+    block l is stored at (p // 16) * 128 + l * 16 + p % 16 (the first halves
+    of the 8 blocks, then the second halves), as include/qmv.h states."""
+    q = np.asarray(q)
+    n, K = q.shape
+    l = np.arange(8)[:, None]
+    p = np.arange(32)[None, :]
+    pos = ((p // 16) * 128 + l * 16 + p % 16).reshape(-1)   # natural index l * 32 + p -> stored position
+    g = q.reshape(n, K // 256, 256)
+    return g[:, :, pos].reshape(n, K)

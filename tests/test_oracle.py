@@ -437,3 +437,17 @@ def test_moe_given_h_reproduces_the_computed_path():
     a = oracle.moe(2, Wgu, 1, Wd, E, H, F, ids, gates, x)
     b = oracle.moe(2, Wgu, 1, Wd, E, H, F, ids, gates, x, h_in=a["h32"])
     assert np.array_equal(a["y"], b["y"]) and np.array_equal(a["hq"], b["hq"])
+
+
+def test_q8_code_order_helper_follows_the_stated_rule():
+    # the tests read the library's pre-quantized code order through this
+    # helper; build a stored array from the rule element by element
+    n, K = 2, 512
+    nat = (np.arange(n * K).reshape(n, K) % 251).astype(np.int64)
+    stored = np.zeros_like(nat)
+    for t in range(n):
+        for g in range(K // 256):
+            for l in range(8):
+                for p in range(32):
+                    stored[t, g * 256 + (p // 16) * 128 + l * 16 + p % 16] = nat[t, g * 256 + l * 32 + p]
+    assert np.array_equal(L.q8_codes_natural(stored), nat)
