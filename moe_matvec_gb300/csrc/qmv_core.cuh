@@ -568,6 +568,35 @@ constexpr int dense_min_blocks() {
   return NT <= 4 ? 2 : 1;
 }
 
+// Sums over the 32 lanes of V per-lane values v[0 .. V) (V a power of two),
+// as a butterfly: each of the first log2(V) steps (at most 5) exchanges half
+// of the values with the partner lane and keeps the other half, so the
+// values are spread over the lanes instead of each being reduced on its
+// own.  Afterwards v[0 .. max(V / 32, 1)) hold the sums of values idx, idx +
+// 1, ... (idx returned); for V < 32 the 32 / V lanes of a group hold the same
+// sums.  Unrolled by template, so every index is a constant.
+template <int V, int STEP>
+struct LaneButterfly {
+  static __device__ __forceinline__ void run(float (&v)[V], int lane, int& idx) {
+    constexpr int OFF = 16 >> STEP;
+    constexpr int CNT = (V >> STEP) > 1 ? (V >> STEP) : 1;  // values still held before this step
+    if constexpr (CNT > 1) {
+      constexpr int H = CNT / 2;
+      const bool up = (lane & OFF) != 0;
+#pragma unroll
+      for (int i = 0; i < H; i++) {
+        const float keep = up ? v[i + H] : v[i];
+        const float send = up ? v[i] : v[i + H];
+        v[i] = keep + __shfl_xor_sync(FULL, send, OFF);
+      }
+      if (up) idx += H;
+    } else {
+      v[0] += __shfl_xor_sync(FULL, v[0], OFF);
+    }
+    if constexpr (STEP < 4) LaneButterfly<V, STEP + 1>::run(v, lane, idx);
+  }
+};
+
 // Sum of v over the 32 lanes, returned in every lane.
 __device__ __forceinline__ float warp_sum(float v) {
   v += __shfl_xor_sync(FULL, v, 16);

@@ -232,17 +232,22 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
     if (!alive) continue;
     // reduce across lanes and store rows row0 + cw * RW + r
     float* out = p.out + (long long)s * p.ntot * p.M;
+    constexpr int V = RW * NT, HELD = V >= 32 ? V / 32 : 1;
+    float v[V];
 #pragma unroll
-    for (int r = 0; r < RW; r++) {
+    for (int r = 0; r < RW; r++)
 #pragma unroll
-      for (int t = 0; t < NT; t++) {
-        const float v = warp_sum(acc.get(r, t));
-        const int row = cw * RW + r;
-        if (lane == ((r * NT + t) & 31) && t < p.nt && row < nrows)
-          out[(long long)(p.t0 + t) * p.M + row0 + row] = v;
+      for (int t = 0; t < NT; t++) v[r * NT + t] = acc.get(r, t);
+    acc.zero();
+    int idx = 0;
+    LaneButterfly<V, 0>::run(v, lane, idx);
+    if (V >= 32 || (lane & (32 / V - 1)) == 0) {
+#pragma unroll
+      for (int i = 0; i < HELD; i++) {
+        const int o = idx + i, r = o / NT, t = o - r * NT, row = cw * RW + r;
+        if (t < p.nt && row < nrows) out[(long long)(p.t0 + t) * p.M + row0 + row] = v[i];
       }
     }
-    acc.zero();
   }
 }
 
