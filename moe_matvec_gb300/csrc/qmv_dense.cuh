@@ -42,6 +42,7 @@ struct DenseParams {
   int units;           // ceil(M / UNIT_ROWS)
   int stages;
   int act_nck;         // chunks of the activation area
+  int prefetch;        // L2 lookahead of the producer past the ring (iterations)
   unsigned* err;       // device error word
 };
 
@@ -114,7 +115,7 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
       prefetch_tensormap(&map_tile);
       prefetch_tensormap(&map_unit);
       const uint64_t pol = policy_evict_first();
-      // A cursor PREFETCH_STAGES iterations ahead of the ring requests tiles
+      // A cursor p.prefetch iterations ahead of the ring requests tiles
       // into L2, so the CTA's weights keep streaming from HBM while the
       // preceding grid finishes and while the consumers wait for it.
       struct Cursor {
@@ -154,7 +155,7 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
         split_range(p, s, g0, g1);
         const int nck = ((g1 - g0) * GW + KCHUNK - 1) / KCHUNK;
         for (int c = 0; c < nck; c++, ring.advance(p.stages)) {
-          if (ring.n >= p.stages) prefetch_to(ring.n + PREFETCH_STAGES);
+          if (ring.n >= p.stages) prefetch_to(ring.n + p.prefetch);
           if (!producer_acquire(empty, ring, p.stages, p.err)) {
             alive = false;
             break;
