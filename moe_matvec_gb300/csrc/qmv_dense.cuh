@@ -89,7 +89,10 @@ __device__ __forceinline__ void split_range(const DenseParams& p, int s, int& g0
   }
 }
 
-template <int F, int NT>
+// Q8IN: the activations come pre-quantized (bulk copies) instead of as fp32
+// rows quantized while staging; separate instantiations, so each kernel
+// carries only its own staging code.
+template <int F, int NT, bool Q8IN>
 __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
     qmv_dense_kernel(const __grid_constant__ CUtensorMap map_tile, const __grid_constant__ CUtensorMap map_unit,
                      const DenseParams p) {
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
     const int kb0 = g0 * (GW / BLK), nblk = (g1 - g0) * (GW / BLK);
     if (s != staged_split) {
       named_sync(1, CONSUMER_THREADS);  // nobody still reads the previous range
-      if (p.x != nullptr) {
+      if constexpr (!Q8IN) {
         stage_activations<F, NT>(src, kb0, nblk, p.nt, a, cw, lane);
       } else {
         alive = __all_sync(FULL, stage_q8_bulk<F, NT>(src, kb0, nblk, p.nt, a, abar, aphase, p.err, cw, lane)) &&
@@ -233,6 +236,21 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
     if (!alive) continue;
     // reduce across lanes and store rows row0 + cw * RW + r
     float* out = p.out + (long long)s * p.ntot * p.M;
+    if constexpr (NT <= 2) {
+      // few values per lane: one shuffle tree each
+#pragma unroll
+      for (int r = 0; r < RW; r++) {
+#pragma unroll
+        for (int t = 0; t < NT; t++) {
+          const float v = warp_sum(acc.get(r, t));
+          const int row = cw * RW + r;
+          if (lane == ((r * NT + t) & 31) && t < p.nt && row < nrows)
+            out[(long long)(p.t0 + t) * p.M + row0 + row] = v;
+        }
+      }
+      acc.zero();
+      continue;
+    }
     constexpr int V = RW * NT, HELD = V >= 32 ? V / 32 : 1;
     float v[V];
 #pragma unroll

@@ -6,9 +6,9 @@
 
 namespace qmv {
 
-template <int F, int NT>
+template <int F, int NT, bool Q8IN>
 static cudaError_t launch_dense_nt(const DenseLaunch& L) {
-  auto kern = qmv_dense_kernel<F, NT>;
+  auto kern = qmv_dense_kernel<F, NT, Q8IN>;
   static unsigned long long configured = 0;  // bit per device ordinal
   int dev = 0;
   cudaGetDevice(&dev);
@@ -27,16 +27,21 @@ static cudaError_t launch_dense_nt(const DenseLaunch& L) {
   return cudaLaunchKernelEx(&cfg, kern, L.map_tile, L.map_unit, *L.p);
 }
 
-template <int F>
-static cudaError_t launch_dense_fmt(const DenseLaunch& L) {
+template <int F, bool Q8IN>
+static cudaError_t launch_dense_src(const DenseLaunch& L) {
   switch (L.nt_tmpl) {
-    case 1: return launch_dense_nt<F, 1>(L);
-    case 2: return launch_dense_nt<F, 2>(L);
-    case 4: return launch_dense_nt<F, 4>(L);
-    case 8: return launch_dense_nt<F, 8>(L);
-    case 16: return launch_dense_nt<F, 16>(L);
+    case 1: return launch_dense_nt<F, 1, Q8IN>(L);
+    case 2: return launch_dense_nt<F, 2, Q8IN>(L);
+    case 4: return launch_dense_nt<F, 4, Q8IN>(L);
+    case 8: return launch_dense_nt<F, 8, Q8IN>(L);
+    case 16: return launch_dense_nt<F, 16, Q8IN>(L);
   }
   return cudaErrorInvalidValue;
+}
+
+template <int F>
+static cudaError_t launch_dense_fmt(const DenseLaunch& L) {
+  return L.p->x != nullptr ? launch_dense_src<F, false>(L) : launch_dense_src<F, true>(L);
 }
 
 }  // namespace qmv
