@@ -315,26 +315,57 @@ __global__ void __launch_bounds__(THREADS, 1)
     alive = __all_sync(FULL, alive);
     if (!alive) continue;
     const int row0 = u * UNIT_ROWS;
+    if constexpr (NT <= 2) {
+      // few values per lane: one shuffle tree each
 #pragma unroll
-    for (int t = 0; t < NT; t++) {
-      if (t >= nt) break;  // slots of this group without a token
-      if constexpr (MODE == MOE_GATE_UP) {
+      for (int t = 0; t < NT; t++) {
+        if (t >= nt) break;  // slots of this group without a token
+        if constexpr (MODE == MOE_GATE_UP) {
 #pragma unroll
-        for (int i = 0; i < 2; i++) {
-          const float g = warp_sum(acc.get(i, t));
-          const float v = warp_sum(acc.get(2 + i, t));
-          const int j = 2 * cw + i;
-          if (lane == ((2 * t + i) & 31) && j < nvalid) {
-            const float h = g / (1.0f + expf(-g)) * v;
-            p.dst[(long long)rt.slots[first + t] * p.R + row0 + j] = h;
+          for (int i = 0; i < 2; i++) {
+            const float g = warp_sum(acc.get(i, t));
+            const float v = warp_sum(acc.get(2 + i, t));
+            const int j = 2 * cw + i;
+            if (lane == ((2 * t + i) & 31) && j < nvalid) {
+              const float h = g / (1.0f + expf(-g)) * v;
+              p.dst[(long long)rt.slots[first + t] * p.R + row0 + j] = h;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < RW; r++) {
+            const float v = warp_sum(acc.get(r, t));
+            if (lane == ((r * NT + t) & 31) && roff[r] < nvalid)
+              p.dst[(long long)rt.slots[first + t] * p.R + row0 + roff[r]] = v;
           }
         }
-      } else {
+      }
+    } else {
+      // butterfly over all RW x NT values; value r * NT + t ends in lane
+      // group idx.  GATE_UP: rows 0, 1 are gate, rows 2, 3 the matching up
+      // rows, so each up sum lies 16 lanes above its gate sum.
+      constexpr int V = RW * NT, HELD = V >= 32 ? V / 32 : 1;
+      float v[V];
 #pragma unroll
-        for (int r = 0; r < RW; r++) {
-          const float v = warp_sum(acc.get(r, t));
-          if (lane == ((r * NT + t) & 31) && roff[r] < nvalid)
-            p.dst[(long long)rt.slots[first + t] * p.R + row0 + roff[r]] = v;
+      for (int r = 0; r < RW; r++)
+#pragma unroll
+        for (int t = 0; t < NT; t++) v[r * NT + t] = acc.get(r, t);
+      int idx = 0;
+      LaneButterfly<V, 0>::run(v, lane, idx);
+      const bool lead = V >= 32 || (lane & (32 / V - 1)) == 0;
+#pragma unroll
+      for (int i = 0; i < HELD; i++) {
+        const int o = idx + i, r = o / NT, t = o - r * NT;
+        if constexpr (MODE == MOE_GATE_UP) {
+          const float up = __shfl_down_sync(FULL, v[i], 16);
+          const int j = 2 * cw + r;
+          if (lead && lane < 16 && t < nt && j < nvalid) {
+            const float g = v[i];
+            p.dst[(long long)rt.slots[first + t] * p.R + row0 + j] = g / (1.0f + expf(-g)) * up;
+          }
+        } else {
+          if (lead && t < nt && roff[r] < nvalid)
+            p.dst[(long long)rt.slots[first + t] * p.R + row0 + roff[r]] = v[i];
         }
       }
     }
