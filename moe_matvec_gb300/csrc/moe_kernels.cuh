@@ -143,7 +143,7 @@ struct MoeWalk {
 };
 
 template <int F, int NT, int MODE>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, NT <= 4 ? 2 : 1)
     moe_qmv_kernel(const __grid_constant__ CUtensorMap map_tile, const __grid_constant__ CUtensorMap map_unit,
                    const MoeParams p) {
   constexpr int CB = chunk_bytes<F>();

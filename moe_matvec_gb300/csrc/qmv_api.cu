@@ -301,7 +301,7 @@ static int run_moe_proj(int mode, int fmt, const void* pool, MoeParams& p, int n
     return QMV_ERR_SHAPE;
   L.p = &p;
   L.nt_tmpl = nt;
-  L.grid = device_sm_count();
+  L.grid = device_sm_count() * (nt <= 4 && smem <= TWO_PER_SM_BYTES ? 2 : 1);
   L.smem = smem - static_bytes;
   L.stream = stream;
   L.pdl = true;
