@@ -51,6 +51,8 @@ struct MoeRouting {
   int pair_expert[MOE_MAX_SLOTS];            // per (expert, token group)
   int pair_first[MOE_MAX_SLOTS];
   int pair_count[MOE_MAX_SLOTS];
+  int pair_cost[MOE_MAX_SLOTS + 1];          // prefix sums of the groups' work weights
+                                             // (< 512 x 2^17 units x 22 < 2^31)
   int n_pairs;
 };
 
@@ -66,7 +68,8 @@ __device__ __forceinline__ int slot_status(const int32_t* ids, int top_k, int E,
 }
 
 // Build the expert groups (called by all threads of the CTA).
-__device__ __forceinline__ void build_routing(MoeRouting& rt, const MoeParams& p, int nt_group, bool report) {
+__device__ __forceinline__ void build_routing(MoeRouting& rt, const MoeParams& p, int nt_group, bool report,
+                                              int unit_base, int units_per_pair) {
   const int S = p.n_tok * p.top_k;
   const int E = p.n_experts;
   for (int e = threadIdx.x; e < E; e += blockDim.x) rt.mask[e] = 0ull;
@@ -117,27 +120,80 @@ __device__ __forceinline__ void build_routing(MoeRouting& rt, const MoeParams& p
       rt.slots[rt.off[e] + rank] = s;
     }
   }
+  // work weight of a group per 8-row unit: its decode (unit_base) plus one
+  // per token slot it computes (slots go in pairs from two on)
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    long long carry = 0;
+    if (lane == 0) rt.pair_cost[0] = 0;
+    for (int base = 0; base < rt.n_pairs; base += 32) {
+      const int q = base + lane;
+      long long w = 0;
+      if (q < rt.n_pairs) {
+        const int c = rt.pair_count[q];
+        w = (long long)(unit_base + (nt_group >= 2 ? (c + 1) & ~1 : c)) * units_per_pair;
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long a = __shfl_up_sync(FULL, w, o);
+        if (lane >= o) w += a;
+      }
+      if (q < rt.n_pairs) rt.pair_cost[q + 1] = (int)(carry + w);
+      carry += __shfl_sync(FULL, w, 31);
+    }
+  }
   __syncthreads();
 }
 
-// Walk over the flattened (pair, unit) space of this CTA.
+// Walk over this CTA's part of the flattened (pair, unit) space.  The parts
+// are cut by work, not by units: a unit of a group that computes more token
+// slots weighs more (pair_cost), so CTAs end together.  A cut at work
+// position P falls on the first unit that starts at or after P; every CTA
+// computes the same cuts.
 struct MoeWalk {
   long long f, f_end;
-  int units, tile_units;
-  __device__ MoeWalk(int n_pairs, int units_per_pair, int tile_units_) {
-    const long long total = (long long)n_pairs * units_per_pair;
-    f = total * blockIdx.x / gridDim.x;
-    f_end = total * (blockIdx.x + 1) / gridDim.x;
+  int units, tile_units, q, u;  // pair and unit at f
+  __device__ static long long locate(const MoeRouting& rt, int units, long long P) {
+    int lo = 0, hi = rt.n_pairs;  // pair lo with pair_cost[lo] <= P < pair_cost[lo + 1]
+    if (P >= rt.pair_cost[hi]) return (long long)hi * units;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (rt.pair_cost[mid] <= P)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    const long long d = P - rt.pair_cost[lo];
+    const long long w = (rt.pair_cost[lo + 1] - rt.pair_cost[lo]) / units;  // weight of one unit
+    const long long uu = w < (1ll << 31) && d < (1ll << 31) ? (long long)(((unsigned)d + (unsigned)w - 1u) / (unsigned)w)
+                                                           : (d + w - 1) / w;
+    return (long long)lo * units + uu;
+  }
+  __device__ MoeWalk(const MoeRouting& rt, int units_per_pair, int tile_units_) {
+    const long long C = rt.pair_cost[rt.n_pairs];
     units = units_per_pair;
     tile_units = tile_units_;
-  }
-  __device__ bool next(int& q, int& u, int& nu) {
-    if (f >= f_end) return false;
+    const unsigned G = gridDim.x, b = blockIdx.x;
+    // C * b / G in 64 bits without a 64-bit division when C fits in 32 bits
+    const long long P0 = C < (1ll << 32) ? (long long)(((unsigned long long)C * b) / G) : C * b / G;
+    const long long P1 = C < (1ll << 32) ? (long long)(((unsigned long long)C * (b + 1)) / G) : C * (b + 1) / G;
+    f = locate(rt, units, P0);
+    f_end = locate(rt, units, P1);
     q = (int)(f / units);
     u = (int)(f - (long long)q * units);
+  }
+  __device__ bool next(int& tq, int& tu, int& nu) {
+    if (f >= f_end) return false;
+    tq = q;
+    tu = u;
     const long long lim = f_end - f;
     nu = (int)min((long long)min(tile_units, units - u), lim);
     f += nu;
+    u += nu;
+    if (u == units) {
+      u = 0;
+      q++;
+    }
     return true;
   }
 };
@@ -169,8 +225,10 @@ __global__ void __launch_bounds__(THREADS, NT <= 4 ? 2 : 1)
   // after every GATE_UP CTA passed that wait, so its ids are complete.
   if (MODE == MOE_GATE_UP) pdl_wait();
   pdl_launch_dependents();
-  build_routing(rt, p, NT, MODE == MOE_GATE_UP && blockIdx.x == 0);
   const int units_per_pair = p.R / UNIT_ROWS;
+  // decode work of one unit relative to one token slot of it
+  constexpr int UNIT_BASE = F == QMV_IQ4_XS ? 6 : (F == QMV_Q4_K ? 2 : 1);
+  build_routing(rt, p, NT, MODE == MOE_GATE_UP && blockIdx.x == 0, UNIT_BASE, units_per_pair);
   const int nck = (p.K + KCHUNK - 1) / KCHUNK;
 
   if (warp == CONSUMER_WARPS) {
@@ -182,7 +240,7 @@ __global__ void __launch_bounds__(THREADS, NT <= 4 ? 2 : 1)
       // L2 lookahead of PREFETCH_STAGES iterations past the ring (see the
       // dense kernel): the expert rows keep streaming while the consumers
       // stage activations or wait for the preceding grid.
-      MoeWalk pw(rt.n_pairs, units_per_pair, TILE_UNITS);
+      MoeWalk pw(rt, units_per_pair, TILE_UNITS);
       int pq = 0, pu = 0, pnu = 0, pc = 0;
       bool pvalid = pw.next(pq, pu, pnu);
       long long pf_n = 0;
@@ -208,7 +266,7 @@ __global__ void __launch_bounds__(THREADS, NT <= 4 ? 2 : 1)
           }
         }
       };
-      MoeWalk walk(rt.n_pairs, units_per_pair, TILE_UNITS);
+      MoeWalk walk(rt, units_per_pair, TILE_UNITS);
       int q, u, nu;
       Ring ring;
       bool alive = true;
@@ -251,7 +309,7 @@ __global__ void __launch_bounds__(THREADS, NT <= 4 ? 2 : 1)
   if (MODE == MOE_DOWN) pdl_wait();  // h comes from the preceding kernel
   const int cw = warp;
   bool alive = true;
-  MoeWalk walk(rt.n_pairs, units_per_pair, TILE_UNITS);
+  MoeWalk walk(rt, units_per_pair, TILE_UNITS);
   int q, u, nu;
   Ring ring;
   int staged_pair = -1, nt = 0, first = 0;
