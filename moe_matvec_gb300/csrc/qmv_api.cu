@@ -129,7 +129,8 @@ constexpr int TWO_PER_SM_STAGES = 4;
 // overlap under programmatic dependent launch) with a short ring; otherwise
 // one CTA per SM with a deeper ring.
 static bool plan_stages(int nt, size_t act, int stage_bytes, size_t budget, int& stages, size_t& smem) {
-  const size_t fixed = act + 2 * MAX_STAGES * sizeof(uint64_t) + 128;
+  // mbarriers (full, empty, 2 more) and the cross-warp sums of thin tiles
+  const size_t fixed = act + 2 * MAX_STAGES * sizeof(uint64_t) + 128 + CONSUMER_WARPS * RW * 16 * sizeof(float);
   if (nt <= 4 && fixed + 2 * (size_t)stage_bytes <= TWO_PER_SM_BYTES) {
     int st = (int)((TWO_PER_SM_BYTES - fixed) / stage_bytes);
     stages = st > TWO_PER_SM_STAGES ? TWO_PER_SM_STAGES : st;

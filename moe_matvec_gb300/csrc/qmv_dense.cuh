@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
   uint64_t* full = reinterpret_cast<uint64_t*>(stages + p.stages * STAGE_BYTES + act_area_bytes(F, NT, p.act_nck));
   uint64_t* empty = full + MAX_STAGES;
   uint64_t* abar = full + 2 * MAX_STAGES;  // bulk copies of pre-quantized activations
+  float* red = reinterpret_cast<float*>(abar + 2);  // [CONSUMER_WARPS][RW * NT]: cross-warp sums of thin tiles
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) mbar_init(abar, 1);
@@ -220,50 +221,71 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
     const long long row0 = (long long)u * UNIT_ROWS;
     const int nrows = (int)min((long long)nu * UNIT_ROWS, p.M - row0);
     const int nck = (nblk * BLK + KCHUNK - 1) / KCHUNK;
+    // Thin tiles (one or two units) would leave most warps without rows:
+    // there the tile's 2 * nu row groups of RW rows are each taken by ks
+    // warps, warp part k working on the chunks c with c mod ks == k, and the
+    // parts are added across warps (in part order) before the store.
+    const int ks = nu == 1 ? 4 : (nu == 2 ? 2 : 1);
+    const int rg = CONSUMER_WARPS / ks;  // warps per part (row groups with rows: 2 * nu)
+    const int grp = cw % rg, part = cw / rg;
     for (int c = 0; c < nck && alive; c++, ring.advance(p.stages)) {
       const int st = ring.st;
       if (!mbar_wait(&full[st], ring.parity(), p.err)) {
         alive = false;
         break;
       }
-      if (cw * RW < nrows)
-        cons.chunk(stage_base + st * STAGE_BYTES + cw * RW * CB, aq_base + c * ACT_BYTES, ad_base + c * 128,
+      if (grp * RW < nrows && (c & (ks - 1)) == part)  // ks is 1, 2 or 4
+        cons.chunk(stage_base + st * STAGE_BYTES + grp * RW * CB, aq_base + c * ACT_BYTES, ad_base + c * 128,
                    as_base + c * 128, sq, sd, p.nt, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
     alive = __all_sync(FULL, alive);
     if (!alive) continue;
-    // reduce across lanes and store rows row0 + cw * RW + r
+    // reduce across lanes and store rows row0 + grp * RW + r
     float* out = p.out + (long long)s * p.ntot * p.M;
-    if constexpr (NT <= 2) {
-      // few values per lane: one shuffle tree each
-#pragma unroll
-      for (int r = 0; r < RW; r++) {
-#pragma unroll
-        for (int t = 0; t < NT; t++) {
-          const float v = warp_sum(acc.get(r, t));
-          const int row = cw * RW + r;
-          if (lane == ((r * NT + t) & 31) && t < p.nt && row < nrows)
-            out[(long long)(p.t0 + t) * p.M + row0 + row] = v;
-        }
-      }
-      acc.zero();
-      continue;
-    }
     constexpr int V = RW * NT, HELD = V >= 32 ? V / 32 : 1;
     float v[V];
-#pragma unroll
-    for (int r = 0; r < RW; r++)
-#pragma unroll
-      for (int t = 0; t < NT; t++) v[r * NT + t] = acc.get(r, t);
-    acc.zero();
     int idx = 0;
-    LaneButterfly<V, 0>::run(v, lane, idx);
-    if (V >= 32 || (lane & (32 / V - 1)) == 0) {
+    bool lead;  // this lane holds sums idx .. idx + HELD - 1 (V >= 32: all lanes)
+    if constexpr (NT <= 2) {
+      // few values per lane: one shuffle tree each; lane o keeps sum o
+#pragma unroll
+      for (int r = 0; r < RW; r++)
+#pragma unroll
+        for (int t = 0; t < NT; t++) {
+          const float w = warp_sum(acc.get(r, t));
+          if (lane == r * NT + t) v[0] = w;
+        }
+      idx = lane;
+      lead = lane < V;
+    } else {
+#pragma unroll
+      for (int r = 0; r < RW; r++)
+#pragma unroll
+        for (int t = 0; t < NT; t++) v[r * NT + t] = acc.get(r, t);
+      LaneButterfly<V, 0>::run(v, lane, idx);
+      lead = V >= 32 || (lane & (32 / V - 1)) == 0;
+    }
+    acc.zero();
+    if (ks > 1) {
+      if (lead)
+#pragma unroll
+        for (int i = 0; i < HELD; i++) red[cw * V + idx + i] = v[i];
+      named_sync(2, CONSUMER_THREADS);
+      if (part == 0 && lead)
+#pragma unroll
+        for (int i = 0; i < HELD; i++) {
+          float w = red[grp * V + idx + i];
+          for (int k = 1; k < ks; k++) w += red[(k * rg + grp) * V + idx + i];
+          v[i] = w;
+        }
+      named_sync(2, CONSUMER_THREADS);  // red is free for the next tile
+    }
+    if (part == 0 && lead) {
 #pragma unroll
       for (int i = 0; i < HELD; i++) {
-        const int o = idx + i, r = o / NT, t = o - r * NT, row = cw * RW + r;
+        const int o = idx + i, r = o / NT, t = o - r * NT, row = grp * RW + r;
         if (t < p.nt && row < nrows) out[(long long)(p.t0 + t) * p.M + row0 + row] = v[i];
       }
     }
