@@ -500,6 +500,33 @@ def run_extra(torch, api, synth, stream, dev, peak):
     return out
 
 
+def run_profile_moe(args):
+    """Two eager MoE decode calls at --profile-moe tokens (for ncu captures)."""
+    import torch
+    from moe_matvec_gb300 import api, synth
+    api.load()
+    n = args.profile_moe
+    c = synth.MOE_CASE
+    g = torch.Generator(device="cuda")
+    g.manual_seed(2200)
+    H, F, E = c.hidden, c.ffn, c.n_experts
+    wg = torch.empty((E, 2 * F, api.row_bytes(c.fmt_gate_up, H)), dtype=torch.uint8, device="cuda")
+    wd = torch.empty((E, H, api.row_bytes(c.fmt_down, F)), dtype=torch.uint8, device="cuda")
+    for e in range(E):
+        wg[e] = api.quantize_weights(c.fmt_gate_up, torch.randn((2 * F, H), generator=g, device="cuda") * 0.02)
+        wd[e] = api.quantize_weights(c.fmt_down, torch.randn((H, F), generator=g, device="cuda") * 0.02)
+    ex = api.moe_experts(E, H, F, c.fmt_gate_up, c.fmt_down, wg, wd)
+    x = torch.from_numpy(synth.activations(2400 + n, n, H)).cuda()
+    y = torch.empty((n, H), device="cuda")
+    ws = torch.empty(api.moe_workspace_bytes(ex, n, c.top_k), dtype=torch.uint8, device="cuda")
+    for k in range(2):
+        a, b = synth.routing(2300 + 17 * n + k, n, E, c.top_k)
+        api.moe_run(ex, torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda(), x, ws=ws, out=y)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_run": "moe_128x_top8_h4096_f1536", "n_tok": n, "calls": 2}))
+    return 0
+
+
 def run_profile(args):
     """A few eager calls of the timed workload (for ncu captures)."""
     import torch
@@ -528,11 +555,14 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--profile", action="store_true", help="a few eager calls only (for ncu)")
+    ap.add_argument("--profile-moe", type=int, default=0, help="two eager MoE calls at this many tokens (for ncu)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile_moe:
+        return run_profile_moe(args)
     if args.profile:
         return run_profile(args)
     return run_ours(args)
