@@ -318,7 +318,6 @@ __global__ void __launch_bounds__(THREADS, NT <= 4 ? 2 : 1)
   acc.zero();
   const uint32_t stage_base = smem_u32(stages), aq_base = smem_u32(a.q), ad_base = smem_u32(a.d),
                  as_base = smem_u32(a.s);
-  const uint32_t sq = p.act_nck * ACT_BYTES, sd = p.act_nck * 32 * 4;  // slot strides of the area
   int roff[RW];  // stage row of each of the warp's rows
   if constexpr (MODE == MOE_GATE_UP) {
     roff[0] = 2 * cw;
@@ -364,8 +363,8 @@ __global__ void __launch_bounds__(THREADS, NT <= 4 ? 2 : 1)
         // GATE_UP: rows (2cw, 2cw + 1) of the gate half and the same of the
         // up half, 16 rows apart; DOWN: 4 consecutive rows
         constexpr int PS = (MODE == MOE_GATE_UP ? 16 : 2) * CB;
-        cons.template chunk<PS>(stage_base + st * STAGE_BYTES + roff[0] * CB, aq_base + c * ACT_BYTES,
-                                ad_base + c * 128, as_base + c * 128, sq, sd, nt, acc);
+        cons.template chunk<PS>(stage_base + st * STAGE_BYTES + roff[0] * CB, aq_base + c * NT * ACT_BYTES,
+                                ad_base + c * NT * 128, as_base + c * NT * 128, nt, acc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);

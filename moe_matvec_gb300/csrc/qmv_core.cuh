@@ -40,28 +40,31 @@ __device__ __forceinline__ int act_pos(int l, int p) {
   return (l >> 3) * 256 + (p >> 4) * 128 + (l & 7) * 16 + (p & 15);
 }
 
-// Activation area of nt_slots token slots over nck chunks, per slot:
-//   codes  nck * 1024 bytes (each 256-element group in act_pos order),
-//   scales nck * 32 fp32 d (block order),
-//   sums   nck * 32 int32 s (Q4_K only: its min term needs them).
-// This is also the order of the library's pre-quantized activation rows
-// (codes) and of their scale / sum rows, so those arrive by bulk copies.
+// Activation area of nt_slots token slots over nck chunks, chunk-major:
+//   codes  [chunk][slot] 1024 bytes (each 256-element group in act_pos order),
+//   scales [chunk][slot] 32 fp32 d (block order),
+//   sums   [chunk][slot] 32 int32 s (Q4_K only: its min term needs them),
+// so that within a chunk every slot sits at a fixed offset.  A slot's chunk
+// of codes, scales or sums is one contiguous piece of the library's
+// pre-quantized activation rows, so those arrive by bulk copies.
 __host__ __device__ constexpr size_t act_area_bytes(int F, int nt_slots, int nck) {
   return (size_t)nck * nt_slots * (ACT_BYTES + 32 * sizeof(float) * (F == QMV_Q4_K ? 2 : 1));
 }
 
 struct ActArea {
-  uint8_t* q;  // [slot][nck * 1024]
-  float* d;    // [slot][nck * 32]
-  int32_t* s;  // [slot][nck * 32]
-  int nck;
-  __device__ void carve(uint8_t* base, int F, int nt_slots, int nck_) {
-    nck = nck_;
+  uint8_t* q;  // [nck][ns][1024]
+  float* d;    // [nck][ns][32]
+  int32_t* s;  // [nck][ns][32]
+  int ns;      // slots per chunk
+  __device__ void carve(uint8_t* base, int F, int nt_slots, int nck) {
+    ns = nt_slots;
     q = base;
     d = reinterpret_cast<float*>(base + (size_t)nck * nt_slots * ACT_BYTES);
     s = reinterpret_cast<int32_t*>(d + (size_t)nck * nt_slots * 32);
     (void)F;
   }
+  __device__ __forceinline__ uint8_t* codes(int c, int t) const { return q + ((size_t)c * ns + t) * ACT_BYTES; }
+  __device__ __forceinline__ int scale(int c, int t) const { return (c * ns + t) * 32; }
 };
 
 // Where the activation rows come from: fp32 rows (quantized while staging)
@@ -233,9 +236,9 @@ __device__ __forceinline__ void stage_activations(const ActSource& src, int kb0,
     }
 #pragma unroll
     for (int u = 0; u < SU; u++) {
-      store_codes<F>(a.q + ((size_t)tt[u] * a.nck + cc[u]) * ACT_BYTES, l[u], li, w0[u], w1[u]);
+      store_codes<F>(a.codes(cc[u], tt[u]), l[u], li, w0[u], w1[u]);
       if (li == 0) {
-        const int di = (tt[u] * a.nck + cc[u]) * 32 + l[u];
+        const int di = a.scale(cc[u], tt[u]) + l[u];
         a.d[di] = dd[u];
         if constexpr (F == QMV_Q4_K) a.s[di] = ss[u];
       }
@@ -244,45 +247,48 @@ __device__ __forceinline__ void stage_activations(const ActSource& src, int kb0,
 }
 
 // Pre-quantized activations (the library's layout) of blocks [kb0, kb0 +
-// nblk) of tokens [0, nt), brought into the area by bulk copies: per token
-// the codes, the scales and (Q4_K) the sums are contiguous in global memory
-// and land contiguous in the slot.  Warp 0 issues them (its lane 0 first
-// posts the byte count on `bar`); every consumer zeroes the scales past
-// nblk of the last chunk meanwhile, waits for `bar` (phase `parity`) and,
-// for IQ4_XS, reorders each block's codes into the interleaved order its
-// decode reads.  Returns false (timeout bit set) if the copies never land.
+// nblk) of tokens [0, nt), brought into the area by bulk copies, one per
+// (token, chunk) and kind (codes, scales, Q4_K sums): each is one contiguous
+// piece in global memory and in the area.  Lane 0 of warp 0 first posts the
+// byte count on `bar`; then every consumer thread issues its share of the
+// copies, zeroes the scales past nblk of the last chunk, waits for `bar`
+// (phase `parity`) and, for IQ4_XS, reorders each block's codes into the
+// interleaved order its decode reads.  Returns false (timeout bit set) if
+// the copies never land.
 template <int F, int NT>
 __device__ __forceinline__ bool stage_q8_bulk(const ActSource& src, int kb0, int nblk, int nt, const ActArea& a,
                                               uint64_t* bar, uint32_t parity, unsigned* err, int cw, int lane) {
   constexpr int NCOPY = F == QMV_Q4_K ? 3 : 2;
   const int nck = (nblk + 31) / 32;
-  if (cw == 0) {
-    if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nt * nblk * (32 + 4 * (NCOPY - 1))));
-    __syncwarp();
-    for (int i = lane; i < nt * NCOPY; i += 32) {
-      const int t = i / NCOPY, k = i - t * NCOPY;
-      const long long row = src.row(t);
+  if (cw == 0 && lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nt * nblk * (32 + 4 * (NCOPY - 1))));
+  named_sync(1, CONSUMER_THREADS);  // the byte count is posted before any copy completes
+  {
+    // one copy per (token, chunk, kind): codes, scales, sums; spread over all consumer threads
+    for (int i = cw * 32 + lane; i < nt * nck * NCOPY; i += CONSUMER_THREADS) {
+      const int t = i / (nck * NCOPY), r = i - t * nck * NCOPY, c = r / NCOPY, k = r - c * NCOPY;
+      const int nb = min(32, nblk - c * 32);
+      const long long row = src.row(t), b0 = (long long)kb0 + c * 32;  // first block of the piece
       if (k == 0)
-        bulk_copy_g2s(a.q + (size_t)t * a.nck * ACT_BYTES, src.xq + row * src.ld + (long long)kb0 * 32,
-                      (uint32_t)nblk * 32, bar);
+        bulk_copy_g2s(a.codes(c, t), src.xq + row * src.ld + b0 * 32, (uint32_t)nb * 32, bar);
       else if (k == 1)
-        bulk_copy_g2s(a.d + (size_t)t * a.nck * 32, src.xd + row * (src.ld / 32) + kb0, (uint32_t)nblk * 4, bar);
+        bulk_copy_g2s(a.d + a.scale(c, t), src.xd + row * (src.ld / 32) + b0, (uint32_t)nb * 4, bar);
       else
-        bulk_copy_g2s(a.s + (size_t)t * a.nck * 32, src.xs + row * (src.ld / 32) + kb0, (uint32_t)nblk * 4, bar);
+        bulk_copy_g2s(a.s + a.scale(c, t), src.xs + row * (src.ld / 32) + b0, (uint32_t)nb * 4, bar);
     }
   }
-  const int tail = nck * 32 - nblk;
+  // scales (and sums) of the blocks past nblk in the last chunk: zero
+  const int nb_last = nblk - (nck - 1) * 32, tail = 32 - nb_last;
   for (int i = cw * 32 + lane; i < nt * tail; i += CONSUMER_THREADS) {
-    const int t = i / tail, b = nblk + (i - t * tail);
-    a.d[t * a.nck * 32 + b] = 0.f;
-    if constexpr (F == QMV_Q4_K) a.s[t * a.nck * 32 + b] = 0;
+    const int t = i / tail, b = nb_last + (i - t * tail);
+    a.d[a.scale(nck - 1, t) + b] = 0.f;
+    if constexpr (F == QMV_Q4_K) a.s[a.scale(nck - 1, t) + b] = 0;
   }
   const bool ok = mbar_wait(bar, parity, err);
   if constexpr (F == QMV_IQ4_XS) {
     // x_0..15 and x_16..31 of a block sit in two 16-byte pieces; interleave
     for (int i = cw * 32 + lane; i < nt * nck * 32; i += CONSUMER_THREADS) {
       const int t = i / (nck * 32), r = i - t * nck * 32, c = r >> 5, l = r & 31;
-      uint8_t* chunk = a.q + ((size_t)t * a.nck + c) * ACT_BYTES;
+      uint8_t* chunk = a.codes(c, t);
       uint4* p0 = reinterpret_cast<uint4*>(chunk + act_pos(l, 0));
       uint4* p1 = reinterpret_cast<uint4*>(chunk + act_pos(l, 16));
       const uint4 lo = *p0, hi = *p1;
@@ -407,12 +413,14 @@ struct Consumer {
   // starts at row0 + (r & 1) * chunk_bytes + (r >> 1) * PAIR_STRIDE (rows in
   // pairs: consecutive rows use PAIR_STRIDE = 2 * chunk_bytes).  aq / ad /
   // as: shared addresses of this chunk's activation codes / scales / sums in
-  // token slot 0; slot t is sq (codes) or sd (scales, sums) bytes further.
+  // token slot 0; slot t is t * 1024 (codes) or t * 128 (scales, sums) bytes
+  // further.
   // nt: slots holding tokens (the accumulators of the others are left as
   // they are).
   template <int PAIR_STRIDE = 2 * chunk_bytes<F>()>
-  __device__ __forceinline__ void chunk(uint32_t row0, uint32_t aq, uint32_t ad, uint32_t as, uint32_t sq,
-                                        uint32_t sd, int nt, AccTile<NT>& acc) const {
+  __device__ __forceinline__ void chunk(uint32_t row0, uint32_t aq, uint32_t ad, uint32_t as, int nt,
+                                        AccTile<NT>& acc) const {
+    constexpr uint32_t sq = ACT_BYTES, sd = 32 * 4;
     constexpr int CB = chunk_bytes<F>();
     uint32_t w[RW][8];  // decoded operands, paired with activation words 0..7
     float sA[RW];       // multiplier of d_x * isum

@@ -198,7 +198,6 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
   acc.zero();
   const uint32_t stage_base = smem_u32(stages), aq_base = smem_u32(a.q), ad_base = smem_u32(a.d),
                  as_base = smem_u32(a.s);
-  const uint32_t sq = p.act_nck * ACT_BYTES, sd = p.act_nck * 32 * 4;  // slot strides of the area
   const ActSource src{p.x, p.xq, p.xd, p.xs, p.K, nullptr, p.t0, nullptr, nullptr, nullptr};
   uint32_t aphase = 0;
 
@@ -235,8 +234,8 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
         break;
       }
       if (grp * RW < nrows && (c & (ks - 1)) == part)  // ks is 1, 2 or 4
-        cons.chunk(stage_base + st * STAGE_BYTES + grp * RW * CB, aq_base + c * ACT_BYTES, ad_base + c * 128,
-                   as_base + c * 128, sq, sd, p.nt, acc);
+        cons.chunk(stage_base + st * STAGE_BYTES + grp * RW * CB, aq_base + c * NT * ACT_BYTES,
+                   ad_base + c * NT * 128, as_base + c * NT * 128, p.nt, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
