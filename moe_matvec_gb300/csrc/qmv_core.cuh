@@ -174,7 +174,7 @@ __device__ __forceinline__ void store_codes(uint8_t* chunk, int l, int li, uint3
 template <int F, int NT>
 __device__ __forceinline__ void stage_activations(const ActSource& src, int kb0, int nblk, int nt, const ActArea& a,
                                                   int cw, int lane) {
-  constexpr int SU = 4;
+  constexpr int SU = NT >= 8 ? 8 : 4;
   const int sub = lane >> 2, li = lane & 3;
   const int nck = (nblk + 31) / 32;
   int sh = 0;

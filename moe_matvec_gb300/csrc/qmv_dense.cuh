@@ -194,8 +194,6 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
   Ring ring;
   int staged_split = -1;
   const Consumer<F, NT> cons(lane);
-  AccTile<NT> acc;
-  acc.zero();
   const uint32_t stage_base = smem_u32(stages), aq_base = smem_u32(a.q), ad_base = smem_u32(a.d),
                  as_base = smem_u32(a.s);
   const ActSource src{p.x, p.xq, p.xd, p.xs, p.K, nullptr, p.t0, nullptr, nullptr, nullptr};
@@ -220,6 +218,8 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
     const long long row0 = (long long)u * UNIT_ROWS;
     const int nrows = (int)min((long long)nu * UNIT_ROWS, p.M - row0);
     const int nck = (nblk * BLK + KCHUNK - 1) / KCHUNK;
+    AccTile<NT> acc;  // zeroed per tile: no accumulator is live while staging
+    acc.zero();
     // Thin tiles (one or two units) would leave most warps without rows:
     // there the tile's 2 * nu row groups of RW rows are each taken by ks
     // warps, warp part k working on the chunks c with c mod ks == k, and the
