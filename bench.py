@@ -13,8 +13,10 @@ chain slower").
 Inputs are synthetic and seeded (N(0, 0.02) weights quantized on the GPU by
 the library's quantizer, N(0, 1) activations).  Weights rotate over 12
 replicas (600 MB, > 4x the 129 MB L2), so every call streams from HBM.
-Timed region: CUDA-graph replays of whole steps, CUDA events on the
-launching stream.  `e2e` repeats the steps through the public API with the
+Each call is the library's matvec with a caller workspace (qmv_splitk_run,
+which picks one split for this shape and, from 4 tokens on, quantizes the
+activations once into the workspace).  Timed region: CUDA-graph replays of
+whole steps, CUDA events on the launching stream.  `e2e` repeats the steps through the public API with the
 activations copied in from pinned host memory and the outputs copied back,
 every step.  `--impl reference` times the CPU oracle on a bounded sample of
 the same workload on the host cores.  Under torchrun (N > 1) every rank runs
@@ -261,11 +263,19 @@ def run_ours(args):
     Ws = [W0] + [W0.clone() for _ in range(REPLICAS - 1)]
     xs = {n: torch.from_numpy(synth.activations(1010 + n, n, K)).to(dev) for n in NTOKS}
     ys = {n: torch.empty((n, M), device=dev) for n in NTOKS}
+    # the library's matvec with a caller workspace (qmv_splitk_run; one split
+    # for this shape): with 4+ tokens it quantizes the activations once
+    splits = {n: api.splitk_choose(FMT, M, K, n) for n in NTOKS}
+    wss = {n: torch.empty(max(16, api.splitk_workspace_fast_bytes(M, K, n, splits[n])), dtype=torch.uint8,
+                          device=dev) for n in NTOKS}
     torch.cuda.synchronize()
+
+    def matvec(W, n, s):
+        api.splitk_run(FMT, W, xs[n], M, K, n_split=splits[n], ws=wss[n], out=ys[n], stream=s)
 
     def step(r, s):
         for n in NTOKS:
-            api.run(FMT, Ws[r % REPLICAS], xs[n], M, K, out=ys[n], stream=s)
+            matvec(Ws[r % REPLICAS], n, s)
 
     # one graph = REPLICAS steps, each on its own replica
     with torch.cuda.stream(stream):
@@ -290,7 +300,7 @@ def run_ours(args):
         gn = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gn, stream=stream):
             for r in range(REPLICAS):
-                api.run(FMT, Ws[r], xs[n], M, K, out=ys[n], stream=stream)
+                matvec(Ws[r], n, stream)
         with torch.cuda.stream(stream):
             gn.replay()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -322,7 +332,8 @@ def run_ours(args):
     ms = e0.elapsed_time(e1)
     step_bytes = BYTES_PER_CALL * len(NTOKS)
     value, tmax = aggregate(gather_floats(ms, world), [step_bytes * steps] * world)
-    launches = steps * len(NTOKS)
+    # one matvec kernel per call, plus the activation quantizer from 4 tokens on
+    launches = steps * sum(2 if n >= 4 else 1 for n in NTOKS)
 
     extra = None
     if not args.no_extra:
@@ -340,7 +351,7 @@ def run_ours(args):
         for i in range(e2e_steps):
             for n in NTOKS:
                 xs[n].copy_(xh[n], non_blocking=True)
-                api.run(FMT, Ws[i % REPLICAS], xs[n], M, K, out=ys[n], stream=stream)
+                matvec(Ws[i % REPLICAS], n, stream)
                 yh[n].copy_(ys[n], non_blocking=True)
     a1.record(stream)
     a1.synchronize()
@@ -445,8 +456,13 @@ def run_extra(torch, api, synth, stream, dev, peak):
         for n in ns:
             x = torch.from_numpy(synth.activations(3000 + n, n, K)).to(dev)
             y = torch.empty((n, M), device=dev)
-            calls = [(lambda W=W: api.run(fmt, W, x, M, K, out=y, stream=stream)) for W in Ws]
-            res[str(n)] = line(rb, _graph_us(torch, stream, calls))
+            S = api.splitk_choose(fmt, M, K, n)
+            ws = torch.empty(max(16, api.splitk_workspace_fast_bytes(M, K, n, S)), dtype=torch.uint8, device=dev)
+            calls = [(lambda W=W: api.splitk_run(fmt, W, x, M, K, n_split=S, ws=ws, out=y, stream=stream))
+                     for W in Ws]
+            r = line(rb, _graph_us(torch, stream, calls))
+            r["n_split"] = S
+            res[str(n)] = r
         out[name] = {"format": ["Q8_0", "Q4_K", "IQ4_XS"][fmt], "bytes_per_call": rb, "replicas": len(Ws),
                      "n_tok": res}
         del Ws
@@ -459,7 +475,7 @@ def run_extra(torch, api, synth, stream, dev, peak):
             x = torch.from_numpy(synth.activations(3100 + n, n, K)).to(dev)
             y = torch.empty((n, M), device=dev)
             S = api.splitk_choose(0, M, K, n)
-            ws = torch.empty(max(16, api.splitk_workspace_bytes(M, n, S)), dtype=torch.uint8, device=dev)
+            ws = torch.empty(max(16, api.splitk_workspace_fast_bytes(M, K, n, S)), dtype=torch.uint8, device=dev)
             calls = [(lambda W=W: api.splitk_run(0, W, x, M, K, n_split=S, ws=ws, out=y, stream=stream))
                      for W in Ws]
             r = line(rb, _graph_us(torch, stream, calls, reps=10 if rb > 2 ** 28 else 20))
@@ -540,7 +556,9 @@ def run_profile(args):
     for rnd in range(2):
         for n in NTOKS:
             x = torch.from_numpy(synth.activations(1010 + n, n, K)).cuda()
-            api.run(FMT, Ws[(rnd * len(NTOKS) + n) % 3], x, M, K)
+            S = api.splitk_choose(FMT, M, K, n)
+            ws = torch.empty(max(16, api.splitk_workspace_fast_bytes(M, K, n, S)), dtype=torch.uint8, device="cuda")
+            api.splitk_run(FMT, Ws[(rnd * len(NTOKS) + n) % 3], x, M, K, n_split=S, ws=ws)
     torch.cuda.synchronize()
     print(json.dumps({"profile_run": WORKLOAD, "calls": 2 * len(NTOKS)}))
     return 0

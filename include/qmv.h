@@ -175,7 +175,13 @@ int qmv_run_q8(int fmt, const void* W, const int8_t* xq, const float* xd,
  * the workspace, pass 2 adds them in the fixed order s = 0..n_split-1, so the
  * result is bitwise reproducible for a given (shape, n_tok, n_split).
  * n_split = 0 picks a split count from the shape (qmv_splitk_choose).
- * ws must hold qmv_splitk_workspace_bytes(M, n_tok, n_split) bytes. */
+ * ws must hold qmv_splitk_workspace_bytes(M, n_tok, n_split) bytes (none
+ * for n_split = 1).  If it holds that (rounded up to 256) plus
+ * qmv_act_q8_bytes(K, n_tok) more and n_tok >= 4, the activations are
+ * quantized once into the rest of the workspace (one more kernel launch)
+ * and each CTA copies its K-range in instead of quantizing it again: the same
+ * arithmetic (bitwise equal results), less work per CTA. */
+size_t qmv_act_q8_bytes(int64_t K, int n_tok);
 int qmv_splitk_choose(int fmt, int64_t M, int64_t K, int n_tok);
 size_t qmv_splitk_workspace_bytes(int64_t M, int n_tok, int n_split);
 int qmv_splitk_run(int fmt, const void* W, const float* x, float* y, int64_t M,

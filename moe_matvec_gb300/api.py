@@ -48,6 +48,7 @@ _SIGS = {
     "qmv_run_q8": (_int, [_int, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _vp]),
     "qmv_splitk_choose": (_int, [_int, _i64, _i64, _int]),
     "qmv_splitk_workspace_bytes": (_sz, [_i64, _int, _int]),
+    "qmv_act_q8_bytes": (_sz, [_i64, _int]),
     "qmv_splitk_run": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _int, _int, _vp, _sz, _vp]),
     "qmv_splitk_run_static": (_int, [_int, _vp, _vp, _vp, _i64, _i64, _int, _int, _vp]),
     "moe_qmv_workspace_bytes": (_sz, [ctypes.POINTER(MoeExperts), _int, _int]),
@@ -162,17 +163,27 @@ def splitk_workspace_bytes(M: int, n_tok: int, n_split: int) -> int:
     return int(load().qmv_splitk_workspace_bytes(M, n_tok, n_split))
 
 
+def act_q8_bytes(K: int, n_tok: int) -> int:
+    return int(load().qmv_act_q8_bytes(K, n_tok))
+
+
+def splitk_workspace_fast_bytes(M: int, K: int, n_tok: int, n_split: int) -> int:
+    """Workspace that lets qmv_splitk_run quantize the activations once."""
+    part = splitk_workspace_bytes(M, n_tok, n_split) if n_split > 1 else 0
+    return ((part + 255) // 256) * 256 + act_q8_bytes(K, n_tok)
+
+
 def splitk_run(fmt: int, W: torch.Tensor, x: torch.Tensor, M: int, K: int, n_split: int = 0,
                ws: torch.Tensor | None = None, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Split-K matvec; n_split = 0 picks the split from the shape."""
+    """Split-K matvec; n_split = 0 picks the split from the shape.  Without a
+    given workspace, one large enough for pre-quantized activations is made."""
     n = x.shape[0]
     if n_split == 0:
         n_split = splitk_choose(fmt, M, K, n)
     if out is None:
         out = torch.empty((n, M), dtype=torch.float32, device=x.device)
-    need = splitk_workspace_bytes(M, n, n_split) if n_split > 1 else 0
-    if ws is None and need:
-        ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+    if ws is None:
+        ws = torch.empty(max(16, splitk_workspace_fast_bytes(M, K, n, n_split)), dtype=torch.uint8, device=x.device)
     wsb = ws.numel() * ws.element_size() if ws is not None else 0
     _check(load().qmv_splitk_run(int(fmt), _ptr(W), _ptr(x), _ptr(out), M, K, n, n_split, _ptr(ws), wsb,
                                  _stream(stream)), "qmv_splitk_run")

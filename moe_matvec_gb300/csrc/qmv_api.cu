@@ -365,7 +365,7 @@ int qmv_splitk_choose(int fmt, int64_t M, int64_t K, int n_tok) {
   if (!fmt_ok(fmt)) return QMV_ERR_FORMAT;
   if (M <= 0 || K <= 0 || K % group_weights(fmt)) return QMV_ERR_SHAPE;
   const long long units = (M + UNIT_ROWS - 1) / UNIT_ROWS;
-  const long long want = 4ll * device_sm_count();  // >= 4 row units per CTA
+  const long long want = 2ll * device_sm_count();  // >= 2 row units per SM
   if (units >= want) return 1;
   const long long chunks = (K + KCHUNK - 1) / KCHUNK;
   long long target = (want + units - 1) / units;
@@ -380,6 +380,12 @@ int qmv_splitk_choose(int fmt, int64_t M, int64_t K, int n_tok) {
 size_t qmv_splitk_workspace_bytes(int64_t M, int n_tok, int n_split) {
   if (M <= 0 || n_tok <= 0 || n_split <= 0) return 0;
   return (size_t)n_split * n_tok * M * sizeof(float);
+}
+
+size_t qmv_act_q8_bytes(int64_t K, int n_tok) {
+  if (K <= 0 || K > MAX_K || K % 256 || n_tok < 1 || n_tok > QMV_MAX_TOKENS) return 0;
+  const size_t nb = (size_t)n_tok * (size_t)(K / 32);
+  return align256((size_t)n_tok * (size_t)K) + 2 * align256(nb * 4);
 }
 
 int qmv_splitk_run(int fmt, const void* W, const float* x, float* y, int64_t M, int64_t K, int n_tok, int n_split,
@@ -401,9 +407,30 @@ int qmv_splitk_run(int fmt, const void* W, const float* x, float* y, int64_t M, 
       if (ws_bytes < qmv_splitk_workspace_bytes(M, n_tok, n_split)) return QMV_ERR_WORKSPACE;
     }
   }
-  if (n_split == 1) return run_dense(fmt, W, x, nullptr, nullptr, nullptr, y, M, K, n_tok, 1, stream);
+  // With room after the partial sums and 4 or more tokens, the activations
+  // are quantized once into the workspace (one more launch) and every CTA
+  // brings its range in by bulk copies; otherwise each CTA quantizes its
+  // range while staging.  Same arithmetic, bitwise equal results.
+  const size_t part = n_split > 1 ? align256(qmv_splitk_workspace_bytes(M, n_tok, n_split)) : 0;
+  const size_t q8 = qmv_act_q8_bytes(K, n_tok);
+  const int8_t* xq = nullptr;
+  const float* xd = nullptr;
+  const int32_t* xs = nullptr;
+  if (n_tok >= 4 && ws && aligned16(ws) && q8 && ws_bytes >= part + q8) {
+    uint8_t* base = static_cast<uint8_t*>(ws) + part;
+    const size_t nb = (size_t)n_tok * (size_t)(K / 32);
+    int8_t* q = reinterpret_cast<int8_t*>(base);
+    float* d = reinterpret_cast<float*>(base + align256((size_t)n_tok * (size_t)K));
+    int32_t* sm = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(d) + align256(nb * 4));
+    if (launch_act_quant(x, (int)K, n_tok, q, d, sm, stream, true) != cudaSuccess) return QMV_ERR_CUDA;
+    xq = q;
+    xd = d;
+    xs = sm;
+  }
+  const float* xf = xq ? nullptr : x;
+  if (n_split == 1) return run_dense(fmt, W, xf, xq, xd, xs, y, M, K, n_tok, 1, stream);
   float* partial = static_cast<float*>(ws);
-  rc = run_dense(fmt, W, x, nullptr, nullptr, nullptr, partial, M, K, n_tok, n_split, stream);
+  rc = run_dense(fmt, W, xf, xq, xd, xs, partial, M, K, n_tok, n_split, stream);
   if (rc) return rc;
   return launch_splitk_reduce(partial, y, M, n_tok, n_split, stream, true) == cudaSuccess ? QMV_OK : QMV_ERR_CUDA;
 }

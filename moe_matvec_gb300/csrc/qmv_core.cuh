@@ -171,10 +171,9 @@ __device__ __forceinline__ void store_codes(uint8_t* chunk, int l, int li, uint3
 // the next power of two, which the consumers read in pairs).  Called by all
 // consumer warps; a warp step covers SU units of 8 blocks with all of its
 // loads issued first and no branch inside a unit, so the units overlap.
-template <int F, int NT>
+template <int F, int NT, int SU = 4>
 __device__ __forceinline__ void stage_activations(const ActSource& src, int kb0, int nblk, int nt, const ActArea& a,
                                                   int cw, int lane) {
-  constexpr int SU = NT >= 8 ? 8 : 4;
   const int sub = lane >> 2, li = lane & 3;
   const int nck = (nblk + 31) / 32;
   int sh = 0;

@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
     if (s != staged_split) {
       named_sync(1, CONSUMER_THREADS);  // nobody still reads the previous range
       if constexpr (!Q8IN) {
-        stage_activations<F, NT>(src, kb0, nblk, p.nt, a, cw, lane);
+        stage_activations<F, NT, (NT >= 8 ? 8 : 4)>(src, kb0, nblk, p.nt, a, cw, lane);
       } else {
         alive = __all_sync(FULL, stage_q8_bulk<F, NT>(src, kb0, nblk, p.nt, a, abar, aphase, p.err, cw, lane)) &&
                 alive;

@@ -226,3 +226,20 @@ def test_splitk_full_size_sampled(lib, M, K, n, seed, wseed):
     rows = sample_rows(M)
     yr, sabs = oracle.qmv(0, Wn[rows], x, K)
     assert_within(y[:, rows], yr, sabs, what=f"splitk {M}x{K} n{n}")
+
+
+@pytest.mark.parametrize("fmt,M,K,n,S", [(0, 64, 8192, 4, 4), (1, 40, 6144, 7, 3), (2, 72, 8192, 5, 8),
+                                         (0, 100, 4096, 16, 1), (1, 24, 4096, 9, 2), (1, 17408, 5120, 16, 1)])
+def test_splitk_quantized_once_is_bitwise_equal(lib, fmt, M, K, n, S):
+    # a workspace with room for the activations makes split-K quantize them
+    # once instead of per CTA: the same arithmetic, so the same bits
+    w = synth.weights(90 + fmt + S, M, K)
+    x = synth.activations(91 + n, n, K)
+    Wd, xd = dev(oracle.quantize(fmt, w)), dev(x)
+    small = torch.empty(max(16, lib.splitk_workspace_bytes(M, n, S) if S > 1 else 16), dtype=torch.uint8,
+                        device="cuda")
+    y_per_cta = lib.splitk_run(fmt, Wd, xd, M, K, n_split=S, ws=small)
+    y_once = lib.splitk_run(fmt, Wd, xd, M, K, n_split=S)
+    assert torch.equal(y_per_cta, y_once)
+    yr, sabs = oracle.qmv(fmt, oracle.quantize(fmt, w), x, K)
+    assert_within(y_once.cpu().numpy(), yr, sabs, what=f"splitk once S{S}")
