@@ -150,6 +150,19 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Register re-split between warpgroups (all four warps of a warpgroup run
+// the same instruction): dec gives registers back to the CTA's pool, inc
+// takes them (waiting until the pool holds them; the launcher checks that
+// the CTA was launched with enough registers for every warpgroup's share).
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Programmatic dependent launch: wait for the preceding grid's results
 // (no-op when launched without the attribute).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -11,9 +11,10 @@ struct DenseParams;
 
 struct DenseLaunch {
   const DenseParams* p;
-  CUtensorMap map_tile;  // box: TILE_ROWS rows x one chunk
+  CUtensorMap map_tile;  // box: a tile's rows (4 per consumer warp) x one chunk
   CUtensorMap map_unit;  // box: UNIT_ROWS rows x one chunk
   int nt_tmpl;           // compiled token count (1, 2, 4, 8, 16)
+  int cw;                // consumer warps (8, or 12 from 8 tokens on)
   int grid;
   size_t smem;
   cudaStream_t stream;

@@ -115,6 +115,7 @@ static int check_device() {
 // ---------------------------------------------------------------------------
 struct Plan {
   int nt_tmpl, passes_tok, stages, grid;
+  int cw, tile_rows;
   int act_nck;
   size_t smem;
 };
@@ -128,9 +129,9 @@ constexpr int TWO_PER_SM_STAGES = 4;
 // small token counts aim for two CTAs per SM (so that consecutive calls
 // overlap under programmatic dependent launch) with a short ring; otherwise
 // one CTA per SM with a deeper ring.
-static bool plan_stages(int nt, size_t act, int stage_bytes, size_t budget, int& stages, size_t& smem) {
+static bool plan_stages(int nt, int cw, size_t act, int stage_bytes, size_t budget, int& stages, size_t& smem) {
   // mbarriers (full, empty, 2 more) and the cross-warp sums of thin tiles
-  const size_t fixed = act + 2 * MAX_STAGES * sizeof(uint64_t) + 128 + CONSUMER_WARPS * RW * 16 * sizeof(float);
+  const size_t fixed = act + 2 * MAX_STAGES * sizeof(uint64_t) + 128 + (size_t)cw * RW * 16 * sizeof(float);
   if (nt <= 4 && fixed + 2 * (size_t)stage_bytes <= TWO_PER_SM_BYTES) {
     int st = (int)((TWO_PER_SM_BYTES - fixed) / stage_bytes);
     stages = st > TWO_PER_SM_STAGES ? TWO_PER_SM_STAGES : st;
@@ -151,13 +152,20 @@ static bool plan_dense(int fmt, long long M, long long K, int n_tok, int n_split
   const long long groups = K / gw;
   const long long max_range = ((groups + n_split - 1) / n_split) * gw;  // weights
   pl.act_nck = (int)((max_range + KCHUNK - 1) / KCHUNK);
-  const int stage_bytes = TILE_ROWS * chunk_bytes_of(fmt);
   const size_t budget = (size_t)device_smem_optin();
   int nt = 16;
   while (nt > n_tok && nt > 1) nt >>= 1;
   if (nt < n_tok && nt < 16) nt <<= 1;  // smallest power of two >= n_tok (<= 16)
+  // from 8 tokens on twelve consumer warps where their tiles fit, else eight
   for (;; nt >>= 1) {
-    if (plan_stages(nt, act_area_bytes(fmt, nt, pl.act_nck), stage_bytes, budget, pl.stages, pl.smem)) break;
+    bool ok = false;
+    for (int cw = nt >= 8 ? 12 : 8; cw >= 8 && !ok; cw -= 4) {
+      pl.cw = cw;
+      pl.tile_rows = cw * RW;
+      ok = plan_stages(nt, cw, act_area_bytes(fmt, nt, pl.act_nck), pl.tile_rows * chunk_bytes_of(fmt), budget,
+                       pl.stages, pl.smem);
+    }
+    if (ok) break;
     if (nt == 1) return false;
   }
   pl.nt_tmpl = nt;
@@ -185,7 +193,7 @@ static int run_dense(int fmt, const void* W, const float* x, const int8_t* xq, c
   if (!plan_dense(fmt, M, K, n_tok, n_split, pl)) return QMV_ERR_SHAPE;
   const long long rb = qmv_row_bytes(fmt, K);
   DenseLaunch L;
-  if (!encode_rows(&L.map_tile, W, M, rb, chunk_bytes_of(fmt), TILE_ROWS)) return QMV_ERR_CUDA;
+  if (!encode_rows(&L.map_tile, W, M, rb, chunk_bytes_of(fmt), pl.tile_rows)) return QMV_ERR_CUDA;
   if (!encode_rows(&L.map_unit, W, M, rb, chunk_bytes_of(fmt), UNIT_ROWS)) return QMV_ERR_CUDA;
   DenseParams p;
   p.x = x;
@@ -204,13 +212,14 @@ static int run_dense(int fmt, const void* W, const float* x, const int8_t* xq, c
   // L2 lookahead: at most PREFETCH_STAGES tiles per CTA and PREFETCH_BYTES
   // in all, so prefetched tiles are still in L2 when the ring takes them
   {
-    const long long per = (long long)pl.grid * TILE_ROWS * chunk_bytes_of(fmt);
+    const long long per = (long long)pl.grid * pl.tile_rows * chunk_bytes_of(fmt);
     long long pf = PREFETCH_BYTES / per;
     p.prefetch = (int)(pf > PREFETCH_STAGES ? PREFETCH_STAGES : (pf < 1 ? 1 : pf));
   }
   p.err = device_error_word();
   L.p = &p;
   L.nt_tmpl = pl.nt_tmpl;
+  L.cw = pl.cw;
   L.grid = pl.grid;
   L.smem = pl.smem;
   L.stream = stream;
@@ -297,7 +306,7 @@ static int run_moe_proj(int mode, int fmt, const void* pool, MoeParams& p, int n
   // activation area when sizing, and leave them out of the dynamic size
   const size_t static_bytes = sizeof(MoeRouting) + 16 * sizeof(int) + 256;
   size_t smem = 0;
-  if (!plan_stages(nt, act_area_bytes(fmt, nt, p.act_nck) + static_bytes, stage_bytes,
+  if (!plan_stages(nt, CONSUMER_WARPS, act_area_bytes(fmt, nt, p.act_nck) + static_bytes, stage_bytes,
                    (size_t)device_smem_optin(), p.stages, smem))
     return QMV_ERR_SHAPE;
   L.p = &p;

@@ -33,6 +33,26 @@ constexpr long long PREFETCH_BYTES = 64ll << 20;      // lookahead of all CTAs t
 constexpr int ACT_BYTES = KCHUNK;                     // codes per token per chunk
 constexpr unsigned FULL = 0xffffffffu;
 
+// CTA shape with CW consumer warps.  Eight consumers run beside one producer
+// warp.  Twelve consumers (three per scheduler, for kernels whose warps are
+// register-bound) run beside a producer warpgroup whose four warps hand all
+// but REG_PRODUCER registers each to the consumers (REG_CONSUMER each):
+// 128 x REG_PRODUCER + 384 x REG_CONSUMER = 65,536, the registers of a
+// 512-thread CTA launched at 128 per thread.
+template <int CW>
+struct Shape {
+  static_assert(CW == 8 || CW == 12, "8 or 12 consumer warps");
+  static constexpr int TILE_ROWS = CW * RW;
+  static constexpr int CONSUMER_THREADS = CW * 32;
+  static constexpr int PRODUCER_WARPS = CW == 8 ? 1 : 4;
+  static constexpr int THREADS = (CW + PRODUCER_WARPS) * 32;
+  static constexpr bool RESPLIT = CW != 8;
+  static constexpr int REG_LAUNCH = 65536 / THREADS;  // 128 when re-split
+  static constexpr int REG_PRODUCER = 32, REG_CONSUMER = 160;
+  static_assert(!RESPLIT || PRODUCER_WARPS * 32 * REG_PRODUCER + CW * 32 * REG_CONSUMER <= THREADS * REG_LAUNCH,
+                "register re-split exceeds the launch's registers");
+};
+
 // Byte p (0..31) of block l (0..31) of a token's 1024-byte chunk of codes:
 // within every 8 blocks the first 16 bytes come first, then the last 16, so
 // that the 8 lanes of a quarter-warp read 128 contiguous bytes.
@@ -171,7 +191,7 @@ __device__ __forceinline__ void store_codes(uint8_t* chunk, int l, int li, uint3
 // the next power of two, which the consumers read in pairs).  Called by all
 // consumer warps; a warp step covers SU units of 8 blocks with all of its
 // loads issued first and no branch inside a unit, so the units overlap.
-template <int F, int NT, int SU = 4>
+template <int F, int NT, int SU = 4, int CW = CONSUMER_WARPS>
 __device__ __forceinline__ void stage_activations(const ActSource& src, int kb0, int nblk, int nt, const ActArea& a,
                                                   int cw, int lane) {
   const int sub = lane >> 2, li = lane & 3;
@@ -180,7 +200,7 @@ __device__ __forceinline__ void stage_activations(const ActSource& src, int kb0,
   while ((1 << sh) < nt) sh++;
   if (NT >= 2 && sh == 0) sh = 1;
   const int total = nck * 32 << sh;  // a multiple of 32 = blocks of one warp step
-  for (int base = cw * 8 * SU; base < total; base += CONSUMER_WARPS * 8 * SU) {
+  for (int base = cw * 8 * SU; base < total; base += CW * 8 * SU) {
     int tt[SU], cc[SU], l[SU];
     long long gblk[SU];
     bool real[SU];
@@ -254,16 +274,16 @@ __device__ __forceinline__ void stage_activations(const ActSource& src, int kb0,
 // (phase `parity`) and, for IQ4_XS, reorders each block's codes into the
 // interleaved order its decode reads.  Returns false (timeout bit set) if
 // the copies never land.
-template <int F, int NT>
+template <int F, int NT, int CW = CONSUMER_WARPS>
 __device__ __forceinline__ bool stage_q8_bulk(const ActSource& src, int kb0, int nblk, int nt, const ActArea& a,
                                               uint64_t* bar, uint32_t parity, unsigned* err, int cw, int lane) {
   constexpr int NCOPY = F == QMV_Q4_K ? 3 : 2;
   const int nck = (nblk + 31) / 32;
   if (cw == 0 && lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nt * nblk * (32 + 4 * (NCOPY - 1))));
-  named_sync(1, CONSUMER_THREADS);  // the byte count is posted before any copy completes
+  named_sync(1, CW * 32);  // the byte count is posted before any copy completes
   {
     // one copy per (token, chunk, kind): codes, scales, sums; spread over all consumer threads
-    for (int i = cw * 32 + lane; i < nt * nck * NCOPY; i += CONSUMER_THREADS) {
+    for (int i = cw * 32 + lane; i < nt * nck * NCOPY; i += CW * 32) {
       const int t = i / (nck * NCOPY), r = i - t * nck * NCOPY, c = r / NCOPY, k = r - c * NCOPY;
       const int nb = min(32, nblk - c * 32);
       const long long row = src.row(t), b0 = (long long)kb0 + c * 32;  // first block of the piece
@@ -277,7 +297,7 @@ __device__ __forceinline__ bool stage_q8_bulk(const ActSource& src, int kb0, int
   }
   // scales (and sums) of the blocks past nblk in the last chunk: zero
   const int nb_last = nblk - (nck - 1) * 32, tail = 32 - nb_last;
-  for (int i = cw * 32 + lane; i < nt * tail; i += CONSUMER_THREADS) {
+  for (int i = cw * 32 + lane; i < nt * tail; i += CW * 32) {
     const int t = i / tail, b = nb_last + (i - t * tail);
     a.d[a.scale(nck - 1, t) + b] = 0.f;
     if constexpr (F == QMV_Q4_K) a.s[a.scale(nck - 1, t) + b] = 0;
@@ -285,7 +305,7 @@ __device__ __forceinline__ bool stage_q8_bulk(const ActSource& src, int kb0, int
   const bool ok = mbar_wait(bar, parity, err);
   if constexpr (F == QMV_IQ4_XS) {
     // x_0..15 and x_16..31 of a block sit in two 16-byte pieces; interleave
-    for (int i = cw * 32 + lane; i < nt * nck * 32; i += CONSUMER_THREADS) {
+    for (int i = cw * 32 + lane; i < nt * nck * 32; i += CW * 32) {
       const int t = i / (nck * 32), r = i - t * nck * 32, c = r >> 5, l = r & 31;
       uint8_t* chunk = a.codes(c, t);
       uint4* p0 = reinterpret_cast<uint4*>(chunk + act_pos(l, 0));
@@ -616,11 +636,12 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // Pipeline barriers of a CTA: init by thread 0, then __syncthreads.
-__device__ __forceinline__ void init_pipeline(uint64_t* full, uint64_t* empty, int stages) {
+__device__ __forceinline__ void init_pipeline(uint64_t* full, uint64_t* empty, int stages,
+                                              int consumers = CONSUMER_WARPS) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; s++) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CONSUMER_WARPS);
+      mbar_init(&empty[s], consumers);
     }
     fence_mbar_init();
   }

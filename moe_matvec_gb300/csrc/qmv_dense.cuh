@@ -7,8 +7,10 @@
 // Machines", section "A single decode row is not a large matrix
 // multiplication": weight reads dominate).
 //
-// Structure (persistent CTAs):
-//   - the last warp (producer): one elected lane streams the CTA's weight
+// Structure (persistent CTAs; 8 consumer warps and a producer warp, or from
+// 8 tokens on 12 consumer warps and a producer warpgroup that hands its
+// registers to them):
+//   - the producer: one elected lane streams the CTA's weight
 //     tiles, TILE_ROWS rows x 1024 weights, with 2-D TMA loads into a ring of
 //     shared-memory stages guarded by full/empty mbarriers.  The weights are
 //     read-only inputs, so streaming starts at once, before the preceding
@@ -47,8 +49,9 @@ struct DenseParams {
 };
 
 // Per-CTA walk over its tiles: a contiguous range of the flattened
-// (split, 8-row unit) space, cut into tiles of up to TILE_ROWS / UNIT_ROWS
-// units that stay inside one split.
+// (split, 8-row unit) space, cut into tiles of up to TU units that stay
+// inside one split.
+template <int TU>
 struct TileWalk {
   long long f, f_end;
   int units, s, u;  // split and unit at f
@@ -67,7 +70,7 @@ struct TileWalk {
     tu = u;
     const long long lim = f_end - f;
     const int rest = units - u;
-    nu = (int)min((long long)min(TILE_ROWS / UNIT_ROWS, rest), lim);
+    nu = (int)min((long long)min(TU, rest), lim);
     f += nu;
     u += nu;
     if (u == units) {
@@ -89,13 +92,20 @@ __device__ __forceinline__ void split_range(const DenseParams& p, int s, int& g0
   }
 }
 
+// Consumer warps of the dense kernel (CW): from 8 tokens on the warps are
+// register-bound (the accumulators of 4 rows x NT tokens), and twelve of
+// them (three per scheduler) hide more latency than eight, where their
+// larger tiles leave room for a ring of weight stages.
+
 // Q8IN: the activations come pre-quantized (bulk copies) instead of as fp32
 // rows quantized while staging; separate instantiations, so each kernel
 // carries only its own staging code.
-template <int F, int NT, bool Q8IN>
-__global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
+template <int F, int NT, bool Q8IN, int CW>
+__global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT>())
     qmv_dense_kernel(const __grid_constant__ CUtensorMap map_tile, const __grid_constant__ CUtensorMap map_unit,
                      const DenseParams p) {
+  using SH = Shape<CW>;
+  constexpr int TILE_ROWS = SH::TILE_ROWS, TU = TILE_ROWS / UNIT_ROWS, CONSUMER_THREADS = SH::CONSUMER_THREADS;
   constexpr int CB = chunk_bytes<F>();
   constexpr int GW = Fmt<F>::GW, GB = Fmt<F>::GB;
   constexpr int STAGE_BYTES = TILE_ROWS * CB;
@@ -106,16 +116,17 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
   uint64_t* full = reinterpret_cast<uint64_t*>(stages + p.stages * STAGE_BYTES + act_area_bytes(F, NT, p.act_nck));
   uint64_t* empty = full + MAX_STAGES;
   uint64_t* abar = full + 2 * MAX_STAGES;  // bulk copies of pre-quantized activations
-  float* red = reinterpret_cast<float*>(abar + 2);  // [CONSUMER_WARPS][RW * NT]: cross-warp sums of thin tiles
+  float* red = reinterpret_cast<float*>(abar + 2);  // [CW][RW * NT]: cross-warp sums of thin tiles
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) mbar_init(abar, 1);
-  init_pipeline(full, empty, p.stages);
+  init_pipeline(full, empty, p.stages, CW);
   pdl_launch_dependents();
 
-  if (warp == CONSUMER_WARPS) {
+  if (warp >= CW) {
     // ---------------- producer ----------------
-    if (lane == 0) {
+    if constexpr (SH::RESPLIT) regs_dec<SH::REG_PRODUCER>();
+    if (warp == CW && lane == 0) {
       prefetch_tensormap(&map_tile);
       prefetch_tensormap(&map_unit);
       const uint64_t pol = policy_evict_first();
@@ -123,7 +134,7 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
       // into L2, so the CTA's weights keep streaming from HBM while the
       // preceding grid finishes and while the consumers wait for it.
       struct Cursor {
-        TileWalk w;
+        TileWalk<TU> w;
         int s, u, nu, g0, g1, nck, c;
         bool valid;
         __device__ Cursor(const DenseParams& p) : w(p), c(0) { load(p); }
@@ -144,13 +155,13 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
         for (; pf.valid && pf_n < target; pf_n++, pf.advance(p)) {
           if (pf_n < p.stages) continue;  // these go straight to shared memory
           const int x = (pf.g0 * GB + pf.c * CB) / 8;
-          if (pf.nu == TILE_ROWS / UNIT_ROWS)
+          if (pf.nu == TU)
             tma_prefetch_2d(&map_tile, x, pf.u * UNIT_ROWS);
           else
             for (int i = 0; i < pf.nu; i++) tma_prefetch_2d(&map_unit, x, (pf.u + i) * UNIT_ROWS);
         }
       };
-      TileWalk walk(p);
+      TileWalk<TU> walk(p);
       int s, u, nu;
       Ring ring;
       bool alive = true;
@@ -167,7 +178,7 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
           const int st = ring.st;
           uint8_t* dst = stages + st * STAGE_BYTES;
           const int x = (g0 * GB + c * CB) / 8;
-          if (nu == TILE_ROWS / UNIT_ROWS) {
+          if (nu == TU) {
             mbar_arrive_expect_tx(&full[st], STAGE_BYTES);
             tma_load_2d(dst, &map_tile, &full[st], x, u * UNIT_ROWS, pol);
           } else {
@@ -186,10 +197,11 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
   // A consumer that gives up on a wait keeps walking the tiles (without
   // waiting or computing) so that the named barriers of the others still
   // complete; the timeout bit is already set.
+  if constexpr (SH::RESPLIT) regs_inc<SH::REG_CONSUMER>();
   pdl_wait();  // activations may come from the preceding kernel
   const int cw = warp;
   bool alive = true;
-  TileWalk walk(p);
+  TileWalk<TU> walk(p);
   int s, u, nu;
   Ring ring;
   int staged_split = -1;
@@ -206,9 +218,9 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
     if (s != staged_split) {
       named_sync(1, CONSUMER_THREADS);  // nobody still reads the previous range
       if constexpr (!Q8IN) {
-        stage_activations<F, NT, (NT >= 8 ? 8 : 4)>(src, kb0, nblk, p.nt, a, cw, lane);
+        stage_activations<F, NT, (NT >= 8 ? 8 : 4), CW>(src, kb0, nblk, p.nt, a, cw, lane);
       } else {
-        alive = __all_sync(FULL, stage_q8_bulk<F, NT>(src, kb0, nblk, p.nt, a, abar, aphase, p.err, cw, lane)) &&
+        alive = __all_sync(FULL, stage_q8_bulk<F, NT, CW>(src, kb0, nblk, p.nt, a, abar, aphase, p.err, cw, lane)) &&
                 alive;
         aphase ^= 1;
       }
@@ -220,12 +232,13 @@ __global__ void __launch_bounds__(THREADS, dense_min_blocks<NT>())
     const int nck = (nblk * BLK + KCHUNK - 1) / KCHUNK;
     AccTile<NT> acc;  // zeroed per tile: no accumulator is live while staging
     acc.zero();
-    // Thin tiles (one or two units) would leave most warps without rows:
-    // there the tile's 2 * nu row groups of RW rows are each taken by ks
-    // warps, warp part k working on the chunks c with c mod ks == k, and the
-    // parts are added across warps (in part order) before the store.
-    const int ks = nu == 1 ? 4 : (nu == 2 ? 2 : 1);
-    const int rg = CONSUMER_WARPS / ks;  // warps per part (row groups with rows: 2 * nu)
+    // Thin tiles (a few units) would leave most warps without rows: there
+    // the tile's 2 * nu row groups of RW rows are each taken by ks warps
+    // (the most of 4, 2, 1 that the warps cover), warp part k working on the
+    // chunks c with c mod ks == k, and the parts are added across warps (in
+    // part order) before the store.
+    const int ks = 8 * nu <= CW ? 4 : (4 * nu <= CW ? 2 : 1);
+    const int rg = CW / ks;  // warps per part (row groups with rows: 2 * nu <= rg)
     const int grp = cw % rg, part = cw / rg;
     for (int c = 0; c < nck && alive; c++, ring.advance(p.stages)) {
       const int st = ring.st;

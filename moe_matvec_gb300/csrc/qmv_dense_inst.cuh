@@ -6,13 +6,24 @@
 
 namespace qmv {
 
-template <int F, int NT, bool Q8IN>
+template <int F, int NT, bool Q8IN, int CW>
 static cudaError_t launch_dense_nt(const DenseLaunch& L) {
-  auto kern = qmv_dense_kernel<F, NT, Q8IN>;
+  using SH = Shape<CW>;
+  auto kern = qmv_dense_kernel<F, NT, Q8IN, CW>;
   static unsigned long long configured = 0;  // bit per device ordinal
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !((configured >> dev) & 1ull)) {
+    if constexpr (SH::RESPLIT) {
+      // the warpgroups' register shares must fit in what the CTA is launched
+      // with, or the consumers' request for more would never be granted
+      cudaFuncAttributes fa;
+      cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return e;
+      if ((long long)fa.numRegs * SH::THREADS <
+          (long long)SH::PRODUCER_WARPS * 32 * SH::REG_PRODUCER + (long long)CW * 32 * SH::REG_CONSUMER)
+        return cudaErrorInvalidConfiguration;
+    }
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, device_smem_optin());
     if (e != cudaSuccess) return e;
     // all of the unified L1/shared array as shared memory, so that two CTAs
@@ -23,18 +34,18 @@ static cudaError_t launch_dense_nt(const DenseLaunch& L) {
   }
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  make_config(cfg, attr, dim3(L.grid), dim3(THREADS), L.smem, L.stream, L.pdl);
+  make_config(cfg, attr, dim3(L.grid), dim3(SH::THREADS), L.smem, L.stream, L.pdl);
   return cudaLaunchKernelEx(&cfg, kern, L.map_tile, L.map_unit, *L.p);
 }
 
 template <int F, bool Q8IN>
 static cudaError_t launch_dense_src(const DenseLaunch& L) {
   switch (L.nt_tmpl) {
-    case 1: return launch_dense_nt<F, 1, Q8IN>(L);
-    case 2: return launch_dense_nt<F, 2, Q8IN>(L);
-    case 4: return launch_dense_nt<F, 4, Q8IN>(L);
-    case 8: return launch_dense_nt<F, 8, Q8IN>(L);
-    case 16: return launch_dense_nt<F, 16, Q8IN>(L);
+    case 1: return launch_dense_nt<F, 1, Q8IN, 8>(L);
+    case 2: return launch_dense_nt<F, 2, Q8IN, 8>(L);
+    case 4: return launch_dense_nt<F, 4, Q8IN, 8>(L);
+    case 8: return L.cw == 12 ? launch_dense_nt<F, 8, Q8IN, 12>(L) : launch_dense_nt<F, 8, Q8IN, 8>(L);
+    case 16: return L.cw == 12 ? launch_dense_nt<F, 16, Q8IN, 12>(L) : launch_dense_nt<F, 16, Q8IN, 8>(L);
   }
   return cudaErrorInvalidValue;
 }
