@@ -237,35 +237,8 @@ __global__ void __launch_bounds__(THREADS, NT <= 4 ? 2 : 1)
       prefetch_tensormap(&map_tile);
       prefetch_tensormap(&map_unit);
       const uint64_t pol = policy_evict_first();
-      // L2 lookahead of PREFETCH_STAGES iterations past the ring (see the
-      // dense kernel): the expert rows keep streaming while the consumers
-      // stage activations or wait for the preceding grid.
-      MoeWalk pw(rt, units_per_pair, TILE_UNITS);
-      int pq = 0, pu = 0, pnu = 0, pc = 0;
-      bool pvalid = pw.next(pq, pu, pnu);
-      long long pf_n = 0;
-      auto prefetch_to = [&](long long target) {
-        for (; pvalid && pf_n < target; pf_n++) {
-          if (pf_n >= p.stages) {
-            const int base = rt.pair_expert[pq] * p.pool_rows;
-            const int x = pc * CB / 8;
-            if (MODE == MOE_GATE_UP) {
-              for (int i = 0; i < pnu; i++) {
-                tma_prefetch_2d(&map_unit, x, base + (pu + i) * UNIT_ROWS);
-                tma_prefetch_2d(&map_unit, x, base + p.R + (pu + i) * UNIT_ROWS);
-              }
-            } else if (pnu == TILE_UNITS) {
-              tma_prefetch_2d(&map_tile, x, base + pu * UNIT_ROWS);
-            } else {
-              for (int i = 0; i < pnu; i++) tma_prefetch_2d(&map_unit, x, base + (pu + i) * UNIT_ROWS);
-            }
-          }
-          if (++pc == nck) {
-            pc = 0;
-            pvalid = pw.next(pq, pu, pnu);
-          }
-        }
-      };
+      // No L2 lookahead past the ring: it would queue expert rows ahead of
+      // the activation reads on the critical path (see the dense kernel).
       MoeWalk walk(rt, units_per_pair, TILE_UNITS);
       int q, u, nu;
       Ring ring;
@@ -273,7 +246,6 @@ __global__ void __launch_bounds__(THREADS, NT <= 4 ? 2 : 1)
       while (alive && walk.next(q, u, nu)) {
         const int base = rt.pair_expert[q] * p.pool_rows;
         for (int c = 0; c < nck; c++, ring.advance(p.stages)) {
-          if (ring.n >= p.stages) prefetch_to(ring.n + PREFETCH_STAGES);
           if (!producer_acquire(empty, ring, p.stages, p.err)) {
             alive = false;
             break;

@@ -209,13 +209,6 @@ static int run_dense(int fmt, const void* W, const float* x, const int8_t* xq, c
   p.units = (int)((M + UNIT_ROWS - 1) / UNIT_ROWS);
   p.stages = pl.stages;
   p.act_nck = pl.act_nck;
-  // L2 lookahead: at most PREFETCH_STAGES tiles per CTA and PREFETCH_BYTES
-  // in all, so prefetched tiles are still in L2 when the ring takes them
-  {
-    const long long per = (long long)pl.grid * pl.tile_rows * chunk_bytes_of(fmt);
-    long long pf = PREFETCH_BYTES / per;
-    p.prefetch = (int)(pf > PREFETCH_STAGES ? PREFETCH_STAGES : (pf < 1 ? 1 : pf));
-  }
   p.err = device_error_word();
   L.p = &p;
   L.nt_tmpl = pl.nt_tmpl;

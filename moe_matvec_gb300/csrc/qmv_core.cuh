@@ -28,8 +28,6 @@ constexpr int UNIT_ROWS = 8;                          // partition / tail-box gr
 constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;    // + producer warp
 constexpr int CONSUMER_THREADS = CONSUMER_WARPS * 32;
 constexpr int MAX_STAGES = 8;
-constexpr int PREFETCH_STAGES = 16;                   // L2 lookahead of the producer (iterations, at most)
-constexpr long long PREFETCH_BYTES = 64ll << 20;      // lookahead of all CTAs together: half of L2
 constexpr int ACT_BYTES = KCHUNK;                     // codes per token per chunk
 constexpr unsigned FULL = 0xffffffffu;
 
@@ -591,9 +589,9 @@ struct Consumer {
 // Two CTAs fit on an SM for small token counts (so that consecutive calls
 // overlap under programmatic dependent launch); larger token counts keep more
 // accumulators in registers.
-template <int NT>
+template <int NT, int CW = CONSUMER_WARPS>
 constexpr int dense_min_blocks() {
-  return NT <= 4 ? 2 : 1;
+  return NT <= 4 && CW == CONSUMER_WARPS ? 2 : 1;
 }
 
 // Sums over the 32 lanes of V per-lane values v[0 .. V) (V a power of two),

@@ -44,7 +44,6 @@ struct DenseParams {
   int units;           // ceil(M / UNIT_ROWS)
   int stages;
   int act_nck;         // chunks of the activation area
-  int prefetch;        // L2 lookahead of the producer past the ring (iterations)
   unsigned* err;       // device error word
 };
 
@@ -101,7 +100,7 @@ __device__ __forceinline__ void split_range(const DenseParams& p, int s, int& g0
 // rows quantized while staging; separate instantiations, so each kernel
 // carries only its own staging code.
 template <int F, int NT, bool Q8IN, int CW>
-__global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT>())
+__global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT, CW>())
     qmv_dense_kernel(const __grid_constant__ CUtensorMap map_tile, const __grid_constant__ CUtensorMap map_unit,
                      const DenseParams p) {
   using SH = Shape<CW>;
@@ -115,11 +114,14 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT>())
   a.carve(stages + p.stages * STAGE_BYTES, F, NT, p.act_nck);
   uint64_t* full = reinterpret_cast<uint64_t*>(stages + p.stages * STAGE_BYTES + act_area_bytes(F, NT, p.act_nck));
   uint64_t* empty = full + MAX_STAGES;
-  uint64_t* abar = full + 2 * MAX_STAGES;  // bulk copies of pre-quantized activations
+  uint64_t* abar = full + 2 * MAX_STAGES;  // [0] bulk copies of pre-quantized activations, [1] first staging done
   float* red = reinterpret_cast<float*>(abar + 2);  // [CW][RW * NT]: cross-warp sums of thin tiles
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) mbar_init(abar, 1);
+  if (threadIdx.x == 0) {
+    mbar_init(abar, 1);
+    mbar_init(abar + 1, 1);
+  }
   init_pipeline(full, empty, p.stages, CW);
   pdl_launch_dependents();
 
@@ -130,37 +132,13 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT>())
       prefetch_tensormap(&map_tile);
       prefetch_tensormap(&map_unit);
       const uint64_t pol = policy_evict_first();
-      // A cursor p.prefetch iterations ahead of the ring requests tiles
-      // into L2, so the CTA's weights keep streaming from HBM while the
-      // preceding grid finishes and while the consumers wait for it.
-      struct Cursor {
-        TileWalk<TU> w;
-        int s, u, nu, g0, g1, nck, c;
-        bool valid;
-        __device__ Cursor(const DenseParams& p) : w(p), c(0) { load(p); }
-        __device__ void load(const DenseParams& p) {
-          valid = w.next(s, u, nu);
-          if (valid) {
-            split_range(p, s, g0, g1);
-            nck = ((g1 - g0) * GW + KCHUNK - 1) / KCHUNK;
-          }
-          c = 0;
-        }
-        __device__ void advance(const DenseParams& p) {
-          if (++c == nck) load(p);
-        }
-      } pf(p);
-      long long pf_n = 0;
-      auto prefetch_to = [&](long long target) {
-        for (; pf.valid && pf_n < target; pf_n++, pf.advance(p)) {
-          if (pf_n < p.stages) continue;  // these go straight to shared memory
-          const int x = (pf.g0 * GB + pf.c * CB) / 8;
-          if (pf.nu == TU)
-            tma_prefetch_2d(&map_tile, x, pf.u * UNIT_ROWS);
-          else
-            for (int i = 0; i < pf.nu; i++) tma_prefetch_2d(&map_unit, x, (pf.u + i) * UNIT_ROWS);
-        }
-      };
+      // The ring alone keeps enough bytes in flight: a deeper L2 lookahead
+      // only queues weight reads ahead of the activation reads at the start
+      // of the call, which sit on the critical path.  For the same reason,
+      // with pre-quantized activations (whose bulk copies are then the
+      // critical path) only GATE stages are requested before the consumers
+      // have staged them.
+      constexpr long long GATE = Q8IN ? 2 : -1;
       TileWalk<TU> walk(p);
       int s, u, nu;
       Ring ring;
@@ -170,7 +148,10 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT>())
         split_range(p, s, g0, g1);
         const int nck = ((g1 - g0) * GW + KCHUNK - 1) / KCHUNK;
         for (int c = 0; c < nck; c++, ring.advance(p.stages)) {
-          if (ring.n >= p.stages) prefetch_to(ring.n + p.prefetch);
+          if (ring.n == GATE && !mbar_wait(abar + 1, 0, p.err)) {
+            alive = false;
+            break;
+          }
           if (!producer_acquire(empty, ring, p.stages, p.err)) {
             alive = false;
             break;
@@ -225,6 +206,7 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT>())
         aphase ^= 1;
       }
       named_sync(1, CONSUMER_THREADS);
+      if (threadIdx.x == 0 && staged_split < 0) mbar_arrive(abar + 1);  // the producer may go on
       staged_split = s;
     }
     const long long row0 = (long long)u * UNIT_ROWS;
