@@ -209,6 +209,9 @@ static int run_dense(int fmt, const void* W, const float* x, const int8_t* xq, c
   p.units = (int)((M + UNIT_ROWS - 1) / UNIT_ROWS);
   p.stages = pl.stages;
   p.act_nck = pl.act_nck;
+  // L2 lookahead only for small matrices (a few microseconds of HBM time):
+  // there the CTAs' tiles past the ring are requested at the start of the call
+  p.prefetch = M * rb <= PREFETCH_ALL_BYTES ? PREFETCH_STAGES : 0;
   p.err = device_error_word();
   L.p = &p;
   L.nt_tmpl = pl.nt_tmpl;

@@ -28,6 +28,8 @@ constexpr int UNIT_ROWS = 8;                          // partition / tail-box gr
 constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;    // + producer warp
 constexpr int CONSUMER_THREADS = CONSUMER_WARPS * 32;
 constexpr int MAX_STAGES = 8;
+constexpr int PREFETCH_STAGES = 16;                   // L2 lookahead of the producer (iterations, at most)
+constexpr long long PREFETCH_ALL_BYTES = 40ll << 20;  // matrices up to this size: all tiles requested at once
 constexpr int ACT_BYTES = KCHUNK;                     // codes per token per chunk
 constexpr unsigned FULL = 0xffffffffu;
 

@@ -44,6 +44,7 @@ struct DenseParams {
   int units;           // ceil(M / UNIT_ROWS)
   int stages;
   int act_nck;         // chunks of the activation area
+  int prefetch;        // L2 lookahead of the producer past the ring (iterations; 0: none)
   unsigned* err;       // device error word
 };
 
@@ -137,8 +138,39 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT, CW>()
       // of the call, which sit on the critical path.  For the same reason,
       // with pre-quantized activations (whose bulk copies are then the
       // critical path) only GATE stages are requested before the consumers
-      // have staged them.
+      // have staged them.  Only small matrices (p.prefetch > 0: a few
+      // microseconds of HBM time in all) have their tiles past the ring
+      // requested into L2 at once, so that the last ones do not wait for a
+      // free stage at the end of a short call.
       constexpr long long GATE = Q8IN ? 2 : -1;
+      struct Cursor {
+        TileWalk<TU> w;
+        int s, u, nu, g0, g1, nck, c;
+        bool valid;
+        __device__ Cursor(const DenseParams& p) : w(p), c(0) { load(p); }
+        __device__ void load(const DenseParams& p) {
+          valid = w.next(s, u, nu);
+          if (valid) {
+            split_range(p, s, g0, g1);
+            nck = ((g1 - g0) * GW + KCHUNK - 1) / KCHUNK;
+          }
+          c = 0;
+        }
+        __device__ void advance(const DenseParams& p) {
+          if (++c == nck) load(p);
+        }
+      } pf(p);
+      long long pf_n = 0;
+      auto prefetch_to = [&](long long target) {
+        for (; pf.valid && pf_n < target; pf_n++, pf.advance(p)) {
+          if (pf_n < p.stages) continue;  // these go straight to shared memory
+          const int x = (pf.g0 * GB + pf.c * CB) / 8;
+          if (pf.nu == TU)
+            tma_prefetch_2d(&map_tile, x, pf.u * UNIT_ROWS);
+          else
+            for (int i = 0; i < pf.nu; i++) tma_prefetch_2d(&map_unit, x, (pf.u + i) * UNIT_ROWS);
+        }
+      };
       TileWalk<TU> walk(p);
       int s, u, nu;
       Ring ring;
@@ -148,6 +180,7 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT, CW>()
         split_range(p, s, g0, g1);
         const int nck = ((g1 - g0) * GW + KCHUNK - 1) / KCHUNK;
         for (int c = 0; c < nck; c++, ring.advance(p.stages)) {
+          if (p.prefetch > 0 && ring.n >= p.stages) prefetch_to(ring.n + p.prefetch);
           if (ring.n == GATE && !mbar_wait(abar + 1, 0, p.err)) {
             alive = false;
             break;
