@@ -45,6 +45,7 @@ struct MoeParams {
 
 // Expert groups of one launch, in shared memory.
 struct MoeRouting {
+  int ids[MOE_MAX_SLOTS];                    // copy of the launch's ids
   unsigned long long mask[MOE_MAX_EXPERTS];  // tokens routed to each expert
   int off[MOE_MAX_EXPERTS];                  // first slot-list index of each expert
   int slots[MOE_MAX_SLOTS];                  // slots (t * top_k + k), grouped by expert, in token order
@@ -72,12 +73,14 @@ __device__ __forceinline__ void build_routing(MoeRouting& rt, const MoeParams& p
                                               int unit_base, int units_per_pair) {
   const int S = p.n_tok * p.top_k;
   const int E = p.n_experts;
+  // one coalesced read of ids; every later look-up is in shared memory
+  for (int s = threadIdx.x; s < S; s += blockDim.x) rt.ids[s] = p.ids[s];
   for (int e = threadIdx.x; e < E; e += blockDim.x) rt.mask[e] = 0ull;
   __syncthreads();
   for (int s = threadIdx.x; s < S; s += blockDim.x) {
-    const int st = slot_status(p.ids, p.top_k, E, s);
+    const int st = slot_status(rt.ids, p.top_k, E, s);
     if (st == 0)
-      atomicOr(&rt.mask[p.ids[s]], 1ull << (s / p.top_k));
+      atomicOr(&rt.mask[rt.ids[s]], 1ull << (s / p.top_k));
     else if (report)
       set_error(p.err, (unsigned)st);
   }
@@ -114,8 +117,8 @@ __device__ __forceinline__ void build_routing(MoeRouting& rt, const MoeParams& p
   }
   __syncthreads();
   for (int s = threadIdx.x; s < S; s += blockDim.x) {
-    if (slot_status(p.ids, p.top_k, E, s) == 0) {
-      const int e = p.ids[s], t = s / p.top_k;
+    if (slot_status(rt.ids, p.top_k, E, s) == 0) {
+      const int e = rt.ids[s], t = s / p.top_k;
       const int rank = __popcll(rt.mask[e] & ((1ull << t) - 1ull));
       rt.slots[rt.off[e] + rank] = s;
     }

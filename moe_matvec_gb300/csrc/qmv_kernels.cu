@@ -50,13 +50,23 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const float* __restrict_
 }
 
 // y[t][m] = sum_{s=0..S-1} partial[s][t][m], added in the fixed order of s.
+// The partials of a group of splits are all loaded before the first is
+// added, so their latencies overlap.
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ partial, float* __restrict__ y,
                                                             long long n, int n_split) {
   pdl_wait();
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
     float acc = partial[i];
-    for (int s = 1; s < n_split; s++) acc += partial[(long long)s * n + i];
+    int s = 1;
+    for (; s + 8 <= n_split; s += 8) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; j++) v[j] = partial[(long long)(s + j) * n + i];
+#pragma unroll
+      for (int j = 0; j < 8; j++) acc += v[j];
+    }
+    for (; s < n_split; s++) acc += partial[(long long)s * n + i];
     y[i] = acc;
   }
   pdl_launch_dependents();
@@ -65,7 +75,9 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
 // MoE combine: y[t][m] = sum over routed slots k (in k order) of
 // gates[t][k] * o[t * top_k + k][m]; a slot that does not route (id out of
 // range, or repeating an earlier id of the token) adds nothing.  One thread
-// per 4 consecutive outputs of a token.
+// per 4 consecutive outputs of a token; the ids, gates and slot outputs of
+// the token are all loaded before the first is used, so their latencies
+// overlap.
 __global__ void __launch_bounds__(256) moe_combine_kernel(const int32_t* __restrict__ ids,
                                                           const float* __restrict__ gates,
                                                           const float* __restrict__ o, float* __restrict__ y,
@@ -76,18 +88,33 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const int32_t* __restr
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
     const int t = (int)(i / q4), m4 = (int)(i - (long long)t * q4);
+    int e[QMV_MAX_TOPK];
+    float g[QMV_MAX_TOPK];
+#pragma unroll
+    for (int k = 0; k < QMV_MAX_TOPK; k++) {
+      e[k] = k < top_k ? ids[t * top_k + k] : -1;
+      g[k] = k < top_k ? gates[t * top_k + k] : 0.f;
+    }
+    bool ok[QMV_MAX_TOPK];
+#pragma unroll
+    for (int k = 0; k < QMV_MAX_TOPK; k++) {
+      ok[k] = e[k] >= 0 && e[k] < n_experts;
+#pragma unroll
+      for (int kk = 0; kk < k; kk++) ok[k] = ok[k] && e[kk] != e[k];
+    }
+    float4 v[QMV_MAX_TOPK];
+#pragma unroll
+    for (int k = 0; k < QMV_MAX_TOPK; k++)
+      v[k] = ok[k] ? reinterpret_cast<const float4*>(o + ((long long)t * top_k + k) * hidden)[m4]
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < top_k; k++) {
-      const int e = ids[t * top_k + k];
-      bool ok = e >= 0 && e < n_experts;
-      for (int kk = 0; kk < k && ok; kk++) ok = ids[t * top_k + kk] != e;
-      if (!ok) continue;
-      const float g = gates[t * top_k + k];
-      const float4 v = reinterpret_cast<const float4*>(o + ((long long)t * top_k + k) * hidden)[m4];
-      acc.x = fmaf(g, v.x, acc.x);
-      acc.y = fmaf(g, v.y, acc.y);
-      acc.z = fmaf(g, v.z, acc.z);
-      acc.w = fmaf(g, v.w, acc.w);
+#pragma unroll
+    for (int k = 0; k < QMV_MAX_TOPK; k++) {
+      if (!ok[k]) continue;
+      acc.x = fmaf(g[k], v[k].x, acc.x);
+      acc.y = fmaf(g[k], v[k].y, acc.y);
+      acc.z = fmaf(g[k], v[k].z, acc.z);
+      acc.w = fmaf(g[k], v[k].w, acc.w);
     }
     reinterpret_cast<float4*>(y + (long long)t * hidden)[m4] = acc;
   }
