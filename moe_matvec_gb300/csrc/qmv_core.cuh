@@ -340,11 +340,14 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 // sign-replicating mode of a third permute (msb of the selected byte copied
 // to all 8 bits), fed with the word and the word << 4 so that the fourth bits
 // of the four codes sit at byte msbs.
-__device__ __forceinline__ uint32_t iq4_lookup4(uint32_t pl, uint32_t p, uint32_t p4, uint32_t mask_sel) {
-  constexpr uint32_t T0 = 0xBFAD9881u, T1 = 0xF6EADDCFu;  // codes 0..7
-  constexpr uint32_t T2 = 0x26190D01u, T3 = 0x71594535u;  // codes 8..15
-  uint32_t lo = prmt(T0, T1, pl);
-  uint32_t hi = prmt(T2, T3, pl);
+// The codebook as four words (codes 0..7, then 8..15), the data operands
+// of the two table permutes.
+constexpr uint32_t IQ4_T0 = 0xBFAD9881u, IQ4_T1 = 0xF6EADDCFu;
+constexpr uint32_t IQ4_T2 = 0x26190D01u, IQ4_T3 = 0x71594535u;
+__device__ __forceinline__ uint32_t iq4_lookup4(uint32_t pl, uint32_t p, uint32_t p4, uint32_t mask_sel,
+                                                const uint32_t (&t)[4]) {
+  uint32_t lo = prmt(t[0], t[1], pl);
+  uint32_t hi = prmt(t[2], t[3], pl);
   uint32_t m = prmt(p4, p, mask_sel);
   return (hi & m) | (lo & ~m);
 }
@@ -397,6 +400,8 @@ struct Consumer {
   uint32_t fsh;    // bit offset of that field in the word pair at f_off
   uint32_t a_off;  // the lane's block in a token's activation chunk
   uint32_t d_off;  // the lane's scale in a chunk's scales (token slot 0)
+  uint32_t cb[4];  // IQ4_XS: the codebook words, held in registers for the whole kernel (a
+                   // shuffle hides their values, so they are not re-created before every use)
 
   __device__ explicit Consumer(int lane) {
     const int j = lane & 7;
@@ -423,6 +428,12 @@ struct Consumer {
     }
     a_off = act_pos(lane, 0);
     d_off = 4 * lane;
+    if constexpr (F == QMV_IQ4_XS) {
+      cb[0] = __shfl_sync(FULL, IQ4_T0, 0);
+      cb[1] = __shfl_sync(FULL, IQ4_T1, 0);
+      cb[2] = __shfl_sync(FULL, IQ4_T2, 0);
+      cb[3] = __shfl_sync(FULL, IQ4_T3, 0);
+    }
   }
 
   // Q4_K with 4 or more tokens: both nibble halves as 16 x code, one chain.
@@ -489,8 +500,8 @@ struct Consumer {
           const uint32_t pw = qq[i];
           const uint32_t pl = pw & 0x77777777u;
           const uint32_t p4 = pw << 4;
-          w[r][2 * i] = iq4_lookup4(pl, pw, p4, 0xD9C8u);
-          w[r][2 * i + 1] = iq4_lookup4(pl >> 16, pw, p4, 0xFBEAu);
+          w[r][2 * i] = iq4_lookup4(pl, pw, p4, 0xD9C8u, cb);
+          w[r][2 * i + 1] = iq4_lookup4(pl >> 16, pw, p4, 0xFBEAu, cb);
         }
       }
     }
