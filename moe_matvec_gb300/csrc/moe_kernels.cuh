@@ -54,6 +54,7 @@ struct MoeRouting {
   int pair_count[MOE_MAX_SLOTS];
   int pair_cost[MOE_MAX_SLOTS + 1];          // prefix sums of the groups' work weights
                                              // (< 512 x 2^17 units x 22 < 2^31)
+  int wsum[32][3];                           // per-warp totals of the expert scan
   int n_pairs;
 };
 
@@ -68,11 +69,23 @@ __device__ __forceinline__ int slot_status(const int32_t* ids, int top_k, int E,
   return 0;
 }
 
-// Build the expert groups (called by all threads of the CTA).
+// Work weight of a group of c token slots per 8-row unit: its decode
+// (unit_base) plus one per token slot it computes (slots go in pairs from
+// two on).
+__device__ __forceinline__ int group_weight(int c, int nt_group, int unit_base) {
+  return unit_base + (nt_group >= 2 ? (c + 1) & ~1 : c);
+}
+
+// Build the expert groups (called by all threads of the CTA).  The experts
+// are scanned in rounds of (warps x 32): each warp scans its 32 experts'
+// slot, group and work counts with shuffles, the warps' totals go through
+// shared memory, and every expert then writes its slot offset and its
+// groups (expert, first slot, slot count, work prefix).
 __device__ __forceinline__ void build_routing(MoeRouting& rt, const MoeParams& p, int nt_group, bool report,
                                               int unit_base, int units_per_pair) {
   const int S = p.n_tok * p.top_k;
   const int E = p.n_experts;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   // one coalesced read of ids; every later look-up is in shared memory
   for (int s = threadIdx.x; s < S; s += blockDim.x) rt.ids[s] = p.ids[s];
   for (int e = threadIdx.x; e < E; e += blockDim.x) rt.mask[e] = 0ull;
@@ -85,64 +98,68 @@ __device__ __forceinline__ void build_routing(MoeRouting& rt, const MoeParams& p
       set_error(p.err, (unsigned)st);
   }
   __syncthreads();
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    int carry_slots = 0, carry_pairs = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int e = base + lane;
-      const int c = e < E ? __popcll(rt.mask[e]) : 0;
-      const int ng = (c + nt_group - 1) / nt_group;
-      int cs = c, cp = ng;
+  int carry_s = 0, carry_p = 0, carry_w = 0;  // the same in every thread
+  for (int base = 0; base < E; base += nwarps * 32) {
+    const int e = base + warp * 32 + lane;
+    const int c = e < E ? __popcll(rt.mask[e]) : 0;
+    const int ng = (c + nt_group - 1) / nt_group;
+    // work of the expert's groups: ng - 1 full ones and the rest
+    const int w = ng == 0 ? 0
+                          : ((ng - 1) * group_weight(nt_group, nt_group, unit_base) +
+                             group_weight(c - (ng - 1) * nt_group, nt_group, unit_base)) *
+                                units_per_pair;
+    int cs = c, cp = ng, cw = w;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int a = __shfl_up_sync(FULL, cs, o), b = __shfl_up_sync(FULL, cp, o);
-        if (lane >= o) {
-          cs += a;
-          cp += b;
-        }
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(FULL, cs, o), b = __shfl_up_sync(FULL, cp, o), d = __shfl_up_sync(FULL, cw, o);
+      if (lane >= o) {
+        cs += a;
+        cp += b;
+        cw += d;
       }
-      const int off = carry_slots + cs - c, poff = carry_pairs + cp - ng;
-      if (e < E) {
-        rt.off[e] = off;
-        for (int g = 0; g < ng; g++) {
-          rt.pair_expert[poff + g] = e;
-          rt.pair_first[poff + g] = off + g * nt_group;
-          rt.pair_count[poff + g] = min(nt_group, c - g * nt_group);
-        }
-      }
-      carry_slots += __shfl_sync(FULL, cs, 31);
-      carry_pairs += __shfl_sync(FULL, cp, 31);
     }
-    if (lane == 0) rt.n_pairs = carry_pairs;
+    if (lane == 31) {
+      rt.wsum[warp][0] = cs;
+      rt.wsum[warp][1] = cp;
+      rt.wsum[warp][2] = cw;
+    }
+    __syncthreads();
+    int ps = carry_s, pp = carry_p, pw = carry_w;  // before this warp's experts
+    for (int v = 0; v < nwarps; v++) {
+      const int ts = rt.wsum[v][0], tp = rt.wsum[v][1], tw = rt.wsum[v][2];
+      if (v < warp) {
+        ps += ts;
+        pp += tp;
+        pw += tw;
+      }
+      carry_s += ts;
+      carry_p += tp;
+      carry_w += tw;
+    }
+    if (e < E) {
+      const int off = ps + cs - c, poff = pp + cp - ng;
+      int wacc = pw + cw - w;
+      rt.off[e] = off;
+      for (int g = 0; g < ng; g++) {
+        const int cg = min(nt_group, c - g * nt_group);
+        rt.pair_expert[poff + g] = e;
+        rt.pair_first[poff + g] = off + g * nt_group;
+        rt.pair_count[poff + g] = cg;
+        rt.pair_cost[poff + g] = wacc;
+        wacc += group_weight(cg, nt_group, unit_base) * units_per_pair;
+      }
+    }
+    __syncthreads();  // wsum is read before the next round writes it
   }
-  __syncthreads();
+  if (threadIdx.x == 0) {
+    rt.n_pairs = carry_p;
+    rt.pair_cost[carry_p] = carry_w;
+  }
   for (int s = threadIdx.x; s < S; s += blockDim.x) {
     if (slot_status(rt.ids, p.top_k, E, s) == 0) {
       const int e = rt.ids[s], t = s / p.top_k;
       const int rank = __popcll(rt.mask[e] & ((1ull << t) - 1ull));
       rt.slots[rt.off[e] + rank] = s;
-    }
-  }
-  // work weight of a group per 8-row unit: its decode (unit_base) plus one
-  // per token slot it computes (slots go in pairs from two on)
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    long long carry = 0;
-    if (lane == 0) rt.pair_cost[0] = 0;
-    for (int base = 0; base < rt.n_pairs; base += 32) {
-      const int q = base + lane;
-      long long w = 0;
-      if (q < rt.n_pairs) {
-        const int c = rt.pair_count[q];
-        w = (long long)(unit_base + (nt_group >= 2 ? (c + 1) & ~1 : c)) * units_per_pair;
-      }
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const long long a = __shfl_up_sync(FULL, w, o);
-        if (lane >= o) w += a;
-      }
-      if (q < rt.n_pairs) rt.pair_cost[q + 1] = (int)(carry + w);
-      carry += __shfl_sync(FULL, w, 31);
     }
   }
   __syncthreads();
@@ -173,13 +190,15 @@ struct MoeWalk {
     return (long long)lo * units + uu;
   }
   __device__ MoeWalk(const MoeRouting& rt, int units_per_pair, int tile_units_) {
-    const long long C = rt.pair_cost[rt.n_pairs];
+    const unsigned C = (unsigned)rt.pair_cost[rt.n_pairs];  // < 2^31
     units = units_per_pair;
     tile_units = tile_units_;
     const unsigned G = gridDim.x, b = blockIdx.x;
-    // C * b / G in 64 bits without a 64-bit division when C fits in 32 bits
-    const long long P0 = C < (1ll << 32) ? (long long)(((unsigned long long)C * b) / G) : C * b / G;
-    const long long P1 = C < (1ll << 32) ? (long long)(((unsigned long long)C * (b + 1)) / G) : C * (b + 1) / G;
+    // C * b / G exactly in 32-bit arithmetic: C = cq G + cr, so C b / G =
+    // cq b + (cr b) / G with cr b < G^2
+    const unsigned cq = C / G, cr = C - cq * G;
+    const long long P0 = (long long)(cq * b + (cr * b) / G);
+    const long long P1 = (long long)(cq * (b + 1) + (cr * (b + 1)) / G);
     f = locate(rt, units, P0);
     f_end = locate(rt, units, P1);
     q = (int)(f / units);
