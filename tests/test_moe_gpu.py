@@ -110,6 +110,20 @@ def test_moe_small_stagewise(lib, fmt_gu, fmt_d, E, H, F, top_k, n):
     assert lib.get_device_error() == 0
 
 
+@pytest.mark.parametrize("E,top_k,n", [(300, 4, 24), (512, 2, 20)])
+def test_moe_many_experts(lib, E, top_k, n):
+    # more experts than one round of the routing scan covers (32 per warp,
+    # 9 warps): the slot, group and work prefixes carry across rounds
+    H = F = 256
+    ids, gates = synth.routing(900 + E, n, E, top_k)
+    experts = sorted(set(ids.reshape(-1).tolist()))
+    Wgu, Wd = make_pool(0, 1, E, H, F, 901 + E, experts=experts)
+    x = synth.activations(902 + E, n, H)
+    g, _ = run_gpu(0, 1, Wgu, Wd, E, H, F, ids, gates, x)
+    check_stagewise(0, 1, Wgu, Wd, E, H, F, ids, gates, x, g)
+    assert lib.get_device_error() == 0
+
+
 def test_moe_all_tokens_on_the_same_experts(lib):
     # every token picks the same experts: one group per expert overflows the
     # per-group token count and is split into several groups
