@@ -80,6 +80,8 @@ def _load():
         lib.oracle_moe.argtypes = ([ctypes.c_int, _ptr, ctypes.c_int, _ptr] + [ctypes.c_int] * 3
                                    + [_ptr, _ptr, _ptr, ctypes.c_int, ctypes.c_int, _ptr]
                                    + [_ptr] * 11)
+        lib.oracle_route_select.restype = ctypes.c_int
+        lib.oracle_route_select.argtypes = [_ptr] + [ctypes.c_int] * 4 + [_ptr, _ptr]
         _lib = lib
         return lib
 
@@ -192,3 +194,30 @@ def moe(fmt_gu: int, Wgu: np.ndarray, fmt_d: int, Wd: np.ndarray, E: int, H: int
                             _p(out["hd"]), _p(out["hs"]), _p(out["o"]))
     assert rc == 0
     return out
+
+
+GATING_SOFTMAX, GATING_SIGMOID = 0, 1
+
+
+def route_select(logits: np.ndarray, top_k: int, gating: int):
+    """Top-k of router logits [n][E] (fp64; any fp32 logits are exact in it)
+    and the normalised gates (see oracle.c): returns (ids int32 [n][top_k],
+    gates fp64 [n][top_k])."""
+    logits = np.ascontiguousarray(logits, dtype=np.float64)
+    if logits.ndim == 1:
+        logits = logits[None, :]
+    n, E = logits.shape
+    ids = np.empty((n, top_k), np.int32)
+    gates = np.empty((n, top_k), np.float64)
+    rc = _load().oracle_route_select(_p(logits), n, E, int(top_k), int(gating), _p(ids), _p(gates))
+    assert rc == 0
+    return ids, gates
+
+
+def route(fmt: int, Wr: np.ndarray, x: np.ndarray, H: int, top_k: int, gating: int):
+    """Router: logits = What_r Xhat (the quantized matvec above, fp64), then
+    route_select.  Wr uint8 [E][row_bytes]; x fp32 [n][H].  Returns (ids,
+    gates, logits, sabs), sabs the logits' tolerance scale."""
+    logits, sabs = qmv(fmt, Wr, x, H)
+    ids, gates = route_select(logits, top_k, gating)
+    return ids, gates, logits, sabs

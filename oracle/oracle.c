@@ -14,7 +14,9 @@
  *     tolerance scale sum_k |What[m][k] * Xhat[t][k]|;
  *   - the MoE decode layer (routing, gate/up, SwiGLU, requantization of h,
  *     down projection, gate-weighted combine in k order) in fp64 except the
- *     requantization, which uses the fp32 activation rule.
+ *     requantization, which uses the fp32 activation rule;
+ *   - the router's top-k selection and gate normalization (softmax or
+ *     sigmoid) on given logits, in fp64.
  * Sources: small-batch matvecs over Q8_0 / K-quant / IQ4_XS weights and the
  * MoE decode kernels: "Castagna Veloce", section "Kernels for the MI50";
  * gate/up + SwiGLU and Q8 activations shared across weight types: same page,
@@ -568,5 +570,46 @@ int oracle_moe(int fmt_gu, const uint8_t* Wgu, int fmt_d, const uint8_t* Wd, int
   free(hdl);
   free(hsl);
   free(hhat);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Router gating and top-k                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Per token t of logits [n][E] (fp64): the top_k experts in decreasing
+ * order of logit, a tie going to the lower expert index (each pick is the
+ * first maximum among the experts not yet picked), and their gates:
+ *   gating 0 (softmax): g_k = exp(l_k - l_0) / sum_j exp(l_j - l_0) over the
+ *     picked experts (the full softmax renormalised over the picked ones);
+ *   gating 1 (sigmoid): g_k = s_k / sum_j s_j, s = 1 / (1 + exp(-l)).
+ * Source: "Castagna Veloce", section "Fused operations" (router and top-k:
+ * matvec, gating, top-k and weight normalization).  Returns -1 on bad
+ * arguments. */
+int oracle_route_select(const double* logits, int n, int E, int top_k, int gating, int32_t* ids,
+                        double* gates) {
+  if (n <= 0 || E <= 0 || top_k <= 0 || top_k > E || (gating != 0 && gating != 1)) return -1;
+  char* taken = (char*)malloc((size_t)E);
+  if (!taken) return -2;
+  for (int t = 0; t < n; t++) {
+    const double* l = logits + (int64_t)t * E;
+    memset(taken, 0, (size_t)E);
+    for (int k = 0; k < top_k; k++) {
+      int best = -1;
+      for (int e = 0; e < E; e++)
+        if (!taken[e] && (best < 0 || l[e] > l[best])) best = e;
+      taken[best] = 1;
+      ids[t * top_k + k] = best;
+    }
+    double sum = 0.0;
+    for (int k = 0; k < top_k; k++) {
+      double v = l[ids[t * top_k + k]];
+      double w = gating == 0 ? exp(v - l[ids[t * top_k]]) : 1.0 / (1.0 + exp(-v));
+      gates[t * top_k + k] = w;
+      sum += w;
+    }
+    for (int k = 0; k < top_k; k++) gates[t * top_k + k] /= sum;
+  }
+  free(taken);
   return 0;
 }

@@ -451,3 +451,62 @@ def test_q8_code_order_helper_follows_the_stated_rule():
                 for p in range(32):
                     stored[t, g * 256 + (p // 16) * 128 + l * 16 + p % 16] = nat[t, g * 256 + l * 32 + p]
     assert np.array_equal(L.q8_codes_natural(stored), nat)
+
+
+# --------------------------------------------------------------------------
+# router: top-k selection and gate normalization
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("gating", [oracle.GATING_SOFTMAX, oracle.GATING_SIGMOID])
+def test_route_select_matches_a_stable_sort(gating):
+    # the picks are the first top_k of a lexicographic sort by (-logit,
+    # index); logits drawn from few values so that ties are common
+    r = np.random.default_rng(7 + gating)
+    for E, k in [(8, 1), (8, 3), (64, 8), (300, 8)]:
+        logits = r.integers(-3, 4, size=(20, E)).astype(np.float64) * 0.25
+        ids, gates = oracle.route_select(logits, k, gating)
+        for t in range(20):
+            order = np.lexsort((np.arange(E), -logits[t]))
+            assert np.array_equal(ids[t], order[:k])
+            assert abs(gates[t].sum() - 1.0) < 1e-15 * k
+            assert np.all(np.diff(gates[t]) <= 1e-15)  # gates follow the logits' order
+
+
+def test_route_select_closed_forms():
+    # softmax over the picked: logits ln 3, 0 -> 3/4, 1/4 (a third, smaller logit unpicked)
+    ids, g = oracle.route_select(np.array([[np.log(3.0), 0.0, -5.0]]), 2, oracle.GATING_SOFTMAX)
+    assert ids.tolist() == [[0, 1]] and np.allclose(g, [[0.75, 0.25]], rtol=0, atol=1e-15)
+    # sigmoid: s(ln 3) = 3/4, s(0) = 1/2 -> 0.6, 0.4
+    ids, g = oracle.route_select(np.array([[0.0, np.log(3.0), -np.log(3.0)]]), 2, oracle.GATING_SIGMOID)
+    assert ids.tolist() == [[1, 0]] and np.allclose(g, [[0.6, 0.4]], rtol=0, atol=1e-15)
+    # top-1 gives gate 1 and numpy's argmax (first maximum) in both modes
+    r = np.random.default_rng(3)
+    logits = r.standard_normal((50, 16))
+    for gating in (0, 1):
+        ids, g = oracle.route_select(logits, 1, gating)
+        assert np.array_equal(ids[:, 0], logits.argmax(axis=1)) and np.all(g == 1.0)
+
+
+def test_route_select_equals_renormalised_full_softmax():
+    # the plain reading of "softmax gating, then normalise the picked weights"
+    r = np.random.default_rng(11)
+    logits = r.standard_normal((10, 128)) * 2
+    ids, g = oracle.route_select(logits, 8, oracle.GATING_SOFTMAX)
+    full = np.exp(logits - logits.max(axis=1, keepdims=True))
+    full /= full.sum(axis=1, keepdims=True)
+    pick = np.take_along_axis(full, ids.astype(np.int64), axis=1)
+    assert np.allclose(g, pick / pick.sum(axis=1, keepdims=True), rtol=1e-13, atol=0)
+
+
+def test_route_relabelling_experts_permutes_the_picks():
+    # permuting the router rows maps each pick through the permutation
+    r = np.random.default_rng(5)
+    E, H = 32, 512
+    Wr = oracle.quantize(oracle.Q8_0, synth.weights(50, E, H))
+    x = synth.activations(51, 6, H)
+    perm = r.permutation(E)
+    ids, g, _, _ = oracle.route(oracle.Q8_0, Wr, x, H, 4, oracle.GATING_SIGMOID)
+    ids2, g2, _, _ = oracle.route(oracle.Q8_0, Wr[perm], x, H, 4, oracle.GATING_SIGMOID)
+    inv = np.argsort(perm)
+    assert np.array_equal(perm[ids2], ids) and np.array_equal(g, g2)
+    assert np.array_equal(inv[ids], ids2)
