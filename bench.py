@@ -437,9 +437,10 @@ def _replicas(torch, api, fmt, M, K, nbytes_min, dev, seed):
 
 def run_extra(torch, api, synth, stream, dev, peak):
     """µs/call and effective weight GB/s of every other configuration: the
-    Q8_0 GEMV, the IQ4_XS matvecs, split-K (LM head and long K) and the MoE
-    decode layer.  Weight sets rotate over replicas totalling > 2 x L2 (the
-    LM head alone is > 6 x L2); MoE calls rotate over 16 routing draws."""
+    Q8_0 GEMV, the IQ4_XS matvecs, split-K (LM head and long K), the MoE
+    decode layer and the router + top-k step in front of it.  Weight sets
+    rotate over replicas totalling > 2 x L2 (the LM head alone is > 6 x L2);
+    MoE calls rotate over 16 routing draws."""
     out = {}
     l2x2 = 2 * 135 * 2 ** 20
 
@@ -513,6 +514,22 @@ def run_extra(torch, api, synth, stream, dev, peak):
     out["moe_128x_top8_h4096_f1536"] = {"format": "gate/up IQ4_XS, down Q4_K", "bytes_per_expert": per_expert,
                                         "routing_draws": 16, "n_tok": res}
     del wg, wd
+
+    # router + top-k producing those ids / gates: a Q8_0 router of 128
+    # experts over hidden 4096, softmax gating, top-8; router replicas > 2 x L2
+    Ws, rb = _replicas(torch, api, 0, E, H, l2x2, dev, 2500)
+    res = {}
+    for n in c.n_toks:
+        x = torch.from_numpy(synth.activations(2600 + n, n, H)).to(dev)
+        lg = torch.empty((n, E), dtype=torch.float32, device=dev)
+        ri = torch.empty((n, c.top_k), dtype=torch.int32, device=dev)
+        rg = torch.empty((n, c.top_k), dtype=torch.float32, device=dev)
+        calls = [(lambda W=W: api.route_run(0, W, x, E, H, c.top_k, api.GATING_SOFTMAX, logits=lg, ids=ri, gates=rg,
+                                            stream=stream)) for W in Ws]
+        res[str(n)] = line(rb, _graph_us(torch, stream, calls))
+    out["router_q8_0_128x4096_top8"] = {"format": "Q8_0", "gating": "softmax", "bytes_per_call": rb,
+                                        "replicas": len(Ws), "n_tok": res}
+    del Ws
     return out
 
 

@@ -253,6 +253,30 @@ int moe_qmv_run(const moe_experts* e, const int32_t* ids, const float* gates,
                 const float* x, float* y, int n_tok, int top_k, void* ws,
                 size_t ws_bytes, cudaStream_t stream);
 
+/* Router and top-k ("Castagna Veloce", section "Fused operations": router
+ * and top-k in one kernel, i.e. matvec, gating, top-k and weight
+ * normalization), producing the ids and gates moe_qmv_run takes:
+ *   logits[t][e] = What_r[e] . Xhat[t]   (the quantized matvec of qmv_run:
+ *                                        n_experts rows of `hidden` weights
+ *                                        in format fmt, x fp32 [n_tok][hidden])
+ *   ids[t][0..top_k): the top_k experts of token t in decreasing order of
+ *     logit; of equal logits the lower expert index comes first;
+ *   gates[t][k], normalised over the picked experts:
+ *     QMV_GATING_SOFTMAX: exp(l_k - l_0) / sum_j exp(l_j - l_0)
+ *     QMV_GATING_SIGMOID: s_k / sum_j s_j,  s = 1 / (1 + exp(-l)).
+ * logits fp32 [n_tok][n_experts] is written too (caller-owned device memory):
+ * the picks are decided on exactly these values.  ids int32 and gates fp32
+ * [n_tok][top_k].  Two launches (the matvec, then one warp per token for
+ * gating, top-k and normalisation), chained by programmatic dependent launch.
+ * Constraints: hidden a multiple of the format's group size, 1 <= top_k <= 8,
+ * top_k <= n_experts <= 512, 1 <= n_tok <= 64, gating one of the two values
+ * (else QMV_ERR_SHAPE); all pointers 16-byte aligned device memory. */
+#define QMV_GATING_SOFTMAX 0
+#define QMV_GATING_SIGMOID 1
+int moe_route_run(int fmt, const void* Wr, const float* x, int n_experts, int64_t hidden,
+                  int n_tok, int top_k, int gating, float* logits, int32_t* ids, float* gates,
+                  cudaStream_t stream);
+
 /* Diagnostic (no counterpart on the pages): the activation quantizer uses
  * branch-free FMA sequences for d = amax / 127 and 1 / d; this compares them
  * with the IEEE round-to-nearest division and reciprocal on every

@@ -54,6 +54,7 @@ _SIGS = {
     "moe_qmv_workspace_bytes": (_sz, [ctypes.POINTER(MoeExperts), _int, _int]),
     "moe_qmv_workspace_offsets": (_int, [ctypes.POINTER(MoeExperts), _int, _int, ctypes.POINTER(_sz * 5)]),
     "moe_qmv_run": (_int, [ctypes.POINTER(MoeExperts), _vp, _vp, _vp, _vp, _int, _int, _vp, _sz, _vp]),
+    "moe_route_run": (_int, [_int, _vp, _vp, _int, _i64, _int, _int, _int, _vp, _vp, _vp, _vp]),
     "qmv_get_device_error": (_int, [_vp, ctypes.POINTER(_int)]),
     "qmv_check_rounding": (_int, [_vp, _vp]),
     "qmv_strerror": (ctypes.c_char_p, [_int]),
@@ -232,6 +233,29 @@ def moe_run(e: MoeExperts, ids: torch.Tensor, gates: torch.Tensor, x: torch.Tens
     _check(load().moe_qmv_run(ctypes.byref(e), _ptr(ids), _ptr(gates), _ptr(x), _ptr(out), n, top_k, _ptr(ws),
                               ws.numel(), _stream(stream)), "moe_qmv_run")
     return out
+
+
+GATING_SOFTMAX, GATING_SIGMOID = 0, 1
+
+
+def route_run(fmt: int, Wr: torch.Tensor, x: torch.Tensor, n_experts: int, hidden: int, top_k: int,
+              gating: int = GATING_SOFTMAX, logits: torch.Tensor | None = None, ids: torch.Tensor | None = None,
+              gates: torch.Tensor | None = None, stream=None):
+    """Router and top-k: logits fp32 [n][E] = What_r Xhat, then per token the
+    top_k experts by logit (ids int32 [n][top_k]) and their gates normalised
+    over the picked ones (fp32 [n][top_k]).  Returns (ids, gates, logits)."""
+    n = x.shape[0]
+    dev = x.device
+    if logits is None:
+        logits = torch.empty((n, n_experts), dtype=torch.float32, device=dev)
+    if ids is None:
+        ids = torch.empty((n, top_k), dtype=torch.int32, device=dev)
+    if gates is None:
+        gates = torch.empty((n, top_k), dtype=torch.float32, device=dev)
+    _check(load().moe_route_run(int(fmt), _ptr(Wr), _ptr(x), int(n_experts), int(hidden), n, int(top_k),
+                                int(gating), _ptr(logits), _ptr(ids), _ptr(gates), _stream(stream)),
+           "moe_route_run")
+    return ids, gates, logits
 
 
 def check_rounding(stream=None):

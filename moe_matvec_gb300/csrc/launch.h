@@ -15,7 +15,8 @@ struct DenseLaunch {
   CUtensorMap map_unit;  // box: UNIT_ROWS rows x one chunk
   int nt_tmpl;           // compiled token count (1, 2, 4, 8, 16)
   int cw;                // consumer warps (8, or 12 from 8 tokens on)
-  int grid;
+  int grid;              // CTAs per token pass
+  int passes;            // token passes of NT tokens (grid y)
   size_t smem;
   cudaStream_t stream;
   bool pdl;
@@ -47,6 +48,8 @@ cudaError_t launch_moe_down_iq4_xs(const MoeLaunch& L);
 cudaError_t launch_moe_combine(const int32_t* ids, const float* gates, const float* o, float* y, int n_tok,
                                int top_k, int n_experts, int hidden, cudaStream_t stream, bool pdl);
 
+cudaError_t launch_route_topk(const float* logits, int n_tok, int E, int top_k, int gating, int32_t* ids,
+                              float* gates, cudaStream_t stream, bool pdl);
 cudaError_t launch_act_quant(const float* x, int K, int n_tok, int8_t* q, float* d, int32_t* s,
                              cudaStream_t stream, bool pdl);
 cudaError_t launch_splitk_reduce(const float* partial, float* y, long long M, int n_tok, int n_split,

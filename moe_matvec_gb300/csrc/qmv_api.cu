@@ -114,7 +114,7 @@ static int check_device() {
 // Dense / split-K launch planning.
 // ---------------------------------------------------------------------------
 struct Plan {
-  int nt_tmpl, passes_tok, stages, grid;
+  int nt_tmpl, stages, grid;
   int cw, tile_rows;
   int act_nck;
   size_t smem;
@@ -169,7 +169,6 @@ static bool plan_dense(int fmt, long long M, long long K, int n_tok, int n_split
     if (nt == 1) return false;
   }
   pl.nt_tmpl = nt;
-  pl.passes_tok = (n_tok + nt - 1) / nt;
   const long long units = (M + UNIT_ROWS - 1) / UNIT_ROWS;
   const long long work = units * n_split;
   // two CTAs per SM when they fit (more warps to hide latency), else one
@@ -220,9 +219,19 @@ static int run_dense(int fmt, const void* W, const float* x, const int8_t* xq, c
   L.smem = pl.smem;
   L.stream = stream;
   L.pdl = true;
-  for (int t0 = 0; t0 < n_tok; t0 += pl.nt_tmpl) {
-    p.t0 = t0;
-    p.nt = n_tok - t0 < pl.nt_tmpl ? n_tok - t0 : pl.nt_tmpl;
+  // the full token passes in one launch (grid y), so that they run side by
+  // side, and a last partial pass in a second one
+  const int full = n_tok / pl.nt_tmpl, rem = n_tok - full * pl.nt_tmpl;
+  if (full > 0) {
+    p.t0 = 0;
+    p.nt = pl.nt_tmpl;
+    L.passes = full;
+    if (launch_dense_any(fmt, L) != cudaSuccess) return QMV_ERR_CUDA;
+  }
+  if (rem > 0) {
+    p.t0 = full * pl.nt_tmpl;
+    p.nt = rem;
+    L.passes = 1;
     if (launch_dense_any(fmt, L) != cudaSuccess) return QMV_ERR_CUDA;
   }
   return QMV_OK;
@@ -504,6 +513,23 @@ int moe_qmv_run(const moe_experts* e, const int32_t* ids, const float* gates, co
   pd.pool_rows = e->hidden;
   if ((rc = run_moe_proj(MOE_DOWN, e->fmt_down, e->w_down, pd, nt, stream))) return rc;
   return launch_moe_combine(ids, gates, o, y, n_tok, top_k, e->n_experts, e->hidden, stream, true) == cudaSuccess
+             ? QMV_OK
+             : QMV_ERR_CUDA;
+}
+
+int moe_route_run(int fmt, const void* Wr, const float* x, int n_experts, int64_t hidden, int n_tok, int top_k,
+                  int gating, float* logits, int32_t* ids, float* gates, cudaStream_t stream) {
+  int rc = check_dense_args(fmt, Wr, x, logits, n_experts, hidden, n_tok);
+  if (rc) return rc;
+  if (n_experts > MOE_MAX_EXPERTS || (gating != QMV_GATING_SOFTMAX && gating != QMV_GATING_SIGMOID))
+    return QMV_ERR_SHAPE;
+  if (top_k < 1 || top_k > QMV_MAX_TOPK || top_k > n_experts) return QMV_ERR_NTOK;
+  if (!ids || !gates) return QMV_ERR_NULL;
+  if (!aligned16(ids) || !aligned16(gates)) return QMV_ERR_ALIGN;
+  if ((rc = check_device())) return rc;
+  if ((rc = run_dense(fmt, Wr, x, nullptr, nullptr, nullptr, logits, n_experts, hidden, n_tok, 1, stream)))
+    return rc;
+  return launch_route_topk(logits, n_tok, n_experts, top_k, gating, ids, gates, stream, true) == cudaSuccess
              ? QMV_OK
              : QMV_ERR_CUDA;
 }

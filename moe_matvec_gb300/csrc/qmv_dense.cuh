@@ -37,8 +37,8 @@ struct DenseParams {
   long long M;
   int K;               // weights per row
   int ntot;            // tokens held by x / out
-  int t0;              // first token of this pass
-  int nt;              // tokens of this pass (<= NT)
+  int t0;              // first token of this launch's first pass (blockIdx.y: pass of NT tokens)
+  int nt;              // tokens of every pass of this launch (<= NT)
   int n_split;
   int groups;          // K / group weights
   int units;           // ceil(M / UNIT_ROWS)
@@ -222,7 +222,9 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT, CW>()
   const Consumer<F, NT> cons(lane);
   const uint32_t stage_base = smem_u32(stages), aq_base = smem_u32(a.q), ad_base = smem_u32(a.d),
                  as_base = smem_u32(a.s);
-  const ActSource src{p.x, p.xq, p.xd, p.xs, p.K, nullptr, p.t0, nullptr, nullptr, nullptr};
+  // token pass blockIdx.y: tokens t0 .. t0 + ntk - 1 of the call
+  const int t0 = p.t0 + blockIdx.y * NT, ntk = p.nt;
+  const ActSource src{p.x, p.xq, p.xd, p.xs, p.K, nullptr, t0, nullptr, nullptr, nullptr};
   uint32_t aphase = 0;
 
   while (walk.next(s, u, nu)) {
@@ -232,9 +234,9 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT, CW>()
     if (s != staged_split) {
       named_sync(1, CONSUMER_THREADS);  // nobody still reads the previous range
       if constexpr (!Q8IN) {
-        stage_activations<F, NT, (NT >= 8 ? 8 : 4), CW>(src, kb0, nblk, p.nt, a, cw, lane);
+        stage_activations<F, NT, (NT >= 8 ? 8 : 4), CW>(src, kb0, nblk, ntk, a, cw, lane);
       } else {
-        alive = __all_sync(FULL, stage_q8_bulk<F, NT, CW>(src, kb0, nblk, p.nt, a, abar, aphase, p.err, cw, lane)) &&
+        alive = __all_sync(FULL, stage_q8_bulk<F, NT, CW>(src, kb0, nblk, ntk, a, abar, aphase, p.err, cw, lane)) &&
                 alive;
         aphase ^= 1;
       }
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT, CW>()
       }
       if (grp * RW < nrows && (c & (ks - 1)) == part)  // ks is 1, 2 or 4
         cons.chunk(stage_base + st * STAGE_BYTES + grp * RW * CB, aq_base + c * NT * ACT_BYTES,
-                   ad_base + c * NT * 128, as_base + c * NT * 128, p.nt, acc);
+                   ad_base + c * NT * 128, as_base + c * NT * 128, ntk, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
@@ -313,7 +315,7 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT, CW>()
 #pragma unroll
       for (int i = 0; i < HELD; i++) {
         const int o = idx + i, r = o / NT, t = o - r * NT, row = grp * RW + r;
-        if (t < p.nt && row < nrows) out[(long long)(p.t0 + t) * p.M + row0 + row] = v[i];
+        if (t < ntk && row < nrows) out[(long long)(t0 + t) * p.M + row0 + row] = v[i];
       }
     }
   }

@@ -34,7 +34,7 @@ static cudaError_t launch_dense_nt(const DenseLaunch& L) {
   }
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
-  make_config(cfg, attr, dim3(L.grid), dim3(SH::THREADS), L.smem, L.stream, L.pdl);
+  make_config(cfg, attr, dim3(L.grid, L.passes), dim3(SH::THREADS), L.smem, L.stream, L.pdl);
   return cudaLaunchKernelEx(&cfg, kern, L.map_tile, L.map_unit, *L.p);
 }
 

@@ -121,6 +121,87 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const int32_t* __restr
   pdl_launch_dependents();
 }
 
+// Router gating and top-k: one warp per token over its logits [E] (E <=
+// 512, held as up to 16 values per lane).  Each of the top_k picks is a warp
+// arg-max over the experts not yet picked (larger logit first, the lower
+// index on a tie), so the picks come out in decreasing order of logit; the
+// gates are then normalised over the picked experts (softmax: exp(l_k - l_0)
+// over their sum; sigmoid: s_k over the sum of s).
+constexpr int ROUTE_MAX_PER_LANE = 16;
+__global__ void __launch_bounds__(128) route_topk_kernel(const float* __restrict__ logits, int n_tok, int E,
+                                                         int top_k, int gating, int32_t* __restrict__ ids,
+                                                         float* __restrict__ gates) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (t < n_tok) {
+    float l[ROUTE_MAX_PER_LANE];
+#pragma unroll
+    for (int i = 0; i < ROUTE_MAX_PER_LANE; i++) {
+      const int e = i * 32 + lane;  // expert of slot i of this lane
+      l[i] = e < E ? logits[(long long)t * E + e] : 0.f;
+    }
+    unsigned taken = 0;  // bit i: slot i picked (or past E)
+#pragma unroll
+    for (int i = 0; i < ROUTE_MAX_PER_LANE; i++)
+      if (i * 32 + lane >= E) taken |= 1u << i;
+    float pick_l[QMV_MAX_TOPK];
+    int pick_e[QMV_MAX_TOPK];
+#pragma unroll
+    for (int k = 0; k < QMV_MAX_TOPK; k++) {
+      if (k >= top_k) break;
+      // this lane's first maximum among its untaken slots (slots are in
+      // increasing expert order, so the first one is the lowest index)
+      int bi = -1;
+      float bl = 0.f;
+#pragma unroll
+      for (int i = 0; i < ROUTE_MAX_PER_LANE; i++)
+        if (!((taken >> i) & 1u) && (bi < 0 || l[i] > bl)) {
+          bi = i;
+          bl = l[i];
+        }
+      int be = bi < 0 ? 0x7fffffff : bi * 32 + lane;
+      // warp arg-max: larger logit wins, an equal logit goes to the lower expert
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        const bool other = oe != 0x7fffffff && (be == 0x7fffffff || ol > bl || (ol == bl && oe < be));
+        if (other) {
+          bl = ol;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      pick_l[k] = bl;
+      pick_e[k] = be;
+    }
+    float w[QMV_MAX_TOPK], sum = 0.f;
+#pragma unroll
+    for (int k = 0; k < QMV_MAX_TOPK; k++) {
+      if (k >= top_k) break;
+      w[k] = gating == QMV_GATING_SOFTMAX ? expf(pick_l[k] - pick_l[0]) : 1.0f / (1.0f + expf(-pick_l[k]));
+      sum += w[k];
+    }
+#pragma unroll
+    for (int k = 0; k < QMV_MAX_TOPK; k++) {
+      if (k < top_k && lane == k) {
+        ids[t * top_k + k] = pick_e[k];
+        gates[t * top_k + k] = w[k] / sum;
+      }
+    }
+  }
+  pdl_launch_dependents();
+}
+
+cudaError_t launch_route_topk(const float* logits, int n_tok, int E, int top_k, int gating, int32_t* ids,
+                              float* gates, cudaStream_t stream, bool pdl) {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  make_config(cfg, attr, dim3((unsigned)((n_tok + 3) / 4)), dim3(128), 0, stream, pdl);
+  return cudaLaunchKernelEx(&cfg, route_topk_kernel, logits, n_tok, E, top_k, gating, ids, gates);
+}
+
 cudaError_t launch_moe_combine(const int32_t* ids, const float* gates, const float* o, float* y, int n_tok,
                                int top_k, int n_experts, int hidden, cudaStream_t stream, bool pdl) {
   const long long total = (long long)n_tok * (hidden / 4);

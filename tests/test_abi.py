@@ -22,7 +22,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("qmv_run", "qmv_splitk_run", "moe_qmv_run", "qmv_quantize_act", "qmv_get_device_error"):
+    for n in ("qmv_run", "qmv_splitk_run", "moe_qmv_run", "moe_route_run", "qmv_quantize_act",
+              "qmv_get_device_error"):
         assert n in names
 
 

@@ -49,3 +49,17 @@ def test_quantize_entry_points_reject_bad_arguments(L):
 
 def test_device_error_needs_an_output_pointer(L):
     assert L.qmv_get_device_error(None, None) == -4
+
+
+def test_route_rejects_bad_arguments(L):
+    # fmt, Wr, x, E, hidden, n_tok, top_k, gating, logits, ids, gates, stream
+    assert L.moe_route_run(7, A, A, 128, 4096, 1, 8, 0, A, A, A, None) == -1
+    assert L.moe_route_run(0, A, A, 128, 100, 1, 8, 0, A, A, A, None) == -2
+    assert L.moe_route_run(0, A, A, 513, 4096, 1, 8, 0, A, A, A, None) == -2     # > 512 experts
+    assert L.moe_route_run(0, A, A, 128, 4096, 1, 8, 2, A, A, A, None) == -2     # unknown gating
+    assert L.moe_route_run(0, A, A, 128, 4096, 0, 8, 0, A, A, A, None) == -3
+    assert L.moe_route_run(0, A, A, 128, 4096, 1, 9, 0, A, A, A, None) == -3     # top_k > 8
+    assert L.moe_route_run(0, A, A, 4, 4096, 1, 5, 0, A, A, A, None) == -3       # top_k > experts
+    assert L.moe_route_run(0, A, A, 128, 4096, 1, 8, 0, A, None, A, None) == -4
+    assert L.moe_route_run(0, A, A, 128, 4096, 1, 8, 0, None, A, A, None) == -4
+    assert L.moe_route_run(0, A, A, 128, 4096, 1, 8, 0, A, A, MIS, None) == -5
