@@ -188,6 +188,33 @@ int qmv_splitk_run(int fmt, const void* W, const float* x, float* y, int64_t M,
                    int64_t K, int n_tok, int n_split, void* ws, size_t ws_bytes,
                    cudaStream_t stream);
 
+/* Matvec plus residual ("Castagna Veloce", section "Fused operations":
+ * matvec + residual add): y[t][m] = (What Xhat)[t][m] + r[t][m], the fp32
+ * addition made once, after the dot product is complete (in the matvec's
+ * store, or in the ordered second pass of split-K).  r fp32 [n_tok][M]
+ * (device, 16-byte aligned) may be y itself (y += What Xhat).  Arguments,
+ * workspace and split choice as qmv_splitk_run; r NULL -> QMV_ERR_NULL. */
+int qmv_run_residual(int fmt, const void* W, const float* x, const float* r, float* y,
+                     int64_t M, int64_t K, int n_tok, int n_split, void* ws,
+                     size_t ws_bytes, cudaStream_t stream);
+
+/* Sibling matvecs sharing one x ("Castagna Veloce", section "Fused
+ * operations": batched sibling matvecs, and Q8 activations reused across
+ * weight types): y_i = What_i Xhat for i < count, each W_i of format fmts[i]
+ * with M[i] rows of the same K weights (K a multiple of every format's group
+ * size), x fp32 [n_tok][K], y_i fp32 [n_tok][M[i]].  fmts, W, M and y are
+ * host arrays of count (1..QMV_MAX_SIBLINGS) entries; the matrices and
+ * outputs are device memory.  From 4 tokens the activations are quantized
+ * once into ws (at least qmv_act_q8_bytes(K, n_tok) bytes, 16-byte aligned)
+ * and every matvec copies them in; with fewer tokens each matvec quantizes
+ * them while staging and ws may be NULL.  One launch per matvec (plus the
+ * quantizer), chained by programmatic dependent launch.  Results are
+ * bitwise those of qmv_run on each W_i. */
+#define QMV_MAX_SIBLINGS 8
+int qmv_run_siblings(int count, const int* fmts, const void* const* W, const int64_t* M,
+                     float* const* y, const float* x, int64_t K, int n_tok, void* ws,
+                     size_t ws_bytes, cudaStream_t stream);
+
 /* qmv_splitk_run for callers that cannot allocate device memory (the pages
  * have no counterpart to this entry point; it exists for embedding).  Some
  * callers may not call cudaMalloc: a plugin running while its host framework

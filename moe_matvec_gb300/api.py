@@ -55,6 +55,8 @@ _SIGS = {
     "moe_qmv_workspace_offsets": (_int, [ctypes.POINTER(MoeExperts), _int, _int, ctypes.POINTER(_sz * 5)]),
     "moe_qmv_run": (_int, [ctypes.POINTER(MoeExperts), _vp, _vp, _vp, _vp, _int, _int, _vp, _sz, _vp]),
     "moe_route_run": (_int, [_int, _vp, _vp, _int, _i64, _int, _int, _int, _vp, _vp, _vp, _vp]),
+    "qmv_run_residual": (_int, [_int, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _vp, _sz, _vp]),
+    "qmv_run_siblings": (_int, [_int, _vp, _vp, _vp, _vp, _vp, _i64, _int, _vp, _sz, _vp]),
     "qmv_get_device_error": (_int, [_vp, ctypes.POINTER(_int)]),
     "qmv_check_rounding": (_int, [_vp, _vp]),
     "qmv_strerror": (ctypes.c_char_p, [_int]),
@@ -189,6 +191,40 @@ def splitk_run(fmt: int, W: torch.Tensor, x: torch.Tensor, M: int, K: int, n_spl
     _check(load().qmv_splitk_run(int(fmt), _ptr(W), _ptr(x), _ptr(out), M, K, n, n_split, _ptr(ws), wsb,
                                  _stream(stream)), "qmv_splitk_run")
     return out
+
+
+def run_residual(fmt: int, W: torch.Tensor, x: torch.Tensor, r: torch.Tensor, M: int, K: int,
+                 out: torch.Tensor | None = None, n_split: int = 0, ws: torch.Tensor | None = None,
+                 stream=None) -> torch.Tensor:
+    """y = What Xhat + r (r fp32 [n][M]; out may be r for y += What Xhat)."""
+    n = x.shape[0]
+    if n_split == 0:
+        n_split = splitk_choose(fmt, M, K, n)
+    if out is None:
+        out = torch.empty((n, M), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = torch.empty(max(16, splitk_workspace_fast_bytes(M, K, n, n_split)), dtype=torch.uint8, device=x.device)
+    _check(load().qmv_run_residual(int(fmt), _ptr(W), _ptr(x), _ptr(r), _ptr(out), M, K, n, n_split, _ptr(ws),
+                                   ws.numel(), _stream(stream)), "qmv_run_residual")
+    return out
+
+
+def run_siblings(mats, x: torch.Tensor, K: int, outs=None, ws: torch.Tensor | None = None, stream=None):
+    """Sibling matvecs sharing x: mats is a list of (fmt, W, M); returns the
+    list of y_i fp32 [n][M_i]."""
+    n = x.shape[0]
+    c = len(mats)
+    if outs is None:
+        outs = [torch.empty((n, M), dtype=torch.float32, device=x.device) for _, _, M in mats]
+    if ws is None:
+        ws = torch.empty(max(16, act_q8_bytes(K, n)), dtype=torch.uint8, device=x.device)
+    fm = (ctypes.c_int * c)(*[int(f) for f, _, _ in mats])
+    Wp = (ctypes.c_void_p * c)(*[W.data_ptr() for _, W, _ in mats])
+    Mp = (ctypes.c_int64 * c)(*[int(M) for _, _, M in mats])
+    yp = (ctypes.c_void_p * c)(*[o.data_ptr() for o in outs])
+    _check(load().qmv_run_siblings(c, fm, Wp, Mp, yp, _ptr(x), K, n, _ptr(ws), ws.numel(), _stream(stream)),
+           "qmv_run_siblings")
+    return outs
 
 
 STATIC_SCRATCH_BYTES = 8 << 20

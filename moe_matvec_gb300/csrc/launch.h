@@ -52,7 +52,7 @@ cudaError_t launch_route_topk(const float* logits, int n_tok, int E, int top_k, 
                               float* gates, cudaStream_t stream, bool pdl);
 cudaError_t launch_act_quant(const float* x, int K, int n_tok, int8_t* q, float* d, int32_t* s,
                              cudaStream_t stream, bool pdl);
-cudaError_t launch_splitk_reduce(const float* partial, float* y, long long M, int n_tok, int n_split,
+cudaError_t launch_splitk_reduce(const float* partial, float* y, const float* add, long long M, int n_tok, int n_split,
                                  cudaStream_t stream, bool pdl);
 cudaError_t launch_quantize_weights(int fmt, const float* w, long long M, int K, void* W, cudaStream_t stream);
 cudaError_t launch_check_rounding(unsigned long long* bad, cudaStream_t stream);

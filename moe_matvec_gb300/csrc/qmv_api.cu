@@ -187,7 +187,8 @@ static cudaError_t launch_dense_any(int fmt, const DenseLaunch& L) {
 
 // Runs pass 1 (all token passes) writing `out` (y, or the split partials).
 static int run_dense(int fmt, const void* W, const float* x, const int8_t* xq, const float* xd, const int32_t* xs,
-                     float* out, long long M, long long K, int n_tok, int n_split, cudaStream_t stream) {
+                     float* out, long long M, long long K, int n_tok, int n_split, cudaStream_t stream,
+                     const float* add = nullptr) {
   Plan pl;
   if (!plan_dense(fmt, M, K, n_tok, n_split, pl)) return QMV_ERR_SHAPE;
   const long long rb = qmv_row_bytes(fmt, K);
@@ -200,6 +201,7 @@ static int run_dense(int fmt, const void* W, const float* x, const int8_t* xq, c
   p.xd = xd;
   p.xs = xs;
   p.out = out;
+  p.add = n_split == 1 ? add : nullptr;
   p.M = M;
   p.K = (int)K;
   p.ntot = n_tok;
@@ -402,8 +404,9 @@ size_t qmv_act_q8_bytes(int64_t K, int n_tok) {
   return align256((size_t)n_tok * (size_t)K) + 2 * align256(nb * 4);
 }
 
-int qmv_splitk_run(int fmt, const void* W, const float* x, float* y, int64_t M, int64_t K, int n_tok, int n_split,
-                   void* ws, size_t ws_bytes, cudaStream_t stream) {
+// Split-K matvec (n_split 0: chosen from the shape), y = What Xhat (+ add).
+static int splitk_impl(int fmt, const void* W, const float* x, const float* add, float* y, int64_t M, int64_t K,
+                       int n_tok, int n_split, void* ws, size_t ws_bytes, cudaStream_t stream) {
   int rc = check_dense_args(fmt, W, x, y, M, K, n_tok);
   if (rc) return rc;
   if (n_split < 0 || n_split > 256 || n_split > K / group_weights(fmt)) return QMV_ERR_SHAPE;
@@ -442,11 +445,56 @@ int qmv_splitk_run(int fmt, const void* W, const float* x, float* y, int64_t M, 
     xs = sm;
   }
   const float* xf = xq ? nullptr : x;
-  if (n_split == 1) return run_dense(fmt, W, xf, xq, xd, xs, y, M, K, n_tok, 1, stream);
+  if (n_split == 1) return run_dense(fmt, W, xf, xq, xd, xs, y, M, K, n_tok, 1, stream, add);
   float* partial = static_cast<float*>(ws);
   rc = run_dense(fmt, W, xf, xq, xd, xs, partial, M, K, n_tok, n_split, stream);
   if (rc) return rc;
-  return launch_splitk_reduce(partial, y, M, n_tok, n_split, stream, true) == cudaSuccess ? QMV_OK : QMV_ERR_CUDA;
+  return launch_splitk_reduce(partial, y, add, M, n_tok, n_split, stream, true) == cudaSuccess ? QMV_OK
+                                                                                                : QMV_ERR_CUDA;
+}
+
+int qmv_splitk_run(int fmt, const void* W, const float* x, float* y, int64_t M, int64_t K, int n_tok, int n_split,
+                   void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return splitk_impl(fmt, W, x, nullptr, y, M, K, n_tok, n_split, ws, ws_bytes, stream);
+}
+
+int qmv_run_residual(int fmt, const void* W, const float* x, const float* r, float* y, int64_t M, int64_t K,
+                     int n_tok, int n_split, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!r) return QMV_ERR_NULL;
+  if (!aligned16(r)) return QMV_ERR_ALIGN;
+  return splitk_impl(fmt, W, x, r, y, M, K, n_tok, n_split, ws, ws_bytes, stream);
+}
+
+int qmv_run_siblings(int count, const int* fmts, const void* const* W, const int64_t* M, float* const* y,
+                     const float* x, int64_t K, int n_tok, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (count < 1 || count > QMV_MAX_SIBLINGS) return QMV_ERR_SHAPE;
+  if (!fmts || !W || !M || !y) return QMV_ERR_NULL;
+  int rc;
+  for (int i = 0; i < count; i++)
+    if ((rc = check_dense_args(fmts[i], W[i], x, y[i], M[i], K, n_tok))) return rc;
+  const size_t q8 = qmv_act_q8_bytes(K, n_tok);
+  if (n_tok >= 4) {
+    if (!ws) return QMV_ERR_NULL;
+    if (!aligned16(ws)) return QMV_ERR_ALIGN;
+    if (ws_bytes < q8) return QMV_ERR_WORKSPACE;
+  }
+  if ((rc = check_device())) return rc;
+  if (n_tok < 4) {
+    // few tokens: every matvec quantizes the activations while staging
+    for (int i = 0; i < count; i++)
+      if ((rc = run_dense(fmts[i], W[i], x, nullptr, nullptr, nullptr, y[i], M[i], K, n_tok, 1, stream))) return rc;
+    return QMV_OK;
+  }
+  // the activations quantized once, every matvec copies them in
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  const size_t nb = (size_t)n_tok * (size_t)(K / 32);
+  int8_t* q = reinterpret_cast<int8_t*>(base);
+  float* d = reinterpret_cast<float*>(base + align256((size_t)n_tok * (size_t)K));
+  int32_t* sm = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(d) + align256(nb * 4));
+  if (launch_act_quant(x, (int)K, n_tok, q, d, sm, stream, true) != cudaSuccess) return QMV_ERR_CUDA;
+  for (int i = 0; i < count; i++)
+    if ((rc = run_dense(fmts[i], W[i], nullptr, q, d, sm, y[i], M[i], K, n_tok, 1, stream))) return rc;
+  return QMV_OK;
 }
 
 size_t moe_qmv_workspace_bytes(const moe_experts* e, int n_tok, int top_k) {

@@ -34,6 +34,7 @@ struct DenseParams {
   const float* xd;     // [ntot][K/32]
   const int32_t* xs;   // [ntot][K/32]
   float* out;          // y [ntot][M] (n_split == 1) or partial [n_split][ntot][M]
+  const float* add;    // n_split == 1: added to y after the dot product ([ntot][M], may be out), or nullptr
   long long M;
   int K;               // weights per row
   int ntot;            // tokens held by x / out
@@ -315,7 +316,10 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT, CW>()
 #pragma unroll
       for (int i = 0; i < HELD; i++) {
         const int o = idx + i, r = o / NT, t = o - r * NT, row = grp * RW + r;
-        if (t < ntk && row < nrows) out[(long long)(t0 + t) * p.M + row0 + row] = v[i];
+        if (t < ntk && row < nrows) {
+          const long long o = (long long)(t0 + t) * p.M + row0 + row;
+          out[o] = p.add ? v[i] + p.add[o] : v[i];
+        }
       }
     }
   }

@@ -49,11 +49,12 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const float* __restrict_
   }
 }
 
-// y[t][m] = sum_{s=0..S-1} partial[s][t][m], added in the fixed order of s.
-// The partials of a group of splits are all loaded before the first is
-// added, so their latencies overlap.
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ partial, float* __restrict__ y,
-                                                            long long n, int n_split) {
+// y[t][m] = sum_{s=0..S-1} partial[s][t][m], added in the fixed order of s,
+// then + add[t][m] when add is given (add may be y).  The partials of a
+// group of splits are all loaded before the first is added, so their
+// latencies overlap.
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ partial, float* y,
+                                                            const float* add, long long n, int n_split) {
   pdl_wait();
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
@@ -67,7 +68,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
       for (int j = 0; j < 8; j++) acc += v[j];
     }
     for (; s < n_split; s++) acc += partial[(long long)s * n + i];
-    y[i] = acc;
+    y[i] = add ? acc + add[i] : acc;
   }
   pdl_launch_dependents();
 }
@@ -262,7 +263,7 @@ cudaError_t launch_act_quant(const float* x, int K, int n_tok, int8_t* q, float*
   return cudaLaunchKernelEx(&cfg, act_quant_kernel, x, K, n_tok, q, d, s);
 }
 
-cudaError_t launch_splitk_reduce(const float* partial, float* y, long long M, int n_tok, int n_split,
+cudaError_t launch_splitk_reduce(const float* partial, float* y, const float* add, long long M, int n_tok, int n_split,
                                  cudaStream_t stream, bool pdl) {
   const long long n = M * n_tok;
   long long ctas = (n + 255) / 256;
@@ -271,7 +272,7 @@ cudaError_t launch_splitk_reduce(const float* partial, float* y, long long M, in
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   make_config(cfg, attr, dim3((unsigned)ctas), dim3(256), 0, stream, pdl);
-  return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, partial, y, n, n_split);
+  return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, partial, y, add, n, n_split);
 }
 
 }  // namespace qmv

@@ -63,3 +63,20 @@ def test_route_rejects_bad_arguments(L):
     assert L.moe_route_run(0, A, A, 128, 4096, 1, 8, 0, A, None, A, None) == -4
     assert L.moe_route_run(0, A, A, 128, 4096, 1, 8, 0, None, A, A, None) == -4
     assert L.moe_route_run(0, A, A, 128, 4096, 1, 8, 0, A, A, MIS, None) == -5
+
+
+def test_residual_and_siblings_reject_bad_arguments(L):
+    need = L.qmv_splitk_workspace_bytes(64, 2, 4)
+    assert L.qmv_run_residual(0, A, A, None, A, 64, 4096, 2, 1, A, need, None) == -4
+    assert L.qmv_run_residual(0, A, A, MIS, A, 64, 4096, 2, 1, A, need, None) == -5
+    assert L.qmv_run_residual(0, A, A, A, A, 64, 4096, 2, 4, A, need - 1, None) == -6
+    fm = (ctypes.c_int * 2)(0, 1)
+    Wp = (ctypes.c_void_p * 2)(A, A)
+    Mp = (ctypes.c_int64 * 2)(64, 64)
+    yp = (ctypes.c_void_p * 2)(A, A)
+    assert L.qmv_run_siblings(0, fm, Wp, Mp, yp, A, 4096, 2, A, 1 << 20, None) == -2
+    assert L.qmv_run_siblings(9, fm, Wp, Mp, yp, A, 4096, 2, A, 1 << 20, None) == -2
+    assert L.qmv_run_siblings(2, None, Wp, Mp, yp, A, 4096, 2, A, 1 << 20, None) == -4
+    bad = (ctypes.c_int * 2)(0, 2)                                     # IQ4_XS needs K % 512
+    assert L.qmv_run_siblings(2, bad, Wp, Mp, yp, A, 256 + 1024, 2, A, 1 << 20, None) == -2
+    assert L.qmv_run_siblings(2, fm, Wp, Mp, yp, A, 4096, 8, A, 16, None) == -6    # workspace too small
