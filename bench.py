@@ -438,7 +438,8 @@ def _replicas(torch, api, fmt, M, K, nbytes_min, dev, seed):
 def run_extra(torch, api, synth, stream, dev, peak):
     """µs/call and effective weight GB/s of every other configuration: the
     Q8_0 GEMV, the IQ4_XS matvecs, split-K (LM head and long K), the MoE
-    decode layer and the router + top-k step in front of it.  Weight sets
+    decode layer, the router + top-k step in front of it, sibling matvecs
+    sharing x and the matvec with a residual add.  Weight sets
     rotate over replicas totalling > 2 x L2 (the LM head alone is > 6 x L2);
     MoE calls rotate over 16 routing draws."""
     out = {}
@@ -529,6 +530,45 @@ def run_extra(torch, api, synth, stream, dev, peak):
         res[str(n)] = line(rb, _graph_us(torch, stream, calls))
     out["router_q8_0_128x4096_top8"] = {"format": "Q8_0", "gating": "softmax", "bytes_per_call": rb,
                                         "replicas": len(Ws), "n_tok": res}
+    del Ws
+
+    # sibling matvecs sharing x (q / k / v shapes, Q4_K, hidden 5120), against
+    # the same three matrices as separate calls
+    Hs = 5120
+    shapes = [(5120, 2700), (1024, 2701), (1024, 2702)]
+    tot_rows = sum(Ms for Ms, _ in shapes)
+    sets = [_replicas(torch, api, 1, Ms, Hs, l2x2 * Ms // tot_rows, dev, sd) for Ms, sd in shapes]
+    reps = min(len(w) for w, _ in sets)
+    rb = sum(b for _, b in sets)
+    res = {}
+    for n in (1, 4, 16):
+        x = torch.from_numpy(synth.activations(2710 + n, n, Hs)).to(dev)
+        ys = [torch.empty((n, Ms), device=dev) for Ms, _ in shapes]
+        ws = torch.empty(max(16, api.act_q8_bytes(Hs, n)), dtype=torch.uint8, device=dev)
+        fused = [(lambda i=i: api.run_siblings([(1, sets[j][0][i], shapes[j][0]) for j in range(3)], x, Hs,
+                                               outs=ys, ws=ws, stream=stream)) for i in range(reps)]
+        wss = [torch.empty(max(16, api.splitk_workspace_fast_bytes(Ms, Hs, n, 1)), dtype=torch.uint8, device=dev)
+               for Ms, _ in shapes]
+        sep = [(lambda i=i: [api.splitk_run(1, sets[j][0][i], x, shapes[j][0], Hs, n_split=1, ws=wss[j], out=ys[j],
+                                            stream=stream) for j in range(3)]) for i in range(reps)]
+        r = line(rb, _graph_us(torch, stream, fused))
+        r["separate_us_per_call"] = round(_graph_us(torch, stream, sep), 3)
+        res[str(n)] = r
+    out["siblings_q4_k_qkv_5120"] = {"format": "Q4_K", "rows": [m for m, _ in shapes], "K": Hs,
+                                     "bytes_per_call": rb, "replicas": reps, "n_tok": res}
+    del sets
+
+    # matvec + residual add in place (y += W x) on the Q4_K 17408 x 5120 matrix
+    Ws, rb = _replicas(torch, api, 1, 17408, 5120, l2x2, dev, 2800)
+    res = {}
+    for n in (1, 16):
+        x = torch.from_numpy(synth.activations(2810 + n, n, 5120)).to(dev)
+        y = torch.zeros((n, 17408), device=dev)
+        ws = torch.empty(max(16, api.splitk_workspace_fast_bytes(17408, 5120, n, 1)), dtype=torch.uint8, device=dev)
+        calls = [(lambda W=W: api.run_residual(1, W, x, y, 17408, 5120, out=y, n_split=1, ws=ws, stream=stream))
+                 for W in Ws]
+        res[str(n)] = line(rb, _graph_us(torch, stream, calls))
+    out["residual_q4_k_17408x5120"] = {"format": "Q4_K", "bytes_per_call": rb, "replicas": len(Ws), "n_tok": res}
     del Ws
     return out
 

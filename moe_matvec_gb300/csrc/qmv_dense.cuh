@@ -258,6 +258,10 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT, CW>()
     const int ks = 8 * nu <= CW ? 4 : (4 * nu <= CW ? 2 : 1);
     const int rg = CW / ks;  // warps per part (row groups with rows: 2 * nu <= rg)
     const int grp = cw % rg, part = cw / rg;
+    // residual add: the values this warp adds at the store are requested
+    // into L1 now, so the store does not wait for them
+    if (p.add && part == 0 && lane < ntk && grp * RW < nrows)
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(p.add + (long long)(t0 + lane) * p.M + row0 + grp * RW));
     for (int c = 0; c < nck && alive; c++, ring.advance(p.stages)) {
       const int st = ring.st;
       if (!mbar_wait(&full[st], ring.parity(), p.err)) {
