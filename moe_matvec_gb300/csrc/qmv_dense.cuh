@@ -101,7 +101,9 @@ __device__ __forceinline__ void split_range(const DenseParams& p, int s, int& g0
 // Q8IN: the activations come pre-quantized (bulk copies) instead of as fp32
 // rows quantized while staging; separate instantiations, so each kernel
 // carries only its own staging code.
-template <int F, int NT, bool Q8IN, int CW>
+// ADD: the residual of p.add is added at the store (separate instantiations,
+// so the plain matvec carries none of its code).
+template <int F, int NT, bool Q8IN, int CW, bool ADD>
 __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT, CW>())
     qmv_dense_kernel(const __grid_constant__ CUtensorMap map_tile, const __grid_constant__ CUtensorMap map_unit,
                      const DenseParams p) {
@@ -260,8 +262,9 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT, CW>()
     const int grp = cw % rg, part = cw / rg;
     // residual add: the values this warp adds at the store are requested
     // into L1 now, so the store does not wait for them
-    if (p.add && part == 0 && lane < ntk && grp * RW < nrows)
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(p.add + (long long)(t0 + lane) * p.M + row0 + grp * RW));
+    if constexpr (ADD)
+      if (part == 0 && lane < ntk && grp * RW < nrows)
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(p.add + (long long)(t0 + lane) * p.M + row0 + grp * RW));
     for (int c = 0; c < nck && alive; c++, ring.advance(p.stages)) {
       const int st = ring.st;
       if (!mbar_wait(&full[st], ring.parity(), p.err)) {
@@ -322,7 +325,10 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT, CW>()
         const int o = idx + i, r = o / NT, t = o - r * NT, row = grp * RW + r;
         if (t < ntk && row < nrows) {
           const long long o = (long long)(t0 + t) * p.M + row0 + row;
-          out[o] = p.add ? v[i] + p.add[o] : v[i];
+          if constexpr (ADD)
+            out[o] = v[i] + p.add[o];
+          else
+            out[o] = v[i];
         }
       }
     }

@@ -6,10 +6,10 @@
 
 namespace qmv {
 
-template <int F, int NT, bool Q8IN, int CW>
+template <int F, int NT, bool Q8IN, int CW, bool ADD>
 static cudaError_t launch_dense_nt(const DenseLaunch& L) {
   using SH = Shape<CW>;
-  auto kern = qmv_dense_kernel<F, NT, Q8IN, CW>;
+  auto kern = qmv_dense_kernel<F, NT, Q8IN, CW, ADD>;
   static unsigned long long configured = 0;  // bit per device ordinal
   int dev = 0;
   cudaGetDevice(&dev);
@@ -38,21 +38,23 @@ static cudaError_t launch_dense_nt(const DenseLaunch& L) {
   return cudaLaunchKernelEx(&cfg, kern, L.map_tile, L.map_unit, *L.p);
 }
 
-template <int F, bool Q8IN>
+template <int F, bool Q8IN, bool ADD>
 static cudaError_t launch_dense_src(const DenseLaunch& L) {
   switch (L.nt_tmpl) {
-    case 1: return launch_dense_nt<F, 1, Q8IN, 8>(L);
-    case 2: return launch_dense_nt<F, 2, Q8IN, 8>(L);
-    case 4: return launch_dense_nt<F, 4, Q8IN, 8>(L);
-    case 8: return L.cw == 12 ? launch_dense_nt<F, 8, Q8IN, 12>(L) : launch_dense_nt<F, 8, Q8IN, 8>(L);
-    case 16: return L.cw == 12 ? launch_dense_nt<F, 16, Q8IN, 12>(L) : launch_dense_nt<F, 16, Q8IN, 8>(L);
+    case 1: return launch_dense_nt<F, 1, Q8IN, 8, ADD>(L);
+    case 2: return launch_dense_nt<F, 2, Q8IN, 8, ADD>(L);
+    case 4: return launch_dense_nt<F, 4, Q8IN, 8, ADD>(L);
+    case 8: return L.cw == 12 ? launch_dense_nt<F, 8, Q8IN, 12, ADD>(L) : launch_dense_nt<F, 8, Q8IN, 8, ADD>(L);
+    case 16: return L.cw == 12 ? launch_dense_nt<F, 16, Q8IN, 12, ADD>(L) : launch_dense_nt<F, 16, Q8IN, 8, ADD>(L);
   }
   return cudaErrorInvalidValue;
 }
 
 template <int F>
 static cudaError_t launch_dense_fmt(const DenseLaunch& L) {
-  return L.p->x != nullptr ? launch_dense_src<F, false>(L) : launch_dense_src<F, true>(L);
+  const bool q8 = L.p->x == nullptr, add = L.p->add != nullptr;
+  if (add) return q8 ? launch_dense_src<F, true, true>(L) : launch_dense_src<F, false, true>(L);
+  return q8 ? launch_dense_src<F, true, false>(L) : launch_dense_src<F, false, false>(L);
 }
 
 }  // namespace qmv
