@@ -85,9 +85,21 @@
  *                         arranged as for QMV_Q4_K (byte i: c_i | c_{i+16}<<4)
  *   K % 512 == 0; row bytes = 272 * K / 512.
  *
- * Bytes per weight: Q8_0 1.0625, Q4_K 0.5625, IQ4_XS 0.53125 (the same
- * densities as the GGML formats of the same names; GGUF byte compatibility is
- * not a goal).
+ * QMV_Q5_K ("Castagna Veloce", section "Kernels for the MI50": small-batch
+ *   matvecs for the K-quants q4_K, q5_K, q6_K): superblocks of 256 weights
+ *   = 8 sub-blocks of 32, What = d * sc_j * q - dmin * m_j, q in [0,31],
+ *   sc_j, m_j in [0,63].  Group = 1 superblock, 176 bytes:
+ *     header  bytes 0-15 : as QMV_Q4_K (d, dmin, the sc / m string)
+ *     high    bytes [16+4j, 20+4j): sub-block j, a 32-bit little-endian
+ *                         word whose bit i is bit 4 of q_i
+ *     payload bytes [48+16j, 64+16j): sub-block j; byte i holds bits 0-3 of
+ *                         q_i in its low nibble and of q_{i+16} in its high
+ *   K % 256 == 0; row bytes = 176 * K / 256.  Dense matvecs only (not an
+ *   expert format of moe_qmv_run).
+ *
+ * Bytes per weight: Q8_0 1.0625, Q4_K 0.5625, IQ4_XS 0.53125, Q5_K 0.6875
+ * (the same densities as the GGML formats of the same names; GGUF byte
+ * compatibility is not a goal).
  */
 #ifndef QMV_H
 #define QMV_H
@@ -100,7 +112,7 @@
 extern "C" {
 #endif
 
-enum qmv_format { QMV_Q8_0 = 0, QMV_Q4_K = 1, QMV_IQ4_XS = 2 };
+enum qmv_format { QMV_Q8_0 = 0, QMV_Q4_K = 1, QMV_IQ4_XS = 2, QMV_Q5_K = 3 };
 
 enum qmv_status {
   QMV_OK = 0,

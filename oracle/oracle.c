@@ -8,7 +8,7 @@
  *   - the activation quantizer (per-32 int8 with an fp32 scale), in fp32 as
  *     the rule fixes it, so that integer codes are decided in the same
  *     precision as on the GPU;
- *   - the weight quantizers and dequantizers of Q8_0, Q4_K and IQ4_XS, in
+ *   - the weight quantizers and dequantizers of Q8_0, Q4_K, IQ4_XS and Q5_K, in
  *     fp64, following the byte layouts written out in include/qmv.h;
  *   - the matvec y[t][m] = sum_k What[m][k] * Xhat[t][k] in fp64, plus the
  *     tolerance scale sum_k |What[m][k] * Xhat[t][k]|;
@@ -38,6 +38,7 @@
 #define OR_Q8_0 0
 #define OR_Q4_K 1
 #define OR_IQ4_XS 2
+#define OR_Q5_K 3
 
 static const int8_t OR_CB[16] = {-127, -104, -83, -65, -49, -35, -22, -10,
                                  1,    13,   25,  38,  53,  69,  89,  113};
@@ -90,6 +91,7 @@ int64_t oracle_group_weights(int fmt) {
     case OR_Q8_0: return 256;
     case OR_Q4_K: return 256;
     case OR_IQ4_XS: return 512;
+    case OR_Q5_K: return 256;
   }
   return -1;
 }
@@ -99,6 +101,7 @@ int64_t oracle_group_bytes(int fmt) {
     case OR_Q8_0: return 272;
     case OR_Q4_K: return 144;
     case OR_IQ4_XS: return 272;
+    case OR_Q5_K: return 176;
   }
   return -1;
 }
@@ -264,6 +267,67 @@ static void quant_q4_k_group(const float* w, uint8_t* g) {
   }
 }
 
+/* Q5_K group (256 weights, 176 bytes): bytes 0-1 d, 2-3 dmin (fp16), 4-15
+ * the 6-bit sc / m fields as in Q4_K, 16-47 the fifth bit of every weight
+ * (4 bytes per 32-weight sub-block j, little-endian: bit i is weight i's),
+ * 48-175 the low four bits (16 bytes per sub-block, byte i: weight i in the
+ * low nibble, weight i + 16 in the high nibble).  w = d sc_j q - dmin m_j,
+ * q in [0, 31].  The fit is Q4_K's with 31 steps. */
+static void quant_q5_k_group(const float* w, uint8_t* g) {
+  memset(g, 0, 176);
+  double a[8], bmin[8];
+  for (int j = 0; j < 8; j++) {
+    double lo = 0.0, hi = -INFINITY;
+    for (int i = 0; i < 32; i++) {
+      double v = (double)w[32 * j + i];
+      if (v < lo) lo = v;
+      if (v > hi) hi = v;
+    }
+    a[j] = (hi - lo) / 31.0;
+    bmin[j] = -lo;
+  }
+  double amax = 0.0, bmax = 0.0;
+  for (int j = 0; j < 8; j++) {
+    if (a[j] > amax) amax = a[j];
+    if (bmin[j] > bmax) bmax = bmin[j];
+  }
+  uint16_t d16 = oracle_f64_to_f16(amax / 63.0);
+  uint16_t dm16 = oracle_f64_to_f16(bmax / 63.0);
+  double dv = oracle_f16_to_f64(d16), dmv = oracle_f16_to_f64(dm16);
+  wr16(g, d16);
+  wr16(g + 2, dm16);
+  for (int j = 0; j < 8; j++) {
+    double sc = 0.0, m = 0.0;
+    if (dv > 0.0) {
+      sc = nearbyint(a[j] / dv);
+      if (sc > 63.0) sc = 63.0;
+      if (sc < 0.0) sc = 0.0;
+    }
+    if (dmv > 0.0) {
+      m = nearbyint(bmin[j] / dmv);
+      if (m > 63.0) m = 63.0;
+      if (m < 0.0) m = 0.0;
+    }
+    put_bits(g + 4, 12 * j, 6, (unsigned)sc);
+    put_bits(g + 4, 12 * j + 6, 6, (unsigned)m);
+    double S = dv * sc, O = dmv * m;
+    for (int i = 0; i < 32; i++) {
+      double v = (double)w[32 * j + i];
+      int best = 0;
+      double berr = fabs(v - (S * 0.0 - O));
+      for (int q = 1; q < 32; q++) {
+        double e = fabs(v - (S * (double)q - O));
+        if (e < berr) {
+          berr = e;
+          best = q;
+        }
+      }
+      put_nib(g + 48 + 16 * j, i, (unsigned)best & 15u);
+      put_bits(g + 16 + 4 * j, i, 1, (unsigned)best >> 4);
+    }
+  }
+}
+
 static void quant_iq4_xs_superblock(const float* w, uint8_t* meta, uint8_t* payload) {
   double s[8];
   double smax = 0.0;
@@ -323,6 +387,8 @@ int oracle_quantize(int fmt, const float* w, int64_t M, int64_t K, uint8_t* out)
         quant_q8_0_group(wg, g);
       else if (fmt == OR_Q4_K)
         quant_q4_k_group(wg, g);
+      else if (fmt == OR_Q5_K)
+        quant_q5_k_group(wg, g);
       else
         quant_iq4_xs_group(wg, g);
     }
@@ -351,6 +417,15 @@ static void dequant_row(int fmt, const uint8_t* row, int64_t K, double* out) {
         unsigned sc = get_bits(g + 4, 12 * j, 6), m = get_bits(g + 4, 12 * j + 6, 6);
         for (int i = 0; i < 32; i++) {
           unsigned q = get_nib(g + 16 + 16 * j, i);
+          o[32 * j + i] = d * (double)sc * (double)q - dmin * (double)m;
+        }
+      }
+    } else if (fmt == OR_Q5_K) {
+      double d = oracle_f16_to_f64(rd16(g)), dmin = oracle_f16_to_f64(rd16(g + 2));
+      for (int j = 0; j < 8; j++) {
+        unsigned sc = get_bits(g + 4, 12 * j, 6), m = get_bits(g + 4, 12 * j + 6, 6);
+        for (int i = 0; i < 32; i++) {
+          unsigned q = get_nib(g + 48 + 16 * j, i) | (get_bits(g + 16 + 4 * j, i, 1) << 4);
           o[32 * j + i] = d * (double)sc * (double)q - dmin * (double)m;
         }
       }

@@ -70,6 +70,32 @@ def pack_q4_k(d_bits, dmin_bits, sc, m, q) -> bytes:
     return bytes(g)
 
 
+def pack_q5_k(d_bits, dmin_bits, sc, m, q) -> bytes:
+    """One Q5_K group: fp16 d, dmin; sc[8], m[8] in [0,63]; q[8][32] in [0,31]
+    (low four bits in the nibble area at 48, fifth bits at 16, 4 bytes per
+    sub-block, bit i for weight i)."""
+    g = bytearray(176)
+    g[0], g[1] = d_bits & 0xFF, d_bits >> 8
+    g[2], g[3] = dmin_bits & 0xFF, dmin_bits >> 8
+    for j in range(8):
+        _set_bits(g, 4, 12 * j, 6, int(sc[j]))
+        _set_bits(g, 4, 12 * j + 6, 6, int(m[j]))
+        _put_codes(g, 48 + 16 * j, [int(v) & 15 for v in q[j]])
+        for i in range(32):
+            _set_bits(g, 16 + 4 * j, i, 1, int(q[j][i]) >> 4)
+    return bytes(g)
+
+
+def unpack_q5_k(g):
+    g = bytes(g)
+    d, dmin = g[0] | (g[1] << 8), g[2] | (g[3] << 8)
+    sc = [_get_bits(g, 4, 12 * j, 6) for j in range(8)]
+    m = [_get_bits(g, 4, 12 * j + 6, 6) for j in range(8)]
+    q = [[c | (_get_bits(g, 16 + 4 * j, i, 1) << 4) for i, c in enumerate(_get_codes(g, 48 + 16 * j))]
+         for j in range(8)]
+    return d, dmin, sc, m, q
+
+
 def pack_iq4_xs(d_bits, ls, c) -> bytes:
     """One IQ4_XS group (2 superblocks): d_bits[2]; ls[2][8] in [0,63];
     c[2][8][32] codebook indices."""

@@ -193,7 +193,31 @@ def test_iq4_xs_fields_follow_the_rule_and_codes_are_argmins():
                     assert c[s][j] == np.argmin(err, axis=1).tolist()
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2])
+def test_q5_k_fields_follow_the_rule_and_codes_are_argmins():
+    w = _rand_w(2, 512, seed=11)
+    w[1, :32] = np.abs(w[1, :32])
+    w[1, 32:64] = -np.abs(w[1, 32:64])
+    W = oracle.quantize(3, w)
+    assert W.shape[1] == 2 * 176
+    for m in range(2):
+        for gi in range(2):
+            d_bits, dmin_bits, sc, mm, q = L.unpack_q5_k(W[m, 176 * gi:176 * (gi + 1)])
+            wg = w[m, 256 * gi:256 * (gi + 1)].astype(np.float64).reshape(8, 32)
+            lo = np.minimum(0.0, wg.min(1))
+            a = (wg.max(1) - lo) / 31.0
+            b = -lo
+            assert d_bits == L.f16_bits(a.max() / 63.0)
+            assert dmin_bits == L.f16_bits(b.max() / 63.0)
+            d, dmin = L.f16_value(d_bits), L.f16_value(dmin_bits)
+            assert sc == np.clip(np.rint(a / d), 0, 63).astype(int).tolist()
+            assert mm == np.clip(np.rint(b / dmin), 0, 63).astype(int).tolist()
+            for j in range(8):
+                grid = d * sc[j] * np.arange(32) - dmin * mm[j]
+                err = np.abs(wg[j][:, None] - grid[None, :])
+                assert q[j] == np.argmin(err, axis=1).tolist()
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2, 3])
 def test_zero_weights_dequantize_to_zero(fmt):
     w = _rand_w(2, 512)
     w[0] = 0.0
@@ -215,6 +239,21 @@ def test_round_trip_error_bounds():
     err = np.abs(oracle.dequant(1, W, 1024) - w).reshape(8, 32, 32)
     rngb = (w.reshape(8, 32, 32).max(-1) - np.minimum(0, w.reshape(8, 32, 32).min(-1)))
     assert np.all(err.max(-1) <= rngb / 15.0 * 0.5 * 1.2 + 1e-4)
+    # Q5_K: within half a step of the stored grid, or the distance from the
+    # grid's ends to a weight outside them; smaller on average than Q4_K
+    W = oracle.quantize(3, w.astype(np.float32))
+    err = np.abs(oracle.dequant(3, W, 1024) - w).reshape(8, 4, 8, 32)
+    wb = w.reshape(8, 4, 8, 32)
+    for m in range(8):
+        for gi in range(4):
+            d_bits, dmin_bits, sc, mm, _ = L.unpack_q5_k(W[m, 176 * gi:176 * (gi + 1)])
+            d, dmin = L.f16_value(d_bits), L.f16_value(dmin_bits)
+            for j in range(8):
+                lo_g = -dmin * mm[j]
+                hi_g = lo_g + 31 * d * sc[j]
+                bound = max(d * sc[j] / 2, lo_g - wb[m, gi, j].min(), wb[m, gi, j].max() - hi_g)
+                assert err[m, gi, j].max() <= bound * (1 + 1e-12) + 1e-15
+    assert err.mean() < np.abs(oracle.dequant(1, oracle.quantize(1, w.astype(np.float32)), 1024) - w).mean()
     # IQ4_XS: the largest codebook gap is 24 (89 -> 113), so half a gap is 12 steps
     W = oracle.quantize(2, w.astype(np.float32))
     err = np.abs(oracle.dequant(2, W, 1024) - w).reshape(8, 32, 32)
@@ -264,7 +303,19 @@ def test_dequant_iq4_xs_hand_worked():
     assert wh[0, 256 + 100] == 3.0 * L.CODEBOOK[100 % 32 % 16]
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2])
+def test_dequant_q5_k_hand_worked():
+    q = [[0] * 32 for _ in range(8)]
+    q[0][0], q[0][17], q[3][31], q[7][5] = 31, 16, 15, 1
+    g = L.pack_q5_k(L.f16_bits(0.5), L.f16_bits(0.25), [1, 2, 3, 4, 5, 6, 7, 63], [0, 1, 2, 3, 4, 5, 6, 63], q)
+    wh = oracle.dequant(3, np.frombuffer(g, np.uint8)[None, :], 256)[0]
+    assert wh[0] == 0.5 * 1 * 31                     # fifth bit set, low bits 15
+    assert wh[17] == 0.5 * 1 * 16                    # fifth bit only, high-nibble half
+    assert wh[32 * 3 + 31] == 0.5 * 4 * 15 - 0.25 * 3
+    assert wh[32 * 7 + 5] == 0.5 * 63 * 1 - 0.25 * 63
+    assert wh[32 * 2 + 4] == -0.25 * 2
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2, 3])
 def test_dequant_random_fields(fmt):
     r = np.random.default_rng(fmt + 100)
     if fmt == 0:
@@ -278,6 +329,14 @@ def test_dequant_random_fields(fmt):
         sc, m = r.integers(0, 64, 8).tolist(), r.integers(0, 64, 8).tolist()
         q = r.integers(0, 16, (8, 32)).tolist()
         g = L.pack_q4_k(d, dm, sc, m, q)
+        exp = np.concatenate([L.f16_value(d) * sc[j] * np.array(q[j], float) - L.f16_value(dm) * m[j]
+                              for j in range(8)])
+        K = 256
+    elif fmt == 3:
+        d, dm = L.f16_bits(r.uniform(0, 1)), L.f16_bits(r.uniform(0, 1))
+        sc, m = r.integers(0, 64, 8).tolist(), r.integers(0, 64, 8).tolist()
+        q = r.integers(0, 32, (8, 32)).tolist()
+        g = L.pack_q5_k(d, dm, sc, m, q)
         exp = np.concatenate([L.f16_value(d) * sc[j] * np.array(q[j], float) - L.f16_value(dm) * m[j]
                               for j in range(8)])
         K = 256
@@ -302,7 +361,7 @@ def _xhat(x):
     return q.astype(np.float64) * np.repeat(d.astype(np.float64), 32, axis=1)
 
 
-@pytest.mark.parametrize("fmt,K", [(0, 512), (1, 768), (2, 1024)])
+@pytest.mark.parametrize("fmt,K", [(0, 512), (1, 768), (2, 1024), (3, 768)])
 def test_qmv_matches_library_matmul(fmt, K):
     w = _rand_w(37, K, seed=fmt)
     x = synth.activations(fmt, 5, K)
