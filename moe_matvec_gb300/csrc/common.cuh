@@ -32,6 +32,13 @@ template <>
 struct Fmt<QMV_IQ4_XS> {
   static constexpr int GW = 512, GB = 272;
 };
+template <>
+struct Fmt<QMV_Q5_K> {
+  static constexpr int GW = 256, GB = 176;
+};
+// Formats with a per-sub-block minimum (w = d sc q - dmin m): their min term
+// needs each activation block's code sum.
+__host__ __device__ constexpr bool has_min(int F) { return F == QMV_Q4_K || F == QMV_Q5_K; }
 template <int F>
 constexpr int chunk_bytes() {
   return (KCHUNK / Fmt<F>::GW) * Fmt<F>::GB;

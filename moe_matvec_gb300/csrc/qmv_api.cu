@@ -96,9 +96,11 @@ static bool encode_rows(CUtensorMap* map, const void* W, long long rows, long lo
 // Validation helpers.
 // ---------------------------------------------------------------------------
 static int group_weights(int fmt) { return fmt == QMV_IQ4_XS ? 512 : 256; }
-static int group_bytes(int fmt) { return fmt == QMV_Q4_K ? 144 : 272; }
+static int group_bytes(int fmt) { return fmt == QMV_Q4_K ? 144 : (fmt == QMV_Q5_K ? 176 : 272); }
 static int chunk_bytes_of(int fmt) { return (KCHUNK / group_weights(fmt)) * group_bytes(fmt); }
-static bool fmt_ok(int fmt) { return fmt == QMV_Q8_0 || fmt == QMV_Q4_K || fmt == QMV_IQ4_XS; }
+static bool fmt_ok(int fmt) { return fmt == QMV_Q8_0 || fmt == QMV_Q4_K || fmt == QMV_IQ4_XS || fmt == QMV_Q5_K; }
+// formats the MoE kernels are instantiated for
+static bool moe_fmt_ok(int fmt) { return fmt == QMV_Q8_0 || fmt == QMV_Q4_K || fmt == QMV_IQ4_XS; }
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 constexpr long long MAX_K = 1ll << 20;
 constexpr long long MAX_M = 1ll << 30;
@@ -181,6 +183,7 @@ static cudaError_t launch_dense_any(int fmt, const DenseLaunch& L) {
   switch (fmt) {
     case QMV_Q8_0: return launch_dense_q8_0(L);
     case QMV_Q4_K: return launch_dense_q4_k(L);
+    case QMV_Q5_K: return launch_dense_q5_k(L);
     default: return launch_dense_iq4_xs(L);
   }
 }
@@ -271,7 +274,7 @@ static size_t moe_layout(const moe_experts* e, int n_tok, int top_k, size_t off[
 
 static int check_moe_shape(const moe_experts* e, int n_tok, int top_k) {
   if (!e) return QMV_ERR_NULL;
-  if (!fmt_ok(e->fmt_gate_up) || !fmt_ok(e->fmt_down)) return QMV_ERR_FORMAT;
+  if (!moe_fmt_ok(e->fmt_gate_up) || !moe_fmt_ok(e->fmt_down)) return QMV_ERR_FORMAT;
   if (e->n_experts < 1 || e->n_experts > MOE_MAX_EXPERTS || e->hidden <= 0 || e->ffn <= 0 ||
       e->hidden > MAX_K || e->ffn > MAX_K || e->hidden % group_weights(e->fmt_gate_up) ||
       e->ffn % group_weights(e->fmt_down) || e->hidden % UNIT_ROWS || e->ffn % UNIT_ROWS)

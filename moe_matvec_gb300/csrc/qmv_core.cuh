@@ -68,7 +68,7 @@ __device__ __forceinline__ int act_pos(int l, int p) {
 // of codes, scales or sums is one contiguous piece of the library's
 // pre-quantized activation rows, so those arrive by bulk copies.
 __host__ __device__ constexpr size_t act_area_bytes(int F, int nt_slots, int nck) {
-  return (size_t)nck * nt_slots * (ACT_BYTES + 32 * sizeof(float) * (F == QMV_Q4_K ? 2 : 1));
+  return (size_t)nck * nt_slots * (ACT_BYTES + 32 * sizeof(float) * (has_min(F) ? 2 : 1));
 }
 
 struct ActArea {
@@ -259,7 +259,7 @@ __device__ __forceinline__ void stage_activations(const ActSource& src, int kb0,
       if (li == 0) {
         const int di = a.scale(cc[u], tt[u]) + l[u];
         a.d[di] = dd[u];
-        if constexpr (F == QMV_Q4_K) a.s[di] = ss[u];
+        if constexpr (has_min(F)) a.s[di] = ss[u];
       }
     }
   }
@@ -277,7 +277,7 @@ __device__ __forceinline__ void stage_activations(const ActSource& src, int kb0,
 template <int F, int NT, int CW = CONSUMER_WARPS>
 __device__ __forceinline__ bool stage_q8_bulk(const ActSource& src, int kb0, int nblk, int nt, const ActArea& a,
                                               uint64_t* bar, uint32_t parity, unsigned* err, int cw, int lane) {
-  constexpr int NCOPY = F == QMV_Q4_K ? 3 : 2;
+  constexpr int NCOPY = has_min(F) ? 3 : 2;
   const int nck = (nblk + 31) / 32;
   if (cw == 0 && lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nt * nblk * (32 + 4 * (NCOPY - 1))));
   named_sync(1, CW * 32);  // the byte count is posted before any copy completes
@@ -300,7 +300,7 @@ __device__ __forceinline__ bool stage_q8_bulk(const ActSource& src, int kb0, int
   for (int i = cw * 32 + lane; i < nt * tail; i += CW * 32) {
     const int t = i / tail, b = nb_last + (i - t * tail);
     a.d[a.scale(nck - 1, t) + b] = 0.f;
-    if constexpr (F == QMV_Q4_K) a.s[a.scale(nck - 1, t) + b] = 0;
+    if constexpr (has_min(F)) a.s[a.scale(nck - 1, t) + b] = 0;
   }
   const bool ok = mbar_wait(bar, parity, err);
   if constexpr (F == QMV_IQ4_XS) {
@@ -400,6 +400,7 @@ struct Consumer {
   uint32_t fsh;    // bit offset of that field in the word pair at f_off
   uint32_t a_off;  // the lane's block in a token's activation chunk
   uint32_t d_off;  // the lane's scale in a chunk's scales (token slot 0)
+  uint32_t x_off;  // Q5_K: the word of fifth bits of the lane's block in a row chunk
   uint32_t cb[4];  // IQ4_XS: the codebook words, held in registers for the whole kernel (a
                    // shuffle hides their values, so they are not re-created before every use)
 
@@ -418,6 +419,13 @@ struct Consumer {
       // last fields the second word is the first payload word, unused bits)
       f_off = h_off + 4 + 4 * ((12 * j) >> 5);
       fsh = (12 * j) & 31;
+    } else if constexpr (F == QMV_Q5_K) {
+      const int g = lane >> 3;
+      w_off = g * 176 + 48 + 16 * j;
+      h_off = g * 176;
+      f_off = h_off + 4 + 4 * ((12 * j) >> 5);  // the sc / m string as in Q4_K
+      fsh = (12 * j) & 31;
+      x_off = g * 176 + 16 + 4 * j;
     } else {
       const int g = lane >> 4, sb = (lane >> 3) & 1;
       w_off = g * 272 + 16 + 128 * sb + 16 * j;
@@ -486,6 +494,27 @@ struct Consumer {
         const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&dh));
         sA[r] = dd.x * (float)(f & 63u) * 0.0625f;  // the dot product is 16 x the block sum
         sB[r] = dd.y * (float)((f >> 6) & 63u);
+      } else if constexpr (F == QMV_Q5_K) {
+        const uint32_t dh = lds32(row + h_off);  // d | dmin
+        const uint32_t f0 = lds32(row + f_off);
+        const uint32_t f1 = lds32(row + f_off + 4);
+        const uint32_t hb = lds32(row + x_off);  // bit i: fifth bit of weight i
+        const uint4 q = lds128(row + w_off);
+        const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
+        // codes as unsigned bytes: the low four bits from the nibbles, the
+        // fifth from hb, its four bits for a word spread to the bytes by a
+        // multiply (the shifted copies do not overlap) and moved to bit 4
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+          const uint32_t lo = (((hb >> (4 * i)) & 0xFu) * 0x00204081u) & 0x01010101u;
+          const uint32_t hi = (((hb >> (16 + 4 * i)) & 0xFu) * 0x00204081u) & 0x01010101u;
+          w[r][i] = (qq[i] & 0x0F0F0F0Fu) | (lo << 4);
+          w[r][4 + i] = ((qq[i] >> 4) & 0x0F0F0F0Fu) | (hi << 4);
+        }
+        const uint32_t f = __funnelshift_r(f0, f1, fsh);
+        const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&dh));
+        sA[r] = dd.x * (float)(f & 63u);
+        sB[r] = dd.y * (float)((f >> 6) & 63u);
       } else {
         const uint32_t dw = lds32(row + h_off);
         const uint32_t f0 = lds32(row + f_off);
@@ -511,11 +540,11 @@ struct Consumer {
       const uint4 xb = lds128(ap + 128);
       const float dx = __uint_as_float(lds32(dp));
       float dxs = 0.f;
-      if constexpr (F == QMV_Q4_K) dxs = dx * (float)(int)lds32(sp);
+      if constexpr (has_min(F)) dxs = dx * (float)(int)lds32(sp);
 #pragma unroll
       for (int r = 0; r < RW; r++) {
         float v = fmaf(sA[r] * dx, (float)dot(w[r], xa, xb), acc.v[r][0].x);
-        if constexpr (F == QMV_Q4_K) v = fmaf(-sB[r], dxs, v);
+        if constexpr (has_min(F)) v = fmaf(-sB[r], dxs, v);
         acc.v[r][0].x = v;
       }
     } else {
@@ -537,13 +566,13 @@ struct Consumer {
         const uint4 xb1 = lds128(ap + (t + 1) * sq + 128);
         const float2 dx = make_float2(__uint_as_float(lds32(dp + t * sd)), __uint_as_float(lds32(dp + (t + 1) * sd)));
         float2 dxs = make_float2(0.f, 0.f);
-        if constexpr (F == QMV_Q4_K)
+        if constexpr (has_min(F))
           dxs = __fmul2_rn(dx, make_float2((float)(int)lds32(sp + t * sd), (float)(int)lds32(sp + (t + 1) * sd)));
 #pragma unroll
         for (int r = 0; r < RW; r++) {
           const float2 is = make_float2((float)dot(w[r], xa0, xb0), (float)dot(w[r], xa1, xb1));
           float2 v = __ffma2_rn(__fmul2_rn(sA2[r], dx), is, acc.v[r][t >> 1]);
-          if constexpr (F == QMV_Q4_K) v = __ffma2_rn(nsB2[r], dxs, v);
+          if constexpr (has_min(F)) v = __ffma2_rn(nsB2[r], dxs, v);
           acc.v[r][t >> 1] = v;
         }
       }
@@ -551,7 +580,8 @@ struct Consumer {
   }
 
   // Exact int32 dot product of one 32-weight block with the activation words
-  // xa (elements 0..15 of the block) and xb (16..31).  Q4_K: 16 x the sum
+  // xa (elements 0..15 of the block) and xb (16..31) (Q4_K and Q5_K: unsigned
+  // codes, the min term is added by the caller).  Q4_K: 16 x the sum
   // (both nibble halves weigh 16; sA carries the 1/16).  With one token the
   // two halves run as independent chains.
   __device__ __forceinline__ int dot(const uint32_t (&w)[8], uint4 xa, uint4 xb) const {
@@ -575,6 +605,28 @@ struct Consumer {
         ia = dp4a_us(w[3], xa.w, ia);
         ib = dp4a_us(w[7], xb.w, ib);
         return ia * 16 + ib;
+      }
+    } else if constexpr (F == QMV_Q5_K) {
+      // unsigned codes in [0, 31]; with one token the halves as two chains
+      if constexpr (NT == 1) {
+        int ia = dp4a_us(w[0], xa.x, 0);
+        int ib = dp4a_us(w[4], xb.x, 0);
+        ia = dp4a_us(w[1], xa.y, ia);
+        ib = dp4a_us(w[5], xb.y, ib);
+        ia = dp4a_us(w[2], xa.z, ia);
+        ib = dp4a_us(w[6], xb.z, ib);
+        ia = dp4a_us(w[3], xa.w, ia);
+        ib = dp4a_us(w[7], xb.w, ib);
+        return ia + ib;
+      } else {
+        int s = dp4a_us(w[0], xa.x, 0);
+        s = dp4a_us(w[1], xa.y, s);
+        s = dp4a_us(w[2], xa.z, s);
+        s = dp4a_us(w[3], xa.w, s);
+        s = dp4a_us(w[4], xb.x, s);
+        s = dp4a_us(w[5], xb.y, s);
+        s = dp4a_us(w[6], xb.z, s);
+        return dp4a_us(w[7], xb.w, s);
       }
     } else if constexpr (NT == 1) {
       int ia = __dp4a((int)w[0], (int)xa.x, 0);

@@ -1,5 +1,5 @@
 // Weight quantizers (a preparation step, not part of the decode hot path):
-// fp32 weights -> the library's Q8_0 / Q4_K / IQ4_XS groups.  Each scale is
+// fp32 weights -> the library's Q8_0 / Q4_K / IQ4_XS / Q5_K groups.  Each scale is
 // chosen from its block's range and each code is the nearest grid point, in
 // fp64 with every operation written as an explicitly rounded IEEE intrinsic
 // (no contraction), so the bytes do not depend on the compiler.  One thread
@@ -91,6 +91,51 @@ __device__ void group_q4_k(const float* w, uint8_t* g) {
   }
 }
 
+// Q5_K: Q4_K's fit with 31 steps; the low four bits of each code go to the
+// nibble area at byte 48, the fifth to the bit words at byte 16.
+__device__ void group_q5_k(const float* w, uint8_t* g) {
+  double a[8], bm[8], amax = 0.0, bmax = 0.0;
+  for (int j = 0; j < 8; j++) {
+    double lo = 0.0, hi = -INFINITY;
+    for (int i = 0; i < 32; i++) {
+      const double v = (double)w[32 * j + i];
+      lo = fmin(lo, v);
+      hi = fmax(hi, v);
+    }
+    a[j] = __ddiv_rn(__dsub_rn(hi, lo), 31.0);
+    bm[j] = -lo;
+    amax = fmax(amax, a[j]);
+    bmax = fmax(bmax, bm[j]);
+  }
+  const uint16_t d16 = f16_bits(__ddiv_rn(amax, 63.0)), dm16 = f16_bits(__ddiv_rn(bmax, 63.0));
+  const double dv = f16_val(d16), dmv = f16_val(dm16);
+  g[0] = (uint8_t)(d16 & 0xFF);
+  g[1] = (uint8_t)(d16 >> 8);
+  g[2] = (uint8_t)(dm16 & 0xFF);
+  g[3] = (uint8_t)(dm16 >> 8);
+  for (int j = 0; j < 8; j++) {
+    const double sc = dv > 0.0 ? clampd(rint(__ddiv_rn(a[j], dv)), 0.0, 63.0) : 0.0;
+    const double m = dmv > 0.0 ? clampd(rint(__ddiv_rn(bm[j], dmv)), 0.0, 63.0) : 0.0;
+    put_bits(g + 4, 12 * j, 6, (unsigned)sc);
+    put_bits(g + 4, 12 * j + 6, 6, (unsigned)m);
+    const double S = __dmul_rn(dv, sc), O = __dmul_rn(dmv, m);
+    for (int i = 0; i < 32; i++) {
+      const double v = (double)w[32 * j + i];
+      int best = 0;
+      double berr = fabs(__dsub_rn(v, __dsub_rn(__dmul_rn(S, 0.0), O)));
+      for (int q = 1; q < 32; q++) {
+        const double e = fabs(__dsub_rn(v, __dsub_rn(__dmul_rn(S, (double)q), O)));
+        if (e < berr) {
+          berr = e;
+          best = q;
+        }
+      }
+      put_nib(g + 48 + 16 * j, i, (unsigned)best & 15u);
+      put_bits(g + 16 + 4 * j, i, 1, (unsigned)best >> 4);
+    }
+  }
+}
+
 __device__ void superblock_iq4_xs(const float* w, uint8_t* meta, uint8_t* payload) {
   const double cb[16] = {-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113};
   double s[8], smax = 0.0;
@@ -140,6 +185,8 @@ __global__ void __launch_bounds__(128) quantize_kernel(const float* __restrict__
       group_q8_0(src, g);
     else if constexpr (F == QMV_Q4_K)
       group_q4_k(src, g);
+    else if constexpr (F == QMV_Q5_K)
+      group_q5_k(src, g);
     else {
       superblock_iq4_xs(src, g, g + 16);
       superblock_iq4_xs(src + 256, g + 8, g + 16 + 128);
@@ -161,6 +208,7 @@ cudaError_t launch_quantize_weights(int fmt, const float* w, long long M, int K,
   switch (fmt) {
     case QMV_Q8_0: quantize_kernel<QMV_Q8_0><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
     case QMV_Q4_K: quantize_kernel<QMV_Q4_K><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
+    case QMV_Q5_K: quantize_kernel<QMV_Q5_K><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
     default: quantize_kernel<QMV_IQ4_XS><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
   }
   return cudaGetLastError();

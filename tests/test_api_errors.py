@@ -18,6 +18,7 @@ def L():
 
 def test_qmv_run_rejects_bad_arguments(L):
     assert L.qmv_run(7, A, A, A, 16, 256, 1, None) == -1
+    assert L.qmv_run(3, A, A, A, 16, 100, 1, None) == -2        # Q5_K needs K % 256
     assert L.qmv_run(0, A, A, A, 0, 256, 1, None) == -2
     assert L.qmv_run(0, A, A, A, 16, 100, 1, None) == -2
     assert L.qmv_run(2, A, A, A, 16, 256, 1, None) == -2        # IQ4_XS needs K % 512
@@ -42,7 +43,7 @@ def test_quantize_entry_points_reject_bad_arguments(L):
     assert L.qmv_quantize_act(A, 100, 1, A, A, A, None) == -2
     assert L.qmv_quantize_act(A, 256, 0, A, A, A, None) == -3
     assert L.qmv_quantize_act(A, 256, 1, A, None, A, None) == -4
-    assert L.qmv_quantize_weights(3, A, 4, 256, A, None) == -1
+    assert L.qmv_quantize_weights(4, A, 4, 256, A, None) == -1
     assert L.qmv_quantize_weights(1, A, 4, 128, A, None) == -2
     assert L.qmv_quantize_weights(1, A, 4, 256, MIS, None) == -5
 
