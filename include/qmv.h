@@ -97,9 +97,25 @@
  *   K % 256 == 0; row bytes = 176 * K / 256.  Dense matvecs only (not an
  *   expert format of moe_qmv_run).
  *
+ * QMV_Q6_K (same passage): superblocks of 256 weights = 16 sub-blocks of
+ *   16, What = d * sc_i * (q - 32), q in [0,63], sc_i in [0,127].  Each code
+ *   is stored as v = (q - 32) mod 64 (6-bit two's complement).
+ *   Group = 1 superblock, 208 bytes:
+ *     header  bytes 0-1 : d (fp16);  bytes 2-15: 112-bit string, bits
+ *                         [7i, 7i+7) = sc_i (i = 0..15)
+ *     high    bytes [16+8j, 24+8j): 32-weight block j (sub-blocks 2j, 2j+1),
+ *                         two 32-bit little-endian words, the first for
+ *                         weights 0..15, the second for 16..31; weight e of a
+ *                         word (k = e / 4, b = e % 4) has bits 4-5 of its v at
+ *                         bits [8b + 2k, 8b + 2k + 2)
+ *     payload bytes [80+16j, 96+16j): block j; byte i holds bits 0-3 of v_i
+ *                         in its low nibble and of v_{i+16} in its high
+ *   K % 256 == 0; row bytes = 208 * K / 256.  Dense matvecs only.
+ *
  * Bytes per weight: Q8_0 1.0625, Q4_K 0.5625, IQ4_XS 0.53125, Q5_K 0.6875
- * (the same densities as the GGML formats of the same names; GGUF byte
- * compatibility is not a goal).
+ * (the same densities as the GGML formats of the same names), Q6_K 0.8125
+ * (7-bit sub-scales instead of GGML's 8-bit ones); GGUF byte compatibility is
+ * not a goal.
  */
 #ifndef QMV_H
 #define QMV_H
@@ -112,7 +128,7 @@
 extern "C" {
 #endif
 
-enum qmv_format { QMV_Q8_0 = 0, QMV_Q4_K = 1, QMV_IQ4_XS = 2, QMV_Q5_K = 3 };
+enum qmv_format { QMV_Q8_0 = 0, QMV_Q4_K = 1, QMV_IQ4_XS = 2, QMV_Q5_K = 3, QMV_Q6_K = 4 };
 
 enum qmv_status {
   QMV_OK = 0,

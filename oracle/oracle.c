@@ -8,7 +8,7 @@
  *   - the activation quantizer (per-32 int8 with an fp32 scale), in fp32 as
  *     the rule fixes it, so that integer codes are decided in the same
  *     precision as on the GPU;
- *   - the weight quantizers and dequantizers of Q8_0, Q4_K, IQ4_XS and Q5_K, in
+ *   - the weight quantizers and dequantizers of Q8_0, Q4_K, IQ4_XS, Q5_K and Q6_K, in
  *     fp64, following the byte layouts written out in include/qmv.h;
  *   - the matvec y[t][m] = sum_k What[m][k] * Xhat[t][k] in fp64, plus the
  *     tolerance scale sum_k |What[m][k] * Xhat[t][k]|;
@@ -39,6 +39,7 @@
 #define OR_Q4_K 1
 #define OR_IQ4_XS 2
 #define OR_Q5_K 3
+#define OR_Q6_K 4
 
 static const int8_t OR_CB[16] = {-127, -104, -83, -65, -49, -35, -22, -10,
                                  1,    13,   25,  38,  53,  69,  89,  113};
@@ -92,6 +93,7 @@ int64_t oracle_group_weights(int fmt) {
     case OR_Q4_K: return 256;
     case OR_IQ4_XS: return 512;
     case OR_Q5_K: return 256;
+    case OR_Q6_K: return 256;
   }
   return -1;
 }
@@ -102,6 +104,7 @@ int64_t oracle_group_bytes(int fmt) {
     case OR_Q4_K: return 144;
     case OR_IQ4_XS: return 272;
     case OR_Q5_K: return 176;
+    case OR_Q6_K: return 208;
   }
   return -1;
 }
@@ -328,6 +331,67 @@ static void quant_q5_k_group(const float* w, uint8_t* g) {
   }
 }
 
+/* Q6_K group (256 weights = 16 sub-blocks of 16, 208 bytes): bytes 0-1 d
+ * (fp16), bytes 2-15 a 112-bit string of 7-bit sub-scales (bits [7i, 7i+7)
+ * = sc_i), bytes 16-79 the top two bits and bytes 80-207 the low four bits
+ * of each 6-bit code v = (q - 32) mod 64, q in [0, 63].  w = d sc_i (q - 32).
+ * Per 32-weight block j (sub-blocks 2j and 2j+1): two 32-bit words at
+ * 16 + 8j (weights 0..15, then 16..31 of the block), weight e of a word
+ * (k = e / 4, b = e % 4) at bits [8b + 2k, 8b + 2k + 2); 16 nibble bytes at
+ * 80 + 16j as in Q4_K (byte i: weight i low, weight i + 16 high).  The fit:
+ * s_i = amax_i / 31, d = max s_i / 127 (fp16), sc_i = clamp(rne(s_i / d16),
+ * 0, 127), q = argmin over 0..63 of |w - d16 sc_i (q - 32)|, ties to the
+ * lower q. */
+static void q6_k_put(uint8_t* g, int j, int i, unsigned v) {
+  put_nib(g + 80 + 16 * j, i, v & 15u);
+  const int e = i & 15, word = i >> 4;
+  put_bits(g + 16 + 8 * j + 4 * word, 8 * (e & 3) + 2 * (e >> 2), 2, v >> 4);
+}
+static unsigned q6_k_get(const uint8_t* g, int j, int i) {
+  const int e = i & 15, word = i >> 4;
+  return get_nib(g + 80 + 16 * j, i) | (get_bits(g + 16 + 8 * j + 4 * word, 8 * (e & 3) + 2 * (e >> 2), 2) << 4);
+}
+static void quant_q6_k_group(const float* w, uint8_t* g) {
+  memset(g, 0, 208);
+  double s[16], smax = 0.0;
+  for (int i = 0; i < 16; i++) {
+    double amax = 0.0;
+    for (int k = 0; k < 16; k++) {
+      double v = fabs((double)w[16 * i + k]);
+      if (v > amax) amax = v;
+    }
+    s[i] = amax / 31.0;
+    if (s[i] > smax) smax = s[i];
+  }
+  uint16_t d16 = oracle_f64_to_f16(smax / 127.0);
+  double dv = oracle_f16_to_f64(d16);
+  wr16(g, d16);
+  for (int i = 0; i < 16; i++) {
+    double sc = 0.0;
+    if (dv > 0.0) {
+      sc = nearbyint(s[i] / dv);
+      if (sc > 127.0) sc = 127.0;
+      if (sc < 0.0) sc = 0.0;
+    }
+    put_bits(g + 2, 7 * i, 7, (unsigned)sc);
+    double S = dv * sc;
+    for (int k = 0; k < 16; k++) {
+      double v = (double)w[16 * i + k];
+      int best = 0;
+      double berr = fabs(v - S * -32.0);
+      for (int q = 1; q < 64; q++) {
+        double e = fabs(v - S * (double)(q - 32));
+        if (e < berr) {
+          berr = e;
+          best = q;
+        }
+      }
+      const int el = 16 * i + k;  /* weight index in the group */
+      q6_k_put(g, el >> 5, el & 31, (unsigned)(best - 32) & 63u);
+    }
+  }
+}
+
 static void quant_iq4_xs_superblock(const float* w, uint8_t* meta, uint8_t* payload) {
   double s[8];
   double smax = 0.0;
@@ -389,6 +453,8 @@ int oracle_quantize(int fmt, const float* w, int64_t M, int64_t K, uint8_t* out)
         quant_q4_k_group(wg, g);
       else if (fmt == OR_Q5_K)
         quant_q5_k_group(wg, g);
+      else if (fmt == OR_Q6_K)
+        quant_q6_k_group(wg, g);
       else
         quant_iq4_xs_group(wg, g);
     }
@@ -428,6 +494,14 @@ static void dequant_row(int fmt, const uint8_t* row, int64_t K, double* out) {
           unsigned q = get_nib(g + 48 + 16 * j, i) | (get_bits(g + 16 + 4 * j, i, 1) << 4);
           o[32 * j + i] = d * (double)sc * (double)q - dmin * (double)m;
         }
+      }
+    } else if (fmt == OR_Q6_K) {
+      double d = oracle_f16_to_f64(rd16(g));
+      for (int el = 0; el < 256; el++) {
+        unsigned sc = get_bits(g + 2, 7 * (el >> 4), 7);
+        unsigned v = q6_k_get(g, el >> 5, el & 31);
+        int q32 = (int)v - ((v & 32u) ? 64 : 0);  /* q - 32 */
+        o[el] = d * (double)sc * (double)q32;
       }
     } else {
       for (int sb = 0; sb < 2; sb++) {

@@ -96,6 +96,42 @@ def unpack_q5_k(g):
     return d, dmin, sc, m, q
 
 
+def _q6_pos(j, i):
+    """(byte offset of the word, bit) of the top two bits of weight i of block j."""
+    e, word = i % 16, i // 16
+    return 16 + 8 * j + 4 * word, 8 * (e % 4) + 2 * (e // 4)
+
+
+def pack_q6_k(d_bits, sc, q) -> bytes:
+    """One Q6_K group: fp16 d; sc[16] in [0,127] (one per 16 weights);
+    q[256] in [0,63] (w = d sc (q - 32)), stored as v = (q - 32) mod 64."""
+    g = bytearray(208)
+    g[0], g[1] = d_bits & 0xFF, d_bits >> 8
+    for i in range(16):
+        _set_bits(g, 2, 7 * i, 7, int(sc[i]))
+    for j in range(8):
+        v = [(int(q[32 * j + i]) - 32) % 64 for i in range(32)]
+        _put_codes(g, 80 + 16 * j, [x & 15 for x in v])
+        for i in range(32):
+            off, bit = _q6_pos(j, i)
+            _set_bits(g, off, bit, 2, v[i] >> 4)
+    return bytes(g)
+
+
+def unpack_q6_k(g):
+    g = bytes(g)
+    d = g[0] | (g[1] << 8)
+    sc = [_get_bits(g, 2, 7 * i, 7) for i in range(16)]
+    q = []
+    for j in range(8):
+        low = _get_codes(g, 80 + 16 * j)
+        for i in range(32):
+            off, bit = _q6_pos(j, i)
+            v = low[i] | (_get_bits(g, off, bit, 2) << 4)
+            q.append((v + 32) % 64)
+    return d, sc, q
+
+
 def pack_iq4_xs(d_bits, ls, c) -> bytes:
     """One IQ4_XS group (2 superblocks): d_bits[2]; ls[2][8] in [0,63];
     c[2][8][32] codebook indices."""

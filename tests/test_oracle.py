@@ -217,7 +217,26 @@ def test_q5_k_fields_follow_the_rule_and_codes_are_argmins():
                 assert q[j] == np.argmin(err, axis=1).tolist()
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2, 3])
+def test_q6_k_fields_follow_the_rule_and_codes_are_argmins():
+    w = _rand_w(2, 512, seed=13)
+    w[1, :16] = np.abs(w[1, :16])
+    W = oracle.quantize(4, w)
+    assert W.shape[1] == 2 * 208
+    for m in range(2):
+        for gi in range(2):
+            d_bits, sc, q = L.unpack_q6_k(W[m, 208 * gi:208 * (gi + 1)])
+            wg = w[m, 256 * gi:256 * (gi + 1)].astype(np.float64).reshape(16, 16)
+            s_i = np.abs(wg).max(1) / 31.0
+            assert d_bits == L.f16_bits(s_i.max() / 127.0)
+            d = L.f16_value(d_bits)
+            assert sc == np.clip(np.rint(s_i / d), 0, 127).astype(int).tolist()
+            for i in range(16):
+                grid = d * sc[i] * (np.arange(64) - 32)
+                err = np.abs(wg[i][:, None] - grid[None, :])
+                assert q[16 * i:16 * i + 16] == np.argmin(err, axis=1).tolist()
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2, 3, 4])
 def test_zero_weights_dequantize_to_zero(fmt):
     w = _rand_w(2, 512)
     w[0] = 0.0
@@ -254,6 +273,18 @@ def test_round_trip_error_bounds():
                 bound = max(d * sc[j] / 2, lo_g - wb[m, gi, j].min(), wb[m, gi, j].max() - hi_g)
                 assert err[m, gi, j].max() <= bound * (1 + 1e-12) + 1e-15
     assert err.mean() < np.abs(oracle.dequant(1, oracle.quantize(1, w.astype(np.float32)), 1024) - w).mean()
+    # Q6_K: within half a step of the stored grid (it covers +-31 steps of s_i = amax / 31)
+    W = oracle.quantize(4, w.astype(np.float32))
+    err = np.abs(oracle.dequant(4, W, 1024) - w).reshape(8, 4, 16, 16)
+    for m in range(8):
+        for gi in range(4):
+            d_bits, sc, _ = L.unpack_q6_k(W[m, 208 * gi:208 * (gi + 1)])
+            d = L.f16_value(d_bits)
+            wb = np.abs(w.reshape(8, 4, 16, 16)[m, gi])
+            for i in range(16):
+                step = d * sc[i]
+                bound = max(step / 2, wb[i].max() - 31 * step)
+                assert err[m, gi, i].max() <= bound * (1 + 1e-12) + 1e-15
     # IQ4_XS: the largest codebook gap is 24 (89 -> 113), so half a gap is 12 steps
     W = oracle.quantize(2, w.astype(np.float32))
     err = np.abs(oracle.dequant(2, W, 1024) - w).reshape(8, 32, 32)
@@ -315,7 +346,21 @@ def test_dequant_q5_k_hand_worked():
     assert wh[32 * 2 + 4] == -0.25 * 2
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2, 3])
+def test_dequant_q6_k_hand_worked():
+    q = [32] * 256
+    q[0], q[17], q[40], q[255] = 63, 0, 33, 31
+    sc = list(range(1, 17))
+    sc[15] = 127
+    g = L.pack_q6_k(L.f16_bits(0.5), sc, q)
+    wh = oracle.dequant(4, np.frombuffer(g, np.uint8)[None, :], 256)[0]
+    assert wh[0] == 0.5 * 1 * 31
+    assert wh[17] == 0.5 * 2 * -32                   # sub-block 1 (weights 16..31)
+    assert wh[40] == 0.5 * 3 * 1
+    assert wh[255] == 0.5 * 127 * -1
+    assert wh[100] == 0.0
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2, 3, 4])
 def test_dequant_random_fields(fmt):
     r = np.random.default_rng(fmt + 100)
     if fmt == 0:
@@ -331,6 +376,13 @@ def test_dequant_random_fields(fmt):
         g = L.pack_q4_k(d, dm, sc, m, q)
         exp = np.concatenate([L.f16_value(d) * sc[j] * np.array(q[j], float) - L.f16_value(dm) * m[j]
                               for j in range(8)])
+        K = 256
+    elif fmt == 4:
+        d = L.f16_bits(r.uniform(-1, 1))
+        sc = r.integers(0, 128, 16).tolist()
+        q = r.integers(0, 64, 256).tolist()
+        g = L.pack_q6_k(d, sc, q)
+        exp = np.array([L.f16_value(d) * sc[e // 16] * (q[e] - 32) for e in range(256)], float)
         K = 256
     elif fmt == 3:
         d, dm = L.f16_bits(r.uniform(0, 1)), L.f16_bits(r.uniform(0, 1))
@@ -361,7 +413,7 @@ def _xhat(x):
     return q.astype(np.float64) * np.repeat(d.astype(np.float64), 32, axis=1)
 
 
-@pytest.mark.parametrize("fmt,K", [(0, 512), (1, 768), (2, 1024), (3, 768)])
+@pytest.mark.parametrize("fmt,K", [(0, 512), (1, 768), (2, 1024), (3, 768), (4, 512)])
 def test_qmv_matches_library_matmul(fmt, K):
     w = _rand_w(37, K, seed=fmt)
     x = synth.activations(fmt, 5, K)
