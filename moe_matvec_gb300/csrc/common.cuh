@@ -36,6 +36,10 @@ template <>
 struct Fmt<QMV_Q5_K> {
   static constexpr int GW = 256, GB = 176;
 };
+template <>
+struct Fmt<QMV_Q6_K> {
+  static constexpr int GW = 256, GB = 208;
+};
 // Formats with a per-sub-block minimum (w = d sc q - dmin m): their min term
 // needs each activation block's code sum.
 __host__ __device__ constexpr bool has_min(int F) { return F == QMV_Q4_K || F == QMV_Q5_K; }

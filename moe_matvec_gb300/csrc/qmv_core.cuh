@@ -426,6 +426,14 @@ struct Consumer {
       f_off = h_off + 4 + 4 * ((12 * j) >> 5);  // the sc / m string as in Q4_K
       fsh = (12 * j) & 31;
       x_off = g * 176 + 16 + 4 * j;
+    } else if constexpr (F == QMV_Q6_K) {
+      const int g = lane >> 3;
+      w_off = g * 208 + 80 + 16 * j;
+      h_off = g * 208;
+      // sc_{2j}, sc_{2j+1}: bits [14j, 14j + 14) of the 112-bit string at byte 2
+      f_off = h_off + 4 * ((16 + 14 * j) >> 5);
+      fsh = (16 + 14 * j) & 31;
+      x_off = g * 208 + 16 + 8 * j;
     } else {
       const int g = lane >> 4, sb = (lane >> 3) & 1;
       w_off = g * 272 + 16 + 128 * sb + 16 * j;
@@ -462,6 +470,7 @@ struct Consumer {
     constexpr int CB = chunk_bytes<F>();
     uint32_t w[RW][8];  // decoded operands, paired with activation words 0..7
     float sA[RW];       // multiplier of d_x * isum
+    int scl[RW] = {}, sch[RW] = {};  // Q6_K: the integer sub-scales of weights 0..15 and 16..31
     float sB[RW];       // Q4_K: dmin * m, multiplier of d_x * s
 #pragma unroll
     for (int r = 0; r < RW; r++) {
@@ -515,6 +524,26 @@ struct Consumer {
         const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&dh));
         sA[r] = dd.x * (float)(f & 63u);
         sB[r] = dd.y * (float)((f >> 6) & 63u);
+      } else if constexpr (F == QMV_Q6_K) {
+        const uint32_t dw = lds32(row + h_off);
+        const uint32_t f0 = lds32(row + f_off);
+        const uint32_t f1 = lds32(row + f_off + 4);
+        const uint2 hb = lds64(row + x_off);  // top two bits: weights 0..15, 16..31
+        const uint4 q = lds128(row + w_off);
+        const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
+        // each code byte is v << 2 = 4 (q - 32) as int8: the low four bits
+        // from the nibbles at bits 2-5, the top two at bits 6-7 (word k of
+        // a half keeps them at bits 8b + 2k of its bit word)
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+          w[r][i] = ((qq[i] << 2) & 0x3C3C3C3Cu) | ((hb.x << (6 - 2 * i)) & 0xC0C0C0C0u);
+          w[r][4 + i] = ((qq[i] >> 2) & 0x3C3C3C3Cu) | ((hb.y << (6 - 2 * i)) & 0xC0C0C0C0u);
+        }
+        const uint32_t f = __funnelshift_r(f0, f1, fsh);
+        scl[r] = (int)(f & 127u);
+        sch[r] = (int)((f >> 7) & 127u);
+        sA[r] = __half2float(__ushort_as_half((unsigned short)(dw & 0xFFFF))) * 0.25f;  // the dots are 4 x
+        sB[r] = 0.f;
       } else {
         const uint32_t dw = lds32(row + h_off);
         const uint32_t f0 = lds32(row + f_off);
@@ -543,7 +572,7 @@ struct Consumer {
       if constexpr (has_min(F)) dxs = dx * (float)(int)lds32(sp);
 #pragma unroll
       for (int r = 0; r < RW; r++) {
-        float v = fmaf(sA[r] * dx, (float)dot(w[r], xa, xb), acc.v[r][0].x);
+        float v = fmaf(sA[r] * dx, (float)dotr(w[r], xa, xb, scl[r], sch[r]), acc.v[r][0].x);
         if constexpr (has_min(F)) v = fmaf(-sB[r], dxs, v);
         acc.v[r][0].x = v;
       }
@@ -570,12 +599,33 @@ struct Consumer {
           dxs = __fmul2_rn(dx, make_float2((float)(int)lds32(sp + t * sd), (float)(int)lds32(sp + (t + 1) * sd)));
 #pragma unroll
         for (int r = 0; r < RW; r++) {
-          const float2 is = make_float2((float)dot(w[r], xa0, xb0), (float)dot(w[r], xa1, xb1));
+          const float2 is = make_float2((float)dotr(w[r], xa0, xb0, scl[r], sch[r]), (float)dotr(w[r], xa1, xb1, scl[r], sch[r]));
           float2 v = __ffma2_rn(__fmul2_rn(sA2[r], dx), is, acc.v[r][t >> 1]);
           if constexpr (has_min(F)) v = __ffma2_rn(nsB2[r], dxs, v);
           acc.v[r][t >> 1] = v;
         }
       }
+    }
+  }
+
+  // The block's integer dot product with its sub-scales applied (Q6_K: two
+  // halves of 16 weights, each with its own integer scale; other formats
+  // have one scale per block, carried in sA, and ignore lo / hi).
+  __device__ __forceinline__ int dotr(const uint32_t (&w)[8], uint4 xa, uint4 xb, int lo, int hi) const {
+    if constexpr (F == QMV_Q6_K) {
+      int ia = __dp4a((int)w[0], (int)xa.x, 0);
+      int ib = __dp4a((int)w[4], (int)xb.x, 0);
+      ia = __dp4a((int)w[1], (int)xa.y, ia);
+      ib = __dp4a((int)w[5], (int)xb.y, ib);
+      ia = __dp4a((int)w[2], (int)xa.z, ia);
+      ib = __dp4a((int)w[6], (int)xb.z, ib);
+      ia = __dp4a((int)w[3], (int)xa.w, ia);
+      ib = __dp4a((int)w[7], (int)xb.w, ib);
+      return ia * lo + ib * hi;  // |4 x 16 x 128 x 127| x 127 x 2 < 2^31
+    } else {
+      (void)lo;
+      (void)hi;
+      return dot(w, xa, xb);
     }
   }
 

@@ -1,5 +1,5 @@
 // Weight quantizers (a preparation step, not part of the decode hot path):
-// fp32 weights -> the library's Q8_0 / Q4_K / IQ4_XS / Q5_K groups.  Each scale is
+// fp32 weights -> the library's Q8_0 / Q4_K / IQ4_XS / Q5_K / Q6_K groups.  Each scale is
 // chosen from its block's range and each code is the nearest grid point, in
 // fp64 with every operation written as an explicitly rounded IEEE intrinsic
 // (no contraction), so the bytes do not depend on the compiler.  One thread
@@ -136,6 +136,45 @@ __device__ void group_q5_k(const float* w, uint8_t* g) {
   }
 }
 
+// Q6_K: per 16 weights s_i = amax_i / 31, d = max s_i / 127, 7-bit sc_i;
+// codes v = (q - 32) mod 64, low four bits in the nibble area at byte 80,
+// the top two in the block's bit words at byte 16 (weight e of a word at
+// bit 8 (e % 4) + 2 (e / 4)).
+__device__ void group_q6_k(const float* w, uint8_t* g) {
+  double s[16], smax = 0.0;
+  for (int i = 0; i < 16; i++) {
+    double amax = 0.0;
+    for (int k = 0; k < 16; k++) amax = fmax(amax, fabs((double)w[16 * i + k]));
+    s[i] = __ddiv_rn(amax, 31.0);
+    smax = fmax(smax, s[i]);
+  }
+  const uint16_t d16 = f16_bits(__ddiv_rn(smax, 127.0));
+  const double dv = f16_val(d16);
+  g[0] = (uint8_t)(d16 & 0xFF);
+  g[1] = (uint8_t)(d16 >> 8);
+  for (int i = 0; i < 16; i++) {
+    const double sc = dv > 0.0 ? clampd(rint(__ddiv_rn(s[i], dv)), 0.0, 127.0) : 0.0;
+    put_bits(g + 2, 7 * i, 7, (unsigned)sc);
+    const double S = __dmul_rn(dv, sc);
+    for (int k = 0; k < 16; k++) {
+      const double v = (double)w[16 * i + k];
+      int best = 0;
+      double berr = fabs(__dsub_rn(v, __dmul_rn(S, -32.0)));
+      for (int q = 1; q < 64; q++) {
+        const double e = fabs(__dsub_rn(v, __dmul_rn(S, (double)(q - 32))));
+        if (e < berr) {
+          berr = e;
+          best = q;
+        }
+      }
+      const int el = 16 * i + k, j = el >> 5, ii = el & 31, e = ii & 15;
+      const unsigned code = (unsigned)(best - 32) & 63u;
+      put_nib(g + 80 + 16 * j, ii, code & 15u);
+      put_bits(g + 16 + 8 * j + 4 * (ii >> 4), 8 * (e & 3) + 2 * (e >> 2), 2, code >> 4);
+    }
+  }
+}
+
 __device__ void superblock_iq4_xs(const float* w, uint8_t* meta, uint8_t* payload) {
   const double cb[16] = {-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113};
   double s[8], smax = 0.0;
@@ -187,6 +226,8 @@ __global__ void __launch_bounds__(128) quantize_kernel(const float* __restrict__
       group_q4_k(src, g);
     else if constexpr (F == QMV_Q5_K)
       group_q5_k(src, g);
+    else if constexpr (F == QMV_Q6_K)
+      group_q6_k(src, g);
     else {
       superblock_iq4_xs(src, g, g + 16);
       superblock_iq4_xs(src + 256, g + 8, g + 16 + 128);
@@ -209,6 +250,7 @@ cudaError_t launch_quantize_weights(int fmt, const float* w, long long M, int K,
     case QMV_Q8_0: quantize_kernel<QMV_Q8_0><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
     case QMV_Q4_K: quantize_kernel<QMV_Q4_K><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
     case QMV_Q5_K: quantize_kernel<QMV_Q5_K><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
+    case QMV_Q6_K: quantize_kernel<QMV_Q6_K><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
     default: quantize_kernel<QMV_IQ4_XS><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
   }
   return cudaGetLastError();
