@@ -112,10 +112,21 @@
  *                         in its low nibble and of v_{i+16} in its high
  *   K % 256 == 0; row bytes = 208 * K / 256.  Dense matvecs only.
  *
+ * QMV_Q8_G64, QMV_Q8_G128 ("Running GLM-5.3 on Two 8-GPU AMD W7900D
+ *   Machines", section "Why 4-bit today: room for 5/6-bit, but not FP8": KV in
+ *   Q8G64, the LM head in Q8G128): What = d_s * q, q int8, one fp16 d_s
+ *   per 64 (G64) or 128 (G128) consecutive weights.  Group = 8 scale groups
+ *   (512 or 1024 weights), 16 + 512 = 528 or 16 + 1024 = 1040 bytes:
+ *     header  bytes [2s, 2s+2): d_s (s = 0..7)
+ *     payload bytes [256h, 256h+256) after the header: weights 256h..256h+255
+ *             of the group, laid out as a QMV_Q8_0 payload (block j of the
+ *             256: q_0..15 at 16j, q_16..31 at 128+16j)
+ *   K % 512 (G64) or K % 1024 (G128) == 0.  Dense matvecs only.
+ *
  * Bytes per weight: Q8_0 1.0625, Q4_K 0.5625, IQ4_XS 0.53125, Q5_K 0.6875
  * (the same densities as the GGML formats of the same names), Q6_K 0.8125
- * (7-bit sub-scales instead of GGML's 8-bit ones); GGUF byte compatibility is
- * not a goal.
+ * (7-bit sub-scales instead of GGML's 8-bit ones), Q8_G64 1.03125, Q8_G128
+ * 1.015625; GGUF byte compatibility is not a goal.
  */
 #ifndef QMV_H
 #define QMV_H
@@ -128,7 +139,15 @@
 extern "C" {
 #endif
 
-enum qmv_format { QMV_Q8_0 = 0, QMV_Q4_K = 1, QMV_IQ4_XS = 2, QMV_Q5_K = 3, QMV_Q6_K = 4 };
+enum qmv_format {
+  QMV_Q8_0 = 0,
+  QMV_Q4_K = 1,
+  QMV_IQ4_XS = 2,
+  QMV_Q5_K = 3,
+  QMV_Q6_K = 4,
+  QMV_Q8_G64 = 5,
+  QMV_Q8_G128 = 6
+};
 
 enum qmv_status {
   QMV_OK = 0,

@@ -18,11 +18,12 @@ import threading
 
 import numpy as np
 
-Q8_0, Q4_K, IQ4_XS, Q5_K, Q6_K = 0, 1, 2, 3, 4
-FORMATS = (Q8_0, Q4_K, IQ4_XS, Q5_K, Q6_K)
-FORMAT_NAMES = {Q8_0: "Q8_0", Q4_K: "Q4_K", IQ4_XS: "IQ4_XS", Q5_K: "Q5_K", Q6_K: "Q6_K"}
-GROUP_WEIGHTS = {Q8_0: 256, Q4_K: 256, IQ4_XS: 512, Q5_K: 256, Q6_K: 256}
-GROUP_BYTES = {Q8_0: 272, Q4_K: 144, IQ4_XS: 272, Q5_K: 176, Q6_K: 208}
+Q8_0, Q4_K, IQ4_XS, Q5_K, Q6_K, Q8_G64, Q8_G128 = 0, 1, 2, 3, 4, 5, 6
+FORMATS = (Q8_0, Q4_K, IQ4_XS, Q5_K, Q6_K, Q8_G64, Q8_G128)
+FORMAT_NAMES = {Q8_0: "Q8_0", Q4_K: "Q4_K", IQ4_XS: "IQ4_XS", Q5_K: "Q5_K", Q6_K: "Q6_K", Q8_G64: "Q8_G64",
+                Q8_G128: "Q8_G128"}
+GROUP_WEIGHTS = {Q8_0: 256, Q4_K: 256, IQ4_XS: 512, Q5_K: 256, Q6_K: 256, Q8_G64: 512, Q8_G128: 1024}
+GROUP_BYTES = {Q8_0: 272, Q4_K: 144, IQ4_XS: 272, Q5_K: 176, Q6_K: 208, Q8_G64: 528, Q8_G128: 1040}
 # IQ4_XS codebook (int8), part of the format definition.
 CODEBOOK = np.array([-127, -104, -83, -65, -49, -35, -22, -10,
                      1, 13, 25, 38, 53, 69, 89, 113], dtype=np.int64)

@@ -8,7 +8,8 @@
  *   - the activation quantizer (per-32 int8 with an fp32 scale), in fp32 as
  *     the rule fixes it, so that integer codes are decided in the same
  *     precision as on the GPU;
- *   - the weight quantizers and dequantizers of Q8_0, Q4_K, IQ4_XS, Q5_K and Q6_K, in
+ *   - the weight quantizers and dequantizers of Q8_0, Q4_K, IQ4_XS, Q5_K, Q6_K
+ *     and Q8 with one scale per 64 or 128 weights, in
  *     fp64, following the byte layouts written out in include/qmv.h;
  *   - the matvec y[t][m] = sum_k What[m][k] * Xhat[t][k] in fp64, plus the
  *     tolerance scale sum_k |What[m][k] * Xhat[t][k]|;
@@ -40,6 +41,8 @@
 #define OR_IQ4_XS 2
 #define OR_Q5_K 3
 #define OR_Q6_K 4
+#define OR_Q8_G64 5
+#define OR_Q8_G128 6
 
 static const int8_t OR_CB[16] = {-127, -104, -83, -65, -49, -35, -22, -10,
                                  1,    13,   25,  38,  53,  69,  89,  113};
@@ -94,6 +97,8 @@ int64_t oracle_group_weights(int fmt) {
     case OR_IQ4_XS: return 512;
     case OR_Q5_K: return 256;
     case OR_Q6_K: return 256;
+    case OR_Q8_G64: return 512;
+    case OR_Q8_G128: return 1024;
   }
   return -1;
 }
@@ -105,6 +110,8 @@ int64_t oracle_group_bytes(int fmt) {
     case OR_IQ4_XS: return 272;
     case OR_Q5_K: return 176;
     case OR_Q6_K: return 208;
+    case OR_Q8_G64: return 528;
+    case OR_Q8_G128: return 1040;
   }
   return -1;
 }
@@ -392,6 +399,35 @@ static void quant_q6_k_group(const float* w, uint8_t* g) {
   }
 }
 
+/* Q8 with one scale per gs weights (gs = 64 or 128), groups of n256 x 256
+ * weights (2 for gs = 64, 4 for gs = 128): bytes [2s, 2s+2) the fp16 d of
+ * scale group s (8 per group), then n256 payloads of 256 bytes arranged as
+ * Q8_0's.  d = amax / 127 over the gs weights (fp16), q = rne(w / d16)
+ * clamped to +-127 (the Q8_0 rule over a larger block). */
+static void quant_q8_g_group(const float* w, uint8_t* g, int gs, int n256) {
+  memset(g, 0, 16 + 256 * (size_t)n256);
+  for (int sidx = 0; sidx < 8; sidx++) {
+    double amax = 0.0;
+    for (int i = 0; i < gs; i++) {
+      double a = fabs((double)w[gs * sidx + i]);
+      if (a > amax) amax = a;
+    }
+    uint16_t d16 = oracle_f64_to_f16(amax / 127.0);
+    double dv = oracle_f16_to_f64(d16);
+    wr16(g + 2 * sidx, d16);
+    for (int i = 0; i < gs; i++) {
+      const int el = gs * sidx + i, half = el >> 8, b = (el >> 5) & 7, ii = el & 31;
+      double r = 0.0;
+      if (dv > 0.0) {
+        r = nearbyint((double)w[el] / dv);
+        if (r > 127.0) r = 127.0;
+        if (r < -127.0) r = -127.0;
+      }
+      g[16 + 256 * half + q8_0_offset(b, ii)] = (uint8_t)(int8_t)r;
+    }
+  }
+}
+
 static void quant_iq4_xs_superblock(const float* w, uint8_t* meta, uint8_t* payload) {
   double s[8];
   double smax = 0.0;
@@ -455,6 +491,10 @@ int oracle_quantize(int fmt, const float* w, int64_t M, int64_t K, uint8_t* out)
         quant_q5_k_group(wg, g);
       else if (fmt == OR_Q6_K)
         quant_q6_k_group(wg, g);
+      else if (fmt == OR_Q8_G64)
+        quant_q8_g_group(wg, g, 64, 2);
+      else if (fmt == OR_Q8_G128)
+        quant_q8_g_group(wg, g, 128, 4);
       else
         quant_iq4_xs_group(wg, g);
     }
@@ -494,6 +534,12 @@ static void dequant_row(int fmt, const uint8_t* row, int64_t K, double* out) {
           unsigned q = get_nib(g + 48 + 16 * j, i) | (get_bits(g + 16 + 4 * j, i, 1) << 4);
           o[32 * j + i] = d * (double)sc * (double)q - dmin * (double)m;
         }
+      }
+    } else if (fmt == OR_Q8_G64 || fmt == OR_Q8_G128) {
+      const int gs = fmt == OR_Q8_G64 ? 64 : 128;
+      for (int el = 0; el < (int)gw; el++) {
+        double d = oracle_f16_to_f64(rd16(g + 2 * (el / gs)));
+        o[el] = d * (double)(int8_t)g[16 + 256 * (el >> 8) + q8_0_offset((el >> 5) & 7, el & 31)];
       }
     } else if (fmt == OR_Q6_K) {
       double d = oracle_f16_to_f64(rd16(g));

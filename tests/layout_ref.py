@@ -132,6 +132,34 @@ def unpack_q6_k(g):
     return d, sc, q
 
 
+def pack_q8_g(d_bits, q, gs) -> bytes:
+    """One Q8 group with a scale per gs (64 or 128) weights: d_bits[8] fp16
+    patterns, q[8 * gs] int8; 8 * gs weights, each 256 of them laid out as a
+    Q8_0 payload."""
+    n = 8 * gs
+    g = bytearray(16 + n)
+    for s_ in range(8):
+        g[2 * s_], g[2 * s_ + 1] = d_bits[s_] & 0xFF, d_bits[s_] >> 8
+    for el in range(n):
+        half, j, i = el // 256, (el // 32) % 8, el % 32
+        off = 16 * j + i if i < 16 else 128 + 16 * j + (i - 16)
+        g[16 + 256 * half + off] = int(q[el]) & 0xFF
+    return bytes(g)
+
+
+def unpack_q8_g(g, gs):
+    g = bytes(g)
+    n = 8 * gs
+    d = [g[2 * s_] | (g[2 * s_ + 1] << 8) for s_ in range(8)]
+    q = []
+    for el in range(n):
+        half, j, i = el // 256, (el // 32) % 8, el % 32
+        off = 16 * j + i if i < 16 else 128 + 16 * j + (i - 16)
+        v = g[16 + 256 * half + off]
+        q.append(v - 256 if v > 127 else v)
+    return d, q
+
+
 def pack_iq4_xs(d_bits, ls, c) -> bytes:
     """One IQ4_XS group (2 superblocks): d_bits[2]; ls[2][8] in [0,63];
     c[2][8][32] codebook indices."""

@@ -43,7 +43,7 @@ def test_quantize_entry_points_reject_bad_arguments(L):
     assert L.qmv_quantize_act(A, 100, 1, A, A, A, None) == -2
     assert L.qmv_quantize_act(A, 256, 0, A, A, A, None) == -3
     assert L.qmv_quantize_act(A, 256, 1, A, None, A, None) == -4
-    assert L.qmv_quantize_weights(5, A, 4, 256, A, None) == -1
+    assert L.qmv_quantize_weights(7, A, 4, 256, A, None) == -1
     assert L.qmv_quantize_weights(1, A, 4, 128, A, None) == -2
     assert L.qmv_quantize_weights(1, A, 4, 256, MIS, None) == -5
 

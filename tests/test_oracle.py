@@ -236,12 +236,34 @@ def test_q6_k_fields_follow_the_rule_and_codes_are_argmins():
                 assert q[16 * i:16 * i + 16] == np.argmin(err, axis=1).tolist()
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("fmt,gs", [(5, 64), (6, 128)])
+def test_q8_group_scales_and_codes_are_argmins(fmt, gs):
+    K = 2048
+    w = _rand_w(2, K, seed=fmt)
+    W = oracle.quantize(fmt, w)
+    gb = 16 + 8 * gs
+    assert W.shape[1] == K // (8 * gs) * gb
+    cand = np.arange(-127, 128)
+    for m in range(2):
+        for gi in range(K // (8 * gs)):
+            d_bits, q = L.unpack_q8_g(W[m, gb * gi:gb * (gi + 1)], gs)
+            wg = w[m, 8 * gs * gi:8 * gs * (gi + 1)].astype(np.float64).reshape(8, gs)
+            for s_ in range(8):
+                assert d_bits[s_] == L.f16_bits(np.abs(wg[s_]).max() / 127.0)
+                dv = L.f16_value(d_bits[s_])
+                err = np.abs(wg[s_][:, None] - dv * cand[None, :])
+                assert q[gs * s_:gs * (s_ + 1)] == cand[np.argmin(err, axis=1)].tolist()
+    # requantizing the dequantized weights gives the same bytes
+    wh = oracle.dequant(fmt, W, K).astype(np.float32)
+    assert np.array_equal(oracle.quantize(fmt, wh), W)
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2, 3, 4, 5, 6])
 def test_zero_weights_dequantize_to_zero(fmt):
-    w = _rand_w(2, 512)
+    w = _rand_w(2, 1024)
     w[0] = 0.0
     W = oracle.quantize(fmt, w)
-    wh = oracle.dequant(fmt, W, 512)
+    wh = oracle.dequant(fmt, W, 1024)
     assert np.all(wh[0] == 0.0)
 
 
@@ -360,7 +382,7 @@ def test_dequant_q6_k_hand_worked():
     assert wh[100] == 0.0
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("fmt", [0, 1, 2, 3, 4, 5, 6])
 def test_dequant_random_fields(fmt):
     r = np.random.default_rng(fmt + 100)
     if fmt == 0:
@@ -377,6 +399,13 @@ def test_dequant_random_fields(fmt):
         exp = np.concatenate([L.f16_value(d) * sc[j] * np.array(q[j], float) - L.f16_value(dm) * m[j]
                               for j in range(8)])
         K = 256
+    elif fmt in (5, 6):
+        gs = 64 if fmt == 5 else 128
+        d = [L.f16_bits(v) for v in r.uniform(-1, 1, 8)]
+        q = r.integers(-128, 128, 8 * gs).tolist()
+        g = L.pack_q8_g(d, q, gs)
+        exp = np.array([L.f16_value(d[e // gs]) * q[e] for e in range(8 * gs)], float)
+        K = 8 * gs
     elif fmt == 4:
         d = L.f16_bits(r.uniform(-1, 1))
         sc = r.integers(0, 128, 16).tolist()
@@ -413,7 +442,7 @@ def _xhat(x):
     return q.astype(np.float64) * np.repeat(d.astype(np.float64), 32, axis=1)
 
 
-@pytest.mark.parametrize("fmt,K", [(0, 512), (1, 768), (2, 1024), (3, 768), (4, 512)])
+@pytest.mark.parametrize("fmt,K", [(0, 512), (1, 768), (2, 1024), (3, 768), (4, 512), (5, 1024), (6, 2048)])
 def test_qmv_matches_library_matmul(fmt, K):
     w = _rand_w(37, K, seed=fmt)
     x = synth.activations(fmt, 5, K)
