@@ -459,7 +459,8 @@ def run_extra(torch, api, synth, stream, dev, peak):
              ("iq4_xs_6144x2048", 2, 6144, 2048, (1, 4, 8)),
              ("iq4_xs_2048x6144", 2, 2048, 6144, (1, 4, 8)),
              ("q5_k_17408x5120", 3, 17408, 5120, (1, 4, 16)),
-             ("q6_k_17408x5120", 4, 17408, 5120, (1, 4, 16))]
+             ("q6_k_17408x5120", 4, 17408, 5120, (1, 4, 16)),
+             ("q8_g128_lm_head_151936x5120", 6, 151936, 5120, (1, 4, 16))]
     for i, (name, fmt, M, K, ns) in enumerate(dense):
         Ws, rb = _replicas(torch, api, fmt, M, K, l2x2, dev, 2000 + i)
         res = {}
@@ -473,7 +474,7 @@ def run_extra(torch, api, synth, stream, dev, peak):
             r = line(rb, _graph_us(torch, stream, calls))
             r["n_split"] = S
             res[str(n)] = r
-        out[name] = {"format": ["Q8_0", "Q4_K", "IQ4_XS", "Q5_K", "Q6_K"][fmt], "bytes_per_call": rb, "replicas": len(Ws),
+        out[name] = {"format": ["Q8_0", "Q4_K", "IQ4_XS", "Q5_K", "Q6_K", "Q8_G64", "Q8_G128"][fmt], "bytes_per_call": rb, "replicas": len(Ws),
                      "n_tok": res}
         del Ws
 

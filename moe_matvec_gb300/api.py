@@ -15,7 +15,7 @@ import torch
 
 from . import build as _build
 
-Q8_0, Q4_K, IQ4_XS, Q5_K, Q6_K = 0, 1, 2, 3, 4
+Q8_0, Q4_K, IQ4_XS, Q5_K, Q6_K, Q8_G64, Q8_G128 = 0, 1, 2, 3, 4, 5, 6
 FORMATS = {"Q8_0": Q8_0, "Q4_K": Q4_K, "IQ4_XS": IQ4_XS}
 GROUP_WEIGHTS = {Q8_0: 256, Q4_K: 256, IQ4_XS: 512}
 BYTES_PER_WEIGHT = {Q8_0: 272 / 256, Q4_K: 144 / 256, IQ4_XS: 272 / 512}

@@ -40,6 +40,16 @@ template <>
 struct Fmt<QMV_Q6_K> {
   static constexpr int GW = 256, GB = 208;
 };
+template <>
+struct Fmt<QMV_Q8_G64> {
+  static constexpr int GW = 512, GB = 528;
+};
+template <>
+struct Fmt<QMV_Q8_G128> {
+  static constexpr int GW = 1024, GB = 1040;
+};
+// int8 codes used as they are (one fp16 scale per 32, 64 or 128 weights)
+__host__ __device__ constexpr bool is_q8(int F) { return F == QMV_Q8_0 || F == QMV_Q8_G64 || F == QMV_Q8_G128; }
 // Formats with a per-sub-block minimum (w = d sc q - dmin m): their min term
 // needs each activation block's code sum.
 __host__ __device__ constexpr bool has_min(int F) { return F == QMV_Q4_K || F == QMV_Q5_K; }

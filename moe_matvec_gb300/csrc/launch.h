@@ -27,6 +27,8 @@ cudaError_t launch_dense_q4_k(const DenseLaunch& L);
 cudaError_t launch_dense_iq4_xs(const DenseLaunch& L);
 cudaError_t launch_dense_q5_k(const DenseLaunch& L);
 cudaError_t launch_dense_q6_k(const DenseLaunch& L);
+cudaError_t launch_dense_q8_g64(const DenseLaunch& L);
+cudaError_t launch_dense_q8_g128(const DenseLaunch& L);
 
 struct MoeParams;
 

@@ -95,13 +95,22 @@ static bool encode_rows(CUtensorMap* map, const void* W, long long rows, long lo
 // ---------------------------------------------------------------------------
 // Validation helpers.
 // ---------------------------------------------------------------------------
-static int group_weights(int fmt) { return fmt == QMV_IQ4_XS ? 512 : 256; }
+static int group_weights(int fmt) {
+  return fmt == QMV_IQ4_XS || fmt == QMV_Q8_G64 ? 512 : (fmt == QMV_Q8_G128 ? 1024 : 256);
+}
 static int group_bytes(int fmt) {
-  return fmt == QMV_Q4_K ? 144 : (fmt == QMV_Q5_K ? 176 : (fmt == QMV_Q6_K ? 208 : 272));
+  switch (fmt) {
+    case QMV_Q4_K: return 144;
+    case QMV_Q5_K: return 176;
+    case QMV_Q6_K: return 208;
+    case QMV_Q8_G64: return 528;
+    case QMV_Q8_G128: return 1040;
+  }
+  return 272;  // Q8_0, IQ4_XS
 }
 static int chunk_bytes_of(int fmt) { return (KCHUNK / group_weights(fmt)) * group_bytes(fmt); }
 static bool fmt_ok(int fmt) {
-  return fmt == QMV_Q8_0 || fmt == QMV_Q4_K || fmt == QMV_IQ4_XS || fmt == QMV_Q5_K || fmt == QMV_Q6_K;
+  return fmt >= QMV_Q8_0 && fmt <= QMV_Q8_G128;
 }
 // formats the MoE kernels are instantiated for
 static bool moe_fmt_ok(int fmt) { return fmt == QMV_Q8_0 || fmt == QMV_Q4_K || fmt == QMV_IQ4_XS; }
@@ -189,6 +198,8 @@ static cudaError_t launch_dense_any(int fmt, const DenseLaunch& L) {
     case QMV_Q4_K: return launch_dense_q4_k(L);
     case QMV_Q5_K: return launch_dense_q5_k(L);
     case QMV_Q6_K: return launch_dense_q6_k(L);
+    case QMV_Q8_G64: return launch_dense_q8_g64(L);
+    case QMV_Q8_G128: return launch_dense_q8_g128(L);
     default: return launch_dense_iq4_xs(L);
   }
 }

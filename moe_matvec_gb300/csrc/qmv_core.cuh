@@ -411,6 +411,18 @@ struct Consumer {
       w_off = g * 272 + 16 + 16 * j;
       h_off = g * 272 + 2 * j;
       f_off = fsh = 0;
+    } else if constexpr (F == QMV_Q8_G64) {
+      // two 512-weight groups per chunk; 16 blocks each, a scale per 2 blocks
+      const int g = lane >> 4, h = (lane >> 3) & 1;
+      w_off = g * 528 + 16 + 256 * h + 16 * j;
+      h_off = g * 528 + 2 * ((lane & 15) >> 1);
+      f_off = fsh = 0;
+    } else if constexpr (F == QMV_Q8_G128) {
+      // one 1024-weight group per chunk; a scale per 4 blocks
+      const int h = lane >> 3;
+      w_off = 16 + 256 * h + 16 * j;
+      h_off = 2 * (lane >> 2);
+      f_off = fsh = 0;
     } else if constexpr (F == QMV_Q4_K) {
       const int g = lane >> 3;
       w_off = g * 144 + 16 + 16 * j;
@@ -475,7 +487,7 @@ struct Consumer {
 #pragma unroll
     for (int r = 0; r < RW; r++) {
       const uint32_t row = row0 + (r & 1) * CB + (r >> 1) * PAIR_STRIDE;
-      if constexpr (F == QMV_Q8_0) {
+      if constexpr (is_q8(F)) {
         const uint4 x0 = lds128(row + w_off);
         const uint4 x1 = lds128(row + w_off + 128);
         w[r][0] = x0.x; w[r][1] = x0.y; w[r][2] = x0.z; w[r][3] = x0.w;

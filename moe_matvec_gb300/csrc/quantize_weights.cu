@@ -1,5 +1,6 @@
 // Weight quantizers (a preparation step, not part of the decode hot path):
-// fp32 weights -> the library's Q8_0 / Q4_K / IQ4_XS / Q5_K / Q6_K groups.  Each scale is
+// fp32 weights -> the library's Q8_0 / Q4_K / IQ4_XS / Q5_K / Q6_K / Q8 group-64 /
+// group-128 groups.  Each scale is
 // chosen from its block's range and each code is the nearest grid point, in
 // fp64 with every operation written as an explicitly rounded IEEE intrinsic
 // (no contraction), so the bytes do not depend on the compiler.  One thread
@@ -175,6 +176,27 @@ __device__ void group_q6_k(const float* w, uint8_t* g) {
   }
 }
 
+// Q8 with one scale per GS weights over a group of 8 GS: the Q8_0 rule per
+// scale group, codes in Q8_0's payload order per 256 weights.
+template <int GS>
+__device__ void group_q8_g(const float* w, uint8_t* g) {
+  for (int sidx = 0; sidx < 8; sidx++) {
+    double amax = 0.0;
+    for (int i = 0; i < GS; i++) amax = fmax(amax, fabs((double)w[GS * sidx + i]));
+    const uint16_t d16 = f16_bits(__ddiv_rn(amax, 127.0));
+    const double dv = f16_val(d16);
+    g[2 * sidx] = (uint8_t)(d16 & 0xFF);
+    g[2 * sidx + 1] = (uint8_t)(d16 >> 8);
+    for (int i = 0; i < GS; i++) {
+      const int el = GS * sidx + i, half = el >> 8, b = (el >> 5) & 7, ii = el & 31;
+      double r = 0.0;
+      if (dv > 0.0) r = clampd(rint(__ddiv_rn((double)w[el], dv)), -127.0, 127.0);
+      const int off = ii < 16 ? 16 * b + ii : 128 + 16 * b + (ii - 16);
+      g[16 + 256 * half + off] = (uint8_t)(int8_t)(int)r;
+    }
+  }
+}
+
 __device__ void superblock_iq4_xs(const float* w, uint8_t* meta, uint8_t* payload) {
   const double cb[16] = {-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113};
   double s[8], smax = 0.0;
@@ -228,6 +250,10 @@ __global__ void __launch_bounds__(128) quantize_kernel(const float* __restrict__
       group_q5_k(src, g);
     else if constexpr (F == QMV_Q6_K)
       group_q6_k(src, g);
+    else if constexpr (F == QMV_Q8_G64)
+      group_q8_g<64>(src, g);
+    else if constexpr (F == QMV_Q8_G128)
+      group_q8_g<128>(src, g);
     else {
       superblock_iq4_xs(src, g, g + 16);
       superblock_iq4_xs(src + 256, g + 8, g + 16 + 128);
@@ -241,7 +267,8 @@ __global__ void __launch_bounds__(128) quantize_kernel(const float* __restrict__
 }  // namespace
 
 cudaError_t launch_quantize_weights(int fmt, const float* w, long long M, int K, void* W, cudaStream_t stream) {
-  long long groups = M * (K / (fmt == QMV_IQ4_XS ? 512 : 256));
+  const int gw = fmt == QMV_IQ4_XS || fmt == QMV_Q8_G64 ? 512 : (fmt == QMV_Q8_G128 ? 1024 : 256);
+  long long groups = M * (K / gw);
   long long ctas = (groups + 127) / 128;
   const long long cap = 32ll * device_sm_count();
   if (ctas > cap) ctas = cap;
@@ -251,6 +278,8 @@ cudaError_t launch_quantize_weights(int fmt, const float* w, long long M, int K,
     case QMV_Q4_K: quantize_kernel<QMV_Q4_K><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
     case QMV_Q5_K: quantize_kernel<QMV_Q5_K><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
     case QMV_Q6_K: quantize_kernel<QMV_Q6_K><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
+    case QMV_Q8_G64: quantize_kernel<QMV_Q8_G64><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
+    case QMV_Q8_G128: quantize_kernel<QMV_Q8_G128><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
     default: quantize_kernel<QMV_IQ4_XS><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
   }
   return cudaGetLastError();

@@ -15,7 +15,7 @@ from tests.gpu_util import TOL, assert_within, dev, sample_rows
 
 pytestmark = pytest.mark.gpu
 
-GW = {0: 256, 1: 256, 2: 512, 3: 256, 4: 256}
+GW = {0: 256, 1: 256, 2: 512, 3: 256, 4: 256, 5: 512, 6: 1024}
 
 
 # --------------------------------------------------------------------------
@@ -67,7 +67,7 @@ def test_act_quant_bit_exact(lib, n, K):
 # weight quantizer: bit-exact bytes
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("fmt", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("fmt", [0, 1, 2, 3, 4, 5, 6])
 def test_quantize_weights_bit_exact(lib, fmt):
     K = 2048
     w = synth.weights(70 + fmt, 300, K)
@@ -88,7 +88,7 @@ def test_quantize_weights_bit_exact(lib, fmt):
 # --------------------------------------------------------------------------
 
 SMALL = []
-for fmt in (0, 1, 2, 3, 4):
+for fmt in (0, 1, 2, 3, 4, 5, 6):
     for M, K, ns in [(1, 512, (1, 3)), (37, 1536, (1, 2, 5)), (333, 3072, (1, 4, 8, 16)),
                      (1000, 1024, (7, 17, 33, 64)), (64, 7168, (2, 13))]:
         if K % GW[fmt]:
@@ -108,7 +108,7 @@ def test_qmv_small(lib, fmt, M, K, n):
     assert_within(y, yr, sabs, what=f"fmt{fmt} M{M} K{K} n{n}")
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("fmt", [0, 1, 2, 3, 4, 5, 6])
 def test_qmv_prequantized_input_matches_fused(lib, fmt):
     M, K, n = 200, 2048, 5
     w = synth.weights(5 + fmt, M, K)
@@ -124,8 +124,8 @@ def test_qmv_prequantized_input_matches_fused(lib, fmt):
 
 def _exact_case(fmt, r):
     """Weights and activations whose products and sums are exact in fp32:
-    power-of-two scales, small integer codes, K = 512."""
-    K, M, n = 512, 40, 3
+    power-of-two scales, small integer codes, K = 512 (one group where larger)."""
+    K, M, n = max(512, GW[fmt]), 40, 3
     groups = []
     for m in range(M):
         row = b""
@@ -135,6 +135,9 @@ def _exact_case(fmt, r):
             elif fmt == 1:
                 row += L.pack_q4_k(L.f16_bits(2.0 ** -4), L.f16_bits(2.0 ** -5), r.integers(0, 4, 8).tolist(),
                                    r.integers(0, 4, 8).tolist(), r.integers(0, 16, (8, 32)).tolist())
+            elif fmt in (5, 6):
+                gs = 64 if fmt == 5 else 128
+                row += L.pack_q8_g([L.f16_bits(2.0 ** -3)] * 8, r.integers(-63, 64, 8 * gs).tolist(), gs)
             elif fmt == 4:
                 row += L.pack_q6_k(L.f16_bits(2.0 ** -4), r.integers(0, 4, 16).tolist(),
                                    r.integers(24, 41, 256).tolist())
@@ -152,13 +155,13 @@ def _exact_case(fmt, r):
     return W, x, K, M
 
 
-@pytest.mark.parametrize("fmt", [0, 1, 2, 3, 4])
+@pytest.mark.parametrize("fmt", [0, 1, 2, 3, 4, 5, 6])
 def test_qmv_exact_integer_sums(lib, fmt):
     # every partial sum is an integer multiple of 2^-8 below 2^24 * 2^-8, so an
     # exact int32 block sum gives a bit-exact fp32 result in any order
     W, x, K, M = _exact_case(fmt, np.random.default_rng(fmt))
     yr, sabs = oracle.qmv(fmt, W, x, K)
-    unit = {0: 2.0 ** -5, 1: 2.0 ** -7, 2: 2.0 ** -8, 3: 2.0 ** -7, 4: 2.0 ** -6}[fmt]   # d_w * d_x (and dmin * d_x)
+    unit = {0: 2.0 ** -5, 1: 2.0 ** -7, 2: 2.0 ** -8, 3: 2.0 ** -7, 4: 2.0 ** -6, 5: 2.0 ** -5, 6: 2.0 ** -5}[fmt]   # d_w * d_x (and dmin * d_x)
     assert np.all(sabs < 2.0 ** 22 * unit)
     y = lib.run(fmt, dev(W), dev(x), M, K).cpu().numpy()
     assert np.array_equal(y.astype(np.float64), yr)
