@@ -37,6 +37,7 @@ struct MoeLaunch {
   CUtensorMap map_tile;
   CUtensorMap map_unit;
   int nt_tmpl;
+  int cw;  // consumer warps: 8, or 12 beside a producer warpgroup
   int grid;
   size_t smem;
   cudaStream_t stream;

@@ -220,17 +220,20 @@ struct MoeWalk {
   }
 };
 
-template <int F, int NT, int MODE>
-__global__ void __launch_bounds__(THREADS, NT <= 4 ? 2 : 1)
+template <int F, int NT, int MODE, int CW>
+__global__ void __launch_bounds__(Shape<CW>::THREADS, NT <= 4 && CW == CONSUMER_WARPS ? 2 : 1)
     moe_qmv_kernel(const __grid_constant__ CUtensorMap map_tile, const __grid_constant__ CUtensorMap map_unit,
                    const MoeParams p) {
+  using SH = Shape<CW>;
   constexpr int CB = chunk_bytes<F>();
-  constexpr int STAGE_BYTES = TILE_ROWS * CB;
-  // GATE_UP: a tile is up to 2 units of 8 outputs j: gate rows j in stage rows
-  // 0..15, up rows j in stage rows 16..31; warp w takes outputs j0 + 2w and
-  // j0 + 2w + 1 (stage rows 2w, 2w+1 and 16+2w, 17+2w).
-  // DOWN: a tile is up to 4 units of 8 rows; warp w takes rows 4w .. 4w+3.
-  constexpr int TILE_UNITS = MODE == MOE_GATE_UP ? 2 : 4;
+  constexpr int STAGE_BYTES = SH::TILE_ROWS * CB, CONSUMER_THREADS = SH::CONSUMER_THREADS;
+  // GATE_UP: a tile is up to CW / 4 units of 8 outputs j: gate rows j in
+  // stage rows 0 .. HALF - 1, up rows j in stage rows HALF .. 2 HALF - 1
+  // (HALF = 2 CW); warp w takes outputs j0 + 2w and j0 + 2w + 1 (stage rows
+  // 2w, 2w+1 and HALF+2w, HALF+2w+1).
+  // DOWN: a tile is up to CW / 2 units of 8 rows; warp w takes rows 4w .. 4w+3.
+  constexpr int TILE_UNITS = MODE == MOE_GATE_UP ? CW / 4 : CW / 2;
+  constexpr int HALF = 2 * CW;
   __shared__ MoeRouting rt;
   __shared__ int s_rows[16];
   extern __shared__ __align__(128) uint8_t smem[];
@@ -241,7 +244,7 @@ __global__ void __launch_bounds__(THREADS, NT <= 4 ? 2 : 1)
   uint64_t* empty = full + MAX_STAGES;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  init_pipeline(full, empty, p.stages);
+  init_pipeline(full, empty, p.stages, CW);
   // GATE_UP reads ids, which the preceding kernel may produce, so it waits
   // before routing and only then lets the next kernel launch; DOWN launches
   // after every GATE_UP CTA passed that wait, so its ids are complete.
@@ -253,9 +256,10 @@ __global__ void __launch_bounds__(THREADS, NT <= 4 ? 2 : 1)
   build_routing(rt, p, NT, MODE == MOE_GATE_UP && blockIdx.x == 0, UNIT_BASE, units_per_pair);
   const int nck = (p.K + KCHUNK - 1) / KCHUNK;
 
-  if (warp == CONSUMER_WARPS) {
+  if (warp >= CW) {
     // ---------------- producer ----------------
-    if (lane == 0) {
+    if constexpr (SH::RESPLIT) regs_dec<SH::REG_PRODUCER>();
+    if (warp == CW && lane == 0) {
       prefetch_tensormap(&map_tile);
       prefetch_tensormap(&map_unit);
       const uint64_t pol = policy_evict_first();
@@ -280,7 +284,7 @@ __global__ void __launch_bounds__(THREADS, NT <= 4 ? 2 : 1)
             for (int i = 0; i < nu; i++) {
               const int j = (u + i) * UNIT_ROWS;
               tma_load_2d(dst + i * UNIT_ROWS * CB, &map_unit, &full[st], x, base + j, pol);
-              tma_load_2d(dst + (16 + i * UNIT_ROWS) * CB, &map_unit, &full[st], x, base + p.R + j, pol);
+              tma_load_2d(dst + (HALF + i * UNIT_ROWS) * CB, &map_unit, &full[st], x, base + p.R + j, pol);
             }
           } else {
             if (nu == TILE_UNITS) {
@@ -300,6 +304,7 @@ __global__ void __launch_bounds__(THREADS, NT <= 4 ? 2 : 1)
   }
 
   // ---------------- consumers ----------------
+  if constexpr (SH::RESPLIT) regs_inc<SH::REG_CONSUMER>();
   if (MODE == MOE_DOWN) pdl_wait();  // h comes from the preceding kernel
   const int cw = warp;
   bool alive = true;
@@ -316,8 +321,8 @@ __global__ void __launch_bounds__(THREADS, NT <= 4 ? 2 : 1)
   if constexpr (MODE == MOE_GATE_UP) {
     roff[0] = 2 * cw;
     roff[1] = 2 * cw + 1;
-    roff[2] = 16 + 2 * cw;
-    roff[3] = 17 + 2 * cw;
+    roff[2] = HALF + 2 * cw;
+    roff[3] = HALF + 1 + 2 * cw;
   } else {
 #pragma unroll
     for (int r = 0; r < RW; r++) roff[r] = cw * RW + r;
@@ -340,7 +345,7 @@ __global__ void __launch_bounds__(THREADS, NT <= 4 ? 2 : 1)
         src.wd = p.hd;
         src.ws = p.hs;
       }
-      stage_activations<F, NT>(src, 0, nblk, nt, a, cw, lane);
+      stage_activations<F, NT, 4, CW>(src, 0, nblk, nt, a, cw, lane);
       named_sync(1, CONSUMER_THREADS);
       staged_pair = q;
     }
@@ -356,7 +361,7 @@ __global__ void __launch_bounds__(THREADS, NT <= 4 ? 2 : 1)
       if (active) {
         // GATE_UP: rows (2cw, 2cw + 1) of the gate half and the same of the
         // up half, 16 rows apart; DOWN: 4 consecutive rows
-        constexpr int PS = (MODE == MOE_GATE_UP ? 16 : 2) * CB;
+        constexpr int PS = (MODE == MOE_GATE_UP ? HALF : 2) * CB;
         cons.template chunk<PS>(stage_base + st * STAGE_BYTES + roff[0] * CB, aq_base + c * NT * ACT_BYTES,
                                 ad_base + c * NT * 128, as_base + c * NT * 128, nt, acc);
       }

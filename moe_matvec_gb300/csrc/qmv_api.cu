@@ -323,18 +323,23 @@ static int run_moe_proj(int mode, int fmt, const void* pool, MoeParams& p, int n
   const long long rb = qmv_row_bytes(fmt, p.K);
   const long long rows = (long long)p.n_experts * p.pool_rows;
   MoeLaunch L;
-  if (!encode_rows(&L.map_tile, pool, rows, rb, chunk_bytes_of(fmt), TILE_ROWS)) return QMV_ERR_CUDA;
-  if (!encode_rows(&L.map_unit, pool, rows, rb, chunk_bytes_of(fmt), UNIT_ROWS)) return QMV_ERR_CUDA;
   p.act_nck = (p.K + KCHUNK - 1) / KCHUNK;
   p.groups = p.K / group_weights(fmt);
-  const int stage_bytes = TILE_ROWS * chunk_bytes_of(fmt);
   // the routing tables are static shared memory: count them with the
   // activation area when sizing, and leave them out of the dynamic size
   const size_t static_bytes = sizeof(MoeRouting) + 16 * sizeof(int) + 256;
   size_t smem = 0;
-  if (!plan_stages(nt, CONSUMER_WARPS, act_area_bytes(fmt, nt, p.act_nck) + static_bytes, stage_bytes,
-                   (size_t)device_smem_optin(), p.stages, smem))
-    return QMV_ERR_SHAPE;
+  // from 8 token slots on twelve consumer warps (beside a producer warpgroup
+  // that hands its registers to them) where their tiles fit, else eight
+  bool ok = false;
+  for (int cw = nt >= 8 ? 12 : 8; cw >= 8 && !ok; cw -= 4) {
+    L.cw = cw;
+    ok = plan_stages(nt, cw, act_area_bytes(fmt, nt, p.act_nck) + static_bytes, cw * RW * chunk_bytes_of(fmt),
+                     (size_t)device_smem_optin(), p.stages, smem);
+  }
+  if (!ok) return QMV_ERR_SHAPE;
+  if (!encode_rows(&L.map_tile, pool, rows, rb, chunk_bytes_of(fmt), L.cw * RW)) return QMV_ERR_CUDA;
+  if (!encode_rows(&L.map_unit, pool, rows, rb, chunk_bytes_of(fmt), UNIT_ROWS)) return QMV_ERR_CUDA;
   L.p = &p;
   L.nt_tmpl = nt;
   L.grid = device_sm_count() * (nt <= 4 && smem <= TWO_PER_SM_BYTES ? 2 : 1);
