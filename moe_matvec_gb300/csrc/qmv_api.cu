@@ -552,13 +552,17 @@ int moe_qmv_run(const moe_experts* e, const int32_t* ids, const float* gates, co
   // Token slots per expert group: a power of two covering the typical group
   // (tokens per expert ~ lambda = n_tok * top_k / E, plus two standard
   // deviations); larger groups are split into several groups, each reading the
-  // expert's weights again.  Smaller slot counts keep the kernels free of
-  // register spills.
+  // expert's weights again.  From 4 tokens on at least 8 slots: their kernels'
+  // twelve consumer warps (beside a producer warpgroup) run faster than the
+  // smaller slot counts' two CTAs of eight per SM, even for groups of one or
+  // two tokens (empty slots cost no arithmetic).  Below that the single-token
+  // kernels win.
   const double lam = (double)n_tok * top_k / e->n_experts;
   const double want = lam + 2.0 * sqrt(lam);
   int nt = 1;
   while (nt < want && nt < 16) nt <<= 1;
   while (nt > n_tok && nt > 1) nt >>= 1;
+  if (n_tok >= 4 && nt < 8) nt = 8;
 
   MoeParams p{};
   p.ids = ids;

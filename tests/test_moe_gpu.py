@@ -110,10 +110,11 @@ def test_moe_small_stagewise(lib, fmt_gu, fmt_d, E, H, F, top_k, n):
     assert lib.get_device_error() == 0
 
 
-@pytest.mark.parametrize("E,top_k,n", [(300, 4, 24), (512, 2, 20)])
+@pytest.mark.parametrize("E,top_k,n", [(300, 4, 24), (512, 2, 20), (300, 4, 3), (512, 8, 2)])
 def test_moe_many_experts(lib, E, top_k, n):
-    # more experts than one round of the routing scan covers (32 per warp,
-    # 9 warps): the slot, group and work prefixes carry across rounds
+    # many experts; below 4 tokens more than one round of the routing scan
+    # covers (32 per warp, 9 warps): the slot, group and work prefixes carry
+    # across rounds
     H = F = 256
     ids, gates = synth.routing(900 + E, n, E, top_k)
     experts = sorted(set(ids.reshape(-1).tolist()))
