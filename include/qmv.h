@@ -28,9 +28,10 @@
  *   - Activations X are fp32 row-major [n_tok][K]; outputs Y are fp32
  *     row-major [n_tok][M]:  Y[t][m] = sum_k What[m][k] * Xhat[t][k].
  *   - A weight matrix W has M rows; row m occupies qmv_row_bytes(fmt, K)
- *     contiguous bytes starting at W + m * qmv_row_bytes(fmt, K).  A row is a
- *     sequence of GROUPS; every group is a 16-byte header followed by its
- *     payload, so every group (and row) starts on a 16-byte boundary.
+ *     contiguous bytes starting at W + m * qmv_row_bytes(fmt, K).  A row of
+ *     a quantized format is a sequence of GROUPS; every group is a 16-byte
+ *     header followed by its payload, so every group (and row) starts on a
+ *     16-byte boundary.  (F16 / F32 rows are plain arrays of K values.)
  *   - Every pointer argument is device memory owned by the caller (unless a
  *     comment says otherwise).  The library allocates nothing, keeps no
  *     per-call state and never synchronises the stream (except
@@ -123,10 +124,22 @@
  *             256: q_0..15 at 16j, q_16..31 at 128+16j)
  *   K % 512 (G64) or K % 1024 (G128) == 0.  Dense matvecs only.
  *
+ * QMV_F16, QMV_F32 ("Castagna Veloce", section "Kernels for the MI50": the
+ *   small-batch matvec also serves F16 and F32 weights): unquantized rows,
+ *   What = w, IEEE binary16 or binary32, weight k at bytes [2k, 2k+2) or
+ *   [4k, 4k+4) of the row.  There is no header and no activation
+ *   quantization: these formats take x as it is (Xhat = x, fp32), every
+ *   product and sum in fp32 (same accuracy bound).  K % 32 == 0; row bytes
+ *   = 2 K or 4 K.  Dense matvecs only (qmv_run, qmv_splitk_run[_static],
+ *   qmv_run_residual, qmv_run_siblings; not qmv_run_q8, not the MoE pool).
+ *   Their activations are staged in shared memory as fp32 for a CTA's whole
+ *   K-range, so long rows take fewer tokens per pass (more passes over the
+ *   weights); split-K shortens the range.
+ *
  * Bytes per weight: Q8_0 1.0625, Q4_K 0.5625, IQ4_XS 0.53125, Q5_K 0.6875
  * (the same densities as the GGML formats of the same names), Q6_K 0.8125
  * (7-bit sub-scales instead of GGML's 8-bit ones), Q8_G64 1.03125, Q8_G128
- * 1.015625; GGUF byte compatibility is not a goal.
+ * 1.015625, F16 2, F32 4; GGUF byte compatibility is not a goal.
  */
 #ifndef QMV_H
 #define QMV_H
@@ -146,7 +159,9 @@ enum qmv_format {
   QMV_Q5_K = 3,
   QMV_Q6_K = 4,
   QMV_Q8_G64 = 5,
-  QMV_Q8_G128 = 6
+  QMV_Q8_G128 = 6,
+  QMV_F16 = 7,
+  QMV_F32 = 8
 };
 
 enum qmv_status {
@@ -185,6 +200,7 @@ int64_t qmv_row_bytes(int fmt, int64_t K);
  *   IQ4_XS: per sub-block s = amax / 113; d = fp16(max s / 31);
  *           ls = 32 + clamp(rne(s / d), 0, 31);
  *           c = argmin_{0..15} |w - d*(ls-32)*CB[c]| (ties: lower c).
+ *   F16   : fp16(w) per weight;  F32: w as it is.
  * (fp16(.) rounds to nearest even; a zero scale gives zero codes.)  This is a
  * preparation step, not part of the decode hot path. */
 int qmv_quantize_weights(int fmt, const float* w, int64_t M, int64_t K, void* W,
@@ -205,14 +221,16 @@ int qmv_quantize_act(const float* x, int64_t K, int n_tok, int8_t* q, float* d,
 /* Y[t][m] = sum_k What[m][k] * Xhat[t][k] for t < n_tok, m < M: the
  * small-batch quantized matvec.  x fp32 [n_tok][K] is quantized inside the
  * kernel (rule above); every integer block dot product is exact and the block
- * scales are applied in fp32.  Accuracy: |Y - Y_exact| <= 1e-5 *
- * sum_k |What[m][k] * Xhat[t][k]|.  1 <= n_tok <= 64. */
+ * scales are applied in fp32 (F16 / F32 weights: Xhat = x, fp32 products).
+ * Accuracy: |Y - Y_exact| <= 1e-5 * sum_k |What[m][k] * Xhat[t][k]|.
+ * 1 <= n_tok <= 64. */
 int qmv_run(int fmt, const void* W, const float* x, float* y, int64_t M,
             int64_t K, int n_tok, cudaStream_t stream);
 
 /* Same as qmv_run with pre-quantized activations (the layout of
  * qmv_quantize_act); results are bitwise equal to qmv_run on the x they
- * were quantized from. */
+ * were quantized from.  Quantized formats only (QMV_F16 / QMV_F32:
+ * QMV_ERR_FORMAT). */
 int qmv_run_q8(int fmt, const void* W, const int8_t* xq, const float* xd,
                const int32_t* xs, float* y, int64_t M, int64_t K, int n_tok,
                cudaStream_t stream);

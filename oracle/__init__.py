@@ -18,12 +18,16 @@ import threading
 
 import numpy as np
 
-Q8_0, Q4_K, IQ4_XS, Q5_K, Q6_K, Q8_G64, Q8_G128 = 0, 1, 2, 3, 4, 5, 6
-FORMATS = (Q8_0, Q4_K, IQ4_XS, Q5_K, Q6_K, Q8_G64, Q8_G128)
+Q8_0, Q4_K, IQ4_XS, Q5_K, Q6_K, Q8_G64, Q8_G128, F16, F32 = 0, 1, 2, 3, 4, 5, 6, 7, 8
+FORMATS = (Q8_0, Q4_K, IQ4_XS, Q5_K, Q6_K, Q8_G64, Q8_G128)  # block-quantized
+FLOAT_FORMATS = (F16, F32)  # unquantized rows; the activations stay fp32 (Xhat = x)
+ALL_FORMATS = FORMATS + FLOAT_FORMATS
 FORMAT_NAMES = {Q8_0: "Q8_0", Q4_K: "Q4_K", IQ4_XS: "IQ4_XS", Q5_K: "Q5_K", Q6_K: "Q6_K", Q8_G64: "Q8_G64",
-                Q8_G128: "Q8_G128"}
-GROUP_WEIGHTS = {Q8_0: 256, Q4_K: 256, IQ4_XS: 512, Q5_K: 256, Q6_K: 256, Q8_G64: 512, Q8_G128: 1024}
-GROUP_BYTES = {Q8_0: 272, Q4_K: 144, IQ4_XS: 272, Q5_K: 176, Q6_K: 208, Q8_G64: 528, Q8_G128: 1040}
+                Q8_G128: "Q8_G128", F16: "F16", F32: "F32"}
+GROUP_WEIGHTS = {Q8_0: 256, Q4_K: 256, IQ4_XS: 512, Q5_K: 256, Q6_K: 256, Q8_G64: 512, Q8_G128: 1024,
+                 F16: 32, F32: 32}
+GROUP_BYTES = {Q8_0: 272, Q4_K: 144, IQ4_XS: 272, Q5_K: 176, Q6_K: 208, Q8_G64: 528, Q8_G128: 1040,
+               F16: 64, F32: 128}
 # IQ4_XS codebook (int8), part of the format definition.
 CODEBOOK = np.array([-127, -104, -83, -65, -49, -35, -22, -10,
                      1, 13, 25, 38, 53, 69, 89, 113], dtype=np.int64)
@@ -146,7 +150,8 @@ def dequant(fmt: int, W: np.ndarray, K: int) -> np.ndarray:
 
 def qmv(fmt: int, W: np.ndarray, x: np.ndarray, K: int, nthreads: int = 1):
     """y[t][m] = sum_k What[m][k] Xhat[t][k] (fp64) and the tolerance scale
-    sabs[t][m] = sum_k |What[m][k] Xhat[t][k]|; x fp32 [n][K]."""
+    sabs[t][m] = sum_k |What[m][k] Xhat[t][k]|; x fp32 [n][K] (quantized by
+    the activation rule, or used as it is for F16 / F32 weights)."""
     W = np.ascontiguousarray(W, dtype=np.uint8)
     x = np.ascontiguousarray(x, dtype=np.float32)
     if x.ndim == 1:

@@ -10,9 +10,11 @@
  *     precision as on the GPU;
  *   - the weight quantizers and dequantizers of Q8_0, Q4_K, IQ4_XS, Q5_K, Q6_K
  *     and Q8 with one scale per 64 or 128 weights, in
- *     fp64, following the byte layouts written out in include/qmv.h;
+ *     fp64, following the byte layouts written out in include/qmv.h, and the
+ *     conversions of the unquantized F16 / F32 rows;
  *   - the matvec y[t][m] = sum_k What[m][k] * Xhat[t][k] in fp64, plus the
- *     tolerance scale sum_k |What[m][k] * Xhat[t][k]|;
+ *     tolerance scale sum_k |What[m][k] * Xhat[t][k]| (Xhat = x, unquantized,
+ *     for F16 / F32 weights);
  *   - the MoE decode layer (routing, gate/up, SwiGLU, requantization of h,
  *     down projection, gate-weighted combine in k order) in fp64 except the
  *     requantization, which uses the fp32 activation rule;
@@ -43,6 +45,11 @@
 #define OR_Q6_K 4
 #define OR_Q8_G64 5
 #define OR_Q8_G128 6
+#define OR_F16 7
+#define OR_F32 8
+
+/* Unquantized weight rows: activations are used as they are. */
+static int is_float_fmt(int fmt) { return fmt == OR_F16 || fmt == OR_F32; }
 
 static const int8_t OR_CB[16] = {-127, -104, -83, -65, -49, -35, -22, -10,
                                  1,    13,   25,  38,  53,  69,  89,  113};
@@ -99,6 +106,8 @@ int64_t oracle_group_weights(int fmt) {
     case OR_Q6_K: return 256;
     case OR_Q8_G64: return 512;
     case OR_Q8_G128: return 1024;
+    case OR_F16: return 32;
+    case OR_F32: return 32;
   }
   return -1;
 }
@@ -112,6 +121,8 @@ int64_t oracle_group_bytes(int fmt) {
     case OR_Q6_K: return 208;
     case OR_Q8_G64: return 528;
     case OR_Q8_G128: return 1040;
+    case OR_F16: return 64;
+    case OR_F32: return 128;
   }
   return -1;
 }
@@ -495,6 +506,14 @@ int oracle_quantize(int fmt, const float* w, int64_t M, int64_t K, uint8_t* out)
         quant_q8_g_group(wg, g, 64, 2);
       else if (fmt == OR_Q8_G128)
         quant_q8_g_group(wg, g, 128, 4);
+      else if (fmt == OR_F16)
+        for (int i = 0; i < 32; i++) wr16(g + 2 * i, oracle_f64_to_f16((double)wg[i]));
+      else if (fmt == OR_F32)
+        for (int i = 0; i < 32; i++) {
+          uint32_t b;
+          memcpy(&b, &wg[i], 4);
+          for (int k = 0; k < 4; k++) g[4 * i + k] = (uint8_t)(b >> (8 * k));
+        }
       else
         quant_iq4_xs_group(wg, g);
     }
@@ -534,6 +553,16 @@ static void dequant_row(int fmt, const uint8_t* row, int64_t K, double* out) {
           unsigned q = get_nib(g + 48 + 16 * j, i) | (get_bits(g + 16 + 4 * j, i, 1) << 4);
           o[32 * j + i] = d * (double)sc * (double)q - dmin * (double)m;
         }
+      }
+    } else if (fmt == OR_F16) {
+      for (int i = 0; i < 32; i++) o[i] = oracle_f16_to_f64(rd16(g + 2 * i));
+    } else if (fmt == OR_F32) {
+      for (int i = 0; i < 32; i++) {
+        uint32_t b = (uint32_t)g[4 * i] | ((uint32_t)g[4 * i + 1] << 8) | ((uint32_t)g[4 * i + 2] << 16) |
+                     ((uint32_t)g[4 * i + 3] << 24);
+        float f;
+        memcpy(&f, &b, 4);
+        o[i] = (double)f;
       }
     } else if (fmt == OR_Q8_G64 || fmt == OR_Q8_G128) {
       const int gs = fmt == OR_Q8_G64 ? 64 : 128;
@@ -609,8 +638,8 @@ static void* qmv_worker(void* arg) {
 }
 
 /* y[t][m] = sum_k What[m][k] * Xhat[t][k]; sabs[t][m] = sum_k |What Xhat|.
- * x is fp32 [n][K], quantized here with oracle_act_quant.  Rows are split
- * across nthreads POSIX threads (1 = serial). */
+ * x is fp32 [n][K], quantized here with oracle_act_quant (F16 / F32 weights:
+ * Xhat = x).  Rows are split across nthreads POSIX threads (1 = serial). */
 int oracle_qmv(int fmt, const uint8_t* W, int64_t M, int64_t K, const float* x,
                int64_t n, double* y, double* sabs, int nthreads) {
   int64_t rb = oracle_row_bytes(fmt, K);
@@ -623,7 +652,8 @@ int oracle_qmv(int fmt, const uint8_t* W, int64_t M, int64_t K, const float* x,
   oracle_act_quant(x, K, n, q, d, s);
   for (int64_t t = 0; t < n; t++)
     for (int64_t k = 0; k < K; k++)
-      xhat[t * K + k] = (double)d[t * (K / 32) + k / 32] * (double)q[t * K + k];
+      xhat[t * K + k] = is_float_fmt(fmt) ? (double)x[t * K + k]
+                                          : (double)d[t * (K / 32) + k / 32] * (double)q[t * K + k];
   if (nthreads < 1) nthreads = 1;
   if (nthreads > 256) nthreads = 256;
   qmv_job jobs[256];

@@ -493,6 +493,75 @@ def test_qmv_tokens_are_independent_and_threads_agree():
 
 
 # --------------------------------------------------------------------------
+# unquantized rows (F16, F32): plain conversions, no activation rule
+# --------------------------------------------------------------------------
+
+def _float_w(M, K, seed):
+    r = np.random.default_rng(seed)
+    w = (r.standard_normal((M, K)) * 0.05).astype(np.float32)
+    # values at binary16 ties, subnormals, overflow, signed zeros
+    ties = (np.arange(1, 64, dtype=np.uint16) * 37).view(np.float16).astype(np.float64)
+    nxt = (np.arange(1, 64, dtype=np.uint16) * 37 + 1).view(np.float16).astype(np.float64)
+    special = np.concatenate([(ties + nxt) / 2, [2.0 ** -24, 3 * 2.0 ** -26, 65519.0, 65520.0, 7e4, -0.0, 0.0]])
+    w.reshape(-1)[:special.size] = special.astype(np.float32)
+    return w
+
+
+def test_f16_rows_are_numpy_binary16_and_f32_rows_the_bits():
+    M, K = 5, 96
+    w = _float_w(M, K, 1)
+    W16 = oracle.quantize(oracle.F16, w)
+    assert W16.shape == (M, 2 * K)
+    assert np.array_equal(W16.view(np.uint16), w.astype(np.float16).view(np.uint16))
+    d16 = oracle.dequant(oracle.F16, W16, K)
+    assert np.array_equal(d16, w.astype(np.float16).astype(np.float64))
+    W32 = oracle.quantize(oracle.F32, w)
+    assert np.array_equal(W32, w.view(np.uint8).reshape(M, 4 * K))
+    assert np.array_equal(oracle.dequant(oracle.F32, W32, K).view(np.uint64),
+                          w.astype(np.float64).view(np.uint64))
+
+
+def test_f16_conversion_is_the_nearest_binary16_by_brute_force():
+    # every finite binary16 value; the nearest one to each weight, ties to
+    # the even bit pattern (signed zeros compared by value)
+    w = _float_w(1, 512, 2)[0]
+    w = w[np.abs(w) < 65520.0]
+    pats = np.arange(0, 0x7C00, dtype=np.uint32).astype(np.uint16)
+    vals = pats.view(np.float16).astype(np.float64)
+    got = oracle.quantize(oracle.F16, np.pad(w, (0, (-w.size) % 32))[None, :]).view(np.uint16)[0][:w.size]
+    for v, g in zip(w.astype(np.float64), got):
+        dist = np.abs(vals - abs(v))
+        best = np.flatnonzero(dist == dist.min())
+        pick = best[0] if best.size == 1 else best[(pats[best] & 1) == 0][0]
+        assert (g & 0x7FFF) == pats[pick]
+        assert (g >> 15) == (1 if np.signbit(v) else 0)
+
+
+@pytest.mark.parametrize("fmt", [oracle.F16, oracle.F32])
+def test_float_qmv_uses_x_unquantized_exactly(fmt):
+    from fractions import Fraction
+    M, K, n = 3, 64, 2
+    w = _float_w(M, K, 3)
+    w[~np.isfinite(w.astype(np.float16))] = 1.0   # keep F16 rows finite
+    # activations the activation rule would change (one large element per
+    # block leaves the small ones a few codes wide)
+    x = synth.activations(4, n, K)
+    x[:, ::32] = 100.0
+    x[:, 1] = 1e-3
+    W = oracle.quantize(fmt, w)
+    wh = oracle.dequant(fmt, W, K)
+    y, sabs = oracle.qmv(fmt, W, x, K)
+    for t in range(n):
+        for m in range(M):
+            exact = sum(Fraction(float(a)) * Fraction(float(b)) for a, b in zip(wh[m], x[t]))
+            assert abs(Fraction(float(y[t, m])) - exact) <= Fraction(2.0 ** -40) * abs(Fraction(float(sabs[t, m])))
+            assert sabs[t, m] == pytest.approx(float(np.sum(np.abs(wh[m] * x[t].astype(np.float64)))), rel=1e-14)
+    # the quantized-activation product is measurably different
+    yq = _xhat(x) @ wh.T
+    assert np.max(np.abs(yq - y)) > 1e-9 * np.max(sabs)
+
+
+# --------------------------------------------------------------------------
 # MoE
 # --------------------------------------------------------------------------
 
