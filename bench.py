@@ -443,7 +443,8 @@ def _replicas(torch, api, fmt, M, K, nbytes_min, dev, seed):
 
 def run_extra(torch, api, synth, stream, dev, peak):
     """µs/call and effective weight GB/s of every other configuration: the
-    Q8_0 GEMV, the IQ4_XS matvecs, split-K (LM head and long K), the MoE
+    Q8_0 GEMV, the IQ4_XS, Q5_K, Q6_K, Q8_G128, F16 and F32 matvecs, split-K
+    (LM head and long K), the MoE
     decode layer, the router + top-k step in front of it, sibling matvecs
     sharing x and the matvec with a residual add.  Weight sets
     rotate over replicas totalling > 2 x L2 (the LM head alone is > 6 x L2);
@@ -460,7 +461,9 @@ def run_extra(torch, api, synth, stream, dev, peak):
              ("iq4_xs_2048x6144", 2, 2048, 6144, (1, 4, 8)),
              ("q5_k_17408x5120", 3, 17408, 5120, (1, 4, 16)),
              ("q6_k_17408x5120", 4, 17408, 5120, (1, 4, 16)),
-             ("q8_g128_lm_head_151936x5120", 6, 151936, 5120, (1, 4, 16))]
+             ("q8_g128_lm_head_151936x5120", 6, 151936, 5120, (1, 4, 16)),
+             ("f16_17408x5120", 7, 17408, 5120, (1, 4, 16)),
+             ("f32_4096x4096", 8, 4096, 4096, (1, 4, 16))]
     for i, (name, fmt, M, K, ns) in enumerate(dense):
         Ws, rb = _replicas(torch, api, fmt, M, K, l2x2, dev, 2000 + i)
         res = {}
@@ -474,7 +477,8 @@ def run_extra(torch, api, synth, stream, dev, peak):
             r = line(rb, _graph_us(torch, stream, calls))
             r["n_split"] = S
             res[str(n)] = r
-        out[name] = {"format": ["Q8_0", "Q4_K", "IQ4_XS", "Q5_K", "Q6_K", "Q8_G64", "Q8_G128"][fmt], "bytes_per_call": rb, "replicas": len(Ws),
+        out[name] = {"format": ["Q8_0", "Q4_K", "IQ4_XS", "Q5_K", "Q6_K", "Q8_G64", "Q8_G128", "F16", "F32"][fmt],
+                     "bytes_per_call": rb, "replicas": len(Ws),
                      "n_tok": res}
         del Ws
 

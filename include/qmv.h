@@ -134,7 +134,9 @@
  *   qmv_run_residual, qmv_run_siblings; not qmv_run_q8, not the MoE pool).
  *   Their activations are staged in shared memory as fp32 for a CTA's whole
  *   K-range, so long rows take fewer tokens per pass (more passes over the
- *   weights); split-K shortens the range.
+ *   weights), and qmv_run takes rows of up to about 24K weights; split-K
+ *   shortens the range (qmv_splitk_choose picks enough splits for the
+ *   fp32 activations of one pass of up to 16 tokens to take at most 96 KB).
  *
  * Bytes per weight: Q8_0 1.0625, Q4_K 0.5625, IQ4_XS 0.53125, Q5_K 0.6875
  * (the same densities as the GGML formats of the same names), Q6_K 0.8125

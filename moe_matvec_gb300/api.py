@@ -15,10 +15,13 @@ import torch
 
 from . import build as _build
 
-Q8_0, Q4_K, IQ4_XS, Q5_K, Q6_K, Q8_G64, Q8_G128 = 0, 1, 2, 3, 4, 5, 6
-FORMATS = {"Q8_0": Q8_0, "Q4_K": Q4_K, "IQ4_XS": IQ4_XS}
-GROUP_WEIGHTS = {Q8_0: 256, Q4_K: 256, IQ4_XS: 512}
-BYTES_PER_WEIGHT = {Q8_0: 272 / 256, Q4_K: 144 / 256, IQ4_XS: 272 / 512}
+Q8_0, Q4_K, IQ4_XS, Q5_K, Q6_K, Q8_G64, Q8_G128, F16, F32 = 0, 1, 2, 3, 4, 5, 6, 7, 8
+FORMATS = {"Q8_0": Q8_0, "Q4_K": Q4_K, "IQ4_XS": IQ4_XS, "Q5_K": Q5_K, "Q6_K": Q6_K, "Q8_G64": Q8_G64,
+           "Q8_G128": Q8_G128, "F16": F16, "F32": F32}
+GROUP_WEIGHTS = {Q8_0: 256, Q4_K: 256, IQ4_XS: 512, Q5_K: 256, Q6_K: 256, Q8_G64: 512, Q8_G128: 1024,
+                 F16: 32, F32: 32}
+BYTES_PER_WEIGHT = {Q8_0: 272 / 256, Q4_K: 144 / 256, IQ4_XS: 272 / 512, Q5_K: 176 / 256, Q6_K: 208 / 256,
+                    Q8_G64: 528 / 512, Q8_G128: 1040 / 1024, F16: 2.0, F32: 4.0}
 MAX_TOKENS = 64
 MAX_TOPK = 8
 

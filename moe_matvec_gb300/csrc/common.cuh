@@ -13,7 +13,7 @@ namespace qmv {
 
 // ---------------------------------------------------------------------------
 // Format geometry.  A "chunk" is the K-slice one pipeline stage carries:
-// 1024 weights = 32 sub-blocks of 32, one sub-block per lane.
+// 1024 weights = 32 sub-blocks of 32, one sub-block per lane (F32 rows: 512).
 // ---------------------------------------------------------------------------
 constexpr int KCHUNK = 1024;
 constexpr int BLK = 32;
@@ -48,6 +48,19 @@ template <>
 struct Fmt<QMV_Q8_G128> {
   static constexpr int GW = 1024, GB = 1040;
 };
+// unquantized rows: a "group" is one 32-weight block of plain values
+template <>
+struct Fmt<QMV_F16> {
+  static constexpr int GW = 32, GB = 64;
+};
+template <>
+struct Fmt<QMV_F32> {
+  static constexpr int GW = 32, GB = 128;
+};
+__host__ __device__ constexpr bool is_float(int F) { return F == QMV_F16 || F == QMV_F32; }
+// Weights per chunk: 1024, except F32 rows, whose chunk of 512 weights keeps
+// a row chunk at 2048 bytes (the size of an F16 one).
+__host__ __device__ constexpr int kchunk_of(int F) { return F == QMV_F32 ? 512 : KCHUNK; }
 // int8 codes used as they are (one fp16 scale per 32, 64 or 128 weights)
 __host__ __device__ constexpr bool is_q8(int F) { return F == QMV_Q8_0 || F == QMV_Q8_G64 || F == QMV_Q8_G128; }
 // Formats with a per-sub-block minimum (w = d sc q - dmin m): their min term
@@ -55,7 +68,7 @@ __host__ __device__ constexpr bool is_q8(int F) { return F == QMV_Q8_0 || F == Q
 __host__ __device__ constexpr bool has_min(int F) { return F == QMV_Q4_K || F == QMV_Q5_K; }
 template <int F>
 constexpr int chunk_bytes() {
-  return (KCHUNK / Fmt<F>::GW) * Fmt<F>::GB;
+  return (kchunk_of(F) / Fmt<F>::GW) * Fmt<F>::GB;
 }
 
 // ---------------------------------------------------------------------------

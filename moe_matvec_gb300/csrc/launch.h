@@ -29,6 +29,8 @@ cudaError_t launch_dense_q5_k(const DenseLaunch& L);
 cudaError_t launch_dense_q6_k(const DenseLaunch& L);
 cudaError_t launch_dense_q8_g64(const DenseLaunch& L);
 cudaError_t launch_dense_q8_g128(const DenseLaunch& L);
+cudaError_t launch_dense_f16(const DenseLaunch& L);
+cudaError_t launch_dense_f32(const DenseLaunch& L);
 
 struct MoeParams;
 

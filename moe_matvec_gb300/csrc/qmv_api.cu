@@ -96,10 +96,13 @@ static bool encode_rows(CUtensorMap* map, const void* W, long long rows, long lo
 // Validation helpers.
 // ---------------------------------------------------------------------------
 static int group_weights(int fmt) {
+  if (is_float(fmt)) return 32;
   return fmt == QMV_IQ4_XS || fmt == QMV_Q8_G64 ? 512 : (fmt == QMV_Q8_G128 ? 1024 : 256);
 }
 static int group_bytes(int fmt) {
   switch (fmt) {
+    case QMV_F16: return 64;
+    case QMV_F32: return 128;
     case QMV_Q4_K: return 144;
     case QMV_Q5_K: return 176;
     case QMV_Q6_K: return 208;
@@ -108,14 +111,17 @@ static int group_bytes(int fmt) {
   }
   return 272;  // Q8_0, IQ4_XS
 }
-static int chunk_bytes_of(int fmt) { return (KCHUNK / group_weights(fmt)) * group_bytes(fmt); }
+static int chunk_bytes_of(int fmt) { return (kchunk_of(fmt) / group_weights(fmt)) * group_bytes(fmt); }
 static bool fmt_ok(int fmt) {
-  return fmt >= QMV_Q8_0 && fmt <= QMV_Q8_G128;
+  return fmt >= QMV_Q8_0 && fmt <= QMV_F32;
 }
 // formats the MoE kernels are instantiated for
 static bool moe_fmt_ok(int fmt) { return fmt == QMV_Q8_0 || fmt == QMV_Q4_K || fmt == QMV_IQ4_XS; }
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 constexpr long long MAX_K = 1ll << 20;
+// fp32 activations of a split range that split-K choices give F16 / F32
+// rows (for one pass of up to 16 tokens): they fit beside two weight stages
+constexpr long long FLOAT_ACT_BYTES = 96 * 1024;
 constexpr long long MAX_M = 1ll << 30;
 
 static int check_device() {
@@ -166,15 +172,16 @@ static bool plan_dense(int fmt, long long M, long long K, int n_tok, int n_split
   const int gw = group_weights(fmt);
   const long long groups = K / gw;
   const long long max_range = ((groups + n_split - 1) / n_split) * gw;  // weights
-  pl.act_nck = (int)((max_range + KCHUNK - 1) / KCHUNK);
+  pl.act_nck = (int)((max_range + kchunk_of(fmt) - 1) / kchunk_of(fmt));
   const size_t budget = (size_t)device_smem_optin();
   int nt = 16;
   while (nt > n_tok && nt > 1) nt >>= 1;
   if (nt < n_tok && nt < 16) nt <<= 1;  // smallest power of two >= n_tok (<= 16)
   // from 8 tokens on twelve consumer warps where their tiles fit, else eight
+  // (F16 / F32 rows: eight)
   for (;; nt >>= 1) {
     bool ok = false;
-    for (int cw = nt >= 8 ? 12 : 8; cw >= 8 && !ok; cw -= 4) {
+    for (int cw = nt >= 8 && !is_float(fmt) ? 12 : 8; cw >= 8 && !ok; cw -= 4) {
       pl.cw = cw;
       pl.tile_rows = cw * RW;
       ok = plan_stages(nt, cw, act_area_bytes(fmt, nt, pl.act_nck), pl.tile_rows * chunk_bytes_of(fmt), budget,
@@ -200,6 +207,8 @@ static cudaError_t launch_dense_any(int fmt, const DenseLaunch& L) {
     case QMV_Q6_K: return launch_dense_q6_k(L);
     case QMV_Q8_G64: return launch_dense_q8_g64(L);
     case QMV_Q8_G128: return launch_dense_q8_g128(L);
+    case QMV_F16: return launch_dense_f16(L);
+    case QMV_F32: return launch_dense_f32(L);
     default: return launch_dense_iq4_xs(L);
   }
 }
@@ -394,6 +403,7 @@ int qmv_run_q8(int fmt, const void* W, const int8_t* xq, const float* xd, const 
                int64_t K, int n_tok, cudaStream_t stream) {
   int rc = check_dense_args(fmt, W, xq, y, M, K, n_tok);
   if (rc) return rc;
+  if (is_float(fmt)) return QMV_ERR_FORMAT;  // F16 / F32 rows take fp32 activations
   if (!xd || !xs) return QMV_ERR_NULL;
   if (!aligned16(xd) || !aligned16(xs)) return QMV_ERR_ALIGN;
   if ((rc = check_device())) return rc;
@@ -401,14 +411,22 @@ int qmv_run_q8(int fmt, const void* W, const int8_t* xq, const float* xd, const 
 }
 
 int qmv_splitk_choose(int fmt, int64_t M, int64_t K, int n_tok) {
-  (void)n_tok;
   if (!fmt_ok(fmt)) return QMV_ERR_FORMAT;
   if (M <= 0 || K <= 0 || K % group_weights(fmt)) return QMV_ERR_SHAPE;
   const long long units = (M + UNIT_ROWS - 1) / UNIT_ROWS;
   const long long want = 2ll * device_sm_count();  // >= 2 row units per SM
-  if (units >= want) return 1;
-  const long long chunks = (K + KCHUNK - 1) / KCHUNK;
-  long long target = (want + units - 1) / units;
+  // F16 / F32 rows stage a split's fp32 activations whole: enough splits for
+  // one pass of the tokens (up to 16) to fit in FLOAT_ACT_BYTES
+  const long long kc = kchunk_of(fmt), chunks = (K + kc - 1) / kc;
+  long long fmin = 1;
+  if (is_float(fmt)) {
+    long long nt = 1;
+    while (nt < n_tok && nt < 16) nt <<= 1;
+    fmin = (K * nt * 4 + FLOAT_ACT_BYTES - 1) / FLOAT_ACT_BYTES;
+  }
+  if (units >= want && fmin <= 1) return 1;
+  long long target = units >= want ? 1 : (want + units - 1) / units;
+  if (target < fmin) target = fmin;
   if (target > 64) target = 64;
   // smallest divisor of the chunk count that reaches the target, so that
   // every split covers whole chunks
@@ -457,7 +475,7 @@ static int splitk_impl(int fmt, const void* W, const float* x, const float* add,
   const int8_t* xq = nullptr;
   const float* xd = nullptr;
   const int32_t* xs = nullptr;
-  if (n_tok >= 4 && ws && aligned16(ws) && q8 && ws_bytes >= part + q8) {
+  if (n_tok >= 4 && !is_float(fmt) && ws && aligned16(ws) && q8 && ws_bytes >= part + q8) {
     uint8_t* base = static_cast<uint8_t*>(ws) + part;
     const size_t nb = (size_t)n_tok * (size_t)(K / 32);
     int8_t* q = reinterpret_cast<int8_t*>(base);
@@ -496,14 +514,17 @@ int qmv_run_siblings(int count, const int* fmts, const void* const* W, const int
   int rc;
   for (int i = 0; i < count; i++)
     if ((rc = check_dense_args(fmts[i], W[i], x, y[i], M[i], K, n_tok))) return rc;
+  // F16 / F32 siblings take x as it is; the others share one quantization
+  bool quant = false;
+  for (int i = 0; i < count; i++) quant = quant || !is_float(fmts[i]);
   const size_t q8 = qmv_act_q8_bytes(K, n_tok);
-  if (n_tok >= 4) {
+  if (n_tok >= 4 && quant) {
     if (!ws) return QMV_ERR_NULL;
     if (!aligned16(ws)) return QMV_ERR_ALIGN;
     if (ws_bytes < q8) return QMV_ERR_WORKSPACE;
   }
   if ((rc = check_device())) return rc;
-  if (n_tok < 4) {
+  if (n_tok < 4 || !quant) {
     // few tokens: every matvec quantizes the activations while staging
     for (int i = 0; i < count; i++)
       if ((rc = run_dense(fmts[i], W[i], x, nullptr, nullptr, nullptr, y[i], M[i], K, n_tok, 1, stream))) return rc;
@@ -516,8 +537,11 @@ int qmv_run_siblings(int count, const int* fmts, const void* const* W, const int
   float* d = reinterpret_cast<float*>(base + align256((size_t)n_tok * (size_t)K));
   int32_t* sm = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(d) + align256(nb * 4));
   if (launch_act_quant(x, (int)K, n_tok, q, d, sm, stream, true) != cudaSuccess) return QMV_ERR_CUDA;
-  for (int i = 0; i < count; i++)
-    if ((rc = run_dense(fmts[i], W[i], nullptr, q, d, sm, y[i], M[i], K, n_tok, 1, stream))) return rc;
+  for (int i = 0; i < count; i++) {
+    rc = is_float(fmts[i]) ? run_dense(fmts[i], W[i], x, nullptr, nullptr, nullptr, y[i], M[i], K, n_tok, 1, stream)
+                           : run_dense(fmts[i], W[i], nullptr, q, d, sm, y[i], M[i], K, n_tok, 1, stream);
+    if (rc) return rc;
+  }
   return QMV_OK;
 }
 

@@ -67,8 +67,15 @@ __device__ __forceinline__ int act_pos(int l, int p) {
 // so that within a chunk every slot sits at a fixed offset.  A slot's chunk
 // of codes, scales or sums is one contiguous piece of the library's
 // pre-quantized activation rows, so those arrive by bulk copies.
+// (F16 / F32 weights take fp32 activations: [chunk][slot] kchunk_of(F)
+// floats, no scales or sums.)
 __host__ __device__ constexpr size_t act_area_bytes(int F, int nt_slots, int nck) {
-  return (size_t)nck * nt_slots * (ACT_BYTES + 32 * sizeof(float) * (has_min(F) ? 2 : 1));
+  return is_float(F) ? (size_t)nck * nt_slots * kchunk_of(F) * sizeof(float)
+                     : (size_t)nck * nt_slots * (ACT_BYTES + 32 * sizeof(float) * (has_min(F) ? 2 : 1));
+}
+// Bytes of one token slot's activations in a chunk.
+__host__ __device__ constexpr int act_chunk_bytes(int F) {
+  return is_float(F) ? kchunk_of(F) * (int)sizeof(float) : ACT_BYTES;
 }
 
 struct ActArea {
@@ -716,6 +723,144 @@ struct Consumer {
 // Two CTAs fit on an SM for small token counts (so that consecutive calls
 // overlap under programmatic dependent launch); larger token counts keep more
 // accumulators in registers.
+// F16 / F32 weights ("Castagna Veloce", section "Kernels for the MI50": the
+// small-batch matvec over F16 and F32 weights as well): the activations are
+// staged as they are, fp32, and every product and sum is an fp32 FMA.
+//
+// Stage weights [k0, k0 + nw) of tokens [0, nt) of `src` (k0 and nw
+// multiples of 32) into the area, [chunk][slot][kchunk_of(F)] floats, zero
+// past nw in the last chunk; slots from nt on are left as they are (the
+// consumer never stores their sums).  F16: within each 256-element piece,
+// elements 8l .. 8l+3 sit at 4l and 8l+4 .. 8l+7 at 128 + 4l, so that the
+// lanes' two 16-byte loads of a piece are each 512 contiguous bytes.  Called
+// by all consumer warps.
+template <int F, int NT, int CW = CONSUMER_WARPS>
+__device__ __forceinline__ void stage_float(const ActSource& src, long long k0, int nw, int nt, const ActArea& a,
+                                            int cw, int lane) {
+  constexpr int KC = kchunk_of(F), Q = KC / 4;  // float4 per slot chunk
+  constexpr int B = 8;                           // loads in flight per thread
+  const int nck = (nw + KC - 1) / KC;
+  const int per_tok = nck * Q, total = nt * per_tok;
+  float4* dst = reinterpret_cast<float4*>(a.q);
+  for (int base = cw * 32 + lane; base < total; base += B * CW * 32) {
+    float4 v[B];
+#pragma unroll
+    for (int j = 0; j < B; j++) {  // all loads first
+      const int i = base + j * CW * 32;
+      v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < total) {
+        const int t = i / per_tok, e4 = i - t * per_tok;  // float4 e4 of the token's range
+        if (4 * e4 < nw) v[j] = __ldg(reinterpret_cast<const float4*>(src.x + src.row(t) * src.ld + k0) + e4);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < B; j++) {
+      const int i = base + j * CW * 32;
+      if (i < total) {
+        const int t = i / per_tok, e4 = i - t * per_tok, c = e4 / Q;
+        int o = e4 - c * Q;  // float4 within the chunk
+        if constexpr (F == QMV_F16) o = (o & ~63) | ((o & 1) << 5) | ((o >> 1) & 31);
+        dst[((size_t)c * NT + t) * Q + o] = v[j];
+      }
+    }
+  }
+}
+
+// Consumer step for F16 / F32 rows: a row chunk (2048 bytes) is four
+// 512-byte pieces; in piece s lane l takes the 16 bytes at 512 s + 16 l, that
+// is 8 F16 or 4 F32 weights at element E s + (E / 32) l (E: weights per
+// piece), paired with the same elements of every token's activations.
+template <int F, int NT>
+struct FloatConsumer {
+  uint32_t w_off, x_off;  // the lane's bytes in a row chunk / a token's chunk of activations
+  __device__ explicit FloatConsumer(int lane) {
+    w_off = 16 * lane;
+    x_off = 16 * lane;  // F16: and 512 bytes further (the staging's order)
+  }
+  template <int PAIR_STRIDE = 2 * chunk_bytes<F>()>
+  __device__ __forceinline__ void chunk(uint32_t row0, uint32_t aq, uint32_t ad, uint32_t as, int nt,
+                                        AccTile<NT>& acc) const {
+    (void)ad;
+    (void)as;
+    constexpr int CB = chunk_bytes<F>();
+    constexpr int EL = F == QMV_F16 ? 8 : 4;     // weights per lane per piece
+    constexpr uint32_t sq = kchunk_of(F) * 4;   // bytes of a token slot's chunk
+    // the pieces stay a loop: unrolled, the step's code (up to 2048 FMAs
+    // for 16 tokens) outgrows the instruction cache
+#pragma unroll 1
+    for (int s = 0; s < 4; s++) {
+      float w[RW][EL];
+#pragma unroll
+      for (int r = 0; r < RW; r++) {
+        const uint4 q = lds128(row0 + (r & 1) * CB + (r >> 1) * PAIR_STRIDE + 512 * s + w_off);
+        if constexpr (F == QMV_F16) {
+          const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int i = 0; i < 4; i++) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&qq[i]));
+            w[r][2 * i] = f.x;
+            w[r][2 * i + 1] = f.y;
+          }
+        } else {
+          w[r][0] = __uint_as_float(q.x);
+          w[r][1] = __uint_as_float(q.y);
+          w[r][2] = __uint_as_float(q.z);
+          w[r][3] = __uint_as_float(q.w);
+        }
+      }
+      const uint32_t xp = aq + 4 * EL * 32 * s + x_off;  // piece s of the token's chunk
+      // tokens in pairs (slot t + 1 past nt holds stale values: its sums are
+      // never stored), 2 RW independent chains
+#pragma unroll
+      for (int t = 0; t < NT; t += 2) {
+        if (t >= nt) break;
+        float xa[EL], xb[EL];
+        load_x(xp + t * sq, xa);
+        if constexpr (NT > 1) load_x(xp + (t + 1) * sq, xb);
+#pragma unroll
+        for (int i = 0; i < EL; i++)
+#pragma unroll
+          for (int r = 0; r < RW; r++) {
+            acc.v[r][t >> 1].x = fmaf(w[r][i], xa[i], acc.v[r][t >> 1].x);
+            if constexpr (NT > 1) acc.v[r][t >> 1].y = fmaf(w[r][i], xb[i], acc.v[r][t >> 1].y);
+          }
+      }
+    }
+  }
+
+  template <int EL>
+  static __device__ __forceinline__ void load_x(uint32_t a, float (&xv)[EL]) {
+    const uint4 x0 = lds128(a);
+    xv[0] = __uint_as_float(x0.x);
+    xv[1] = __uint_as_float(x0.y);
+    xv[2] = __uint_as_float(x0.z);
+    xv[3] = __uint_as_float(x0.w);
+    if constexpr (EL == 8) {
+      const uint4 x1 = lds128(a + 512);
+      xv[4] = __uint_as_float(x1.x);
+      xv[5] = __uint_as_float(x1.y);
+      xv[6] = __uint_as_float(x1.z);
+      xv[7] = __uint_as_float(x1.w);
+    }
+  }
+};
+
+// The consumer of format F.
+template <int F, int NT>
+struct ConsumerSel {
+  using type = Consumer<F, NT>;
+};
+template <int NT>
+struct ConsumerSel<QMV_F16, NT> {
+  using type = FloatConsumer<QMV_F16, NT>;
+};
+template <int NT>
+struct ConsumerSel<QMV_F32, NT> {
+  using type = FloatConsumer<QMV_F32, NT>;
+};
+template <int F, int NT>
+using ConsumerOf = typename ConsumerSel<F, NT>::type;
+
 template <int NT, int CW = CONSUMER_WARPS>
 constexpr int dense_min_blocks() {
   return NT <= 4 && CW == CONSUMER_WARPS ? 2 : 1;

@@ -104,14 +104,15 @@ __device__ __forceinline__ void split_range(const DenseParams& p, int s, int& g0
 // ADD: the residual of p.add is added at the store (separate instantiations,
 // so the plain matvec carries none of its code).
 template <int F, int NT, bool Q8IN, int CW, bool ADD>
-__global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT, CW>())
+__global__ void __launch_bounds__(Shape<CW>::THREADS, is_float(F) ? 1 : dense_min_blocks<NT, CW>())
     qmv_dense_kernel(const __grid_constant__ CUtensorMap map_tile, const __grid_constant__ CUtensorMap map_unit,
                      const DenseParams p) {
   using SH = Shape<CW>;
   constexpr int TILE_ROWS = SH::TILE_ROWS, TU = TILE_ROWS / UNIT_ROWS, CONSUMER_THREADS = SH::CONSUMER_THREADS;
-  constexpr int CB = chunk_bytes<F>();
+  constexpr int CB = chunk_bytes<F>(), KC = kchunk_of(F), ACTB = act_chunk_bytes(F);
   constexpr int GW = Fmt<F>::GW, GB = Fmt<F>::GB;
   constexpr int STAGE_BYTES = TILE_ROWS * CB;
+  static_assert(!is_float(F) || !Q8IN, "F16 / F32 rows take fp32 activations");
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stages = smem;
   ActArea a;
@@ -155,7 +156,7 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT, CW>()
           valid = w.next(s, u, nu);
           if (valid) {
             split_range(p, s, g0, g1);
-            nck = ((g1 - g0) * GW + KCHUNK - 1) / KCHUNK;
+            nck = ((g1 - g0) * GW + KC - 1) / KC;
           }
           c = 0;
         }
@@ -181,7 +182,7 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT, CW>()
       while (alive && walk.next(s, u, nu)) {
         int g0, g1;
         split_range(p, s, g0, g1);
-        const int nck = ((g1 - g0) * GW + KCHUNK - 1) / KCHUNK;
+        const int nck = ((g1 - g0) * GW + KC - 1) / KC;
         for (int c = 0; c < nck; c++, ring.advance(p.stages)) {
           if (p.prefetch > 0 && ring.n >= p.stages) prefetch_to(ring.n + p.prefetch);
           if (ring.n == GATE && !mbar_wait(abar + 1, 0, p.err)) {
@@ -222,7 +223,7 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT, CW>()
   int s, u, nu;
   Ring ring;
   int staged_split = -1;
-  const Consumer<F, NT> cons(lane);
+  const ConsumerOf<F, NT> cons(lane);
   const uint32_t stage_base = smem_u32(stages), aq_base = smem_u32(a.q), ad_base = smem_u32(a.d),
                  as_base = smem_u32(a.s);
   // token pass blockIdx.y: tokens t0 .. t0 + ntk - 1 of the call
@@ -236,7 +237,9 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT, CW>()
     const int kb0 = g0 * (GW / BLK), nblk = (g1 - g0) * (GW / BLK);
     if (s != staged_split) {
       named_sync(1, CONSUMER_THREADS);  // nobody still reads the previous range
-      if constexpr (!Q8IN) {
+      if constexpr (is_float(F)) {
+        stage_float<F, NT, CW>(src, (long long)kb0 * BLK, nblk * BLK, ntk, a, cw, lane);
+      } else if constexpr (!Q8IN) {
         stage_activations<F, NT, (NT >= 8 ? 8 : 4), CW>(src, kb0, nblk, ntk, a, cw, lane);
       } else {
         alive = __all_sync(FULL, stage_q8_bulk<F, NT, CW>(src, kb0, nblk, ntk, a, abar, aphase, p.err, cw, lane)) &&
@@ -249,7 +252,7 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT, CW>()
     }
     const long long row0 = (long long)u * UNIT_ROWS;
     const int nrows = (int)min((long long)nu * UNIT_ROWS, p.M - row0);
-    const int nck = (nblk * BLK + KCHUNK - 1) / KCHUNK;
+    const int nck = (nblk * BLK + KC - 1) / KC;
     AccTile<NT> acc;  // zeroed per tile: no accumulator is live while staging
     acc.zero();
     // Thin tiles (a few units) would leave most warps without rows: there
@@ -272,7 +275,7 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, dense_min_blocks<NT, CW>()
         break;
       }
       if (grp * RW < nrows && (c & (ks - 1)) == part)  // ks is 1, 2 or 4
-        cons.chunk(stage_base + st * STAGE_BYTES + grp * RW * CB, aq_base + c * NT * ACT_BYTES,
+        cons.chunk(stage_base + st * STAGE_BYTES + grp * RW * CB, aq_base + c * NT * ACTB,
                    ad_base + c * NT * 128, as_base + c * NT * 128, ntk, acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);

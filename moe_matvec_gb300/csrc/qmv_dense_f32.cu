@@ -1,0 +1,7 @@
+// Dense matvec kernels for the QMV_F32 weight format (one unit per format so the
+// instantiations compile in parallel).
+#include "qmv_dense_inst.cuh"
+
+namespace qmv {
+cudaError_t launch_dense_f32(const DenseLaunch& L) { return launch_dense_fmt<QMV_F32>(L); }
+}  // namespace qmv

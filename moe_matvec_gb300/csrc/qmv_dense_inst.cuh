@@ -40,21 +40,39 @@ static cudaError_t launch_dense_nt(const DenseLaunch& L) {
 
 template <int F, bool Q8IN, bool ADD>
 static cudaError_t launch_dense_src(const DenseLaunch& L) {
-  switch (L.nt_tmpl) {
-    case 1: return launch_dense_nt<F, 1, Q8IN, 8, ADD>(L);
-    case 2: return launch_dense_nt<F, 2, Q8IN, 8, ADD>(L);
-    case 4: return launch_dense_nt<F, 4, Q8IN, 8, ADD>(L);
-    case 8: return L.cw == 12 ? launch_dense_nt<F, 8, Q8IN, 12, ADD>(L) : launch_dense_nt<F, 8, Q8IN, 8, ADD>(L);
-    case 16: return L.cw == 12 ? launch_dense_nt<F, 16, Q8IN, 12, ADD>(L) : launch_dense_nt<F, 16, Q8IN, 8, ADD>(L);
+  if constexpr (is_float(F)) {
+    // F16 / F32 rows: eight consumer warps at every token count
+    switch (L.nt_tmpl) {
+      case 1: return launch_dense_nt<F, 1, false, 8, ADD>(L);
+      case 2: return launch_dense_nt<F, 2, false, 8, ADD>(L);
+      case 4: return launch_dense_nt<F, 4, false, 8, ADD>(L);
+      case 8: return launch_dense_nt<F, 8, false, 8, ADD>(L);
+      case 16: return launch_dense_nt<F, 16, false, 8, ADD>(L);
+    }
+    return cudaErrorInvalidValue;
+  } else {
+    switch (L.nt_tmpl) {
+      case 1: return launch_dense_nt<F, 1, Q8IN, 8, ADD>(L);
+      case 2: return launch_dense_nt<F, 2, Q8IN, 8, ADD>(L);
+      case 4: return launch_dense_nt<F, 4, Q8IN, 8, ADD>(L);
+      case 8: return L.cw == 12 ? launch_dense_nt<F, 8, Q8IN, 12, ADD>(L) : launch_dense_nt<F, 8, Q8IN, 8, ADD>(L);
+      case 16:
+        return L.cw == 12 ? launch_dense_nt<F, 16, Q8IN, 12, ADD>(L) : launch_dense_nt<F, 16, Q8IN, 8, ADD>(L);
+    }
+    return cudaErrorInvalidValue;
   }
-  return cudaErrorInvalidValue;
 }
 
 template <int F>
 static cudaError_t launch_dense_fmt(const DenseLaunch& L) {
   const bool q8 = L.p->x == nullptr, add = L.p->add != nullptr;
-  if (add) return q8 ? launch_dense_src<F, true, true>(L) : launch_dense_src<F, false, true>(L);
-  return q8 ? launch_dense_src<F, true, false>(L) : launch_dense_src<F, false, false>(L);
+  if constexpr (is_float(F)) {
+    if (q8) return cudaErrorInvalidValue;
+    return add ? launch_dense_src<F, false, true>(L) : launch_dense_src<F, false, false>(L);
+  } else {
+    if (add) return q8 ? launch_dense_src<F, true, true>(L) : launch_dense_src<F, false, true>(L);
+    return q8 ? launch_dense_src<F, true, false>(L) : launch_dense_src<F, false, false>(L);
+  }
 }
 
 }  // namespace qmv

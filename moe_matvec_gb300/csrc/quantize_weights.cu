@@ -266,7 +266,30 @@ __global__ void __launch_bounds__(128) quantize_kernel(const float* __restrict__
 
 }  // namespace
 
+// F16 / F32 rows: one conversion per weight (binary16 rounded to nearest
+// even, or the fp32 value as it is); the rows are the flat [M][K] array.
+template <int F>
+__global__ void convert_rows_kernel(const float* __restrict__ w, long long n, uint8_t* __restrict__ out) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    if constexpr (F == QMV_F16)
+      reinterpret_cast<__half*>(out)[i] = __float2half_rn(w[i]);
+    else
+      reinterpret_cast<float*>(out)[i] = w[i];
+  }
+}
+
 cudaError_t launch_quantize_weights(int fmt, const float* w, long long M, int K, void* W, cudaStream_t stream) {
+  if (fmt == QMV_F16 || fmt == QMV_F32) {
+    const long long n = M * K;
+    long long ctas = (n + 255) / 256;
+    const long long cap = 32ll * device_sm_count();
+    if (ctas > cap) ctas = cap;
+    if (fmt == QMV_F16)
+      convert_rows_kernel<QMV_F16><<<(unsigned)ctas, 256, 0, stream>>>(w, n, static_cast<uint8_t*>(W));
+    else
+      convert_rows_kernel<QMV_F32><<<(unsigned)ctas, 256, 0, stream>>>(w, n, static_cast<uint8_t*>(W));
+    return cudaGetLastError();
+  }
   const int gw = fmt == QMV_IQ4_XS || fmt == QMV_Q8_G64 ? 512 : (fmt == QMV_Q8_G128 ? 1024 : 256);
   long long groups = M * (K / gw);
   long long ctas = (groups + 127) / 128;

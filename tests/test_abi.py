@@ -44,5 +44,6 @@ def test_strerror_and_row_bytes_need_no_device():
     assert lib.qmv_row_bytes(1, 5120) == 2880
     assert lib.qmv_row_bytes(2, 2048) == 1088
     assert lib.qmv_row_bytes(2, 256) == -2      # IQ4_XS needs K % 512 == 0
-    assert lib.qmv_row_bytes(7, 256) == -1
+    assert lib.qmv_row_bytes(7, 256) == 512 and lib.qmv_row_bytes(8, 256) == 1024   # F16 / F32 rows
+    assert lib.qmv_row_bytes(9, 256) == -1
     assert api.strerror(-6) == "workspace too small"

@@ -17,7 +17,7 @@ def L():
 
 
 def test_qmv_run_rejects_bad_arguments(L):
-    assert L.qmv_run(7, A, A, A, 16, 256, 1, None) == -1
+    assert L.qmv_run(9, A, A, A, 16, 256, 1, None) == -1
     assert L.qmv_run(3, A, A, A, 16, 100, 1, None) == -2        # Q5_K needs K % 256
     assert L.qmv_run(0, A, A, A, 0, 256, 1, None) == -2
     assert L.qmv_run(0, A, A, A, 16, 100, 1, None) == -2
@@ -27,6 +27,20 @@ def test_qmv_run_rejects_bad_arguments(L):
     assert L.qmv_run(0, None, A, A, 16, 256, 1, None) == -4
     assert L.qmv_run(0, A, MIS, A, 16, 256, 1, None) == -5
     assert L.qmv_run_q8(1, A, A, None, A, A, 16, 256, 1, None) == -4
+
+
+def test_float_rows_shape_and_entry_points(L):
+    # F16 / F32: K % 32, plain rows, fp32 activations only, no MoE pool (the
+    # router takes them)
+    assert L.qmv_row_bytes(7, 96) == 192 and L.qmv_row_bytes(8, 96) == 384
+    assert L.qmv_row_bytes(7, 100) == -2
+    assert L.qmv_run(8, A, A, A, 16, 100, 1, None) == -2
+    assert L.qmv_run_q8(7, A, A, A, A, A, 16, 256, 1, None) == -1
+    assert L.qmv_run_q8(8, A, A, A, A, A, 16, 256, 1, None) == -1
+    assert L.qmv_quantize_weights(7, A, 4, 48, A, None) == -2
+    ex = api.MoeExperts(128, 4096, 1536, 7, 1, 0, A, A)
+    assert L.moe_qmv_workspace_bytes(ctypes.byref(ex), 4, 8) == 0
+    assert L.moe_qmv_run(ctypes.byref(ex), A, A, A, A, 4, 8, A, 1 << 30, None) == -1
 
 
 def test_splitk_rejects_bad_workspace(L):
@@ -43,7 +57,7 @@ def test_quantize_entry_points_reject_bad_arguments(L):
     assert L.qmv_quantize_act(A, 100, 1, A, A, A, None) == -2
     assert L.qmv_quantize_act(A, 256, 0, A, A, A, None) == -3
     assert L.qmv_quantize_act(A, 256, 1, A, None, A, None) == -4
-    assert L.qmv_quantize_weights(7, A, 4, 256, A, None) == -1
+    assert L.qmv_quantize_weights(9, A, 4, 256, A, None) == -1
     assert L.qmv_quantize_weights(1, A, 4, 128, A, None) == -2
     assert L.qmv_quantize_weights(1, A, 4, 256, MIS, None) == -5
 
@@ -54,7 +68,7 @@ def test_device_error_needs_an_output_pointer(L):
 
 def test_route_rejects_bad_arguments(L):
     # fmt, Wr, x, E, hidden, n_tok, top_k, gating, logits, ids, gates, stream
-    assert L.moe_route_run(7, A, A, 128, 4096, 1, 8, 0, A, A, A, None) == -1
+    assert L.moe_route_run(9, A, A, 128, 4096, 1, 8, 0, A, A, A, None) == -1
     assert L.moe_route_run(0, A, A, 128, 100, 1, 8, 0, A, A, A, None) == -2
     assert L.moe_route_run(0, A, A, 513, 4096, 1, 8, 0, A, A, A, None) == -2     # > 512 experts
     assert L.moe_route_run(0, A, A, 128, 4096, 1, 8, 2, A, A, A, None) == -2     # unknown gating

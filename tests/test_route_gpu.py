@@ -20,7 +20,8 @@ pytestmark = pytest.mark.gpu
 
 CASES = [(0, 128, 4096, 1, 8, 0), (0, 128, 4096, 4, 8, 1), (0, 128, 4096, 64, 8, 0),
          (1, 64, 2048, 16, 6, 0), (2, 256, 1024, 33, 8, 1), (0, 512, 512, 5, 2, 0),
-         (1, 8, 256, 3, 8, 1), (2, 37, 512, 7, 1, 0)]
+         (1, 8, 256, 3, 8, 1), (2, 37, 512, 7, 1, 0),
+         (8, 128, 4096, 4, 8, 0), (7, 256, 2048, 16, 8, 1)]   # unquantized (F32 / F16) router rows
 
 
 def route_gpu(fmt, Wr, x, E, H, top_k, gating):
