@@ -613,6 +613,27 @@ def run_profile_moe(args):
     return 0
 
 
+def run_profile_float(args):
+    """Two eager F16 17408 x 5120 calls at --profile-float tokens, in the bench's
+    launch configuration (split chosen from the shape, workspace given), for
+    ncu captures."""
+    import torch
+    from moe_matvec_gb300 import api, synth
+    api.load()
+    fmt, Mf, Kf, n = 7, 17408, 5120, args.profile_float
+    g = torch.Generator(device="cuda")
+    g.manual_seed(2007)
+    W = api.quantize_weights(fmt, torch.randn((Mf, Kf), generator=g, device="cuda") * 0.02)
+    x = torch.from_numpy(synth.activations(3000 + n, n, Kf)).cuda()
+    S = api.splitk_choose(fmt, Mf, Kf, n)
+    ws = torch.empty(max(16, api.splitk_workspace_fast_bytes(Mf, Kf, n, S)), dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        api.splitk_run(fmt, W, x, Mf, Kf, n_split=S, ws=ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_run": "f16_17408x5120", "n_tok": n, "n_split": S, "calls": 2}))
+    return 0
+
+
 def run_profile(args):
     """A few eager calls of the timed workload (for ncu captures)."""
     import torch
@@ -644,6 +665,8 @@ def main(argv=None):
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--profile", action="store_true", help="a few eager calls only (for ncu)")
     ap.add_argument("--profile-moe", type=int, default=0, help="two eager MoE calls at this many tokens (for ncu)")
+    ap.add_argument("--profile-float", type=int, default=0,
+                    help="two eager F16 17408 x 5120 calls at this many tokens (for ncu)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -651,6 +674,8 @@ def main(argv=None):
         return run_reference(args)
     if args.profile_moe:
         return run_profile_moe(args)
+    if args.profile_float:
+        return run_profile_float(args)
     if args.profile:
         return run_profile(args)
     return run_ours(args)
