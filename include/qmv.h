@@ -311,8 +311,8 @@ typedef struct moe_experts {
   int32_t n_experts;   /* E */
   int32_t hidden;      /* H: K of gate/up, M of down */
   int32_t ffn;         /* F: rows of gate (and of up), K of down */
-  int32_t fmt_gate_up; /* any qmv_format */
-  int32_t fmt_down;    /* any qmv_format */
+  int32_t fmt_gate_up; /* QMV_Q8_0, QMV_Q4_K or QMV_IQ4_XS */
+  int32_t fmt_down;    /* QMV_Q8_0, QMV_Q4_K or QMV_IQ4_XS */
   int32_t reserved;
   const void* w_gate_up; /* [E][2F rows][row_bytes(fmt_gate_up, H)]:
                             rows 0..F-1 gate, rows F..2F-1 up */
