@@ -18,7 +18,8 @@ which picks one split for this shape and, from 4 tokens on, quantizes the
 activations once into the workspace).  Timed region: CUDA-graph replays of
 whole steps, CUDA events on the launching stream.  `e2e` repeats the steps through the public API with the
 activations copied in from pinned host memory and the outputs copied back,
-every step.  `--impl reference` times the CPU oracle on a bounded sample of
+every step (two device buffer sets, each copy direction on its own stream, so
+that a step's copies overlap its neighbours' matvecs).  `--impl reference` times the CPU oracle on a bounded sample of
 the same workload on the host cores.  Under torchrun (N > 1) every rank runs
 the same single-GPU workload (replicas: nothing in the path is sharded), the
 time is the maximum over ranks and the value sums the ranks' bytes.
@@ -357,20 +358,46 @@ def run_ours(args):
         extra = run_extra(torch, api, synth, stream, dev, measured_peaks()[0]["hbm_gbs"])
 
     # e2e: public API with host buffers, eager launches; every step copies its
-    # inputs in (one copy) and reads its results back (one copy)
+    # inputs in from pinned host memory (one copy) and reads its results back
+    # (one copy).  Two device buffer sets and one stream per copy direction
+    # let step i's copies overlap the matvecs of its neighbours, as a serving
+    # loop would run them.
     xh = x_all.cpu().pin_memory()
-    yh = torch.empty((sum(NTOKS), M)).pin_memory()
+    yh = [torch.empty((sum(NTOKS), M)).pin_memory() for _ in range(2)]
+    xb = [x_all, torch.empty_like(x_all)]
+    yb = [y_all, torch.empty_like(y_all)]
+    views = [({n: xb[b][offs[i]:offs[i + 1]] for i, n in enumerate(NTOKS)},
+              {n: yb[b][offs[i]:offs[i + 1]] for i, n in enumerate(NTOKS)}) for b in range(2)]
+    h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "out", "back")}
     e2e_steps = max(REPLICAS, min(steps, 2000))
     barrier(world)
     torch.cuda.synchronize()
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a0.record(stream)
-    with torch.cuda.stream(stream):
-        for i in range(e2e_steps):
-            x_all.copy_(xh, non_blocking=True)
-            for n in NTOKS:
-                matvec(Ws[i % REPLICAS], n, stream)
-            yh.copy_(y_all, non_blocking=True)
+    h2d.wait_event(a0)
+    d2h.wait_event(a0)
+    for i in range(e2e_steps):
+        b = i % 2
+        with torch.cuda.stream(h2d):
+            if i >= 2:
+                h2d.wait_event(ev["out"][b])        # step i - 2 has read xb[b]
+            xb[b].copy_(xh, non_blocking=True)
+            ev["in"][b].record(h2d)
+        stream.wait_event(ev["in"][b])
+        if i >= 2:
+            stream.wait_event(ev["back"][b])        # step i - 2's results are out of yb[b]
+        xv, yv = views[b]
+        for n in NTOKS:
+            api.splitk_run(FMT, Ws[i % REPLICAS], xv[n], M, K, n_split=splits[n], ws=wss[n], out=yv[n],
+                           stream=stream)
+        ev["out"][b].record(stream)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(ev["out"][b])
+            yh[b].copy_(yb[b], non_blocking=True)
+            ev["back"][b].record(d2h)
+    stream.wait_event(ev["back"][(e2e_steps - 1) % 2])
+    stream.wait_event(ev["back"][(e2e_steps - 2) % 2])
     a1.record(stream)
     a1.synchronize()
     barrier(world)
