@@ -95,3 +95,14 @@ def test_residual_and_siblings_reject_bad_arguments(L):
     bad = (ctypes.c_int * 2)(0, 2)                                     # IQ4_XS needs K % 512
     assert L.qmv_run_siblings(2, bad, Wp, Mp, yp, A, 256 + 1024, 2, A, 1 << 20, None) == -2
     assert L.qmv_run_siblings(2, fm, Wp, Mp, yp, A, 4096, 8, A, 16, None) == -6    # workspace too small
+
+
+def test_split_choice_fits_float_activations(L):
+    # F16 / F32 rows: enough splits that one pass of up to 16 tokens' fp32
+    # activations of a split range takes at most 96 KB (host logic only)
+    assert L.qmv_splitk_choose(7, 17408, 5120, 16) == 5      # 5 chunks of 1024: 64 KB each
+    assert L.qmv_splitk_choose(7, 17408, 5120, 1) == 1
+    assert L.qmv_splitk_choose(8, 4096, 4096, 16) == 4       # 8 chunks of 512
+    s = L.qmv_splitk_choose(8, 64, 65536, 2)
+    assert s >= 6 and 128 % s == 0 and (65536 // s) * 2 * 4 <= 96 * 1024
+    assert L.qmv_splitk_choose(1, 17408, 5120, 16) == 1      # quantized rows: the row count decides
