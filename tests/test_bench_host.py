@@ -64,3 +64,26 @@ def test_reference_arm_is_rank_zero_only(monkeypatch):
 def test_single_rank_aggregate():
     value, t = bench.aggregate([4.0], [8e9])
     assert t == 4.0 and value == pytest.approx(2000.0)
+
+
+def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
+    # the oracle timed on the host cores: one JSON line with the contract's
+    # keys (a tiny row sample here, so the test stays fast)
+    import json
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    real = bench.oracle_sample
+    monkeypatch.setattr(bench, "oracle_sample", lambda rows, seed=4242: real(min(rows, 8), seed))
+
+    class Args:
+        gpus, steps, warmup = 1, 2, 3
+
+    assert bench.run_reference(Args()) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == "GB/s"
+    assert line["higher_is_better"] is True and line["steps"] == 2 and line["warmup"] == 3
+    assert line["config"]["workload"] == bench.WORKLOAD
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] > 0
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
