@@ -118,7 +118,8 @@ def row_bytes(fmt: int, K: int) -> int:
 
 
 def quantize_weights(fmt: int, w: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """fp32 weights [M][K] -> quantized rows uint8 [M][row_bytes]."""
+    """fp32 weights [M][K] -> rows of format fmt, uint8 [M][row_bytes] (F16 / F32: the values
+    converted, binary16 rounded to nearest even)."""
     M, K = w.shape
     rb = row_bytes(fmt, K)
     if out is None:
@@ -140,7 +141,7 @@ def quantize_act(x: torch.Tensor, stream=None):
 
 def run(fmt: int, W: torch.Tensor, x: torch.Tensor, M: int, K: int, out: torch.Tensor | None = None,
         stream=None) -> torch.Tensor:
-    """y [n][M] = What x Xhat (quantized matvec), x fp32 [n][K]."""
+    """y [n][M] = What x Xhat (quantized matvec; F16 / F32 rows: Xhat = x), x fp32 [n][K]."""
     n = x.shape[0]
     if out is None:
         out = torch.empty((n, M), dtype=torch.float32, device=x.device)
@@ -150,7 +151,7 @@ def run(fmt: int, W: torch.Tensor, x: torch.Tensor, M: int, K: int, out: torch.T
 
 def run_q8(fmt: int, W: torch.Tensor, xq: torch.Tensor, xd: torch.Tensor, xs: torch.Tensor, M: int, K: int,
            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Matvec with activations already quantized by quantize_act."""
+    """Matvec with activations already quantized by quantize_act (quantized formats only)."""
     n = xq.shape[0]
     if out is None:
         out = torch.empty((n, M), dtype=torch.float32, device=xq.device)
