@@ -2,6 +2,8 @@
 // picks the compiled token-group size and raises the dynamic shared-memory
 // limit once per device.
 #pragma once
+#include <atomic>
+
 #include "launch.h"
 #include "moe_kernels.cuh"
 
@@ -11,10 +13,12 @@ template <int F, int NT, int MODE, int CW>
 static cudaError_t launch_moe_nt(const MoeLaunch& L) {
   using SH = Shape<CW>;
   auto kern = moe_qmv_kernel<F, NT, MODE, CW>;
-  static unsigned long long configured = 0;  // bit per device ordinal
+  // bit per device ordinal; host threads racing on a first launch both
+  // set the same attributes, which is harmless
+  static std::atomic<unsigned long long> configured{0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !((configured >> dev) & 1ull)) {
+  if (dev < 64 && !((configured.load(std::memory_order_acquire) >> dev) & 1ull)) {
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
@@ -28,7 +32,7 @@ static cudaError_t launch_moe_nt(const MoeLaunch& L) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
-    configured |= 1ull << dev;
+    configured.fetch_or(1ull << dev, std::memory_order_acq_rel);
   }
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];

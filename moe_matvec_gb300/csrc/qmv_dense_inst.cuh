@@ -1,6 +1,8 @@
 // Launcher of the dense matvec kernel for one format: picks the compiled
 // token count and raises the dynamic shared-memory limit once per device.
 #pragma once
+#include <atomic>
+
 #include "launch.h"
 #include "qmv_dense.cuh"
 
@@ -10,10 +12,12 @@ template <int F, int NT, bool Q8IN, int CW, bool ADD>
 static cudaError_t launch_dense_nt(const DenseLaunch& L) {
   using SH = Shape<CW>;
   auto kern = qmv_dense_kernel<F, NT, Q8IN, CW, ADD>;
-  static unsigned long long configured = 0;  // bit per device ordinal
+  // bit per device ordinal; host threads racing on a first launch both
+  // set the same attributes, which is harmless
+  static std::atomic<unsigned long long> configured{0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !((configured >> dev) & 1ull)) {
+  if (dev < 64 && !((configured.load(std::memory_order_acquire) >> dev) & 1ull)) {
     if constexpr (SH::RESPLIT) {
       // the warpgroups' register shares must fit in what the CTA is launched
       // with, or the consumers' request for more would never be granted
@@ -30,7 +34,7 @@ static cudaError_t launch_dense_nt(const DenseLaunch& L) {
     // (of this call or of the next one) can be resident together
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
-    configured |= 1ull << dev;
+    configured.fetch_or(1ull << dev, std::memory_order_acq_rel);
   }
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
