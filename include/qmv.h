@@ -36,6 +36,9 @@
  *     comment says otherwise).  The library allocates nothing, keeps no
  *     per-call state and never synchronises the stream (except
  *     qmv_get_device_error).  Calls are stream-ordered and asynchronous.
+ *   - Calls may come from several host threads at once (the library's
+ *     per-device lookups are made once under a lock; the only shared device
+ *     buffer is qmv_splitk_run_static's scratch array, see there).
  *   - Every data pointer must be 16-byte aligned (QMV_ERR_ALIGN otherwise).
  *   - Return value: 0 on success, a negative QMV_ERR_* code on a host-side
  *     argument error (nothing is launched then).  Errors detected on the
