@@ -12,11 +12,13 @@ chain slower").
 
 Inputs are synthetic and seeded (N(0, 0.02) weights quantized on the GPU by
 the library's quantizer, N(0, 1) activations).  Weights rotate over 12
-replicas (600 MB, > 4x the 129 MB L2), so every call streams from HBM.
+replicas (600 MB, > 4x the 129 MB L2), one replica per step, so every call
+streams from HBM.
 Each call is the library's matvec with a caller workspace (qmv_splitk_run,
 which picks one split for this shape and, from 4 tokens on, quantizes the
-activations once into the workspace).  Timed region: CUDA-graph replays of
-whole steps, CUDA events on the launching stream.  `e2e` repeats the steps through the public API with the
+activations once into the workspace).  Timed region: exactly --steps steps,
+each the replay of a captured one-step graph, CUDA events on the launching
+stream.  `e2e` repeats the steps through the public API with the
 activations copied in from pinned host memory and the outputs copied back,
 every step (two device buffer sets, each copy direction on its own stream, so
 that a step's copies overlap its neighbours' matvecs).  `--impl reference` times the CPU oracle on a bounded sample of
@@ -283,21 +285,23 @@ def run_ours(args):
         for n in NTOKS:
             matvec(Ws[r % REPLICAS], n, s)
 
-    # one graph = REPLICAS steps, each on its own replica
+    # one graph per replica, each one whole step on that replica; step i of
+    # the run replays graph i mod REPLICAS, so exactly --steps steps are timed
+    # after exactly --warmup untimed ones, every step streaming from HBM
     with torch.cuda.stream(stream):
         for r in range(REPLICAS):          # eager warm-up (also builds everything)
             step(r, stream)
     stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for r in range(REPLICAS):
+    graphs = []
+    for r in range(REPLICAS):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
             step(r, stream)
-    reps = max(1, (args.steps + REPLICAS - 1) // REPLICAS)
-    steps = reps * REPLICAS
-    warm_reps = max(1, (args.warmup + REPLICAS - 1) // REPLICAS)
+        graphs.append(gr)
+    steps = args.steps
     with torch.cuda.stream(stream):
-        for _ in range(warm_reps):
-            graph.replay()
+        for i in range(args.warmup):
+            graphs[i % REPLICAS].replay()
     stream.synchronize()
 
     # per-token-count graphs for the per-call breakdown
@@ -341,8 +345,8 @@ def run_ours(args):
         time.sleep(0.25)
         e0.record(stream)
         with torch.cuda.stream(stream):
-            for _ in range(reps):
-                graph.replay()
+            for i in range(steps):
+                graphs[(args.warmup + i) % REPLICAS].replay()
         e1.record(stream)
         e1.synchronize()
     torch.cuda.synchronize()
@@ -417,7 +421,7 @@ def run_ours(args):
             "peak_kind": peak_kind, "kernel": "qmv_dense_kernel<Q4_K>",
             "algorithmic_bytes_per_launch": BYTES_PER_CALL}
     line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": steps,
-            "warmup": warm_reps * REPLICAS, "ms_per_step": tmax / steps, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": tmax / steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int8xint8->int32, f32",
             "data": "synthetic N(0,0.02) weights quantized on GPU, N(0,1) activations",
             "config": {"workload": WORKLOAD, "format": "Q4_K", "M": M, "K": K, "n_tok": list(NTOKS),
@@ -430,10 +434,10 @@ def run_ours(args):
                     "d2h_bytes_per_step": sum(n * M * 4 for n in NTOKS),
                     "ms_per_step": e2e_ms / e2e_steps},
             "gpu_launches": launches, "clocks": clk.summary()}
-    if extra is not None:
-        line["workloads"] = extra
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
+    if extra is not None:
+        line["workloads"] = extra          # last: the long block of the other configurations
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -673,6 +677,33 @@ def run_profile_float(args):
     return 0
 
 
+def run_profile_dense(args):
+    """Eager calls of one dense configuration fmt:M:K:n_tok in the bench's
+    launch configuration (split from the shape, workspace with room for the
+    once-quantized activations), rotating over replicas larger than L2 in all,
+    for ncu captures: --profile-dense 2:6144:2048:1."""
+    import torch
+    from moe_matvec_gb300 import api, synth
+    api.load()
+    fmt, Md, Kd, n = (int(v) for v in args.profile_dense.split(":"))
+    g = torch.Generator(device="cuda")
+    g.manual_seed(2000 + fmt)
+    W0 = api.quantize_weights(fmt, torch.randn((Md, Kd), generator=g, device="cuda") * 0.02)
+    rb = Md * api.row_bytes(fmt, Kd)
+    Ws = [W0] + [W0.clone() for _ in range(max(1, -(-2 * 135 * 2 ** 20 // rb)) - 1)]
+    x = torch.from_numpy(synth.activations(3000 + n, n, Kd)).cuda()
+    y = torch.empty((n, Md), device="cuda")
+    S = api.splitk_choose(fmt, Md, Kd, n)
+    ws = torch.empty(max(16, api.splitk_workspace_fast_bytes(Md, Kd, n, S)), dtype=torch.uint8, device="cuda")
+    calls = max(4, len(Ws))
+    for i in range(calls):
+        api.splitk_run(fmt, Ws[i % len(Ws)], x, Md, Kd, n_split=S, ws=ws, out=y)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_run": f"fmt{fmt}_{Md}x{Kd}", "n_tok": n, "n_split": S, "calls": calls,
+                      "replicas": len(Ws)}))
+    return 0
+
+
 def run_profile(args):
     """A few eager calls of the timed workload (for ncu captures)."""
     import torch
@@ -706,6 +737,8 @@ def main(argv=None):
     ap.add_argument("--profile-moe", type=int, default=0, help="two eager MoE calls at this many tokens (for ncu)")
     ap.add_argument("--profile-float", type=int, default=0,
                     help="two eager F16 17408 x 5120 calls at this many tokens (for ncu)")
+    ap.add_argument("--profile-dense", default="",
+                    help="eager calls of one dense configuration fmt:M:K:n_tok (for ncu)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -715,6 +748,8 @@ def main(argv=None):
         return run_profile_moe(args)
     if args.profile_float:
         return run_profile_float(args)
+    if args.profile_dense:
+        return run_profile_dense(args)
     if args.profile:
         return run_profile(args)
     return run_ours(args)

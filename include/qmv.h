@@ -55,7 +55,10 @@
  *     q_i  = clamp(rne(x_i * id), -127, 127)     (fp32 product, then round
  *                                                 half to even to an integer)
  *     s    = sum_i q_i                           (int32)
- *   and Xhat_i = d * q_i.  Non-finite x is outside the contract.
+ *   and Xhat_i = d * q_i.  (A block whose amax is below about 3.7e-37 has a
+ *   subnormal d whose reciprocal overflows to infinity: its nonzero elements
+ *   get +-127 and its zero elements, 0 * inf being no number, get 0.)
+ *   Non-finite x is outside the contract.
  *
  * ------------------------------------------------------------------------
  * Weight formats (values are What; fp16 fields are IEEE binary16, little
@@ -291,7 +294,11 @@ int qmv_run_siblings(int count, const int* fmts, const void* const* W, const int
  * captures a CUDA graph (allocation is not allowed during capture), or a host
  * that owns all device memory.  This variant takes no workspace: the partial
  * sums go to a static device array of QMV_STATIC_SCRATCH_BYTES that the
- * library holds on every GPU that loads it, until the process exits.
+ * library holds on every GPU that loads it, until the process exits.  With a
+ * split above one and 4 or more tokens, the activations quantized once
+ * (qmv_act_q8_bytes(K, n_tok)) are placed in the array too, after the
+ * partial sums, when both fit (as qmv_splitk_run does with a large enough
+ * workspace).
  *   - Rejects split shapes whose partial sums exceed that size with
  *     QMV_ERR_WORKSPACE (qmv_splitk_workspace_bytes(M, n_tok, n_split) must
  *     be <= QMV_STATIC_SCRATCH_BYTES; n_split = 0 picks the split as
@@ -300,8 +307,9 @@ int qmv_run_siblings(int count, const int* fmts, const void* const* W, const int
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.
  *   - Every call shares the array: calls that can overlap on the GPU (other
- *     streams, concurrently launched graphs) race.  Nothing needs clearing:
- *     each call overwrites every partial sum it reads.
+ *     streams, concurrently launched graphs) race, on the partial sums and
+ *     the quantized activations alike.  Nothing needs clearing: each call
+ *     overwrites every value it reads.
  *   - Allocates nothing (no cudaMalloc / cudaFree, no allocating library).
  * Results are bitwise equal to qmv_splitk_run with the same n_split. */
 #define QMV_STATIC_SCRATCH_BYTES (8u << 20)
@@ -381,6 +389,18 @@ int moe_route_run(int fmt, const void* Wr, const float* x, int n_experts, int64_
  * mismatches[0] (division) and mismatches[1] (reciprocal), device memory,
  * 16-byte aligned.  Both must stay 0. */
 int qmv_check_rounding(unsigned long long* mismatches, cudaStream_t stream);
+
+/* Diagnostic (no counterpart on the pages): sets the cycle limit of the
+ * consumer warps' waits for weight stages in the matvec and MoE kernels
+ * launched after this returns (process-wide; cycles <= 0 restores the
+ * default of about 2^31 cycles, about a second).  With a short limit a call
+ * whose weight stages arrive late gives up: the kernel returns, sets
+ * QMV_DEVERR_TIMEOUT and leaves its outputs unspecified; the context stays
+ * usable and the next call (with the default limit) is correct.  Only the
+ * consumers' waits are shortened: the producer's waits and the waits for
+ * bulk copies of activations keep the default, so no copy lands in shared
+ * memory after a CTA has exited.  Exists to test that timeout path. */
+int qmv_set_consumer_wait_limit(long long cycles);
 
 /* Synchronises `stream`, then reads and clears the device error word
  * (QMV_DEVERR_* bits, 0 if none) into *err. */

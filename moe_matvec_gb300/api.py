@@ -61,6 +61,7 @@ _SIGS = {
     "qmv_run_residual": (_int, [_int, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _vp, _sz, _vp]),
     "qmv_run_siblings": (_int, [_int, _vp, _vp, _vp, _vp, _vp, _i64, _int, _vp, _sz, _vp]),
     "qmv_get_device_error": (_int, [_vp, ctypes.POINTER(_int)]),
+    "qmv_set_consumer_wait_limit": (_int, [ctypes.c_longlong]),
     "qmv_check_rounding": (_int, [_vp, _vp]),
     "qmv_strerror": (ctypes.c_char_p, [_int]),
 }
@@ -304,6 +305,12 @@ def check_rounding(stream=None):
     bad = torch.zeros(2, dtype=torch.int64, device="cuda")
     _check(load().qmv_check_rounding(_ptr(bad), _stream(stream)), "qmv_check_rounding")
     return [int(v) for v in bad.cpu()]
+
+
+def set_consumer_wait_limit(cycles: int) -> None:
+    """Cycle limit of the kernels' consumer waits for weight stages (0: the
+    default, about a second); a diagnostic for the timeout path."""
+    _check(load().qmv_set_consumer_wait_limit(int(cycles)), "qmv_set_consumer_wait_limit")
 
 
 def get_device_error(stream=None) -> int:

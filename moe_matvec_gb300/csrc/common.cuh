@@ -138,6 +138,41 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
   return true;
 }
 
+// Non-blocking test of a phase (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// A consumer warp's wait for a weight stage, with the caller's cycle limit
+// (a launch parameter, WAIT_CYCLES unless a test shortened it).  Below the
+// default the barrier is polled without suspending, so a short limit runs
+// out as soon as the stage is late.  Called by all lanes of the warp; the
+// verdict is the same in every lane (a stage counts as landed only if every
+// lane saw it), so the warp never splits between the barriers that follow.
+__device__ __forceinline__ bool consumer_wait(uint64_t* bar, uint32_t parity, unsigned* err, long long limit) {
+  bool ok;
+  if (limit >= WAIT_CYCLES) {
+    ok = mbar_wait(bar, parity, err);
+  } else {
+    ok = mbar_test_wait(bar, parity);
+    if (!ok) {
+      const long long t0 = clock64();
+      while (!(ok = mbar_test_wait(bar, parity)))
+        if (clock64() - t0 > limit) {
+          set_error(err, QMV_DEVERR_TIMEOUT);
+          break;
+        }
+    }
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+
 // L2 policy for streamed weights: evict first, so activations and outputs
 // stay resident.
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -239,31 +274,6 @@ __device__ __forceinline__ float ldg_stream(const float* p) {
   float v;
   asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
   return v;
-}
-
-// ---------------------------------------------------------------------------
-// Activation quantization of one 32-element block held one element per lane
-// (every lane of the warp participates).  Rule: amax = max |x|;
-// d = amax / 127; id = 1 / d (0 if d == 0); q = rne(x * id) in [-127, 127];
-// s = sum q.  The divisions are IEEE (no fast-math), the product is an
-// explicit round-to-nearest multiply, so the codes are bit-identical to any
-// IEEE fp32 implementation of the rule.
-// ---------------------------------------------------------------------------
-struct ActQ {
-  int q;
-  float d;
-  int s;
-};
-__device__ __forceinline__ ActQ act_quant_lane(float x) {
-  unsigned ab = __float_as_uint(fabsf(x));
-  unsigned mb = __reduce_max_sync(0xffffffffu, ab);
-  float amax = __uint_as_float(mb);
-  float d = __fdiv_rn(amax, 127.0f);
-  float id = d > 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
-  int q = __float2int_rn(__fmul_rn(x, id));
-  q = max(-127, min(127, q));
-  int s = __reduce_add_sync(0xffffffffu, q);
-  return {q, d, s};
 }
 
 }  // namespace qmv

@@ -161,7 +161,10 @@ __device__ __forceinline__ void quant_units(const float4 (&v)[SU][2], uint32_t (
 #pragma unroll
     for (int k = 0; k < 8; k++) {
       float p = __fmul_rn(f[k], id[u]);
-      if (slow) p = fminf(fmaxf(p, -127.0f), 127.0f);
+      // slow path: clamp (1 / d overflows to infinity for blocks whose amax
+      // is below about 3.7e-37; a zero element then gives 0 * inf, not a
+      // number, whose code is 0)
+      if (slow) p = p != p ? 0.0f : fminf(fmaxf(p, -127.0f), 127.0f);
       q[k] = __float2int_rn(p);
     }
     w0[u] = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) | ((uint32_t)(q[2] & 0xFF) << 16) |

@@ -47,6 +47,7 @@ struct DenseParams {
   int act_nck;         // chunks of the activation area
   int prefetch;        // L2 lookahead of the producer past the ring (iterations; 0: none)
   unsigned* err;       // device error word
+  long long wait;      // cycle limit of the consumers' waits for weight stages
 };
 
 // Per-CTA walk over its tiles: a contiguous range of the flattened
@@ -270,7 +271,7 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, is_float(F) ? 1 : dense_mi
         asm volatile("prefetch.global.L1 [%0];" ::"l"(p.add + (long long)(t0 + lane) * p.M + row0 + grp * RW));
     for (int c = 0; c < nck && alive; c++, ring.advance(p.stages)) {
       const int st = ring.st;
-      if (!mbar_wait(&full[st], ring.parity(), p.err)) {
+      if (!consumer_wait(&full[st], ring.parity(), p.err, p.wait)) {
         alive = false;
         break;
       }
@@ -280,8 +281,9 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, is_float(F) ? 1 : dense_mi
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
-    alive = __all_sync(FULL, alive);
-    if (!alive) continue;
+    // a warp that gave up on a wait (alive is warp-uniform) stores nothing;
+    // with ks > 1 it still takes part in the cross-warp barriers below
+    if (!alive && ks == 1) continue;
     // reduce across lanes and store rows row0 + grp * RW + r
     float* out = p.out + (long long)s * p.ntot * p.M;
     constexpr int V = RW * NT, HELD = V >= 32 ? V / 32 : 1;
@@ -321,6 +323,7 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, is_float(F) ? 1 : dense_mi
           v[i] = w;
         }
       named_sync(2, CONSUMER_THREADS);  // red is free for the next tile
+      if (!alive) continue;
     }
     if (part == 0 && lead) {
 #pragma unroll

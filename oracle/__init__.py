@@ -84,7 +84,7 @@ def _load():
         lib.oracle_moe.restype = ctypes.c_int
         lib.oracle_moe.argtypes = ([ctypes.c_int, _ptr, ctypes.c_int, _ptr] + [ctypes.c_int] * 3
                                    + [_ptr, _ptr, _ptr, ctypes.c_int, ctypes.c_int, _ptr]
-                                   + [_ptr] * 11)
+                                   + [_ptr] * 12 + [ctypes.c_int])
         lib.oracle_route_select.restype = ctypes.c_int
         lib.oracle_route_select.argtypes = [_ptr] + [ctypes.c_int] * 4 + [_ptr, _ptr]
         _lib = lib
@@ -175,10 +175,14 @@ def moe_slot_valid(ids: np.ndarray, E: int, t: int, k: int) -> bool:
 
 
 def moe(fmt_gu: int, Wgu: np.ndarray, fmt_d: int, Wd: np.ndarray, E: int, H: int, F: int,
-        ids: np.ndarray, gates: np.ndarray, x: np.ndarray, h_in: np.ndarray | None = None):
+        ids: np.ndarray, gates: np.ndarray, x: np.ndarray, h_in: np.ndarray | None = None,
+        nthreads: int = 1):
     """MoE decode layer (see oracle.c).  Wgu uint8 [E][2F][rb], Wd uint8
     [E][H][rb]; ids int32 [n][top_k]; gates fp32 [n][top_k]; x fp32 [n][H].
-    Returns a dict of y, ybound, g, u, gabs, uabs, h32, hq, hd, hs, o."""
+    Returns a dict of y, ybound, g, u, gabs, uabs, h32, hq, hd, hs, o, oabs
+    (oabs[p][m] = sum_i |Wdown_e[m][i] Hhat_p[i]|, the tolerance scale of o).
+    The per-slot projections run on nthreads threads (0: all host cores); the
+    result does not depend on the thread count."""
     Wgu = np.ascontiguousarray(Wgu, dtype=np.uint8)
     Wd = np.ascontiguousarray(Wd, dtype=np.uint8)
     ids = np.ascontiguousarray(ids, dtype=np.int32)
@@ -186,18 +190,21 @@ def moe(fmt_gu: int, Wgu: np.ndarray, fmt_d: int, Wd: np.ndarray, E: int, H: int
     x = np.ascontiguousarray(x, dtype=np.float32)
     n, top_k = ids.shape
     S = n * top_k
+    if nthreads <= 0:
+        nthreads = os.cpu_count() or 1
     out = dict(
         y=np.empty((n, H)), ybound=np.empty((n, H)), g=np.empty((S, F)), u=np.empty((S, F)),
         gabs=np.empty((S, F)), uabs=np.empty((S, F)), h32=np.empty((S, F), np.float32),
         hq=np.empty((S, F), np.int8), hd=np.empty((S, F // 32), np.float32),
-        hs=np.empty((S, F // 32), np.int32), o=np.empty((S, H)))
+        hs=np.empty((S, F // 32), np.int32), o=np.empty((S, H)), oabs=np.empty((S, H)))
     if h_in is not None:
         h_in = np.ascontiguousarray(h_in, dtype=np.float32).reshape(S, F)
     rc = _load().oracle_moe(int(fmt_gu), _p(Wgu), int(fmt_d), _p(Wd), int(E), int(H), int(F),
                             _p(ids), _p(gates), _p(x), n, top_k, _p(h_in),
                             _p(out["y"]), _p(out["ybound"]), _p(out["g"]), _p(out["u"]),
                             _p(out["gabs"]), _p(out["uabs"]), _p(out["h32"]), _p(out["hq"]),
-                            _p(out["hd"]), _p(out["hs"]), _p(out["o"]))
+                            _p(out["hd"]), _p(out["hs"]), _p(out["o"]), _p(out["oabs"]),
+                            int(nthreads))
     assert rc == 0
     return out
 

@@ -197,6 +197,10 @@ void oracle_act_quant(const float* x, int64_t K, int64_t n, int8_t* q, float* d,
         float r = rintf(p); /* default rounding mode: half to even */
         if (r > 127.0f) r = 127.0f;
         if (r < -127.0f) r = -127.0f;
+        /* a block whose largest magnitude is below about 3.7e-37 has a
+         * subnormal d whose reciprocal overflows to infinity; its zero
+         * elements then give 0 * inf, not a number: their code is 0 */
+        if (p != p) r = 0.0f;
         q[t * K + j * 32 + i] = (int8_t)r;
         sum += (int32_t)r;
       }
@@ -688,6 +692,119 @@ int oracle_moe_slot_valid(const int32_t* ids, int top_k, int E, int t, int k) {
   return 1;
 }
 
+/* Work of one thread over slots [p0, p1) of one of the two per-slot phases
+ * of the MoE layer (the slots are independent: each reads only the inputs and
+ * writes only its own rows). */
+typedef struct {
+  int fmt_gu, fmt_d;
+  const uint8_t *Wgu, *Wd;
+  int64_t rb_gu, rb_d;
+  int E, H, F, top_k;
+  const int32_t* ids;
+  const double* xhat;  /* [n][H] */
+  const float* h_in;   /* [S][F] or NULL */
+  double *g, *u, *gabs, *uabs;  /* phase 1 outputs (may be NULL) */
+  float* hloc;                  /* phase 1: fp32 h [S][F] */
+  const int8_t* hq;             /* phase 2 inputs: quantized h */
+  const float* hd;
+  double *oloc, *oaloc;         /* phase 2 outputs [S][H] */
+  int p0, p1;
+} moe_job;
+
+/* gate / up / SwiGLU of slots [p0, p1) */
+static void* moe_gate_up_worker(void* arg) {
+  moe_job* j = (moe_job*)arg;
+  const int H = j->H, F = j->F;
+  double* wrow = (double*)malloc(sizeof(double) * (size_t)H);
+  if (!wrow) return NULL;
+  for (int p = j->p0; p < j->p1; p++) {
+    int t = p / j->top_k, k = p % j->top_k;
+    int valid = oracle_moe_slot_valid(j->ids, j->top_k, j->E, t, k);
+    int32_t e = j->ids[p];
+    for (int r = 0; r < F; r++) {
+      double gv = 0.0, uv = 0.0, ga = 0.0, ua = 0.0;
+      if (valid) {
+        const uint8_t* base = j->Wgu + (int64_t)e * 2 * F * j->rb_gu;
+        dequant_row(j->fmt_gu, base + (int64_t)r * j->rb_gu, H, wrow);
+        for (int i = 0; i < H; i++) {
+          double pr = wrow[i] * j->xhat[(int64_t)t * H + i];
+          gv += pr;
+          ga += fabs(pr);
+        }
+        dequant_row(j->fmt_gu, base + (int64_t)(F + r) * j->rb_gu, H, wrow);
+        for (int i = 0; i < H; i++) {
+          double pr = wrow[i] * j->xhat[(int64_t)t * H + i];
+          uv += pr;
+          ua += fabs(pr);
+        }
+      }
+      if (j->g) j->g[(int64_t)p * F + r] = gv;
+      if (j->u) j->u[(int64_t)p * F + r] = uv;
+      if (j->gabs) j->gabs[(int64_t)p * F + r] = ga;
+      if (j->uabs) j->uabs[(int64_t)p * F + r] = ua;
+      double hv = valid ? gv / (1.0 + exp(-gv)) * uv : 0.0;
+      j->hloc[(int64_t)p * F + r] = j->h_in ? (valid ? j->h_in[(int64_t)p * F + r] : 0.0f) : (float)hv;
+    }
+  }
+  free(wrow);
+  return NULL;
+}
+
+/* down projection o = Wdown_e Hhat of slots [p0, p1) */
+static void* moe_down_worker(void* arg) {
+  moe_job* j = (moe_job*)arg;
+  const int H = j->H, F = j->F;
+  double* wrow = (double*)malloc(sizeof(double) * (size_t)F);
+  double* hhat = (double*)malloc(sizeof(double) * (size_t)F);
+  if (!wrow || !hhat) {
+    free(wrow);
+    free(hhat);
+    return NULL;
+  }
+  for (int p = j->p0; p < j->p1; p++) {
+    int t = p / j->top_k, k = p % j->top_k;
+    int valid = oracle_moe_slot_valid(j->ids, j->top_k, j->E, t, k);
+    int32_t e = j->ids[p];
+    for (int i = 0; i < F; i++)
+      hhat[i] = (double)j->hd[(int64_t)p * (F / 32) + i / 32] * (double)j->hq[(int64_t)p * F + i];
+    for (int m = 0; m < H; m++) {
+      double ov = 0.0, oa = 0.0;
+      if (valid) {
+        dequant_row(j->fmt_d, j->Wd + ((int64_t)e * H + m) * j->rb_d, F, wrow);
+        for (int i = 0; i < F; i++) {
+          double pr = wrow[i] * hhat[i];
+          ov += pr;
+          oa += fabs(pr);
+        }
+      }
+      j->oloc[(int64_t)p * H + m] = ov;
+      j->oaloc[(int64_t)p * H + m] = oa;
+    }
+  }
+  free(wrow);
+  free(hhat);
+  return NULL;
+}
+
+/* Runs fn over the slots [0, S) split into nthreads contiguous ranges. */
+static void moe_parallel(void* (*fn)(void*), moe_job proto, int S, int nthreads) {
+  moe_job jobs[256];
+  pthread_t th[256];
+  if (nthreads > S) nthreads = S;
+  if (nthreads < 1) nthreads = 1;
+  for (int i = 0; i < nthreads; i++) {
+    jobs[i] = proto;
+    jobs[i].p0 = (int)((int64_t)S * i / nthreads);
+    jobs[i].p1 = (int)((int64_t)S * (i + 1) / nthreads);
+  }
+  if (nthreads == 1) {
+    fn(&jobs[0]);
+    return;
+  }
+  for (int i = 0; i < nthreads; i++) pthread_create(&th[i], NULL, fn, &jobs[i]);
+  for (int i = 0; i < nthreads; i++) pthread_join(th[i], NULL);
+}
+
 /* Full MoE layer.  Optional outputs may be NULL.  If h_in is non-NULL it
  * supplies the fp32 h of every slot (for grading the down/combine stage on
  * given h); otherwise h is computed from x.
@@ -697,104 +814,95 @@ int oracle_moe_slot_valid(const int32_t* ids, int top_k, int E, int t, int k) {
  *   gabs, uabs [n*top_k][F]  sum_i |What x Xhat| of those rows
  *   h32    [n*top_k][F]  fp32 h (as computed here, or h_in)
  *   hq, hd, hs           activation quantization of h32
- *   o      [n*top_k][H]  down projections (fp64) */
+ *   o      [n*top_k][H]  down projections (fp64)
+ *   oabs   [n*top_k][H]  sum_i |Wdown_e[m][i] Hhat_i| of those rows
+ * The slots' gate/up and down projections are computed by nthreads POSIX
+ * threads (1 = serial); the combine then adds the slots of each token in k
+ * order, so the result does not depend on the thread count. */
 int oracle_moe(int fmt_gu, const uint8_t* Wgu, int fmt_d, const uint8_t* Wd, int E,
                int H, int F, const int32_t* ids, const float* gates, const float* x,
                int n, int top_k, const float* h_in, double* y, double* ybound,
                double* g, double* u, double* gabs, double* uabs, float* h32,
-               int8_t* hq, float* hd, int32_t* hs, double* o) {
+               int8_t* hq, float* hd, int32_t* hs, double* o, double* oabs, int nthreads) {
   int64_t rb_gu = oracle_row_bytes(fmt_gu, H), rb_d = oracle_row_bytes(fmt_d, F);
   if (rb_gu < 0 || rb_d < 0 || E <= 0 || n <= 0 || top_k <= 0) return -1;
+  if (nthreads > 256) nthreads = 256;
   int S = n * top_k;
   int8_t* xq = (int8_t*)malloc((size_t)n * H);
   float* xd = (float*)malloc(sizeof(float) * (size_t)n * (H / 32));
   int32_t* xs = (int32_t*)malloc(sizeof(int32_t) * (size_t)n * (H / 32));
   double* xhat = (double*)malloc(sizeof(double) * (size_t)n * H);
-  double* wrow = (double*)malloc(sizeof(double) * (size_t)(H > F ? H : F));
   float* hloc = (float*)malloc(sizeof(float) * (size_t)S * F);
   int8_t* hql = (int8_t*)malloc((size_t)S * F);
   float* hdl = (float*)malloc(sizeof(float) * (size_t)S * (F / 32));
   int32_t* hsl = (int32_t*)malloc(sizeof(int32_t) * (size_t)S * (F / 32));
-  double* hhat = (double*)malloc(sizeof(double) * (size_t)F);
-  if (!xq || !xd || !xs || !xhat || !wrow || !hloc || !hql || !hdl || !hsl || !hhat) return -2;
+  double* oloc = (double*)malloc(sizeof(double) * (size_t)S * H);
+  double* oaloc = (double*)malloc(sizeof(double) * (size_t)S * H);
+  if (!xq || !xd || !xs || !xhat || !hloc || !hql || !hdl || !hsl || !oloc || !oaloc) return -2;
   oracle_act_quant(x, H, n, xq, xd, xs);
   for (int64_t i = 0; i < (int64_t)n * H; i++)
     xhat[i] = (double)xd[i / 32] * (double)xq[i];
 
-  /* gate / up / SwiGLU per slot */
-  for (int p = 0; p < S; p++) {
-    int t = p / top_k, k = p % top_k;
-    int valid = oracle_moe_slot_valid(ids, top_k, E, t, k);
-    int32_t e = ids[p];
-    for (int j = 0; j < F; j++) {
-      double gv = 0.0, uv = 0.0, ga = 0.0, ua = 0.0;
-      if (valid) {
-        const uint8_t* base = Wgu + (int64_t)e * 2 * F * rb_gu;
-        dequant_row(fmt_gu, base + (int64_t)j * rb_gu, H, wrow);
-        for (int i = 0; i < H; i++) {
-          double pr = wrow[i] * xhat[(int64_t)t * H + i];
-          gv += pr;
-          ga += fabs(pr);
-        }
-        dequant_row(fmt_gu, base + (int64_t)(F + j) * rb_gu, H, wrow);
-        for (int i = 0; i < H; i++) {
-          double pr = wrow[i] * xhat[(int64_t)t * H + i];
-          uv += pr;
-          ua += fabs(pr);
-        }
-      }
-      if (g) g[(int64_t)p * F + j] = gv;
-      if (u) u[(int64_t)p * F + j] = uv;
-      if (gabs) gabs[(int64_t)p * F + j] = ga;
-      if (uabs) uabs[(int64_t)p * F + j] = ua;
-      double hv = valid ? gv / (1.0 + exp(-gv)) * uv : 0.0;
-      hloc[(int64_t)p * F + j] = h_in ? (valid ? h_in[(int64_t)p * F + j] : 0.0f) : (float)hv;
-    }
-  }
+  moe_job proto;
+  memset(&proto, 0, sizeof(proto));
+  proto.fmt_gu = fmt_gu;
+  proto.fmt_d = fmt_d;
+  proto.Wgu = Wgu;
+  proto.Wd = Wd;
+  proto.rb_gu = rb_gu;
+  proto.rb_d = rb_d;
+  proto.E = E;
+  proto.H = H;
+  proto.F = F;
+  proto.top_k = top_k;
+  proto.ids = ids;
+  proto.xhat = xhat;
+  proto.h_in = h_in;
+  proto.g = g;
+  proto.u = u;
+  proto.gabs = gabs;
+  proto.uabs = uabs;
+  proto.hloc = hloc;
+  proto.hq = hql;
+  proto.hd = hdl;
+  proto.oloc = oloc;
+  proto.oaloc = oaloc;
+
+  /* gate / up / SwiGLU per slot, then the requantization of h */
+  moe_parallel(moe_gate_up_worker, proto, S, nthreads);
   oracle_act_quant(hloc, F, S, hql, hdl, hsl);
   if (h32) memcpy(h32, hloc, sizeof(float) * (size_t)S * F);
   if (hq) memcpy(hq, hql, (size_t)S * F);
   if (hd) memcpy(hd, hdl, sizeof(float) * (size_t)S * (F / 32));
   if (hs) memcpy(hs, hsl, sizeof(int32_t) * (size_t)S * (F / 32));
 
-  /* down projection and combine */
+  /* down projection per slot, then the combine in slot (= k) order */
+  moe_parallel(moe_down_worker, proto, S, nthreads);
   for (int64_t i = 0; i < (int64_t)n * H; i++) {
     if (y) y[i] = 0.0;
     if (ybound) ybound[i] = 0.0;
   }
   for (int p = 0; p < S; p++) {
-    int t = p / top_k, k = p % top_k;
-    int valid = oracle_moe_slot_valid(ids, top_k, E, t, k);
-    int32_t e = ids[p];
-    for (int i = 0; i < F; i++)
-      hhat[i] = (double)hdl[(int64_t)p * (F / 32) + i / 32] * (double)hql[(int64_t)p * F + i];
+    int t = p / top_k;
     double gt = (double)gates[p];
     for (int m = 0; m < H; m++) {
-      double ov = 0.0, oa = 0.0;
-      if (valid) {
-        const uint8_t* row = Wd + ((int64_t)e * H + m) * rb_d;
-        dequant_row(fmt_d, row, F, wrow);
-        for (int i = 0; i < F; i++) {
-          double pr = wrow[i] * hhat[i];
-          ov += pr;
-          oa += fabs(pr);
-        }
-      }
-      if (o) o[(int64_t)p * H + m] = ov;
+      double ov = oloc[(int64_t)p * H + m], oa = oaloc[(int64_t)p * H + m];
       if (y) y[(int64_t)t * H + m] += gt * ov;
       if (ybound) ybound[(int64_t)t * H + m] += fabs(gt) * oa;
     }
   }
+  if (o) memcpy(o, oloc, sizeof(double) * (size_t)S * H);
+  if (oabs) memcpy(oabs, oaloc, sizeof(double) * (size_t)S * H);
   free(xq);
   free(xd);
   free(xs);
   free(xhat);
-  free(wrow);
   free(hloc);
   free(hql);
   free(hdl);
   free(hsl);
-  free(hhat);
+  free(oloc);
+  free(oaloc);
   return 0;
 }
 

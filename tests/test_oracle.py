@@ -110,6 +110,70 @@ def test_act_quant_invariants(scale):
     assert np.all(err <= d[..., None] * (0.5 + 1e-5))   # nearest grid point
 
 
+def _act_quant_numpy(x):
+    """The activation rule restated with numpy fp32 element-wise operations,
+    one line per step of the rule (amax; d = amax / 127; id = 1 / d or 0;
+    q = clamp(rne(x * id)); s = sum q), independently of the oracle's C."""
+    xb = np.ascontiguousarray(x, np.float32).reshape(-1, 32)
+    amax = np.abs(xb).max(axis=1)
+    d = amax / np.float32(127.0)
+    pos = d > 0
+    with np.errstate(divide="ignore", over="ignore"):
+        inv = np.where(pos, np.float32(1.0) / np.where(pos, d, np.float32(1.0)), np.float32(0.0))
+    inv = inv.astype(np.float32)
+    with np.errstate(invalid="ignore", over="ignore"):
+        p = xb * inv[:, None]                     # fp32 products, round to nearest
+        r = np.clip(np.rint(p), -127.0, 127.0)    # round half to even, clamp
+    r = np.where(np.isnan(p), 0.0, r)             # 0 * inf (1 / d overflowed): code 0
+    q = r.astype(np.int8)
+    return q, d, q.astype(np.int32).sum(axis=1)
+
+
+def _near_tie_blocks(nb, seed):
+    """Blocks whose products x * id fall on or within two ulps of k + 1/2:
+    the largest element a fixes d = a / 127 and id = 1 / d, every other
+    element is (k + 1/2) / id (k a random integer) moved by -2..2 ulps."""
+    r = np.random.default_rng(seed)
+    a = (r.uniform(0.5, 2.0, nb) * 2.0 ** r.integers(-100, 100, nb)).astype(np.float32)
+    d = a / np.float32(127.0)
+    inv = (np.float32(1.0) / d).astype(np.float32)
+    k = r.integers(-127, 127, (nb, 32)).astype(np.float64)
+    x = ((k + 0.5) / inv[:, None].astype(np.float64)).astype(np.float32)
+    x = (x.view(np.int32) + r.integers(-2, 3, (nb, 32)).astype(np.int32)).view(np.float32)
+    x = np.clip(x, -a[:, None], a[:, None])
+    x[np.arange(nb), r.integers(0, 32, nb)] = a * np.where(r.random(nb) < 0.5, 1, -1).astype(np.float32)
+    return x
+
+
+def test_act_quant_matches_a_naive_numpy_restatement_on_a_million_blocks():
+    # random blocks over a wide range of scales, blocks crowded with near and
+    # exact .5 ties, tiny blocks (subnormal d, 1/d overflowing) with zeros,
+    # zero blocks: the oracle's codes, scales and sums must be those of the
+    # rule written out with numpy's IEEE fp32 operations, bit for bit
+    r = np.random.default_rng(12345)
+    nb_rand, nb_tie = 600_000, 400_000
+    xr = r.standard_normal((nb_rand, 32)).astype(np.float32)
+    xr *= (2.0 ** r.integers(-120, 120, nb_rand)).astype(np.float32)[:, None]
+    xr[:1000] = 0.0
+    tiny = r.standard_normal((2000, 32)).astype(np.float32) * np.float32(1e-38)
+    tiny[:, 5] = 0.0
+    xr[1000:3000] = tiny
+    xt = _near_tie_blocks(nb_tie, 54321)
+    x = np.concatenate([xr, xt]).reshape(-1, 1024)    # 1e6 blocks as rows of 32 blocks
+    q, d, s = oracle.act_quant(x)
+    nq, nd, ns = _act_quant_numpy(x)
+    assert np.array_equal(q.reshape(-1, 32), nq)
+    assert np.array_equal(d.reshape(-1).view(np.uint32), nd.view(np.uint32))
+    assert np.array_equal(s.reshape(-1), ns)
+    # the tie-heavy blocks really do hit exact halves (where the rounding
+    # direction decides the code) and land on both sides of them
+    _, dt, _ = _act_quant_numpy(xt)
+    inv = (np.float32(1.0) / dt).astype(np.float32)
+    pt = (xt * inv[:, None]).astype(np.float64)
+    assert (np.abs(pt - np.floor(pt)) == 0.5).sum() > 10_000
+    assert (np.abs(np.abs(pt - np.floor(pt)) - 0.5) < 1e-6 * np.abs(pt)).sum() > 100_000
+
+
 # --------------------------------------------------------------------------
 # weight quantizers
 # --------------------------------------------------------------------------
@@ -637,6 +701,29 @@ def test_moe_invalid_slots_contribute_zero():
     ref = oracle.moe(2, Wgu, 1, Wd, E, H, F, ok_ids, ok_g, x)
     assert np.array_equal(bad["y"], ref["y"])
     assert not oracle.moe_slot_valid(ids, E, 0, 1) and not oracle.moe_slot_valid(ids, E, 1, 1)
+
+
+def test_moe_thread_count_does_not_change_any_output():
+    Wgu, Wd = _moe_pool()
+    x = synth.activations(15, 5, H)
+    ids, gates = synth.routing(16, 5, E, TOPK)
+    a = oracle.moe(2, Wgu, 1, Wd, E, H, F, ids, gates, x, nthreads=1)
+    for nt in (3, 0):
+        b = oracle.moe(2, Wgu, 1, Wd, E, H, F, ids, gates, x, nthreads=nt)
+        for k in a:
+            assert np.array_equal(a[k], b[k]), k
+
+
+def test_moe_slot_outputs_are_the_down_matvec_of_the_quantized_h():
+    # o and its tolerance scale oabs, slot by slot, are the plain matvec of the
+    # down weights with the slot's fp32 h (quantized by the activation rule)
+    Wgu, Wd = _moe_pool()
+    x = synth.activations(17, 3, H)
+    ids, gates = synth.routing(18, 3, E, TOPK)
+    out = oracle.moe(2, Wgu, 1, Wd, E, H, F, ids, gates, x, nthreads=2)
+    for p, e in enumerate(ids.reshape(-1)):
+        yo, so = oracle.qmv(1, Wd[e], out["h32"][p][None, :], F)
+        assert np.array_equal(out["o"][p], yo[0]) and np.array_equal(out["oabs"][p], so[0])
 
 
 def test_moe_given_h_reproduces_the_computed_path():

@@ -29,6 +29,9 @@ def _tricky_activations(n, K, seed):
     x[0, 64] = 127 * 3.0
     x[min(1, n - 1), 96:128] *= 1e-30                    # tiny but normal
     x[n - 1, -32:] = np.float32(1e30)                    # huge, all equal
+    if K >= 512:
+        x[n - 1, 224:256] *= np.float32(1e-38)           # 1 / d overflows to infinity ...
+        x[n - 1, 230] = 0.0                              # ... and 0 * inf gives code 0
     return x
 
 
@@ -195,6 +198,31 @@ def test_qmv_full_size_sampled(lib, name, fmt, M, K, n, seed, wseed):
     yr, sabs = oracle.qmv(fmt, Wn[rows], x, K)
     assert_within(y[:, rows], yr, sabs, what=f"{name} n{n}")
     assert np.all(np.isfinite(y))
+
+
+BENCH_CASE = next(c for c in synth.DENSE_CASES if c.workload == "q4_k")
+
+
+@pytest.mark.parametrize("n_idx,n", list(enumerate(BENCH_CASE.n_toks)))
+def test_bench_call_full_size(lib, n_idx, n):
+    # the exact call the benchmark times for Q4_K 17408 x 5120: qmv_splitk_run
+    # with the split chosen from the shape and a workspace with room for the
+    # once-quantized activations (from 4 tokens: the standalone quantizer,
+    # then the matvec kernel with pre-quantized input), checked element by
+    # element on the first and last 512 rows (every tile and 8-row unit of
+    # the first and last CTAs' ranges) and 256 random rows
+    c = BENCH_CASE
+    Wn = _full_weights(c.fmt, c.M, c.K, synth.seed_for(c.index, c.shape_index, 0))
+    x = synth.activations(synth.seed_for(c.index, c.shape_index, n_idx), n, c.K)
+    S = lib.splitk_choose(c.fmt, c.M, c.K, n)
+    ws = torch.empty(max(16, lib.splitk_workspace_fast_bytes(c.M, c.K, n, S)), dtype=torch.uint8, device="cuda")
+    y = lib.splitk_run(c.fmt, dev(Wn), dev(x), c.M, c.K, n_split=S, ws=ws).cpu().numpy()
+    r = np.random.default_rng(n)
+    rows = np.unique(np.concatenate([np.arange(512), np.arange(c.M - 512, c.M), r.integers(0, c.M, 256)]))
+    yr, sabs = oracle.qmv(c.fmt, Wn[rows], x, c.K, nthreads=8)
+    assert_within(y[:, rows], yr, sabs, what=f"bench call n{n} S{S}")
+    assert np.all(np.isfinite(y))
+    assert lib.get_device_error() == 0
 
 
 # --------------------------------------------------------------------------

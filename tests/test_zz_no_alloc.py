@@ -2,10 +2,12 @@
 
 It serves callers that may not call cudaMalloc themselves (for instance a
 plugin that runs while its host framework captures a CUDA graph, or a host
-that owns all of the device memory): the partial sums go to a static device
-array inside the library instead of a caller workspace.  Two calls in a row
-share that array; each must match qmv_splitk_run with a caller-allocated
-workspace, within the tolerance of the other parity tests."""
+that owns all of the device memory): the partial sums (and, from 4 tokens,
+the once-quantized activations) go to a static device array inside the
+library instead of a caller workspace.  Two calls in a row share that array;
+each must give the same bits as qmv_splitk_run with a caller-allocated
+workspace and the same split, and lie within the parity tolerance of the
+oracle."""
 import ctypes
 
 import numpy as np
@@ -21,6 +23,8 @@ pytestmark = pytest.mark.gpu
 
 def test_static_scratch_matches_workspace_entry_point_on_two_calls(lib):
     cases = [(0, 512, 65536, 4, 16), (1, 300, 8192, 7, 0)]   # fmt, M, K, n_tok, n_split (0 = auto)
+    # the automatic split of the second call is above one, so both calls use the array
+    assert lib.splitk_choose(1, 300, 8192, 7) > 1
     for call, (fmt, M, K, n, S) in enumerate(cases):
         w = synth.weights(900 + call, M, K)
         x = synth.activations(901 + call, n, K)
@@ -29,8 +33,10 @@ def test_static_scratch_matches_workspace_entry_point_on_two_calls(lib):
         y_static = lib.splitk_run_static(fmt, Wd, xd, M, K, n_split=S)
         y_ws = lib.splitk_run(fmt, Wd, xd, M, K, n_split=S)
         torch.cuda.synchronize()
-        _, sabs = oracle.qmv(fmt, Wn, x, K)
-        assert_within(y_static.cpu().numpy(), y_ws.cpu().numpy(), sabs, what=f"call {call}: static vs workspace")
+        a, b = y_static.cpu().numpy(), y_ws.cpu().numpy()
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32)), f"call {call}: static vs workspace bits"
+        yr, sabs = oracle.qmv(fmt, Wn, x, K)
+        assert_within(a, yr, sabs, what=f"call {call}: static vs oracle")
     assert lib.get_device_error() == 0
 
 
