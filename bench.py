@@ -570,6 +570,29 @@ def run_extra(torch, api, synth, stream, dev, peak):
         res[str(n)] = r
     out["moe_128x_top8_h4096_f1536"] = {"format": "gate/up IQ4_XS, down Q4_K", "bytes_per_expert": per_expert,
                                         "routing_draws": 16, "n_tok": res}
+
+    # the same layer for prompt-sized batches on the tensor cores
+    # (moe_qmv_prefill_run): tokens / s, effective weight GB/s of the touched
+    # experts and tensor-core TFLOP/s (2 x multiply-adds of the contraction)
+    res = {}
+    macs_per_slot = 2 * F * H + H * F
+    for n in (512, 2048):
+        sets = [synth.routing(2350 + 17 * n + k, n, E, c.top_k) for k in range(2)]
+        ids = [torch.from_numpy(a).to(dev) for a, _ in sets]
+        gates = [torch.from_numpy(b).to(dev) for _, b in sets]
+        x = torch.from_numpy(synth.activations(2450 + n, n, H)).to(dev)
+        y = torch.empty((n, H), device=dev)
+        ws = torch.empty(api.moe_prefill_workspace_bytes(ex, n, c.top_k), dtype=torch.uint8, device=dev)
+        calls = [(lambda k=k: api.moe_prefill_run(ex, ids[k], gates[k], x, ws=ws, out=y, stream=stream))
+                 for k in range(len(sets))]
+        us = _graph_us(torch, stream, calls, reps=5)
+        distinct = sum(len(np.unique(a)) for a, _ in sets) / len(sets)
+        r = line(distinct * per_expert, us)
+        r["tokens_per_s"] = round(n / (us * 1e-6), 1)
+        r["tensor_tflops"] = round(2.0 * n * c.top_k * macs_per_slot / (us * 1e-6) / 1e12, 2)
+        res[str(n)] = r
+    out["moe_prefill_128x_top8_h4096_f1536"] = {"format": "gate/up IQ4_XS, down Q4_K", "kernel": "tcgen05 f16",
+                                                "bytes_per_expert": per_expert, "n_tok": res}
     del wg, wd
 
     # router + top-k producing those ids / gates: a Q8_0 router of 128
@@ -677,6 +700,33 @@ def run_profile_float(args):
     return 0
 
 
+def run_profile_prefill(args):
+    """Two eager calls of the tensor-core MoE layer at --profile-prefill tokens
+    (full-size pool), for ncu captures."""
+    import torch
+    from moe_matvec_gb300 import api, synth
+    api.load()
+    n = args.profile_prefill
+    c = synth.MOE_CASE
+    g = torch.Generator(device="cuda")
+    g.manual_seed(2200)
+    H, F, E = c.hidden, c.ffn, c.n_experts
+    wg = torch.empty((E, 2 * F, api.row_bytes(c.fmt_gate_up, H)), dtype=torch.uint8, device="cuda")
+    wd = torch.empty((E, H, api.row_bytes(c.fmt_down, F)), dtype=torch.uint8, device="cuda")
+    for e in range(E):
+        wg[e] = api.quantize_weights(c.fmt_gate_up, torch.randn((2 * F, H), generator=g, device="cuda") * 0.02)
+        wd[e] = api.quantize_weights(c.fmt_down, torch.randn((H, F), generator=g, device="cuda") * 0.02)
+    ex = api.moe_experts(E, H, F, c.fmt_gate_up, c.fmt_down, wg, wd)
+    x = torch.from_numpy(synth.activations(2450 + n, n, H)).cuda()
+    ws = torch.empty(api.moe_prefill_workspace_bytes(ex, n, c.top_k), dtype=torch.uint8, device="cuda")
+    for k in range(2):
+        a, b = synth.routing(2350 + 17 * n + k, n, E, c.top_k)
+        api.moe_prefill_run(ex, torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda(), x, ws=ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_run": "moe_prefill_128x_top8_h4096_f1536", "n_tok": n, "calls": 2}))
+    return 0
+
+
 def run_profile_dense(args):
     """Eager calls of one dense configuration fmt:M:K:n_tok in the bench's
     launch configuration (split from the shape, workspace with room for the
@@ -737,6 +787,8 @@ def main(argv=None):
     ap.add_argument("--profile-moe", type=int, default=0, help="two eager MoE calls at this many tokens (for ncu)")
     ap.add_argument("--profile-float", type=int, default=0,
                     help="two eager F16 17408 x 5120 calls at this many tokens (for ncu)")
+    ap.add_argument("--profile-prefill", type=int, default=0,
+                    help="two eager tensor-core MoE calls at this many tokens (for ncu)")
     ap.add_argument("--profile-dense", default="",
                     help="eager calls of one dense configuration fmt:M:K:n_tok (for ncu)")
     args = ap.parse_args(argv)
@@ -750,6 +802,8 @@ def main(argv=None):
         return run_profile_float(args)
     if args.profile_dense:
         return run_profile_dense(args)
+    if args.profile_prefill:
+        return run_profile_prefill(args)
     if args.profile:
         return run_profile(args)
     return run_ours(args)

@@ -190,6 +190,7 @@ enum qmv_status {
 #define QMV_DEVERR_TIMEOUT 0x4      /* a pipeline wait exceeded its limit */
 
 #define QMV_MAX_TOKENS 64
+#define QMV_MAX_PREFILL_TOKENS 16384 /* moe_qmv_prefill_run */
 #define QMV_MAX_TOPK 8
 
 /* Bytes of one quantized row of K weights; negative QMV_ERR_* if fmt or K is
@@ -358,6 +359,27 @@ int moe_qmv_run(const moe_experts* e, const int32_t* ids, const float* gates,
                 const float* x, float* y, int n_tok, int top_k, void* ws,
                 size_t ws_bytes, cudaStream_t stream);
 
+/* The same MoE layer for large batches (prefill, "Castagna Veloce", section
+ * "Kernels for the MI50", second bullet: the expert-grouped quantized MoE
+ * GEMM for prompt processing), 1 <= n_tok <= QMV_MAX_PREFILL_TOKENS, on the
+ * tcgen05 tensor cores: per routed expert, tiles of 128 weight rows times up
+ * to 64 of its token slots; each 32-weight block's integer dot products are
+ * formed exactly by the tensor core (the codes of weights and activations
+ * held as f16, accumulated in fp32) and its fp32 scales applied as in
+ * moe_qmv_run, so the result satisfies the same bounds (h within the gate/up
+ * tolerance, q8(h) by the activation rule, o and y within 1e-5 *
+ * sum |What Hhat| times the gates).  Arguments and the meaning of ids, gates,
+ * x and y as moe_qmv_run; each expert's weights are read once per 64 of its
+ * slots.  The workspace holds h, its quantization and o at the offsets
+ * moe_qmv_prefill_workspace_offsets returns (the five entries of
+ * moe_qmv_workspace_offsets), plus the quantized x and the per-expert slot
+ * lists.  Constraints as moe_qmv_run, and hidden and ffn multiples of 128.
+ * Five launches, no programmatic dependent launch. */
+size_t moe_qmv_prefill_workspace_bytes(const moe_experts* e, int n_tok, int top_k);
+int moe_qmv_prefill_workspace_offsets(const moe_experts* e, int n_tok, int top_k, size_t offsets[5]);
+int moe_qmv_prefill_run(const moe_experts* e, const int32_t* ids, const float* gates, const float* x, float* y,
+                        int n_tok, int top_k, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Router and top-k ("Castagna Veloce", section "Fused operations": router
  * and top-k in one kernel, i.e. matvec, gating, top-k and weight
  * normalization), producing the ids and gates moe_qmv_run takes:
@@ -389,6 +411,28 @@ int moe_route_run(int fmt, const void* Wr, const float* x, int n_experts, int64_
  * mismatches[0] (division) and mismatches[1] (reciprocal), device memory,
  * 16-byte aligned.  Both must stay 0. */
 int qmv_check_rounding(unsigned long long* mismatches, cudaStream_t stream);
+
+/* Diagnostic (no counterpart on the pages): Df = A B^T for one 128 x N
+ * tile of int8 codes over one 32-element block, through the tcgen05 tensor
+ * cores with the codes held exactly as f16 and an fp32 accumulator (the
+ * tcgen05 MMA of sm_103a has no int8 kind).  A int8 [128][32], B int8
+ * [N][32], Df fp32 [128][N], row-major device memory; 16 <= N <= 256,
+ * N % 16 == 0.  Every product and partial sum is an integer below 2^24 in
+ * magnitude, so Df equals the exact integer dot products. */
+int qmv_tc_probe(const int8_t* A, const int8_t* B, int N, float* Df, cudaStream_t stream);
+
+/* Diagnostic: measured issue rates per SM per SM clock (median over the
+ * SMs, one CTA per SM, clock64 around a fixed amount of work):
+ *   [0] dp4a, [1] prmt, [2] fp32 FMA, [3] packed fp32x2 FMA, [4] int32 to
+ *   fp32 conversion (thread instructions per clock);
+ *   [5] mma.sync m16n8k32 s8, [6] mma.sync m16n8k16 f16 (multiply-adds);
+ *   [7], [8], [9] tcgen05 f16 MMA, M = 128, N = 256, 64, 32 (multiply-adds).
+ * Writes min(count, 10) values to the host array rates and returns how many
+ * (or a negative QMV_ERR_*).  scratch: device memory of at least
+ * qmv_measure_pipes_scratch_bytes() bytes, 16-byte aligned.  Synchronises
+ * the stream. */
+size_t qmv_measure_pipes_scratch_bytes(void);
+int qmv_measure_pipes(double* rates, int count, void* scratch, size_t scratch_bytes, cudaStream_t stream);
 
 /* Diagnostic (no counterpart on the pages): sets the cycle limit of the
  * consumer warps' waits for weight stages in the matvec and MoE kernels

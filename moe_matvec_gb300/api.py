@@ -57,11 +57,17 @@ _SIGS = {
     "moe_qmv_workspace_bytes": (_sz, [ctypes.POINTER(MoeExperts), _int, _int]),
     "moe_qmv_workspace_offsets": (_int, [ctypes.POINTER(MoeExperts), _int, _int, ctypes.POINTER(_sz * 5)]),
     "moe_qmv_run": (_int, [ctypes.POINTER(MoeExperts), _vp, _vp, _vp, _vp, _int, _int, _vp, _sz, _vp]),
+    "moe_qmv_prefill_workspace_bytes": (_sz, [ctypes.POINTER(MoeExperts), _int, _int]),
+    "moe_qmv_prefill_workspace_offsets": (_int, [ctypes.POINTER(MoeExperts), _int, _int, ctypes.POINTER(_sz * 5)]),
+    "moe_qmv_prefill_run": (_int, [ctypes.POINTER(MoeExperts), _vp, _vp, _vp, _vp, _int, _int, _vp, _sz, _vp]),
     "moe_route_run": (_int, [_int, _vp, _vp, _int, _i64, _int, _int, _int, _vp, _vp, _vp, _vp]),
     "qmv_run_residual": (_int, [_int, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _vp, _sz, _vp]),
     "qmv_run_siblings": (_int, [_int, _vp, _vp, _vp, _vp, _vp, _i64, _int, _vp, _sz, _vp]),
     "qmv_get_device_error": (_int, [_vp, ctypes.POINTER(_int)]),
     "qmv_set_consumer_wait_limit": (_int, [ctypes.c_longlong]),
+    "qmv_tc_probe": (_int, [_vp, _vp, _int, _vp, _vp]),
+    "qmv_measure_pipes_scratch_bytes": (_sz, []),
+    "qmv_measure_pipes": (_int, [ctypes.POINTER(ctypes.c_double), _int, _vp, _sz, _vp]),
     "qmv_check_rounding": (_int, [_vp, _vp]),
     "qmv_strerror": (ctypes.c_char_p, [_int]),
 }
@@ -249,7 +255,12 @@ def splitk_run_static(fmt: int, W: torch.Tensor, x: torch.Tensor, M: int, K: int
 
 def moe_experts(n_experts: int, hidden: int, ffn: int, fmt_gate_up: int, fmt_down: int, w_gate_up: torch.Tensor,
                 w_down: torch.Tensor) -> MoeExperts:
-    return MoeExperts(n_experts, hidden, ffn, fmt_gate_up, fmt_down, 0, _ptr(w_gate_up), _ptr(w_down))
+    """The expert pool descriptor.  It holds references to the two weight
+    tensors, so their device memory stays allocated as long as the descriptor
+    lives (the C struct itself keeps only their addresses)."""
+    e = MoeExperts(n_experts, hidden, ffn, fmt_gate_up, fmt_down, 0, _ptr(w_gate_up), _ptr(w_down))
+    e._tensors = (w_gate_up, w_down)
+    return e
 
 
 def moe_workspace_bytes(e: MoeExperts, n_tok: int, top_k: int) -> int:
@@ -273,6 +284,34 @@ def moe_run(e: MoeExperts, ids: torch.Tensor, gates: torch.Tensor, x: torch.Tens
         ws = torch.empty(moe_workspace_bytes(e, n, top_k), dtype=torch.uint8, device=x.device)
     _check(load().moe_qmv_run(ctypes.byref(e), _ptr(ids), _ptr(gates), _ptr(x), _ptr(out), n, top_k, _ptr(ws),
                               ws.numel(), _stream(stream)), "moe_qmv_run")
+    return out
+
+
+MAX_PREFILL_TOKENS = 16384
+
+
+def moe_prefill_workspace_bytes(e: MoeExperts, n_tok: int, top_k: int) -> int:
+    return int(load().moe_qmv_prefill_workspace_bytes(ctypes.byref(e), n_tok, top_k))
+
+
+def moe_prefill_workspace_offsets(e: MoeExperts, n_tok: int, top_k: int):
+    arr = (_sz * 5)()
+    _check(load().moe_qmv_prefill_workspace_offsets(ctypes.byref(e), n_tok, top_k, ctypes.byref(arr)),
+           "moe_qmv_prefill_workspace_offsets")
+    return list(arr)
+
+
+def moe_prefill_run(e: MoeExperts, ids: torch.Tensor, gates: torch.Tensor, x: torch.Tensor,
+                    ws: torch.Tensor | None = None, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The MoE layer for large batches on the tensor cores (moe_qmv_prefill_run);
+    arguments as moe_run, n up to MAX_PREFILL_TOKENS."""
+    n, top_k = ids.shape
+    if out is None:
+        out = torch.empty((n, e.hidden), dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = torch.empty(moe_prefill_workspace_bytes(e, n, top_k), dtype=torch.uint8, device=x.device)
+    _check(load().moe_qmv_prefill_run(ctypes.byref(e), _ptr(ids), _ptr(gates), _ptr(x), _ptr(out), n, top_k,
+                                      _ptr(ws), ws.numel(), _stream(stream)), "moe_qmv_prefill_run")
     return out
 
 
@@ -305,6 +344,29 @@ def check_rounding(stream=None):
     bad = torch.zeros(2, dtype=torch.int64, device="cuda")
     _check(load().qmv_check_rounding(_ptr(bad), _stream(stream)), "qmv_check_rounding")
     return [int(v) for v in bad.cpu()]
+
+
+def tc_probe(A: torch.Tensor, B: torch.Tensor, stream=None) -> torch.Tensor:
+    """A int8 [128][32], B int8 [N][32] -> A B^T fp32 [128][N] through the
+    tcgen05 tensor cores (codes as f16, fp32 accumulator)."""
+    N = B.shape[0]
+    out = torch.empty((128, N), dtype=torch.float32, device=A.device)
+    _check(load().qmv_tc_probe(_ptr(A), _ptr(B), N, _ptr(out), _stream(stream)), "qmv_tc_probe")
+    return out
+
+
+PIPE_NAMES = ("dp4a", "prmt", "ffma", "ffma2", "i2f", "mma_sync_s8_mac", "mma_sync_f16_mac",
+              "tcgen05_f16_n256_mac", "tcgen05_f16_n64_mac", "tcgen05_f16_n32_mac")
+
+
+def measure_pipes(stream=None) -> dict:
+    """Measured per-SM per-clock rates (see qmv_measure_pipes), by name."""
+    L = load()
+    scratch = torch.empty(int(L.qmv_measure_pipes_scratch_bytes()), dtype=torch.uint8, device="cuda")
+    arr = (ctypes.c_double * len(PIPE_NAMES))()
+    n = L.qmv_measure_pipes(arr, len(PIPE_NAMES), _ptr(scratch), scratch.numel(), _stream(stream))
+    _check(n if n < 0 else 0, "qmv_measure_pipes")
+    return {PIPE_NAMES[i]: float(arr[i]) for i in range(n)}
 
 
 def set_consumer_wait_limit(cycles: int) -> None:

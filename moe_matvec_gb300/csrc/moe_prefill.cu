@@ -1,0 +1,718 @@
+// Expert-grouped MoE layer for large batches (prefill) on the tcgen05 tensor
+// cores.
+//
+// The same layer as moe_qmv_run -- gate/up projections with SwiGLU, the
+// activation rule applied to h, the down projection and the gate-weighted
+// combine in k order -- for batches of hundreds to thousands of tokens, where
+// each routed expert receives enough tokens for its weights to form a dense
+// contraction ("Castagna Veloce", section "Kernels for the MI50", second
+// bullet: the expert-grouped quantized MoE GEMM for prompt processing).
+//
+// Steps (one stream, five launches):
+//   route   : per expert, the list of its valid slots (t * top_k + k) in
+//             token order, its count and the list's offset (one CTA per
+//             expert scanning all slots, so the lists are stable);
+//   quantize: x by the activation rule (the library's standalone quantizer);
+//   gate/up : per work item (expert, 128 outputs j, up to 64 of its slots):
+//             for every 32-weight block of the hidden dimension, the CUDA
+//             cores decode the 128 gate rows and 128 up rows into f16 tiles
+//             (the int8 / 4-bit codes are exact in f16), the tensor core
+//             forms the exact integer block dot products with the 64 slots'
+//             int8 activation codes (also exact in f16, accumulated in fp32:
+//             every partial sum is an integer below 2^24), and the epilogue
+//             applies the fp32 block scales (d_w (x sub-scale) x d_x, and the
+//             Q4_K minimum term) exactly as the decode kernels do; at the end
+//             h = silu(g) u, quantized by the activation rule (one warp per
+//             32-wide block of j);
+//   down    : the same over the quantized h, o[slot] = Wdown_e Hhat;
+//   combine : y[t] = sum_k gates[t][k] o[t, k] in k order (the decode
+//             path's combine kernel).
+// The block scales are applied per 32-weight block because they are
+// arbitrary fp32 / fp16 values (no block-scaled MMA kind can carry them
+// exactly); the integer part of every block is exact, as on the dp4a path.
+// Two shared-memory tile buffers and two TMEM accumulators let the tensor
+// core multiply block k while the threads decode block k + 1 and scale
+// block k - 1.
+#include "launch.h"
+#include "qmv_core.cuh"
+#include "tc_core.cuh"
+
+namespace qmv {
+
+constexpr int PF_M = 128;        // weight rows per tile (the MMA's M)
+constexpr int PF_N = 64;         // token slots per tile (the MMA's N at most)
+constexpr int PF_THREADS = 256;  // 8 warps
+constexpr int PF_RING = 3;       // slots of the per-block scale ring
+constexpr int PF_MAX_E = 512;
+constexpr int PF_GATE_UP = 0, PF_DOWN = 1;
+constexpr int PF_A_TILE = PF_M * 64;  // bytes: 128 rows x 32 f16
+constexpr int PF_B_TILE = PF_N * 64;  // bytes: 64 rows x 32 f16
+
+struct PrefillParams {
+  const uint8_t* W;   // expert pool [E][pool_rows][rb]
+  long long rb;       // bytes per row
+  int pool_rows;      // rows per expert (2F for gate/up, H for down)
+  int K;              // reduction length
+  int R;              // outputs per expert (F for gate/up, H for down)
+  int E, top_k, n_tok;
+  const int* cnt;     // [E] valid slots per expert
+  const int* off;     // [E] first entry of the expert's list
+  const int* list;    // [S] slots grouped by expert, token order within
+  const int8_t* bq;   // activation codes: gate/up x (library layout, row t), down hq (natural, row slot)
+  const float* bd;    // [rows][K/32]
+  const int32_t* bs;  // [rows][K/32]
+  float* h;           // gate/up outputs: h [S][F] and its quantization
+  int8_t* hq;
+  float* hd;
+  int32_t* hs;
+  float* o;           // down output [S][H]
+  unsigned* err;
+};
+
+// ---------------------------------------------------------------------------
+// Routing: CTA e counts the valid slots routed to expert e and those routed
+// to lower experts (its list's offset), then writes its slots in order.  A
+// slot is valid when its id lies in [0, E) and does not repeat an earlier id
+// of the same token (the error word records the others, CTA 0 only).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int pf_slot_state(const int32_t* ids, int top_k, int E, int s, int& id) {
+  const int t = s / top_k, k = s - t * top_k;
+  id = ids[s];
+  if (id < 0 || id >= E) return QMV_DEVERR_EXPERT_RANGE;
+  for (int kk = 0; kk < k; kk++)
+    if (ids[t * top_k + kk] == id) return QMV_DEVERR_EXPERT_DUP;
+  return 0;
+}
+
+__global__ void __launch_bounds__(256) prefill_route_kernel(const int32_t* __restrict__ ids, int n_tok, int top_k,
+                                                            int E, int* __restrict__ cnt, int* __restrict__ off,
+                                                            int* __restrict__ list, unsigned* err) {
+  const int e = blockIdx.x, S = n_tok * top_k;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ int wc[8][2];
+  int n_eq = 0, n_lt = 0;  // running totals (the same in every thread)
+  // pass 1: counts
+  for (int s0 = 0; s0 < S; s0 += 256) {
+    const int s = s0 + threadIdx.x;
+    bool eq = false, lt = false;
+    if (s < S) {
+      int id;
+      const int st = pf_slot_state(ids, top_k, E, s, id);
+      if (st && e == 0) set_error(err, (unsigned)st);
+      eq = st == 0 && id == e;
+      lt = st == 0 && id < e;
+    }
+    const unsigned beq = __ballot_sync(FULL, eq), blt = __ballot_sync(FULL, lt);
+    if (lane == 0) {
+      wc[warp][0] = __popc(beq);
+      wc[warp][1] = __popc(blt);
+    }
+    __syncthreads();
+    for (int w = 0; w < 8; w++) {
+      n_eq += wc[w][0];
+      n_lt += wc[w][1];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    cnt[e] = n_eq;
+    off[e] = n_lt;
+  }
+  // pass 2: the expert's slots in order
+  int base = n_lt;
+  for (int s0 = 0; s0 < S && base < n_lt + n_eq; s0 += 256) {
+    const int s = s0 + threadIdx.x;
+    bool eq = false;
+    if (s < S) {
+      int id;
+      eq = pf_slot_state(ids, top_k, E, s, id) == 0 && id == e;
+    }
+    const unsigned beq = __ballot_sync(FULL, eq);
+    if (lane == 0) wc[warp][0] = __popc(beq);
+    __syncthreads();
+    int pre = 0, tot = 0;
+    for (int w = 0; w < 8; w++) {
+      pre += w < warp ? wc[w][0] : 0;
+      tot += wc[w][0];
+    }
+    if (eq) list[base + pre + __popc(beq & ((1u << lane) - 1u))] = s;
+    base += tot;
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Decoding one 32-weight block of a row into f16 pairs, in the K order the
+// activation tile uses for that format (Q8_0 / Q4_K: natural; IQ4_XS:
+// interleaved, K position 2i = element i, 2i + 1 = element i + 16, the order
+// its codebook decode yields), with the block's scales: the block adds
+// d_x (sA isum - sB s_x) to an output (sB, Q4_K's minimum term, else 0).
+// ---------------------------------------------------------------------------
+template <int F>
+struct PfFmt;
+template <>
+struct PfFmt<QMV_Q8_0> {
+  static constexpr int GW = 256, GB = 272, BPG = 8;  // weights, bytes, blocks per group
+  static constexpr bool INTERLEAVED = false, MIN = false;
+};
+template <>
+struct PfFmt<QMV_Q4_K> {
+  static constexpr int GW = 256, GB = 144, BPG = 8;
+  static constexpr bool INTERLEAVED = false, MIN = true;
+};
+template <>
+struct PfFmt<QMV_IQ4_XS> {
+  static constexpr int GW = 512, GB = 272, BPG = 16;
+  static constexpr bool INTERLEAVED = true, MIN = false;
+};
+
+// Bytes 0-1 / 2-3 of w (values 0..255 below 1024) as an f16 pair.
+__device__ __forceinline__ uint32_t u8x2_to_f16x2(uint32_t w, uint32_t sel) {
+  const uint32_t h = __byte_perm(w, 0x64646464u, sel);  // 0x64 | byte: 1024 + byte
+  __half2 v = *reinterpret_cast<const __half2*>(&h);
+  v = __hsub2(v, __half2half2(__ushort_as_half(0x6400u)));  // - 1024
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// The payload bytes of block jj of a group: where they start in the group.
+template <int F>
+__device__ __forceinline__ int pf_payload(int jj, int half) {
+  if constexpr (F == QMV_Q8_0) return 16 + 128 * half + 16 * jj;  // codes 16 half .. 16 half + 15
+  if constexpr (F == QMV_Q4_K) return 16 + 16 * jj;
+  return 16 + 128 * (jj >> 3) + 16 * (jj & 7);  // IQ4_XS
+}
+
+// Scales of block jj from the group's 16-byte header.
+template <int F>
+__device__ __forceinline__ void pf_scales(const uint4 hdr, int jj, float& sA, float& sB) {
+  if constexpr (F == QMV_Q8_0) {
+    const int wi = jj >> 1;
+    const uint32_t w = wi == 0 ? hdr.x : (wi == 1 ? hdr.y : (wi == 2 ? hdr.z : hdr.w));
+    sA = __half2float(__ushort_as_half((unsigned short)((jj & 1) ? w >> 16 : w & 0xFFFFu)));
+    sB = 0.f;
+  } else if constexpr (F == QMV_Q4_K) {
+    // d | dmin in the first word; field jj at bits [12 jj, 12 jj + 12) of the
+    // 96-bit string in words 1..3
+    const int b = 12 * jj, wi = b >> 5, sh = b & 31;
+    const uint32_t lo = wi == 0 ? hdr.y : (wi == 1 ? hdr.z : hdr.w);
+    const uint32_t hi = wi == 0 ? hdr.z : (wi == 1 ? hdr.w : 0u);
+    const uint32_t f = __funnelshift_r(lo, hi, sh);
+    const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hdr.x));
+    sA = dd.x * (float)(f & 63u);
+    sB = dd.y * (float)((f >> 6) & 63u);
+  } else {
+    // superblock sb = jj / 8: d in bytes [8 sb, 8 sb + 2), ls_j at bits
+    // [16 + 6 j, 22 + 6 j) of the superblock's 8-byte header
+    const int sb = jj >> 3, j = jj & 7;
+    const uint32_t w0 = sb ? hdr.z : hdr.x, w1 = sb ? hdr.w : hdr.y;
+    const int b = 16 + 6 * j;
+    const uint32_t f = b < 32 ? __funnelshift_r(w0, w1, b) : w1 >> (b - 32);
+    sA = __half2float(__ushort_as_half((unsigned short)(w0 & 0xFFFFu))) * (float)((int)(f & 63u) - 32);
+    sB = 0.f;
+  }
+}
+
+// 16 K positions (the half `half` of the block) as 8 f16 pairs out[0..7],
+// from the block's payload word group p (Q8_0: the 16 codes of that half;
+// Q4_K / IQ4_XS: the block's 16 payload bytes).
+template <int F>
+__device__ __forceinline__ void pf_decode_half(const uint4 p, int half, const uint32_t (&cb)[4], uint32_t (&out)[8]) {
+  const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+  if constexpr (F == QMV_Q8_0) {
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      out[2 * i] = tc::s8x2_to_f16x2(w[i]);
+      out[2 * i + 1] = tc::s8x2_to_f16x2(w[i] >> 16);
+    }
+  } else if constexpr (F == QMV_Q4_K) {
+    // half 0: low nibbles (elements 0..15), half 1: high nibbles (16..31)
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      const uint32_t n = (half ? w[i] >> 4 : w[i]) & 0x0F0F0F0Fu;
+      out[2 * i] = u8x2_to_f16x2(n, 0x5140u);
+      out[2 * i + 1] = u8x2_to_f16x2(n, 0x7362u);
+    }
+  } else {
+    // half 0: payload bytes 0..7 (K positions 0..15), half 1: bytes 8..15;
+    // each 32-bit word holds 8 nibbles = K positions in order
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+      const uint32_t pw = w[2 * half + i];
+      const uint32_t pl = pw & 0x77777777u, p4 = pw << 4;
+      const uint32_t c0 = iq4_lookup4(pl, pw, p4, 0xD9C8u, cb);        // K positions 8i .. 8i+3
+      const uint32_t c1 = iq4_lookup4(pl >> 16, pw, p4, 0xFBEAu, cb);  // 8i+4 .. 8i+7
+      out[4 * i] = tc::s8x2_to_f16x2(c0);
+      out[4 * i + 1] = tc::s8x2_to_f16x2(c0 >> 16);
+      out[4 * i + 2] = tc::s8x2_to_f16x2(c1);
+      out[4 * i + 3] = tc::s8x2_to_f16x2(c1 >> 16);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The projection kernel.
+// ---------------------------------------------------------------------------
+template <int F, int MODE>
+__global__ void __launch_bounds__(PF_THREADS, 1) moe_prefill_kernel(const PrefillParams p) {
+  using FM = PfFmt<F>;
+  constexpr int NA = MODE == PF_GATE_UP ? 2 : 1;  // weight tiles per item (gate, up)
+  constexpr int TB = NA * PF_N;                    // TMEM columns per buffer
+  constexpr int TCOLS = MODE == PF_GATE_UP ? 256 : 128;
+  constexpr bool HALF = MODE == PF_DOWN;           // two threads per weight row
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* a_buf = smem;                                              // [2][NA][A tile]
+  uint8_t* b_buf = a_buf + 2 * NA * PF_A_TILE;                        // [2][B tile]
+  float* ring_sa = reinterpret_cast<float*>(b_buf + 2 * PF_B_TILE);  // [RING][NA * 128]
+  float* ring_sb = ring_sa + PF_RING * NA * PF_M;                     // [RING][NA * 128]
+  float* ring_dx = ring_sb + PF_RING * NA * PF_M;                     // [RING][64]
+  float* ring_dxs = ring_dx + PF_RING * PF_N;                         // [RING][64]
+  __shared__ uint64_t bar[2];
+  __shared__ uint32_t tslot;
+  __shared__ int prefix[PF_MAX_E + 1];  // work items before each expert
+  __shared__ int s_slot[PF_N];
+  __shared__ int s_part[PF_THREADS / 32];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp == 0) {
+    tc::tmem_alloc(&tslot, TCOLS);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+  }
+  // work items of each expert: (R / 128) row tiles x ceil(cnt / 64) slot tiles;
+  // block scan of the counts (two experts per thread)
+  const int mtiles = p.R / PF_M;
+  {
+    int c0 = 0, c1 = 0;
+    const int e0 = 2 * tid, e1 = 2 * tid + 1;
+    if (e0 < p.E) c0 = mtiles * ((p.cnt[e0] + PF_N - 1) / PF_N);
+    if (e1 < p.E) c1 = mtiles * ((p.cnt[e1] + PF_N - 1) / PF_N);
+    int v = c0 + c1, incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(FULL, incl, o);
+      if (lane >= o) incl += a;
+    }
+    if (lane == 31) s_part[warp] = incl;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < warp; w++) before += s_part[w];
+    const int excl = before + incl - v;
+    if (e0 <= p.E) prefix[e0] = excl;
+    if (e1 <= p.E) prefix[e1] = excl + c0;
+    if (tid == PF_THREADS - 1 && 2 * PF_THREADS <= p.E) prefix[p.E] = before + incl;  // E = 512
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tslot;
+  const int total = prefix[p.E];
+  const long long i0 = (long long)total * blockIdx.x / gridDim.x, i1 = (long long)total * (blockIdx.x + 1) / gridDim.x;
+
+  // this thread's weight row (decode) and epilogue place
+  const int arow = tid & (PF_M - 1);
+  const int atile = HALF ? 0 : tid >> 7;  // gate / up
+  const int ahalf = HALF ? tid >> 7 : 0;
+  const int q4 = warp & 3, hh = warp >> 2;  // TMEM lane quarter, slot half
+  const int erow = 32 * q4 + lane;          // epilogue row within the tile
+  uint32_t cb[4];
+  cb[0] = __shfl_sync(FULL, IQ4_T0, 0);
+  cb[1] = __shfl_sync(FULL, IQ4_T1, 0);
+  cb[2] = __shfl_sync(FULL, IQ4_T2, 0);
+  cb[3] = __shfl_sync(FULL, IQ4_T3, 0);
+  const int nK = p.K / 32;
+  long long it = 0;  // K steps issued by this CTA (ring / buffer / phase position)
+
+  for (long long item = i0; item < i1; item++) {
+    // locate (expert, row tile, slot tile)
+    int lo = 0, hi = p.E;  // prefix[lo] <= item < prefix[lo + 1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (prefix[mid] <= item)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    const int e = lo, cnt_e = p.cnt[e];
+    const int ntl = (cnt_e + PF_N - 1) / PF_N;
+    const int idx = (int)(item - prefix[e]), mt = idx / ntl, nt = idx - mt * ntl;
+    const int count = min(PF_N, cnt_e - nt * PF_N);
+    const int nmma = (count + 15) & ~15;
+    __syncthreads();  // the previous item's readers of s_slot are done
+    if (tid < PF_N) s_slot[tid] = tid < count ? p.list[p.off[e] + nt * PF_N + tid] : -1;
+    __syncthreads();
+
+    // the decode thread's weight row
+    const int j0 = mt * PF_M;
+    const long long wrow = (long long)e * p.pool_rows + (MODE == PF_GATE_UP ? atile * p.R : 0) + j0 + arow;
+    const uint8_t* rowp = p.W + wrow * p.rb;
+    // B staging: slot tile row n, core matrix q
+    const int bn = tid >> 2, bqq = tid & 3;
+    const int bslot = bn < count ? s_slot[bn] : -1;
+    const long long brow = bslot < 0 ? -1 : (MODE == PF_GATE_UP ? bslot / p.top_k : bslot);
+
+    float acc[NA][32];
+#pragma unroll
+    for (int a = 0; a < NA; a++)
+#pragma unroll
+      for (int i = 0; i < 32; i++) acc[a][i] = 0.f;
+    const bool ep_active = 32 * hh < count;
+
+    // prefetched raw weight bytes of the next block
+    uint4 hdr, pay0, pay1 = make_uint4(0, 0, 0, 0);
+    auto load_block = [&](int kb, uint4& h, uint4& q0, uint4& q1) {
+      const int g = kb / FM::BPG, jj = kb - g * FM::BPG;
+      const uint8_t* gp = rowp + (long long)g * FM::GB;
+      h = __ldg(reinterpret_cast<const uint4*>(gp));
+      if constexpr (F == QMV_Q8_0) {
+        if (HALF) {
+          q0 = __ldg(reinterpret_cast<const uint4*>(gp + pf_payload<F>(jj, ahalf)));
+        } else {
+          q0 = __ldg(reinterpret_cast<const uint4*>(gp + pf_payload<F>(jj, 0)));
+          q1 = __ldg(reinterpret_cast<const uint4*>(gp + pf_payload<F>(jj, 1)));
+        }
+      } else {
+        q0 = __ldg(reinterpret_cast<const uint4*>(gp + pf_payload<F>(jj, 0)));
+      }
+    };
+    load_block(0, hdr, pay0, pay1);
+
+    const long long base = it;  // this item's first K step
+    for (int k = 0; k <= nK; k++) {
+      const long long cur = base + k;  // the K step decoded / issued in this iteration
+      if (k < nK) {
+        const int buf = (int)(cur & 1), slot = (int)(cur % PF_RING);
+        // ---- decode the weights of block k into the A tile ----
+        const int jj = k % FM::BPG;
+        float sA, sB;
+        pf_scales<F>(hdr, jj, sA, sB);
+        uint8_t* at = a_buf + (buf * NA + atile) * PF_A_TILE;
+        if (HALF) {
+          uint32_t o[8];
+          pf_decode_half<F>(pay0, ahalf, cb, o);
+          *reinterpret_cast<uint4*>(at + tc::kmajor_offset(arow, 32 * ahalf, 64)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(at + tc::kmajor_offset(arow, 32 * ahalf + 16, 64)) =
+              make_uint4(o[4], o[5], o[6], o[7]);
+        } else {
+#pragma unroll
+          for (int hv = 0; hv < 2; hv++) {
+            uint32_t o[8];
+            pf_decode_half<F>(F == QMV_Q8_0 && hv ? pay1 : pay0, hv, cb, o);
+            *reinterpret_cast<uint4*>(at + tc::kmajor_offset(arow, 32 * hv, 64)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(at + tc::kmajor_offset(arow, 32 * hv + 16, 64)) =
+                make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        }
+        if (!HALF || ahalf == 0) {
+          ring_sa[slot * NA * PF_M + atile * PF_M + arow] = sA;
+          if constexpr (FM::MIN) ring_sb[slot * NA * PF_M + atile * PF_M + arow] = sB;
+        }
+        if (k + 1 < nK) load_block(k + 1, hdr, pay0, pay1);
+        // ---- the activation codes of block k into the B tile ----
+        {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (brow >= 0) {
+            const int8_t* src = p.bq + brow * (long long)p.K;
+            uint32_t lo, hi2;  // natural: 8 codes; interleaved: 4 + 4 codes
+            if (MODE == PF_GATE_UP) {
+              // library layout: element e of block l in group g at g*256 + (e/16)*128 + l*16 + e%16
+              const int g = k >> 3, l = k & 7;
+              const int8_t* gp = src + g * 256 + l * 16;
+              if (FM::INTERLEAVED) {
+                lo = *reinterpret_cast<const uint32_t*>(gp + 4 * bqq);
+                hi2 = *reinterpret_cast<const uint32_t*>(gp + 128 + 4 * bqq);
+              } else {
+                const uint2 u = *reinterpret_cast<const uint2*>(gp + (bqq >> 1) * 128 + 8 * (bqq & 1));
+                lo = u.x;
+                hi2 = u.y;
+              }
+            } else {
+              const int8_t* gp = src + k * 32;
+              if (FM::INTERLEAVED) {
+                lo = *reinterpret_cast<const uint32_t*>(gp + 4 * bqq);
+                hi2 = *reinterpret_cast<const uint32_t*>(gp + 16 + 4 * bqq);
+              } else {
+                const uint2 u = *reinterpret_cast<const uint2*>(gp + 8 * bqq);
+                lo = u.x;
+                hi2 = u.y;
+              }
+            }
+            if (FM::INTERLEAVED) {
+              const uint32_t a0 = __byte_perm(lo, hi2, 0x5140u), a1 = __byte_perm(lo, hi2, 0x7362u);
+              v = make_uint4(tc::s8x2_to_f16x2(a0), tc::s8x2_to_f16x2(a0 >> 16), tc::s8x2_to_f16x2(a1),
+                             tc::s8x2_to_f16x2(a1 >> 16));
+            } else {
+              v = make_uint4(tc::s8x2_to_f16x2(lo), tc::s8x2_to_f16x2(lo >> 16), tc::s8x2_to_f16x2(hi2),
+                             tc::s8x2_to_f16x2(hi2 >> 16));
+            }
+          }
+          *reinterpret_cast<uint4*>(b_buf + buf * PF_B_TILE + tc::kmajor_offset(bn, 16 * bqq, 64)) = v;
+          if (tid < PF_N) {
+            float dx = 0.f, dxs = 0.f;
+            if (tid < count) {
+              const int sl = s_slot[tid];
+              const long long r = MODE == PF_GATE_UP ? sl / p.top_k : sl;
+              dx = p.bd[r * (p.K / 32) + k];
+              if constexpr (FM::MIN) dxs = dx * (float)p.bs[r * (p.K / 32) + k];
+            }
+            ring_dx[slot * PF_N + tid] = dx;
+            ring_dxs[slot * PF_N + tid] = dxs;
+          }
+        }
+        tc::fence_smem_to_async();
+        tc::fence_before_sync();
+        __syncthreads();
+        tc::fence_after_sync();
+        if (tid == 0) {
+          const uint32_t idesc = tc::idesc_f16_f32(PF_M, nmma);
+          const uint32_t sb = smem_u32(b_buf + buf * PF_B_TILE);
+#pragma unroll
+          for (int a = 0; a < NA; a++) {
+            const uint32_t sa = smem_u32(a_buf + (buf * NA + a) * PF_A_TILE);
+            const uint32_t d = tmem + (uint32_t)(buf * TB + a * PF_N);
+            tc::mma_f16(d, tc::smem_desc(sa, 128, 512), tc::smem_desc(sb, 128, 512), idesc, false);
+            tc::mma_f16(d, tc::smem_desc(sa + 256, 128, 512), tc::smem_desc(sb + 256, 128, 512), idesc, true);
+          }
+          tc::commit(&bar[buf]);
+        }
+      }
+      if (k >= 1) {
+        // ---- epilogue of block k - 1: scale its integer sums into acc ----
+        const long long prev = cur - 1;
+        const int pbuf = (int)(prev & 1), pslot = (int)(prev % PF_RING);
+        mbar_wait(&bar[pbuf], (uint32_t)((prev >> 1) & 1), p.err);
+        tc::fence_after_sync();
+        // the warp's lanes leave the wait (and thread 0 the MMA issue) on
+        // their own; the TMEM loads below are warp-aligned instructions
+        __syncwarp();
+        if (ep_active) {
+          const float* dxp = ring_dx + pslot * PF_N + 32 * hh;
+          const float* dxsp = ring_dxs + pslot * PF_N + 32 * hh;
+#pragma unroll
+          for (int a = 0; a < NA; a++) {
+            float D[32];
+            tc::tmem_ld_x32(tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)(pbuf * TB + a * PF_N + 32 * hh), D);
+            const float sa = ring_sa[pslot * NA * PF_M + a * PF_M + erow];
+            const float2 sa2 = make_float2(sa, sa);
+            float2 nsb2 = make_float2(0.f, 0.f);
+            if constexpr (FM::MIN) {
+              const float sb = ring_sb[pslot * NA * PF_M + a * PF_M + erow];
+              nsb2 = make_float2(-sb, -sb);
+            }
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const float2 dx = *reinterpret_cast<const float2*>(dxp + i);
+              float2 v = __ffma2_rn(__fmul2_rn(sa2, dx), make_float2(D[i], D[i + 1]),
+                                    make_float2(acc[a][i], acc[a][i + 1]));
+              if constexpr (FM::MIN) v = __ffma2_rn(nsb2, *reinterpret_cast<const float2*>(dxsp + i), v);
+              acc[a][i] = v.x;
+              acc[a][i + 1] = v.y;
+            }
+          }
+        }
+        tc::fence_before_sync();
+      }
+    }
+    it += nK;
+
+    // ---- outputs ----
+    if (ep_active) {
+      const int j = j0 + erow;
+      if constexpr (MODE == PF_GATE_UP) {
+        const int F_ = p.R;
+#pragma unroll
+        for (int i = 0; i < 32; i++) {
+          const int n = 32 * hh + i;
+          if (n >= count) break;  // warp-uniform
+          const long long sl = s_slot[n];
+          const float g = acc[0][i], u = acc[1][i];
+          const float hv = g / (1.0f + expf(-g)) * u;
+          p.h[sl * F_ + j] = hv;
+          // the activation rule over the warp's 32 consecutive j (one block)
+          const unsigned ab = __float_as_uint(fabsf(hv));
+          const float amax = __uint_as_float(__reduce_max_sync(FULL, ab));
+          const float d = __fdiv_rn(amax, 127.0f);
+          const float id = d > 0.0f ? __frcp_rn(d) : 0.0f;
+          float pq = __fmul_rn(hv, id);
+          pq = pq != pq ? 0.0f : fminf(fmaxf(pq, -127.0f), 127.0f);
+          const int q = __float2int_rn(pq);
+          const int s = __reduce_add_sync(FULL, q);
+          p.hq[sl * F_ + j] = (int8_t)q;
+          if (lane == 0) {
+            p.hd[sl * (F_ / 32) + j / 32] = d;
+            p.hs[sl * (F_ / 32) + j / 32] = s;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; i++) {
+          const int n = 32 * hh + i;
+          if (n >= count) break;
+          p.o[(long long)s_slot[n] * p.R + j] = acc[0][i];
+        }
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, TCOLS);
+}
+
+template <int F, int MODE>
+static cudaError_t launch_prefill(const PrefillParams& p, int grid, cudaStream_t stream) {
+  constexpr int NA = MODE == PF_GATE_UP ? 2 : 1;
+  const size_t smem = (size_t)2 * NA * PF_A_TILE + 2 * PF_B_TILE + (size_t)PF_RING * NA * PF_M * 2 * sizeof(float) +
+                      (size_t)PF_RING * PF_N * 2 * sizeof(float);
+  auto kern = moe_prefill_kernel<F, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, PF_THREADS, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int MODE>
+static cudaError_t launch_prefill_fmt(int fmt, const PrefillParams& p, int grid, cudaStream_t stream) {
+  switch (fmt) {
+    case QMV_Q8_0: return launch_prefill<QMV_Q8_0, MODE>(p, grid, stream);
+    case QMV_Q4_K: return launch_prefill<QMV_Q4_K, MODE>(p, grid, stream);
+    default: return launch_prefill<QMV_IQ4_XS, MODE>(p, grid, stream);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int PF_NOFF = 11;
+
+size_t al256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+int pf_group_weights(int fmt) { return fmt == QMV_IQ4_XS ? 512 : 256; }
+
+// [0] h f32 [S][F], [1] hq i8 [S][F], [2] hd f32 [S][F/32], [3] hs i32
+// [S][F/32], [4] o f32 [S][H], [5] xq i8 [n][H], [6] xd f32 [n][H/32],
+// [7] xs i32 [n][H/32], [8] cnt i32 [E], [9] off i32 [E], [10] list i32 [S]
+size_t pf_layout(const moe_experts* e, int n_tok, int top_k, size_t off[PF_NOFF]) {
+  const size_t S = (size_t)n_tok * top_k, F = (size_t)e->ffn, H = (size_t)e->hidden, n = (size_t)n_tok;
+  const size_t sizes[PF_NOFF] = {S * F * 4, S * F, S * (F / 32) * 4, S * (F / 32) * 4, S * H * 4,
+                                 n * H,     n * (H / 32) * 4,        n * (H / 32) * 4, (size_t)e->n_experts * 4,
+                                 (size_t)e->n_experts * 4, S * 4};
+  size_t cur = 0;
+  for (int i = 0; i < PF_NOFF; i++) {
+    off[i] = cur;
+    cur = al256(cur + sizes[i]);
+  }
+  return cur;
+}
+
+int pf_check(const moe_experts* e, int n_tok, int top_k) {
+  if (!e) return QMV_ERR_NULL;
+  const int fg = e->fmt_gate_up, fd = e->fmt_down;
+  const bool ok_fmt = (fg == QMV_Q8_0 || fg == QMV_Q4_K || fg == QMV_IQ4_XS) &&
+                      (fd == QMV_Q8_0 || fd == QMV_Q4_K || fd == QMV_IQ4_XS);
+  if (!ok_fmt) return QMV_ERR_FORMAT;
+  if (e->n_experts < 1 || e->n_experts > PF_MAX_E || e->hidden <= 0 || e->ffn <= 0 || e->hidden > (1 << 20) ||
+      e->ffn > (1 << 20) || e->hidden % PF_M || e->ffn % PF_M || e->hidden % pf_group_weights(fg) ||
+      e->ffn % pf_group_weights(fd))
+    return QMV_ERR_SHAPE;
+  if (n_tok < 1 || n_tok > QMV_MAX_PREFILL_TOKENS || top_k < 1 || top_k > QMV_MAX_TOPK || top_k > e->n_experts)
+    return QMV_ERR_NTOK;
+  return QMV_OK;
+}
+}  // namespace
+
+}  // namespace qmv
+
+using namespace qmv;
+
+extern "C" size_t moe_qmv_prefill_workspace_bytes(const moe_experts* e, int n_tok, int top_k) {
+  if (pf_check(e, n_tok, top_k)) return 0;
+  size_t off[PF_NOFF];
+  return pf_layout(e, n_tok, top_k, off);
+}
+
+extern "C" int moe_qmv_prefill_workspace_offsets(const moe_experts* e, int n_tok, int top_k, size_t offsets[5]) {
+  int rc = pf_check(e, n_tok, top_k);
+  if (rc) return rc;
+  if (!offsets) return QMV_ERR_NULL;
+  size_t off[PF_NOFF];
+  pf_layout(e, n_tok, top_k, off);
+  for (int i = 0; i < 5; i++) offsets[i] = off[i];
+  return QMV_OK;
+}
+
+extern "C" int moe_qmv_prefill_run(const moe_experts* e, const int32_t* ids, const float* gates, const float* x,
+                                   float* y, int n_tok, int top_k, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  int rc = pf_check(e, n_tok, top_k);
+  if (rc) return rc;
+  if (!ids || !gates || !x || !y || !ws || !e->w_gate_up || !e->w_down) return QMV_ERR_NULL;
+  auto a16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+  if (!a16(ids) || !a16(gates) || !a16(x) || !a16(y) || !a16(ws) || !a16(e->w_gate_up) || !a16(e->w_down))
+    return QMV_ERR_ALIGN;
+  size_t off[PF_NOFF];
+  if (ws_bytes < pf_layout(e, n_tok, top_k, off)) return QMV_ERR_WORKSPACE;
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QMV_ERR_CUDA;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) return QMV_ERR_DEVICE;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  float* h = reinterpret_cast<float*>(w + off[0]);
+  int8_t* hq = reinterpret_cast<int8_t*>(w + off[1]);
+  float* hd = reinterpret_cast<float*>(w + off[2]);
+  int32_t* hs = reinterpret_cast<int32_t*>(w + off[3]);
+  float* o = reinterpret_cast<float*>(w + off[4]);
+  int8_t* xq = reinterpret_cast<int8_t*>(w + off[5]);
+  float* xd = reinterpret_cast<float*>(w + off[6]);
+  int32_t* xs = reinterpret_cast<int32_t*>(w + off[7]);
+  int* cnt = reinterpret_cast<int*>(w + off[8]);
+  int* offs = reinterpret_cast<int*>(w + off[9]);
+  int* list = reinterpret_cast<int*>(w + off[10]);
+  const int E = e->n_experts, H = e->hidden, F = e->ffn;
+  unsigned* err = device_error_word();
+
+  prefill_route_kernel<<<E, 256, 0, stream>>>(ids, n_tok, top_k, E, cnt, offs, list, err);
+  if (cudaGetLastError() != cudaSuccess) return QMV_ERR_CUDA;
+  if (launch_act_quant(x, H, n_tok, xq, xd, xs, stream, false) != cudaSuccess) return QMV_ERR_CUDA;
+
+  const int grid = device_sm_count();
+  PrefillParams p{};
+  p.E = E;
+  p.top_k = top_k;
+  p.n_tok = n_tok;
+  p.cnt = cnt;
+  p.off = offs;
+  p.list = list;
+  p.err = err;
+  // gate / up + SwiGLU + the activation rule on h
+  p.W = static_cast<const uint8_t*>(e->w_gate_up);
+  p.rb = qmv_row_bytes(e->fmt_gate_up, H);
+  p.pool_rows = 2 * F;
+  p.K = H;
+  p.R = F;
+  p.bq = xq;
+  p.bd = xd;
+  p.bs = xs;
+  p.h = h;
+  p.hq = hq;
+  p.hd = hd;
+  p.hs = hs;
+  if (launch_prefill_fmt<PF_GATE_UP>(e->fmt_gate_up, p, grid, stream) != cudaSuccess) return QMV_ERR_CUDA;
+  // down
+  PrefillParams pd = p;
+  pd.W = static_cast<const uint8_t*>(e->w_down);
+  pd.rb = qmv_row_bytes(e->fmt_down, F);
+  pd.pool_rows = H;
+  pd.K = F;
+  pd.R = H;
+  pd.bq = hq;
+  pd.bd = hd;
+  pd.bs = hs;
+  pd.o = o;
+  if (launch_prefill_fmt<PF_DOWN>(e->fmt_down, pd, grid, stream) != cudaSuccess) return QMV_ERR_CUDA;
+  return launch_moe_combine(ids, gates, o, y, n_tok, top_k, E, H, stream, false) == cudaSuccess ? QMV_OK
+                                                                                                 : QMV_ERR_CUDA;
+}

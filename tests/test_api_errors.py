@@ -106,3 +106,4 @@ def test_split_choice_fits_float_activations(L):
     s = L.qmv_splitk_choose(8, 64, 65536, 2)
     assert s >= 6 and 128 % s == 0 and (65536 // s) * 2 * 4 <= 96 * 1024
     assert L.qmv_splitk_choose(1, 17408, 5120, 16) == 1      # quantized rows: the row count decides
+

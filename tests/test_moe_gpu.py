@@ -161,6 +161,31 @@ def test_moe_all_tokens_on_the_same_experts(lib):
     check_stagewise(2, 1, Wgu, Wd, E, H, F, ids, gates, x, g)
 
 
+def test_moe_descriptor_keeps_its_weights_alive(lib):
+    # the descriptor is built from temporary device tensors and other tensors
+    # are allocated afterwards: the binding keeps the weights referenced, so
+    # their memory is not recycled under the C struct's raw addresses
+    E, H, F, top_k, n = 6, 512, 512, 2, 8
+    Wgu, Wd = make_pool(2, 1, E, H, F, 95)
+    ex = api.moe_experts(E, H, F, 2, 1, dev(Wgu), dev(Wd))
+    filler = [torch.full((Wgu.size // 4,), 7.0, device="cuda") for _ in range(4)]
+    ids, gates = synth.routing(96, n, E, top_k)
+    x = synth.activations(97, n, H)
+    ws = torch.zeros(api.moe_workspace_bytes(ex, n, top_k), dtype=torch.uint8, device="cuda")
+    y = api.moe_run(ex, dev(ids), dev(gates), dev(x), ws=ws)
+    torch.cuda.synchronize()
+    off = api.moe_workspace_offsets(ex, n, top_k)
+    S, w = n * top_k, ws.cpu().numpy()
+    g = dict(y=y.cpu().numpy(),
+             h=w[off[0]:off[0] + S * F * 4].view(np.float32).reshape(S, F),
+             hq=w[off[1]:off[1] + S * F].view(np.int8).reshape(S, F),
+             hd=w[off[2]:off[2] + S * F // 32 * 4].view(np.float32).reshape(S, F // 32),
+             hs=w[off[3]:off[3] + S * F // 32 * 4].view(np.int32).reshape(S, F // 32),
+             o=w[off[4]:off[4] + S * H * 4].view(np.float32).reshape(S, H))
+    check_stagewise(2, 1, Wgu, Wd, E, H, F, ids, gates, x, g)
+    del filler
+
+
 def test_moe_relabelling_experts_is_bitwise_invariant(lib):
     E, H, F, top_k, n = 12, 512, 512, 4, 16
     Wgu, Wd = make_pool(2, 1, E, H, F, 90)

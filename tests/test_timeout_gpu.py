@@ -51,7 +51,8 @@ def test_moe_call_with_short_wait_limit_returns_and_the_next_call_is_correct(lib
     Wd = np.stack([oracle.quantize(1, synth.weights(1301 + 2 * e, H, F)) for e in range(E)])
     ids, gates = synth.routing(1302, n, E, top_k)
     x = synth.activations(1303, n, H)
-    ex = api.moe_experts(E, H, F, 2, 1, dev(Wgu), dev(Wd))
+    Wgu_d, Wd_d = dev(Wgu), dev(Wd)          # kept alive for the calls
+    ex = api.moe_experts(E, H, F, 2, 1, Wgu_d, Wd_d)
     ws = torch.zeros(api.moe_workspace_bytes(ex, n, top_k), dtype=torch.uint8, device="cuda")
     idd, gd, xd = dev(ids), dev(gates), dev(x)
     y0 = api.moe_run(ex, idd, gd, xd, ws=ws).clone()
