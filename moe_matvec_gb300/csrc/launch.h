@@ -64,6 +64,11 @@ cudaError_t launch_splitk_reduce(const float* partial, float* y, const float* ad
 cudaError_t launch_quantize_weights(int fmt, const float* w, long long M, int K, void* W, cudaStream_t stream);
 cudaError_t launch_check_rounding(unsigned long long* bad, cudaStream_t stream);
 
+// 2-D TMA map over `rows` rows of `row_bytes` bytes (8-byte elements), box
+// box_rows x box_bytes; false if the driver's encoder is unavailable or
+// rejects the arguments.
+bool encode_rows(CUtensorMap* map, const void* W, long long rows, long long row_bytes, int box_bytes, int box_rows);
+
 // Maximum dynamic shared memory a CTA may use on the current device.
 int device_smem_optin();
 unsigned* device_error_word();  // address of the device error word (current device)

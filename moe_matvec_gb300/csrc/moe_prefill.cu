@@ -30,9 +30,16 @@
 // The block scales are applied per 32-weight block because they are
 // arbitrary fp32 / fp16 values (no block-scaled MMA kind can carry them
 // exactly); the integer part of every block is exact, as on the dp4a path.
-// Two shared-memory tile buffers and two TMEM accumulators let the tensor
-// core multiply block k while the threads decode block k + 1 and scale
-// block k - 1.
+// PF_LAG + 1 shared-memory tile buffers and TMEM accumulators let the tensor
+// core work on block k while the threads decode block k + 1 and scale block
+// k - PF_LAG (the MMA's completion latency stays off the critical path).
+// Reuse conditions, with the iteration order decode(k), barrier, MMA(k),
+// epilogue(k - LAG): a tile buffer is rewritten by decode(k) after this
+// thread waited for MMA(k - NBUF) in epilogue(k - NBUF) (NBUF >= LAG + 1);
+// a TMEM accumulator is rewritten by MMA(k) after every thread read it in
+// epilogue(k - NBUF), before barrier k (NBUF >= LAG + 1); a scale-ring slot
+// is rewritten by decode(k + RING) after barrier k + RING - 1, which every
+// thread passes only after epilogue(k) (RING >= LAG + 2).
 #include "launch.h"
 #include "qmv_core.cuh"
 #include "tc_core.cuh"
@@ -42,7 +49,9 @@ namespace qmv {
 constexpr int PF_M = 128;        // weight rows per tile (the MMA's M)
 constexpr int PF_N = 64;         // token slots per tile (the MMA's N at most)
 constexpr int PF_THREADS = 256;  // 8 warps
-constexpr int PF_RING = 3;       // slots of the per-block scale ring
+constexpr int PF_LAG = 1;        // steps between a block's MMA and its epilogue
+constexpr int PF_NBUF = PF_LAG + 1;  // smem tile buffers and TMEM accumulators
+constexpr int PF_RING = 2 * PF_NBUF;  // slots of the per-block scale ring
 constexpr int PF_MAX_E = 512;
 constexpr int PF_GATE_UP = 0, PF_DOWN = 1;
 constexpr int PF_A_TILE = PF_M * 64;  // bytes: 128 rows x 32 f16
@@ -250,46 +259,116 @@ __device__ __forceinline__ void pf_decode_half(const uint4 p, int half, const ui
 }
 
 // ---------------------------------------------------------------------------
-// The projection kernel.
+// The projection kernel: 8 decode / epilogue warps and one issue warp,
+// synchronised by mbarriers only (no CTA barrier inside a work item).
+//
+// Data movement per unit of 4 blocks (128 weights of K): the issue warp posts
+// the stage's byte count on its full mbarrier and issues 2-D TMA loads of the
+// tiles' rows (a 16-byte box of the group header and 64-byte boxes of the
+// block payloads, 128 rows each); the slots' 128 activation codes and 4
+// block scales (and code sums) are bulk-copied by the decode threads, one copy
+// each.  Stages form a ring of NST units.
+// Per block k the decode warps wait for the block's unit and for the tile
+// buffer (MMA k - NBUF done), decode their rows into the f16 A tile and the
+// slots' codes into the B tile, and arrive on tile_full; the issue warp waits
+// for tile_full and for the TMEM accumulator (epilogue k - NBUF done), issues
+// the MMAs and commits them to mma_done; the decode warps then run the
+// epilogue of block k - LAG (wait mma_done, TMEM loads, scales) and arrive on
+// acc_free.  A unit's stage is released (stage_empty) after its last block's
+// decode.  Reuse chains: a scale-ring slot written at decode(k) is read by
+// epilogue(k) and rewritten at decode(k + RING), which follows
+// mma_done(k + RING - NBUF), which follows acc_free(k + RING - 2 NBUF): so
+// RING >= 2 NBUF; every parity wait is at most one phase behind its barrier.
+// Epilogue: gate/up -- warps 0-3 scale the gate sums, warps 4-7 the up sums,
+// each for all slots of the item (rows = TMEM lanes of the warp's quarter);
+// down -- the two warp halves share the slots.
 // ---------------------------------------------------------------------------
+constexpr int PF_UB = 4;           // K blocks per unit (128 weights)
+constexpr int PF_DEC = 256;        // decode / epilogue threads (8 warps)
+constexpr int PF_ALL = PF_DEC + 32;  // + the issue warp
+
 template <int F, int MODE>
-__global__ void __launch_bounds__(PF_THREADS, 1) moe_prefill_kernel(const PrefillParams p) {
+struct PfStage {
+  static constexpr int NA = MODE == PF_GATE_UP ? 2 : 1;
+  static constexpr int NPIECE = F == QMV_Q8_0 ? 2 : 1;   // 64-byte payload boxes per row
+  static constexpr int HDR = PF_M * 16;                  // per tile
+  static constexpr int PAY = PF_M * 64;                  // per tile and piece
+  static constexpr int CODES = PF_N * 128;               // 128 codes per slot
+  static constexpr int SC = PF_N * 16;                   // 4 scales (or sums) per slot
+  static constexpr int W_BYTES = NA * (HDR + NPIECE * PAY);
+  static constexpr int BYTES = W_BYTES + CODES + 2 * SC;
+  static constexpr int NST = NA * NPIECE > 2 ? 3 : 4;    // units in flight
+  __device__ static int hdr(int a) { return a * HDR; }
+  __device__ static int pay(int a, int piece) { return NA * HDR + (a * NPIECE + piece) * PAY; }
+};
+
+// Payload box (64 bytes: blocks jj0 .. jj0 + 3) of a unit starting at block
+// jj0 of its group, piece 0 or 1 (Q8_0: codes 0-15 / 16-31 of the blocks).
+template <int F>
+__device__ __forceinline__ int pf_unit_payload(int jj0, int piece) {
+  if constexpr (F == QMV_Q8_0) return 16 + 128 * piece + 16 * jj0;
+  if constexpr (F == QMV_Q4_K) return 16 + 16 * jj0;
+  return 16 + 128 * (jj0 >> 3) + 16 * (jj0 & 7);  // IQ4_XS
+}
+
+template <int F, int MODE>
+__global__ void __launch_bounds__(PF_ALL, 1)
+    moe_prefill_kernel(const __grid_constant__ CUtensorMap map_hdr, const __grid_constant__ CUtensorMap map_pay,
+                       const PrefillParams p) {
   using FM = PfFmt<F>;
-  constexpr int NA = MODE == PF_GATE_UP ? 2 : 1;  // weight tiles per item (gate, up)
+  using SG = PfStage<F, MODE>;
+  constexpr int NA = SG::NA;
   constexpr int TB = NA * PF_N;                    // TMEM columns per buffer
   constexpr int TCOLS = MODE == PF_GATE_UP ? 256 : 128;
+  static_assert(PF_NBUF * TB <= TCOLS, "TMEM accumulators");
+  static_assert(PF_RING >= 2 * PF_NBUF && PF_LAG < PF_NBUF, "reuse chains");
   constexpr bool HALF = MODE == PF_DOWN;           // two threads per weight row
+  constexpr int NST = SG::NST;
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* a_buf = smem;                                              // [2][NA][A tile]
-  uint8_t* b_buf = a_buf + 2 * NA * PF_A_TILE;                        // [2][B tile]
-  float* ring_sa = reinterpret_cast<float*>(b_buf + 2 * PF_B_TILE);  // [RING][NA * 128]
-  float* ring_sb = ring_sa + PF_RING * NA * PF_M;                     // [RING][NA * 128]
-  float* ring_dx = ring_sb + PF_RING * NA * PF_M;                     // [RING][64]
-  float* ring_dxs = ring_dx + PF_RING * PF_N;                         // [RING][64]
-  __shared__ uint64_t bar[2];
+  uint8_t* stg = smem;                                            // [NST][stage]
+  uint8_t* a_buf = stg + NST * SG::BYTES;                         // [NBUF][NA][A tile]; item end: up sums
+  uint8_t* b_buf = a_buf + PF_NBUF * NA * PF_A_TILE;              // [NBUF][B tile]
+  float* ring_sa = reinterpret_cast<float*>(b_buf + PF_NBUF * PF_B_TILE);  // [RING][NA * 128]
+  float* ring_sb = ring_sa + PF_RING * NA * PF_M;                          // [RING][NA * 128]
+  float* ring_dx = ring_sb + PF_RING * NA * PF_M;                          // [RING][64]
+  float* ring_dxs = ring_dx + PF_RING * PF_N;                              // [RING][64]
+  __shared__ uint64_t tile_full[PF_NBUF], mma_done[PF_NBUF], acc_free[PF_NBUF];
+  __shared__ uint64_t full[4], stage_empty[4];
   __shared__ uint32_t tslot;
   __shared__ int prefix[PF_MAX_E + 1];  // work items before each expert
   __shared__ int s_slot[PF_N];
-  __shared__ int s_part[PF_THREADS / 32];
+  __shared__ int s_part[PF_ALL / 32];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool issuer = warp == PF_DEC / 32;
   if (warp == 0) {
     tc::tmem_alloc(&tslot, TCOLS);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
+    for (int b = 0; b < PF_NBUF; b++) {
+      mbar_init(&tile_full[b], PF_DEC);
+      mbar_init(&mma_done[b], 1);
+      mbar_init(&acc_free[b], PF_DEC);
+    }
+    for (int b = 0; b < NST; b++) {
+      mbar_init(&full[b], 1);
+      mbar_init(&stage_empty[b], PF_DEC);
+    }
     fence_mbar_init();
   }
+  if (issuer && lane == 0) {
+    prefetch_tensormap(&map_hdr);
+    prefetch_tensormap(&map_pay);
+  }
   // work items of each expert: (R / 128) row tiles x ceil(cnt / 64) slot tiles;
-  // block scan of the counts (two experts per thread)
+  // block scan of the counts (two experts per decode thread)
   const int mtiles = p.R / PF_M;
   {
     int c0 = 0, c1 = 0;
     const int e0 = 2 * tid, e1 = 2 * tid + 1;
-    if (e0 < p.E) c0 = mtiles * ((p.cnt[e0] + PF_N - 1) / PF_N);
-    if (e1 < p.E) c1 = mtiles * ((p.cnt[e1] + PF_N - 1) / PF_N);
+    if (!issuer && e0 < p.E) c0 = mtiles * ((p.cnt[e0] + PF_N - 1) / PF_N);
+    if (!issuer && e1 < p.E) c1 = mtiles * ((p.cnt[e1] + PF_N - 1) / PF_N);
     int v = c0 + c1, incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -301,9 +380,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1) moe_prefill_kernel(const Prefil
     int before = 0;
     for (int w = 0; w < warp; w++) before += s_part[w];
     const int excl = before + incl - v;
-    if (e0 <= p.E) prefix[e0] = excl;
-    if (e1 <= p.E) prefix[e1] = excl + c0;
-    if (tid == PF_THREADS - 1 && 2 * PF_THREADS <= p.E) prefix[p.E] = before + incl;  // E = 512
+    if (!issuer) {
+      if (e0 <= p.E) prefix[e0] = excl;
+      if (e1 <= p.E) prefix[e1] = excl + c0;
+      if (tid == PF_DEC - 1 && 2 * PF_DEC <= p.E) prefix[p.E] = before + incl;  // E = 512
+    }
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -312,19 +393,27 @@ __global__ void __launch_bounds__(PF_THREADS, 1) moe_prefill_kernel(const Prefil
   const int total = prefix[p.E];
   const long long i0 = (long long)total * blockIdx.x / gridDim.x, i1 = (long long)total * (blockIdx.x + 1) / gridDim.x;
 
-  // this thread's weight row (decode) and epilogue place
+  // a decode thread's weight row and epilogue place
   const int arow = tid & (PF_M - 1);
-  const int atile = HALF ? 0 : tid >> 7;  // gate / up
-  const int ahalf = HALF ? tid >> 7 : 0;
-  const int q4 = warp & 3, hh = warp >> 2;  // TMEM lane quarter, slot half
-  const int erow = 32 * q4 + lane;          // epilogue row within the tile
+  const int atile = HALF ? 0 : (tid >> 7) & 1;  // gate / up
+  const int ahalf = HALF ? (tid >> 7) & 1 : 0;
+  const int q4 = warp & 3, wh = (warp >> 2) & 1;  // TMEM lane quarter; gate / up (gate/up) or slot half (down)
+  const int erow = 32 * q4 + lane;                // epilogue row within the tile
   uint32_t cb[4];
   cb[0] = __shfl_sync(FULL, IQ4_T0, 0);
   cb[1] = __shfl_sync(FULL, IQ4_T1, 0);
   cb[2] = __shfl_sync(FULL, IQ4_T2, 0);
   cb[3] = __shfl_sync(FULL, IQ4_T3, 0);
-  const int nK = p.K / 32;
-  long long it = 0;  // K steps issued by this CTA (ring / buffer / phase position)
+  const uint64_t pol = policy_evict_first();
+  const int nK = p.K / 32, nU = nK / PF_UB;
+  // bounded waits; after its first timeout (error bit set) a thread stops
+  // waiting, so a stalled pipeline costs one limit per thread, not one per wait
+  bool dead = false;
+  auto pw = [&](uint64_t* b, uint32_t parity) {
+    if (!dead && !mbar_wait(b, parity, p.err)) dead = true;
+  };
+  long long it = 0;  // K steps of this CTA (buffer / ring / phase position)
+  long long ut = 0;  // units of this CTA (stage / phase position)
 
   for (long long item = i0; item < i1; item++) {
     // locate (expert, row tile, slot tile)
@@ -341,132 +430,42 @@ __global__ void __launch_bounds__(PF_THREADS, 1) moe_prefill_kernel(const Prefil
     const int idx = (int)(item - prefix[e]), mt = idx / ntl, nt = idx - mt * ntl;
     const int count = min(PF_N, cnt_e - nt * PF_N);
     const int nmma = (count + 15) & ~15;
-    __syncthreads();  // the previous item's readers of s_slot are done
+    __syncthreads();  // the previous item's readers of s_slot, the stages and the up sums are done
     if (tid < PF_N) s_slot[tid] = tid < count ? p.list[p.off[e] + nt * PF_N + tid] : -1;
     __syncthreads();
-
-    // the decode thread's weight row
     const int j0 = mt * PF_M;
-    const long long wrow = (long long)e * p.pool_rows + (MODE == PF_GATE_UP ? atile * p.R : 0) + j0 + arow;
-    const uint8_t* rowp = p.W + wrow * p.rb;
-    // B staging: slot tile row n, core matrix q
-    const int bn = tid >> 2, bqq = tid & 3;
-    const int bslot = bn < count ? s_slot[bn] : -1;
-    const long long brow = bslot < 0 ? -1 : (MODE == PF_GATE_UP ? bslot / p.top_k : bslot);
+    const long long base = it, ubase = ut;  // this item's first K step and unit
 
-    float acc[NA][32];
+    if (issuer) {
+      // ---- the issue warp: weight boxes of each unit, and the MMAs ----
+      if (lane == 0) {
+        auto issue_w = [&](int u, int st) {
+          uint8_t* sp = stg + st * SG::BYTES;
+          mbar_arrive_expect_tx(&full[st], (uint32_t)(SG::W_BYTES + count * (128 + 16 + (FM::MIN ? 16 : 0))));
+          const int g = (PF_UB * u) / FM::BPG, jj0 = (PF_UB * u) % FM::BPG;
 #pragma unroll
-    for (int a = 0; a < NA; a++)
+          for (int a = 0; a < NA; a++) {
+            const int row0 = e * p.pool_rows + (MODE == PF_GATE_UP ? a * p.R : 0) + j0;
+            tma_load_2d(sp + SG::hdr(a), &map_hdr, &full[st], g * FM::GB / 8, row0, pol);
 #pragma unroll
-      for (int i = 0; i < 32; i++) acc[a][i] = 0.f;
-    const bool ep_active = 32 * hh < count;
-
-    // prefetched raw weight bytes of the next block
-    uint4 hdr, pay0, pay1 = make_uint4(0, 0, 0, 0);
-    auto load_block = [&](int kb, uint4& h, uint4& q0, uint4& q1) {
-      const int g = kb / FM::BPG, jj = kb - g * FM::BPG;
-      const uint8_t* gp = rowp + (long long)g * FM::GB;
-      h = __ldg(reinterpret_cast<const uint4*>(gp));
-      if constexpr (F == QMV_Q8_0) {
-        if (HALF) {
-          q0 = __ldg(reinterpret_cast<const uint4*>(gp + pf_payload<F>(jj, ahalf)));
-        } else {
-          q0 = __ldg(reinterpret_cast<const uint4*>(gp + pf_payload<F>(jj, 0)));
-          q1 = __ldg(reinterpret_cast<const uint4*>(gp + pf_payload<F>(jj, 1)));
-        }
-      } else {
-        q0 = __ldg(reinterpret_cast<const uint4*>(gp + pf_payload<F>(jj, 0)));
-      }
-    };
-    load_block(0, hdr, pay0, pay1);
-
-    const long long base = it;  // this item's first K step
-    for (int k = 0; k <= nK; k++) {
-      const long long cur = base + k;  // the K step decoded / issued in this iteration
-      if (k < nK) {
-        const int buf = (int)(cur & 1), slot = (int)(cur % PF_RING);
-        // ---- decode the weights of block k into the A tile ----
-        const int jj = k % FM::BPG;
-        float sA, sB;
-        pf_scales<F>(hdr, jj, sA, sB);
-        uint8_t* at = a_buf + (buf * NA + atile) * PF_A_TILE;
-        if (HALF) {
-          uint32_t o[8];
-          pf_decode_half<F>(pay0, ahalf, cb, o);
-          *reinterpret_cast<uint4*>(at + tc::kmajor_offset(arow, 32 * ahalf, 64)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(at + tc::kmajor_offset(arow, 32 * ahalf + 16, 64)) =
-              make_uint4(o[4], o[5], o[6], o[7]);
-        } else {
-#pragma unroll
-          for (int hv = 0; hv < 2; hv++) {
-            uint32_t o[8];
-            pf_decode_half<F>(F == QMV_Q8_0 && hv ? pay1 : pay0, hv, cb, o);
-            *reinterpret_cast<uint4*>(at + tc::kmajor_offset(arow, 32 * hv, 64)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(at + tc::kmajor_offset(arow, 32 * hv + 16, 64)) =
-                make_uint4(o[4], o[5], o[6], o[7]);
+            for (int pc = 0; pc < SG::NPIECE; pc++)
+              tma_load_2d(sp + SG::pay(a, pc), &map_pay, &full[st], (g * FM::GB + pf_unit_payload<F>(jj0, pc)) / 8,
+                          row0, pol);
           }
-        }
-        if (!HALF || ahalf == 0) {
-          ring_sa[slot * NA * PF_M + atile * PF_M + arow] = sA;
-          if constexpr (FM::MIN) ring_sb[slot * NA * PF_M + atile * PF_M + arow] = sB;
-        }
-        if (k + 1 < nK) load_block(k + 1, hdr, pay0, pay1);
-        // ---- the activation codes of block k into the B tile ----
-        {
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (brow >= 0) {
-            const int8_t* src = p.bq + brow * (long long)p.K;
-            uint32_t lo, hi2;  // natural: 8 codes; interleaved: 4 + 4 codes
-            if (MODE == PF_GATE_UP) {
-              // library layout: element e of block l in group g at g*256 + (e/16)*128 + l*16 + e%16
-              const int g = k >> 3, l = k & 7;
-              const int8_t* gp = src + g * 256 + l * 16;
-              if (FM::INTERLEAVED) {
-                lo = *reinterpret_cast<const uint32_t*>(gp + 4 * bqq);
-                hi2 = *reinterpret_cast<const uint32_t*>(gp + 128 + 4 * bqq);
-              } else {
-                const uint2 u = *reinterpret_cast<const uint2*>(gp + (bqq >> 1) * 128 + 8 * (bqq & 1));
-                lo = u.x;
-                hi2 = u.y;
-              }
-            } else {
-              const int8_t* gp = src + k * 32;
-              if (FM::INTERLEAVED) {
-                lo = *reinterpret_cast<const uint32_t*>(gp + 4 * bqq);
-                hi2 = *reinterpret_cast<const uint32_t*>(gp + 16 + 4 * bqq);
-              } else {
-                const uint2 u = *reinterpret_cast<const uint2*>(gp + 8 * bqq);
-                lo = u.x;
-                hi2 = u.y;
-              }
-            }
-            if (FM::INTERLEAVED) {
-              const uint32_t a0 = __byte_perm(lo, hi2, 0x5140u), a1 = __byte_perm(lo, hi2, 0x7362u);
-              v = make_uint4(tc::s8x2_to_f16x2(a0), tc::s8x2_to_f16x2(a0 >> 16), tc::s8x2_to_f16x2(a1),
-                             tc::s8x2_to_f16x2(a1 >> 16));
-            } else {
-              v = make_uint4(tc::s8x2_to_f16x2(lo), tc::s8x2_to_f16x2(lo >> 16), tc::s8x2_to_f16x2(hi2),
-                             tc::s8x2_to_f16x2(hi2 >> 16));
-            }
+        };
+        for (int u = 0; u < NST - 1 && u < nU; u++) issue_w(u, (int)((ubase + u) % NST));
+        for (int k = 0; k < nK; k++) {
+          const long long cur = base + k;
+          const int u = k / PF_UB, l = k - u * PF_UB;
+          if (l == 0 && u + NST - 1 < nU) {
+            const long long U = ubase + u + NST - 1;  // its stage held unit U - NST
+            if (u >= 1) pw(&stage_empty[U % NST], (uint32_t)(((U - NST) / NST) & 1));
+            issue_w(u + NST - 1, (int)(U % NST));
           }
-          *reinterpret_cast<uint4*>(b_buf + buf * PF_B_TILE + tc::kmajor_offset(bn, 16 * bqq, 64)) = v;
-          if (tid < PF_N) {
-            float dx = 0.f, dxs = 0.f;
-            if (tid < count) {
-              const int sl = s_slot[tid];
-              const long long r = MODE == PF_GATE_UP ? sl / p.top_k : sl;
-              dx = p.bd[r * (p.K / 32) + k];
-              if constexpr (FM::MIN) dxs = dx * (float)p.bs[r * (p.K / 32) + k];
-            }
-            ring_dx[slot * PF_N + tid] = dx;
-            ring_dxs[slot * PF_N + tid] = dxs;
-          }
-        }
-        tc::fence_smem_to_async();
-        tc::fence_before_sync();
-        __syncthreads();
-        tc::fence_after_sync();
-        if (tid == 0) {
+          const int buf = (int)(cur % PF_NBUF);
+          pw(&tile_full[buf], (uint32_t)((cur / PF_NBUF) & 1));
+          if (cur >= PF_NBUF) pw(&acc_free[buf], (uint32_t)(((cur - PF_NBUF) / PF_NBUF) & 1));
+          tc::fence_after_sync();
           const uint32_t idesc = tc::idesc_f16_f32(PF_M, nmma);
           const uint32_t sb = smem_u32(b_buf + buf * PF_B_TILE);
 #pragma unroll
@@ -476,85 +475,242 @@ __global__ void __launch_bounds__(PF_THREADS, 1) moe_prefill_kernel(const Prefil
             tc::mma_f16(d, tc::smem_desc(sa, 128, 512), tc::smem_desc(sb, 128, 512), idesc, false);
             tc::mma_f16(d, tc::smem_desc(sa + 256, 128, 512), tc::smem_desc(sb + 256, 128, 512), idesc, true);
           }
-          tc::commit(&bar[buf]);
+          tc::commit(&mma_done[buf]);
         }
       }
-      if (k >= 1) {
-        // ---- epilogue of block k - 1: scale its integer sums into acc ----
-        const long long prev = cur - 1;
-        const int pbuf = (int)(prev & 1), pslot = (int)(prev % PF_RING);
-        mbar_wait(&bar[pbuf], (uint32_t)((prev >> 1) & 1), p.err);
-        tc::fence_after_sync();
-        // the warp's lanes leave the wait (and thread 0 the MMA issue) on
-        // their own; the TMEM loads below are warp-aligned instructions
-        __syncwarp();
-        if (ep_active) {
-          const float* dxp = ring_dx + pslot * PF_N + 32 * hh;
-          const float* dxsp = ring_dxs + pslot * PF_N + 32 * hh;
+      __syncwarp();
+    } else {
+      // ---- the decode / epilogue warps ----
+      // their copies of a unit's slot data: kind [codes lo, (codes hi), d, (s)] x slot
+      constexpr int CPS = (MODE == PF_GATE_UP ? 2 : 1) + 1 + (FM::MIN ? 1 : 0);
+      const int ckind = tid / PF_N, cslot = tid - ckind * PF_N;
+      const bool cact = ckind < CPS && cslot < count;
+      const long long crow = cact ? (MODE == PF_GATE_UP ? s_slot[cslot] / p.top_k : s_slot[cslot]) : -1;
+      auto issue_c = [&](int u, int st) {
+        if (!cact) return;
+        uint8_t* sp = stg + st * SG::BYTES;
+        const int kd = MODE == PF_GATE_UP ? ckind : (ckind == 0 ? 0 : ckind + 1);  // 0 lo, 1 hi, 2 d, 3 s
+        if (kd <= 1) {
+          const int8_t* src = p.bq + crow * (long long)p.K;
+          uint8_t* cd = sp + SG::W_BYTES + cslot * 128;
+          if (MODE == PF_GATE_UP)  // library layout: elements 0-15 of the unit's blocks, then 16-31 (128 further)
+            bulk_copy_g2s(cd + 64 * kd, src + (u >> 1) * 256 + (u & 1) * 64 + 128 * kd, 64, &full[st]);
+          else
+            bulk_copy_g2s(cd, src + u * 128, 128, &full[st]);
+        } else if (kd == 2) {
+          bulk_copy_g2s(sp + SG::W_BYTES + SG::CODES + cslot * 16, p.bd + crow * (p.K / 32) + PF_UB * u, 16, &full[st]);
+        } else {
+          bulk_copy_g2s(sp + SG::W_BYTES + SG::CODES + SG::SC + cslot * 16, p.bs + crow * (p.K / 32) + PF_UB * u, 16,
+                        &full[st]);
+        }
+      };
+      for (int u = 0; u < NST - 1 && u < nU; u++) issue_c(u, (int)((ubase + u) % NST));
+      // B staging: slot tile row n, core matrix q (K positions 8q .. 8q + 7)
+      const int bn = tid >> 2, bqq = tid & 3;
+      const bool bval = bn < count;
+      // epilogue: slots [en0, en0 + ecnt) of the warp
+      const int ecnt = MODE == PF_GATE_UP ? count : (count > 32 ? min(32, count - 32 * wh) : min(16, count - 16 * wh));
+      const int en0 = MODE == PF_GATE_UP ? 0 : (count > 32 ? 32 * wh : 16 * wh);
+      float acc[MODE == PF_GATE_UP ? 64 : 32];
 #pragma unroll
-          for (int a = 0; a < NA; a++) {
-            float D[32];
-            tc::tmem_ld_x32(tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)(pbuf * TB + a * PF_N + 32 * hh), D);
-            const float sa = ring_sa[pslot * NA * PF_M + a * PF_M + erow];
-            const float2 sa2 = make_float2(sa, sa);
-            float2 nsb2 = make_float2(0.f, 0.f);
-            if constexpr (FM::MIN) {
-              const float sb = ring_sb[pslot * NA * PF_M + a * PF_M + erow];
-              nsb2 = make_float2(-sb, -sb);
+      for (int i = 0; i < (MODE == PF_GATE_UP ? 64 : 32); i++) acc[i] = 0.f;
+
+      for (int k = 0; k < nK + PF_LAG; k++) {
+        const long long cur = base + k;
+        if (k < nK) {
+          const int buf = (int)(cur % PF_NBUF), slot = (int)(cur % PF_RING);
+          const int u = k / PF_UB, l = k - u * PF_UB;
+          const int st = (int)((ubase + u) % NST);
+          const uint8_t* sp = stg + st * SG::BYTES;
+          if (l == 0) {
+            if (u + NST - 1 < nU) {
+              const long long U = ubase + u + NST - 1;  // its stage held unit U - NST
+              if (u >= 1) pw(&stage_empty[U % NST], (uint32_t)(((U - NST) / NST) & 1));
+              issue_c(u + NST - 1, (int)(U % NST));
             }
+            pw(&full[st], (uint32_t)(((ubase + u) / NST) & 1));  // the unit has landed
+          }
+          if (cur >= PF_NBUF) pw(&mma_done[buf], (uint32_t)(((cur - PF_NBUF) / PF_NBUF) & 1));
+          // ---- decode the weights of block k into the A tile ----
+          const uint4 hdr = *reinterpret_cast<const uint4*>(sp + SG::hdr(atile) + arow * 16);
+          const int jj = k % FM::BPG;
+          float sA, sB;
+          pf_scales<F>(hdr, jj, sA, sB);
+          uint8_t* at = a_buf + (buf * NA + atile) * PF_A_TILE;
+          if (HALF) {
+            const uint4 pay =
+                *reinterpret_cast<const uint4*>(sp + SG::pay(0, SG::NPIECE == 2 ? ahalf : 0) + arow * 64 + 16 * l);
+            uint32_t o[8];
+            pf_decode_half<F>(pay, ahalf, cb, o);
+            *reinterpret_cast<uint4*>(at + tc::kmajor_offset(arow, 32 * ahalf, 64)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(at + tc::kmajor_offset(arow, 32 * ahalf + 16, 64)) =
+                make_uint4(o[4], o[5], o[6], o[7]);
+          } else {
+#pragma unroll
+            for (int hv = 0; hv < 2; hv++) {
+              const uint4 pay =
+                  *reinterpret_cast<const uint4*>(sp + SG::pay(atile, SG::NPIECE == 2 ? hv : 0) + arow * 64 + 16 * l);
+              uint32_t o[8];
+              pf_decode_half<F>(pay, hv, cb, o);
+              *reinterpret_cast<uint4*>(at + tc::kmajor_offset(arow, 32 * hv, 64)) = make_uint4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<uint4*>(at + tc::kmajor_offset(arow, 32 * hv + 16, 64)) =
+                  make_uint4(o[4], o[5], o[6], o[7]);
+            }
+          }
+          if (!HALF || ahalf == 0) {
+            ring_sa[slot * NA * PF_M + atile * PF_M + arow] = sA;
+            if constexpr (FM::MIN) ring_sb[slot * NA * PF_M + atile * PF_M + arow] = sB;
+          }
+          // ---- the activation codes of block k into the B tile ----
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (bval) {
+            const uint8_t* cr = sp + SG::W_BYTES + bn * 128;
+            uint32_t x0, x1;
+            if (FM::INTERLEAVED) {  // elements 4q .. 4q+3 and 16+4q .. 16+4q+3
+              const int o0 = MODE == PF_GATE_UP ? l * 16 + 4 * bqq : l * 32 + 4 * bqq;
+              const int o1 = MODE == PF_GATE_UP ? 64 + l * 16 + 4 * bqq : l * 32 + 16 + 4 * bqq;
+              const uint32_t lo2 = *reinterpret_cast<const uint32_t*>(cr + o0),
+                             hi2 = *reinterpret_cast<const uint32_t*>(cr + o1);
+              x0 = __byte_perm(lo2, hi2, 0x5140u);
+              x1 = __byte_perm(lo2, hi2, 0x7362u);
+            } else {  // elements 8q .. 8q+7
+              const int o0 = MODE == PF_GATE_UP ? (bqq >> 1) * 64 + l * 16 + 8 * (bqq & 1) : l * 32 + 8 * bqq;
+              const uint2 w = *reinterpret_cast<const uint2*>(cr + o0);
+              x0 = w.x;
+              x1 = w.y;
+            }
+            v = make_uint4(tc::s8x2_to_f16x2(x0), tc::s8x2_to_f16x2(x0 >> 16), tc::s8x2_to_f16x2(x1),
+                           tc::s8x2_to_f16x2(x1 >> 16));
+          }
+          *reinterpret_cast<uint4*>(b_buf + buf * PF_B_TILE + tc::kmajor_offset(bn, 16 * bqq, 64)) = v;
+          if (tid < PF_N) {
+            float dx = 0.f, dxs = 0.f;
+            if (tid < count) {
+              dx = reinterpret_cast<const float*>(sp + SG::W_BYTES + SG::CODES)[tid * 4 + l];
+              if constexpr (FM::MIN)
+                dxs = dx * (float)reinterpret_cast<const int*>(sp + SG::W_BYTES + SG::CODES + SG::SC)[tid * 4 + l];
+            }
+            ring_dx[slot * PF_N + tid] = dx;
+            ring_dxs[slot * PF_N + tid] = dxs;
+          }
+          tc::fence_smem_to_async();
+          mbar_arrive(&tile_full[buf]);
+          if (l == PF_UB - 1) mbar_arrive(&stage_empty[st]);  // this thread is done with the unit's stage
+        }
+        if (k >= PF_LAG) {
+          // ---- epilogue of block k - LAG: scale its integer sums into acc ----
+          const long long prev = cur - PF_LAG;
+          const int pbuf = (int)(prev % PF_NBUF), pslot = (int)(prev % PF_RING);
+          pw(&mma_done[pbuf], (uint32_t)((prev / PF_NBUF) & 1));
+          tc::fence_after_sync();
+          __syncwarp();  // the TMEM loads below are warp-aligned instructions
+          const int a_ep = MODE == PF_GATE_UP ? wh : 0;
+          const uint32_t tcol = tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)(pbuf * TB + a_ep * PF_N + en0);
+          const float sa = ring_sa[pslot * NA * PF_M + a_ep * PF_M + erow];
+          const float2 sa2 = make_float2(sa, sa);
+          float2 nsb2 = make_float2(0.f, 0.f);
+          if constexpr (FM::MIN) {
+            const float sb = ring_sb[pslot * NA * PF_M + a_ep * PF_M + erow];
+            nsb2 = make_float2(-sb, -sb);
+          }
+          const float* dxp = ring_dx + pslot * PF_N + en0;
+          const float* dxsp = ring_dxs + pslot * PF_N + en0;
+          auto scale_into = [&](const float (&D)[32], int a0, int nv) {
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
-              const float2 dx = *reinterpret_cast<const float2*>(dxp + i);
-              float2 v = __ffma2_rn(__fmul2_rn(sa2, dx), make_float2(D[i], D[i + 1]),
-                                    make_float2(acc[a][i], acc[a][i + 1]));
-              if constexpr (FM::MIN) v = __ffma2_rn(nsb2, *reinterpret_cast<const float2*>(dxsp + i), v);
-              acc[a][i] = v.x;
-              acc[a][i + 1] = v.y;
+              if (i < nv) {
+                const float2 dx = *reinterpret_cast<const float2*>(dxp + a0 + i);
+                float2 r = __ffma2_rn(__fmul2_rn(sa2, dx), make_float2(D[i], D[i + 1]),
+                                      make_float2(acc[a0 + i], acc[a0 + i + 1]));
+                if constexpr (FM::MIN) r = __ffma2_rn(nsb2, *reinterpret_cast<const float2*>(dxsp + a0 + i), r);
+                acc[a0 + i] = r.x;
+                acc[a0 + i + 1] = r.y;
+              }
+            }
+          };
+          if (MODE == PF_GATE_UP) {
+            if (count > 32) {
+              float D0[32], D1[32];
+              tc::tmem_ld2_x32(tcol, tcol + 32, D0, D1);
+              scale_into(D0, 0, 32);
+              if constexpr (MODE == PF_GATE_UP) scale_into(D1, 32, 32);
+            } else {
+              float D0[32];
+              tc::tmem_ld_x32(tcol, D0);
+              scale_into(D0, 0, 32);
+            }
+          } else if (ecnt > 0) {
+            if (count > 32) {
+              float D0[32];
+              tc::tmem_ld_x32(tcol, D0);
+              scale_into(D0, 0, 32);
+            } else {
+              uint32_t r16[16];
+              tc::tmem_ld_x16(tcol, r16);
+              float D0[32];
+#pragma unroll
+              for (int i = 0; i < 16; i++) D0[i] = __uint_as_float(r16[i]);
+#pragma unroll
+              for (int i = 16; i < 32; i++) D0[i] = 0.f;
+              scale_into(D0, 0, 16);
+            }
+          }
+          tc::fence_before_sync();
+          mbar_arrive(&acc_free[pbuf]);  // this thread's reads of the accumulator are complete
+        }
+      }
+      // ---- outputs of the down projection ----
+      if constexpr (MODE == PF_DOWN) {
+        const int j = j0 + erow;
+#pragma unroll
+        for (int i = 0; i < 32; i++) {
+          if (i >= ecnt) break;  // warp-uniform
+          p.o[(long long)s_slot[en0 + i] * p.R + j] = acc[i];
+        }
+      } else {
+        // gate/up: the up sums to the gate warps through shared memory (the
+        // A tiles are free: the last MMA has completed), [slot][row]
+        float* up = reinterpret_cast<float*>(a_buf);
+        if (wh == 1) {
+#pragma unroll
+          for (int i = 0; i < 64; i++) {
+            if (i >= count) break;  // warp-uniform
+            up[i * PF_M + erow] = acc[i];
+          }
+        }
+        named_sync(1, PF_DEC);
+        if (wh == 0) {
+          const int F_ = p.R, j = j0 + erow;
+#pragma unroll
+          for (int i = 0; i < 64; i++) {
+            if (i >= count) break;  // warp-uniform
+            const long long sl = s_slot[i];
+            const float g = acc[i], uu = up[i * PF_M + erow];
+            const float hv = g / (1.0f + expf(-g)) * uu;
+            p.h[sl * F_ + j] = hv;
+            // the activation rule over the warp's 32 consecutive j (one block)
+            const unsigned ab = __float_as_uint(fabsf(hv));
+            const float amax = __uint_as_float(__reduce_max_sync(FULL, ab));
+            const float d = __fdiv_rn(amax, 127.0f);
+            const float id = d > 0.0f ? __frcp_rn(d) : 0.0f;
+            float pq = __fmul_rn(hv, id);
+            pq = pq != pq ? 0.0f : fminf(fmaxf(pq, -127.0f), 127.0f);
+            const int q = __float2int_rn(pq);
+            const int s = __reduce_add_sync(FULL, q);
+            p.hq[sl * F_ + j] = (int8_t)q;
+            if (lane == 0) {
+              p.hd[sl * (F_ / 32) + j / 32] = d;
+              p.hs[sl * (F_ / 32) + j / 32] = s;
             }
           }
         }
-        tc::fence_before_sync();
       }
     }
     it += nK;
-
-    // ---- outputs ----
-    if (ep_active) {
-      const int j = j0 + erow;
-      if constexpr (MODE == PF_GATE_UP) {
-        const int F_ = p.R;
-#pragma unroll
-        for (int i = 0; i < 32; i++) {
-          const int n = 32 * hh + i;
-          if (n >= count) break;  // warp-uniform
-          const long long sl = s_slot[n];
-          const float g = acc[0][i], u = acc[1][i];
-          const float hv = g / (1.0f + expf(-g)) * u;
-          p.h[sl * F_ + j] = hv;
-          // the activation rule over the warp's 32 consecutive j (one block)
-          const unsigned ab = __float_as_uint(fabsf(hv));
-          const float amax = __uint_as_float(__reduce_max_sync(FULL, ab));
-          const float d = __fdiv_rn(amax, 127.0f);
-          const float id = d > 0.0f ? __frcp_rn(d) : 0.0f;
-          float pq = __fmul_rn(hv, id);
-          pq = pq != pq ? 0.0f : fminf(fmaxf(pq, -127.0f), 127.0f);
-          const int q = __float2int_rn(pq);
-          const int s = __reduce_add_sync(FULL, q);
-          p.hq[sl * F_ + j] = (int8_t)q;
-          if (lane == 0) {
-            p.hd[sl * (F_ / 32) + j / 32] = d;
-            p.hs[sl * (F_ / 32) + j / 32] = s;
-          }
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; i++) {
-          const int n = 32 * hh + i;
-          if (n >= count) break;
-          p.o[(long long)s_slot[n] * p.R + j] = acc[0][i];
-        }
-      }
-    }
+    ut += nU;
+  }
+  if (dead) {  // let copies this thread may not have waited for land before the CTA exits
+    for (int i = 0; i < 1000; i++) __nanosleep(10000);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -563,13 +719,20 @@ __global__ void __launch_bounds__(PF_THREADS, 1) moe_prefill_kernel(const Prefil
 
 template <int F, int MODE>
 static cudaError_t launch_prefill(const PrefillParams& p, int grid, cudaStream_t stream) {
-  constexpr int NA = MODE == PF_GATE_UP ? 2 : 1;
-  const size_t smem = (size_t)2 * NA * PF_A_TILE + 2 * PF_B_TILE + (size_t)PF_RING * NA * PF_M * 2 * sizeof(float) +
-                      (size_t)PF_RING * PF_N * 2 * sizeof(float);
+  using SG = PfStage<F, MODE>;
+  constexpr int NA = SG::NA;
+  const size_t smem = (size_t)SG::NST * SG::BYTES + (size_t)PF_NBUF * NA * PF_A_TILE + PF_NBUF * PF_B_TILE +
+                      (size_t)PF_RING * NA * PF_M * 2 * sizeof(float) + (size_t)PF_RING * PF_N * 2 * sizeof(float);
+  // the pool's rows as 8-byte elements; boxes of 128 rows x 16 bytes (group
+  // header) and x 64 bytes (4 blocks of payload)
+  const long long rows = (long long)p.E * p.pool_rows;
+  CUtensorMap map_hdr, map_pay;
+  if (!encode_rows(&map_hdr, p.W, rows, p.rb, 16, PF_M) || !encode_rows(&map_pay, p.W, rows, p.rb, 64, PF_M))
+    return cudaErrorInvalidValue;
   auto kern = moe_prefill_kernel<F, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, PF_THREADS, smem, stream>>>(p);
+  kern<<<grid, PF_ALL, smem, stream>>>(map_hdr, map_pay, p);
   return cudaGetLastError();
 }
 

@@ -84,8 +84,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 
 // 2-D map over a weight matrix seen as rows x (row_bytes / 8) 8-byte
 // elements; box = box_rows x (box_bytes / 8).
-static bool encode_rows(CUtensorMap* map, const void* W, long long rows, long long row_bytes, int box_bytes,
-                        int box_rows) {
+bool encode_rows(CUtensorMap* map, const void* W, long long rows, long long row_bytes, int box_bytes,
+                 int box_rows) {
   auto enc = encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)(row_bytes / 8), (cuuint64_t)rows};
