@@ -304,6 +304,9 @@ def run_ours(args):
             graphs[i % REPLICAS].replay()
     stream.synchronize()
 
+    # measured issue rates of the pipes (denominators of the ALU roofline)
+    pipe_rates = api.measure_pipes(stream)
+
     # per-token-count graphs for the per-call breakdown
     per_n = {}
     for n in NTOKS:
@@ -416,6 +419,21 @@ def run_ours(args):
 
     peaks, peak_kind = measured_peaks()
     achieved = step_bytes * steps / (ms * 1e-3) / 1e9
+    # the 8- and 16-token calls are bound by the dp4a pipe, not by HBM: their
+    # dp4a rate (one per 4 weights per token) against the measured per-SM
+    # dp4a rate x SMs x the SM clock sampled during the timed region
+    clk_summary = clk.summary()
+    sm_mhz = clk_summary.get("sm_mhz") or peaks.get("sm_max_mhz", 2070.0)
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_peak = pipe_rates["dp4a"] * nsm * sm_mhz * 1e6
+    roof_alu = {"bound": "alu", "pipe": "dp4a", "unit": "dp4a/s", "peak": round(alu_peak, 1),
+                "peak_kind": "measured (qmv_measure_pipes dp4a per SM per clock x SMs x sampled SM clock)",
+                "kernel": "qmv_dense_kernel<Q4_K, 8 / 16 tokens>", "per_n": {}}
+    for n in (8, 16):
+        dp4a = M * K * n / 4
+        a = dp4a / (per_n[str(n)]["us_per_call"] * 1e-6)
+        roof_alu["per_n"][str(n)] = {"achieved": round(a, 1), "frac": round(a / alu_peak, 4),
+                                     "dp4a_per_call": int(dp4a)}
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": recorded_traffic(),
             "peak_kind": peak_kind, "kernel": "qmv_dense_kernel<Q4_K>",
@@ -433,7 +451,8 @@ def run_ours(args):
                     "h2d_bytes_per_step": sum(n * K * 4 for n in NTOKS),
                     "d2h_bytes_per_step": sum(n * M * 4 for n in NTOKS),
                     "ms_per_step": e2e_ms / e2e_steps},
-            "gpu_launches": launches, "clocks": clk.summary()}
+            "gpu_launches": launches, "clocks": clk_summary, "roofline_alu": roof_alu,
+            "pipe_rates_per_sm_clk": {k: round(v, 2) for k, v in pipe_rates.items()}}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     if extra is not None:

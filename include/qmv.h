@@ -339,8 +339,11 @@ typedef struct moe_experts {
  *                                                     the activation rule)
  *   y[t] = sum_{k=0..top_k-1} gates[t][k] * o_{t,k}, added in k order.
  * ids int32 [n_tok][top_k], gates fp32 [n_tok][top_k], x fp32 [n_tok][H],
- * y fp32 [n_tok][H].  Every routed expert's weights are read once per call,
- * for all of the tokens routed to it.  A slot whose id is outside
+ * y fp32 [n_tok][H].  The slots routed to one expert are computed in groups
+ * of up to G slots, G a power of two up to 16 chosen from the mean load
+ * n_tok * top_k / n_experts (at least 8 from 4 tokens on); each group streams
+ * the expert's weights once, so an expert with more than G slots in the call
+ * is read once per group (ceil(slots / G) times).  A slot whose id is outside
  * [0, n_experts) or repeats an earlier id of the same token contributes 0 and
  * sets the device error word.  gates are used as given (not renormalised).
  * The workspace holds the intermediates at the offsets of
