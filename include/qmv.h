@@ -232,7 +232,11 @@ int qmv_quantize_act(const float* x, int64_t K, int n_tok, int8_t* q, float* d,
  * kernel (rule above); every integer block dot product is exact and the block
  * scales are applied in fp32 (F16 / F32 weights: Xhat = x, fp32 products).
  * Accuracy: |Y - Y_exact| <= 1e-5 * sum_k |What[m][k] * Xhat[t][k]|.
- * 1 <= n_tok <= 64. */
+ * 1 <= n_tok <= 64.  Tokens run in passes of up to 16; for QMV_Q4_K a pass
+ * of 5 to 16 tokens forms its integer block dot products on the tensor
+ * cores (f16 operands holding the integers, fp32 accumulation: exact) and
+ * applies the scales by the same fp32 formula, in a different summation
+ * order than passes of 1 to 4 tokens. */
 int qmv_run(int fmt, const void* W, const float* x, float* y, int64_t M,
             int64_t K, int n_tok, cudaStream_t stream);
 

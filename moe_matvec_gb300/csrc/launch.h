@@ -31,6 +31,14 @@ cudaError_t launch_dense_q8_g64(const DenseLaunch& L);
 cudaError_t launch_dense_q8_g128(const DenseLaunch& L);
 cudaError_t launch_dense_f16(const DenseLaunch& L);
 cudaError_t launch_dense_f32(const DenseLaunch& L);
+// Tensor-core Q4_K matvec (nt_tmpl 8 or 16; map_tile: box MMA_TILE_ROWS rows
+// x MMA_BOX_BYTES, map_unit: UNIT_ROWS rows x MMA_BOX_BYTES) and the shared
+// memory it takes with `stages` weight stages and split ranges of at most
+// nbmax blocks.
+constexpr int MMA_BOX_BYTES = 432;
+constexpr int MMA_TILE_ROWS = 64;
+cudaError_t launch_mma_q4_k(const DenseLaunch& L);
+size_t mma_smem_bytes(int nt, int stages, int nbmax);
 
 struct MoeParams;
 

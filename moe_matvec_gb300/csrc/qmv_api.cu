@@ -249,6 +249,9 @@ static int run_dense(int fmt, const void* W, const float* x, const int8_t* xq, c
   p.prefetch = M * rb <= PREFETCH_ALL_BYTES ? PREFETCH_STAGES : 0;
   p.err = device_error_word();
   p.wait = g_consumer_wait.load(std::memory_order_relaxed);
+  p.w = static_cast<const uint8_t*>(W);
+  p.rb = rb;
+  p.nbmax = 0;
   L.p = &p;
   L.nt_tmpl = pl.nt_tmpl;
   L.cw = pl.cw;
@@ -256,6 +259,28 @@ static int run_dense(int fmt, const void* W, const float* x, const int8_t* xq, c
   L.smem = pl.smem;
   L.stream = stream;
   L.pdl = true;
+  // Q4_K passes of 8 or 16 token slots: the tensor-core kernel, whenever its
+  // shared memory (activation area, partial sums and at least two weight
+  // stages) fits; it takes one CTA per SM.
+  bool mma = false;
+  if (fmt == QMV_Q4_K && pl.nt_tmpl >= 8 && rb >= MMA_BOX_BYTES) {
+    const int nbmax = (int)(((p.groups + n_split - 1) / n_split) * 8);
+    int st = MAX_STAGES;
+    while (st >= 2 && mma_smem_bytes(pl.nt_tmpl, st, nbmax) > (size_t)device_smem_optin()) st--;
+    CUtensorMap mt, mu;
+    if (st >= 2 && encode_rows(&mt, W, M, rb, MMA_BOX_BYTES, MMA_TILE_ROWS) &&
+        encode_rows(&mu, W, M, rb, MMA_BOX_BYTES, UNIT_ROWS)) {
+      mma = true;
+      L.map_tile = mt;
+      L.map_unit = mu;
+      p.nbmax = nbmax;
+      p.stages = st;
+      L.smem = mma_smem_bytes(pl.nt_tmpl, st, nbmax);
+      const long long work = (long long)p.units * n_split;
+      L.grid = (int)(work < device_sm_count() ? work : device_sm_count());
+    }
+  }
+  auto launch = [&]() { return mma ? launch_mma_q4_k(L) : launch_dense_any(fmt, L); };
   // the full token passes in one launch (grid y), so that they run side by
   // side, and a last partial pass in a second one
   const int full = n_tok / pl.nt_tmpl, rem = n_tok - full * pl.nt_tmpl;
@@ -263,13 +288,13 @@ static int run_dense(int fmt, const void* W, const float* x, const int8_t* xq, c
     p.t0 = 0;
     p.nt = pl.nt_tmpl;
     L.passes = full;
-    if (launch_dense_any(fmt, L) != cudaSuccess) return QMV_ERR_CUDA;
+    if (launch() != cudaSuccess) return QMV_ERR_CUDA;
   }
   if (rem > 0) {
     p.t0 = full * pl.nt_tmpl;
     p.nt = rem;
     L.passes = 1;
-    if (launch_dense_any(fmt, L) != cudaSuccess) return QMV_ERR_CUDA;
+    if (launch() != cudaSuccess) return QMV_ERR_CUDA;
   }
   return QMV_OK;
 }

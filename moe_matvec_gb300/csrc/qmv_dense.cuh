@@ -48,6 +48,10 @@ struct DenseParams {
   int prefetch;        // L2 lookahead of the producer past the ring (iterations; 0: none)
   unsigned* err;       // device error word
   long long wait;      // cycle limit of the consumers' waits for weight stages
+  // used by the tensor-core kernel (qmv_mma.cuh), which copies rows itself
+  const uint8_t* w;    // the weight rows
+  long long rb;        // bytes per row
+  int nbmax;           // blocks of the longest split range
 };
 
 // Per-CTA walk over its tiles: a contiguous range of the flattened

@@ -170,6 +170,43 @@ def test_qmv_exact_integer_sums(lib, fmt):
     assert np.array_equal(y.astype(np.float64), yr)
 
 
+@pytest.mark.parametrize("n", [5, 8, 12, 16, 21])
+def test_q4_k_block_sums_exact_at_their_extremes(lib, n):
+    # Q4_K from 5 tokens forms its block sums on the tensor cores, with the
+    # weights entering as 1024 + q: the largest sums (all codes 15 against
+    # all +-127, and the mixed rows) must still come out exact.  Scales are
+    # powers of two, so the fp32 result is bit-exact in any order.
+    r = np.random.default_rng(n)
+    K, M = 1024, 72
+    rows = []
+    for m in range(M):
+        row = b""
+        for gi in range(K // 256):
+            if m % 3 == 0:
+                codes = [[15] * 32] * 8
+            elif m % 3 == 1:
+                codes = [[0] * 32] * 8
+            else:
+                codes = r.integers(0, 16, (8, 32)).tolist()
+            row += L.pack_q4_k(L.f16_bits(2.0 ** -4), L.f16_bits(2.0 ** -5), r.integers(0, 4, 8).tolist(),
+                               r.integers(0, 4, 8).tolist(), codes)
+        rows.append(np.frombuffer(row, np.uint8))
+    W = np.stack(rows)
+    kx = r.integers(-127, 128, (n, K))
+    kx[0] = 127
+    kx[1] = -127
+    kx[2, :512] = 127
+    kx[2, 512:] = -127
+    kx[:, ::32] = np.where(kx[:, ::32] < 0, -127, 127)   # every block's amax is 127: d_x = 2^-2
+    x = (kx * 2.0 ** -2).astype(np.float32)
+    yr, _ = oracle.qmv(1, W, x, K)
+    y = lib.run(1, dev(W), dev(x), M, K).cpu().numpy()
+    assert np.array_equal(y.astype(np.float64), yr)
+    q, d, s = lib.quantize_act(dev(x))
+    y8 = lib.run_q8(1, dev(W), q, d, s, M, K).cpu().numpy()
+    assert np.array_equal(y8, y)
+
+
 # --------------------------------------------------------------------------
 # full-size workloads, sampled rows, in the benchmark's launch configuration
 # --------------------------------------------------------------------------
