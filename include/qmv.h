@@ -441,17 +441,17 @@ int qmv_tc_probe(const int8_t* A, const int8_t* B, int N, float* Df, cudaStream_
 size_t qmv_measure_pipes_scratch_bytes(void);
 int qmv_measure_pipes(double* rates, int count, void* scratch, size_t scratch_bytes, cudaStream_t stream);
 
-/* Diagnostic (no counterpart on the pages): sets the cycle limit of the
- * consumer warps' waits for weight stages in the matvec and MoE kernels
- * launched after this returns (process-wide; cycles <= 0 restores the
- * default of about 2^31 cycles, about a second).  With a short limit a call
- * whose weight stages arrive late gives up: the kernel returns, sets
- * QMV_DEVERR_TIMEOUT and leaves its outputs unspecified; the context stays
- * usable and the next call (with the default limit) is correct.  Only the
- * consumers' waits are shortened: the producer's waits and the waits for
- * bulk copies of activations keep the default, so no copy lands in shared
- * memory after a CTA has exited.  Exists to test that timeout path. */
-int qmv_set_consumer_wait_limit(long long cycles);
+/* Diagnostic (no counterpart on the pages): the library's bounded wait, made
+ * to run out.  Every mbarrier wait in the kernels gives up after about 2^31
+ * SM cycles (about a second), sets QMV_DEVERR_TIMEOUT and returns, so a
+ * stalled pipeline never hangs the GPU; the limit is a compile-time constant
+ * of the kernels, whose hot loops then carry no other code.  This launches
+ * one warp that runs the same wait loop, with limit_cycles (1 .. 2^31) as its
+ * limit, on an mbarrier that nothing ever completes: it gives up, sets
+ * QMV_DEVERR_TIMEOUT in the device error word and returns.  cycles (device,
+ * may be NULL) receives the SM cycles the wait lasted (at least
+ * limit_cycles).  The context stays usable. */
+int qmv_wait_probe(long long limit_cycles, unsigned long long* cycles, cudaStream_t stream);
 
 /* Synchronises `stream`, then reads and clears the device error word
  * (QMV_DEVERR_* bits, 0 if none) into *err. */

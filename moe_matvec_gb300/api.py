@@ -64,7 +64,7 @@ _SIGS = {
     "qmv_run_residual": (_int, [_int, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _vp, _sz, _vp]),
     "qmv_run_siblings": (_int, [_int, _vp, _vp, _vp, _vp, _vp, _i64, _int, _vp, _sz, _vp]),
     "qmv_get_device_error": (_int, [_vp, ctypes.POINTER(_int)]),
-    "qmv_set_consumer_wait_limit": (_int, [ctypes.c_longlong]),
+    "qmv_wait_probe": (_int, [ctypes.c_longlong, _vp, _vp]),
     "qmv_tc_probe": (_int, [_vp, _vp, _int, _vp, _vp]),
     "qmv_measure_pipes_scratch_bytes": (_sz, []),
     "qmv_measure_pipes": (_int, [ctypes.POINTER(ctypes.c_double), _int, _vp, _sz, _vp]),
@@ -369,10 +369,13 @@ def measure_pipes(stream=None) -> dict:
     return {PIPE_NAMES[i]: float(arr[i]) for i in range(n)}
 
 
-def set_consumer_wait_limit(cycles: int) -> None:
-    """Cycle limit of the kernels' consumer waits for weight stages (0: the
-    default, about a second); a diagnostic for the timeout path."""
-    _check(load().qmv_set_consumer_wait_limit(int(cycles)), "qmv_set_consumer_wait_limit")
+def wait_probe(limit_cycles: int, stream=None) -> int:
+    """Runs the kernels' bounded mbarrier wait with `limit_cycles` as its limit
+    on a barrier that never completes (qmv_wait_probe); returns the SM cycles
+    the wait lasted before it gave up.  Sets QMV_DEVERR_TIMEOUT."""
+    cyc = torch.zeros(1, dtype=torch.int64, device="cuda")
+    _check(load().qmv_wait_probe(int(limit_cycles), _ptr(cyc), _stream(stream)), "qmv_wait_probe")
+    return int(cyc.item())
 
 
 def get_device_error(stream=None) -> int:

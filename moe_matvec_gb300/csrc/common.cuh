@@ -122,55 +122,26 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
-// Bounded wait: gives up after ~2^31 SM cycles (about a second), sets the
-// timeout bit and returns false.  No wait in this library is unbounded.
+// Bounded wait: gives up after `limit` SM cycles, sets the timeout bit and
+// returns false.  No wait in this library is unbounded: the kernels use
+// mbar_wait below (about a second, a compile-time constant, so that their hot
+// loops carry no other code); the wait probe (qmv_wait_probe) runs the same
+// loop with a caller's limit on a barrier that never completes.
 constexpr long long WAIT_CYCLES = 1ll << 31;
 constexpr uint32_t WAIT_SUSPEND_NS = 1u << 20;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
+__device__ __forceinline__ bool mbar_wait_until(uint64_t* bar, uint32_t parity, unsigned* err, long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   long long t0 = clock64();
   while (!mbar_try_wait_suspend(bar, parity, WAIT_SUSPEND_NS)) {
-    if (clock64() - t0 > WAIT_CYCLES) {
+    if (clock64() - t0 > limit) {
       set_error(err, QMV_DEVERR_TIMEOUT);
       return false;
     }
   }
   return true;
 }
-
-// Non-blocking test of a phase (never suspends the thread).
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// A consumer warp's wait for a weight stage, with the caller's cycle limit
-// (a launch parameter, WAIT_CYCLES unless a test shortened it).  Below the
-// default the barrier is polled without suspending, so a short limit runs
-// out as soon as the stage is late.  Called by all lanes of the warp; the
-// verdict is the same in every lane (a stage counts as landed only if every
-// lane saw it), so the warp never splits between the barriers that follow.
-__device__ __forceinline__ bool consumer_wait(uint64_t* bar, uint32_t parity, unsigned* err, long long limit) {
-  bool ok;
-  if (limit >= WAIT_CYCLES) {
-    ok = mbar_wait(bar, parity, err);
-  } else {
-    ok = mbar_test_wait(bar, parity);
-    if (!ok) {
-      const long long t0 = clock64();
-      while (!(ok = mbar_test_wait(bar, parity)))
-        if (clock64() - t0 > limit) {
-          set_error(err, QMV_DEVERR_TIMEOUT);
-          break;
-        }
-    }
-  }
-  return __all_sync(0xffffffffu, ok);
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
+  return mbar_wait_until(bar, parity, err, WAIT_CYCLES);
 }
 
 // L2 policy for streamed weights: evict first, so activations and outputs

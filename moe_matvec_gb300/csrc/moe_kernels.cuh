@@ -41,7 +41,6 @@ struct MoeParams {
   int groups;           // K / group weights
   int stages, act_nck;
   unsigned* err;
-  long long wait;       // cycle limit of the consumers' waits for weight stages
 };
 
 // Expert groups of one launch, in shared memory.
@@ -355,7 +354,7 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, NT <= 4 && CW == CONSUMER_
     const bool active = MODE == MOE_GATE_UP ? 2 * cw < nvalid : cw * RW < nvalid;
     for (int c = 0; c < nck && alive; c++, ring.advance(p.stages)) {
       const int st = ring.st;
-      if (!consumer_wait(&full[st], ring.parity(), p.err, p.wait)) {
+      if (!mbar_wait(&full[st], ring.parity(), p.err)) {
         alive = false;
         break;
       }
@@ -369,7 +368,8 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, NT <= 4 && CW == CONSUMER_
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
-    if (!alive) continue;  // warp-uniform: the wait's verdict is the same in every lane
+    alive = __all_sync(FULL, alive);  // warp-uniform from here on
+    if (!alive) continue;
     const int row0 = u * UNIT_ROWS;
     if constexpr (NT <= 2) {
       // few values per lane: one shuffle tree each

@@ -3,7 +3,6 @@
 #include <cudaTypedefs.h>
 #include <string.h>
 
-#include <atomic>
 #include <mutex>
 
 #include <cmath>
@@ -16,10 +15,6 @@ namespace qmv {
 
 static __device__ unsigned int g_qmv_error = 0;
 
-// Cycle limit of the consumer warps' waits for weight stages, passed to every
-// matvec launch (WAIT_CYCLES unless a test shortened it with
-// qmv_set_consumer_wait_limit).
-static std::atomic<long long> g_consumer_wait{WAIT_CYCLES};
 
 // ---------------------------------------------------------------------------
 // Device facts (cached per device ordinal).
@@ -248,7 +243,6 @@ static int run_dense(int fmt, const void* W, const float* x, const int8_t* xq, c
   // there the CTAs' tiles past the ring are requested at the start of the call
   p.prefetch = M * rb <= PREFETCH_ALL_BYTES ? PREFETCH_STAGES : 0;
   p.err = device_error_word();
-  p.wait = g_consumer_wait.load(std::memory_order_relaxed);
   p.w = static_cast<const uint8_t*>(W);
   p.rb = rb;
   p.nbmax = 0;
@@ -626,7 +620,6 @@ int moe_qmv_run(const moe_experts* e, const int32_t* ids, const float* gates, co
   p.top_k = top_k;
   p.n_experts = e->n_experts;
   p.err = device_error_word();
-  p.wait = g_consumer_wait.load(std::memory_order_relaxed);
   // gate / up + SwiGLU: h [S][F]
   p.src = x;
   p.dst = h;
@@ -675,10 +668,6 @@ int qmv_check_rounding(unsigned long long* mismatches, cudaStream_t stream) {
   return launch_check_rounding(mismatches, stream) == cudaSuccess ? QMV_OK : QMV_ERR_CUDA;
 }
 
-int qmv_set_consumer_wait_limit(long long cycles) {
-  g_consumer_wait.store(cycles <= 0 || cycles > WAIT_CYCLES ? WAIT_CYCLES : cycles, std::memory_order_relaxed);
-  return QMV_OK;
-}
 
 int qmv_get_device_error(cudaStream_t stream, int* err) {
   if (!err) return QMV_ERR_NULL;

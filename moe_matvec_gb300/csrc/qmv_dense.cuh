@@ -47,7 +47,6 @@ struct DenseParams {
   int act_nck;         // chunks of the activation area
   int prefetch;        // L2 lookahead of the producer past the ring (iterations; 0: none)
   unsigned* err;       // device error word
-  long long wait;      // cycle limit of the consumers' waits for weight stages
   // used by the tensor-core kernel (qmv_mma.cuh), which copies rows itself
   const uint8_t* w;    // the weight rows
   long long rb;        // bytes per row
@@ -275,7 +274,7 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, is_float(F) ? 1 : dense_mi
         asm volatile("prefetch.global.L1 [%0];" ::"l"(p.add + (long long)(t0 + lane) * p.M + row0 + grp * RW));
     for (int c = 0; c < nck && alive; c++, ring.advance(p.stages)) {
       const int st = ring.st;
-      if (!consumer_wait(&full[st], ring.parity(), p.err, p.wait)) {
+      if (!mbar_wait(&full[st], ring.parity(), p.err)) {
         alive = false;
         break;
       }
@@ -285,8 +284,9 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, is_float(F) ? 1 : dense_mi
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
-    // a warp that gave up on a wait (alive is warp-uniform) stores nothing;
-    // with ks > 1 it still takes part in the cross-warp barriers below
+    // a warp that gave up on a wait stores nothing; with ks > 1 it still
+    // takes part in the cross-warp barriers below
+    alive = __all_sync(FULL, alive);  // warp-uniform from here on
     if (!alive && ks == 1) continue;
     // reduce across lanes and store rows row0 + grp * RW + r
     float* out = p.out + (long long)s * p.ntot * p.M;

@@ -354,7 +354,8 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
 
     for (int c = 0; c < nck && alive; c++, ring.advance(p.stages)) {
       const int st = ring.st;
-      if (!consumer_wait(&full[st], ring.parity(), p.err, p.wait)) {
+      // the stage's work is warp-wide (ldmatrix, mma.sync): the lanes vote
+      if (!__all_sync(FULL, mbar_wait(&full[st], ring.parity(), p.err))) {
         alive = false;
         break;
       }

@@ -10,6 +10,8 @@
 //     int-to-float conversion), of the legacy warp-level MMA and of tcgen05
 //     MMAs, each measured on every SM with clock64 around a fixed amount of
 //     work.  These are the denominators of the path's ALU roofline.
+//   qmv_wait_probe: the kernels' bounded mbarrier wait, run with a
+//     caller's cycle limit on a barrier that never completes.
 // Every wait is bounded; tensor memory is always released before exit.
 #include <algorithm>
 #include <vector>
@@ -292,9 +294,33 @@ static double median_rate(const std::vector<long long>& cyc, double ops) {
   return med > 0 ? ops / med : 0.0;
 }
 
+// One warp waits on an mbarrier that nothing ever completes, with the
+// library's bounded wait loop and the caller's limit (qmv_wait_probe).
+__global__ void wait_probe_kernel(long long limit, unsigned* err, unsigned long long* cycles) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const long long t0 = clock64();
+  const bool ok = mbar_wait_until(&bar, 0, err, limit);  // phase 0 never completes
+  const long long t1 = clock64();
+  if (threadIdx.x == 0 && cycles) *cycles = ok ? 0ull : (unsigned long long)(t1 - t0);
+}
+
 }  // namespace qmv
 
 using namespace qmv;
+
+extern "C" int qmv_wait_probe(long long limit_cycles, unsigned long long* cycles, cudaStream_t stream) {
+  if (limit_cycles < 1 || limit_cycles > WAIT_CYCLES) return QMV_ERR_SHAPE;
+  if (cycles && (reinterpret_cast<uintptr_t>(cycles) & 7u)) return QMV_ERR_ALIGN;
+  unsigned* err = device_error_word();
+  if (!err) return QMV_ERR_CUDA;
+  wait_probe_kernel<<<1, 32, 0, stream>>>(limit_cycles, err, cycles);
+  return cudaGetLastError() == cudaSuccess ? QMV_OK : QMV_ERR_CUDA;
+}
 
 extern "C" int qmv_tc_probe(const int8_t* A, const int8_t* B, int N, float* Df, cudaStream_t stream) {
   if (!A || !B || !Df) return QMV_ERR_NULL;

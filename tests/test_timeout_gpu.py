@@ -1,11 +1,13 @@
 """The kernels' bounded waits, made to run out on purpose.
 
-Every wait in the library has a cycle limit after which the kernel gives up,
-sets QMV_DEVERR_TIMEOUT in the device error word and returns, so a stalled
-pipeline never hangs the GPU.  qmv_set_consumer_wait_limit shortens the limit
-of the consumer warps' waits for weight stages; a bandwidth-bound matvec then
-finds a stage that has not landed yet, gives up, and the next call (with the
-default limit restored) must be correct and leave no error behind."""
+Every mbarrier wait in the library has a cycle limit after which the kernel
+gives up, sets QMV_DEVERR_TIMEOUT in the device error word and returns, so a
+stalled pipeline never hangs the GPU.  In the matvec and MoE kernels that limit
+is a compile-time constant (about a second).  qmv_wait_probe runs the same
+wait loop with a short limit on an mbarrier that nothing ever completes (a
+flag that nothing sets): the wait must give up after its limit, the call must
+return, the error must be reported, and the next matvec and MoE calls must be
+correct and leave no error behind."""
 import numpy as np
 import pytest
 import torch
@@ -17,26 +19,32 @@ from tests.gpu_util import assert_within, dev, sample_rows
 pytestmark = pytest.mark.gpu
 
 
-def test_short_consumer_wait_limit_times_out_and_the_next_call_is_correct(lib):
-    # 71 MB of Q8_0 weights at one token: the consumers outrun HBM and wait
-    # on most stages, so with a one-cycle limit some wait is late
+@pytest.mark.parametrize("limit", [1, 1 << 16, 1 << 22])
+def test_wait_on_a_barrier_nothing_completes_gives_up_after_its_limit(lib, limit):
+    assert lib.get_device_error() == 0
+    cycles = lib.wait_probe(limit)                # synchronises: the kernel returned
+    assert cycles >= limit
+    assert cycles < limit + (1 << 26)             # one suspend (about a millisecond) past the limit at most
+    assert lib.get_device_error() == api.DEVERR_TIMEOUT
+    assert lib.get_device_error() == 0            # reading the word clears it
+
+
+def test_wait_probe_rejects_limits_outside_its_range(lib):
+    for bad in (0, -5, (1 << 31) + 1):
+        with pytest.raises(api.QmvError):
+            lib.wait_probe(bad)
+    assert lib.get_device_error() == 0
+
+
+def test_matvec_after_a_timeout_is_correct(lib):
     fmt, M, K, n = 0, 4096, 16384, 1
     Wn = oracle.quantize(fmt, synth.weights(1234, M, K))
     x = synth.activations(1235, n, K)
     Wd, xd = dev(Wn), dev(x)
     y0 = lib.run(fmt, Wd, xd, M, K)
     assert lib.get_device_error() == 0
-    err = 0
-    lib.set_consumer_wait_limit(1)
-    try:
-        for _ in range(3):
-            lib.run(fmt, Wd, xd, M, K)
-            err = lib.get_device_error()      # the call returned: the stream synchronised
-            if err:
-                break
-    finally:
-        lib.set_consumer_wait_limit(0)
-    assert err == api.DEVERR_TIMEOUT
+    lib.wait_probe(1 << 20)
+    assert lib.get_device_error() == api.DEVERR_TIMEOUT
     y1 = lib.run(fmt, Wd, xd, M, K)
     assert lib.get_device_error() == 0
     assert torch.equal(y0, y1)
@@ -45,7 +53,7 @@ def test_short_consumer_wait_limit_times_out_and_the_next_call_is_correct(lib):
     assert_within(y1.cpu().numpy()[:, rows], yr, sabs, what="after the timeout")
 
 
-def test_moe_call_with_short_wait_limit_returns_and_the_next_call_is_correct(lib):
+def test_moe_after_a_timeout_is_correct(lib):
     E, H, F, top_k, n = 16, 2048, 1536, 4, 8
     Wgu = np.stack([oracle.quantize(2, synth.weights(1300 + 2 * e, 2 * F, H)) for e in range(E)])
     Wd = np.stack([oracle.quantize(1, synth.weights(1301 + 2 * e, H, F)) for e in range(E)])
@@ -57,13 +65,8 @@ def test_moe_call_with_short_wait_limit_returns_and_the_next_call_is_correct(lib
     idd, gd, xd = dev(ids), dev(gates), dev(x)
     y0 = api.moe_run(ex, idd, gd, xd, ws=ws).clone()
     assert lib.get_device_error() == 0
-    lib.set_consumer_wait_limit(1)
-    try:
-        api.moe_run(ex, idd, gd, xd, ws=ws)
-        err = lib.get_device_error()
-    finally:
-        lib.set_consumer_wait_limit(0)
-    assert err in (0, api.DEVERR_TIMEOUT)     # whether a stage was late is timing; either way it returned
+    lib.wait_probe(1 << 20)
+    assert lib.get_device_error() == api.DEVERR_TIMEOUT
     y1 = api.moe_run(ex, idd, gd, xd, ws=ws)
     assert lib.get_device_error() == 0
     assert torch.equal(y0, y1)
