@@ -255,9 +255,12 @@ static int run_dense(int fmt, const void* W, const float* x, const int8_t* xq, c
   L.pdl = true;
   // Q4_K passes of 8 or 16 token slots: the tensor-core kernel, whenever its
   // shared memory (activation area, partial sums and at least two weight
-  // stages) fits; it takes one CTA per SM.
+  // stages) fits and the matrix is tall enough to repay its larger fixed cost
+  // per call (measured on K = 5120: it overtakes the dp4a kernel from about
+  // 7000 rows at 8 tokens and 5800 rows at 16); it takes one CTA per SM.
   bool mma = false;
-  if (fmt == QMV_Q4_K && pl.nt_tmpl >= 8 && rb >= MMA_BOX_BYTES) {
+  const long long mma_min_rows = pl.nt_tmpl == 8 ? 7168 : 6144;
+  if (fmt == QMV_Q4_K && pl.nt_tmpl >= 8 && rb >= MMA_BOX_BYTES && M >= mma_min_rows) {
     const int nbmax = (int)(((p.groups + n_split - 1) / n_split) * 8);
     int st = MAX_STAGES;
     while (st >= 2 && mma_smem_bytes(pl.nt_tmpl, st, nbmax) > (size_t)device_smem_optin()) st--;

@@ -158,20 +158,14 @@ __device__ __forceinline__ void quant_units(const float4 (&v)[SU][2], uint32_t (
   for (int u = 0; u < SU; u++) {
     float f[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w, v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
     int q[8];
-    if (!slow) {
+    // The slow path clamps the integer: the conversion takes +-inf (1 / d
+    // overflows to infinity for blocks whose amax is below about 3.7e-37) to
+    // the ends of the int range and a not-a-number (0 * inf, a zero element of
+    // such a block) to 0, the codes the rule gives them.
 #pragma unroll
-      for (int k = 0; k < 8; k++) q[k] = __float2int_rn(__fmul_rn(f[k], id[u]));
-    } else {
-      // slow path (a separate loop, so the fast one carries none of it):
-      // clamp (1 / d overflows to infinity for blocks whose amax is below
-      // about 3.7e-37; a zero element then gives 0 * inf, not a number,
-      // whose code is 0)
-#pragma unroll
-      for (int k = 0; k < 8; k++) {
-        float p = __fmul_rn(f[k], id[u]);
-        p = p != p ? 0.0f : fminf(fmaxf(p, -127.0f), 127.0f);
-        q[k] = __float2int_rn(p);
-      }
+    for (int k = 0; k < 8; k++) {
+      q[k] = __float2int_rn(__fmul_rn(f[k], id[u]));
+      if (slow) q[k] = min(max(q[k], -127), 127);
     }
     w0[u] = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) | ((uint32_t)(q[2] & 0xFF) << 16) |
             ((uint32_t)q[3] << 24);

@@ -284,10 +284,16 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, is_float(F) ? 1 : dense_mi
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
     }
-    // a warp that gave up on a wait stores nothing; with ks > 1 it still
-    // takes part in the cross-warp barriers below
-    alive = __all_sync(FULL, alive);  // warp-uniform from here on
-    if (!alive && ks == 1) continue;
+    alive = __all_sync(FULL, alive);
+    if (!alive) {
+      // a warp that gave up on a wait stores nothing, but still takes part
+      // in the cross-warp barriers of a thin tile
+      if (ks > 1) {
+        named_sync(2, CONSUMER_THREADS);
+        named_sync(2, CONSUMER_THREADS);
+      }
+      continue;
+    }
     // reduce across lanes and store rows row0 + grp * RW + r
     float* out = p.out + (long long)s * p.ntot * p.M;
     constexpr int V = RW * NT, HELD = V >= 32 ? V / 32 : 1;
@@ -327,7 +333,6 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, is_float(F) ? 1 : dense_mi
           v[i] = w;
         }
       named_sync(2, CONSUMER_THREADS);  // red is free for the next tile
-      if (!alive) continue;
     }
     if (part == 0 && lead) {
 #pragma unroll

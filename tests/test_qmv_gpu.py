@@ -170,6 +170,26 @@ def test_qmv_exact_integer_sums(lib, fmt):
     assert np.array_equal(y.astype(np.float64), yr)
 
 
+@pytest.mark.parametrize("M,K,n,S", [(7171, 1024, 5, 1), (7171, 1024, 8, 1), (9000, 2048, 13, 1), (7171, 1024, 16, 1),
+                                     (7171, 1024, 33, 1), (7200, 6144, 8, 3), (8192, 1792, 16, 2)])
+def test_q4_k_tensor_core_matvec(lib, M, K, n, S):
+    # the tensor-core kernel (Q4_K, passes of 5-16 tokens, tall matrices):
+    # ragged tiles, token passes with a partial last one, split ranges with
+    # odd numbers of superblocks; every output against the oracle, the
+    # pre-quantized path bitwise equal to the fused one
+    seed = 7000 + M + K + n
+    w = synth.weights(seed, M, K)
+    x = synth.activations(seed + 1, n, K)
+    Wn = oracle.quantize(1, w)
+    Wd, xd = dev(Wn), dev(x)
+    y = lib.run(1, Wd, xd, M, K) if S == 1 else lib.splitk_run(1, Wd, xd, M, K, n_split=S)
+    yr, sabs = oracle.qmv(1, Wn, x, K)
+    assert_within(y.cpu().numpy(), yr, sabs, what=f"M{M} K{K} n{n} S{S}")
+    q, d, s = lib.quantize_act(xd)
+    if S == 1:
+        assert torch.equal(lib.run_q8(1, Wd, q, d, s, M, K), y)
+
+
 @pytest.mark.parametrize("n", [5, 8, 12, 16, 21])
 def test_q4_k_block_sums_exact_at_their_extremes(lib, n):
     # Q4_K from 5 tokens forms its block sums on the tensor cores, with the
@@ -177,7 +197,7 @@ def test_q4_k_block_sums_exact_at_their_extremes(lib, n):
     # all +-127, and the mixed rows) must still come out exact.  Scales are
     # powers of two, so the fp32 result is bit-exact in any order.
     r = np.random.default_rng(n)
-    K, M = 1024, 72
+    K, M = 1024, 8200   # tall enough for the tensor-core kernel, with a ragged last tile
     rows = []
     for m in range(M):
         row = b""
