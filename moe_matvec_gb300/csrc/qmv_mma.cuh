@@ -61,24 +61,22 @@ constexpr int MK_RW = MK_CW / 2;                   // warps whose sums one reduc
 //   codes [NT][apitch]            staged activation codes of the split range
 //                                 (the library's Q8 order, 16 bytes of padding
 //                                 per token so that 8 tokens hit 8 bank groups)
-//   tsc [nbmax][3][NT] f32        per block and token: d_x, d_x * s, -1024 * s
+//   dx [NT][dpitch] f32, xs [NT][dpitch] i32   block scales and code sums
 //   scl [12 warps][2 blocks][64 rows] float4  (a_r, a_r, -c_r, -c_r)
-//   red [6 warps][NT][72] f32     partial sums of a tile (two rounds); before that, the
-//                                 landing area of the pre-quantized scales and
-//                                 sums ([NT][dpitch] each)
+//   red [6 warps][NT][72] f32     partial sums of a tile (two rounds)
 //   mbarriers: full[8], empty[8], activation copies, first staging done
 struct MmaLayout {
-  size_t codes, tsc, scl, red, bars, total;
+  size_t codes, dx, xs, scl, red, bars, total;
   int apitch, dpitch;
   __host__ __device__ MmaLayout(int nt, int stages, int nbmax) {
     apitch = nbmax * 32 + 16;
     dpitch = nbmax + 4;
     codes = (size_t)stages * MK_STAGE;
-    tsc = codes + (size_t)nt * apitch;
-    scl = tsc + (size_t)nbmax * 3 * nt * 4;
+    dx = codes + (size_t)nt * apitch;
+    xs = dx + (size_t)nt * dpitch * 4;
+    scl = xs + (size_t)nt * dpitch * 4;
     red = scl + (size_t)MK_CW * 2 * MK_ROWS * 16;
-    const size_t sums = (size_t)MK_RW * nt * MK_RED_LD * 4, land = (size_t)2 * nt * dpitch * 4;
-    bars = red + (sums > land ? sums : land);
+    bars = red + (size_t)MK_RW * nt * MK_RED_LD * 4;
     total = bars + (2 * MAX_STAGES + 2) * 8;
   }
 };
@@ -123,24 +121,15 @@ __device__ __forceinline__ uint32_t u4x2_f16(uint32_t w) {
   return r;
 }
 
-// Per block and token, the scalars of the fold: d_x, d_x * s (the min
-// term's multiplier, the product the dp4a path forms) and -1024 * s (the MMA's
-// C operand, exact).
-__device__ __forceinline__ void mk_put_scalars(float* tsc, int nt_slots, int b, int t, float dx, int sum) {
-  float* e = tsc + (size_t)b * 3 * nt_slots + t;
-  e[0] = dx;
-  e[nt_slots] = dx * (float)sum;
-  e[2 * nt_slots] = -1024.0f * (float)sum;
-}
-
-// Token slots [nt, NT) of the scalars: zero (their sums are never stored;
-// zeros keep them finite).
+// Token slots [nt, NT) of the block scales and sums: zero (their sums are
+// never stored; zeros keep them finite).
 template <int NT>
-__device__ __forceinline__ void mk_zero_slots(float* tsc, int nt, int nblk, int tid) {
+__device__ __forceinline__ void mk_zero_slots(float* dxa, int32_t* xsa, int dpitch, int nt, int nblk, int tid) {
   const int rest = NT - nt;
   for (int i = tid; i < rest * nblk; i += MK_CW * 32) {
-    const int b = i / rest, t = nt + (i - b * rest);
-    mk_put_scalars(tsc, NT, b, t, 0.0f, 0);
+    const int t = nt + i / nblk, b = i - (t - nt) * nblk;
+    dxa[t * dpitch + b] = 0.0f;
+    xsa[t * dpitch + b] = 0;
   }
 }
 
@@ -149,7 +138,8 @@ __device__ __forceinline__ void mk_zero_slots(float* tsc, int nt, int nblk, int 
 // (quant_units, the dense path's code); codes in the library's Q8 order.
 template <int NT>
 __device__ __forceinline__ void mk_stage_fp32(const DenseParams& p, int t0, int nt, int kb0, int nblk,
-                                              uint8_t* codes, float* tsc, int apitch, int cw, int lane) {
+                                              uint8_t* codes, float* dxa, int32_t* xsa, int apitch, int dpitch,
+                                              int cw, int lane) {
   constexpr int SU = 4;
   const int sub = lane >> 2, li = lane & 3;
   const int total = nt * nblk;
@@ -178,26 +168,26 @@ __device__ __forceinline__ void mk_stage_fp32(const DenseParams& p, int t0, int 
     for (int u = 0; u < SU; u++) {
       if (real[u]) {
         *reinterpret_cast<uint2*>(codes + (size_t)tt[u] * apitch + act_pos(bb[u], 8 * li)) = make_uint2(w0[u], w1[u]);
-        if (li == 0) mk_put_scalars(tsc, NT, bb[u], tt[u], dd[u], ss[u]);
+        if (li == 0) {
+          dxa[tt[u] * dpitch + bb[u]] = dd[u];
+          xsa[tt[u] * dpitch + bb[u]] = ss[u];
+        }
       }
     }
   }
-  mk_zero_slots<NT>(tsc, nt, nblk, cw * 32 + lane);
+  mk_zero_slots<NT>(dxa, xsa, dpitch, nt, nblk, cw * 32 + lane);
 }
 
 // The same from pre-quantized rows (the library's Q8 layout): three bulk
-// copies per token (codes; scales and sums into the landing area), then the
-// scalars of the fold from the landed ones.  Warp 0 lane 0 posts the byte
+// copies per token (codes, scales, sums).  Warp 0 lane 0 posts the byte
 // count first.  Returns false (timeout bit set) if the copies never land.
 template <int NT>
 __device__ __forceinline__ bool mk_stage_q8(const DenseParams& p, int t0, int nt, int kb0, int nblk, uint8_t* codes,
-                                            float* tsc, float* land, int apitch, int dpitch, uint64_t* bar,
+                                            float* ldx, int32_t* lxs, int apitch, int dpitch, uint64_t* bar,
                                             uint32_t parity, int cw, int lane) {
-  float* ldx = land;
-  int32_t* lxs = reinterpret_cast<int32_t*>(land + (size_t)NT * dpitch);
   if (cw == 0 && lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(nt * nblk * (BLK + 8)));
-  // the landing area held the previous tile's partial sums (written and read
-  // by the generic proxy): order those accesses before the copies' writes
+  // the previous range's scales and sums were read (and its unused token
+  // slots written) by the generic proxy: order that before the copies
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   named_sync(1, MK_CW * 32);  // the byte count is posted before any copy completes
   const long long nbr = p.K / BLK;
@@ -211,13 +201,8 @@ __device__ __forceinline__ bool mk_stage_q8(const DenseParams& p, int t0, int nt
     else
       bulk_copy_g2s(lxs + t * dpitch, p.xs + row * nbr + kb0, (uint32_t)nblk * 4, bar);
   }
-  const bool ok = mbar_wait(bar, parity, p.err);
-  for (int i = cw * 32 + lane; i < nt * nblk; i += MK_CW * 32) {
-    const int t = i / nblk, b = i - t * nblk;
-    mk_put_scalars(tsc, NT, b, t, ldx[t * dpitch + b], lxs[t * dpitch + b]);
-  }
-  mk_zero_slots<NT>(tsc, nt, nblk, cw * 32 + lane);
-  return ok;
+  mk_zero_slots<NT>(ldx, lxs, dpitch, nt, nblk, cw * 32 + lane);
+  return mbar_wait(bar, parity, p.err);
 }
 
 // Fields sc_j, m_j, sc_j+1, m_j+1 (6 bits each, from bit 0) of the sub-block
@@ -237,7 +222,8 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
   const MmaLayout L(NT, p.stages, p.nbmax);
   uint8_t* stages = smem;
   uint8_t* codes = smem + L.codes;
-  float* tsc = reinterpret_cast<float*>(smem + L.tsc);
+  float* dxa = reinterpret_cast<float*>(smem + L.dx);
+  int32_t* xsa = reinterpret_cast<int32_t*>(smem + L.xs);
   float4* scl = reinterpret_cast<float4*>(smem + L.scl);
   float* red = reinterpret_cast<float*>(smem + L.red);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
@@ -332,9 +318,9 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
     if (s != staged_split) {
       named_sync(1, MK_CW * 32);  // nobody still reads the previous range (or the partial sums)
       if (!q8in) {
-        mk_stage_fp32<NT>(p, t0, ntk, kb0, nblk, codes, tsc, apitch, cw, lane);
+        mk_stage_fp32<NT>(p, t0, ntk, kb0, nblk, codes, dxa, xsa, apitch, dpitch, cw, lane);
       } else {
-        alive = __all_sync(FULL, mk_stage_q8<NT>(p, t0, ntk, kb0, nblk, codes, tsc, red, apitch, dpitch, abar,
+        alive = __all_sync(FULL, mk_stage_q8<NT>(p, t0, ntk, kb0, nblk, codes, dxa, xsa, apitch, dpitch, abar,
                                                  aphase, cw, lane)) &&
                 alive;
         aphase ^= 1;
@@ -388,7 +374,6 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
           uint32_t B[TG][4];
           float2 DX[TG], DS[TG];
           float C[TG][4];  // the MMA's C operand: -1024 s of tokens 2 t4, 2 t4 + 1 (rows g and g + 8)
-          const float* e = tsc + (size_t)kb * 3 * NT + 2 * t4;  // tokens 2 t4, 2 t4 + 1
 #pragma unroll
           for (int h = 0; h < TG; h++) {
             const uint32_t x0 = lds32(ra + h * 8 * apitch), x1 = lds32(ra + h * 8 * apitch + 128);
@@ -396,9 +381,14 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
             B[h][1] = s8x2_f16(x0 >> 8);
             B[h][2] = s8x2_f16(x1);
             B[h][3] = s8x2_f16(x1 >> 8);
-            DX[h] = *reinterpret_cast<const float2*>(e + 8 * h);
-            DS[h] = *reinterpret_cast<const float2*>(e + NT + 8 * h);
-            const float2 ns = *reinterpret_cast<const float2*>(e + 2 * NT + 8 * h);
+            // block scales and code sums of tokens 2 t4, 2 t4 + 1 of the tile:
+            // d_x, d_x * s (the min term's multiplier, the product the dp4a path
+            // forms) and -1024 * s (the MMA's C operand, exact)
+            const int tk = (8 * h + 2 * t4) * dpitch + kb;
+            DX[h] = make_float2(dxa[tk], dxa[tk + dpitch]);
+            const float2 sf = make_float2((float)xsa[tk], (float)xsa[tk + dpitch]);
+            DS[h] = __fmul2_rn(DX[h], sf);
+            const float2 ns = __fmul2_rn(sf, make_float2(-1024.0f, -1024.0f));
             C[h][0] = C[h][2] = ns.x;
             C[h][1] = C[h][3] = ns.y;
           }
