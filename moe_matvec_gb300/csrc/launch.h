@@ -37,6 +37,12 @@ cudaError_t launch_dense_f32(const DenseLaunch& L);
 // nbmax blocks.
 constexpr int MMA_BOX_BYTES = 432;
 constexpr int MMA_TILE_ROWS = 64;
+// Tensor-core F16 matvec (nt_tmpl 8 or 16; boxes of MMA_F16_BOX_BYTES x
+// MMA_TILE_ROWS / UNIT_ROWS rows) and its shared memory for split ranges of at
+// most kmax weights.
+constexpr int MMA_F16_BOX_BYTES = 528;
+cudaError_t launch_mma_f16(const DenseLaunch& L);
+size_t mma_f16_smem_bytes(int nt, int stages, int kmax);
 cudaError_t launch_mma_q4_k(const DenseLaunch& L);
 size_t mma_smem_bytes(int nt, int stages, int nbmax);
 

@@ -277,7 +277,30 @@ static int run_dense(int fmt, const void* W, const float* x, const int8_t* xq, c
       L.grid = (int)(work < device_sm_count() ? work : device_sm_count());
     }
   }
-  auto launch = [&]() { return mma ? launch_mma_q4_k(L) : launch_dense_any(fmt, L); };
+  // F16 rows, passes of 8 or 16 token slots: the tensor-core F16 kernel when
+  // the split range's two f16 parts of the activations fit beside at least
+  // two weight stages, and the matrix is tall enough for its fixed cost
+  bool mma_f16 = false;
+  if (fmt == QMV_F16 && pl.nt_tmpl >= 8 && rb >= MMA_F16_BOX_BYTES && M >= 4096) {
+    const int kmax = (int)(((p.groups + n_split - 1) / n_split) * 32);
+    int st = MAX_STAGES;
+    while (st >= 2 && mma_f16_smem_bytes(pl.nt_tmpl, st, kmax) > (size_t)device_smem_optin()) st--;
+    CUtensorMap mt, mu;
+    if (st >= 2 && encode_rows(&mt, W, M, rb, MMA_F16_BOX_BYTES, MMA_TILE_ROWS) &&
+        encode_rows(&mu, W, M, rb, MMA_F16_BOX_BYTES, UNIT_ROWS)) {
+      mma_f16 = true;
+      L.map_tile = mt;
+      L.map_unit = mu;
+      p.nbmax = kmax / 32;
+      p.stages = st;
+      L.smem = mma_f16_smem_bytes(pl.nt_tmpl, st, kmax);
+      const long long work = (long long)p.units * n_split;
+      L.grid = (int)(work < device_sm_count() ? work : device_sm_count());
+    }
+  }
+  auto launch = [&]() {
+    return mma ? launch_mma_q4_k(L) : (mma_f16 ? launch_mma_f16(L) : launch_dense_any(fmt, L));
+  };
   // the full token passes in one launch (grid y), so that they run side by
   // side, and a last partial pass in a second one
   const int full = n_tok / pl.nt_tmpl, rem = n_tok - full * pl.nt_tmpl;

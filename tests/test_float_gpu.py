@@ -132,3 +132,40 @@ def test_float_full_size_sampled(lib, fmt, n):
     yr, sabs = oracle.qmv(fmt, Wn[rows], x, K)
     assert_within(y[:, rows], yr, sabs, what=f"fmt{fmt} n{n} S{S}")
     assert np.all(np.isfinite(y))
+
+
+@pytest.mark.parametrize("M,K,n,S", [(4200, 2048, 16, 0), (4200, 2048, 8, 0), (5000, 3072, 12, 0),
+                                     (4104, 1056, 21, 2), (6000, 5120, 16, 0)])
+def test_f16_tensor_core_matvec(lib, M, K, n, S):
+    # F16 rows, passes of 5-16 tokens, tall matrices, split ranges: the
+    # tensor-core kernel (activations scaled per token by a power of two and
+    # split into two f16 parts).  Tokens over a wide range of magnitudes, a
+    # zero token, special weights; every output against the oracle.
+    seed = 5000 + M + K + n
+    w = _weights(oracle.F16, M, K, seed)
+    x = synth.activations(seed + 1, n, K)
+    x[1] *= np.float32(1e-30)
+    x[2] *= np.float32(1e30)
+    x[3] = 0.0
+    x[4, :100] *= np.float32(1e-20)      # small elements beside large ones in one range
+    Wn = oracle.quantize(oracle.F16, w)
+    y = lib.splitk_run(oracle.F16, dev(Wn), dev(x), M, K, n_split=S).cpu().numpy()
+    yr, sabs = oracle.qmv(oracle.F16, Wn, x, K)
+    assert np.all(np.isfinite(y))
+    assert_within(y, yr, sabs, what=f"F16 M{M} K{K} n{n} S{S}")
+    assert np.all(y[3] == 0.0)
+
+
+def test_f16_tensor_core_exact_sums(lib):
+    # weights k * 2^-6 and activations j * 2^-3 (as the exact-sum test
+    # above) on a tall matrix: the tensor-core kernel's products and fp32
+    # accumulation are exact, so the result is bit for bit the oracle's
+    r = np.random.default_rng(11)
+    M, K, n = 4200, 2048, 16
+    w = (r.integers(-60, 61, (M, K)) * 2.0 ** -6).astype(np.float32)
+    x = (r.integers(-100, 101, (n, K)) * 2.0 ** -3).astype(np.float32)
+    Wn = oracle.quantize(oracle.F16, w)
+    yr, sabs = oracle.qmv(oracle.F16, Wn, x, K)
+    assert np.all(sabs < 2.0 ** 24 * 2.0 ** -9)
+    y = lib.splitk_run(oracle.F16, dev(Wn), dev(x), M, K, n_split=0).cpu().numpy()
+    assert np.array_equal(y.astype(np.float64), yr)
