@@ -328,6 +328,11 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, NT <= 4 && CW == CONSUMER_
     for (int r = 0; r < RW; r++) roff[r] = cw * RW + r;
   }
   const int nblk = p.K / BLK;
+  // rows whose length is 512 past a multiple of 1024 (the down projection of
+  // an FFN of 1536) end in a half chunk; the tiles of 8 and 16 tokens split it
+  // between lane pairs (at fewer tokens the extra code spills registers and
+  // costs more than the zero fill it saves)
+  const bool half_last = NT >= 8 && p.K % KCHUNK == KCHUNK / 2;
 
   while (walk.next(q, u, nu)) {
     if (q != staged_pair) {
@@ -362,8 +367,17 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, NT <= 4 && CW == CONSUMER_
         // GATE_UP: rows (2cw, 2cw + 1) of the gate half and the same of the
         // up half, 16 rows apart; DOWN: 4 consecutive rows
         constexpr int PS = (MODE == MOE_GATE_UP ? HALF : 2) * CB;
-        cons.template chunk<PS>(stage_base + st * STAGE_BYTES + roff[0] * CB, aq_base + c * NT * ACT_BYTES,
-                                ad_base + c * NT * 128, as_base + c * NT * 128, nt, acc);
+        const uint32_t rows = stage_base + st * STAGE_BYTES + roff[0] * CB;
+        if (MODE == MOE_DOWN && NT >= 8 && half_last && c == nck - 1) {
+          // the last 512 weights of the rows: a half chunk, each block split
+          // between two lanes (no lane works on zero fill)
+          const Consumer<F, NT> ch(lane & 15);
+          ch.template chunk_half<PS>(lane >> 4, rows, aq_base + c * NT * ACT_BYTES, ad_base + c * NT * 128,
+                                     as_base + c * NT * 128, nt, acc);
+        } else {
+          cons.template chunk<PS>(rows, aq_base + c * NT * ACT_BYTES, ad_base + c * NT * 128,
+                                  as_base + c * NT * 128, nt, acc);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);

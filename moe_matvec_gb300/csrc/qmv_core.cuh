@@ -630,6 +630,121 @@ struct Consumer {
     }
   }
 
+  // The same step over a half chunk: the last 16 blocks of a row whose
+  // length is 512 past a multiple of 1024 (the MoE down projection's 1536),
+  // where a whole-chunk step would leave half of the lanes decoding and
+  // multiplying zero fill.  Here every block is split between two lanes:
+  // lane l < 16 takes weights 0..15 of block l (operand words 0..3 with
+  // activation group xa), lane l + 16 weights 16..31 (words 4..7 with xb).
+  // The consumer must have been built for block lane % 16; h = lane / 16.
+  // Each half's integer sum is exact and scaled by the block's scales as in
+  // chunk(); the block's min term is added by its h = 0 lane only.  The
+  // lanes' sums meet in the caller's cross-lane reduction as before.
+  template <int PAIR_STRIDE = 2 * chunk_bytes<F>()>
+  __device__ __forceinline__ void chunk_half(int h, uint32_t row0, uint32_t aq, uint32_t ad, uint32_t as, int nt,
+                                             AccTile<NT>& acc) const {
+    static_assert(F == QMV_Q8_0 || F == QMV_Q4_K || F == QMV_IQ4_XS, "the expert formats");
+    constexpr uint32_t sq = ACT_BYTES, sd = 32 * 4;
+    constexpr int CB = chunk_bytes<F>();
+    uint32_t w[RW][4];  // decoded operands of the lane's half, paired with activation words 4h..4h+3
+    float sA[RW], sB[RW];
+#pragma unroll
+    for (int r = 0; r < RW; r++) {
+      const uint32_t row = row0 + (r & 1) * CB + (r >> 1) * PAIR_STRIDE;
+      if constexpr (F == QMV_Q8_0) {
+        const uint4 x = lds128(row + w_off + 128 * h);
+        w[r][0] = x.x; w[r][1] = x.y; w[r][2] = x.z; w[r][3] = x.w;
+        const uint32_t hw = lds32(row + (h_off & ~3u));
+        sA[r] = __half2float(__ushort_as_half((unsigned short)((h_off & 2) ? hw >> 16 : hw & 0xFFFF)));
+        sB[r] = 0.f;
+      } else if constexpr (F == QMV_Q4_K) {
+        const uint32_t dh = lds32(row + h_off);  // d | dmin
+        const uint32_t f0 = lds32(row + f_off);
+        const uint32_t f1 = lds32(row + f_off + 4);
+        const uint4 q = lds128(row + w_off);
+        const uint32_t qq[4] = {q.x, q.y, q.z, q.w};
+        // both halves as 16 x code (h = 0: the low nibbles shifted up); sA
+        // carries the 1/16 as in chunk()
+#pragma unroll
+        for (int i = 0; i < 4; i++) w[r][i] = (h == 0 ? qq[i] << 4 : qq[i]) & 0xF0F0F0F0u;
+        const uint32_t f = __funnelshift_r(f0, f1, fsh);
+        const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&dh));
+        sA[r] = dd.x * (float)(f & 63u) * 0.0625f;
+        sB[r] = h == 0 ? dd.y * (float)((f >> 6) & 63u) : 0.f;
+      } else {
+        const uint32_t dw = lds32(row + h_off);
+        const uint32_t f0 = lds32(row + f_off);
+        const uint32_t f1 = lds32(row + f_off + 4);
+        const uint2 q = lds64(row + w_off + 8 * h);  // payload words 2h, 2h + 1
+        const int ls = (int)(__funnelshift_r(f0, f1, fsh) & 63u);
+        sA[r] = __half2float(__ushort_as_half((unsigned short)(dw & 0xFFFF))) * (float)(ls - 32);
+        sB[r] = 0.f;
+        const uint32_t qq[2] = {q.x, q.y};
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+          const uint32_t pw = qq[i];
+          const uint32_t pl = pw & 0x77777777u;
+          const uint32_t p4 = pw << 4;
+          w[r][2 * i] = iq4_lookup4(pl, pw, p4, 0xD9C8u, cb);
+          w[r][2 * i + 1] = iq4_lookup4(pl >> 16, pw, p4, 0xFBEAu, cb);
+        }
+      }
+    }
+    const uint32_t ap = aq + a_off + 128 * h, dp = ad + d_off, sp = as + d_off;
+    if constexpr (NT == 1) {
+      const uint4 x = lds128(ap);
+      const float dx = __uint_as_float(lds32(dp));
+      float dxs = 0.f;
+      if constexpr (has_min(F)) dxs = dx * (float)(int)lds32(sp);
+#pragma unroll
+      for (int r = 0; r < RW; r++) {
+        float v = fmaf(sA[r] * dx, (float)dot_half(w[r], x), acc.v[r][0].x);
+        if constexpr (has_min(F)) v = fmaf(-sB[r], dxs, v);
+        acc.v[r][0].x = v;
+      }
+    } else {
+      float2 sA2[RW], nsB2[RW];
+#pragma unroll
+      for (int r = 0; r < RW; r++) {
+        sA2[r] = make_float2(sA[r], sA[r]);
+        nsB2[r] = make_float2(-sB[r], -sB[r]);
+      }
+#pragma unroll
+      for (int t = 0; t < NT; t += 2) {
+        if (t >= nt) break;
+        const uint4 x0 = lds128(ap + t * sq);
+        const uint4 x1 = lds128(ap + (t + 1) * sq);
+        const float2 dx = make_float2(__uint_as_float(lds32(dp + t * sd)), __uint_as_float(lds32(dp + (t + 1) * sd)));
+        float2 dxs = make_float2(0.f, 0.f);
+        if constexpr (has_min(F))
+          dxs = __fmul2_rn(dx, make_float2((float)(int)lds32(sp + t * sd), (float)(int)lds32(sp + (t + 1) * sd)));
+#pragma unroll
+        for (int r = 0; r < RW; r++) {
+          const float2 is = make_float2((float)dot_half(w[r], x0), (float)dot_half(w[r], x1));
+          float2 v = __ffma2_rn(__fmul2_rn(sA2[r], dx), is, acc.v[r][t >> 1]);
+          if constexpr (has_min(F)) v = __ffma2_rn(nsB2[r], dxs, v);
+          acc.v[r][t >> 1] = v;
+        }
+      }
+    }
+  }
+
+  // Exact int32 dot product of one half block (four operand words) with its
+  // four activation words (Q4_K: 16 x the sum, unsigned codes).
+  __device__ __forceinline__ int dot_half(const uint32_t (&w)[4], uint4 x) const {
+    if constexpr (F == QMV_Q4_K) {
+      int s = dp4a_us(w[0], x.x, 0);
+      s = dp4a_us(w[1], x.y, s);
+      s = dp4a_us(w[2], x.z, s);
+      return dp4a_us(w[3], x.w, s);
+    } else {
+      int s = __dp4a((int)w[0], (int)x.x, 0);
+      s = __dp4a((int)w[1], (int)x.y, s);
+      s = __dp4a((int)w[2], (int)x.z, s);
+      return __dp4a((int)w[3], (int)x.w, s);
+    }
+  }
+
   // The block's integer dot product with its sub-scales applied (Q6_K: two
   // halves of 16 weights, each with its own integer scale; other formats
   // have one scale per block, carried in sA, and ignore lo / hi).
