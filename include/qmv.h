@@ -181,13 +181,15 @@ enum qmv_status {
   QMV_ERR_ALIGN = -5,     /* a pointer is not 16-byte aligned */
   QMV_ERR_WORKSPACE = -6, /* workspace too small */
   QMV_ERR_CUDA = -7,      /* a CUDA runtime call or launch failed */
-  QMV_ERR_DEVICE = -8     /* no usable sm_103 device */
+  QMV_ERR_DEVICE = -8,    /* no usable sm_103 device */
+  QMV_ERR_UNAVAILABLE = -9 /* the call needs a build this library was not made as */
 };
 
 /* Device error word bits (qmv_get_device_error). */
 #define QMV_DEVERR_EXPERT_RANGE 0x1 /* an expert id outside [0, n_experts) */
 #define QMV_DEVERR_EXPERT_DUP 0x2   /* an expert id repeated within a token */
 #define QMV_DEVERR_TIMEOUT 0x4      /* a pipeline wait exceeded its limit */
+#define QMV_DEVERR_RANGE 0x8        /* debug build: an access failed its range check (and was skipped) */
 
 #define QMV_MAX_TOKENS 64
 #define QMV_MAX_PREFILL_TOKENS 16384 /* moe_qmv_prefill_run */
@@ -452,6 +454,21 @@ int qmv_measure_pipes(double* rates, int count, void* scratch, size_t scratch_by
  * may be NULL) receives the SM cycles the wait lasted (at least
  * limit_cycles).  The context stays usable. */
 int qmv_wait_probe(long long limit_cycles, unsigned long long* cycles, cudaStream_t stream);
+
+/* Debug builds (the library compiled with QMV_DEBUG, e.g. by the package's
+ * build(debug=True)) check every global access of the kernels against the
+ * extent of its buffer, which the host derives from the call's arguments
+ * (y: n_tok x M, the split partials, the workspace parts, ...), and every
+ * shared-memory access against the CTA's allocation; an access that fails
+ * its check is skipped and sets QMV_DEVERR_RANGE.  This stands in for a
+ * memory checker: no check traps.  This call makes every later call hand the
+ * extents of its result buffers (y, logits, ids, gates, the quantizers'
+ * outputs; not the workspace) to those checks n elements short (n = 0
+ * restores them), so that in-bounds stores near the end fail their checks:
+ * a test of the checks that touches no memory out of bounds (the stores into
+ * the results' last n elements are then skipped).  Release builds:
+ * QMV_ERR_UNAVAILABLE.  Not thread-safe with respect to calls in flight. */
+int qmv_debug_shrink_outputs(int64_t n);
 
 /* Synchronises `stream`, then reads and clears the device error word
  * (QMV_DEVERR_* bits, 0 if none) into *err. */

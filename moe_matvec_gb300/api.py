@@ -8,6 +8,7 @@ library raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -28,6 +29,7 @@ MAX_TOPK = 8
 DEVERR_EXPERT_RANGE = 0x1
 DEVERR_EXPERT_DUP = 0x2
 DEVERR_TIMEOUT = 0x4
+DEVERR_RANGE = 0x8
 
 
 class QmvError(RuntimeError):
@@ -64,6 +66,7 @@ _SIGS = {
     "qmv_run_residual": (_int, [_int, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _vp, _sz, _vp]),
     "qmv_run_siblings": (_int, [_int, _vp, _vp, _vp, _vp, _vp, _i64, _int, _vp, _sz, _vp]),
     "qmv_get_device_error": (_int, [_vp, ctypes.POINTER(_int)]),
+    "qmv_debug_shrink_outputs": (_int, [_i64]),
     "qmv_wait_probe": (_int, [ctypes.c_longlong, _vp, _vp]),
     "qmv_tc_probe": (_int, [_vp, _vp, _int, _vp, _vp]),
     "qmv_measure_pipes_scratch_bytes": (_sz, []),
@@ -75,14 +78,9 @@ _SIGS = {
 _lib = None
 
 
-def load(path: str | None = None):
-    """Load (building first if needed) libqmv.so and declare its signatures."""
-    global _lib
-    if _lib is not None:
-        return _lib
-    path = path or _build.build()
+def _open(path: str):
     if not os.path.exists(path):
-        raise ImportError(f"libqmv.so not found at {path}")
+        raise ImportError(f"library not found at {path}")
     lib = ctypes.CDLL(path)
     for name, (res, args) in _SIGS.items():
         fn = getattr(lib, name, None)
@@ -90,8 +88,49 @@ def load(path: str | None = None):
             continue
         fn.restype = res
         fn.argtypes = args
-    _lib = lib
     return lib
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) libqmv.so and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    _lib = _open(path or _build.build())
+    return _lib
+
+
+_debug_lib = None
+
+
+def load_debug():
+    """The QMV_DEBUG build of the library (libqmv_debug.so: every kernel access
+    range-checked in software, see qmv_debug_shrink_outputs in qmv.h), built if
+    needed.  It is not made the current library: run calls through it with
+    `using(load_debug())`."""
+    global _debug_lib
+    if _debug_lib is None:
+        _debug_lib = _open(_build.build(debug=True))
+    return _debug_lib
+
+
+@contextlib.contextmanager
+def using(lib):
+    """Within the block, every call of this module goes to `lib` (a library
+    from load() or load_debug())."""
+    global _lib
+    prev = load()
+    _lib = lib
+    try:
+        yield lib
+    finally:
+        _lib = prev
+
+
+def debug_shrink_outputs(n: int) -> None:
+    """Debug library only (inside `using(load_debug())`): later calls hand the
+    range checks their result buffers' extents n elements short (0 restores)."""
+    _check(load().qmv_debug_shrink_outputs(int(n)), "qmv_debug_shrink_outputs")
 
 
 def strerror(code: int) -> str:

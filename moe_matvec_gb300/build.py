@@ -2,7 +2,9 @@
 
 Every .cu unit under csrc/ is compiled in parallel, then linked into
 moe_matvec_gb300/_build/libqmv.so.  Rebuilds only when a source is newer than
-the library."""
+the library.  build(debug=True) compiles the same sources with QMV_DEBUG (the
+kernels' software range checks, see qmv_debug_shrink_outputs in qmv.h) into
+moe_matvec_gb300/_build_debug/libqmv_debug.so."""
 from __future__ import annotations
 
 import concurrent.futures as cf
@@ -17,6 +19,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libqmv.so")
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(BUILD_DEBUG, "libqmv_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
           "-I", os.path.join(ROOT, "include")]
@@ -40,22 +44,25 @@ def _deps():
         os.path.join(ROOT, "include", "qmv.h")]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(debug: bool = False) -> bool:
+    lib = LIB_DEBUG if debug else LIB
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, debug: bool = False) -> str:
+    lib, bdir = (LIB_DEBUG, BUILD_DEBUG) if debug else (LIB, BUILD)
+    if not force and up_to_date(debug):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
+    flags = COMMON + (["-DQMV_DEBUG"] if debug else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *COMMON, "-c", src, "-o", obj]
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *ARCH, *flags, "-c", src, "-o", obj]
         if os.path.basename(src) in NO_FMAD:
             cmd.insert(1, "-fmad=false")
         if ptxas_info:
@@ -72,15 +79,14 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         for _, err in results:
             if err:
                 sys.stderr.write(err)
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = lib + f".{os.getpid()}.tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp] + [o for o, _ in results] + ["-lcudart"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True, ptxas_info="-v" in sys.argv)
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="-v" in sys.argv, debug="--debug" in sys.argv))

@@ -80,6 +80,63 @@ __device__ __forceinline__ void set_error(unsigned* err, unsigned bits) {
 }
 
 // ---------------------------------------------------------------------------
+// Software range checks (builds with QMV_DEBUG defined).
+// ---------------------------------------------------------------------------
+// A checked access tests its index against a bound that does not come from
+// the kernel's own tiling: a global buffer against the extent the host
+// derived from the call's arguments, a dynamic shared-memory address against
+// the CTA's allocation (%dynamic_smem_size), a static shared array against
+// its declared length.  A failed check sets QMV_DEVERR_RANGE and the access
+// is skipped; nothing traps.
+// Every check is written QMV_CHECK(in_range(...)) (or smem_in_range,
+// in_array), and the extents and the parameters that carry them are written
+// QMV_DEBUG_ONLY(...).  In release builds QMV_CHECK is the literal true and
+// QMV_DEBUG_ONLY drops its argument, so not even the checks' arguments reach
+// the compiler: the release kernels' parameter blocks and code are those of
+// a library without checks.
+#ifdef QMV_DEBUG
+#define QMV_DEBUG_ONLY(...) __VA_ARGS__
+#define QMV_CHECK(...) (__VA_ARGS__)
+#else
+#define QMV_DEBUG_ONLY(...)
+#define QMV_CHECK(...) true
+#endif
+
+// elements [i, i + n) of a buffer of len elements
+__device__ __forceinline__ bool in_range(long long i, long long n, long long len, unsigned* err) {
+  if (i >= 0 && n >= 0 && i <= len - n) return true;
+  set_error(err, QMV_DEVERR_RANGE);
+  return false;
+}
+
+// index i of a static (shared-memory) array of N elements
+template <class T, int N>
+__device__ __forceinline__ bool in_array(const T (&)[N], long long i, unsigned* err) {
+  return in_range(i, 1, N, err);
+}
+
+__device__ __forceinline__ uint32_t dynamic_smem_size() {
+  uint32_t r;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(r));
+  return r;
+}
+
+// shared-window address of the CTA's dynamic shared memory
+__device__ __forceinline__ uint32_t dynamic_smem_base() {
+  extern __shared__ __align__(16) uint8_t qmv_dynamic_smem[];
+  return static_cast<uint32_t>(__cvta_generic_to_shared(qmv_dynamic_smem));
+}
+
+// bytes [addr, addr + n) (a shared-window address) inside the CTA's dynamic
+// shared memory
+__device__ __forceinline__ bool smem_in_range(uint32_t addr, uint32_t n, unsigned* err) {
+  return in_range((long long)addr - (long long)dynamic_smem_base(), n, dynamic_smem_size(), err);
+}
+__device__ __forceinline__ bool smem_in_range(const void* p, uint32_t n, unsigned* err) {
+  return smem_in_range(static_cast<uint32_t>(__cvta_generic_to_shared(p)), n, err);
+}
+
+// ---------------------------------------------------------------------------
 // Shared-memory address helpers and mbarriers.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -98,6 +155,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Completes `bytes` of the current phase's expected transaction count without
+// a copy: a copy skipped by a failed range check still lets the phase end.
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;

@@ -71,7 +71,8 @@ cudaError_t launch_moe_combine(const int32_t* ids, const float* gates, const flo
 
 cudaError_t launch_route_topk(const float* logits, int n_tok, int E, int top_k, int gating, int32_t* ids,
                               float* gates, cudaStream_t stream, bool pdl);
-cudaError_t launch_act_quant(const float* x, int K, int n_tok, int8_t* q, float* d, int32_t* s,
+// q_len: the extent (elements) of q for the range checks (d, s: q_len / 32)
+cudaError_t launch_act_quant(const float* x, int K, int n_tok, int8_t* q, float* d, int32_t* s, long long q_len,
                              cudaStream_t stream, bool pdl);
 cudaError_t launch_splitk_reduce(const float* partial, float* y, const float* add, long long M, int n_tok, int n_split,
                                  cudaStream_t stream, bool pdl);
@@ -86,6 +87,11 @@ bool encode_rows(CUtensorMap* map, const void* W, long long rows, long long row_
 // Maximum dynamic shared memory a CTA may use on the current device.
 int device_smem_optin();
 unsigned* device_error_word();  // address of the device error word (current device)
+// Extent (elements) that the range checks of QMV_DEBUG builds take for a
+// result buffer of the caller (y, logits, ids, gates, quantizer outputs) of
+// n elements: n, or n less the amount set by qmv_debug_shrink_outputs (never
+// below 0).  Workspace buffers always take their full extents.
+long long output_extent(long long n);
 int device_sm_count();
 
 // Fill a launch config with the optional programmatic-dependent-launch

@@ -41,6 +41,12 @@ struct MoeParams {
   int groups;           // K / group weights
   int stages, act_nck;
   unsigned* err;
+  // QMV_DEBUG builds: extents of the buffers (elements), derived on the host
+  // from the call's arguments, for the range checks
+  QMV_DEBUG_ONLY(long long ids_len;  // ids: n_tok * top_k
+                 long long src_len;  // GATE_UP x: n_tok * K; DOWN h: S * K
+                 long long dst_len;  // S * R
+                 long long hq_len;)  // DOWN: S * K (0 for GATE_UP)
 };
 
 // Expert groups of one launch, in shared memory.
@@ -87,21 +93,24 @@ __device__ __forceinline__ void build_routing(MoeRouting& rt, const MoeParams& p
   const int E = p.n_experts;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   // one coalesced read of ids; every later look-up is in shared memory
-  for (int s = threadIdx.x; s < S; s += blockDim.x) rt.ids[s] = p.ids[s];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) rt.mask[e] = 0ull;
+  for (int s = threadIdx.x; s < S; s += blockDim.x)
+    rt.ids[s] = QMV_CHECK(in_array(rt.ids, s, p.err)) && QMV_CHECK(in_range(s, 1, p.ids_len, p.err)) ? p.ids[s] : -1;
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    if (QMV_CHECK(in_array(rt.mask, e, p.err))) rt.mask[e] = 0ull;
   __syncthreads();
   for (int s = threadIdx.x; s < S; s += blockDim.x) {
     const int st = slot_status(rt.ids, p.top_k, E, s);
-    if (st == 0)
-      atomicOr(&rt.mask[rt.ids[s]], 1ull << (s / p.top_k));
-    else if (report)
+    if (st == 0) {
+      if (QMV_CHECK(in_array(rt.mask, rt.ids[s], p.err))) atomicOr(&rt.mask[rt.ids[s]], 1ull << (s / p.top_k));
+    } else if (report) {
       set_error(p.err, (unsigned)st);
+    }
   }
   __syncthreads();
   int carry_s = 0, carry_p = 0, carry_w = 0;  // the same in every thread
   for (int base = 0; base < E; base += nwarps * 32) {
     const int e = base + warp * 32 + lane;
-    const int c = e < E ? __popcll(rt.mask[e]) : 0;
+    const int c = e < E && QMV_CHECK(in_array(rt.mask, e, p.err)) ? __popcll(rt.mask[e]) : 0;
     const int ng = (c + nt_group - 1) / nt_group;
     // work of the expert's groups: ng - 1 full ones and the rest
     const int w = ng == 0 ? 0
@@ -118,7 +127,7 @@ __device__ __forceinline__ void build_routing(MoeRouting& rt, const MoeParams& p
         cw += d;
       }
     }
-    if (lane == 31) {
+    if (lane == 31 && QMV_CHECK(in_array(rt.wsum, warp, p.err))) {
       rt.wsum[warp][0] = cs;
       rt.wsum[warp][1] = cp;
       rt.wsum[warp][2] = cw;
@@ -136,12 +145,13 @@ __device__ __forceinline__ void build_routing(MoeRouting& rt, const MoeParams& p
       carry_p += tp;
       carry_w += tw;
     }
-    if (e < E) {
+    if (e < E && QMV_CHECK(in_array(rt.off, e, p.err))) {
       const int off = ps + cs - c, poff = pp + cp - ng;
       int wacc = pw + cw - w;
       rt.off[e] = off;
       for (int g = 0; g < ng; g++) {
         const int cg = min(nt_group, c - g * nt_group);
+        if (!QMV_CHECK(in_array(rt.pair_expert, poff + g, p.err))) continue;
         rt.pair_expert[poff + g] = e;
         rt.pair_first[poff + g] = off + g * nt_group;
         rt.pair_count[poff + g] = cg;
@@ -152,14 +162,15 @@ __device__ __forceinline__ void build_routing(MoeRouting& rt, const MoeParams& p
     __syncthreads();  // wsum is read before the next round writes it
   }
   if (threadIdx.x == 0) {
-    rt.n_pairs = carry_p;
-    rt.pair_cost[carry_p] = carry_w;
+    // every index the walk reads (pair_cost[0 .. n_pairs]) is at most n_pairs
+    rt.n_pairs = QMV_CHECK(in_array(rt.pair_cost, carry_p, p.err)) ? carry_p : 0;
+    if (QMV_CHECK(in_array(rt.pair_cost, carry_p, p.err))) rt.pair_cost[carry_p] = carry_w;
   }
   for (int s = threadIdx.x; s < S; s += blockDim.x) {
     if (slot_status(rt.ids, p.top_k, E, s) == 0) {
       const int e = rt.ids[s], t = s / p.top_k;
       const int rank = __popcll(rt.mask[e] & ((1ull << t) - 1ull));
-      rt.slots[rt.off[e] + rank] = s;
+      if (QMV_CHECK(in_array(rt.slots, rt.off[e] + rank, p.err))) rt.slots[rt.off[e] + rank] = s;
     }
   }
   __syncthreads();
@@ -270,7 +281,7 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, NT <= 4 && CW == CONSUMER_
       Ring ring;
       bool alive = true;
       while (alive && walk.next(q, u, nu)) {
-        const int base = rt.pair_expert[q] * p.pool_rows;
+        const int base = (QMV_CHECK(in_array(rt.pair_expert, q, p.err)) ? rt.pair_expert[q] : 0) * p.pool_rows;
         for (int c = 0; c < nck; c++, ring.advance(p.stages)) {
           if (!producer_acquire(empty, ring, p.stages, p.err)) {
             alive = false;
@@ -279,7 +290,9 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, NT <= 4 && CW == CONSUMER_
           const int st = ring.st;
           uint8_t* dst = stages + st * STAGE_BYTES;
           const int x = c * CB / 8;
-          if constexpr (MODE == MOE_GATE_UP) {
+          if (!QMV_CHECK(smem_in_range(dst, MODE == MOE_GATE_UP ? (HALF + nu * UNIT_ROWS) * CB : nu * UNIT_ROWS * CB, p.err))) {
+            mbar_arrive(&full[st]);  // skipped: the stage completes without data
+          } else if constexpr (MODE == MOE_GATE_UP) {
             mbar_arrive_expect_tx(&full[st], 2 * nu * UNIT_ROWS * CB);
             for (int i = 0; i < nu; i++) {
               const int j = (u + i) * UNIT_ROWS;
@@ -336,15 +349,17 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, NT <= 4 && CW == CONSUMER_
 
   while (walk.next(q, u, nu)) {
     if (q != staged_pair) {
-      first = rt.pair_first[q];
-      nt = rt.pair_count[q];
+      first = QMV_CHECK(in_array(rt.pair_first, q, p.err)) ? rt.pair_first[q] : 0;
+      nt = QMV_CHECK(in_array(rt.pair_count, q, p.err)) ? rt.pair_count[q] : 0;
       named_sync(1, CONSUMER_THREADS);
-      if (threadIdx.x < nt) {
+      if (threadIdx.x < nt && QMV_CHECK(in_array(rt.slots, first + threadIdx.x, p.err)) &&
+          QMV_CHECK(in_array(s_rows, threadIdx.x, p.err))) {
         const int slot = rt.slots[first + threadIdx.x];
         s_rows[threadIdx.x] = MODE == MOE_GATE_UP ? slot / p.top_k : slot;
       }
       named_sync(1, CONSUMER_THREADS);
-      ActSource src{p.src, nullptr, nullptr, nullptr, p.K, s_rows, 0, nullptr, nullptr, nullptr};
+      ActSource src{p.src, nullptr, nullptr, nullptr, p.K, s_rows, 0, nullptr, nullptr, nullptr
+                    QMV_DEBUG_ONLY(, p.src_len, p.hq_len, p.err)};
       if (MODE == MOE_DOWN && u == 0) {  // the CTA that owns the group's first unit publishes q8(h)
         src.wq = p.hq;
         src.wd = p.hd;
@@ -368,7 +383,10 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, NT <= 4 && CW == CONSUMER_
         // up half, 16 rows apart; DOWN: 4 consecutive rows
         constexpr int PS = (MODE == MOE_GATE_UP ? HALF : 2) * CB;
         const uint32_t rows = stage_base + st * STAGE_BYTES + roff[0] * CB;
-        if (MODE == MOE_DOWN && NT >= 8 && half_last && c == nck - 1) {
+        if (!QMV_CHECK(chunk_reads_in_range<F, NT>(rows, PS + 2 * CB, aq_base + c * NT * ACT_BYTES,
+                                                   ad_base + c * NT * 128, as_base + c * NT * 128, p.err))) {
+          // skipped (QMV_DEBUG builds only)
+        } else if (MODE == MOE_DOWN && NT >= 8 && half_last && c == nck - 1) {
           // the last 512 weights of the rows: a half chunk, each block split
           // between two lanes (no lane works on zero fill)
           const Consumer<F, NT> ch(lane & 15);
@@ -385,6 +403,10 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, NT <= 4 && CW == CONSUMER_
     alive = __all_sync(FULL, alive);  // warp-uniform from here on
     if (!alive) continue;
     const int row0 = u * UNIT_ROWS;
+    // (QMV_DEBUG builds) element i of the output row of group slot si lies in dst
+    QMV_DEBUG_ONLY(auto dst_ok = [&](int si, long long i) {
+      return in_array(rt.slots, si, p.err) && in_range((long long)rt.slots[si] * p.R + i, 1, p.dst_len, p.err);
+    };)
     if constexpr (NT <= 2) {
       // few values per lane: one shuffle tree each
 #pragma unroll
@@ -398,14 +420,14 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, NT <= 4 && CW == CONSUMER_
             const int j = 2 * cw + i;
             if (lane == ((2 * t + i) & 31) && j < nvalid) {
               const float h = g / (1.0f + expf(-g)) * v;
-              p.dst[(long long)rt.slots[first + t] * p.R + row0 + j] = h;
+              if (QMV_CHECK(dst_ok(first + t, row0 + j))) p.dst[(long long)rt.slots[first + t] * p.R + row0 + j] = h;
             }
           }
         } else {
 #pragma unroll
           for (int r = 0; r < RW; r++) {
             const float v = warp_sum(acc.get(r, t));
-            if (lane == ((r * NT + t) & 31) && roff[r] < nvalid)
+            if (lane == ((r * NT + t) & 31) && roff[r] < nvalid && QMV_CHECK(dst_ok(first + t, row0 + roff[r])))
               p.dst[(long long)rt.slots[first + t] * p.R + row0 + roff[r]] = v;
           }
         }
@@ -431,10 +453,11 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, NT <= 4 && CW == CONSUMER_
           const int j = 2 * cw + r;
           if (lead && lane < 16 && t < nt && j < nvalid) {
             const float g = v[i];
-            p.dst[(long long)rt.slots[first + t] * p.R + row0 + j] = g / (1.0f + expf(-g)) * up;
+            if (QMV_CHECK(dst_ok(first + t, row0 + j)))
+              p.dst[(long long)rt.slots[first + t] * p.R + row0 + j] = g / (1.0f + expf(-g)) * up;
           }
         } else {
-          if (lead && t < nt && roff[r] < nvalid)
+          if (lead && t < nt && roff[r] < nvalid && QMV_CHECK(dst_ok(first + t, row0 + roff[r])))
             p.dst[(long long)rt.slots[first + t] * p.R + row0 + roff[r]] = v[i];
         }
       }

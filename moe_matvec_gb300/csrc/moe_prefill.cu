@@ -76,6 +76,11 @@ struct PrefillParams {
   int32_t* hs;
   float* o;           // down output [S][H]
   unsigned* err;
+  // QMV_DEBUG builds: extents of the buffers (elements), derived on the host
+  // from the call's arguments, for the range checks
+  QMV_DEBUG_ONLY(long long bq_len;     // codes: gate/up n_tok * H, down S * F (bd, bs: bq_len / 32)
+                 long long out_len;    // gate/up h, hq: S * F (hd, hs: out_len / 32); down o: S * H
+                 long long list_len;)  // list: S (cnt, off: E)
 };
 
 // ---------------------------------------------------------------------------
@@ -95,7 +100,9 @@ __device__ __forceinline__ int pf_slot_state(const int32_t* ids, int top_k, int 
 
 __global__ void __launch_bounds__(256) prefill_route_kernel(const int32_t* __restrict__ ids, int n_tok, int top_k,
                                                             int E, int* __restrict__ cnt, int* __restrict__ off,
-                                                            int* __restrict__ list, unsigned* err) {
+                                                            int* __restrict__ list, unsigned* err
+                                                                QMV_DEBUG_ONLY(, long long ids_len, long long cnt_len,
+                                                                               long long list_len)) {
   const int e = blockIdx.x, S = n_tok * top_k;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __shared__ int wc[8][2];
@@ -104,7 +111,7 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(const int32_t* __res
   for (int s0 = 0; s0 < S; s0 += 256) {
     const int s = s0 + threadIdx.x;
     bool eq = false, lt = false;
-    if (s < S) {
+    if (s < S && QMV_CHECK(in_range(s, 1, ids_len, err))) {  // (the reads are ids[t top_k .. s])
       int id;
       const int st = pf_slot_state(ids, top_k, E, s, id);
       if (st && e == 0) set_error(err, (unsigned)st);
@@ -112,7 +119,7 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(const int32_t* __res
       lt = st == 0 && id < e;
     }
     const unsigned beq = __ballot_sync(FULL, eq), blt = __ballot_sync(FULL, lt);
-    if (lane == 0) {
+    if (lane == 0 && QMV_CHECK(in_array(wc, warp, err))) {
       wc[warp][0] = __popc(beq);
       wc[warp][1] = __popc(blt);
     }
@@ -123,7 +130,7 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(const int32_t* __res
     }
     __syncthreads();
   }
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && QMV_CHECK(in_range(e, 1, cnt_len, err))) {
     cnt[e] = n_eq;
     off[e] = n_lt;
   }
@@ -132,19 +139,20 @@ __global__ void __launch_bounds__(256) prefill_route_kernel(const int32_t* __res
   for (int s0 = 0; s0 < S && base < n_lt + n_eq; s0 += 256) {
     const int s = s0 + threadIdx.x;
     bool eq = false;
-    if (s < S) {
+    if (s < S && QMV_CHECK(in_range(s, 1, ids_len, err))) {
       int id;
       eq = pf_slot_state(ids, top_k, E, s, id) == 0 && id == e;
     }
     const unsigned beq = __ballot_sync(FULL, eq);
-    if (lane == 0) wc[warp][0] = __popc(beq);
+    if (lane == 0 && QMV_CHECK(in_array(wc, warp, err))) wc[warp][0] = __popc(beq);
     __syncthreads();
     int pre = 0, tot = 0;
     for (int w = 0; w < 8; w++) {
       pre += w < warp ? wc[w][0] : 0;
       tot += wc[w][0];
     }
-    if (eq) list[base + pre + __popc(beq & ((1u << lane) - 1u))] = s;
+    if (eq && QMV_CHECK(in_range(base + pre + __popc(beq & ((1u << lane) - 1u)), 1, list_len, err)))
+      list[base + pre + __popc(beq & ((1u << lane) - 1u))] = s;
     base += tot;
     __syncthreads();
   }
@@ -367,30 +375,31 @@ __global__ void __launch_bounds__(PF_ALL, 1)
   {
     int c0 = 0, c1 = 0;
     const int e0 = 2 * tid, e1 = 2 * tid + 1;
-    if (!issuer && e0 < p.E) c0 = mtiles * ((p.cnt[e0] + PF_N - 1) / PF_N);
-    if (!issuer && e1 < p.E) c1 = mtiles * ((p.cnt[e1] + PF_N - 1) / PF_N);
+    if (!issuer && e0 < p.E && QMV_CHECK(in_range(e0, 1, p.E, p.err))) c0 = mtiles * ((p.cnt[e0] + PF_N - 1) / PF_N);
+    if (!issuer && e1 < p.E && QMV_CHECK(in_range(e1, 1, p.E, p.err))) c1 = mtiles * ((p.cnt[e1] + PF_N - 1) / PF_N);
     int v = c0 + c1, incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int a = __shfl_up_sync(FULL, incl, o);
       if (lane >= o) incl += a;
     }
-    if (lane == 31) s_part[warp] = incl;
+    if (lane == 31 && QMV_CHECK(in_array(s_part, warp, p.err))) s_part[warp] = incl;
     __syncthreads();
     int before = 0;
     for (int w = 0; w < warp; w++) before += s_part[w];
     const int excl = before + incl - v;
     if (!issuer) {
-      if (e0 <= p.E) prefix[e0] = excl;
-      if (e1 <= p.E) prefix[e1] = excl + c0;
-      if (tid == PF_DEC - 1 && 2 * PF_DEC <= p.E) prefix[p.E] = before + incl;  // E = 512
+      if (e0 <= p.E && QMV_CHECK(in_array(prefix, e0, p.err))) prefix[e0] = excl;
+      if (e1 <= p.E && QMV_CHECK(in_array(prefix, e1, p.err))) prefix[e1] = excl + c0;
+      if (tid == PF_DEC - 1 && 2 * PF_DEC <= p.E && QMV_CHECK(in_array(prefix, p.E, p.err)))
+        prefix[p.E] = before + incl;  // E = 512
     }
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tslot;
-  const int total = prefix[p.E];
+  const int total = QMV_CHECK(in_array(prefix, p.E, p.err)) ? prefix[p.E] : 0;
   const long long i0 = (long long)total * blockIdx.x / gridDim.x, i1 = (long long)total * (blockIdx.x + 1) / gridDim.x;
 
   // a decode thread's weight row and epilogue place
@@ -425,13 +434,17 @@ __global__ void __launch_bounds__(PF_ALL, 1)
       else
         hi = mid;
     }
-    const int e = lo, cnt_e = p.cnt[e];
+    // (the search reads prefix[1 .. E - 1], the item's expert prefix[e] and p.cnt[e], e < E)
+    const int e = lo, cnt_e = QMV_CHECK(in_range(e, 1, p.E, p.err)) ? p.cnt[e] : 0;
     const int ntl = (cnt_e + PF_N - 1) / PF_N;
     const int idx = (int)(item - prefix[e]), mt = idx / ntl, nt = idx - mt * ntl;
     const int count = min(PF_N, cnt_e - nt * PF_N);
     const int nmma = (count + 15) & ~15;
     __syncthreads();  // the previous item's readers of s_slot, the stages and the up sums are done
-    if (tid < PF_N) s_slot[tid] = tid < count ? p.list[p.off[e] + nt * PF_N + tid] : -1;
+    if (tid < PF_N) {
+      const long long li = tid < count && QMV_CHECK(in_range(e, 1, p.E, p.err)) ? (long long)p.off[e] + nt * PF_N + tid : -1;
+      s_slot[tid] = li >= 0 && QMV_CHECK(in_range(li, 1, p.list_len, p.err)) ? p.list[li] : -1;
+    }
     __syncthreads();
     const int j0 = mt * PF_M;
     const long long base = it, ubase = ut;  // this item's first K step and unit
@@ -442,6 +455,10 @@ __global__ void __launch_bounds__(PF_ALL, 1)
         auto issue_w = [&](int u, int st) {
           uint8_t* sp = stg + st * SG::BYTES;
           mbar_arrive_expect_tx(&full[st], (uint32_t)(SG::W_BYTES + count * (128 + 16 + (FM::MIN ? 16 : 0))));
+          if (!QMV_CHECK(smem_in_range(sp, SG::W_BYTES, p.err))) {
+            mbar_complete_tx(&full[st], SG::W_BYTES);  // skipped: the phase still completes
+            return;
+          }
           const int g = (PF_UB * u) / FM::BPG, jj0 = (PF_UB * u) % FM::BPG;
 #pragma unroll
           for (int a = 0; a < NA; a++) {
@@ -490,19 +507,30 @@ __global__ void __launch_bounds__(PF_ALL, 1)
         if (!cact) return;
         uint8_t* sp = stg + st * SG::BYTES;
         const int kd = MODE == PF_GATE_UP ? ckind : (ckind == 0 ? 0 : ckind + 1);  // 0 lo, 1 hi, 2 d, 3 s
+        // one copy: global element gi of codes (kd <= 1) or of scales / sums, to dst
+        long long gi;
+        uint8_t* dst;
+        uint32_t bytes;
         if (kd <= 1) {
-          const int8_t* src = p.bq + crow * (long long)p.K;
-          uint8_t* cd = sp + SG::W_BYTES + cslot * 128;
-          if (MODE == PF_GATE_UP)  // library layout: elements 0-15 of the unit's blocks, then 16-31 (128 further)
-            bulk_copy_g2s(cd + 64 * kd, src + (u >> 1) * 256 + (u & 1) * 64 + 128 * kd, 64, &full[st]);
-          else
-            bulk_copy_g2s(cd, src + u * 128, 128, &full[st]);
-        } else if (kd == 2) {
-          bulk_copy_g2s(sp + SG::W_BYTES + SG::CODES + cslot * 16, p.bd + crow * (p.K / 32) + PF_UB * u, 16, &full[st]);
+          // gate/up: the library layout, elements 0-15 of the unit's blocks, then 16-31 (128 further)
+          gi = crow * (long long)p.K + (MODE == PF_GATE_UP ? (u >> 1) * 256 + (u & 1) * 64 + 128 * kd : u * 128);
+          dst = sp + SG::W_BYTES + cslot * 128 + (MODE == PF_GATE_UP ? 64 * kd : 0);
+          bytes = MODE == PF_GATE_UP ? 64 : 128;
         } else {
-          bulk_copy_g2s(sp + SG::W_BYTES + SG::CODES + SG::SC + cslot * 16, p.bs + crow * (p.K / 32) + PF_UB * u, 16,
-                        &full[st]);
+          gi = crow * (p.K / 32) + PF_UB * u;
+          dst = sp + SG::W_BYTES + SG::CODES + (kd == 3 ? SG::SC : 0) + cslot * 16;
+          bytes = 16;
         }
+        if (!QMV_CHECK(in_range(gi, kd <= 1 ? bytes : bytes / 4, kd <= 1 ? p.bq_len : p.bq_len / 32, p.err)) || !QMV_CHECK(smem_in_range(dst, bytes, p.err))) {
+          mbar_complete_tx(&full[st], bytes);  // skipped: the phase still completes
+          return;
+        }
+        if (kd <= 1)
+          bulk_copy_g2s(dst, p.bq + gi, bytes, &full[st]);
+        else if (kd == 2)
+          bulk_copy_g2s(dst, p.bd + gi, bytes, &full[st]);
+        else
+          bulk_copy_g2s(dst, p.bs + gi, bytes, &full[st]);
       };
       for (int u = 0; u < NST - 1 && u < nU; u++) issue_c(u, (int)((ubase + u) % NST));
       // B staging: slot tile row n, core matrix q (K positions 8q .. 8q + 7)
@@ -532,38 +560,44 @@ __global__ void __launch_bounds__(PF_ALL, 1)
           }
           if (cur >= PF_NBUF) pw(&mma_done[buf], (uint32_t)(((cur - PF_NBUF) / PF_NBUF) & 1));
           // ---- decode the weights of block k into the A tile ----
-          const uint4 hdr = *reinterpret_cast<const uint4*>(sp + SG::hdr(atile) + arow * 16);
+          const uint8_t* hp = sp + SG::hdr(atile) + arow * 16;
+          const uint4 hdr = QMV_CHECK(smem_in_range(hp, 16, p.err)) ? *reinterpret_cast<const uint4*>(hp) : make_uint4(0, 0, 0, 0);
           const int jj = k % FM::BPG;
           float sA, sB;
           pf_scales<F>(hdr, jj, sA, sB);
           uint8_t* at = a_buf + (buf * NA + atile) * PF_A_TILE;
+          // a 16-byte load from the stage and a 16-byte store into the A tile
+          auto ld16 = [&](const uint8_t* q) {
+            return QMV_CHECK(smem_in_range(q, 16, p.err)) ? *reinterpret_cast<const uint4*>(q) : make_uint4(0, 0, 0, 0);
+          };
+          auto st16 = [&](uint8_t* q, uint4 v) {
+            if (QMV_CHECK(smem_in_range(q, 16, p.err))) *reinterpret_cast<uint4*>(q) = v;
+          };
           if (HALF) {
-            const uint4 pay =
-                *reinterpret_cast<const uint4*>(sp + SG::pay(0, SG::NPIECE == 2 ? ahalf : 0) + arow * 64 + 16 * l);
+            const uint4 pay = ld16(sp + SG::pay(0, SG::NPIECE == 2 ? ahalf : 0) + arow * 64 + 16 * l);
             uint32_t o[8];
             pf_decode_half<F>(pay, ahalf, cb, o);
-            *reinterpret_cast<uint4*>(at + tc::kmajor_offset(arow, 32 * ahalf, 64)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(at + tc::kmajor_offset(arow, 32 * ahalf + 16, 64)) =
-                make_uint4(o[4], o[5], o[6], o[7]);
+            st16(at + tc::kmajor_offset(arow, 32 * ahalf, 64), make_uint4(o[0], o[1], o[2], o[3]));
+            st16(at + tc::kmajor_offset(arow, 32 * ahalf + 16, 64), make_uint4(o[4], o[5], o[6], o[7]));
           } else {
 #pragma unroll
             for (int hv = 0; hv < 2; hv++) {
-              const uint4 pay =
-                  *reinterpret_cast<const uint4*>(sp + SG::pay(atile, SG::NPIECE == 2 ? hv : 0) + arow * 64 + 16 * l);
+              const uint4 pay = ld16(sp + SG::pay(atile, SG::NPIECE == 2 ? hv : 0) + arow * 64 + 16 * l);
               uint32_t o[8];
               pf_decode_half<F>(pay, hv, cb, o);
-              *reinterpret_cast<uint4*>(at + tc::kmajor_offset(arow, 32 * hv, 64)) = make_uint4(o[0], o[1], o[2], o[3]);
-              *reinterpret_cast<uint4*>(at + tc::kmajor_offset(arow, 32 * hv + 16, 64)) =
-                  make_uint4(o[4], o[5], o[6], o[7]);
+              st16(at + tc::kmajor_offset(arow, 32 * hv, 64), make_uint4(o[0], o[1], o[2], o[3]));
+              st16(at + tc::kmajor_offset(arow, 32 * hv + 16, 64), make_uint4(o[4], o[5], o[6], o[7]));
             }
           }
           if (!HALF || ahalf == 0) {
-            ring_sa[slot * NA * PF_M + atile * PF_M + arow] = sA;
-            if constexpr (FM::MIN) ring_sb[slot * NA * PF_M + atile * PF_M + arow] = sB;
+            const int ri = slot * NA * PF_M + atile * PF_M + arow;
+            if (QMV_CHECK(smem_in_range(ring_sa + ri, 4, p.err))) ring_sa[ri] = sA;
+            if constexpr (FM::MIN)
+              if (QMV_CHECK(smem_in_range(ring_sb + ri, 4, p.err))) ring_sb[ri] = sB;
           }
           // ---- the activation codes of block k into the B tile ----
           uint4 v = make_uint4(0, 0, 0, 0);
-          if (bval) {
+          if (bval && QMV_CHECK(smem_in_range(sp + SG::W_BYTES + bn * 128, 128, p.err))) {  // the slot's codes
             const uint8_t* cr = sp + SG::W_BYTES + bn * 128;
             uint32_t x0, x1;
             if (FM::INTERLEAVED) {  // elements 4q .. 4q+3 and 16+4q .. 16+4q+3
@@ -582,16 +616,18 @@ __global__ void __launch_bounds__(PF_ALL, 1)
             v = make_uint4(tc::s8x2_to_f16x2(x0), tc::s8x2_to_f16x2(x0 >> 16), tc::s8x2_to_f16x2(x1),
                            tc::s8x2_to_f16x2(x1 >> 16));
           }
-          *reinterpret_cast<uint4*>(b_buf + buf * PF_B_TILE + tc::kmajor_offset(bn, 16 * bqq, 64)) = v;
+          st16(b_buf + buf * PF_B_TILE + tc::kmajor_offset(bn, 16 * bqq, 64), v);
           if (tid < PF_N) {
             float dx = 0.f, dxs = 0.f;
-            if (tid < count) {
-              dx = reinterpret_cast<const float*>(sp + SG::W_BYTES + SG::CODES)[tid * 4 + l];
+            const float* dp = reinterpret_cast<const float*>(sp + SG::W_BYTES + SG::CODES) + tid * 4 + l;
+            const int* sq = reinterpret_cast<const int*>(sp + SG::W_BYTES + SG::CODES + SG::SC) + tid * 4 + l;
+            if (tid < count && QMV_CHECK(smem_in_range(dp, 4, p.err))) {
+              dx = *dp;
               if constexpr (FM::MIN)
-                dxs = dx * (float)reinterpret_cast<const int*>(sp + SG::W_BYTES + SG::CODES + SG::SC)[tid * 4 + l];
+                if (QMV_CHECK(smem_in_range(sq, 4, p.err))) dxs = dx * (float)*sq;
             }
-            ring_dx[slot * PF_N + tid] = dx;
-            ring_dxs[slot * PF_N + tid] = dxs;
+            if (QMV_CHECK(smem_in_range(ring_dx + slot * PF_N + tid, 4, p.err))) ring_dx[slot * PF_N + tid] = dx;
+            if (QMV_CHECK(smem_in_range(ring_dxs + slot * PF_N + tid, 4, p.err))) ring_dxs[slot * PF_N + tid] = dxs;
           }
           tc::fence_smem_to_async();
           mbar_arrive(&tile_full[buf]);
@@ -606,11 +642,12 @@ __global__ void __launch_bounds__(PF_ALL, 1)
           __syncwarp();  // the TMEM loads below are warp-aligned instructions
           const int a_ep = MODE == PF_GATE_UP ? wh : 0;
           const uint32_t tcol = tmem + ((uint32_t)(32 * q4) << 16) + (uint32_t)(pbuf * TB + a_ep * PF_N + en0);
-          const float sa = ring_sa[pslot * NA * PF_M + a_ep * PF_M + erow];
+          const int ri = pslot * NA * PF_M + a_ep * PF_M + erow;
+          const float sa = QMV_CHECK(smem_in_range(ring_sa + ri, 4, p.err)) ? ring_sa[ri] : 0.f;
           const float2 sa2 = make_float2(sa, sa);
           float2 nsb2 = make_float2(0.f, 0.f);
           if constexpr (FM::MIN) {
-            const float sb = ring_sb[pslot * NA * PF_M + a_ep * PF_M + erow];
+            const float sb = QMV_CHECK(smem_in_range(ring_sb + ri, 4, p.err)) ? ring_sb[ri] : 0.f;
             nsb2 = make_float2(-sb, -sb);
           }
           const float* dxp = ring_dx + pslot * PF_N + en0;
@@ -618,7 +655,7 @@ __global__ void __launch_bounds__(PF_ALL, 1)
           auto scale_into = [&](const float (&D)[32], int a0, int nv) {
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
-              if (i < nv) {
+              if (i < nv && QMV_CHECK(smem_in_range(dxp + a0 + i, 8, p.err)) && QMV_CHECK(smem_in_range(dxsp + a0 + i, 8, p.err))) {
                 const float2 dx = *reinterpret_cast<const float2*>(dxp + a0 + i);
                 float2 r = __ffma2_rn(__fmul2_rn(sa2, dx), make_float2(D[i], D[i + 1]),
                                       make_float2(acc[a0 + i], acc[a0 + i + 1]));
@@ -665,7 +702,9 @@ __global__ void __launch_bounds__(PF_ALL, 1)
 #pragma unroll
         for (int i = 0; i < 32; i++) {
           if (i >= ecnt) break;  // warp-uniform
-          p.o[(long long)s_slot[en0 + i] * p.R + j] = acc[i];
+          if (!QMV_CHECK(in_array(s_slot, en0 + i, p.err))) continue;
+          const long long oi = (long long)s_slot[en0 + i] * p.R + j;
+          if (QMV_CHECK(in_range(oi, 1, p.out_len, p.err))) p.o[oi] = acc[i];
         }
       } else {
         // gate/up: the up sums to the gate warps through shared memory (the
@@ -675,7 +714,7 @@ __global__ void __launch_bounds__(PF_ALL, 1)
 #pragma unroll
           for (int i = 0; i < 64; i++) {
             if (i >= count) break;  // warp-uniform
-            up[i * PF_M + erow] = acc[i];
+            if (QMV_CHECK(smem_in_range(up + i * PF_M + erow, 4, p.err))) up[i * PF_M + erow] = acc[i];
           }
         }
         named_sync(1, PF_DEC);
@@ -684,10 +723,11 @@ __global__ void __launch_bounds__(PF_ALL, 1)
 #pragma unroll
           for (int i = 0; i < 64; i++) {
             if (i >= count) break;  // warp-uniform
-            const long long sl = s_slot[i];
-            const float g = acc[i], uu = up[i * PF_M + erow];
+            const long long sl = QMV_CHECK(in_array(s_slot, i, p.err)) ? s_slot[i] : 0;
+            const float g = acc[i], uu = QMV_CHECK(smem_in_range(up + i * PF_M + erow, 4, p.err)) ? up[i * PF_M + erow] : 0.f;
+            const bool put_ok = QMV_CHECK(in_range(sl * F_ + j, 1, p.out_len, p.err));
             const float hv = g / (1.0f + expf(-g)) * uu;
-            p.h[sl * F_ + j] = hv;
+            if (put_ok) p.h[sl * F_ + j] = hv;
             // the activation rule over the warp's 32 consecutive j (one block)
             const unsigned ab = __float_as_uint(fabsf(hv));
             const float amax = __uint_as_float(__reduce_max_sync(FULL, ab));
@@ -697,8 +737,8 @@ __global__ void __launch_bounds__(PF_ALL, 1)
             pq = pq != pq ? 0.0f : fminf(fmaxf(pq, -127.0f), 127.0f);
             const int q = __float2int_rn(pq);
             const int s = __reduce_add_sync(FULL, q);
-            p.hq[sl * F_ + j] = (int8_t)q;
-            if (lane == 0) {
+            if (put_ok) p.hq[sl * F_ + j] = (int8_t)q;
+            if (lane == 0 && QMV_CHECK(in_range(sl * (F_ / 32) + j / 32, 1, p.out_len / 32, p.err))) {
               p.hd[sl * (F_ / 32) + j / 32] = d;
               p.hs[sl * (F_ / 32) + j / 32] = s;
             }
@@ -837,9 +877,11 @@ extern "C" int moe_qmv_prefill_run(const moe_experts* e, const int32_t* ids, con
   const int E = e->n_experts, H = e->hidden, F = e->ffn;
   unsigned* err = device_error_word();
 
-  prefill_route_kernel<<<E, 256, 0, stream>>>(ids, n_tok, top_k, E, cnt, offs, list, err);
+  const long long S = (long long)n_tok * top_k;
+  prefill_route_kernel<<<E, 256, 0, stream>>>(ids, n_tok, top_k, E, cnt, offs, list, err QMV_DEBUG_ONLY(, S, E, S));
   if (cudaGetLastError() != cudaSuccess) return QMV_ERR_CUDA;
-  if (launch_act_quant(x, H, n_tok, xq, xd, xs, stream, false) != cudaSuccess) return QMV_ERR_CUDA;
+  if (launch_act_quant(x, H, n_tok, xq, xd, xs, (long long)n_tok * H, stream, false) != cudaSuccess)
+    return QMV_ERR_CUDA;
 
   const int grid = device_sm_count();
   PrefillParams p{};
@@ -850,6 +892,7 @@ extern "C" int moe_qmv_prefill_run(const moe_experts* e, const int32_t* ids, con
   p.off = offs;
   p.list = list;
   p.err = err;
+  QMV_DEBUG_ONLY(p.list_len = S;)
   // gate / up + SwiGLU + the activation rule on h
   p.W = static_cast<const uint8_t*>(e->w_gate_up);
   p.rb = qmv_row_bytes(e->fmt_gate_up, H);
@@ -863,6 +906,7 @@ extern "C" int moe_qmv_prefill_run(const moe_experts* e, const int32_t* ids, con
   p.hq = hq;
   p.hd = hd;
   p.hs = hs;
+  QMV_DEBUG_ONLY(p.bq_len = (long long)n_tok * H; p.out_len = S * F;)
   if (launch_prefill_fmt<PF_GATE_UP>(e->fmt_gate_up, p, grid, stream) != cudaSuccess) return QMV_ERR_CUDA;
   // down
   PrefillParams pd = p;
@@ -875,6 +919,7 @@ extern "C" int moe_qmv_prefill_run(const moe_experts* e, const int32_t* ids, con
   pd.bd = hd;
   pd.bs = hs;
   pd.o = o;
+  QMV_DEBUG_ONLY(pd.bq_len = S * F; pd.out_len = S * H;)
   if (launch_prefill_fmt<PF_DOWN>(e->fmt_down, pd, grid, stream) != cudaSuccess) return QMV_ERR_CUDA;
   return launch_moe_combine(ids, gates, o, y, n_tok, top_k, E, H, stream, false) == cudaSuccess ? QMV_OK
                                                                                                  : QMV_ERR_CUDA;

@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include <cmath>
@@ -56,6 +57,12 @@ unsigned* device_error_word() {
 int device_sm_count() {
   const DevInfo* d = dev_info();
   return d ? d->sms : 1;
+}
+
+static std::atomic<long long> g_output_shrink{0};
+long long output_extent(long long n) {
+  const long long v = n - g_output_shrink.load(std::memory_order_relaxed);
+  return v > 0 ? v : 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -246,6 +253,10 @@ static int run_dense(int fmt, const void* W, const float* x, const int8_t* xq, c
   p.w = static_cast<const uint8_t*>(W);
   p.rb = rb;
   p.nbmax = 0;
+  // y is the caller's result; split partials live in the workspace
+  QMV_DEBUG_ONLY(p.x_len = (long long)n_tok * K;
+                 p.out_len = n_split == 1 ? output_extent((long long)n_tok * M) : (long long)n_split * n_tok * M;
+                 p.add_len = p.add ? (long long)n_tok * M : 0;)
   L.p = &p;
   L.nt_tmpl = pl.nt_tmpl;
   L.cw = pl.cw;
@@ -440,7 +451,10 @@ int qmv_quantize_act(const float* x, int64_t K, int n_tok, int8_t* q, float* d, 
   if (!aligned16(x) || !aligned16(q) || !aligned16(d) || !aligned16(sum)) return QMV_ERR_ALIGN;
   int rc = check_device();
   if (rc) return rc;
-  return launch_act_quant(x, (int)K, n_tok, q, d, sum, stream, true) == cudaSuccess ? QMV_OK : QMV_ERR_CUDA;
+  return launch_act_quant(x, (int)K, n_tok, q, d, sum, output_extent((long long)n_tok * K), stream, true) ==
+                 cudaSuccess
+             ? QMV_OK
+             : QMV_ERR_CUDA;
 }
 
 int qmv_run(int fmt, const void* W, const float* x, float* y, int64_t M, int64_t K, int n_tok,
@@ -533,7 +547,8 @@ static int splitk_impl(int fmt, const void* W, const float* x, const float* add,
     int8_t* q = reinterpret_cast<int8_t*>(base);
     float* d = reinterpret_cast<float*>(base + align256((size_t)n_tok * (size_t)K));
     int32_t* sm = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(d) + align256(nb * 4));
-    if (launch_act_quant(x, (int)K, n_tok, q, d, sm, stream, true) != cudaSuccess) return QMV_ERR_CUDA;
+    if (launch_act_quant(x, (int)K, n_tok, q, d, sm, (long long)n_tok * K, stream, true) != cudaSuccess)
+      return QMV_ERR_CUDA;
     xq = q;
     xd = d;
     xs = sm;
@@ -588,7 +603,8 @@ int qmv_run_siblings(int count, const int* fmts, const void* const* W, const int
   int8_t* q = reinterpret_cast<int8_t*>(base);
   float* d = reinterpret_cast<float*>(base + align256((size_t)n_tok * (size_t)K));
   int32_t* sm = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(d) + align256(nb * 4));
-  if (launch_act_quant(x, (int)K, n_tok, q, d, sm, stream, true) != cudaSuccess) return QMV_ERR_CUDA;
+  if (launch_act_quant(x, (int)K, n_tok, q, d, sm, (long long)n_tok * K, stream, true) != cudaSuccess)
+    return QMV_ERR_CUDA;
   for (int i = 0; i < count; i++) {
     rc = is_float(fmts[i]) ? run_dense(fmts[i], W[i], x, nullptr, nullptr, nullptr, y[i], M[i], K, n_tok, 1, stream)
                            : run_dense(fmts[i], W[i], nullptr, q, d, sm, y[i], M[i], K, n_tok, 1, stream);
@@ -641,17 +657,20 @@ int moe_qmv_run(const moe_experts* e, const int32_t* ids, const float* gates, co
   if (n_tok >= 4 && nt < 8) nt = 8;
 
   MoeParams p{};
+  const long long S = (long long)n_tok * top_k;
   p.ids = ids;
   p.n_tok = n_tok;
   p.top_k = top_k;
   p.n_experts = e->n_experts;
   p.err = device_error_word();
+  QMV_DEBUG_ONLY(p.ids_len = S;)
   // gate / up + SwiGLU: h [S][F]
   p.src = x;
   p.dst = h;
   p.K = e->hidden;
   p.R = e->ffn;
   p.pool_rows = 2 * e->ffn;
+  QMV_DEBUG_ONLY(p.src_len = (long long)n_tok * e->hidden; p.dst_len = S * e->ffn; p.hq_len = 0;)
   if ((rc = run_moe_proj(MOE_GATE_UP, e->fmt_gate_up, e->w_gate_up, p, nt, stream))) return rc;
   // down (h quantized while staging, published to the workspace): o [S][H]
   MoeParams pd = p;
@@ -663,6 +682,7 @@ int moe_qmv_run(const moe_experts* e, const int32_t* ids, const float* gates, co
   pd.K = e->ffn;
   pd.R = e->hidden;
   pd.pool_rows = e->hidden;
+  QMV_DEBUG_ONLY(pd.src_len = S * e->ffn; pd.dst_len = S * e->hidden; pd.hq_len = S * e->ffn;)
   if ((rc = run_moe_proj(MOE_DOWN, e->fmt_down, e->w_down, pd, nt, stream))) return rc;
   return launch_moe_combine(ids, gates, o, y, n_tok, top_k, e->n_experts, e->hidden, stream, true) == cudaSuccess
              ? QMV_OK
@@ -695,6 +715,17 @@ int qmv_check_rounding(unsigned long long* mismatches, cudaStream_t stream) {
 }
 
 
+int qmv_debug_shrink_outputs(int64_t n) {
+#ifdef QMV_DEBUG
+  if (n < 0) return QMV_ERR_SHAPE;
+  g_output_shrink.store(n, std::memory_order_relaxed);
+  return QMV_OK;
+#else
+  (void)n;
+  return QMV_ERR_UNAVAILABLE;
+#endif
+}
+
 int qmv_get_device_error(cudaStream_t stream, int* err) {
   if (!err) return QMV_ERR_NULL;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return QMV_ERR_CUDA;
@@ -716,6 +747,7 @@ const char* qmv_strerror(int code) {
     case QMV_ERR_WORKSPACE: return "workspace too small";
     case QMV_ERR_CUDA: return "CUDA runtime error";
     case QMV_ERR_DEVICE: return "no usable sm_103 device";
+    case QMV_ERR_UNAVAILABLE: return "not available in this build";
   }
   return "unknown status";
 }

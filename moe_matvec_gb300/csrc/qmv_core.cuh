@@ -94,6 +94,18 @@ struct ActArea {
   __device__ __forceinline__ int scale(int c, int t) const { return (c * ns + t) * 32; }
 };
 
+// The shared-memory ranges one consumer step reads: rows_bytes of weight
+// rows from `rows`, and one chunk's activations of NT token slots (codes or
+// fp32 values at aq, scales at ad, Q4_K / Q5_K sums at as).
+template <int F, int NT>
+__device__ __forceinline__ bool chunk_reads_in_range(uint32_t rows, uint32_t rows_bytes, uint32_t aq, uint32_t ad,
+                                                     uint32_t as, unsigned* err) {
+  bool ok = smem_in_range(rows, rows_bytes, err) && smem_in_range(aq, NT * act_chunk_bytes(F), err);
+  if constexpr (!is_float(F)) ok = ok && smem_in_range(ad, NT * 128, err);
+  if constexpr (has_min(F)) ok = ok && smem_in_range(as, NT * 128, err);
+  return ok;
+}
+
 // Where the activation rows come from: fp32 rows (quantized while staging)
 // or pre-quantized rows in the library's Q8 activation layout (codes of each
 // 256-element group in act_pos order, one scale and one sum per block); token
@@ -112,6 +124,10 @@ struct ActSource {
   int8_t* wq;
   float* wd;
   int32_t* ws;
+  // QMV_DEBUG builds: extents for the range checks and the error word
+  QMV_DEBUG_ONLY(long long x_len;  // elements of x (or of xq; xd and xs hold x_len / 32)
+                 long long w_len;  // elements of wq (wd and ws hold w_len / 32)
+                 unsigned* err;)
   __device__ __forceinline__ long long row(int t) const { return rows ? (long long)rows[t] : row0 + t; }
 };
 
@@ -184,15 +200,17 @@ __device__ __forceinline__ void quant_units(const float4 (&v)[SU][2], uint32_t (
 // lanes 0, 1 of the block take the elements 16.. of lanes 2, 3.  Called by
 // full warps.
 template <int F>
-__device__ __forceinline__ void store_codes(uint8_t* chunk, int l, int li, uint32_t w0, uint32_t w1) {
+__device__ __forceinline__ void store_codes(uint8_t* chunk, int l, int li, uint32_t w0,
+                                            uint32_t w1 QMV_DEBUG_ONLY(, unsigned* err)) {
   if constexpr (F == QMV_IQ4_XS) {
     const uint32_t h0 = __shfl_xor_sync(FULL, w0, 2), h1 = __shfl_xor_sync(FULL, w1, 2);
-    if (li < 2)
+    if (li < 2 && QMV_CHECK(smem_in_range(chunk + act_pos(l, 16 * li), 16, err)))
       *reinterpret_cast<uint4*>(chunk + act_pos(l, 16 * li)) =
           make_uint4(__byte_perm(w0, h0, 0x5140), __byte_perm(w0, h0, 0x7362), __byte_perm(w1, h1, 0x5140),
                      __byte_perm(w1, h1, 0x7362));
   } else {
-    *reinterpret_cast<uint2*>(chunk + act_pos(l, 8 * li)) = make_uint2(w0, w1);
+    if (QMV_CHECK(smem_in_range(chunk + act_pos(l, 8 * li), 8, err)))
+      *reinterpret_cast<uint2*>(chunk + act_pos(l, 8 * li)) = make_uint2(w0, w1);
   }
 }
 
@@ -227,6 +245,7 @@ __device__ __forceinline__ void stage_activations(const ActSource& src, int kb0,
       const int b = cc[u] * 32 + l[u];
       real[u] = tt[u] < nt && b < nblk;
       gblk[u] = real[u] ? src.row(tt[u]) * (src.ld / 32) + kb0 + b : 0;
+      if (real[u] && !QMV_CHECK(in_range(gblk[u] * 32, 32, src.x_len, src.err))) real[u] = false;
       v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
       w0[u] = w1[u] = 0u;
       dd[u] = 0.f;
@@ -253,7 +272,7 @@ __device__ __forceinline__ void stage_activations(const ActSource& src, int kb0,
       if (src.wq != nullptr) {
 #pragma unroll
         for (int u = 0; u < SU; u++) {
-          if (real[u]) {
+          if (real[u] && QMV_CHECK(in_range(gblk[u] * 32, 32, src.w_len, src.err))) {
             reinterpret_cast<uint2*>(src.wq + gblk[u] * 32)[li] = make_uint2(w0[u], w1[u]);
             if (li == 0) {
               src.wd[gblk[u]] = dd[u];
@@ -265,11 +284,12 @@ __device__ __forceinline__ void stage_activations(const ActSource& src, int kb0,
     }
 #pragma unroll
     for (int u = 0; u < SU; u++) {
-      store_codes<F>(a.codes(cc[u], tt[u]), l[u], li, w0[u], w1[u]);
+      store_codes<F>(a.codes(cc[u], tt[u]), l[u], li, w0[u], w1[u] QMV_DEBUG_ONLY(, src.err));
       if (li == 0) {
         const int di = a.scale(cc[u], tt[u]) + l[u];
-        a.d[di] = dd[u];
-        if constexpr (has_min(F)) a.s[di] = ss[u];
+        if (QMV_CHECK(smem_in_range(a.d + di, 4, src.err))) a.d[di] = dd[u];
+        if constexpr (has_min(F))
+          if (QMV_CHECK(smem_in_range(a.s + di, 4, src.err))) a.s[di] = ss[u];
       }
     }
   }
@@ -297,20 +317,27 @@ __device__ __forceinline__ bool stage_q8_bulk(const ActSource& src, int kb0, int
       const int t = i / (nck * NCOPY), r = i - t * nck * NCOPY, c = r / NCOPY, k = r - c * NCOPY;
       const int nb = min(32, nblk - c * 32);
       const long long row = src.row(t), b0 = (long long)kb0 + c * 32;  // first block of the piece
+      const uint32_t bytes = (uint32_t)nb * (k == 0 ? 32 : 4);
+      void* dst = k == 0 ? (void*)a.codes(c, t) : k == 1 ? (void*)(a.d + a.scale(c, t)) : (void*)(a.s + a.scale(c, t));
+      if (!QMV_CHECK(in_range((row * (src.ld / 32) + b0) * 32, nb * 32, src.x_len, err)) || !QMV_CHECK(smem_in_range(dst, bytes, err))) {
+        mbar_complete_tx(bar, bytes);  // skipped: the phase still completes
+        continue;
+      }
       if (k == 0)
-        bulk_copy_g2s(a.codes(c, t), src.xq + row * src.ld + b0 * 32, (uint32_t)nb * 32, bar);
+        bulk_copy_g2s(dst, src.xq + row * src.ld + b0 * 32, bytes, bar);
       else if (k == 1)
-        bulk_copy_g2s(a.d + a.scale(c, t), src.xd + row * (src.ld / 32) + b0, (uint32_t)nb * 4, bar);
+        bulk_copy_g2s(dst, src.xd + row * (src.ld / 32) + b0, bytes, bar);
       else
-        bulk_copy_g2s(a.s + a.scale(c, t), src.xs + row * (src.ld / 32) + b0, (uint32_t)nb * 4, bar);
+        bulk_copy_g2s(dst, src.xs + row * (src.ld / 32) + b0, bytes, bar);
     }
   }
   // scales (and sums) of the blocks past nblk in the last chunk: zero
   const int nb_last = nblk - (nck - 1) * 32, tail = 32 - nb_last;
   for (int i = cw * 32 + lane; i < nt * tail; i += CW * 32) {
     const int t = i / tail, b = nb_last + (i - t * tail);
-    a.d[a.scale(nck - 1, t) + b] = 0.f;
-    if constexpr (has_min(F)) a.s[a.scale(nck - 1, t) + b] = 0;
+    if (QMV_CHECK(smem_in_range(a.d + a.scale(nck - 1, t) + b, 4, err))) a.d[a.scale(nck - 1, t) + b] = 0.f;
+    if constexpr (has_min(F))
+      if (QMV_CHECK(smem_in_range(a.s + a.scale(nck - 1, t) + b, 4, err))) a.s[a.scale(nck - 1, t) + b] = 0;
   }
   const bool ok = mbar_wait(bar, parity, err);
   if constexpr (F == QMV_IQ4_XS) {
@@ -320,6 +347,7 @@ __device__ __forceinline__ bool stage_q8_bulk(const ActSource& src, int kb0, int
       uint8_t* chunk = a.codes(c, t);
       uint4* p0 = reinterpret_cast<uint4*>(chunk + act_pos(l, 0));
       uint4* p1 = reinterpret_cast<uint4*>(chunk + act_pos(l, 16));
+      if (!QMV_CHECK(smem_in_range(p0, 16, err)) || !QMV_CHECK(smem_in_range(p1, 16, err))) continue;
       const uint4 lo = *p0, hi = *p1;
       *p0 = make_uint4(__byte_perm(lo.x, hi.x, 0x5140), __byte_perm(lo.x, hi.x, 0x7362),
                        __byte_perm(lo.y, hi.y, 0x5140), __byte_perm(lo.y, hi.y, 0x7362));
@@ -868,7 +896,8 @@ __device__ __forceinline__ void stage_float(const ActSource& src, long long k0, 
       v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (i < total) {
         const int t = i / per_tok, e4 = i - t * per_tok;  // float4 e4 of the token's range
-        if (4 * e4 < nw) v[j] = __ldg(reinterpret_cast<const float4*>(src.x + src.row(t) * src.ld + k0) + e4);
+        if (4 * e4 < nw && QMV_CHECK(in_range(src.row(t) * src.ld + k0 + 4 * e4, 4, src.x_len, src.err)))
+          v[j] = __ldg(reinterpret_cast<const float4*>(src.x + src.row(t) * src.ld + k0) + e4);
       }
     }
 #pragma unroll
@@ -878,7 +907,7 @@ __device__ __forceinline__ void stage_float(const ActSource& src, long long k0, 
         const int t = i / per_tok, e4 = i - t * per_tok, c = e4 / Q;
         int o = e4 - c * Q;  // float4 within the chunk
         if constexpr (F == QMV_F16) o = (o & ~63) | ((o & 1) << 5) | ((o >> 1) & 31);
-        dst[((size_t)c * NT + t) * Q + o] = v[j];
+        if (QMV_CHECK(smem_in_range(dst + ((size_t)c * NT + t) * Q + o, 16, src.err))) dst[((size_t)c * NT + t) * Q + o] = v[j];
       }
     }
   }

@@ -51,6 +51,11 @@ struct DenseParams {
   const uint8_t* w;    // the weight rows
   long long rb;        // bytes per row
   int nbmax;           // blocks of the longest split range
+  // QMV_DEBUG builds: extents of the caller's buffers (elements), derived on
+  // the host from the call's arguments, for the range checks
+  QMV_DEBUG_ONLY(long long x_len;    // x or xq: ntot * K
+                 long long out_len;  // out: ntot * M, or n_split * ntot * M
+                 long long add_len;) // add: ntot * M (0 without add)
 };
 
 // Per-CTA walk over its tiles: a contiguous range of the flattened
@@ -200,7 +205,9 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, is_float(F) ? 1 : dense_mi
           const int st = ring.st;
           uint8_t* dst = stages + st * STAGE_BYTES;
           const int x = (g0 * GB + c * CB) / 8;
-          if (nu == TU) {
+          if (!QMV_CHECK(smem_in_range(dst, nu * UNIT_ROWS * CB, p.err))) {
+            mbar_arrive(&full[st]);  // skipped: the stage completes without data
+          } else if (nu == TU) {
             mbar_arrive_expect_tx(&full[st], STAGE_BYTES);
             tma_load_2d(dst, &map_tile, &full[st], x, u * UNIT_ROWS, pol);
           } else {
@@ -232,7 +239,8 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, is_float(F) ? 1 : dense_mi
                  as_base = smem_u32(a.s);
   // token pass blockIdx.y: tokens t0 .. t0 + ntk - 1 of the call
   const int t0 = p.t0 + blockIdx.y * NT, ntk = p.nt;
-  const ActSource src{p.x, p.xq, p.xd, p.xs, p.K, nullptr, t0, nullptr, nullptr, nullptr};
+  const ActSource src{p.x, p.xq, p.xd, p.xs, p.K, nullptr, t0, nullptr, nullptr, nullptr
+                          QMV_DEBUG_ONLY(, p.x_len, 0, p.err)};
   uint32_t aphase = 0;
 
   while (walk.next(s, u, nu)) {
@@ -270,7 +278,8 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, is_float(F) ? 1 : dense_mi
     // residual add: the values this warp adds at the store are requested
     // into L1 now, so the store does not wait for them
     if constexpr (ADD)
-      if (part == 0 && lane < ntk && grp * RW < nrows)
+      if (part == 0 && lane < ntk && grp * RW < nrows &&
+          QMV_CHECK(in_range((long long)(t0 + lane) * p.M + row0 + grp * RW, 1, p.add_len, p.err)))
         asm volatile("prefetch.global.L1 [%0];" ::"l"(p.add + (long long)(t0 + lane) * p.M + row0 + grp * RW));
     for (int c = 0; c < nck && alive; c++, ring.advance(p.stages)) {
       const int st = ring.st;
@@ -278,7 +287,10 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, is_float(F) ? 1 : dense_mi
         alive = false;
         break;
       }
-      if (grp * RW < nrows && (c & (ks - 1)) == part)  // ks is 1, 2 or 4
+      if (grp * RW < nrows && (c & (ks - 1)) == part &&  // ks is 1, 2 or 4
+          QMV_CHECK(chunk_reads_in_range<F, NT>(stage_base + st * STAGE_BYTES + grp * RW * CB, RW * CB,
+                                      aq_base + c * NT * ACTB, ad_base + c * NT * 128, as_base + c * NT * 128,
+                                      p.err)))
         cons.chunk(stage_base + st * STAGE_BYTES + grp * RW * CB, aq_base + c * NT * ACTB,
                    ad_base + c * NT * 128, as_base + c * NT * 128, ntk, acc);
       __syncwarp();
@@ -323,13 +335,15 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, is_float(F) ? 1 : dense_mi
     if (ks > 1) {
       if (lead)
 #pragma unroll
-        for (int i = 0; i < HELD; i++) red[cw * V + idx + i] = v[i];
+        for (int i = 0; i < HELD; i++)
+          if (QMV_CHECK(smem_in_range(red + cw * V + idx + i, 4, p.err))) red[cw * V + idx + i] = v[i];
       named_sync(2, CONSUMER_THREADS);
       if (part == 0 && lead)
 #pragma unroll
         for (int i = 0; i < HELD; i++) {
-          float w = red[grp * V + idx + i];
-          for (int k = 1; k < ks; k++) w += red[(k * rg + grp) * V + idx + i];
+          float w = QMV_CHECK(smem_in_range(red + grp * V + idx + i, 4, p.err)) ? red[grp * V + idx + i] : 0.f;
+          for (int k = 1; k < ks; k++)
+            if (QMV_CHECK(smem_in_range(red + (k * rg + grp) * V + idx + i, 4, p.err))) w += red[(k * rg + grp) * V + idx + i];
           v[i] = w;
         }
       named_sync(2, CONSUMER_THREADS);  // red is free for the next tile
@@ -340,8 +354,9 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, is_float(F) ? 1 : dense_mi
         const int o = idx + i, r = o / NT, t = o - r * NT, row = grp * RW + r;
         if (t < ntk && row < nrows) {
           const long long o = (long long)(t0 + t) * p.M + row0 + row;
+          if (!QMV_CHECK(in_range((long long)s * p.ntot * p.M + o, 1, p.out_len, p.err))) continue;
           if constexpr (ADD)
-            out[o] = v[i] + p.add[o];
+            out[o] = v[i] + (QMV_CHECK(in_range(o, 1, p.add_len, p.err)) ? p.add[o] : 0.f);
           else
             out[o] = v[i];
         }

@@ -12,7 +12,9 @@ namespace qmv {
 // predecessor before it reads x or writes q / d / s.
 __global__ void __launch_bounds__(256) act_quant_kernel(const float* __restrict__ x, int K, int n_tok,
                                                         int8_t* __restrict__ q, float* __restrict__ d,
-                                                        int32_t* __restrict__ s) {
+                                                        int32_t* __restrict__ s
+                                                            QMV_DEBUG_ONLY(, unsigned* err, long long x_len,
+                                                                           long long q_len)) {
   pdl_launch_dependents();
   pdl_wait();
   constexpr int SU = 4;
@@ -28,7 +30,7 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const float* __restrict_
 #pragma unroll
     for (int u = 0; u < SU; u++) {
       v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (g0 + u < groups) {
+      if (g0 + u < groups && QMV_CHECK(in_range((g0 + u) * 256 + sub * 32 + 8 * li, 8, x_len, err))) {
         const float4* p = reinterpret_cast<const float4*>(x + (g0 + u) * 256 + sub * 32) + 2 * li;
         v[u][0] = __ldg(p);
         v[u][1] = __ldg(p + 1);
@@ -39,8 +41,9 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const float* __restrict_
     for (int u = 0; u < SU; u++) {
       if (g0 + u < groups) {
         const long long g = g0 + u;
-        *reinterpret_cast<uint2*>(q + g * 256 + act_pos(sub, 8 * li)) = make_uint2(w0[u], w1[u]);
-        if (li == 0) {
+        if (QMV_CHECK(in_range(g * 256 + act_pos(sub, 8 * li), 8, q_len, err)))
+          *reinterpret_cast<uint2*>(q + g * 256 + act_pos(sub, 8 * li)) = make_uint2(w0[u], w1[u]);
+        if (li == 0 && QMV_CHECK(in_range(g * 8 + sub, 1, q_len / 32, err))) {
           d[g * 8 + sub] = dd[u];
           s[g * 8 + sub] = ss[u];
         }
@@ -54,10 +57,14 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const float* __restrict_
 // group of splits are all loaded before the first is added, so their
 // latencies overlap.
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ partial, float* y,
-                                                            const float* add, long long n, int n_split) {
+                                                            const float* add, long long n, int n_split
+                                                                QMV_DEBUG_ONLY(, unsigned* err, long long part_len,
+                                                                               long long y_len, long long add_len)) {
   pdl_wait();
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    // the checks cover partial[s n + i] for every s (i and the last split)
+    if (!QMV_CHECK(in_range(i, 1, part_len, err)) || !QMV_CHECK(in_range((long long)(n_split - 1) * n + i, 1, part_len, err))) continue;
     float acc = partial[i];
     int s = 1;
     for (; s + 8 <= n_split; s += 8) {
@@ -68,7 +75,8 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
       for (int j = 0; j < 8; j++) acc += v[j];
     }
     for (; s < n_split; s++) acc += partial[(long long)s * n + i];
-    y[i] = add ? acc + add[i] : acc;
+    if (!QMV_CHECK(in_range(i, 1, y_len, err))) continue;
+    y[i] = add ? acc + (QMV_CHECK(in_range(i, 1, add_len, err)) ? add[i] : 0.f) : acc;
   }
   pdl_launch_dependents();
 }
@@ -82,7 +90,9 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
 __global__ void __launch_bounds__(256) moe_combine_kernel(const int32_t* __restrict__ ids,
                                                           const float* __restrict__ gates,
                                                           const float* __restrict__ o, float* __restrict__ y,
-                                                          int n_tok, int top_k, int n_experts, int hidden) {
+                                                          int n_tok, int top_k, int n_experts, int hidden
+                                                              QMV_DEBUG_ONLY(, unsigned* err, long long ids_len,
+                                                                             long long o_len, long long y_len)) {
   pdl_wait();
   const int q4 = hidden / 4;
   const long long total = (long long)n_tok * q4;
@@ -93,8 +103,9 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const int32_t* __restr
     float g[QMV_MAX_TOPK];
 #pragma unroll
     for (int k = 0; k < QMV_MAX_TOPK; k++) {
-      e[k] = k < top_k ? ids[t * top_k + k] : -1;
-      g[k] = k < top_k ? gates[t * top_k + k] : 0.f;
+      const bool in = k < top_k && QMV_CHECK(in_range((long long)t * top_k + k, 1, ids_len, err));
+      e[k] = in ? ids[t * top_k + k] : -1;
+      g[k] = in ? gates[t * top_k + k] : 0.f;
     }
     bool ok[QMV_MAX_TOPK];
 #pragma unroll
@@ -102,6 +113,7 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const int32_t* __restr
       ok[k] = e[k] >= 0 && e[k] < n_experts;
 #pragma unroll
       for (int kk = 0; kk < k; kk++) ok[k] = ok[k] && e[kk] != e[k];
+      ok[k] = ok[k] && QMV_CHECK(in_range(((long long)t * top_k + k) * hidden + 4 * m4, 4, o_len, err));
     }
     float4 v[QMV_MAX_TOPK];
 #pragma unroll
@@ -117,7 +129,7 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const int32_t* __restr
       acc.z = fmaf(g[k], v[k].z, acc.z);
       acc.w = fmaf(g[k], v[k].w, acc.w);
     }
-    reinterpret_cast<float4*>(y + (long long)t * hidden)[m4] = acc;
+    if (QMV_CHECK(in_range((long long)t * hidden + 4 * m4, 4, y_len, err))) reinterpret_cast<float4*>(y + (long long)t * hidden)[m4] = acc;
   }
   pdl_launch_dependents();
 }
@@ -131,7 +143,9 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const int32_t* __restr
 constexpr int ROUTE_MAX_PER_LANE = 16;
 __global__ void __launch_bounds__(128) route_topk_kernel(const float* __restrict__ logits, int n_tok, int E,
                                                          int top_k, int gating, int32_t* __restrict__ ids,
-                                                         float* __restrict__ gates) {
+                                                         float* __restrict__ gates
+                                                             QMV_DEBUG_ONLY(, unsigned* err, long long logits_len,
+                                                                            long long ids_len)) {
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
@@ -140,7 +154,7 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const float* __restrict
 #pragma unroll
     for (int i = 0; i < ROUTE_MAX_PER_LANE; i++) {
       const int e = i * 32 + lane;  // expert of slot i of this lane
-      l[i] = e < E ? logits[(long long)t * E + e] : 0.f;
+      l[i] = e < E && QMV_CHECK(in_range((long long)t * E + e, 1, logits_len, err)) ? logits[(long long)t * E + e] : 0.f;
     }
     unsigned taken = 0;  // bit i: slot i picked (or past E)
 #pragma unroll
@@ -186,7 +200,7 @@ __global__ void __launch_bounds__(128) route_topk_kernel(const float* __restrict
     }
 #pragma unroll
     for (int k = 0; k < QMV_MAX_TOPK; k++) {
-      if (k < top_k && lane == k) {
+      if (k < top_k && lane == k && QMV_CHECK(in_range((long long)t * top_k + k, 1, ids_len, err))) {
         ids[t * top_k + k] = pick_e[k];
         gates[t * top_k + k] = w[k] / sum;
       }
@@ -200,7 +214,9 @@ cudaError_t launch_route_topk(const float* logits, int n_tok, int E, int top_k, 
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   make_config(cfg, attr, dim3((unsigned)((n_tok + 3) / 4)), dim3(128), 0, stream, pdl);
-  return cudaLaunchKernelEx(&cfg, route_topk_kernel, logits, n_tok, E, top_k, gating, ids, gates);
+  return cudaLaunchKernelEx(&cfg, route_topk_kernel, logits, n_tok, E, top_k, gating, ids, gates
+                            QMV_DEBUG_ONLY(, device_error_word(), (long long)n_tok * E,
+                                           output_extent((long long)n_tok * top_k)));
 }
 
 cudaError_t launch_moe_combine(const int32_t* ids, const float* gates, const float* o, float* y, int n_tok,
@@ -212,7 +228,11 @@ cudaError_t launch_moe_combine(const int32_t* ids, const float* gates, const flo
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   make_config(cfg, attr, dim3((unsigned)ctas), dim3(256), 0, stream, pdl);
-  return cudaLaunchKernelEx(&cfg, moe_combine_kernel, ids, gates, o, y, n_tok, top_k, n_experts, hidden);
+  const long long S = (long long)n_tok * top_k;
+  (void)S;
+  return cudaLaunchKernelEx(&cfg, moe_combine_kernel, ids, gates, o, y, n_tok, top_k, n_experts, hidden
+                            QMV_DEBUG_ONLY(, device_error_word(), S, S * hidden,
+                                           output_extent((long long)n_tok * hidden)));
 }
 
 // Every non-negative float against the IEEE operations: [0] counts inputs
@@ -250,7 +270,7 @@ void make_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, dim3 grid, 
   cfg.numAttrs = pdl ? 1 : 0;
 }
 
-cudaError_t launch_act_quant(const float* x, int K, int n_tok, int8_t* q, float* d, int32_t* s,
+cudaError_t launch_act_quant(const float* x, int K, int n_tok, int8_t* q, float* d, int32_t* s, long long q_len,
                              cudaStream_t stream, bool pdl) {
   const long long groups = (long long)K / 256 * n_tok;
   long long ctas = (groups + 31) / 32;  // 8 warps x 4 groups
@@ -260,7 +280,9 @@ cudaError_t launch_act_quant(const float* x, int K, int n_tok, int8_t* q, float*
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   make_config(cfg, attr, dim3((unsigned)ctas), dim3(256), 0, stream, pdl);
-  return cudaLaunchKernelEx(&cfg, act_quant_kernel, x, K, n_tok, q, d, s);
+  (void)q_len;
+  return cudaLaunchKernelEx(&cfg, act_quant_kernel, x, K, n_tok, q, d, s
+                            QMV_DEBUG_ONLY(, device_error_word(), (long long)n_tok * K, q_len));
 }
 
 cudaError_t launch_splitk_reduce(const float* partial, float* y, const float* add, long long M, int n_tok, int n_split,
@@ -272,7 +294,9 @@ cudaError_t launch_splitk_reduce(const float* partial, float* y, const float* ad
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attr[1];
   make_config(cfg, attr, dim3((unsigned)ctas), dim3(256), 0, stream, pdl);
-  return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, partial, y, add, n, n_split);
+  return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, partial, y, add, n, n_split
+                            QMV_DEBUG_ONLY(, device_error_word(), (long long)n_split * n, output_extent(n),
+                                           add ? n : 0ll));
 }
 
 }  // namespace qmv

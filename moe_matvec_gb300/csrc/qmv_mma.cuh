@@ -124,13 +124,29 @@ __device__ __forceinline__ uint32_t u4x2_f16(uint32_t w) {
 // Token slots [nt, NT) of the block scales and sums: zero (their sums are
 // never stored; zeros keep them finite).
 template <int NT>
-__device__ __forceinline__ void mk_zero_slots(float* dxa, int32_t* xsa, int dpitch, int nt, int nblk, int tid) {
+__device__ __forceinline__ void mk_zero_slots(float* dxa, int32_t* xsa, int dpitch, int nt, int nblk, int tid,
+                                              unsigned* err) {
   const int rest = NT - nt;
   for (int i = tid; i < rest * nblk; i += MK_CW * 32) {
     const int t = nt + i / nblk, b = i - (t - nt) * nblk;
-    dxa[t * dpitch + b] = 0.0f;
-    xsa[t * dpitch + b] = 0;
+    if (QMV_CHECK(smem_in_range(dxa + t * dpitch + b, 4, err))) dxa[t * dpitch + b] = 0.0f;
+    if (QMV_CHECK(smem_in_range(xsa + t * dpitch + b, 4, err))) xsa[t * dpitch + b] = 0;
   }
+}
+
+// The shared-memory ranges of a warp's step over blocks kbase, kbase + 1 of
+// a chunk: the weight stage, the NT token slots' codes (the 256-byte group
+// that holds both blocks), scales and sums of those blocks, and the warp's
+// scale area.
+template <int NT>
+__device__ __forceinline__ bool mk_step_in_range(uint32_t sbase, uint32_t codes_base, const float* dxa,
+                                                 const int32_t* xsa, const float4* wscl, int apitch, int dpitch,
+                                                 int kbase, unsigned* err) {
+  const uint32_t g = (uint32_t)(kbase >> 3) * 256;
+  return smem_in_range(sbase, MK_STAGE, err) && smem_in_range(codes_base + g, (NT - 1) * apitch + 256, err) &&
+         smem_in_range(dxa + kbase, ((NT - 1) * dpitch + 2) * 4, err) &&
+         smem_in_range(xsa + kbase, ((NT - 1) * dpitch + 2) * 4, err) &&
+         smem_in_range(wscl, 2 * MK_ROWS * 16, err);
 }
 
 // Activation staging of tokens [0, nt) of the pass (rows t0 + t of x),
@@ -155,6 +171,8 @@ __device__ __forceinline__ void mk_stage_fp32(const DenseParams& p, int t0, int 
       real[u] = idx < total;
       tt[u] = real[u] ? idx / nblk : 0;
       bb[u] = idx - tt[u] * nblk;
+      if (real[u] && !QMV_CHECK(in_range((long long)(t0 + tt[u]) * p.K + (long long)(kb0 + bb[u]) * BLK, BLK, p.x_len, p.err)))
+        real[u] = false;
       v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (real[u]) {
         const float4* src = reinterpret_cast<const float4*>(p.x + (long long)(t0 + tt[u]) * p.K +
@@ -167,15 +185,17 @@ __device__ __forceinline__ void mk_stage_fp32(const DenseParams& p, int t0, int 
 #pragma unroll
     for (int u = 0; u < SU; u++) {
       if (real[u]) {
-        *reinterpret_cast<uint2*>(codes + (size_t)tt[u] * apitch + act_pos(bb[u], 8 * li)) = make_uint2(w0[u], w1[u]);
-        if (li == 0) {
+        uint8_t* q = codes + (size_t)tt[u] * apitch + act_pos(bb[u], 8 * li);
+        if (QMV_CHECK(smem_in_range(q, 8, p.err))) *reinterpret_cast<uint2*>(q) = make_uint2(w0[u], w1[u]);
+        if (li == 0 && QMV_CHECK(smem_in_range(dxa + tt[u] * dpitch + bb[u], 4, p.err)) &&
+            QMV_CHECK(smem_in_range(xsa + tt[u] * dpitch + bb[u], 4, p.err))) {
           dxa[tt[u] * dpitch + bb[u]] = dd[u];
           xsa[tt[u] * dpitch + bb[u]] = ss[u];
         }
       }
     }
   }
-  mk_zero_slots<NT>(dxa, xsa, dpitch, nt, nblk, cw * 32 + lane);
+  mk_zero_slots<NT>(dxa, xsa, dpitch, nt, nblk, cw * 32 + lane, p.err);
 }
 
 // The same from pre-quantized rows (the library's Q8 layout): three bulk
@@ -194,14 +214,21 @@ __device__ __forceinline__ bool mk_stage_q8(const DenseParams& p, int t0, int nt
   for (int i = cw * 32 + lane; i < 3 * nt; i += MK_CW * 32) {
     const int t = i / 3, k = i - 3 * t;
     const long long row = t0 + t;
+    const uint32_t bytes = (uint32_t)nblk * (k == 0 ? BLK : 4);
+    void* dst = k == 0 ? (void*)(codes + (size_t)t * apitch) : k == 1 ? (void*)(ldx + t * dpitch) : (void*)(lxs + t * dpitch);
+    if (!QMV_CHECK(in_range(row * p.K + (long long)kb0 * BLK, (long long)nblk * BLK, p.x_len, p.err)) ||
+        !QMV_CHECK(smem_in_range(dst, bytes, p.err))) {
+      mbar_complete_tx(bar, bytes);  // skipped: the phase still completes
+      continue;
+    }
     if (k == 0)
-      bulk_copy_g2s(codes + (size_t)t * apitch, p.xq + row * p.K + (long long)kb0 * BLK, (uint32_t)nblk * BLK, bar);
+      bulk_copy_g2s(dst, p.xq + row * p.K + (long long)kb0 * BLK, bytes, bar);
     else if (k == 1)
-      bulk_copy_g2s(ldx + t * dpitch, p.xd + row * nbr + kb0, (uint32_t)nblk * 4, bar);
+      bulk_copy_g2s(dst, p.xd + row * nbr + kb0, bytes, bar);
     else
-      bulk_copy_g2s(lxs + t * dpitch, p.xs + row * nbr + kb0, (uint32_t)nblk * 4, bar);
+      bulk_copy_g2s(dst, p.xs + row * nbr + kb0, bytes, bar);
   }
-  mk_zero_slots<NT>(ldx, lxs, dpitch, nt, nblk, cw * 32 + lane);
+  mk_zero_slots<NT>(ldx, lxs, dpitch, nt, nblk, cw * 32 + lane, p.err);
   return mbar_wait(bar, parity, p.err);
 }
 
@@ -272,7 +299,9 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
           const int st = ring.st;
           uint8_t* dst = stages + st * MK_STAGE;
           const int x = (g0 + c * MK_GROUPS) * (144 / 8);  // 8-byte elements; x * 8 = 144 * group
-          if (nu == MK_UNITS) {
+          if (!QMV_CHECK(smem_in_range(dst, nu * UNIT_ROWS * MK_PITCH, p.err))) {
+            mbar_arrive(&full[st]);  // skipped: the stage completes without data
+          } else if (nu == MK_UNITS) {
             mbar_arrive_expect_tx(&full[st], MK_STAGE);
             tma_load_2d(dst, &map_tile, &full[st], x, u * UNIT_ROWS, pol);
           } else {
@@ -346,7 +375,9 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
         break;
       }
       const int kbase = c * MK_BLOCKS + 2 * cw;  // this warp's first block, relative to kb0
-      if (kbase < nblk) {  // (a last chunk of one or two superblocks leaves warps 4-11 or 8-11 idle)
+      // (a last chunk of one or two superblocks leaves warps 4-11 or 8-11 idle)
+      if (kbase < nblk && QMV_CHECK(mk_step_in_range<NT>(stage_base + st * MK_STAGE, codes_base, dxa, xsa, wscl, apitch,
+                                               dpitch, kbase, p.err))) {
         const uint32_t sbase = stage_base + st * MK_STAGE;
         {
           // (a, a, -c, -c) of rows 2 lane, 2 lane + 1 for both blocks
@@ -453,6 +484,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 2; i++) {
             float* q = red + ((cw % MK_RW) * NT + 8 * h + 2 * t4) * MK_RED_LD + 16 * r + 8 * i + g;
+            if (!QMV_CHECK(smem_in_range(q, MK_RED_LD * 4 + 4, p.err))) continue;
             q[0] = acc[r][h][i].x;
             q[MK_RED_LD] = acc[r][h][i].y;
           }
@@ -468,6 +500,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 2; i++) {
             const float* q = red + (cw * NT + 8 * h + 2 * t4) * MK_RED_LD + 16 * r + 8 * i + g;
+            if (!QMV_CHECK(smem_in_range(q, MK_RED_LD * 4 + 4, p.err))) continue;
             acc[r][h][i].x += q[0];
             acc[r][h][i].y += q[MK_RED_LD];
           }
@@ -478,12 +511,14 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
     float* out = p.out + (long long)s * p.ntot * p.M;
     for (int o = threadIdx.x; o < NT * MK_ROWS; o += MK_CW * 32) {
       const int tok = o / MK_ROWS, r = o - tok * MK_ROWS;
-      float v = red[tok * MK_RED_LD + r];
+      float v = QMV_CHECK(smem_in_range(red + tok * MK_RED_LD + r, 4, p.err)) ? red[tok * MK_RED_LD + r] : 0.f;
 #pragma unroll
-      for (int w = 1; w < MK_RW; w++) v += red[(w * NT + tok) * MK_RED_LD + r];
+      for (int w = 1; w < MK_RW; w++)
+        if (QMV_CHECK(smem_in_range(red + (w * NT + tok) * MK_RED_LD + r, 4, p.err))) v += red[(w * NT + tok) * MK_RED_LD + r];
       if (tok < ntk && r < nrows) {
         const long long oi = (long long)(t0 + tok) * p.M + row0 + r;
-        out[oi] = p.add ? v + p.add[oi] : v;
+        if (!QMV_CHECK(in_range((long long)s * p.ntot * p.M + oi, 1, p.out_len, p.err))) continue;
+        out[oi] = p.add ? v + (QMV_CHECK(in_range(oi, 1, p.add_len, p.err)) ? p.add[oi] : 0.f) : v;
       }
     }
   }

@@ -56,6 +56,17 @@ struct MfLayout {
   }
 };
 
+// The shared-memory ranges of a warp's step at weight kc of a chunk: the
+// weight stage and the NT token rows of both activation parts over the
+// step's 32 weights.
+template <int NT>
+__device__ __forceinline__ bool mf_step_in_range(uint32_t sbase, uint32_t xh_base, uint32_t xl_base, int xpitch,
+                                                 int kc, unsigned* err) {
+  const uint32_t n = (uint32_t)((NT - 1) * xpitch + 64);
+  return smem_in_range(sbase, MF_STAGE, err) && smem_in_range(xh_base + 2 * kc, n, err) &&
+         smem_in_range(xl_base + 2 * kc, n, err);
+}
+
 template <int NT>
 __global__ void __launch_bounds__(MF_THREADS, 1)
     qmv_mma_f16_kernel(const __grid_constant__ CUtensorMap map_tile, const __grid_constant__ CUtensorMap map_unit,
@@ -98,7 +109,9 @@ __global__ void __launch_bounds__(MF_THREADS, 1)
           const int st = ring.st;
           uint8_t* dst = stages + st * MF_STAGE;
           const int x = (g0 * BLK + c * MF_KC) / 4;  // 8-byte elements (4 weights); x * 8 = 2 * first weight
-          if (nu == MK_UNITS) {
+          if (!QMV_CHECK(smem_in_range(dst, nu * UNIT_ROWS * MF_PITCH, p.err))) {
+            mbar_arrive(&full[st]);  // skipped: the stage completes without data
+          } else if (nu == MK_UNITS) {
             mbar_arrive_expect_tx(&full[st], MF_STAGE);
             tma_load_2d(dst, &map_tile, &full[st], x, u * UNIT_ROWS, pol);
           } else {
@@ -146,6 +159,7 @@ __global__ void __launch_bounds__(MF_THREADS, 1)
         float m = 0.0f;
         if (real)
           for (int k = 4 * lane; k < klen; k += 128) {
+            if (!QMV_CHECK(in_range(xr - p.x + k, 4, p.x_len, p.err))) continue;
             const float4 v = __ldg(reinterpret_cast<const float4*>(xr + k));
             m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
           }
@@ -158,15 +172,15 @@ __global__ void __launch_bounds__(MF_THREADS, 1)
         uint8_t* lrow = xl + (size_t)tt * xpitch;
         for (int k = 2 * lane; k < klen; k += 64) {
           float2 v = make_float2(0.0f, 0.0f);
-          if (real) v = __ldg(reinterpret_cast<const float2*>(xr + k));
+          if (real && QMV_CHECK(in_range(xr - p.x + k, 2, p.x_len, p.err))) v = __ldg(reinterpret_cast<const float2*>(xr + k));
           const float a = v.x * sc, b = v.y * sc;  // exact: a power of two
           const __half2 hi = __floats2half2_rn(a, b);
           const float2 hf = __half22float2(hi);
           const __half2 lo = __floats2half2_rn(a - hf.x, b - hf.y);  // the differences are exact
-          *reinterpret_cast<__half2*>(hrow + 2 * k) = hi;
-          *reinterpret_cast<__half2*>(lrow + 2 * k) = lo;
+          if (QMV_CHECK(smem_in_range(hrow + 2 * k, 4, p.err))) *reinterpret_cast<__half2*>(hrow + 2 * k) = hi;
+          if (QMV_CHECK(smem_in_range(lrow + 2 * k, 4, p.err))) *reinterpret_cast<__half2*>(lrow + 2 * k) = lo;
         }
-        if (lane == 0) inv[tt] = 1.0f / sc;  // exact
+        if (lane == 0 && QMV_CHECK(smem_in_range(inv + tt, 4, p.err))) inv[tt] = 1.0f / sc;  // exact
       }
       named_sync(1, MF_CW * 32);
       staged_split = s;
@@ -187,7 +201,8 @@ __global__ void __launch_bounds__(MF_THREADS, 1)
         break;
       }
       const int kc = c * MF_KC + 32 * cw;  // this warp's first weight of the chunk, relative to the range
-      if (kc < klen) {                     // (klen is a multiple of 32: both steps are in range)
+      // (klen is a multiple of 32: both steps are in range)
+      if (kc < klen && QMV_CHECK(mf_step_in_range<NT>(stage_base + st * MF_STAGE, xh_base, xl_base, xpitch, kc, p.err))) {
         const uint32_t sbase = stage_base + st * MF_STAGE + 64 * cw;
 #pragma unroll
         for (int ss = 0; ss < 2; ss++) {
@@ -219,6 +234,7 @@ __global__ void __launch_bounds__(MF_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 2; i++) {
           float* q = red + (cw * NT + 8 * h + 2 * t4) * MK_RED_LD + 16 * r + 8 * i + g;
+          if (!QMV_CHECK(smem_in_range(q, MK_RED_LD * 4 + 4, p.err))) continue;
           q[0] = acc[r][h][2 * i];
           q[MK_RED_LD] = acc[r][h][2 * i + 1];
         }
@@ -226,13 +242,16 @@ __global__ void __launch_bounds__(MF_THREADS, 1)
     float* out = p.out + (long long)s * p.ntot * p.M;
     for (int o = threadIdx.x; o < NT * MK_ROWS; o += MF_CW * 32) {
       const int tok = o / MK_ROWS, r = o - tok * MK_ROWS;
-      float v = red[tok * MK_RED_LD + r];
+      float v = QMV_CHECK(smem_in_range(red + tok * MK_RED_LD + r, 4, p.err)) ? red[tok * MK_RED_LD + r] : 0.f;
 #pragma unroll
-      for (int w = 1; w < MF_CW; w++) v += red[(w * NT + tok) * MK_RED_LD + r];
+      for (int w = 1; w < MF_CW; w++)
+        if (QMV_CHECK(smem_in_range(red + (w * NT + tok) * MK_RED_LD + r, 4, p.err))) v += red[(w * NT + tok) * MK_RED_LD + r];
       if (tok < ntk && r < nrows) {
         const long long oi = (long long)(t0 + tok) * p.M + row0 + r;
+        if (!QMV_CHECK(in_range((long long)s * p.ntot * p.M + oi, 1, p.out_len, p.err)) || !QMV_CHECK(smem_in_range(inv + tok, 4, p.err)))
+          continue;
         v *= inv[tok];
-        out[oi] = p.add ? v + p.add[oi] : v;
+        out[oi] = p.add ? v + (QMV_CHECK(in_range(oi, 1, p.add_len, p.err)) ? p.add[oi] : 0.f) : v;
       }
     }
   }

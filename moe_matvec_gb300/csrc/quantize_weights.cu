@@ -233,12 +233,18 @@ __device__ void superblock_iq4_xs(const float* w, uint8_t* meta, uint8_t* payloa
 
 template <int F>
 __global__ void __launch_bounds__(128) quantize_kernel(const float* __restrict__ w, long long n_groups, int K,
-                                                       uint8_t* __restrict__ W) {
+                                                       uint8_t* __restrict__ W
+                                                           QMV_DEBUG_ONLY(, unsigned* err, long long w_len,
+                                                                          long long W_len)) {
   constexpr int GW = Fmt<F>::GW, GB = Fmt<F>::GB;
   const long long gpr = K / GW;
   for (long long gi = (long long)blockIdx.x * blockDim.x + threadIdx.x; gi < n_groups;
        gi += (long long)gridDim.x * blockDim.x) {
     const long long row = gi / gpr, col = gi - row * gpr;
+    // the group reads w[row K + col GW ..] (GW values) and writes GB bytes at W + gi GB
+    if (!QMV_CHECK(in_range(row * K + col * GW, GW, w_len, err)) ||
+        !QMV_CHECK(in_range(gi * GB, GB, W_len, err)))
+      continue;
     const float* src = w + row * K + col * GW;
     __align__(16) uint8_t g[GB];
     for (int i = 0; i < GB; i++) g[i] = 0;
@@ -269,13 +275,23 @@ __global__ void __launch_bounds__(128) quantize_kernel(const float* __restrict__
 // F16 / F32 rows: one conversion per weight (binary16 rounded to nearest
 // even, or the fp32 value as it is); the rows are the flat [M][K] array.
 template <int F>
-__global__ void convert_rows_kernel(const float* __restrict__ w, long long n, uint8_t* __restrict__ out) {
+__global__ void convert_rows_kernel(const float* __restrict__ w, long long n, uint8_t* __restrict__ out
+                                        QMV_DEBUG_ONLY(, unsigned* err, long long out_len)) {
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    if (!QMV_CHECK(in_range(i, 1, out_len, err))) continue;  // (w holds the same n elements)
     if constexpr (F == QMV_F16)
       reinterpret_cast<__half*>(out)[i] = __float2half_rn(w[i]);
     else
       reinterpret_cast<float*>(out)[i] = w[i];
   }
+}
+
+// extents: w holds M K values, W the M (K / GW) groups of GB bytes
+template <int F>
+static void quantize_groups(const float* w, long long M, int K, uint8_t* W, long long ctas, cudaStream_t stream) {
+  const long long groups = M * (K / Fmt<F>::GW);
+  quantize_kernel<F><<<(unsigned)ctas, 128, 0, stream>>>(
+      w, groups, K, W QMV_DEBUG_ONLY(, device_error_word(), M * K, output_extent(groups * Fmt<F>::GB)));
 }
 
 cudaError_t launch_quantize_weights(int fmt, const float* w, long long M, int K, void* W, cudaStream_t stream) {
@@ -285,9 +301,11 @@ cudaError_t launch_quantize_weights(int fmt, const float* w, long long M, int K,
     const long long cap = 32ll * device_sm_count();
     if (ctas > cap) ctas = cap;
     if (fmt == QMV_F16)
-      convert_rows_kernel<QMV_F16><<<(unsigned)ctas, 256, 0, stream>>>(w, n, static_cast<uint8_t*>(W));
+      convert_rows_kernel<QMV_F16><<<(unsigned)ctas, 256, 0, stream>>>(
+          w, n, static_cast<uint8_t*>(W) QMV_DEBUG_ONLY(, device_error_word(), output_extent(n)));
     else
-      convert_rows_kernel<QMV_F32><<<(unsigned)ctas, 256, 0, stream>>>(w, n, static_cast<uint8_t*>(W));
+      convert_rows_kernel<QMV_F32><<<(unsigned)ctas, 256, 0, stream>>>(
+          w, n, static_cast<uint8_t*>(W) QMV_DEBUG_ONLY(, device_error_word(), output_extent(n)));
     return cudaGetLastError();
   }
   const int gw = fmt == QMV_IQ4_XS || fmt == QMV_Q8_G64 ? 512 : (fmt == QMV_Q8_G128 ? 1024 : 256);
@@ -297,13 +315,13 @@ cudaError_t launch_quantize_weights(int fmt, const float* w, long long M, int K,
   if (ctas > cap) ctas = cap;
   uint8_t* out = static_cast<uint8_t*>(W);
   switch (fmt) {
-    case QMV_Q8_0: quantize_kernel<QMV_Q8_0><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
-    case QMV_Q4_K: quantize_kernel<QMV_Q4_K><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
-    case QMV_Q5_K: quantize_kernel<QMV_Q5_K><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
-    case QMV_Q6_K: quantize_kernel<QMV_Q6_K><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
-    case QMV_Q8_G64: quantize_kernel<QMV_Q8_G64><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
-    case QMV_Q8_G128: quantize_kernel<QMV_Q8_G128><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
-    default: quantize_kernel<QMV_IQ4_XS><<<(unsigned)ctas, 128, 0, stream>>>(w, groups, K, out); break;
+    case QMV_Q8_0: quantize_groups<QMV_Q8_0>(w, M, K, out, ctas, stream); break;
+    case QMV_Q4_K: quantize_groups<QMV_Q4_K>(w, M, K, out, ctas, stream); break;
+    case QMV_Q5_K: quantize_groups<QMV_Q5_K>(w, M, K, out, ctas, stream); break;
+    case QMV_Q6_K: quantize_groups<QMV_Q6_K>(w, M, K, out, ctas, stream); break;
+    case QMV_Q8_G64: quantize_groups<QMV_Q8_G64>(w, M, K, out, ctas, stream); break;
+    case QMV_Q8_G128: quantize_groups<QMV_Q8_G128>(w, M, K, out, ctas, stream); break;
+    default: quantize_groups<QMV_IQ4_XS>(w, M, K, out, ctas, stream); break;
   }
   return cudaGetLastError();
 }

@@ -66,6 +66,14 @@ def test_device_error_needs_an_output_pointer(L):
     assert L.qmv_get_device_error(None, None) == -4
 
 
+def test_release_library_has_no_debug_switch(L):
+    # the extent-shrinking switch of the range-checked build is not in the
+    # release library: it answers QMV_ERR_UNAVAILABLE and changes nothing
+    assert L.qmv_debug_shrink_outputs(1) == -9
+    assert L.qmv_debug_shrink_outputs(0) == -9
+    assert "not available" in api.strerror(-9)
+
+
 def test_route_rejects_bad_arguments(L):
     # fmt, Wr, x, E, hidden, n_tok, top_k, gating, logits, ids, gates, stream
     assert L.moe_route_run(9, A, A, 128, 4096, 1, 8, 0, A, A, A, None) == -1
