@@ -161,12 +161,16 @@ constexpr int TWO_PER_SM_STAGES = 4;
 static bool plan_stages(int nt, int cw, size_t act, int stage_bytes, size_t budget, int& stages, size_t& smem) {
   // mbarriers (full, empty, 2 more) and the cross-warp sums of thin tiles
   const size_t fixed = act + 2 * MAX_STAGES * sizeof(uint64_t) + 128 + (size_t)cw * RW * 16 * sizeof(float);
-  if (nt <= 4 && fixed + 2 * (size_t)stage_bytes <= TWO_PER_SM_BYTES) {
+  if (nt <= 4 && cw == 8 && fixed + 2 * (size_t)stage_bytes <= TWO_PER_SM_BYTES) {  // two CTAs per SM
     int st = (int)((TWO_PER_SM_BYTES - fixed) / stage_bytes);
     stages = st > TWO_PER_SM_STAGES ? TWO_PER_SM_STAGES : st;
   } else if (fixed + 2 * (size_t)stage_bytes <= budget) {
+    // one CTA per SM; twelve warps with up to 4 token slots still take at
+    // most 4 stages (deeper rings only queue weight reads ahead of the
+    // activation staging)
+    const int cap = nt <= 4 && cw == 12 ? TWO_PER_SM_STAGES : MAX_STAGES;
     int st = (int)((budget - fixed) / stage_bytes);
-    stages = st > MAX_STAGES ? MAX_STAGES : st;
+    stages = st > cap ? cap : st;
   } else {
     return false;
   }
@@ -176,7 +180,7 @@ static bool plan_stages(int nt, int cw, size_t act, int stage_bytes, size_t budg
 
 // Choose the compiled token count and the number of stages so that the
 // activation area plus at least two weight stages fit in shared memory.
-static bool plan_dense(int fmt, long long M, long long K, int n_tok, int n_split, Plan& pl) {
+static bool plan_dense(int fmt, long long M, long long K, int n_tok, int n_split, bool q8in, Plan& pl) {
   const int gw = group_weights(fmt);
   const long long groups = K / gw;
   const long long max_range = ((groups + n_split - 1) / n_split) * gw;  // weights
@@ -185,11 +189,20 @@ static bool plan_dense(int fmt, long long M, long long K, int n_tok, int n_split
   int nt = 16;
   while (nt > n_tok && nt > 1) nt >>= 1;
   if (nt < n_tok && nt < 16) nt <<= 1;  // smallest power of two >= n_tok (<= 16)
-  // from 8 tokens on twelve consumer warps where their tiles fit, else eight
-  // (F16 / F32 rows: eight)
+  // Twelve consumer warps where their tiles fit, else eight (F16 / F32 rows:
+  // eight), from 8 tokens on and at 4 tokens; at 4 tokens with pre-quantized
+  // activations on a tall matrix (8+ units of rows per SM) two CTAs of eight
+  // per SM instead.  Measured on GB300 at 4 tokens, pre-quantized: Q4_K 17408
+  // x 5120 17.0 us with two CTAs of eight against 17.8 with twelve, Q4_K 5120
+  // x 5120 10.3 against 9.7, IQ4_XS 6144 x 2048 7.9 against 6.8; at 3 tokens
+  // (staged from fp32, where the eight-warp kernel spills) twelve always:
+  // Q4_K 17408 x 5120 18.4 -> 16.4, Q6_K 21.3 -> 18.4, Q4_K 5120 x 5120 11.5
+  // -> 8.5, IQ4_XS 2048 x 6144 10.5 -> 7.7.
+  const long long work_units = (M + UNIT_ROWS - 1) / UNIT_ROWS * n_split;
+  const bool twelve_at_4 = !(q8in && work_units >= 8ll * device_sm_count());
   for (;; nt >>= 1) {
     bool ok = false;
-    for (int cw = nt >= 8 && !is_float(fmt) ? 12 : 8; cw >= 8 && !ok; cw -= 4) {
+    for (int cw = !is_float(fmt) && (nt >= 8 || (nt == 4 && twelve_at_4)) ? 12 : 8; cw >= 8 && !ok; cw -= 4) {
       pl.cw = cw;
       pl.tile_rows = cw * RW;
       ok = plan_stages(nt, cw, act_area_bytes(fmt, nt, pl.act_nck), pl.tile_rows * chunk_bytes_of(fmt), budget,
@@ -202,7 +215,7 @@ static bool plan_dense(int fmt, long long M, long long K, int n_tok, int n_split
   const long long units = (M + UNIT_ROWS - 1) / UNIT_ROWS;
   const long long work = units * n_split;
   // two CTAs per SM when they fit (more warps to hide latency), else one
-  const int ctas = device_sm_count() * (pl.smem <= TWO_PER_SM_BYTES && nt <= 4 ? 2 : 1);
+  const int ctas = device_sm_count() * (pl.smem <= TWO_PER_SM_BYTES && nt <= 4 && pl.cw == 8 ? 2 : 1);
   pl.grid = (int)(work < ctas ? work : ctas);
   return true;
 }
@@ -226,7 +239,7 @@ static int run_dense(int fmt, const void* W, const float* x, const int8_t* xq, c
                      float* out, long long M, long long K, int n_tok, int n_split, cudaStream_t stream,
                      const float* add = nullptr) {
   Plan pl;
-  if (!plan_dense(fmt, M, K, n_tok, n_split, pl)) return QMV_ERR_SHAPE;
+  if (!plan_dense(fmt, M, K, n_tok, n_split, xq != nullptr, pl)) return QMV_ERR_SHAPE;
   const long long rb = qmv_row_bytes(fmt, K);
   DenseLaunch L;
   if (!encode_rows(&L.map_tile, W, M, rb, chunk_bytes_of(fmt), pl.tile_rows)) return QMV_ERR_CUDA;

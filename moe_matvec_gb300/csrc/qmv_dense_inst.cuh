@@ -58,7 +58,7 @@ static cudaError_t launch_dense_src(const DenseLaunch& L) {
     switch (L.nt_tmpl) {
       case 1: return launch_dense_nt<F, 1, Q8IN, 8, ADD>(L);
       case 2: return launch_dense_nt<F, 2, Q8IN, 8, ADD>(L);
-      case 4: return launch_dense_nt<F, 4, Q8IN, 8, ADD>(L);
+      case 4: return L.cw == 12 ? launch_dense_nt<F, 4, Q8IN, 12, ADD>(L) : launch_dense_nt<F, 4, Q8IN, 8, ADD>(L);
       case 8: return L.cw == 12 ? launch_dense_nt<F, 8, Q8IN, 12, ADD>(L) : launch_dense_nt<F, 8, Q8IN, 8, ADD>(L);
       case 16:
         return L.cw == 12 ? launch_dense_nt<F, 16, Q8IN, 12, ADD>(L) : launch_dense_nt<F, 16, Q8IN, 8, ADD>(L);
