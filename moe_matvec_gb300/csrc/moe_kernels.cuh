@@ -318,7 +318,6 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, NT <= 4 && CW == CONSUMER_
 
   // ---------------- consumers ----------------
   if constexpr (SH::RESPLIT) regs_inc<SH::REG_CONSUMER>();
-  if (MODE == MOE_DOWN) pdl_wait();  // h comes from the preceding kernel
   const int cw = warp;
   bool alive = true;
   MoeWalk walk(rt, units_per_pair, TILE_UNITS);
@@ -346,12 +345,15 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, NT <= 4 && CW == CONSUMER_
   // between lane pairs (at fewer tokens the extra code spills registers and
   // costs more than the zero fill it saves)
   const bool half_last = NT >= 8 && p.K % KCHUNK == KCHUNK / 2;
+  // DOWN: h comes from the preceding kernel; waited for only now, so that
+  // the set-up above runs while that kernel finishes
+  if (MODE == MOE_DOWN) pdl_wait();
 
   while (walk.next(q, u, nu)) {
     if (q != staged_pair) {
       first = QMV_CHECK(in_array(rt.pair_first, q, p.err)) ? rt.pair_first[q] : 0;
       nt = QMV_CHECK(in_array(rt.pair_count, q, p.err)) ? rt.pair_count[q] : 0;
-      named_sync(1, CONSUMER_THREADS);
+      if (staged_pair >= 0) named_sync(1, CONSUMER_THREADS);  // nobody still reads the previous group's rows
       if (threadIdx.x < nt && QMV_CHECK(in_array(rt.slots, first + threadIdx.x, p.err)) &&
           QMV_CHECK(in_array(s_rows, threadIdx.x, p.err))) {
         const int slot = rt.slots[first + threadIdx.x];

@@ -227,7 +227,6 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, is_float(F) ? 1 : dense_mi
   // waiting or computing) so that the named barriers of the others still
   // complete; the timeout bit is already set.
   if constexpr (SH::RESPLIT) regs_inc<SH::REG_CONSUMER>();
-  pdl_wait();  // activations may come from the preceding kernel
   const int cw = warp;
   bool alive = true;
   TileWalk<TU> walk(p);
@@ -242,13 +241,17 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, is_float(F) ? 1 : dense_mi
   const ActSource src{p.x, p.xq, p.xd, p.xs, p.K, nullptr, t0, nullptr, nullptr, nullptr
                           QMV_DEBUG_ONLY(, p.x_len, 0, p.err)};
   uint32_t aphase = 0;
+  // the activations may come from the preceding kernel: wait for it only
+  // now, so that the set-up above (which reads parameters only) runs while
+  // it finishes
+  pdl_wait();
 
   while (walk.next(s, u, nu)) {
     int g0, g1;
     split_range(p, s, g0, g1);
     const int kb0 = g0 * (GW / BLK), nblk = (g1 - g0) * (GW / BLK);
     if (s != staged_split) {
-      named_sync(1, CONSUMER_THREADS);  // nobody still reads the previous range
+      if (staged_split >= 0) named_sync(1, CONSUMER_THREADS);  // nobody still reads the previous range
       if constexpr (is_float(F)) {
         stage_float<F, NT, CW>(src, (long long)kb0 * BLK, nblk * BLK, ntk, a, cw, lane);
       } else if constexpr (!Q8IN) {

@@ -322,7 +322,6 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
   // the timeout bit is already set.
   constexpr int RP = MK_UNITS / 2;  // row pairs (16 rows: the MMA's M) of a tile
   regs_inc<MK_REG_CONSUMER>();
-  pdl_wait();  // activations may come from the preceding kernel
   const int cw = warp, g = lane >> 2, t4 = lane & 3;
   const int t0 = p.t0 + blockIdx.y * NT, ntk = p.nt;
   const int apitch = L.apitch, dpitch = L.dpitch;
@@ -340,12 +339,15 @@ __global__ void __launch_bounds__(MK_THREADS, 1)
   int staged_split = -1;
   uint32_t aphase = 0;
 
+  // the activations may come from the preceding kernel: wait for it only
+  // now, so that the set-up above (parameters only) runs while it finishes
+  pdl_wait();
   while (walk.next(s, u, nu)) {
     int g0, g1;
     split_range(p, s, g0, g1);
     const int kb0 = g0 * 8, nblk = (g1 - g0) * 8;
     if (s != staged_split) {
-      named_sync(1, MK_CW * 32);  // nobody still reads the previous range (or the partial sums)
+      if (staged_split >= 0) named_sync(1, MK_CW * 32);  // nobody still reads the previous range (or the partial sums)
       if (!q8in) {
         mk_stage_fp32<NT>(p, t0, ntk, kb0, nblk, codes, dxa, xsa, apitch, dpitch, cw, lane);
       } else {

@@ -127,7 +127,6 @@ __global__ void __launch_bounds__(MF_THREADS, 1)
   }
 
   // ---------------- consumers ----------------
-  pdl_wait();  // activations may come from the preceding kernel
   const int cw = warp, g = lane >> 2, t4 = lane & 3;
   const int t0 = p.t0 + blockIdx.y * NT, ntk = p.nt;
   const int xpitch = L.xpitch;
@@ -144,12 +143,15 @@ __global__ void __launch_bounds__(MF_THREADS, 1)
   Ring ring;
   int staged_split = -1;
 
+  // the activations may come from the preceding kernel: wait for it only
+  // now, so that the set-up above (parameters only) runs while it finishes
+  pdl_wait();
   while (walk.next(s, u, nu)) {
     int g0, g1;
     split_range(p, s, g0, g1);
     const int klen = (g1 - g0) * BLK, nck = (klen + MF_KC - 1) / MF_KC;
     if (s != staged_split) {
-      named_sync(1, MF_CW * 32);  // nobody still reads the previous range
+      if (staged_split >= 0) named_sync(1, MF_CW * 32);  // nobody still reads the previous range
       // the split range's activations: per token the power of two s_t that
       // puts its largest magnitude in [2^14, 2^15) (2^127 at most, for a zero
       // or tiny range), then the two f16 parts of x s_t
