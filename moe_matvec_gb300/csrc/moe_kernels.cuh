@@ -82,6 +82,81 @@ __device__ __forceinline__ int group_weight(int c, int nt_group, int unit_base) 
   return unit_base + (nt_group >= 2 ? (c + 1) & ~1 : c);
 }
 
+// The expert groups of a launch with at most 32 slots, built by warp 0 alone
+// in registers while the other warps wait at the closing barrier: lane s
+// holds slot s as a key (expert, token, slot), a bitonic sort across the
+// lanes puts the routed slots in (expert, token) order, which is the slot
+// list, and ballots, bit scans and one warp scan give every group (expert,
+// first slot, slot count) and its work prefix.  The tables are the general
+// build's, with a short chain of shuffles in place of its shared-memory
+// atomics and barriers, which cost about a microsecond per step beside a
+// decoding CTA on the same SM.
+__device__ __forceinline__ void build_routing_small(MoeRouting& rt, const MoeParams& p, int nt_group, bool report,
+                                                    int unit_base, int units_per_pair) {
+  const int S = p.n_tok * p.top_k, E = p.n_experts;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int t = lane / p.top_k, k = lane - t * p.top_k;
+    int e = -1;
+    if (lane < S && QMV_CHECK(in_range(lane, 1, p.ids_len, p.err))) e = p.ids[lane];
+    // the slot does not route when its id is out of range or repeats an
+    // earlier id of the same token (lanes t top_k .. lane - 1)
+    bool dup = false;
+#pragma unroll
+    for (int kk = 1; kk < QMV_MAX_TOPK; kk++) {
+      const int o = __shfl_up_sync(FULL, e, kk);
+      dup = dup || (kk <= k && o == e);
+    }
+    const int st = lane >= S ? 0 : (e < 0 || e >= E ? QMV_DEVERR_EXPERT_RANGE : (dup ? QMV_DEVERR_EXPERT_DUP : 0));
+    if (report && st) set_error(p.err, (unsigned)st);
+    // key: expert (9 bits), token (6 bits), slot (9 bits); slots that do
+    // not route sort last
+    unsigned key = lane < S && st == 0 ? ((unsigned)e << 15) | ((unsigned)t << 9) | (unsigned)lane : 0xFFFFFFFFu;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        const unsigned other = __shfl_xor_sync(FULL, key, stride);
+        const bool up = (lane & size) == 0, lower = (lane & stride) == 0;
+        key = up == lower ? min(key, other) : max(key, other);
+      }
+    const int V = __popc(__ballot_sync(FULL, key != 0xFFFFFFFFu));  // routed slots: lanes 0 .. V - 1
+    const bool have = lane < V;
+    const int se = (int)(key >> 15);
+    if (have && QMV_CHECK(in_array(rt.slots, lane, p.err))) rt.slots[lane] = (int)(key & 511u);
+    // runs of equal experts, cut into groups of up to nt_group slots
+    const int prev = __shfl_up_sync(FULL, se, 1);
+    const unsigned starts = __ballot_sync(FULL, have && (lane == 0 || prev != se));
+    const unsigned upto = 0xFFFFFFFFu >> (31 - lane);  // bits 0 .. lane
+    const int rs = 31 - __clz(starts & upto);          // the run's first lane
+    const unsigned later = starts & ~upto;
+    const int re = later ? __ffs(later) - 1 : V;       // the lane past the run
+    const bool begins = have && ((lane - rs) & (nt_group - 1)) == 0;
+    const int cnt = min(nt_group, re - lane);
+    const unsigned bmask = __ballot_sync(FULL, begins);
+    const int w = begins ? group_weight(cnt, nt_group, unit_base) * units_per_pair : 0;
+    int incl = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(FULL, incl, o);
+      if (lane >= o) incl += a;
+    }
+    const int pi = __popc(bmask & ((1u << lane) - 1u));
+    if (begins && QMV_CHECK(in_array(rt.pair_expert, pi, p.err))) {
+      rt.pair_expert[pi] = se;
+      rt.pair_first[pi] = lane;
+      rt.pair_count[pi] = cnt;
+      rt.pair_cost[pi] = incl - w;
+    }
+    const int total = __shfl_sync(FULL, incl, 31);
+    if (lane == 0) {
+      rt.n_pairs = __popc(bmask);
+      rt.pair_cost[__popc(bmask)] = total;
+    }
+  }
+  __syncthreads();
+}
+
 // Build the expert groups (called by all threads of the CTA).  The experts
 // are scanned in rounds of (warps x 32): each warp scans its 32 experts'
 // slot, group and work counts with shuffles, the warps' totals go through
@@ -90,6 +165,10 @@ __device__ __forceinline__ int group_weight(int c, int nt_group, int unit_base) 
 __device__ __forceinline__ void build_routing(MoeRouting& rt, const MoeParams& p, int nt_group, bool report,
                                               int unit_base, int units_per_pair) {
   const int S = p.n_tok * p.top_k;
+  if (S <= 32) {
+    build_routing_small(rt, p, nt_group, report, unit_base, units_per_pair);
+    return;
+  }
   const int E = p.n_experts;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   // one coalesced read of ids; every later look-up is in shared memory
