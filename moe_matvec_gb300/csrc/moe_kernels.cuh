@@ -446,7 +446,9 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, NT <= 4 && CW == CONSUMER_
         src.wd = p.hd;
         src.ws = p.hs;
       }
-      stage_activations<F, NT, 4, CW>(src, 0, nblk, nt, a, cw, lane);
+      // 1-2 slots: two units of 8 blocks per warp step, so that a single
+      // token's row spreads over more warps (and fewer registers are live)
+      stage_activations<F, NT, (NT <= 2 ? 2 : 4), CW>(src, 0, nblk, nt, a, cw, lane);
       named_sync(1, CONSUMER_THREADS);
       staged_pair = q;
     }

@@ -255,7 +255,9 @@ __global__ void __launch_bounds__(Shape<CW>::THREADS, is_float(F) ? 1 : dense_mi
       if constexpr (is_float(F)) {
         stage_float<F, NT, CW>(src, (long long)kb0 * BLK, nblk * BLK, ntk, a, cw, lane);
       } else if constexpr (!Q8IN) {
-        stage_activations<F, NT, (NT >= 8 ? 8 : 4), CW>(src, kb0, nblk, ntk, a, cw, lane);
+        // one token: two units of 8 blocks per warp step, so that its row
+        // spreads over more warps (IQ4_XS 6144 x 2048: 4.58 -> 4.18 us)
+        stage_activations<F, NT, (NT >= 8 ? 8 : NT == 1 ? 2 : 4), CW>(src, kb0, nblk, ntk, a, cw, lane);
       } else {
         alive = __all_sync(FULL, stage_q8_bulk<F, NT, CW>(src, kb0, nblk, ntk, a, abar, aphase, p.err, cw, lane)) &&
                 alive;
