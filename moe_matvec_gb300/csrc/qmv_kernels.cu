@@ -85,8 +85,8 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
 // gates[t][k] * o[t * top_k + k][m]; a slot that does not route (id out of
 // range, or repeating an earlier id of the token) adds nothing.  One thread
 // per 4 consecutive outputs of a token; the ids, gates and slot outputs of
-// the token are all loaded before the first is used, so their latencies
-// overlap.
+// the token are all loaded before the first is used (the outputs do not wait
+// for the ids), so their latencies overlap.
 __global__ void __launch_bounds__(256) moe_combine_kernel(const int32_t* __restrict__ ids,
                                                           const float* __restrict__ gates,
                                                           const float* __restrict__ o, float* __restrict__ y,
@@ -99,6 +99,15 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const int32_t* __restr
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
     const int t = (int)(i / q4), m4 = (int)(i - (long long)t * q4);
+    // the slot outputs' addresses do not depend on the ids: loaded at once,
+    // beside the ids and gates (a slot that does not route is skipped below,
+    // whatever its o holds)
+    float4 v[QMV_MAX_TOPK];
+#pragma unroll
+    for (int k = 0; k < QMV_MAX_TOPK; k++)
+      v[k] = k < top_k && QMV_CHECK(in_range(((long long)t * top_k + k) * hidden + 4 * m4, 4, o_len, err))
+                 ? reinterpret_cast<const float4*>(o + ((long long)t * top_k + k) * hidden)[m4]
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
     int e[QMV_MAX_TOPK];
     float g[QMV_MAX_TOPK];
 #pragma unroll
@@ -113,13 +122,7 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const int32_t* __restr
       ok[k] = e[k] >= 0 && e[k] < n_experts;
 #pragma unroll
       for (int kk = 0; kk < k; kk++) ok[k] = ok[k] && e[kk] != e[k];
-      ok[k] = ok[k] && QMV_CHECK(in_range(((long long)t * top_k + k) * hidden + 4 * m4, 4, o_len, err));
     }
-    float4 v[QMV_MAX_TOPK];
-#pragma unroll
-    for (int k = 0; k < QMV_MAX_TOPK; k++)
-      v[k] = ok[k] ? reinterpret_cast<const float4*>(o + ((long long)t * top_k + k) * hidden)[m4]
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < QMV_MAX_TOPK; k++) {
