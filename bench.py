@@ -702,9 +702,15 @@ def run_profile_moe(args):
     ws = torch.empty(api.moe_workspace_bytes(ex, n, c.top_k), dtype=torch.uint8, device="cuda")
     for k in range(2):
         a, b = synth.routing(2300 + 17 * n + k, n, E, c.top_k)
+        if args.skew:
+            # every token picks the same top_k experts (each in its own order):
+            # n slots per expert, so the expert groups split into n / slots groups
+            a = np.stack([np.random.default_rng(2500 + 31 * k + t).permutation(c.top_k) for t in range(n)])
+            a = a.astype(np.int32)
         api.moe_run(ex, torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda(), x, ws=ws, out=y)
     torch.cuda.synchronize()
-    print(json.dumps({"profile_run": "moe_128x_top8_h4096_f1536", "n_tok": n, "calls": 2}))
+    print(json.dumps({"profile_run": "moe_128x_top8_h4096_f1536", "n_tok": n, "calls": 2,
+                      "routing": "all tokens on experts 0-7" if args.skew else "random"}))
     return 0
 
 
@@ -814,6 +820,7 @@ def main(argv=None):
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--profile", action="store_true", help="a few eager calls only (for ncu)")
     ap.add_argument("--profile-moe", type=int, default=0, help="two eager MoE calls at this many tokens (for ncu)")
+    ap.add_argument("--skew", action="store_true", help="with --profile-moe: every token on the same top_k experts")
     ap.add_argument("--profile-float", type=int, default=0,
                     help="two eager F16 17408 x 5120 calls at this many tokens (for ncu)")
     ap.add_argument("--profile-prefill", type=int, default=0,

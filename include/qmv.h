@@ -349,7 +349,10 @@ typedef struct moe_experts {
  * of up to G slots, G a power of two up to 16 chosen from the mean load
  * n_tok * top_k / n_experts (at least 8 from 4 tokens on); each group streams
  * the expert's weights once, so an expert with more than G slots in the call
- * is read once per group (ceil(slots / G) times).  A slot whose id is outside
+ * is streamed once per group (ceil(slots / G) times); the groups of one
+ * expert run side by side, so the repeats are served from L2 (measured on
+ * GB300 with 64 tokens on the same 8 experts, 8 groups each: 1.02x / 1.11x
+ * one read per expert from DRAM for gate/up / down).  A slot whose id is outside
  * [0, n_experts) or repeats an earlier id of the same token contributes 0 and
  * sets the device error word.  gates are used as given (not renormalised).
  * The workspace holds the intermediates at the offsets of
