@@ -257,10 +257,12 @@ int qmv_run_q8(int fmt, const void* W, const int8_t* xq, const float* xd,
  * n_split = 0 picks a split count from the shape (qmv_splitk_choose).
  * ws must hold qmv_splitk_workspace_bytes(M, n_tok, n_split) bytes (none
  * for n_split = 1).  If it holds that (rounded up to 256) plus
- * qmv_act_q8_bytes(K, n_tok) more and n_tok >= 4, the activations are
- * quantized once into the rest of the workspace (one more kernel launch)
- * and each CTA copies its K-range in instead of quantizing it again: the same
- * arithmetic (bitwise equal results), less work per CTA. */
+ * qmv_act_q8_bytes(K, n_tok) more and the call has more than 8 tokens, or
+ * 5-8 tokens with a split, K > 4096 or M >= 7168 (the shapes where it
+ * measured faster), the activations are quantized once into the rest of the
+ * workspace (one more kernel launch) and each CTA copies its K-range in
+ * instead of quantizing it again: the same arithmetic (bitwise equal
+ * results), less work per CTA. */
 size_t qmv_act_q8_bytes(int64_t K, int n_tok);
 int qmv_splitk_choose(int fmt, int64_t M, int64_t K, int n_tok);
 size_t qmv_splitk_workspace_bytes(int64_t M, int n_tok, int n_split);
@@ -302,7 +304,7 @@ int qmv_run_siblings(int count, const int* fmts, const void* const* W, const int
  * that owns all device memory.  This variant takes no workspace: the partial
  * sums go to a static device array of QMV_STATIC_SCRATCH_BYTES that the
  * library holds on every GPU that loads it, until the process exits.  With a
- * split above one and 4 or more tokens, the activations quantized once
+ * split above one and more than 4 tokens, the activations quantized once
  * (qmv_act_q8_bytes(K, n_tok)) are placed in the array too, after the
  * partial sums, when both fit (as qmv_splitk_run does with a large enough
  * workspace).

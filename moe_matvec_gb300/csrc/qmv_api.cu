@@ -545,16 +545,23 @@ static int splitk_impl(int fmt, const void* W, const float* x, const float* add,
       if (ws_bytes < qmv_splitk_workspace_bytes(M, n_tok, n_split)) return QMV_ERR_WORKSPACE;
     }
   }
-  // With room after the partial sums and 4 or more tokens, the activations
+  // With room after the partial sums and more than 4 tokens, the activations
   // are quantized once into the workspace (one more launch) and every CTA
   // brings its range in by bulk copies; otherwise each CTA quantizes its
-  // range while staging.  Same arithmetic, bitwise equal results.
+  // range while staging.  Same arithmetic, bitwise equal results.  Measured
+  // on GB300 (graph replay): up to 4 tokens staging from fp32 is faster on
+  // every shape (Q4_K 17408 x 5120 16.2 against 16.5 us, IQ4_XS 6144 x 2048
+  // 5.2 against 6.5); at 5-8 tokens it is faster for one split of K <= 4096
+  // below the 8-slot tensor-core kernel's height (IQ4_XS 6144 x 2048 7.6
+  // against 8.4, Q8_0 4096 x 4096 9.4 against 9.8) and slower above (Q4_K
+  // 5120 x 5120 12.9 against 12.6); at 16 tokens quantizing once wins.
   const size_t part = n_split > 1 ? align256(qmv_splitk_workspace_bytes(M, n_tok, n_split)) : 0;
   const size_t q8 = qmv_act_q8_bytes(K, n_tok);
   const int8_t* xq = nullptr;
   const float* xd = nullptr;
   const int32_t* xs = nullptr;
-  if (n_tok >= 4 && !is_float(fmt) && ws && aligned16(ws) && q8 && ws_bytes >= part + q8) {
+  const bool stage_fp32 = n_tok <= 4 || (n_tok <= 8 && n_split == 1 && K <= 4096 && M < 7168);
+  if (!stage_fp32 && !is_float(fmt) && ws && aligned16(ws) && q8 && ws_bytes >= part + q8) {
     uint8_t* base = static_cast<uint8_t*>(ws) + part;
     const size_t nb = (size_t)n_tok * (size_t)(K / 32);
     int8_t* q = reinterpret_cast<int8_t*>(base);

@@ -14,7 +14,7 @@
 // first call made on that device, which is why that first call should come
 // before any stream capture.  All calls share the array: calls that may run
 // at the same time on the GPU (different streams, or graphs launched
-// concurrently) race on it.  With a split above one and 4 or more tokens,
+// concurrently) race on it.  With a split above one and more than 4 tokens,
 // the activations quantized once are placed in it too, after the partial
 // sums, when both fit (the same arithmetic as the per-CTA quantization,
 // bitwise equal results).  Nothing in it needs clearing: every call writes

@@ -2,7 +2,7 @@
 
 It serves callers that may not call cudaMalloc themselves (for instance a
 plugin that runs while its host framework captures a CUDA graph, or a host
-that owns all of the device memory): the partial sums (and, from 4 tokens,
+that owns all of the device memory): the partial sums (and, above 4 tokens,
 the once-quantized activations) go to a static device array inside the
 library instead of a caller workspace.  Two calls in a row share that array;
 each must give the same bits as qmv_splitk_run with a caller-allocated
@@ -22,8 +22,9 @@ pytestmark = pytest.mark.gpu
 
 
 def test_static_scratch_matches_workspace_entry_point_on_two_calls(lib):
-    cases = [(0, 512, 65536, 4, 16), (1, 300, 8192, 7, 0)]   # fmt, M, K, n_tok, n_split (0 = auto)
-    # the automatic split of the second call is above one, so both calls use the array
+    # fmt, M, K, n_tok, n_split (0 = auto); 6 and 7 tokens quantize the activations into the array
+    cases = [(0, 512, 65536, 4, 16), (0, 512, 65536, 6, 16), (1, 300, 8192, 7, 0)]
+    # the automatic split of the last call is above one, so it uses the array
     assert lib.splitk_choose(1, 300, 8192, 7) > 1
     for call, (fmt, M, K, n, S) in enumerate(cases):
         w = synth.weights(900 + call, M, K)
