@@ -1,5 +1,5 @@
 """Canary bytes around every output and workspace buffer of every entry point
-(a stand-in for a memory checker, which this GPU pool does not offer).
+(a stand-in for a device memory checker).
 
 Each result or workspace buffer is a view into a larger allocation whose
 4 KiB guard bands on both sides hold seeded random bytes, and whose own bytes

@@ -1,6 +1,5 @@
 """The range-checked build (libqmv_debug.so: the same sources compiled with
-QMV_DEBUG), a stand-in for a memory checker, which this GPU pool does not
-offer.  Every global access of its kernels is checked against the extent of
+QMV_DEBUG), a stand-in for a device memory checker.  Every global access of its kernels is checked against the extent of
 its buffer as the host derives it from the call's arguments, every shared-
 memory access against the CTA's allocation; a failed check skips the access
 and sets QMV_DEVERR_RANGE.
