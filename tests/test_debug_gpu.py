@@ -1,8 +1,8 @@
 """The range-checked build (libqmv_debug.so: the same sources compiled with
-QMV_DEBUG), a stand-in for a device memory checker.  Every global access of its kernels is checked against the extent of
-its buffer as the host derives it from the call's arguments, every shared-
-memory access against the CTA's allocation; a failed check skips the access
-and sets QMV_DEVERR_RANGE.
+QMV_DEBUG), a stand-in for a device memory checker.  Every global access of
+its kernels is checked against the extent of its buffer as the host derives
+it from the call's arguments, every shared-memory access against the CTA's
+allocation; a failed check skips the access and sets QMV_DEVERR_RANGE.
 
   * Every kernel family, on tiny, ragged and tall shapes, runs through the
     debug library without a failed check, and its results are bitwise those
