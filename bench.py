@@ -15,7 +15,7 @@ the library's quantizer, N(0, 1) activations).  Weights rotate over 12
 replicas (600 MB, > 4x the 129 MB L2), one replica per step, so every call
 streams from HBM.
 Each call is the library's matvec with a caller workspace (qmv_splitk_run,
-which picks one split for this shape and, from 4 tokens on, quantizes the
+which picks one split for this shape and, above 4 tokens, quantizes the
 activations once into the workspace).  Timed region: exactly --steps steps,
 each the replay of a captured one-step graph, CUDA events on the launching
 stream.  `e2e` repeats the steps through the public API with the
@@ -273,7 +273,7 @@ def run_ours(args):
     xs = {n: x_all[offs[i]:offs[i + 1]] for i, n in enumerate(NTOKS)}
     ys = {n: y_all[offs[i]:offs[i + 1]] for i, n in enumerate(NTOKS)}
     # the library's matvec with a caller workspace (qmv_splitk_run; one split
-    # for this shape): with 4+ tokens it quantizes the activations once
+    # for this shape): above 4 tokens it quantizes the activations once
     splits = {n: api.splitk_choose(FMT, M, K, n) for n in NTOKS}
     wss = {n: torch.empty(max(16, api.splitk_workspace_fast_bytes(M, K, n, splits[n])), dtype=torch.uint8,
                           device=dev) for n in NTOKS}
