@@ -264,7 +264,7 @@ BENCH_CASE = next(c for c in synth.DENSE_CASES if c.workload == "q4_k")
 def test_bench_call_full_size(lib, n_idx, n):
     # the exact call the benchmark times for Q4_K 17408 x 5120: qmv_splitk_run
     # with the split chosen from the shape and a workspace with room for the
-    # once-quantized activations (from 4 tokens: the standalone quantizer,
+    # once-quantized activations (above 4 tokens: the standalone quantizer,
     # then the matvec kernel with pre-quantized input), checked element by
     # element on the first and last 512 rows (every tile and 8-row unit of
     # the first and last CTAs' ranges) and 256 random rows
