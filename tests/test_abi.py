@@ -37,6 +37,23 @@ def test_library_builds_loads_and_exports_every_declared_symbol():
     assert not missing, missing
 
 
+@pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                    reason="nvcc not available")
+def test_debug_library_builds_exports_every_symbol_and_takes_its_switch():
+    # the range-checked build (QMV_DEBUG) of the same sources: the same
+    # symbols, and its extent switch (host state only, no device touched)
+    # accepts n >= 0 and rejects a negative n; the release library has no
+    # switch (tests/test_api_errors.py)
+    from moe_matvec_gb300 import api
+    lib = api.load_debug()
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert lib.qmv_debug_shrink_outputs(-1) == -2
+    assert lib.qmv_debug_shrink_outputs(7) == 0
+    assert lib.qmv_debug_shrink_outputs(0) == 0
+    assert lib.qmv_row_bytes(1, 5120) == 2880
+
+
 def test_strerror_and_row_bytes_need_no_device():
     from moe_matvec_gb300 import api
     lib = api.load()
